@@ -1,0 +1,438 @@
+"""Benchmark of the gated-delta-rule forward library on one (or N) GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Headline workload: Gated DeltaNet prefill, 4 sequences x 4096 tokens, 16 heads, d=128,
+bf16 q/k/v, scalar decay, fp32 state, chunk 64 ("gdn_prefill").  A step is one
+kda_prefill_fwd call over that batch (every stage of the prefill path); the metric is
+prefill tokens/s.  The decode step (256 sequences x 32 heads, per-channel decay) is
+measured in the same run and reported under "also" as decode steps/s.
+
+Multi-GPU: every rank runs an independent replica on its own batch (sequences never
+interact, so nothing is exchanged); value = all ranks' tokens / the slowest rank's time.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "prefill tokens/s"
+UNIT = "tokens/s"
+L2_BYTES = 129e6
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def prefill_algorithmic_bytes(p) -> dict:
+    """Bytes the method must move once: inputs read, o written, touched states read+written."""
+    qkv = 2 if p.qkv_dtype == "bf16" else 4
+    st = 2 if p.state_dtype == "bf16" else 4
+    T, HK, HV, d = p.total_tokens, p.num_k_heads, p.num_v_heads, p.d_k
+    g_elems = T * HV * (d if p.decay_kind == "per_channel" else 1)
+    live = int(np.count_nonzero(p.lengths))
+    return dict(q=T * HK * d * qkv, k=T * HK * d * qkv, v=T * HV * d * qkv, beta=T * HV * 4,
+                g=g_elems * 4, o=T * HV * d * 4, state=2 * live * HV * d * d * st)
+
+
+def decode_algorithmic_bytes(dp) -> dict:
+    qkv = 2 if dp.qkv_dtype == "bf16" else 4
+    st = 2 if dp.state_dtype == "bf16" else 4
+    B, HK, HV, d = dp.num_seqs, dp.num_k_heads, dp.num_v_heads, dp.d_k
+    g_elems = B * HV * (d if dp.decay_kind == "per_channel" else 1)
+    return dict(q=B * HK * d * qkv, k=B * HK * d * qkv, v=B * HV * d * qkv, beta=B * HV * 4,
+                g=g_elems * 4, o=B * HV * d * 4, state=2 * B * HV * d * d * st)
+
+
+def prefill_flops(p) -> float:
+    """Chunk-form multiply-adds x 2 per token and value head (d_k = d_v = d)."""
+    d, C = p.d_k, p.chunk
+    macs = 3 * d * d + 2.5 * C * d + C * C / 6.0
+    return 2.0 * macs * p.total_tokens * p.num_v_heads
+
+
+# The prefill kernels in launch order, with the part of the algorithmic traffic each
+# one carries (the chunk-parallel kernel reads every input once; the scan writes o and
+# reads/writes the states).
+PREFILL_STAGES = [("plan", ()), ("chunk_local", ("q", "k", "v", "beta", "g")),
+                  ("state_scan", ("o", "state"))]
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d.get("hbm_gbs"), "bf16_tflops": d.get("bf16_tflops"),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("KDA_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def reduce_max(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate(units_per_rank: float, seconds: float, world: int, device=None) -> tuple:
+    """Whole-job throughput: all ranks' units over the slowest rank's time (weak scaling)."""
+    slowest = reduce_max(seconds, world, device)
+    return units_per_rank * world / slowest, slowest
+
+
+# ----------------------------------------------------------------------------- CPU side
+
+def cpu_oracle_prefill(p, pair_fraction: float = 1.0):
+    """Times the fp64 oracle on (a seeded subset of) the workload's (sequence, head) pairs."""
+    import oracle
+    npairs = p.num_seqs * p.num_v_heads
+    mask = np.zeros(npairs, np.uint8)
+    take = max(1, int(round(npairs * pair_fraction)))
+    mask[np.random.Generator(np.random.PCG64(7)).permutation(npairs)[:take]] = 1
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.run(p, pair_mask=mask, nthreads=threads)
+    dt = time.perf_counter() - t0
+    # tokens-equivalent: the sampled pairs' token-head work over the workload's heads
+    lengths = p.lengths
+    tok_heads = float(sum(lengths[i // p.num_v_heads] for i in np.flatnonzero(mask)))
+    return tok_heads / p.num_v_heads / dt, dt, threads, take, npairs
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    p = workloads.workload(args.workload)
+    frac = 0.25 if args.workload != "tiny_gdn" else 1.0
+    for _ in range(args.warmup):
+        cpu_oracle_prefill(p, frac)
+    tok, secs = 0.0, 0.0
+    for _ in range(args.steps):
+        r, dt, threads, take, npairs = cpu_oracle_prefill(p, frac)
+        tok += r * dt            # token-equivalents of this step's sample
+        secs += dt
+    value = tok / secs if secs > 0 else 0.0
+    sample = (f"{take} of {npairs} (sequence, value head) pairs of {args.workload} per step, "
+              f"fp64, {threads} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / max(args.steps, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(p),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(p) -> dict:
+    return {"workload": p.name, "num_seqs": p.num_seqs, "total_tokens": p.total_tokens,
+            "num_k_heads": p.num_k_heads, "num_v_heads": p.num_v_heads, "d_k": p.d_k,
+            "d_v": p.d_v, "decay": p.decay_kind, "qkv_dtype": p.qkv_dtype,
+            "state_dtype": p.state_dtype, "chunk": p.chunk}
+
+
+# ----------------------------------------------------------------------------- GPU side
+
+def time_prefill(p, dev, steps, warmup):
+    import torch
+    import gated_delta_rule_deltanet_gb300 as kda
+    from workloads import torch_io
+    t = torch_io.prefill_inputs(p, dev)
+    T, HV, d = p.total_tokens, p.num_v_heads, p.d_v
+    out = torch.empty((T, HV, d), dtype=torch.float32, device=dev)
+    params = kda.kda._prefill_params(t["q"], t["k"], t["v"], t["beta"], t["log_decay"],
+                                     t["input_row_offsets"], t["slot_idx"], t["state_pool"],
+                                     p.chunk, p.scale, True, False)
+    ws = torch.empty(kda.workspace_size(params), dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.prefill(**t, chunk=p.chunk, scale=p.scale, out=out, workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    nst = len(PREFILL_STAGES) + 1
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for s in range(steps):
+        kda.set_stage_events(evs[s])
+        step()
+    end.record()
+    kda.set_stage_events([])
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    stage_ms = [float(np.mean([evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)]))
+                for i in range(nst - 1)]
+    return total_ms / steps, stage_ms, t, out
+
+
+def time_prefill_e2e(p, dev, steps, warmup):
+    """Through the public API with host buffers: pinned H2D of the step's inputs, the call,
+    D2H of the outputs, all inside the timed region."""
+    import torch
+    import gated_delta_rule_deltanet_gb300 as kda
+    from workloads import torch_io
+    host = {"q": torch_io.tensor(p.q, p.qkv_dtype, pin=True),
+            "k": torch_io.tensor(p.k, p.qkv_dtype, pin=True),
+            "v": torch_io.tensor(p.v, p.qkv_dtype, pin=True),
+            "beta": torch_io.tensor(p.beta, "f32", pin=True),
+            "log_decay": torch_io.tensor(p.g, "f32", pin=True),
+            "input_row_offsets": torch_io.index(p.offsets).pin_memory(),
+            "slot_idx": torch_io.index(p.slot_idx).pin_memory()}
+    pool = torch_io.tensor(p.pool, p.state_dtype, dev)
+    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    T, HV, d = p.total_tokens, p.num_v_heads, p.d_v
+    out = torch.empty((T, HV, d), dtype=torch.float32, device=dev)
+    out_host = torch.empty((T, HV, d), dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        kda.prefill(**devb, state_pool=pool, chunk=p.chunk, scale=p.scale, out=out)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+def time_decode(dp, dev, steps, warmup):
+    import torch
+    import gated_delta_rule_deltanet_gb300 as kda
+    from workloads import torch_io
+    t = torch_io.decode_inputs(dp, dev)
+    B, HV, d = dp.num_seqs, dp.num_v_heads, dp.d_v
+    out = torch.empty((B, HV, d), dtype=torch.float32, device=dev)
+
+    def step(s):
+        i = s % dp.steps
+        kda.decode_step(t["q"][i], t["k"][i], t["v"][i], t["beta"][i], t["log_decay"][i],
+                        t["slot_idx"], t["state_pool"], out=out)
+
+    for s in range(warmup):
+        step(s)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for s in range(steps):
+        step(s)
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def ours_arm(args, rank, world, local):
+    import torch
+    import gated_delta_rule_deltanet_gb300 as kda
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kda.load()
+    peaks = load_peaks()
+    p = workloads.workload(args.workload)
+
+    # timed region: K prefill steps on resident inputs (inputs > L2, no flush needed)
+    barrier(world)
+    clocks = ClockSampler(local)
+    clocks.start()
+    ms, stage_ms, t_dev, _ = time_prefill(p, dev, args.steps, args.warmup)
+    clk = clocks.stop()
+    barrier(world)
+    tokens = p.total_tokens
+    value, slowest_s = aggregate(tokens * args.steps, ms * args.steps / 1e3, world, dev)
+    ms_per_step = 1e3 * slowest_s / args.steps
+    del t_dev
+
+    # end to end through the public API with host buffers
+    e2e_ms, h2d, d2h = time_prefill_e2e(p, dev, max(3, args.steps // 2), 2)
+    e2e_value, _ = aggregate(tokens, e2e_ms / 1e3, world, dev)
+
+    # roofline of the dominant kernel (its share of the algorithmic bytes / its time)
+    abytes = prefill_algorithmic_bytes(p)
+    dom = int(np.argmax(stage_ms))
+    name, parts = PREFILL_STAGES[dom]
+    dom_bytes = float(sum(abytes[x] for x in parts))
+    achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "peak_source": peaks["source"], "kernel_ms": stage_ms[dom],
+                "stage_ms": {n: m for (n, _), m in zip(PREFILL_STAGES, stage_ms)}}
+    path_bytes = float(sum(abytes.values()))
+    also = []
+    if not args.no_decode:
+        dp = workloads.workload("kda_decode")
+        dms = time_decode(dp, dev, max(args.steps, 20), max(args.warmup, 3))
+        dbytes = float(sum(decode_algorithmic_bytes(dp).values()))
+        dval, _ = aggregate(1.0, dms / 1e3, world, dev)      # one step per dms
+        also.append({"workload": "kda_decode", "metric": "decode steps/s", "value": dval,
+                     "unit": "steps/s", "ms_per_step": dms,
+                     "tokens_per_s": dval * dp.num_seqs,
+                     "roofline": {"bound": "hbm", "kernel": "decode_step",
+                                  "achieved": dbytes / (dms / 1e3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": dbytes / (dms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                  "traffic": None}})
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        rate, dt, threads, take, npairs = cpu_oracle_prefill(p, 1.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{take} of {npairs} (sequence, value head) pairs of {p.name} "
+                         f"(the whole workload), fp64, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic",
+                "config": {**workload_config(p),
+                           "l2": f"inputs larger than L2 ({path_bytes / 1e6:.0f} MB moved "
+                                 f"per step vs 129 MB L2); no flush"},
+                "path_roofline": {"algorithmic_bytes": path_bytes,
+                                  "achieved_gbs": path_bytes / (ms_per_step / 1e3) / 1e9,
+                                  "frac_hbm": path_bytes / (ms_per_step / 1e3) / 1e9
+                                  / peaks["hbm_gbs"],
+                                  "flops": prefill_flops(p)},
+                "roofline": roofline, "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "gpu_launches": len(PREFILL_STAGES) * args.steps,
+                "clocks": clk, "also": also}
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gdn_prefill",
+                    choices=[w for w in workloads.WORKLOADS if w != "kda_decode"])
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            reference_arm(args, rank, world)
+        else:
+            ours_arm(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,17 @@
+"""GB300-native forward pass of the gated delta rule (KDA / Gated DeltaNet / DeltaNet).
+
+The computation lives in libkda.so (hand-written CUDA for sm_103a, C ABI in
+include/kda.h).  This package only builds it and marshals torch tensors into
+it:
+
+    prefill(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk=64)
+    decode_step(q, k, v, beta, log_decay, slot_idx, state_pool)
+
+There is no CPU or eager fallback: if the library is missing, calls raise.
+"""
+from .kda import (decode_step, get_device_error, make_params, prefill,  # noqa: F401
+                  set_stage_events, workspace_size)
+from ._lib import KdaError, KdaParams, load  # noqa: F401
+
+__all__ = ["prefill", "decode_step", "workspace_size", "get_device_error", "make_params",
+           "set_stage_events", "KdaError", "KdaParams", "load"]

@@ -1,0 +1,211 @@
+// api.cu -- the C ABI: argument validation, workspace sizing and dispatch.
+//
+// Validation follows the argument checks of the chunked DeltaNet launcher in
+// "From Attention to Learned Memory" (sec. 4: shapes, dtypes, chunk size in
+// {16, 32, 64}), extended to the ragged batch, GQA ratio and slot pool of the
+// Modular "gated_delta" module.  Everything here runs on the host before any
+// launch; device-only checks live in the plan and decode kernels.
+#include <mutex>
+
+#include "kda_common.cuh"
+
+namespace kda {
+cudaError_t launch_decode(const Problem& P, bool qbf16, bool sbf16, bool perch, cudaStream_t s,
+                          const Stages& st);
+cudaError_t launch_prefill_simt(const Problem& P, void* workspace, bool qbf16, bool perch,
+                                bool sbf16, cudaStream_t stream, const Stages& st);
+size_t simt_workspace_bytes(const Problem& P);
+}  // namespace kda
+
+using kda::Problem;
+
+static_assert(sizeof(kda_params_t) == 88, "kda_params_t layout is part of the ABI");
+
+// The device error word (one per device that loads the library).
+__device__ int32_t g_kda_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mutex;
+int32_t* g_err_ptr[kMaxDevices] = {};
+
+int32_t* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mutex);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_kda_device_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+std::mutex g_stage_mutex;
+kda::Stages g_stages = {};
+
+kda::Stages current_stages() {
+  std::lock_guard<std::mutex> lock(g_stage_mutex);
+  return g_stages;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t elem_size(int32_t dt) { return dt == KDA_DTYPE_BF16 ? 2 : 4; }
+
+// Checks shared by prefill and decode; fills the launch record's sizes.
+kda_status_t check_common(const kda_params_t* p, Problem* P) {
+  if (!p) return KDA_ERR_INVALID_ARG;
+  if (p->num_seqs < 0 || p->num_k_heads <= 0 || p->num_v_heads <= 0 || p->num_slots <= 0)
+    return KDA_ERR_INVALID_ARG;
+  if (p->num_v_heads % p->num_k_heads != 0) return KDA_ERR_INVALID_ARG;
+  if (p->num_v_heads > 65535) return KDA_ERR_UNSUPPORTED;
+  if (p->d_k != p->d_v) return KDA_ERR_UNSUPPORTED;
+  if (p->d_k != 16 && p->d_k != 128) return KDA_ERR_UNSUPPORTED;
+  if (p->qkv_dtype != KDA_DTYPE_F32 && p->qkv_dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
+  if (p->state_dtype != KDA_DTYPE_F32 && p->state_dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
+  if (p->decay_kind != KDA_DECAY_SCALAR && p->decay_kind != KDA_DECAY_PER_CHANNEL)
+    return KDA_ERR_INVALID_ARG;
+  if (p->flags & ~KDA_FLAG_CHECKED) return KDA_ERR_INVALID_ARG;
+  const int64_t es = static_cast<int64_t>(elem_size(p->qkv_dtype));
+  const int64_t dq = static_cast<int64_t>(p->num_k_heads) * p->d_k;
+  const int64_t dv = static_cast<int64_t>(p->num_v_heads) * p->d_v;
+  const int64_t qs = p->q_row_stride ? p->q_row_stride : dq;
+  const int64_t ks = p->k_row_stride ? p->k_row_stride : dq;
+  const int64_t vs = p->v_row_stride ? p->v_row_stride : dv;
+  if (qs < dq || ks < dq || vs < dv) return KDA_ERR_INVALID_ARG;
+  if ((qs * es) % 16 || (ks * es) % 16 || (vs * es) % 16) return KDA_ERR_INVALID_ARG;
+  P->num_seqs = p->num_seqs;
+  P->HK = p->num_k_heads;
+  P->HV = p->num_v_heads;
+  P->D = p->d_k;
+  P->num_slots = p->num_slots;
+  P->chunk = p->chunk;
+  P->T = p->total_tokens;
+  P->scale = p->scale > 0.f ? p->scale : 1.0f / sqrtf(static_cast<float>(p->d_k));
+  P->l2norm = p->l2norm_qk ? 1 : 0;
+  P->flags = p->flags;
+  P->q_stride = qs;
+  P->k_stride = ks;
+  P->v_stride = vs;
+  return KDA_OK;
+}
+
+kda_status_t check_prefill(const kda_params_t* p, Problem* P) {
+  kda_status_t s = check_common(p, P);
+  if (s != KDA_OK) return s;
+  if (p->total_tokens < 0 || p->total_tokens > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  if (p->chunk != 16 && p->chunk != 32 && p->chunk != 64) return KDA_ERR_UNSUPPORTED;
+  if (p->num_seqs > 0x3fffffff) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+kda_status_t to_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int kda_abi_version(void) { return KDA_ABI_VERSION; }
+
+const char* kda_status_string(kda_status_t s) {
+  switch (s) {
+    case KDA_OK: return "ok";
+    case KDA_ERR_INVALID_ARG: return "invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+    case KDA_ERR_CUDA: return "CUDA error";
+    case KDA_ERR_DEVICE: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+kda_status_t kda_prefill_workspace_size(const kda_params_t* p, size_t* bytes) {
+  Problem P{};
+  if (!bytes) return KDA_ERR_INVALID_ARG;
+  kda_status_t s = check_prefill(p, &P);
+  if (s != KDA_OK) return s;
+  *bytes = kda::simt_workspace_bytes(P);
+  return KDA_OK;
+}
+
+kda_status_t kda_prefill_fwd(const kda_params_t* p, const void* q, const void* k, const void* v,
+                             const float* beta, const float* log_decay,
+                             const uint32_t* input_row_offsets, const uint32_t* slot_idx,
+                             void* state_pool, float* o, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  Problem P{};
+  kda_status_t s = check_prefill(p, &P);
+  if (s != KDA_OK) return s;
+  if (p->num_seqs == 0) return KDA_OK;
+  if (!input_row_offsets || !slot_idx || !state_pool) return KDA_ERR_INVALID_ARG;
+  if (p->total_tokens > 0 && (!q || !k || !v || !beta || !log_decay || !o)) return KDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(state_pool, 16) || !aligned(beta, 4) || !aligned(log_decay, 4) ||
+      !aligned(input_row_offsets, 4) || !aligned(slot_idx, 4))
+    return KDA_ERR_INVALID_ARG;
+  const size_t need = kda::simt_workspace_bytes(P);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
+  P.q = q; P.k = k; P.v = v; P.beta = beta; P.g = log_decay;
+  P.offsets = input_row_offsets; P.slot_idx = slot_idx;
+  P.pool = state_pool; P.o = o;
+  P.err = device_error_word();
+  if (!P.err) return KDA_ERR_CUDA;
+  const bool qbf16 = p->qkv_dtype == KDA_DTYPE_BF16;
+  const bool sbf16 = p->state_dtype == KDA_DTYPE_BF16;
+  const bool perch = p->decay_kind == KDA_DECAY_PER_CHANNEL;
+  const kda::Stages st = current_stages();
+  return to_status(kda::launch_prefill_simt(P, workspace, qbf16, perch, sbf16,
+                                            static_cast<cudaStream_t>(stream), st));
+}
+
+kda_status_t kda_decode_step(const kda_params_t* p, const void* q, const void* k, const void* v,
+                             const float* beta, const float* log_decay, const uint32_t* slot_idx,
+                             void* state_pool, float* o, void* stream) {
+  Problem P{};
+  kda_status_t s = check_common(p, &P);
+  if (s != KDA_OK) return s;
+  if (p->num_seqs == 0) return KDA_OK;
+  if (static_cast<int64_t>(p->num_seqs) * p->num_v_heads > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !beta || !log_decay || !slot_idx || !state_pool || !o) return KDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(state_pool, 16) || !aligned(beta, 4) || !aligned(log_decay, 4) || !aligned(slot_idx, 4))
+    return KDA_ERR_INVALID_ARG;
+  P.T = p->num_seqs;
+  P.q = q; P.k = k; P.v = v; P.beta = beta; P.g = log_decay;
+  P.slot_idx = slot_idx; P.pool = state_pool; P.o = o;
+  P.err = device_error_word();
+  if (!P.err) return KDA_ERR_CUDA;
+  const kda::Stages st = current_stages();
+  return to_status(kda::launch_decode(P, p->qkv_dtype == KDA_DTYPE_BF16,
+                                      p->state_dtype == KDA_DTYPE_BF16,
+                                      p->decay_kind == KDA_DECAY_PER_CHANNEL,
+                                      static_cast<cudaStream_t>(stream), st));
+}
+
+kda_status_t kda_get_device_error(void* stream, int32_t* code) {
+  if (!code) return KDA_ERR_INVALID_ARG;
+  int32_t* w = device_error_word();
+  if (!w) return KDA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_CUDA;
+  int32_t val = 0;
+  if (cudaMemcpy(&val, w, sizeof(val), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+  if (val != 0) {
+    const int32_t zero = 0;
+    if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return KDA_ERR_CUDA;
+  }
+  *code = val;
+  return val ? KDA_ERR_DEVICE : KDA_OK;
+}
+
+kda_status_t kda_set_stage_events(void* const* events, int32_t count) {
+  if (count < 0 || count > 8) return KDA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_stage_mutex);
+  g_stages.n = events ? count : 0;
+  for (int i = 0; i < g_stages.n; ++i) g_stages.ev[i] = static_cast<cudaEvent_t>(events[i]);
+  return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+// kda_common.cuh -- small device helpers shared by the library's kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// ---------------------------------------------------------------- element access
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Load element i of a q/k/v row stored as fp32 (IS_BF16 = false) or bf16.
+template <bool IS_BF16>
+__device__ __forceinline__ float load_elem(const void* base, int64_t i) {
+  if constexpr (IS_BF16) {
+    return bf16_bits_to_f32(static_cast<const uint16_t*>(base)[i]);
+  } else {
+    return static_cast<const float*>(base)[i];
+  }
+}
+
+// Four consecutive elements (16-byte aligned for fp32, 8-byte for bf16).
+template <bool IS_BF16>
+__device__ __forceinline__ float4 load4(const void* base, int64_t i) {
+  if constexpr (IS_BF16) {
+    uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+  } else {
+    return *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+  }
+}
+
+template <bool IS_BF16>
+__device__ __forceinline__ void store4(void* base, int64_t i, float4 v) {
+  if constexpr (IS_BF16) {
+    uint32_t lo = static_cast<uint32_t>(f32_to_bf16_bits(v.x)) |
+                  (static_cast<uint32_t>(f32_to_bf16_bits(v.y)) << 16);
+    uint32_t hi = static_cast<uint32_t>(f32_to_bf16_bits(v.z)) |
+                  (static_cast<uint32_t>(f32_to_bf16_bits(v.w)) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(base) + i) = make_uint2(lo, hi);
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(base) + i) = v;
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Record the first device-side problem; later ones keep the first code.
+__device__ __forceinline__ void raise_device_error(int32_t* err, int32_t code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// ---------------------------------------------------------------- host-side launch records
+
+// Optional per-kernel timing events (kda_set_stage_events): mark(0) before the
+// first launch of a call, mark(i) after its i-th kernel.
+struct Stages {
+  cudaEvent_t ev[8];
+  int n;
+  void mark(int i, cudaStream_t s) const {
+    if (i < n) cudaEventRecord(ev[i], s);
+  }
+};
+
+// Per-call problem description handed to the kernels (plain values, device pointers).
+struct Problem {
+  int32_t num_seqs, HK, HV, D, num_slots, chunk;
+  int64_t T;
+  float scale;
+  int32_t l2norm;
+  uint32_t flags;
+  int64_t q_stride, k_stride, v_stride;  // elements between tokens
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* beta;
+  const float* g;
+  const uint32_t* offsets;
+  const uint32_t* slot_idx;
+  void* pool;
+  float* o;
+  int32_t* err;
+};
+
+}  // namespace kda

@@ -1,0 +1,89 @@
+// plan.cu -- device-side validation of a ragged batch and its chunk table.
+#include "prefill_plan.cuh"
+
+namespace kda {
+
+size_t plan_layout(const Problem& P, char* base, size_t off, PlanView* out) {
+  auto take = [&](size_t bytes) -> char* {
+    char* p = base ? base + off : nullptr;
+    off += (bytes + 255) & ~size_t(255);
+    return p;
+  };
+  PlanView v;
+  v.info = reinterpret_cast<int32_t*>(take(4 * sizeof(int32_t)));
+  v.seq_chunk0 = reinterpret_cast<int32_t*>(take((static_cast<size_t>(P.num_seqs) + 1) * 4));
+  v.chunks = reinterpret_cast<ChunkInfo*>(take(static_cast<size_t>(plan_max_chunks(P)) * sizeof(ChunkInfo)));
+  if (out) *out = v;
+  return off;
+}
+
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem P, PlanView plan, int max_chunks) {
+  __shared__ int s_bad;
+  __shared__ int s_scan[kPlanThreads];
+  const int B = P.num_seqs, C = P.chunk, tid = threadIdx.x;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+  if (tid == 0 && (P.offsets[0] != 0u || static_cast<int64_t>(P.offsets[B]) != P.T)) atomicOr(&s_bad, 1);
+  for (int b = tid; b < B; b += kPlanThreads) {
+    if (P.offsets[b + 1] < P.offsets[b]) atomicOr(&s_bad, 1);
+    if (P.slot_idx[b] >= static_cast<uint32_t>(P.num_slots)) atomicOr(&s_bad, 2);
+  }
+  if (P.flags & KDA_FLAG_CHECKED) {
+    const int64_t pairs = static_cast<int64_t>(B) * B;
+    for (int64_t pr = tid; pr < pairs; pr += kPlanThreads) {
+      const int i = static_cast<int>(pr / B), j = static_cast<int>(pr % B);
+      if (i < j && P.slot_idx[i] == P.slot_idx[j]) atomicOr(&s_bad, 4);
+    }
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) {
+      raise_device_error(P.err, (s_bad & 1) ? KDA_DEVERR_OFFSETS
+                                : (s_bad & 2) ? KDA_DEVERR_SLOT_RANGE : KDA_DEVERR_SLOT_DUP);
+      plan.info[0] = 0;
+      plan.info[1] = 0;
+    }
+    return;
+  }
+  // chunk counts over a contiguous range of sequences per thread, then a block scan
+  const int per = (B + kPlanThreads - 1) / kPlanThreads;
+  const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) local += static_cast<int>((P.offsets[b + 1] - P.offsets[b] + C - 1) / C);
+  s_scan[tid] = local;
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const int add = tid >= off ? s_scan[tid - off] : 0;
+    __syncthreads();
+    s_scan[tid] += add;
+    __syncthreads();
+  }
+  int base = s_scan[tid] - local;
+  for (int b = b0; b < b1; ++b) {
+    plan.seq_chunk0[b] = base;
+    const uint32_t bos = P.offsets[b], len = P.offsets[b + 1] - bos;
+    const int nb = static_cast<int>((len + C - 1) / C);
+    for (int c = 0; c < nb && base + c < max_chunks; ++c) {
+      ChunkInfo ci;
+      ci.seq = b;
+      ci.n = static_cast<int32_t>(min(static_cast<uint32_t>(C), len - static_cast<uint32_t>(c * C)));
+      ci.t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
+      plan.chunks[base + c] = ci;
+    }
+    base += nb;
+  }
+  if (tid == kPlanThreads - 1) {
+    plan.seq_chunk0[B] = s_scan[tid];
+    plan.info[0] = s_scan[tid];
+    plan.info[1] = 1;
+  }
+}
+
+cudaError_t launch_plan(const Problem& P, const PlanView& plan, cudaStream_t stream) {
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(P, plan, plan_max_chunks(P));
+  return cudaGetLastError();
+}
+
+}  // namespace kda

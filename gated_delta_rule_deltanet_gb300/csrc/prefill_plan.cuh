@@ -1,0 +1,37 @@
+// prefill_plan.cuh -- the ragged chunk table shared by the prefill paths.
+//
+// Chunks restart at every sequence start, so a sequence of length L owns
+// ceil(L / C) chunks and only its last one may be partial.  The table is
+// built on the device from input_row_offsets (the host never sees the
+// offsets, so no synchronisation is needed); its size is bounded on the host
+// by T / C + B, which sizes the grids of the chunk-parallel kernels.
+#pragma once
+
+#include "kda_common.cuh"
+
+namespace kda {
+
+struct ChunkInfo {
+  int32_t seq;  // sequence index b
+  int32_t n;    // tokens in this chunk (1..C)
+  int64_t t0;   // first token (row of the token-major tensors)
+};
+
+struct PlanView {
+  int32_t* info;        // [0] chunks in the table, [1] 1 if the batch is valid
+  int32_t* seq_chunk0;  // [B + 1] first chunk of each sequence (prefix sums)
+  ChunkInfo* chunks;    // [max_chunks]
+};
+
+inline int plan_max_chunks(const Problem& P) {
+  return static_cast<int>(P.T / P.chunk) + P.num_seqs;
+}
+
+// Carves the plan's arrays from `base` starting at byte `off` (256-aligned
+// pieces); returns the new offset.  base == nullptr only measures.
+size_t plan_layout(const Problem& P, char* base, size_t off, PlanView* out);
+
+// Validates offsets / slots and builds the chunk table (one CTA).
+cudaError_t launch_plan(const Problem& P, const PlanView& plan, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,209 @@
+"""Torch-facing binding of libkda.so: argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+checks shapes and dtypes, derives the kda_params_t record from the tensors,
+passes raw device pointers and the current CUDA stream, and turns a non-OK
+status into an exception (the argument checks mirror the chunked DeltaNet
+launcher of "From Attention to Learned Memory", sec. 4).
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import KdaError, KdaParams
+
+_QKV_DTYPES = {torch.float32: _lib.KDA_DTYPE_F32, torch.bfloat16: _lib.KDA_DTYPE_BF16}
+_INDEX_DTYPES = (torch.int32, getattr(torch, "uint32", torch.int32))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream], device) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _row_stride(x: torch.Tensor, name: str) -> int:
+    # [T, H, D] with the last two dims dense; the token stride may be wider
+    # (a column block of a packed buffer)
+    if x.dim() != 3 or x.stride(2) != 1 or x.stride(1) != x.shape[2]:
+        raise ValueError(f"{name} must be [T, H, D] with dense (H, D) rows")
+    return int(x.stride(0)) if x.shape[0] > 1 else int(x.shape[1] * x.shape[2])
+
+
+def _check_cuda(*ts):
+    dev = None
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("all tensors must be on the same device")
+    return dev
+
+
+def make_params(*, num_seqs, num_k_heads, num_v_heads, d, num_slots, total_tokens=0, chunk=64,
+                qkv_dtype=torch.bfloat16, state_dtype=torch.float32, per_channel=True,
+                scale=0.0, l2norm=True, checked=False, q_row_stride=0, k_row_stride=0,
+                v_row_stride=0) -> KdaParams:
+    return KdaParams(num_seqs=num_seqs, num_k_heads=num_k_heads, num_v_heads=num_v_heads, d_k=d,
+                     d_v=d, num_slots=num_slots, total_tokens=total_tokens, chunk=chunk,
+                     qkv_dtype=_QKV_DTYPES[qkv_dtype], state_dtype=_QKV_DTYPES[state_dtype],
+                     decay_kind=(_lib.KDA_DECAY_PER_CHANNEL if per_channel
+                                 else _lib.KDA_DECAY_SCALAR),
+                     scale=float(scale), l2norm_qk=int(bool(l2norm)),
+                     flags=_lib.KDA_FLAG_CHECKED if checked else 0, q_row_stride=q_row_stride,
+                     k_row_stride=k_row_stride, v_row_stride=v_row_stride)
+
+
+def workspace_size(params: KdaParams) -> int:
+    n = ctypes.c_size_t(0)
+    st = _lib.load().kda_prefill_workspace_size(ctypes.byref(params), ctypes.byref(n))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_prefill_workspace_size")
+    return int(n.value)
+
+
+def _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
+                    scale, l2norm, checked):
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:
+        raise ValueError("q, k must be [T, HK, D] and v [T, HV, D]")
+    T, HK, D = q.shape
+    HV = v.shape[1]
+    if v.shape[0] != T or v.shape[2] != D:
+        raise ValueError("v must be [T, HV, D] with the same T and D as q")
+    if q.dtype not in _QKV_DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype: float32 or bfloat16")
+    if beta.dtype != torch.float32 or tuple(beta.shape) != (T, HV) or not beta.is_contiguous():
+        raise ValueError("beta must be contiguous float32 [T, HV]")
+    if log_decay.dtype != torch.float32 or not log_decay.is_contiguous():
+        raise ValueError("log_decay must be contiguous float32")
+    if tuple(log_decay.shape) == (T, HV):
+        per_channel = False
+    elif tuple(log_decay.shape) == (T, HV, D):
+        per_channel = True
+    else:
+        raise ValueError("log_decay must be [T, HV] (scalar) or [T, HV, D] (per channel)")
+    if input_row_offsets.dtype not in _INDEX_DTYPES or slot_idx.dtype not in _INDEX_DTYPES:
+        raise ValueError("input_row_offsets and slot_idx must be int32/uint32")
+    if not input_row_offsets.is_contiguous() or not slot_idx.is_contiguous():
+        raise ValueError("input_row_offsets and slot_idx must be contiguous")
+    B = input_row_offsets.numel() - 1
+    if B < 0 or slot_idx.numel() != B:
+        raise ValueError("input_row_offsets must have B+1 entries and slot_idx B")
+    if (state_pool.dim() != 4 or state_pool.shape[1] != HV or state_pool.shape[2] != D
+            or state_pool.shape[3] != D or state_pool.dtype not in _QKV_DTYPES
+            or not state_pool.is_contiguous()):
+        raise ValueError("state_pool must be contiguous [num_slots, HV, D, D] float32/bfloat16")
+    return make_params(num_seqs=B, num_k_heads=HK, num_v_heads=HV, d=D,
+                       num_slots=state_pool.shape[0], total_tokens=T, chunk=chunk,
+                       qkv_dtype=q.dtype, state_dtype=state_pool.dtype, per_channel=per_channel,
+                       scale=scale, l2norm=l2norm, checked=checked,
+                       q_row_stride=_row_stride(q, "q"), k_row_stride=_row_stride(k, "k"),
+                       v_row_stride=_row_stride(v, "v"))
+
+
+def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+            log_decay: torch.Tensor, input_row_offsets: torch.Tensor, slot_idx: torch.Tensor,
+            state_pool: torch.Tensor, *, chunk: int = 64, scale: float = 0.0,
+            l2norm: bool = True, checked: bool = False, out: Optional[torch.Tensor] = None,
+            workspace: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Chunkwise gated-delta-rule prefill (kda_prefill_fwd).  Returns o [T, HV, D] fp32.
+
+    The pool slots named by slot_idx are updated in place with each sequence's final state.
+    """
+    dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool)
+    p = _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
+                        scale, l2norm, checked)
+    T, HV, D = v.shape
+    if out is None:
+        out = torch.empty((T, HV, D), dtype=torch.float32, device=dev)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (T, HV, D) or not out.is_contiguous():
+        raise ValueError("out must be contiguous float32 [T, HV, D]")
+    need = workspace_size(p)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    st = _lib.load().kda_prefill_fwd(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_decay),
+        _ptr(input_row_offsets), _ptr(slot_idx), _ptr(state_pool), _ptr(out), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream, dev))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_prefill_fwd")
+    return out
+
+
+def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                log_decay: torch.Tensor, slot_idx: torch.Tensor, state_pool: torch.Tensor, *,
+                scale: float = 0.0, l2norm: bool = True, out: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """One recurrent decode step (kda_decode_step) for B sequences.  Returns o [B, HV, D] fp32."""
+    dev = _check_cuda(q, k, v, beta, log_decay, slot_idx, state_pool)
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[0] != q.shape[0]:
+        raise ValueError("q, k must be [B, HK, D] and v [B, HV, D]")
+    B, HK, D = q.shape
+    HV = v.shape[1]
+    if q.dtype not in _QKV_DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype: float32 or bfloat16")
+    if beta.dtype != torch.float32 or tuple(beta.shape) != (B, HV) or not beta.is_contiguous():
+        raise ValueError("beta must be contiguous float32 [B, HV]")
+    if tuple(log_decay.shape) == (B, HV):
+        per_channel = False
+    elif tuple(log_decay.shape) == (B, HV, D):
+        per_channel = True
+    else:
+        raise ValueError("log_decay must be [B, HV] or [B, HV, D]")
+    if log_decay.dtype != torch.float32 or not log_decay.is_contiguous():
+        raise ValueError("log_decay must be contiguous float32")
+    if slot_idx.dtype not in _INDEX_DTYPES or slot_idx.numel() != B or not slot_idx.is_contiguous():
+        raise ValueError("slot_idx must be contiguous int32/uint32 [B]")
+    if (state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (HV, D, D)
+            or state_pool.dtype not in _QKV_DTYPES or not state_pool.is_contiguous()):
+        raise ValueError("state_pool must be contiguous [num_slots, HV, D, D]")
+    p = make_params(num_seqs=B, num_k_heads=HK, num_v_heads=HV, d=D,
+                    num_slots=state_pool.shape[0], qkv_dtype=q.dtype,
+                    state_dtype=state_pool.dtype, per_channel=per_channel, scale=scale,
+                    l2norm=l2norm, q_row_stride=_row_stride(q, "q"),
+                    k_row_stride=_row_stride(k, "k"), v_row_stride=_row_stride(v, "v"))
+    if out is None:
+        out = torch.empty((B, HV, D), dtype=torch.float32, device=dev)
+    st = _lib.load().kda_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                     _ptr(log_decay), _ptr(slot_idx), _ptr(state_pool), _ptr(out),
+                                     _stream_handle(stream, dev))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_decode_step")
+    return out
+
+
+def get_device_error(stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronises the stream and returns (and clears) the device error code (0 = none)."""
+    code = ctypes.c_int32(0)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    st = _lib.load().kda_get_device_error(ctypes.c_void_p(s.cuda_stream), ctypes.byref(code))
+    if st not in (_lib.KDA_OK, _lib.KDA_ERR_DEVICE):
+        raise KdaError(st, "kda_get_device_error")
+    return int(code.value)
+
+
+def set_stage_events(events) -> None:
+    """Register torch.cuda.Event objects (enable_timing=True) that later library calls
+    record on their stream: events[0] before the first kernel, events[i] after kernel i
+    (kda_set_stage_events).  An empty list clears the registration."""
+    events = list(events)
+    if len(events) > 8:
+        raise ValueError("at most 8 stage events")
+    for e in events:
+        e.record()                      # torch creates CUDA events lazily; make them exist
+    handles = (ctypes.c_void_p * max(len(events), 1))(*[e.cuda_event for e in events])
+    st = _lib.load().kda_set_stage_events(handles if events else None, len(events))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_set_stage_events")

@@ -1,0 +1,191 @@
+/*
+ * kda.h -- C ABI of the GB300 gated-delta-rule forward library (libkda.so).
+ *
+ * The library computes the forward pass of the gated delta rule in its general
+ * per-channel form, Kimi Delta Attention (KDA), and its special cases Gated
+ * DeltaNet (one decay per head and token) and DeltaNet (no decay, log-decay 0).
+ * For each sequence b, value head h and token t of the sequence, with key head
+ * kh = h / (num_v_heads / num_k_heads) and S the d_v x d_k state of the
+ * derivation ("You Could Have Come Up With Kimi Delta Attention", sec. 4, the
+ * boxed KDA update; Modular MAX "gated_delta" module, the five per-token steps):
+ *
+ *     k^ = k[t,kh] / sqrt(|k[t,kh]|^2 + 1e-6)        (when l2norm_qk != 0)
+ *     q^ = scale * q[t,kh] / sqrt(|q[t,kh]|^2 + 1e-6)
+ *     S  = S Diag(exp(g[t,h]))                         forget (per key channel)
+ *     e  = beta[t,h] (v[t,h] - S k^)                   predict and correct
+ *     S  = S + e k^T                                   write
+ *     o[t,h] = S q^                                    read, after the write
+ *
+ * Prefill runs the chunkwise (WY/UT) schedule of the same recurrence ("From
+ * Attention to Learned Memory", sec. 4; KDA page sec. 6), which is exact up to
+ * rounding; decode runs one token per sequence.
+ *
+ * Conventions shared by every entry point
+ *   - All data pointers are DEVICE pointers; the caller allocates and owns every
+ *     buffer (inputs, outputs, state pool, workspace).  The library never
+ *     allocates, frees or synchronises on these paths.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t, passed as
+ *     void*; NULL is the legacy default stream).  Inputs must stay valid until
+ *     the stream reaches the enqueued work.
+ *   - Layouts are row-major, token-major (ragged batches are concatenated along
+ *     the token axis, as in the Modular gated_delta module):
+ *         q, k          [T, num_k_heads, d_k]   (row stride settable, see below)
+ *         v             [T, num_v_heads, d_v]
+ *         beta          [T, num_v_heads]                     fp32
+ *         log_decay g   [T, num_v_heads]        (SCALAR)     fp32, g = log alpha <= 0
+ *                       [T, num_v_heads, d_k]   (PER_CHANNEL)
+ *         state_pool    [num_slots, num_v_heads, d_k, d_v]   (the transpose of the
+ *                       derivation's d_v x d_k state: key channel = row)
+ *         o             [T, num_v_heads, d_v]                fp32
+ *   - q/k/v/beta/g are read only, o is write only; the pool slots named by
+ *     slot_idx are read, then overwritten in place with the final state; every
+ *     other slot is left untouched.  Slots named twice in one call race.
+ *   - Errors: argument problems are found on the host before anything is
+ *     enqueued and returned as a status; nothing is launched then.  Problems
+ *     only the device can see (offsets not monotone or not ending at
+ *     total_tokens, a slot index >= num_slots, repeated slots under
+ *     KDA_FLAG_CHECKED) set a device error word and the affected work is
+ *     skipped -- no trap, no fault; read it with kda_get_device_error().
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KDA_ABI_VERSION 1
+
+typedef enum kda_status {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, bad enum value */
+  KDA_ERR_UNSUPPORTED = 2, /* valid but not implemented: head size, chunk, dtype combination */
+  KDA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than kda_prefill_workspace_size */
+  KDA_ERR_CUDA = 4,        /* a CUDA runtime call or a launch failed */
+  KDA_ERR_DEVICE = 5       /* kda_get_device_error: the device flagged bad offsets/slots */
+} kda_status_t;
+
+typedef enum kda_dtype { KDA_DTYPE_F32 = 0, KDA_DTYPE_BF16 = 1 } kda_dtype_t;
+
+typedef enum kda_decay_kind {
+  KDA_DECAY_SCALAR = 0,     /* Gated DeltaNet: one log-decay per (token, value head) */
+  KDA_DECAY_PER_CHANNEL = 1 /* KDA: one log-decay per (token, value head, key channel) */
+} kda_decay_kind_t;
+
+/* Check every sequence's offsets and slot and that slots are distinct on the
+ * device (without it, offsets and slot ranges are still checked, distinctness is not). */
+#define KDA_FLAG_CHECKED 1u
+
+/* Device error codes (kda_get_device_error). */
+#define KDA_DEVERR_NONE 0
+#define KDA_DEVERR_OFFSETS 1   /* input_row_offsets not monotone / not 0..total_tokens */
+#define KDA_DEVERR_SLOT_RANGE 2 /* slot_idx[b] >= num_slots */
+#define KDA_DEVERR_SLOT_DUP 3   /* a slot named twice (KDA_FLAG_CHECKED only) */
+
+typedef struct kda_params {
+  int32_t num_seqs;    /* B: sequences in the ragged batch (prefill) or decode batch */
+  int32_t num_k_heads; /* HK: heads of q and k */
+  int32_t num_v_heads; /* HV: heads of v, beta, g, o and the state; HV % HK == 0 */
+  int32_t d_k;         /* key head size; 16 or 128 */
+  int32_t d_v;         /* value head size; must equal d_k */
+  int32_t num_slots;   /* slots in state_pool */
+  int64_t total_tokens;/* T: rows of the token-major tensors (prefill; ignored by decode) */
+  int32_t chunk;       /* prefill chunk length C: 16, 32 or 64 (ignored by decode) */
+  int32_t qkv_dtype;   /* kda_dtype_t of q, k, v */
+  int32_t state_dtype; /* kda_dtype_t of state_pool (bf16 is rounded to nearest even) */
+  int32_t decay_kind;  /* kda_decay_kind_t of log_decay */
+  float scale;         /* query scale; <= 0 selects 1/sqrt(d_k) */
+  int32_t l2norm_qk;   /* nonzero: L2-normalise q and k rows before use */
+  uint32_t flags;      /* KDA_FLAG_* */
+  /* Elements between consecutive tokens of q, k, v; 0 means dense
+   * (HK*d_k, HK*d_k, HV*d_v).  Lets q, k, v be column blocks of one packed
+   * [T, 2*HK*d_k + HV*d_v] buffer.  Must keep rows 16-byte aligned. */
+  int64_t q_row_stride;
+  int64_t k_row_stride;
+  int64_t v_row_stride;
+} kda_params_t;
+
+/* Version of this ABI (KDA_ABI_VERSION).  Never fails. */
+int kda_abi_version(void);
+
+/* Static, NUL-terminated description of a status code.  Never fails. */
+const char *kda_status_string(kda_status_t status);
+
+/*
+ * Bytes of device workspace kda_prefill_fwd needs for these parameters
+ * (an upper bound that depends only on the params, not on the offsets).
+ * Returns KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED for parameters that
+ * kda_prefill_fwd would reject; *bytes is then left unchanged.
+ */
+kda_status_t kda_prefill_workspace_size(const kda_params_t *p, size_t *bytes);
+
+/*
+ * Chunkwise prefill over a ragged batch ("You Could Have Come Up With Kimi
+ * Delta Attention", sec. 6 and the pipeline of sec. 6.6; "From Attention to
+ * Learned Memory", sec. 4, WY/UT transform and blocked triangular inverse;
+ * Modular "gated_delta" module for the ragged batch, GQA and slot pool).
+ *
+ *   q, k               [T, HK, d_k], qkv_dtype, rows 16-byte aligned
+ *   v                  [T, HV, d_v], qkv_dtype
+ *   beta               [T, HV] fp32
+ *   log_decay          [T, HV] or [T, HV, d_k] fp32 (decay_kind)
+ *   input_row_offsets  [B+1] uint32: sequence b is tokens [off[b], off[b+1]);
+ *                      off[0] = 0, non-decreasing, off[B] = T.  Empty sequences
+ *                      are allowed and leave their slot untouched.
+ *   slot_idx           [B] uint32, each < num_slots: the pool slot holding
+ *                      sequence b's initial state, overwritten with its final state
+ *   state_pool         [num_slots, HV, d_k, d_v], state_dtype, in place
+ *   o                  [T, HV, d_v] fp32, written for every token
+ *   workspace          device scratch of >= kda_prefill_workspace_size bytes,
+ *                      256-byte aligned; contents on entry are ignored
+ * Returns KDA_OK once the work is enqueued.
+ */
+kda_status_t kda_prefill_fwd(const kda_params_t *p, const void *q, const void *k, const void *v,
+                             const float *beta, const float *log_decay,
+                             const uint32_t *input_row_offsets, const uint32_t *slot_idx,
+                             void *state_pool, float *o, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
+ * One recurrent decode step: one token for each of B = num_seqs sequences
+ * ("You Could Have Come Up With Kimi Delta Attention", sec. 5, fused recurrent
+ * kernel; Modular "gated_delta" module, the five per-token steps).
+ *
+ *   q, k        [B, HK, d_k], qkv_dtype     v  [B, HV, d_v], qkv_dtype
+ *   beta        [B, HV] fp32                log_decay [B, HV] or [B, HV, d_k] fp32
+ *   slot_idx    [B] uint32, each < num_slots
+ *   state_pool  [num_slots, HV, d_k, d_v], state_dtype, updated in place
+ *   o           [B, HV, d_v] fp32
+ * total_tokens and chunk are ignored.  Needs no workspace.
+ */
+kda_status_t kda_decode_step(const kda_params_t *p, const void *q, const void *k, const void *v,
+                             const float *beta, const float *log_decay, const uint32_t *slot_idx,
+                             void *state_pool, float *o, void *stream);
+
+/*
+ * Waits for `stream`, then returns the device error word of the current device
+ * in *code (KDA_DEVERR_*) and clears it.  Returns KDA_ERR_DEVICE when the word
+ * was set, KDA_OK when it was clear, KDA_ERR_CUDA when a CUDA call failed.
+ */
+kda_status_t kda_get_device_error(void *stream, int32_t *code);
+
+/*
+ * Measurement aid (no counterpart on the pages).  Registers up to 8 CUDA events
+ * (cudaEvent_t handles passed as void*, created by the caller) that later
+ * kda_prefill_fwd / kda_decode_step calls on this process record on their
+ * stream: events[0] before the first kernel, events[i] after the i-th kernel.
+ * Lets a benchmark time each kernel with CUDA events on the stream the kernel
+ * runs on.  count = 0 (or events = NULL) clears the registration.  The handles
+ * must stay valid while registered; calls from several threads share it.
+ * Returns KDA_ERR_INVALID_ARG for count < 0 or > 8.
+ */
+kda_status_t kda_set_stage_events(void *const *events, int32_t count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -133,12 +133,27 @@ def run(problem, *, pair_mask=None, nthreads: Optional[int] = None, mutant: int 
                       mutant=mutant)
 
 
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """fp64 values rounded to the nearest bf16 value (8 significant bits, ties to even).
+
+    Normal-range numbers only (the state pool never leaves it): x = m 2^e with
+    m in [0.5, 1); m 2^8 is rounded half-to-even to an integer and scaled back.
+    """
+    x = np.asarray(x, np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)
+
+
 def run_decode(dp, *, steps: Optional[int] = None, nthreads: Optional[int] = None,
                seq_mask=None):
     """The oracle on a `workloads.DecodeProblem`: each step is one token per sequence.
 
-    Returns (o fp64 [steps, B, HV, dv], final pool fp64).  `seq_mask` limits the
-    work to some sequences (others keep their initial state and zero output).
+    Between steps the state lives in the pool, so a bf16 pool holds it rounded to
+    bf16 (Modular "gated_delta" module: the pool keeps its own dtype, independent of
+    the working precision); within a step the arithmetic is fp64.
+    Returns (o fp64 [steps, B, HV, dv], final pool fp64, unrounded after the last
+    step).  `seq_mask` limits the work to some sequences (others keep their initial
+    state and zero output).
     """
     steps = dp.steps if steps is None else steps
     B = dp.num_seqs
@@ -149,6 +164,8 @@ def run_decode(dp, *, steps: Optional[int] = None, nthreads: Optional[int] = Non
     if seq_mask is not None:
         pair_mask = np.repeat(np.asarray(seq_mask, dtype=np.uint8), dp.num_v_heads)
     for s in range(steps):
+        if s > 0 and dp.state_dtype == "bf16":
+            pool = round_to_bf16(pool)
         o, pool = run_arrays(offsets=offsets, slot_idx=dp.slot_idx,
                              q=_widen(dp.q[s], dp.qkv_dtype), k=_widen(dp.k[s], dp.qkv_dtype),
                              v=_widen(dp.v[s], dp.qkv_dtype), beta=dp.beta[s], g=dp.g[s],

@@ -1,0 +1,137 @@
+"""The C ABI without a GPU: the library loads, exports every function include/kda.h declares,
+and rejects bad arguments on the host (before anything touches CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_deltanet_gb300 import _lib, build as kbuild
+from gated_delta_rule_deltanet_gb300.kda import make_params
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return _lib.load()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "kda.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_params_struct_layout_matches_header():
+    # kda_params_t: 6 x int32, int64, 4 x int32, float, int32, uint32, (pad), 3 x int64
+    assert ctypes.sizeof(_lib.KdaParams) == 88
+    assert _lib.KdaParams.total_tokens.offset == 24
+    assert _lib.KdaParams.q_row_stride.offset == 64
+
+
+def test_version_and_strings(lib):
+    assert lib.kda_abi_version() == 1
+    for s in range(6):
+        assert lib.kda_status_string(s)
+    assert lib.kda_status_string(0) == b"ok"
+
+
+def good(**kw):
+    base = dict(num_seqs=2, num_k_heads=4, num_v_heads=8, d=128, num_slots=4, total_tokens=100,
+                chunk=64)
+    base.update(kw)
+    return make_params(**base)
+
+
+def ws_status(lib, p):
+    n = ctypes.c_size_t(0)
+    return lib.kda_prefill_workspace_size(ctypes.byref(p), ctypes.byref(n)), n.value
+
+
+def test_workspace_size_positive_and_monotone(lib):
+    s, a = ws_status(lib, good())
+    assert s == _lib.KDA_OK and a > 0
+    s, b = ws_status(lib, good(total_tokens=10_000))
+    assert s == _lib.KDA_OK and b > a
+    s, c = ws_status(lib, good(num_seqs=0, total_tokens=0))
+    assert s == _lib.KDA_OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(num_k_heads=3), _lib.KDA_ERR_INVALID_ARG),        # HV % HK != 0
+    (dict(num_k_heads=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(num_slots=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(num_seqs=-1), _lib.KDA_ERR_INVALID_ARG),
+    (dict(total_tokens=-5), _lib.KDA_ERR_INVALID_ARG),
+    (dict(total_tokens=1 << 31), _lib.KDA_ERR_INVALID_ARG),
+    (dict(d=64), _lib.KDA_ERR_UNSUPPORTED),                 # head size not built
+    (dict(chunk=48), _lib.KDA_ERR_UNSUPPORTED),             # chunk not in {16, 32, 64}
+    (dict(chunk=128), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(q_row_stride=100), _lib.KDA_ERR_INVALID_ARG),     # narrower than a row
+    (dict(q_row_stride=4 * 128 + 1), _lib.KDA_ERR_INVALID_ARG),  # rows not 16-byte aligned
+])
+def test_bad_params_rejected_on_host(lib, kw, status):
+    assert ws_status(lib, good(**kw))[0] == status
+
+
+def test_bad_enums_rejected(lib):
+    p = good()
+    p.qkv_dtype = 7
+    assert ws_status(lib, p)[0] == _lib.KDA_ERR_INVALID_ARG
+    p = good()
+    p.decay_kind = 3
+    assert ws_status(lib, p)[0] == _lib.KDA_ERR_INVALID_ARG
+    p = good()
+    p.flags = 0x80
+    assert ws_status(lib, p)[0] == _lib.KDA_ERR_INVALID_ARG
+    p = good()
+    p.d_v = 16
+    assert ws_status(lib, p)[0] == _lib.KDA_ERR_UNSUPPORTED
+
+
+def test_null_and_misaligned_pointers_rejected_before_launch(lib):
+    """These return before any CUDA call, so they run without a GPU."""
+    p = good()
+    P = ctypes.c_void_p
+    a = P(1 << 20)                     # never dereferenced: validation fails first
+    assert lib.kda_prefill_fwd(None, a, a, a, a, a, a, a, a, a, a, 1 << 30, None) == \
+        _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill_fwd(ctypes.byref(p), a, a, a, a, a, None, a, a, a, a, 1 << 30,
+                               None) == _lib.KDA_ERR_INVALID_ARG
+    mis = P((1 << 20) + 8)
+    assert lib.kda_prefill_fwd(ctypes.byref(p), mis, a, a, a, a, a, a, a, a, a, 1 << 30,
+                               None) == _lib.KDA_ERR_INVALID_ARG
+    # workspace missing / too small / misaligned
+    assert lib.kda_prefill_fwd(ctypes.byref(p), a, a, a, a, a, a, a, a, a, None, 1 << 30,
+                               None) == _lib.KDA_ERR_WORKSPACE
+    assert lib.kda_prefill_fwd(ctypes.byref(p), a, a, a, a, a, a, a, a, a, a, 16, None) == \
+        _lib.KDA_ERR_WORKSPACE
+    assert lib.kda_prefill_fwd(ctypes.byref(p), a, a, a, a, a, a, a, a, a, P((1 << 20) + 16),
+                               1 << 30, None) == _lib.KDA_ERR_WORKSPACE
+    # decode
+    assert lib.kda_decode_step(ctypes.byref(p), a, a, a, a, None, a, a, a, None) == \
+        _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_decode_step(ctypes.byref(p), a, a, mis, a, a, a, a, a, None) == \
+        _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_get_device_error(None, None) == _lib.KDA_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op(lib):
+    """num_seqs = 0 returns OK without touching CUDA (nothing to do)."""
+    p = good(num_seqs=0, total_tokens=0)
+    assert lib.kda_prefill_fwd(ctypes.byref(p), None, None, None, None, None, None, None, None,
+                               None, None, 0, None) == _lib.KDA_OK
+    assert lib.kda_decode_step(ctypes.byref(p), None, None, None, None, None, None, None, None,
+                               None) == _lib.KDA_OK

@@ -1,0 +1,270 @@
+"""Parity of the CUDA library (through the C ABI) with the fp64 oracle.
+
+Tolerance (per tensor): rel = max|x - ref| / max|ref|, ref the fp64 oracle on the same
+inputs; <= 2e-3 for bf16 q/k/v, <= 1e-4 for fp32 q/k/v.  A bf16 state pool is compared
+after discounting half a bf16 ulp of the reference (the storage rounding itself).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_deltanet_gb300 as kda
+import oracle
+import workloads
+from workloads import torch_io
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-3, "f32": 1e-4}
+DEV = "cuda:0"
+
+
+def rel_err(x, ref):
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = np.max(np.abs(ref))
+    assert np.all(np.isfinite(x)), "non-finite output"
+    return float(np.max(np.abs(x - ref)) / (den if den > 0 else 1.0))
+
+
+def rel_err_bf16_storage(x, ref):
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    e = np.floor(np.log2(np.maximum(np.abs(ref), 1e-300)))
+    half_ulp = np.exp2(e - 8)
+    den = np.max(np.abs(ref))
+    return float(np.max(np.maximum(np.abs(x - ref) - half_ulp, 0.0)) / (den if den > 0 else 1.0))
+
+
+def state_err(p, pool_gpu, pool_ref):
+    touched = np.asarray(p.slot_idx, np.int64)
+    x, r = pool_gpu[touched], pool_ref[touched]
+    return rel_err_bf16_storage(x, r) if p.state_dtype == "bf16" else rel_err(x, r)
+
+
+def gpu_prefill(p, chunk=None, **kw):
+    t = torch_io.prefill_inputs(p, DEV)
+    o = kda.prefill(**t, chunk=chunk or p.chunk, scale=p.scale, **kw)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    return o.double().cpu().numpy(), torch_io.pool_to_f64(t["state_pool"]), t
+
+
+def check_prefill(p, chunk=None, nthreads=None):
+    o, pool, _ = gpu_prefill(p, chunk)
+    o_ref, pool_ref = oracle.run(p, nthreads=nthreads)
+    tol = TOL[p.qkv_dtype]
+    eo, es = rel_err(o, o_ref), state_err(p, pool, pool_ref)
+    assert eo <= tol and es <= tol, f"{p.name}: o err {eo:.3e}, state err {es:.3e} (tol {tol})"
+    return eo, es
+
+
+def small(name, lengths, HK, HV, d, qkv, state, decay, chunk, seed, zero=False, slots=None):
+    return workloads.make_problem(name, num_seqs=len(lengths), lengths=lengths, num_k_heads=HK,
+                                  num_v_heads=HV, d=d, qkv_dtype=qkv, state_dtype=state,
+                                  decay_kind=decay, chunk=chunk, zero_state=zero,
+                                  num_slots=slots, seed=seed)
+
+
+def test_tiny_gdn_workload():
+    check_prefill(workloads.workload("tiny_gdn"))
+
+
+# ragged tails, several tiles, every chunk size, both dtypes, GQA, both decay kinds
+SMALL = [
+    ("f32-d16-c16", [1, 15, 16, 17, 64, 100], 1, 2, 16, "f32", "f32", "per_channel", 16),
+    ("f32-d16-c32", [33, 5, 70], 2, 2, 16, "f32", "f32", "scalar", 32),
+    ("f32-d128-c64", [130, 64, 1], 1, 2, 128, "f32", "f32", "per_channel", 64),
+    ("f32-d128-c16", [47, 81], 2, 4, 128, "f32", "bf16", "scalar", 16),
+    ("bf16-d128-c64-kda", [300, 1, 63, 65, 128], 2, 4, 128, "bf16", "f32", "per_channel", 64),
+    ("bf16-d128-c32-gdn", [257, 31], 4, 4, 128, "bf16", "f32", "scalar", 32),
+    ("bf16-d128-c16-kda", [100, 9], 1, 4, 128, "bf16", "bf16", "per_channel", 16),
+    ("bf16-d16-c64", [129, 200], 2, 2, 16, "bf16", "bf16", "per_channel", 64),
+]
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=[c[0] for c in SMALL])
+def test_small_configs(cfg):
+    name, lengths, HK, HV, d, qkv, state, decay, chunk = cfg
+    check_prefill(small(name, lengths, HK, HV, d, qkv, state, decay, chunk, seed=hash(name) % 1000,
+                        slots=len(lengths) + 3))
+
+
+@pytest.mark.parametrize("name", ["gdn_prefill", "kda_prefill", "ragged_gqa_kda"])
+def test_full_prefill_workload(name):
+    """Every output and final state of the full workload against the oracle."""
+    check_prefill(workloads.workload(name))
+
+
+def test_full_decode_workload():
+    """256 sequences x 64 decode steps: every output of every step and the final pool."""
+    dp = workloads.workload("kda_decode")
+    t = torch_io.decode_inputs(dp, DEV)
+    pool = t["state_pool"]
+    outs = []
+    for s in range(dp.steps):
+        outs.append(kda.decode_step(t["q"][s], t["k"][s], t["v"][s], t["beta"][s],
+                                    t["log_decay"][s], t["slot_idx"], pool))
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 0
+    o = torch.stack(outs).double().cpu().numpy()
+    o_ref, pool_ref = oracle.run_decode(dp)
+    eo = rel_err(o, o_ref)
+    es = rel_err(torch_io.pool_to_f64(pool), pool_ref)
+    assert eo <= TOL["bf16"] and es <= TOL["bf16"], (eo, es)
+
+
+@pytest.mark.parametrize("state", ["f32", "bf16"])
+@pytest.mark.parametrize("decay", ["scalar", "per_channel"])
+@pytest.mark.parametrize("d", [16, 128])
+def test_decode_small(state, decay, d):
+    dp = workloads.make_decode_problem("dec", num_seqs=5, steps=7, num_k_heads=2, num_v_heads=4,
+                                       d=d, qkv_dtype="bf16", state_dtype=state,
+                                       decay_kind=decay, zero_state=False, seed=d + 3,
+                                       num_slots=9)
+    t = torch_io.decode_inputs(dp, DEV)
+    outs = [kda.decode_step(t["q"][s], t["k"][s], t["v"][s], t["beta"][s], t["log_decay"][s],
+                            t["slot_idx"], t["state_pool"]) for s in range(dp.steps)]
+    o = torch.stack(outs).double().cpu().numpy()
+    o_ref, pool_ref = oracle.run_decode(dp)
+    pool = torch_io.pool_to_f64(t["state_pool"])
+    assert rel_err(o, o_ref) <= TOL["bf16"]
+    touched = dp.slot_idx.astype(np.int64)
+    err = rel_err_bf16_storage if state == "bf16" else rel_err
+    assert err(pool[touched], pool_ref[touched]) <= TOL["bf16"]
+    untouched = np.setdiff1d(np.arange(dp.num_slots), touched)
+    np.testing.assert_array_equal(pool[untouched],
+                                  workloads.as_f32(dp.pool, state)[untouched].astype(np.float64))
+
+
+def test_decode_steps_equal_prefill_on_gpu():
+    """Two schedules of one recurrence: n decode steps == one prefill of those n tokens."""
+    dp = workloads.make_decode_problem("d", num_seqs=6, steps=20, num_k_heads=2, num_v_heads=4,
+                                       d=128, qkv_dtype="bf16", state_dtype="f32",
+                                       decay_kind="per_channel", zero_state=False, seed=77)
+    t = torch_io.decode_inputs(dp, DEV)
+    pool_a = t["state_pool"].clone()
+    pool_b = t["state_pool"].clone()
+    o_dec = torch.stack([kda.decode_step(t["q"][s], t["k"][s], t["v"][s], t["beta"][s],
+                                         t["log_decay"][s], t["slot_idx"], pool_a)
+                         for s in range(dp.steps)])            # [S, B, HV, D]
+    tm = lambda x: x.transpose(0, 1).reshape((-1,) + tuple(x.shape[2:])).contiguous()
+    offs = torch.arange(dp.num_seqs + 1, dtype=torch.int32, device=DEV) * dp.steps
+    o_pre = kda.prefill(tm(t["q"]), tm(t["k"]), tm(t["v"]), tm(t["beta"]), tm(t["log_decay"]),
+                        offs, t["slot_idx"], pool_b, chunk=16)
+    o_dec = o_dec.transpose(0, 1).reshape(o_pre.shape)
+    assert rel_err(o_pre.cpu().numpy(), o_dec.cpu().numpy()) <= TOL["bf16"]
+    assert rel_err(pool_b.cpu().numpy(), pool_a.cpu().numpy()) <= TOL["bf16"]
+
+
+def test_prefill_split_resumes_from_pool():
+    """S0 is the state of the cached prefix: prefill(x[:a]) then prefill(x[a:]) == prefill(x)."""
+    p = small("split", [333], 2, 4, 128, "bf16", "f32", "per_channel", 64, seed=5)
+    full_o, full_pool, _ = gpu_prefill(p)
+    a = 150
+    def part(lo, hi, pool):
+        q = dict(p.__dict__)
+        sub = workloads.Problem(**{**q, "offsets": np.array([0, hi - lo], np.uint32),
+                                   "q": p.q[lo:hi], "k": p.k[lo:hi], "v": p.v[lo:hi],
+                                   "beta": p.beta[lo:hi], "g": p.g[lo:hi], "pool": pool})
+        return sub
+    t1 = part(0, a, p.pool)
+    o1, pool1, _ = gpu_prefill(t1)
+    t2 = part(a, 333, np.ascontiguousarray(pool1.astype(np.float32)))
+    o2, pool2, _ = gpu_prefill(t2)
+    assert rel_err(np.concatenate([o1, o2]), full_o) <= TOL["bf16"]
+    assert rel_err(pool2, full_pool) <= TOL["bf16"]
+
+
+def test_untouched_slots_and_packing_order():
+    """Slots not in slot_idx are bit-identical; packing order does not change any result."""
+    p = small("pack", [70, 0, 200, 1, 129], 2, 4, 128, "bf16", "bf16", "per_channel", 64,
+              seed=9, slots=11)
+    o, pool, _ = gpu_prefill(p)
+    untouched = np.setdiff1d(np.arange(p.num_slots), p.slot_idx.astype(np.int64))
+    np.testing.assert_array_equal(pool[untouched],
+                                  workloads.as_f32(p.pool, "bf16")[untouched].astype(np.float64))
+    # the empty sequence's slot is untouched too
+    empty_slot = int(p.slot_idx[1])
+    np.testing.assert_array_equal(pool[empty_slot],
+                                  workloads.as_f32(p.pool, "bf16")[empty_slot].astype(np.float64))
+    # reverse the packing order of the sequences
+    order = [4, 3, 2, 1, 0]
+    L = p.lengths
+    segs = [slice(int(p.offsets[b]), int(p.offsets[b + 1])) for b in order]
+    cat = lambda a: np.concatenate([a[s] for s in segs])
+    offs = np.concatenate([[0], np.cumsum(L[order])]).astype(np.uint32)
+    rp = workloads.Problem(**{**p.__dict__, "offsets": offs, "q": cat(p.q), "k": cat(p.k),
+                              "v": cat(p.v), "beta": cat(p.beta), "g": cat(p.g),
+                              "slot_idx": p.slot_idx[order]})
+    o2, pool2, _ = gpu_prefill(rp)
+    for j, b in enumerate(order):
+        np.testing.assert_allclose(o2[int(offs[j]):int(offs[j + 1])], o[segs[j]], rtol=0, atol=0)
+    np.testing.assert_array_equal(pool2, pool)
+
+
+def test_gqa_equals_repeated_heads():
+    """Key head = value head // (HV/HK): GQA equals MHA with q, k repeated per group."""
+    p = small("gqa", [90, 37], 2, 6, 128, "bf16", "f32", "per_channel", 32, seed=13)
+    o, pool, _ = gpu_prefill(p)
+    rep = np.repeat(np.arange(2), 3)
+    m = workloads.Problem(**{**p.__dict__, "num_k_heads": 6,
+                             "q": np.ascontiguousarray(p.q[:, rep]),
+                             "k": np.ascontiguousarray(p.k[:, rep])})
+    o2, pool2, _ = gpu_prefill(m)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(pool, pool2)
+
+
+@pytest.mark.parametrize("decay", ["scalar", "per_channel"])
+def test_chunk_size_invariance(decay):
+    """Every valid chunk size gives the same result (up to rounding)."""
+    p = small("cinv", [200, 77], 2, 2, 128, "bf16", "f32", decay, 64, seed=17)
+    o64, s64, _ = gpu_prefill(p, chunk=64)
+    for c in (16, 32):
+        o, s, _ = gpu_prefill(p, chunk=c)
+        assert rel_err(o, o64) <= TOL["bf16"] and rel_err(s, s64) <= TOL["bf16"]
+
+
+def test_packed_qkv_row_strides():
+    """q, k, v as column blocks of one packed [T, 2 HK D + HV D] buffer."""
+    p = small("packed", [77, 130], 2, 4, 128, "bf16", "f32", "per_channel", 64, seed=21)
+    o_ref, pool_ref, _ = gpu_prefill(p)
+    t = torch_io.prefill_inputs(p, DEV)
+    T, HK, D = t["q"].shape
+    HV = t["v"].shape[1]
+    packed = torch.cat([t["q"].reshape(T, -1), t["k"].reshape(T, -1), t["v"].reshape(T, -1)], 1)
+    q = packed[:, :HK * D].view(T, HK, D)
+    k = packed[:, HK * D:2 * HK * D].view(T, HK, D)
+    v = packed[:, 2 * HK * D:].view(T, HV, D)
+    o = kda.prefill(q, k, v, t["beta"], t["log_decay"], t["input_row_offsets"], t["slot_idx"],
+                    t["state_pool"], chunk=64)
+    np.testing.assert_array_equal(o.double().cpu().numpy(), o_ref)
+    np.testing.assert_array_equal(torch_io.pool_to_f64(t["state_pool"]), pool_ref)
+
+
+def test_device_errors_skip_work_without_faulting():
+    """Bad offsets / slots are caught by the kernels' own checks: error word set, work skipped."""
+    p = small("err", [40, 50], 1, 2, 128, "bf16", "f32", "scalar", 64, seed=23, slots=3)
+    t = torch_io.prefill_inputs(p, DEV)
+    before = t["state_pool"].clone()
+    bad_slots = torch.tensor([0, 7], dtype=torch.int32, device=DEV)       # 7 >= num_slots
+    kda.prefill(**{**t, "slot_idx": bad_slots}, chunk=64)
+    assert kda.get_device_error() == 2
+    assert torch.equal(t["state_pool"], before)
+    bad_offs = torch.tensor([0, 60, 50], dtype=torch.int32, device=DEV)   # ends before T=90
+    kda.prefill(**{**t, "input_row_offsets": bad_offs}, chunk=64)
+    assert kda.get_device_error() == 1
+    dup = torch.tensor([1, 1], dtype=torch.int32, device=DEV)
+    kda.prefill(**{**t, "slot_idx": dup}, chunk=64, checked=True)
+    assert kda.get_device_error() == 3
+    assert torch.equal(t["state_pool"], before)
+    # decode: a slot out of range
+    dp = workloads.make_decode_problem("e", num_seqs=2, steps=1, num_k_heads=1, num_v_heads=2,
+                                       d=128, qkv_dtype="bf16", state_dtype="f32",
+                                       decay_kind="scalar", zero_state=False, seed=3, num_slots=2)
+    td = torch_io.decode_inputs(dp, DEV)
+    kda.decode_step(td["q"][0], td["k"][0], td["v"][0], td["beta"][0], td["log_decay"][0],
+                    torch.tensor([1, 5], dtype=torch.int32, device=DEV), td["state_pool"])
+    assert kda.get_device_error() == 2
+    assert kda.get_device_error() == 0            # reading clears the word

@@ -326,3 +326,17 @@ def test_decode_steps_equal_prefill():
         per_channel=True, pool=workloads.as_f32(dp.pool, dp.state_dtype), scale=0.0, nthreads=2)
     np.testing.assert_allclose(pool_dec, pool_pre, rtol=0, atol=1e-14)
     np.testing.assert_allclose(np.swapaxes(o_dec, 0, 1).reshape(B * S, 4, 8), o_pre, atol=1e-14)
+
+
+def test_round_to_bf16_matches_bit_level_rounding():
+    """The oracle's bf16 rounding equals round-to-nearest-even on the bit pattern (for
+    values exactly representable in fp32, including exact ties)."""
+    import workloads
+    r = rng(50)
+    x = (r.standard_normal(10000) * np.exp(r.uniform(-8, 8, 10000))).astype(np.float32)
+    ties = np.array([1.00390625, 1.01171875, -3.0078125, 0.0], np.float32)  # 1+2^-8, 1+3*2^-8
+    x = np.concatenate([x, ties])
+    ref = workloads.bf16_bits_to_f32(workloads.f32_to_bf16_bits(x)).astype(np.float64)
+    np.testing.assert_array_equal(oracle.round_to_bf16(x.astype(np.float64)), ref)
+    assert oracle.round_to_bf16(np.array([1.00390625]))[0] == 1.0          # tie to even
+    assert oracle.round_to_bf16(np.array([1.01171875]))[0] == 1.015625     # tie to even (up)

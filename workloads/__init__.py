@@ -48,8 +48,10 @@ PER_CHANNEL = "per_channel"
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round fp32 to bf16 (round to nearest, ties to even); returns uint16 bits."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    b = x.view(np.uint32).astype(np.uint64)
-    rounded = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    b = x.view(np.uint32)
+    # add 0x7FFF plus the lowest kept bit, then truncate (no overflow for finite inputs
+    # below the largest bf16 magnitude, which is all these workloads produce)
+    rounded = (b + (np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1)))) >> np.uint32(16)
     return rounded.astype(np.uint16)
 
 
@@ -71,7 +73,7 @@ def _store(x32: np.ndarray, dtype: str) -> np.ndarray:
 def _unit_rows(x: np.ndarray) -> np.ndarray:
     # Input distribution only: directions uniform on the sphere (a Gaussian
     # draw scaled to unit length), as the workload description states.
-    n = np.sqrt(np.sum(x.astype(np.float64) ** 2, axis=-1, keepdims=True))
+    n = np.sqrt(np.einsum("...i,...i->...", x, x, dtype=np.float64))[..., None]
     return (x / n).astype(np.float32)
 
 

@@ -28,7 +28,9 @@ KDA_DEVERR_SLOT_DUP = 3
 # every function include/kda.h declares
 EXPORTS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_size",
            "kda_prefill_fwd", "kda_decode_step", "kda_get_device_error",
-           "kda_set_stage_events")
+           "kda_set_stage_events", "kda_prefill_fwd_no_alloc")
+
+KDA_NO_ALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class KdaParams(ctypes.Structure):
@@ -96,6 +98,8 @@ def load():
         L.kda_decode_step.restype = ctypes.c_int
         L.kda_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
         L.kda_get_device_error.restype = ctypes.c_int
+        L.kda_prefill_fwd_no_alloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P]
+        L.kda_prefill_fwd_no_alloc.restype = ctypes.c_int
         L.kda_set_stage_events.argtypes = [P, ctypes.c_int32]
         L.kda_set_stage_events.restype = ctypes.c_int
         _lib = L

@@ -209,3 +209,45 @@ kda_status_t kda_set_stage_events(void* const* events, int32_t count) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Prefill without device allocation: the scratch is this file-scope array.
+// Host code must not pass the array's name to a kernel (on the host it names a
+// stand-in, not device memory); its device address is looked up once per device
+// with cudaGetSymbolAddress and cached.
+static __device__ __align__(256) unsigned char g_kda_no_alloc_scratch[KDA_NO_ALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_no_alloc_mutex;
+void* g_no_alloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (nullptr on failure).
+void* no_alloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_no_alloc_mutex);
+  if (!g_no_alloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_kda_no_alloc_scratch) != cudaSuccess || !ptr) return nullptr;
+    g_no_alloc_ptr[dev] = ptr;
+  }
+  return g_no_alloc_ptr[dev];
+}
+}  // namespace
+
+extern "C" kda_status_t kda_prefill_fwd_no_alloc(const kda_params_t* p, const void* q,
+                                                 const void* k, const void* v,
+                                                 const float* beta, const float* log_decay,
+                                                 const uint32_t* input_row_offsets,
+                                                 const uint32_t* slot_idx, void* state_pool,
+                                                 float* o, void* stream) {
+  Problem P{};
+  kda_status_t s = check_prefill(p, &P);
+  if (s != KDA_OK) return s;
+  if (kda::simt_workspace_bytes(P) > KDA_NO_ALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
+  if (p->num_seqs == 0) return KDA_OK;
+  void* scratch = no_alloc_scratch();
+  if (!scratch) return KDA_ERR_CUDA;
+  return kda_prefill_fwd(p, q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, o,
+                         scratch, KDA_NO_ALLOC_SCRATCH_BYTES, stream);
+}

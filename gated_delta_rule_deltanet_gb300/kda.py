@@ -142,6 +142,33 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tenso
     return out
 
 
+def prefill_no_alloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                     log_decay: torch.Tensor, input_row_offsets: torch.Tensor,
+                     slot_idx: torch.Tensor, state_pool: torch.Tensor, *, chunk: int = 64,
+                     scale: float = 0.0, l2norm: bool = True, checked: bool = False,
+                     out: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """kda_prefill_fwd_no_alloc: the prefill with the library's built-in scratch array.
+
+    For callers that must not allocate device memory: `out` (fp32 [T, HV, D]) is
+    required and nothing is allocated here or in the library.  Problems needing more
+    than KDA_NO_ALLOC_SCRATCH_BYTES of scratch raise KdaError(KDA_ERR_WORKSPACE).
+    Calls that overlap on the GPU share the scratch and race; keep them on one stream.
+    """
+    dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, out)
+    p = _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
+                        scale, l2norm, checked)
+    T, HV, D = v.shape
+    if out.dtype != torch.float32 or tuple(out.shape) != (T, HV, D) or not out.is_contiguous():
+        raise ValueError("out must be contiguous float32 [T, HV, D]")
+    st = _lib.load().kda_prefill_fwd_no_alloc(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_decay),
+        _ptr(input_row_offsets), _ptr(slot_idx), _ptr(state_pool), _ptr(out),
+        _stream_handle(stream, dev))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_prefill_fwd_no_alloc")
+    return out
+
+
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                 log_decay: torch.Tensor, slot_idx: torch.Tensor, state_pool: torch.Tensor, *,
                 scale: float = 0.0, l2norm: bool = True, out: Optional[torch.Tensor] = None,

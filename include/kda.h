@@ -173,6 +173,39 @@ kda_status_t kda_decode_step(const kda_params_t *p, const void *q, const void *k
 kda_status_t kda_get_device_error(void *stream, int32_t *code);
 
 /*
+ * Prefill without any device allocation: same inputs, outputs and results as
+ * kda_prefill_fwd, but its scratch lives in a fixed array inside the library
+ * instead of a caller-provided workspace.  There is no counterpart on the pages.
+ *
+ * For callers that cannot allocate device memory at the point where they run
+ * the prefill: code hosted inside an engine that owns the device's memory
+ * budget and hands out no allocator, code running under a CUDA stream capture
+ * that must not call cudaMalloc, or a runtime that reserves all of its memory
+ * at start-up.  They still pass every input and output buffer.
+ *
+ *   - The scratch is KDA_NO_ALLOC_SCRATCH_BYTES (64 MiB) of device memory that
+ *     every GPU which loads the library holds until the process exits.
+ *     Problems whose kda_prefill_workspace_size exceeds it are rejected with
+ *     KDA_ERR_WORKSPACE before anything is enqueued (roughly 1,700 tokens x 16
+ *     heads at d = 128, chunk 64; query the size to know).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.  Later calls do no CUDA runtime work besides
+ *     the kernel launches.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls whose work overlaps on the
+ *     GPU -- different streams, or different host threads -- race on it: order
+ *     them on one stream.
+ * Arguments, layouts, errors and the device error word are as in
+ * kda_prefill_fwd.  This entry point calls no cudaMalloc / cudaFree.
+ */
+#define KDA_NO_ALLOC_SCRATCH_BYTES (64u << 20)
+kda_status_t kda_prefill_fwd_no_alloc(const kda_params_t *p, const void *q, const void *k,
+                                      const void *v, const float *beta, const float *log_decay,
+                                      const uint32_t *input_row_offsets, const uint32_t *slot_idx,
+                                      void *state_pool, float *o, void *stream);
+
+/*
  * Measurement aid (no counterpart on the pages).  Registers up to 8 CUDA events
  * (cudaEvent_t handles passed as void*, created by the caller) that later
  * kda_prefill_fwd / kda_decode_step calls on this process record on their

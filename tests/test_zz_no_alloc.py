@@ -1,0 +1,67 @@
+"""kda_prefill_fwd_no_alloc: the prefill for callers that cannot allocate device memory.
+
+Such callers (code inside an engine that owns the device memory budget, code running
+under a stream capture that must not call cudaMalloc, runtimes that reserve all memory
+at start-up) get a prefill whose scratch is a fixed array inside the library.  This
+file is collected last so that a stop-at-first-failure run has already run every other
+test; it also passes on its own in a fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_deltanet_gb300 as kda
+from gated_delta_rule_deltanet_gb300 import _lib
+import workloads
+from workloads import torch_io
+
+TOL_BF16 = 2e-3
+
+
+def rel_err(x, ref):
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert np.all(np.isfinite(x))
+    return float(np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def problem(lengths, seed):
+    return workloads.make_problem("no_alloc", num_seqs=len(lengths), lengths=lengths,
+                                  num_k_heads=2, num_v_heads=4, d=128, qkv_dtype="bf16",
+                                  state_dtype="f32", decay_kind="per_channel", chunk=64,
+                                  zero_state=False, num_slots=len(lengths) + 2, seed=seed)
+
+
+@pytest.mark.gpu
+def test_no_alloc_matches_workspace_prefill_on_two_calls():
+    """Two calls in a row (different batches, so stale scratch from the first call is in
+    place for the second), each equal to the workspace entry point's result."""
+    for lengths, seed in [([100, 37, 64], 31), ([200, 1, 129, 65], 32)]:
+        p = problem(lengths, seed)
+        t = torch_io.prefill_inputs(p, "cuda:0")
+        pool_ref = t["state_pool"].clone()
+        o_ref = kda.prefill(**{**t, "state_pool": pool_ref}, chunk=p.chunk)
+        out = torch.empty_like(o_ref)
+        kda.prefill_no_alloc(**t, chunk=p.chunk, out=out)
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        assert rel_err(out.cpu().numpy(), o_ref.cpu().numpy()) <= TOL_BF16
+        assert rel_err(t["state_pool"].cpu().numpy(), pool_ref.cpu().numpy()) <= TOL_BF16
+
+
+def test_no_alloc_rejects_problems_beyond_its_scratch():
+    """A problem needing more scratch than the built-in array is refused on the host,
+    before anything is enqueued (so this runs without a GPU too)."""
+    lib = _lib.load()
+    big = kda.make_params(num_seqs=1, num_k_heads=16, num_v_heads=16, d=128, num_slots=1,
+                          total_tokens=16384, chunk=64)
+    assert kda.workspace_size(big) > _lib.KDA_NO_ALLOC_SCRATCH_BYTES
+    P = ctypes.c_void_p
+    a = P(1 << 20)
+    st = lib.kda_prefill_fwd_no_alloc(ctypes.byref(big), a, a, a, a, a, a, a, a, a, None)
+    assert st == _lib.KDA_ERR_WORKSPACE
+    small = kda.make_params(num_seqs=1, num_k_heads=2, num_v_heads=4, d=128, num_slots=1,
+                            total_tokens=300, chunk=64)
+    assert kda.workspace_size(small) <= _lib.KDA_NO_ALLOC_SCRATCH_BYTES

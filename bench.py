@@ -66,10 +66,15 @@ def prefill_flops(p) -> float:
 
 
 # The prefill kernels in launch order, with the part of the algorithmic traffic each
-# one carries (the chunk-parallel kernel reads every input once; the scan writes o and
-# reads/writes the states).
-PREFILL_STAGES = [("plan", ()), ("chunk_local", ("q", "k", "v", "beta", "g")),
-                  ("state_scan", ("o", "state"))]
+# one carries.  Tensor-core path: the fused chunk kernel moves everything.  CUDA-core
+# path: the chunk-parallel kernel reads every input once; the scan writes o and
+# reads/writes the states.
+ALL_BYTES = ("q", "k", "v", "beta", "g", "o", "state")
+PREFILL_STAGES = {
+    True: [("plan", ()), ("tc_prefill", ALL_BYTES)],
+    False: [("plan", ()), ("chunk_local", ("q", "k", "v", "beta", "g")),
+            ("state_scan", ("o", "state"))],
+}
 
 
 def load_peaks() -> dict:
@@ -242,14 +247,15 @@ def time_prefill(p, dev, steps, warmup):
     params = kda.kda._prefill_params(t["q"], t["k"], t["v"], t["beta"], t["log_decay"],
                                      t["input_row_offsets"], t["slot_idx"], t["state_pool"],
                                      p.chunk, p.scale, True, False)
-    ws = torch.empty(kda.workspace_size(params), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(kda.workspace_size(params), 1), dtype=torch.uint8, device=dev)
+    stages = PREFILL_STAGES[kda.uses_tensor_cores(params)]
 
     def step():
         kda.prefill(**t, chunk=p.chunk, scale=p.scale, out=out, workspace=ws)
 
     for _ in range(warmup):
         step()
-    nst = len(PREFILL_STAGES) + 1
+    nst = len(stages) + 1
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(steps)]
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -263,7 +269,7 @@ def time_prefill(p, dev, steps, warmup):
     total_ms = start.elapsed_time(end)
     stage_ms = [float(np.mean([evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)]))
                 for i in range(nst - 1)]
-    return total_ms / steps, stage_ms, t, out
+    return total_ms / steps, stage_ms, t, out, stages
 
 
 def time_prefill_e2e(p, dev, steps, warmup):
@@ -343,7 +349,8 @@ def ours_arm(args, rank, world, local):
     barrier(world)
     clocks = ClockSampler(local)
     clocks.start()
-    ms, stage_ms, t_dev, _ = time_prefill(p, dev, args.steps, args.warmup)
+    ms, stage_ms, t_dev, _, stages = time_prefill(p, dev, args.steps, args.warmup)
+    tensor_cores = stages is PREFILL_STAGES[True]
     clk = clocks.stop()
     barrier(world)
     tokens = p.total_tokens
@@ -358,13 +365,16 @@ def ours_arm(args, rank, world, local):
     # roofline of the dominant kernel (its share of the algorithmic bytes / its time)
     abytes = prefill_algorithmic_bytes(p)
     dom = int(np.argmax(stage_ms))
-    name, parts = PREFILL_STAGES[dom]
+    name, parts = stages[dom]
     dom_bytes = float(sum(abytes[x] for x in parts))
     achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                 "peak_source": peaks["source"], "kernel_ms": stage_ms[dom],
-                "stage_ms": {n: m for (n, _), m in zip(PREFILL_STAGES, stage_ms)}}
+                "stage_ms": {n: m for (n, _), m in zip(stages, stage_ms)},
+                "tensor_tflops": prefill_flops(p) / (stage_ms[dom] / 1e3) / 1e12
+                if tensor_cores else None,
+                "tensor_peak_tflops": peaks["bf16_tflops"]}
     path_bytes = float(sum(abytes.values()))
     also = []
     if not args.no_decode:
@@ -392,7 +402,8 @@ def ours_arm(args, rank, world, local):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "f32", "data": "synthetic",
+                "dtype": "f16" if tensor_cores else "f32",
+                "accumulate": "f32", "data": "synthetic",
                 "config": {**workload_config(p),
                            "l2": f"inputs larger than L2 ({path_bytes / 1e6:.0f} MB moved "
                                  f"per step vs 129 MB L2); no flush"},
@@ -404,7 +415,7 @@ def ours_arm(args, rank, world, local):
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-                "gpu_launches": len(PREFILL_STAGES) * args.steps,
+                "gpu_launches": len(stages) * args.steps,
                 "clocks": clk, "also": also}
         print(json.dumps(line), flush=True)
 

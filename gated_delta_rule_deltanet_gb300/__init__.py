@@ -10,8 +10,9 @@ it:
 There is no CPU or eager fallback: if the library is missing, calls raise.
 """
 from .kda import (decode_step, get_device_error, make_params, prefill,  # noqa: F401
-                  prefill_no_alloc, set_stage_events, workspace_size)
+                  prefill_no_alloc, set_stage_events, uses_tensor_cores,
+                  workspace_size)
 from ._lib import KdaError, KdaParams, load  # noqa: F401
 
 __all__ = ["prefill", "decode_step", "workspace_size", "get_device_error", "make_params",
-           "set_stage_events", "prefill_no_alloc", "KdaError", "KdaParams", "load"]
+           "set_stage_events", "prefill_no_alloc", "uses_tensor_cores", "KdaError", "KdaParams", "load"]

@@ -19,16 +19,19 @@ KDA_DTYPE_BF16 = 1
 KDA_DECAY_SCALAR = 0
 KDA_DECAY_PER_CHANNEL = 1
 KDA_FLAG_CHECKED = 1
+KDA_FLAG_CUDA_CORES = 2
 
 KDA_DEVERR_NONE = 0
 KDA_DEVERR_OFFSETS = 1
 KDA_DEVERR_SLOT_RANGE = 2
 KDA_DEVERR_SLOT_DUP = 3
+KDA_DEVERR_TIMEOUT = 4
 
 # every function include/kda.h declares
 EXPORTS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_size",
            "kda_prefill_fwd", "kda_decode_step", "kda_get_device_error",
-           "kda_set_stage_events", "kda_prefill_fwd_no_alloc")
+           "kda_set_stage_events", "kda_prefill_fwd_no_alloc",
+           "kda_prefill_uses_tensor_cores")
 
 KDA_NO_ALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -98,6 +101,8 @@ def load():
         L.kda_decode_step.restype = ctypes.c_int
         L.kda_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
         L.kda_get_device_error.restype = ctypes.c_int
+        L.kda_prefill_uses_tensor_cores.argtypes = [pp]
+        L.kda_prefill_uses_tensor_cores.restype = ctypes.c_int
         L.kda_prefill_fwd_no_alloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P]
         L.kda_prefill_fwd_no_alloc.restype = ctypes.c_int
         L.kda_set_stage_events.argtypes = [P, ctypes.c_int32]

@@ -15,6 +15,10 @@ cudaError_t launch_decode(const Problem& P, bool qbf16, bool sbf16, bool perch, 
 cudaError_t launch_prefill_simt(const Problem& P, void* workspace, bool qbf16, bool perch,
                                 bool sbf16, cudaStream_t stream, const Stages& st);
 size_t simt_workspace_bytes(const Problem& P);
+bool tc_prefill_supported(const Problem& P, bool qbf16);
+size_t tc_workspace_bytes(const Problem& P);
+cudaError_t launch_prefill_tc(const Problem& P, void* workspace, bool perch, bool sbf16,
+                              cudaStream_t stream, const Stages& st);
 }  // namespace kda
 
 using kda::Problem;
@@ -67,7 +71,7 @@ kda_status_t check_common(const kda_params_t* p, Problem* P) {
   if (p->state_dtype != KDA_DTYPE_F32 && p->state_dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
   if (p->decay_kind != KDA_DECAY_SCALAR && p->decay_kind != KDA_DECAY_PER_CHANNEL)
     return KDA_ERR_INVALID_ARG;
-  if (p->flags & ~KDA_FLAG_CHECKED) return KDA_ERR_INVALID_ARG;
+  if (p->flags & ~(KDA_FLAG_CHECKED | KDA_FLAG_CUDA_CORES)) return KDA_ERR_INVALID_ARG;
   const int64_t es = static_cast<int64_t>(elem_size(p->qkv_dtype));
   const int64_t dq = static_cast<int64_t>(p->num_k_heads) * p->d_k;
   const int64_t dv = static_cast<int64_t>(p->num_v_heads) * p->d_v;
@@ -103,6 +107,17 @@ kda_status_t check_prefill(const kda_params_t* p, Problem* P) {
 
 kda_status_t to_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
+// The tensor-core path serves bf16 inputs at d = 128, chunk 64 unless the caller
+// asks for CUDA cores; everything else runs the fp32 CUDA-core path.
+bool use_tc(const kda_params_t* p, const Problem& P) {
+  return !(p->flags & KDA_FLAG_CUDA_CORES) &&
+         kda::tc_prefill_supported(P, p->qkv_dtype == KDA_DTYPE_BF16);
+}
+
+size_t prefill_workspace_bytes(const kda_params_t* p, const Problem& P) {
+  return use_tc(p, P) ? kda::tc_workspace_bytes(P) : kda::simt_workspace_bytes(P);
+}
+
 }  // namespace
 
 extern "C" {
@@ -121,12 +136,18 @@ const char* kda_status_string(kda_status_t s) {
   return "unknown status";
 }
 
+int kda_prefill_uses_tensor_cores(const kda_params_t* p) {
+  Problem P{};
+  if (check_prefill(p, &P) != KDA_OK) return -1;
+  return use_tc(p, P) ? 1 : 0;
+}
+
 kda_status_t kda_prefill_workspace_size(const kda_params_t* p, size_t* bytes) {
   Problem P{};
   if (!bytes) return KDA_ERR_INVALID_ARG;
   kda_status_t s = check_prefill(p, &P);
   if (s != KDA_OK) return s;
-  *bytes = kda::simt_workspace_bytes(P);
+  *bytes = prefill_workspace_bytes(p, P);
   return KDA_OK;
 }
 
@@ -145,7 +166,7 @@ kda_status_t kda_prefill_fwd(const kda_params_t* p, const void* q, const void* k
       !aligned(state_pool, 16) || !aligned(beta, 4) || !aligned(log_decay, 4) ||
       !aligned(input_row_offsets, 4) || !aligned(slot_idx, 4))
     return KDA_ERR_INVALID_ARG;
-  const size_t need = kda::simt_workspace_bytes(P);
+  const size_t need = prefill_workspace_bytes(p, P);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
   P.q = q; P.k = k; P.v = v; P.beta = beta; P.g = log_decay;
   P.offsets = input_row_offsets; P.slot_idx = slot_idx;
@@ -156,6 +177,9 @@ kda_status_t kda_prefill_fwd(const kda_params_t* p, const void* q, const void* k
   const bool sbf16 = p->state_dtype == KDA_DTYPE_BF16;
   const bool perch = p->decay_kind == KDA_DECAY_PER_CHANNEL;
   const kda::Stages st = current_stages();
+  if (use_tc(p, P))
+    return to_status(kda::launch_prefill_tc(P, workspace, perch, sbf16,
+                                            static_cast<cudaStream_t>(stream), st));
   return to_status(kda::launch_prefill_simt(P, workspace, qbf16, perch, sbf16,
                                             static_cast<cudaStream_t>(stream), st));
 }
@@ -244,7 +268,7 @@ extern "C" kda_status_t kda_prefill_fwd_no_alloc(const kda_params_t* p, const vo
   Problem P{};
   kda_status_t s = check_prefill(p, &P);
   if (s != KDA_OK) return s;
-  if (kda::simt_workspace_bytes(P) > KDA_NO_ALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
+  if (prefill_workspace_bytes(p, P) > KDA_NO_ALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
   if (p->num_seqs == 0) return KDA_OK;
   void* scratch = no_alloc_scratch();
   if (!scratch) return KDA_ERR_CUDA;

@@ -51,15 +51,17 @@ def _check_cuda(*ts):
 
 def make_params(*, num_seqs, num_k_heads, num_v_heads, d, num_slots, total_tokens=0, chunk=64,
                 qkv_dtype=torch.bfloat16, state_dtype=torch.float32, per_channel=True,
-                scale=0.0, l2norm=True, checked=False, q_row_stride=0, k_row_stride=0,
-                v_row_stride=0) -> KdaParams:
+                scale=0.0, l2norm=True, checked=False, cuda_cores=False, q_row_stride=0,
+                k_row_stride=0, v_row_stride=0) -> KdaParams:
     return KdaParams(num_seqs=num_seqs, num_k_heads=num_k_heads, num_v_heads=num_v_heads, d_k=d,
                      d_v=d, num_slots=num_slots, total_tokens=total_tokens, chunk=chunk,
                      qkv_dtype=_QKV_DTYPES[qkv_dtype], state_dtype=_QKV_DTYPES[state_dtype],
                      decay_kind=(_lib.KDA_DECAY_PER_CHANNEL if per_channel
                                  else _lib.KDA_DECAY_SCALAR),
                      scale=float(scale), l2norm_qk=int(bool(l2norm)),
-                     flags=_lib.KDA_FLAG_CHECKED if checked else 0, q_row_stride=q_row_stride,
+                     flags=((_lib.KDA_FLAG_CHECKED if checked else 0)
+                            | (_lib.KDA_FLAG_CUDA_CORES if cuda_cores else 0)),
+                     q_row_stride=q_row_stride,
                      k_row_stride=k_row_stride, v_row_stride=v_row_stride)
 
 
@@ -71,8 +73,16 @@ def workspace_size(params: KdaParams) -> int:
     return int(n.value)
 
 
+def uses_tensor_cores(params: KdaParams) -> bool:
+    """Whether kda_prefill_fwd runs these parameters on the tensor-core path."""
+    r = _lib.load().kda_prefill_uses_tensor_cores(ctypes.byref(params))
+    if r < 0:
+        raise KdaError(_lib.KDA_ERR_INVALID_ARG, "kda_prefill_uses_tensor_cores")
+    return bool(r)
+
+
 def _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
-                    scale, l2norm, checked):
+                    scale, l2norm, checked, cuda_cores=False):
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:
         raise ValueError("q, k must be [T, HK, D] and v [T, HV, D]")
     T, HK, D = q.shape
@@ -105,7 +115,7 @@ def _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state
     return make_params(num_seqs=B, num_k_heads=HK, num_v_heads=HV, d=D,
                        num_slots=state_pool.shape[0], total_tokens=T, chunk=chunk,
                        qkv_dtype=q.dtype, state_dtype=state_pool.dtype, per_channel=per_channel,
-                       scale=scale, l2norm=l2norm, checked=checked,
+                       scale=scale, l2norm=l2norm, checked=checked, cuda_cores=cuda_cores,
                        q_row_stride=_row_stride(q, "q"), k_row_stride=_row_stride(k, "k"),
                        v_row_stride=_row_stride(v, "v"))
 
@@ -113,16 +123,17 @@ def _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state
 def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
             log_decay: torch.Tensor, input_row_offsets: torch.Tensor, slot_idx: torch.Tensor,
             state_pool: torch.Tensor, *, chunk: int = 64, scale: float = 0.0,
-            l2norm: bool = True, checked: bool = False, out: Optional[torch.Tensor] = None,
-            workspace: Optional[torch.Tensor] = None,
+            l2norm: bool = True, checked: bool = False, cuda_cores: bool = False,
+            out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Chunkwise gated-delta-rule prefill (kda_prefill_fwd).  Returns o [T, HV, D] fp32.
 
     The pool slots named by slot_idx are updated in place with each sequence's final state.
+    `cuda_cores=True` asks for the fp32 CUDA-core path where the tensor-core path applies.
     """
     dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool)
     p = _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
-                        scale, l2norm, checked)
+                        scale, l2norm, checked, cuda_cores)
     T, HV, D = v.shape
     if out is None:
         out = torch.empty((T, HV, D), dtype=torch.float32, device=dev)
@@ -146,7 +157,8 @@ def prefill_no_alloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
                      log_decay: torch.Tensor, input_row_offsets: torch.Tensor,
                      slot_idx: torch.Tensor, state_pool: torch.Tensor, *, chunk: int = 64,
                      scale: float = 0.0, l2norm: bool = True, checked: bool = False,
-                     out: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                     cuda_cores: bool = False, out: torch.Tensor,
+                     stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """kda_prefill_fwd_no_alloc: the prefill with the library's built-in scratch array.
 
     For callers that must not allocate device memory: `out` (fp32 [T, HV, D]) is
@@ -156,7 +168,7 @@ def prefill_no_alloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
     """
     dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, out)
     p = _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
-                        scale, l2norm, checked)
+                        scale, l2norm, checked, cuda_cores)
     T, HV, D = v.shape
     if out.dtype != torch.float32 or tuple(out.shape) != (T, HV, D) or not out.is_contiguous():
         raise ValueError("out must be contiguous float32 [T, HV, D]")

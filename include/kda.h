@@ -78,12 +78,17 @@ typedef enum kda_decay_kind {
 /* Check every sequence's offsets and slot and that slots are distinct on the
  * device (without it, offsets and slot ranges are still checked, distinctness is not). */
 #define KDA_FLAG_CHECKED 1u
+/* Run the prefill on CUDA cores in fp32 even where the tensor-core path applies
+ * (bf16 q/k/v, d = 128, chunk 64, whose operands are fp16/bf16 with fp32
+ * accumulation).  fp32 q/k/v and the other head sizes and chunks always use it. */
+#define KDA_FLAG_CUDA_CORES 2u
 
 /* Device error codes (kda_get_device_error). */
 #define KDA_DEVERR_NONE 0
 #define KDA_DEVERR_OFFSETS 1   /* input_row_offsets not monotone / not 0..total_tokens */
 #define KDA_DEVERR_SLOT_RANGE 2 /* slot_idx[b] >= num_slots */
 #define KDA_DEVERR_SLOT_DUP 3   /* a slot named twice (KDA_FLAG_CHECKED only) */
+#define KDA_DEVERR_TIMEOUT 4    /* a bounded wait inside a kernel gave up; its work is incomplete */
 
 typedef struct kda_params {
   int32_t num_seqs;    /* B: sequences in the ragged batch (prefill) or decode batch */
@@ -121,6 +126,14 @@ const char *kda_status_string(kda_status_t status);
  * kda_prefill_fwd would reject; *bytes is then left unchanged.
  */
 kda_status_t kda_prefill_workspace_size(const kda_params_t *p, size_t *bytes);
+
+/*
+ * 1 if kda_prefill_fwd would run these parameters on the tensor-core path
+ * (bf16 q/k/v, d = 128, chunk 64, KDA_FLAG_CUDA_CORES clear: fp16/bf16 MMA
+ * operands with fp32 accumulation), 0 if on the fp32 CUDA-core path, -1 if the
+ * parameters are invalid.  Never touches the GPU.
+ */
+int kda_prefill_uses_tensor_cores(const kda_params_t *p);
 
 /*
  * Chunkwise prefill over a ragged batch ("You Could Have Come Up With Kimi
@@ -186,8 +199,10 @@ kda_status_t kda_get_device_error(void *stream, int32_t *code);
  *   - The scratch is KDA_NO_ALLOC_SCRATCH_BYTES (64 MiB) of device memory that
  *     every GPU which loads the library holds until the process exits.
  *     Problems whose kda_prefill_workspace_size exceeds it are rejected with
- *     KDA_ERR_WORKSPACE before anything is enqueued (roughly 1,700 tokens x 16
- *     heads at d = 128, chunk 64; query the size to know).
+ *     KDA_ERR_WORKSPACE before anything is enqueued.  The tensor-core path
+ *     needs only the chunk table (16 bytes per chunk), so it fits for any
+ *     practical batch; the fp32 CUDA-core path needs about 150 KB per chunk and
+ *     value head (roughly 1,700 tokens x 16 heads at d = 128, chunk 64).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
  *     before any stream capture.  Later calls do no CUDA runtime work besides

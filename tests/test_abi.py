@@ -135,3 +135,14 @@ def test_empty_batch_is_a_no_op(lib):
                                None, None, 0, None) == _lib.KDA_OK
     assert lib.kda_decode_step(ctypes.byref(p), None, None, None, None, None, None, None, None,
                                None) == _lib.KDA_OK
+
+
+def test_path_query(lib):
+    from gated_delta_rule_deltanet_gb300 import kda as K
+    import torch
+    assert K.uses_tensor_cores(good())                               # bf16, d=128, chunk 64
+    assert not K.uses_tensor_cores(good(cuda_cores=True))
+    assert not K.uses_tensor_cores(good(chunk=32))
+    assert not K.uses_tensor_cores(good(qkv_dtype=torch.float32))
+    assert not K.uses_tensor_cores(good(d=16))
+    assert lib.kda_prefill_uses_tensor_cores(None) == -1

@@ -268,3 +268,21 @@ def test_device_errors_skip_work_without_faulting():
                     torch.tensor([1, 5], dtype=torch.int32, device=DEV), td["state_pool"])
     assert kda.get_device_error() == 2
     assert kda.get_device_error() == 0            # reading clears the word
+
+
+@pytest.mark.parametrize("decay", ["scalar", "per_channel"])
+@pytest.mark.parametrize("state", ["f32", "bf16"])
+def test_tensor_core_path_matches_cuda_core_path(decay, state):
+    """The tcgen05 path (fp16/bf16 operands) and the fp32 CUDA-core path agree to the
+    tolerance, and each matches the oracle, on ragged lengths around the chunk size."""
+    p = small("tc-vs-simt", [1, 63, 64, 65, 190, 128], 2, 4, 128, "bf16", state, decay, 64,
+              seed=41 if decay == "scalar" else 42, slots=9)
+    assert kda.uses_tensor_cores(kda.make_params(num_seqs=6, num_k_heads=2, num_v_heads=4, d=128,
+                                                 num_slots=9, total_tokens=p.total_tokens))
+    o_tc, s_tc, _ = gpu_prefill(p)
+    o_cc, s_cc, _ = gpu_prefill(p, cuda_cores=True)
+    o_ref, pool_ref = oracle.run(p)
+    tol = TOL["bf16"]
+    assert rel_err(o_tc, o_cc) <= tol
+    assert rel_err(o_tc, o_ref) <= tol and rel_err(o_cc, o_ref) <= tol
+    assert state_err(p, s_tc, pool_ref) <= tol and state_err(p, s_cc, pool_ref) <= tol

@@ -36,15 +36,16 @@ def problem(lengths, seed):
 
 @pytest.mark.gpu
 def test_no_alloc_matches_workspace_prefill_on_two_calls():
-    """Two calls in a row (different batches, so stale scratch from the first call is in
-    place for the second), each equal to the workspace entry point's result."""
-    for lengths, seed in [([100, 37, 64], 31), ([200, 1, 129, 65], 32)]:
+    """Calls in a row (different batches, so stale scratch from the previous call is in
+    place for the next), on both prefill paths, each equal to the workspace entry point."""
+    for lengths, seed, cc in [([100, 37, 64], 31, False), ([200, 1, 129, 65], 32, False),
+                              ([100, 37, 64], 33, True), ([200, 1, 129, 65], 34, True)]:
         p = problem(lengths, seed)
         t = torch_io.prefill_inputs(p, "cuda:0")
         pool_ref = t["state_pool"].clone()
-        o_ref = kda.prefill(**{**t, "state_pool": pool_ref}, chunk=p.chunk)
+        o_ref = kda.prefill(**{**t, "state_pool": pool_ref}, chunk=p.chunk, cuda_cores=cc)
         out = torch.empty_like(o_ref)
-        kda.prefill_no_alloc(**t, chunk=p.chunk, out=out)
+        kda.prefill_no_alloc(**t, chunk=p.chunk, out=out, cuda_cores=cc)
         torch.cuda.synchronize()
         assert kda.get_device_error() == 0
         assert rel_err(out.cpu().numpy(), o_ref.cpu().numpy()) <= TOL_BF16
@@ -56,7 +57,7 @@ def test_no_alloc_rejects_problems_beyond_its_scratch():
     before anything is enqueued (so this runs without a GPU too)."""
     lib = _lib.load()
     big = kda.make_params(num_seqs=1, num_k_heads=16, num_v_heads=16, d=128, num_slots=1,
-                          total_tokens=16384, chunk=64)
+                          total_tokens=16384, chunk=64, cuda_cores=True)
     assert kda.workspace_size(big) > _lib.KDA_NO_ALLOC_SCRATCH_BYTES
     P = ctypes.c_void_p
     a = P(1 << 20)

@@ -26,6 +26,7 @@ KDA_DEVERR_OFFSETS = 1
 KDA_DEVERR_SLOT_RANGE = 2
 KDA_DEVERR_SLOT_DUP = 3
 KDA_DEVERR_TIMEOUT = 4
+KDA_DEVERR_DECAY_RANGE = 5
 
 # every function include/kda.h declares
 EXPORTS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_size",

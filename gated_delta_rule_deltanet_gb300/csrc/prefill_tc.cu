@@ -7,10 +7,11 @@
 // sec. 4, WY/UT transform and the 16x16 blocked inverse) runs as a tcgen05 MMA
 // with fp32 accumulators in tensor memory:
 //
-//   A-GEMM   [K+; Q+] K-^T               -> A_kk (raw), A_qk (raw)      M=128 N=64  K=128
-//            (scalar decay: raw bf16 q, k and exp(G_i - G_j) applied to the
-//             result; per-channel decay: fp16 operands k exp(G - G_a),
-//             q exp(G - G_a), k exp(G_a - G) with a mid-chunk anchor G_a)
+//   A-GEMM   [K+; Q+] K-^T               -> A_kk, A_qk                  M=128 N=64  K=128
+//            (scalar decay: raw bf16 q, k, with the norms and exp(G_i - G_j)
+//             applied to the result; per-channel decay: fp16 operands
+//             k^ exp(G - G_a), q^ exp(G - G_a), k^ exp(G_a - G) of the
+//             normalised rows with a mid-chunk anchor G_a)
 //   solve    T = (I + A_kk)^-1 on CUDA cores (16x16 forward substitution,
 //            then T21 = -T22 A21 T11 merges), TB = T diag(beta)
 //   X        [I; A_qk] TB          = [TB; A_qk TB]                    M=128 N=64  K=64
@@ -21,11 +22,19 @@
 // (E = U - W S are the corrected values and O = Q~ S + A_qk E the outputs of the
 // chunk; folding A_qk into the first operand gives O from the same MMA as E.)
 // Operands are fp16 (10-bit mantissa, the same as tf32) except the raw bf16
-// inputs of the scalar-decay A-GEMM; every value fed to them is bounded (decay
-// factors <= 1, unit keys), so fp16 range is not a constraint.  Per-channel
-// decay uses exp(G_i - G_a) and exp(G_a - G_j) with the anchor at the chunk's
-// middle token, which keeps both factors finite while the cumulative decay over
-// half a chunk stays below ~11 nats per channel.
+// inputs of the scalar-decay A-GEMM.  The decayed keys and queries are bounded
+// by 1 (unit rows, decay factors <= 1); v, E and the state must stay inside the
+// fp16 range (|x| < 65504), which activations and states of normalised-key
+// recurrences do.  Per-channel decay uses exp(G_i - G_a) and exp(G_a - G_j)
+// with the anchor at the chunk's middle token, which keeps both factors finite
+// while the cumulative decay over half a chunk stays below ~11 nats per
+// channel (an average log-decay above -0.34 per token); outside these limits
+// the fp32 CUDA-core path (KDA_FLAG_CUDA_CORES) is exact.
+//
+// The raw inputs of the next chunk are prefetched with cp.async into the
+// staging buffers as soon as the current chunk no longer reads them, so their
+// latency overlaps the chain MMAs.  Staging rows are padded so that threads
+// owning different tokens read different banks.
 //
 // Shared-memory operands use the no-swizzle K-major core-matrix layout of
 // tc_utils.cuh; the two operands written transposed by their producer threads
@@ -44,17 +53,26 @@ constexpr int D = 128;      // head size
 constexpr int BV = 64;      // value columns per CTA
 constexpr int NT = 256;     // threads (8 warps)
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait is declared stuck
+constexpr float kMaxHalfChunkDecay = 11.0f;  // exp(11) < 65504, the largest fp16
+
+// padded staging rows (elements)
+constexpr int KS = D + 8;    // k, q rows: bf16, 272 B
+constexpr int VS = BV + 8;   // v rows: bf16, 144 B
+constexpr int GS = D + 4;    // G rows: fp32, 528 B
 
 // shared-memory map (bytes)
-constexpr uint32_t S_K = 0;                    // k staging bf16 [64][128]
-constexpr uint32_t S_Q = S_K + C * D * 2;      // q staging bf16 [64][128]
-constexpr uint32_t S_V = S_Q + C * D * 2;      // v staging bf16 [64][64]
-constexpr uint32_t S_G = S_V + C * BV * 2;     // log-decay -> cumulative G, fp32 [64][128]
-constexpr uint32_t S_BETA = S_G + C * D * 4;   // beta [64]
-constexpr uint32_t S_RK = S_BETA + 256;        // 1/|k| [64]
-constexpr uint32_t S_RQ = S_RK + 256;          // scale/|q| [64]
-constexpr uint32_t S_GAM = S_RQ + 256;         // exp(G_last) [128]
-constexpr uint32_t S_GA = S_GAM + 512;         // anchor G_a [128]
+constexpr uint32_t S_K = 0;                     // k staging bf16 [64][KS]
+constexpr uint32_t S_Q = S_K + C * KS * 2;      // q staging bf16 [64][KS]
+constexpr uint32_t S_V = S_Q + C * KS * 2;      // v staging bf16 [64][VS]
+constexpr uint32_t S_G = S_V + C * VS * 2;      // per-channel log-decay -> G, fp32 [64][GS]
+constexpr uint32_t S_GS = S_G + C * GS * 4;     // scalar log-decay -> G [64]
+constexpr uint32_t S_BETA = S_GS + 256;         // beta [64]
+constexpr uint32_t S_RK = S_BETA + 256;         // 1/|k| [64]
+constexpr uint32_t S_RQ = S_RK + 256;           // scale/|q| [64]
+constexpr uint32_t S_EG = S_RQ + 256;           // scalar: exp(G_i) [64]
+constexpr uint32_t S_EGL = S_EG + 256;          // scalar: exp(G_last - G_i) [64]
+constexpr uint32_t S_GAM = S_EGL + 256;         // exp(G_last) [128]
+constexpr uint32_t S_GA = S_GAM + 512;          // anchor G_a [128]
 constexpr uint32_t R1 = (S_GA + 512 + 1023) & ~1023u;
 //   A-GEMM operands, then the chain's first operands
 constexpr uint32_t AK = R1;                    // [K+; Q+] 128 x 128 (16-bit)
@@ -63,13 +81,14 @@ constexpr uint32_t A1 = R1;                    // [TB; A_qk TB] 128 x 64 fp16
 constexpr uint32_t A2 = A1 + 128 * 64 * 2;     // [-W; Q~ - A_qk W] 128 x 128 fp16
 constexpr uint32_t R2 = BK + 64 * 128 * 2;
 //   triangular solve, then K~^T and K_end^T
-constexpr int SP = 65;                         // padded row of the fp32 solve tiles
-constexpr uint32_t SOL_A = R2;                 // A_kk fp32 [64][65]
-constexpr uint32_t SOL_T = SOL_A + C * SP * 4; // T fp32 [64][65]
-constexpr uint32_t SOL_X = SOL_T + C * SP * 4; // merge temporaries fp32 [32][33]
+constexpr int SP = 68;                         // padded, 16-byte aligned row of the fp32 solve tiles
+constexpr uint32_t SOL_A = R2;                 // A_kk fp32 [64][SP]
+constexpr uint32_t SOL_T = SOL_A + C * SP * 4; // T fp32 [64][SP]
+constexpr uint32_t SOL_X = SOL_T + C * SP * 4; // merge temporaries fp32 [32][XP]
 constexpr uint32_t KTT = R2;                   // K~^T 128 x 64 fp16
 constexpr uint32_t KET = KTT + 128 * 64 * 2;   // K_end^T 128 x 64 fp16
-constexpr uint32_t R3 = (SOL_X + 32 * 33 * 4 + 127) & ~127u;
+constexpr int XP = 36;                         // row of the merge temporaries
+constexpr uint32_t R3 = (SOL_X + 32 * XP * 4 + 127) & ~127u;
 constexpr uint32_t LMAT = R3;                  // [I; A_qk] 128 x 64 fp16
 constexpr uint32_t TBT = LMAT + 128 * 64 * 2;  // TB^T 64 x 64 fp16
 constexpr uint32_t VT = TBT + 64 * 64 * 2;     // V^T 64 x 64 fp16
@@ -81,7 +100,7 @@ constexpr uint32_t ET_SBO = (C / 8) * LBO_P;
 constexpr uint32_t SMEM_BYTES = ET + (BV / 8) * ET_SBO;
 static_assert(KET + 128 * 64 * 2 <= R3, "K~/K_end alias the solve area");
 static_assert(A2 + 128 * 128 * 2 <= R2, "A1/A2 alias the A-GEMM operands");
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(SMEM_BYTES + 64 <= 227 * 1024, "shared memory budget");
 
 // TMEM columns
 constexpr uint32_t T_A = 0, T_X = 64, T_Y = 128, T_D1 = 256, T_D2 = 320, T_COLS = 512;
@@ -89,14 +108,13 @@ constexpr uint32_t T_A = 0, T_X = 64, T_Y = 128, T_D1 = 256, T_D2 = 320, T_COLS 
 // dense K-major tiles: lbo 128, sbo = (K / 8) * 128
 __host__ __device__ constexpr uint32_t dense_sbo(uint32_t K) { return (K / 8) * 128; }
 
-__device__ __forceinline__ uint32_t f16x8_store(unsigned char* smem, uint32_t off, const float* x) {
+__device__ __forceinline__ void f16x8_store(unsigned char* smem, uint32_t off, const float* x) {
   uint4 v;
   v.x = tc::pack_f16x2(x[0], x[1]);
   v.y = tc::pack_f16x2(x[2], x[3]);
   v.z = tc::pack_f16x2(x[4], x[5]);
   v.w = tc::pack_f16x2(x[6], x[7]);
   *reinterpret_cast<uint4*>(smem + off) = v;
-  return 0;
 }
 
 __device__ __forceinline__ uint16_t f16_bits(float x) {
@@ -107,15 +125,71 @@ __device__ __forceinline__ float bf16_at(const unsigned char* smem, uint32_t off
   return bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(smem + off)[idx]);
 }
 
+// 8 bf16 from a 16-byte aligned smem address, widened to fp32
+__device__ __forceinline__ void bf16x8_load(const unsigned char* p, float* x) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+  }
+}
+
 }  // namespace tcp
+
+// Issues the cp.async copies of one chunk's raw inputs into the staging buffers
+// (rows past the sequence end are zero-filled).
+template <bool PERCH>
+__device__ __forceinline__ void tc_issue_loads(const Problem& P, unsigned char* smem, int64_t t0,
+                                               int n, int kh, int h, int vt, int tid) {
+  using namespace tcp;
+  const int HV = P.HV;
+  const uint32_t sbase = tc::smem_u32(smem);
+  for (int u = tid; u < C * (D / 8); u += NT) {        // k, q: 16 pieces of 16 B per row
+    const int i = u / (D / 8), q8 = u % (D / 8);
+    const bool live = i < n;
+    const int64_t t = live ? t0 + i : t0;
+    const uint32_t nb = live ? 16u : 0u;
+    tc::cp_async16(sbase + S_K + (i * KS + q8 * 8) * 2,
+                   static_cast<const uint16_t*>(P.k) + t * P.k_stride + static_cast<int64_t>(kh) * D + q8 * 8, nb);
+    tc::cp_async16(sbase + S_Q + (i * KS + q8 * 8) * 2,
+                   static_cast<const uint16_t*>(P.q) + t * P.q_stride + static_cast<int64_t>(kh) * D + q8 * 8, nb);
+  }
+  for (int u = tid; u < C * (BV / 8); u += NT) {       // v: 8 pieces per row
+    const int i = u / (BV / 8), q8 = u % (BV / 8);
+    const bool live = i < n;
+    const int64_t t = live ? t0 + i : t0;
+    tc::cp_async16(sbase + S_V + (i * VS + q8 * 8) * 2,
+                   static_cast<const uint16_t*>(P.v) + t * P.v_stride + static_cast<int64_t>(h) * D + vt * BV + q8 * 8,
+                   live ? 16u : 0u);
+  }
+  if (PERCH) {
+    for (int u = tid; u < C * (D / 4); u += NT) {      // g: 32 pieces per row
+      const int i = u / (D / 4), q4 = u % (D / 4);
+      const bool live = i < n;
+      const int64_t t = live ? t0 + i : t0;
+      tc::cp_async16(sbase + S_G + (i * GS + q4 * 4) * 4, P.g + (t * HV + h) * D + q4 * 4,
+                     live ? 16u : 0u);
+    }
+  }
+  if (tid < C) {
+    const bool live = tid < n;
+    const int64_t t = live ? t0 + tid : t0;
+    tc::cp_async4(sbase + S_BETA + tid * 4, P.beta + t * HV + h, live ? 4u : 0u);
+    if (!PERCH) tc::cp_async4(sbase + S_GS + tid * 4, P.g + t * HV + h, live ? 4u : 0u);
+  }
+  tc::cp_async_commit();
+}
 
 template <bool PERCH, bool SBF16>
 __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanView plan) {
   using namespace tcp;
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   __shared__ uint64_t s_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_range;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (plan.info[1] == 0) return;
@@ -127,14 +201,24 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + vt * BV;
 
   float* sG = reinterpret_cast<float*>(smem + S_G);
+  float* sGs = reinterpret_cast<float*>(smem + S_GS);
   float* sBeta = reinterpret_cast<float*>(smem + S_BETA);
   float* sRK = reinterpret_cast<float*>(smem + S_RK);
   float* sRQ = reinterpret_cast<float*>(smem + S_RQ);
+  float* sEG = reinterpret_cast<float*>(smem + S_EG);
+  float* sEGL = reinterpret_cast<float*>(smem + S_EGL);
   float* sGam = reinterpret_cast<float*>(smem + S_GAM);
   float* sGA = reinterpret_cast<float*>(smem + S_GA);
   float* sA = reinterpret_cast<float*>(smem + SOL_A);
   float* sT = reinterpret_cast<float*>(smem + SOL_T);
   float* sX = reinterpret_cast<float*>(smem + SOL_X);
+
+  const uint32_t nchunks = (eos - bos + C - 1) / C;
+  auto chunk_n = [&](uint32_t c) -> int {
+    const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
+    return static_cast<int>(min(static_cast<int64_t>(C), static_cast<int64_t>(eos) - t0));
+  };
+  tc_issue_loads<PERCH>(P, smem, bos, chunk_n(0), kh, h, vt, tid);
 
   if (warp == 0) {
     tc::tmem_alloc(&s_tmem, T_COLS);
@@ -144,6 +228,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     tc::mbar_init(&s_bar, 1);
     tc::fence_mbar_init();
     s_abort = 0;
+    s_range = 0;
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -166,6 +251,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   }
   auto write_state_operand = [&]() {
     // S^T (N = value column j, K = key channel `row`), fp16, padded layout
+#pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int jj = 32 * chalf + j;
       *reinterpret_cast<uint16_t*>(smem + ST + tc::cm_offset(jj, row, LBO_P, ST_SBO)) = f16_bits(S[j]);
@@ -181,106 +267,109 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     return ok;
   };
 
-  const uint32_t nchunks = (eos - bos + C - 1) / C;
   for (uint32_t cidx = 0; cidx < nchunks; ++cidx) {
     const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(cidx) * C;
-    const int n = static_cast<int>(min(static_cast<int64_t>(C), static_cast<int64_t>(eos) - t0));
+    const int n = chunk_n(cidx);
 
     // ---------------------------------------------------------------- phase 0: load
-    for (int u = tid; u < C * (D / 8); u += NT) {       // k, q rows: 16 vectors of 8 bf16
-      const int i = u / (D / 8), q8 = u % (D / 8);
-      uint4 kv = make_uint4(0, 0, 0, 0), qv = kv;
-      if (i < n) {
-        const int64_t t = t0 + i;
-        kv = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(P.k) + t * P.k_stride +
-                                             static_cast<int64_t>(kh) * D + q8 * 8);
-        qv = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(P.q) + t * P.q_stride +
-                                             static_cast<int64_t>(kh) * D + q8 * 8);
-      }
-      *reinterpret_cast<uint4*>(smem + S_K + (i * D + q8 * 8) * 2) = kv;
-      *reinterpret_cast<uint4*>(smem + S_Q + (i * D + q8 * 8) * 2) = qv;
-    }
-    for (int u = tid; u < C * (BV / 8); u += NT) {
-      const int i = u / (BV / 8), q8 = u % (BV / 8);
-      uint4 vv = make_uint4(0, 0, 0, 0);
-      if (i < n)
-        vv = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(P.v) +
-                                             (t0 + i) * P.v_stride + static_cast<int64_t>(h) * D +
-                                             vt * BV + q8 * 8);
-      *reinterpret_cast<uint4*>(smem + S_V + (i * BV + q8 * 8) * 2) = vv;
-    }
-    if (PERCH) {
-      for (int u = tid; u < C * (D / 4); u += NT) {
-        const int i = u / (D / 4), q4 = u % (D / 4);
-        float4 gv = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (i < n) gv = *reinterpret_cast<const float4*>(P.g + ((t0 + i) * HV + h) * D + q4 * 4);
-        *reinterpret_cast<float4*>(sG + i * D + q4 * 4) = gv;
-      }
-    }
-    for (int i = tid; i < C; i += NT) {
-      const bool live = i < n;
-      sBeta[i] = live ? P.beta[(t0 + i) * HV + h] : 0.f;
-      if (!PERCH) sG[i] = live ? P.g[(t0 + i) * HV + h] : 0.f;
-    }
+    tc::cp_async_wait_all();
     __syncthreads();
 
     // ---------------------------------------------------------------- phase 1: prep
-    for (int i = warp; i < C; i += NT / 32) {
+    {                                                   // L2 norms: 4 threads per row
+      const int i = tid >> 2, part = tid & 3;
       float sk = 0.f, sq = 0.f;
-      for (int c = lane; c < D; c += 32) {
-        const float kx = bf16_at(smem, S_K, i * D + c), qx = bf16_at(smem, S_Q, i * D + c);
-        sk += kx * kx;
-        sq += qx * qx;
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        float kx[8], qx[8];
+        bf16x8_load(smem + S_K + (i * KS + part * 32 + g8 * 8) * 2, kx);
+        bf16x8_load(smem + S_Q + (i * KS + part * 32 + g8 * 8) * 2, qx);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          sk += kx[e] * kx[e];
+          sq += qx[e] * qx[e];
+        }
       }
-      sk = warp_sum(sk);
-      sq = warp_sum(sq);
-      if (lane == 0) {
+      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+      if (part == 0) {
         sRK[i] = P.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
         sRQ[i] = (P.l2norm ? rsqrtf(sq + 1e-6f) : 1.f) * P.scale;
       }
     }
     if (PERCH) {
-      if (tid < D) {
+      if (tid < D) {                                    // channel tid: inclusive cumsum
         float acc = 0.f;
-        for (int i = 0; i < C; ++i) {
-          acc += sG[i * D + tid];
-          sG[i * D + tid] = acc;
+#pragma unroll
+        for (int i0 = 0; i0 < C; i0 += 16) {
+          float gv[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) gv[e] = sG[(i0 + e) * GS + tid];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            acc += gv[e];
+            sG[(i0 + e) * GS + tid] = acc;
+          }
         }
         sGam[tid] = __expf(acc);
-        sGA[tid] = sG[((n - 1) / 2) * D + tid];
+        sGA[tid] = sG[((n - 1) / 2) * GS + tid];
       }
-    } else if (tid == 0) {
-      float acc = 0.f;
-      for (int i = 0; i < C; ++i) {
-        acc += sG[i];
-        sG[i] = acc;
+    } else if (warp == 0) {                             // scalar: warp scan of 64 values
+      const float g0 = sGs[2 * lane], g1 = sGs[2 * lane + 1];
+      float s = g0 + g1;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += y;
       }
-      sGam[0] = __expf(acc);
+      const float gl = __shfl_sync(0xffffffffu, s, 31);
+      sGs[2 * lane] = s - g1;
+      sGs[2 * lane + 1] = s;
+      sEG[2 * lane] = __expf(s - g1);
+      sEG[2 * lane + 1] = __expf(s);
+      sEGL[2 * lane] = __expf(gl - (s - g1));
+      sEGL[2 * lane + 1] = __expf(gl - s);
+      const float gam = __expf(gl);
+      sGam[lane] = gam; sGam[lane + 32] = gam; sGam[lane + 64] = gam; sGam[lane + 96] = gam;
     }
     __syncthreads();
-    if (!PERCH) {
-      if (tid < D) sGam[tid] = sGam[0];
-      __syncthreads();
-    }
-    // A-GEMM operands: [K+; Q+] (rows 0-63 keys, 64-127 queries) and K-
-    for (int u = tid; u < 3 * C * (D / 8); u += NT) {
-      const int which = u / (C * (D / 8));          // 0: K+, 1: Q+, 2: K-
-      const int r = (u / (D / 8)) % C, q8 = u % (D / 8);
-      const uint32_t srcbase = which == 1 ? S_Q : S_K;
-      const uint32_t src = srcbase + (r * D + q8 * 8) * 2;
-      const uint32_t dst = which == 2 ? BK + tc::cm_offset(r, q8 * 8, 128, dense_sbo(D))
-                                      : AK + tc::cm_offset(r + (which == 1 ? C : 0), q8 * 8, 128,
-                                                           dense_sbo(D));
+    // A-GEMM operands: [K+; Q+] (rows 0-63 keys, 64-127 queries) and K-; consecutive
+    // threads fill one core matrix (8 rows x 16 B) at a time
+    for (int u = tid; u < C * (D / 8); u += NT) {
+      const int r = (u / (8 * (D / 8))) * 8 + (u & 7), q8 = (u >> 3) % (D / 8);
+      const uint32_t ks = S_K + (r * KS + q8 * 8) * 2, qs = S_Q + (r * KS + q8 * 8) * 2;
+      const uint32_t kp = AK + tc::cm_offset(r, q8 * 8, 128, dense_sbo(D));
+      const uint32_t qp = AK + tc::cm_offset(r + C, q8 * 8, 128, dense_sbo(D));
+      const uint32_t km = BK + tc::cm_offset(r, q8 * 8, 128, dense_sbo(D));
       if (!PERCH) {
-        *reinterpret_cast<uint4*>(smem + dst) = *reinterpret_cast<const uint4*>(smem + src);
+        const uint4 kv = *reinterpret_cast<const uint4*>(smem + ks);
+        *reinterpret_cast<uint4*>(smem + kp) = kv;
+        *reinterpret_cast<uint4*>(smem + km) = kv;
+        *reinterpret_cast<uint4*>(smem + qp) = *reinterpret_cast<const uint4*>(smem + qs);
       } else {
-        float x[8];
+        float kx[8], qx[8], kn[8];
+        bf16x8_load(smem + ks, kx);
+        bf16x8_load(smem + qs, qx);
+        const float rk = sRK[r], rq = sRQ[r];             // normalised rows: entries <= 1
+        const float4 g0 = *reinterpret_cast<const float4*>(sG + r * GS + q8 * 8);
+        const float4 g1 = *reinterpret_cast<const float4*>(sG + r * GS + q8 * 8 + 4);
+        const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const int c = q8 * 8 + e;
-          const float gd = sG[r * D + c] - sGA[c];
-          x[e] = bf16_at(smem, srcbase, r * D + c) * __expf(which == 2 ? -gd : gd);
+          const float gd = gv[e] - sGA[q8 * 8 + e];
+          if (fabsf(gd) > kMaxHalfChunkDecay) s_range = 1;
+          const float f = __expf(gd);                       // exp(G_r - G_a)
+          kx[e] *= rk;
+          qx[e] *= rq;
+          kn[e] = kx[e] * __frcp_rn(f);
+          kx[e] *= f;
+          qx[e] *= f;
         }
-        f16x8_store(smem, dst, x);
+        f16x8_store(smem, kp, kx);
+        f16x8_store(smem, qp, qx);
+        f16x8_store(smem, km, kn);
       }
     }
     tc::fence_async_smem();
@@ -298,6 +387,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
                    s > 0);
       tc::mma_commit(&s_bar);
     }
+    for (int idx = tid; idx < C * SP; idx += NT) sT[idx] = 0.f;
     mma_wait();
 
     // ---------------------------------------------------------------- phase 3: A_kk, A_qk
@@ -308,70 +398,119 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       tc::tmem_wait_ld();
       const bool is_k = row < C;
       const int i = is_k ? row : row - C;
-      const float ri = is_k ? sRK[i] * sBeta[i] : sRQ[i];
+      // scalar decay multiplied raw bf16 rows: apply the norms, scale and exp(G_i - G_j)
+      // here; per-channel decay multiplied normalised, decayed rows already
+      const float ri = is_k ? (PERCH ? 1.f : sRK[i]) * sBeta[i] : (PERCH ? 1.f : sRQ[i]);
       float x[32];
+#pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int j = 32 * chalf + e;
         const float raw = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
-        float a = raw * ri * sRK[j];
-        if (!PERCH) a *= __expf(sG[i] - sG[j]);
+        float a = raw * ri;
+        if (!PERCH) a *= sRK[j] * __expf(sGs[i] - sGs[j]);
         const bool keep = is_k ? (j < i) : (j <= i);
         x[e] = keep ? a : 0.f;
       }
       if (is_k) {
-        for (int e = 0; e < 32; ++e) sA[i * SP + 32 * chalf + e] = x[e];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(sA + i * SP + 32 * chalf + e) =
+              make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
         // identity rows of L = [I; A_qk]
         float idv[32];
+#pragma unroll
         for (int e = 0; e < 32; ++e) idv[e] = (32 * chalf + e == i) ? 1.f : 0.f;
+#pragma unroll
         for (int g8 = 0; g8 < 4; ++g8)
           f16x8_store(smem, LMAT + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, dense_sbo(64)),
                       idv + 8 * g8);
       } else {
+#pragma unroll
         for (int g8 = 0; g8 < 4; ++g8)
           f16x8_store(smem, LMAT + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, dense_sbo(64)),
                       x + 8 * g8);
       }
     }
-    for (int idx = tid; idx < C * SP; idx += NT) sT[idx] = 0.f;
-    tc::fence_before_sync();
     __syncthreads();
 
     // ---------------------------------------------------------------- phase 4: solve
-    if (warp < C / 16 && lane < 16) {
-      const int base = warp * 16, col = base + lane;
+    // diagonal 16x16 blocks: lane (block, column) keeps its column of the block's inverse
+    // in registers and substitutes row by row
+    if (warp < 2) {
+      const int base = (warp * 2 + (lane >> 4)) * 16, col = lane & 15;
+      float t[16];
+#pragma unroll
       for (int r = 0; r < 16; ++r) {
-        const int rr = base + r;
-        float val = r == lane ? 1.f : 0.f;
-        for (int m = lane; m < r; ++m) val -= sA[rr * SP + base + m] * sT[(base + m) * SP + col];
-        sT[rr * SP + col] = r >= lane ? val : 0.f;
-        __syncwarp(0x0000ffffu);
+        float v = r == col ? 1.f : 0.f;
+#pragma unroll
+        for (int m = 0; m < r; ++m) v -= sA[(base + r) * SP + base + m] * t[m];
+        t[r] = v;
       }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) sT[(base + r) * SP + base + col] = t[r];
     }
     __syncthreads();
-    for (int s = 16; s < C; s *= 2) {
-      const int pairs = C / (2 * s);
-      for (int idx = tid; idx < pairs * s * s; idx += NT) {
-        const int p = idx / (s * s), r = (idx / s) % s, c = idx % s;
-        const int r0 = 2 * p * s + s, c0 = 2 * p * s;
-        float acc = 0.f;
-        for (int m = c; m < s; ++m) acc += sA[(r0 + r) * SP + c0 + m] * sT[(c0 + m) * SP + c0 + c];
-        sX[(p * s + r) * 33 + c] = acc;
+    // merges: T21 = -T22 (A21 T11), block size 16 (two pairs) then 32 (one pair);
+    // each thread owns a 1 x 4 strip of the output
+    if (tid < 128) {                                      // X = A21 T11, two 16x16 pairs
+      const int p = tid >> 6, r = (tid >> 2) & 15, c = (tid & 3) * 4;
+      const int r0 = 32 * p + 16, c0 = 32 * p;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float a = sA[(r0 + r) * SP + c0 + m];
+        const float4 t = *reinterpret_cast<const float4*>(sT + (c0 + m) * SP + c0 + c);
+        acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
       }
-      __syncthreads();
-      for (int idx = tid; idx < pairs * s * s; idx += NT) {
-        const int p = idx / (s * s), r = (idx / s) % s, c = idx % s;
-        const int r0 = 2 * p * s + s, c0 = 2 * p * s;
-        float acc = 0.f;
-        for (int m = 0; m <= r; ++m) acc += sT[(r0 + r) * SP + r0 + m] * sX[(p * s + m) * 33 + c];
-        sT[(r0 + r) * SP + c0 + c] = -acc;
-      }
-      __syncthreads();
+      *reinterpret_cast<float4*>(sX + (16 * p + r) * XP + c) = acc;
     }
+    __syncthreads();
+    if (tid < 128) {                                      // T21 = -T22 X
+      const int p = tid >> 6, r = (tid >> 2) & 15, c = (tid & 3) * 4;
+      const int r0 = 32 * p + 16, c0 = 32 * p;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        const float a = sT[(r0 + r) * SP + r0 + m];
+        const float4 x = *reinterpret_cast<const float4*>(sX + (16 * p + m) * XP + c);
+        acc.x += a * x.x; acc.y += a * x.y; acc.z += a * x.z; acc.w += a * x.w;
+      }
+      *reinterpret_cast<float4*>(sT + (r0 + r) * SP + c0 + c) =
+          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    }
+    __syncthreads();
+    {                                                     // X = A21 T11, one 32x32 pair
+      const int r = tid >> 3, c = (tid & 7) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {
+        const float a = sA[(32 + r) * SP + m];
+        const float4 t = *reinterpret_cast<const float4*>(sT + m * SP + c);
+        acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
+      }
+      *reinterpret_cast<float4*>(sX + r * XP + c) = acc;
+    }
+    __syncthreads();
+    {                                                     // T21 = -T22 X
+      const int r = tid >> 3, c = (tid & 7) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int m = 0; m < 32; ++m) {
+        const float a = sT[(32 + r) * SP + 32 + m];
+        const float4 x = *reinterpret_cast<const float4*>(sX + m * XP + c);
+        acc.x += a * x.x; acc.y += a * x.y; acc.z += a * x.z; acc.w += a * x.w;
+      }
+      *reinterpret_cast<float4*>(sT + (32 + r) * SP + c) =
+          make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    }
+    __syncthreads();
     // TB^T[j][m] = T[m][j] beta_j  (N = j, K = m)
     for (int u = tid; u < C * (C / 8); u += NT) {
       const int j = u % C, m8 = u / C;
+      const float bj = sBeta[j];
       float x[8];
-      for (int e = 0; e < 8; ++e) x[e] = sT[(m8 * 8 + e) * SP + j] * sBeta[j];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = sT[(m8 * 8 + e) * SP + j] * bj;
       f16x8_store(smem, TBT + tc::cm_offset(j, m8 * 8, 128, dense_sbo(64)), x);
     }
     tc::fence_async_smem();
@@ -392,14 +531,25 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     // ---------------------------------------------------------------- phase 6: K~^T, K_end^T, V^T
     for (int u = tid; u < D * (C / 8); u += NT) {         // (channel c, 8 tokens)
       const int c = u % D, m8 = u / D;
-      const float Gl = PERCH ? sG[(C - 1) * D + c] : sG[C - 1];
       float kt[8], ke[8];
-      for (int e = 0; e < 8; ++e) {
-        const int m = m8 * 8 + e;
-        const float Gm = PERCH ? sG[m * D + c] : sG[m];
-        const float kx = bf16_at(smem, S_K, m * D + c) * sRK[m];
-        kt[e] = kx * __expf(Gm);
-        ke[e] = kx * __expf(Gl - Gm);
+      if (PERCH) {
+        const float Gl = sG[(C - 1) * GS + c];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int m = m8 * 8 + e;
+          const float Gm = sG[m * GS + c];
+          const float kx = bf16_at(smem, S_K, m * KS + c) * sRK[m];
+          kt[e] = kx * __expf(Gm);
+          ke[e] = kx * __expf(Gl - Gm);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int m = m8 * 8 + e;
+          const float kx = bf16_at(smem, S_K, m * KS + c) * sRK[m];
+          kt[e] = kx * sEG[m];
+          ke[e] = kx * sEGL[m];
+        }
       }
       f16x8_store(smem, KTT + tc::cm_offset(c, m8 * 8, 128, dense_sbo(64)), kt);
       f16x8_store(smem, KET + tc::cm_offset(c, m8 * 8, 128, dense_sbo(64)), ke);
@@ -407,7 +557,8 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     for (int u = tid; u < BV * (C / 8); u += NT) {        // (value column j, 8 tokens)
       const int j = u % BV, m8 = u / BV;
       float x[8];
-      for (int e = 0; e < 8; ++e) x[e] = bf16_at(smem, S_V, (m8 * 8 + e) * BV + j);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = bf16_at(smem, S_V, (m8 * 8 + e) * VS + j);
       f16x8_store(smem, VT + tc::cm_offset(j, m8 * 8, 128, dense_sbo(64)), x);
     }
     tc::fence_async_smem();
@@ -420,10 +571,12 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       tc::tmem_ld16(tmem + lane_addr + T_X + 32 * chalf + 16, r1);
       tc::tmem_wait_ld();
       float x[32];
+#pragma unroll
       for (int e = 0; e < 16; ++e) {
         x[e] = __uint_as_float(r0[e]);
         x[e + 16] = __uint_as_float(r1[e]);
       }
+#pragma unroll
       for (int g8 = 0; g8 < 4; ++g8)
         f16x8_store(smem, A1 + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, dense_sbo(64)),
                     x + 8 * g8);
@@ -446,6 +599,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     mma_wait();
 
     // ---------------------------------------------------------------- phase 9: A2
+#pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int c0 = 64 * chalf + 32 * half;
       uint32_t r0[16], r1[16];
@@ -453,16 +607,32 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       tc::tmem_ld16(tmem + lane_addr + T_Y + c0 + 16, r1);
       tc::tmem_wait_ld();
       float x[32];
-      for (int e = 0; e < 32; ++e) {
-        const float y = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
-        float qt = 0.f;
-        if (row >= C) {
-          const int i = row - C, c = c0 + e;
-          const float Gi = PERCH ? sG[i * D + c] : sG[i];
-          qt = bf16_at(smem, S_Q, i * D + c) * sRQ[i] * __expf(Gi);
+      if (row >= C) {                                     // Q~ = q scale/|q| exp(G)
+        const int i = row - C;
+        const float rq = sRQ[i];
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+          float qv[8];
+          bf16x8_load(smem + S_Q + (i * KS + c0 + 8 * g8) * 2, qv);
+          if (PERCH) {
+            const float4 ga = *reinterpret_cast<const float4*>(sG + i * GS + c0 + 8 * g8);
+            const float4 gb = *reinterpret_cast<const float4*>(sG + i * GS + c0 + 8 * g8 + 4);
+            const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * rq * __expf(gv[e]);
+          } else {
+            const float f = rq * sEG[i];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * f;
+          }
         }
-        x[e] = qt - y;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = 0.f;
       }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] -= __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
+#pragma unroll
       for (int g8 = 0; g8 < 4; ++g8)
         f16x8_store(smem, A2 + tc::cm_offset(row, c0 + 8 * g8, 128, dense_sbo(D)), x + 8 * g8);
     }
@@ -470,6 +640,9 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    // the staging buffers are free: prefetch the next chunk's inputs
+    if (cidx + 1 < nchunks)
+      tc_issue_loads<PERCH>(P, smem, t0 + C, chunk_n(cidx + 1), kh, h, vt, tid);
 
     // ---------------------------------------------------------------- phase 10: [E; O]
     if (tid == 0) {
@@ -494,6 +667,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       tc::tmem_ld16(tmem + lane_addr + T_D1 + 32 * chalf + 16, r1);
       tc::tmem_wait_ld();
       if (row < C) {
+#pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float ev = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
           *reinterpret_cast<uint16_t*>(smem + ET + tc::cm_offset(32 * chalf + e, row, LBO_P, ET_SBO)) =
@@ -501,6 +675,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
         }
       } else if (row - C < n) {
         float* op = P.o + ((t0 + row - C) * HV + h) * D + vt * BV + 32 * chalf;
+#pragma unroll
         for (int e = 0; e < 16; e += 4) {
           *reinterpret_cast<float4*>(op + e) =
               make_float4(__uint_as_float(r0[e]), __uint_as_float(r0[e + 1]),
@@ -535,6 +710,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       tc::tmem_ld16(tmem + lane_addr + T_D2 + 32 * chalf + 16, r1);
       tc::tmem_wait_ld();
       const float gam = sGam[row];
+#pragma unroll
       for (int e = 0; e < 32; ++e)
         S[e] = gam * S[e] + __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
       write_state_operand();
@@ -545,7 +721,9 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     tc::fence_after_sync();
     if (s_abort) break;
   }
+  tc::cp_async_wait_all();
 
+  if (PERCH && s_range && tid == 0) raise_device_error(P.err, KDA_DEVERR_DECAY_RANGE);
   if (s_abort) {
     // give the tensor core a last bounded chance to drain before TMEM is released
     tc::mbar_wait_bounded(&s_bar, phase & 1, kWaitLimit);

@@ -286,3 +286,25 @@ def test_tensor_core_path_matches_cuda_core_path(decay, state):
     assert rel_err(o_tc, o_cc) <= tol
     assert rel_err(o_tc, o_ref) <= tol and rel_err(o_cc, o_ref) <= tol
     assert state_err(p, s_tc, pool_ref) <= tol and state_err(p, s_cc, pool_ref) <= tol
+
+
+def test_decay_range_flagged_and_cuda_core_path_exact():
+    """Per-channel decay stronger than the tensor-core path's fp16 factors allow (about
+    -0.9 nats per token, 29 nats over half a chunk) is reported on the device
+    (KDA_DEVERR_DECAY_RANGE); the fp32 CUDA-core path stays within tolerance."""
+    p = small("strong-decay", [130, 64], 1, 2, 128, "bf16", "f32", "per_channel", 64, seed=51)
+    p.g[:] = (p.g * 6.0).astype(np.float32)               # mean about -0.9 per token
+    t = torch_io.prefill_inputs(p, DEV)
+    kda.prefill(**t, chunk=64)
+    torch.cuda.synchronize()
+    assert kda.get_device_error() == 5
+    o, pool, _ = gpu_prefill(p, cuda_cores=True)
+    o_ref, pool_ref = oracle.run(p)
+    assert rel_err(o, o_ref) <= TOL["bf16"] and state_err(p, pool, pool_ref) <= TOL["bf16"]
+
+
+def test_moderate_decay_stays_on_tensor_cores():
+    """Decay within range (half-chunk decay well under 11 nats) raises nothing."""
+    p = small("mid-decay", [200], 1, 2, 128, "bf16", "f32", "per_channel", 64, seed=52)
+    p.g[:] = (p.g * 2.0).astype(np.float32)               # about -0.3 per token
+    check_prefill(p)

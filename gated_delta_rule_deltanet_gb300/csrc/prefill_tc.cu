@@ -9,9 +9,11 @@
 //
 //   A-GEMM   [K+; Q+] K-^T               -> A_kk, A_qk                  M=128 N=64  K=128
 //            (scalar decay: raw bf16 q, k, with the norms and exp(G_i - G_j)
-//             applied to the result; per-channel decay: fp16 operands
-//             k^ exp(G - G_a), q^ exp(G - G_a), k^ exp(G_a - G) of the
-//             normalised rows with a mid-chunk anchor G_a)
+//             applied to the result; per-channel decay: k^ exp(G - G_a),
+//             q^ exp(G - G_a), k^ exp(G_a - G) of the normalised rows with a
+//             mid-chunk anchor G_a, each split into bf16 high and low halves and
+//             multiplied as hi*hi + hi*lo + lo*hi, ~16-bit precision over the
+//             whole bf16 exponent range)
 //   solve    T = (I + A_kk)^-1 on CUDA cores (16x16 forward substitution,
 //            then T21 = -T22 A21 T11 merges), TB = T diag(beta)
 //   X        [I; A_qk] TB          = [TB; A_qk TB]                    M=128 N=64  K=64
@@ -21,15 +23,13 @@
 //
 // (E = U - W S are the corrected values and O = Q~ S + A_qk E the outputs of the
 // chunk; folding A_qk into the first operand gives O from the same MMA as E.)
-// Operands are fp16 (10-bit mantissa, the same as tf32) except the raw bf16
-// inputs of the scalar-decay A-GEMM.  The decayed keys and queries are bounded
-// by 1 (unit rows, decay factors <= 1); v, E and the state must stay inside the
-// fp16 range (|x| < 65504), which activations and states of normalised-key
-// recurrences do.  Per-channel decay uses exp(G_i - G_a) and exp(G_a - G_j)
-// with the anchor at the chunk's middle token, which keeps both factors finite
-// while the cumulative decay over half a chunk stays below ~11 nats per
-// channel (an average log-decay above -0.34 per token); outside these limits
-// the fp32 CUDA-core path (KDA_FLAG_CUDA_CORES) is exact.
+// Operands after the A-GEMM are fp16 (10-bit mantissa, the same as tf32).  The
+// decayed keys and queries are bounded by 1 (unit rows, decay factors <= 1); v,
+// E and the state must stay inside the fp16 range (|x| < 65504), which
+// activations and states of normalised-key recurrences do.  The anchored
+// per-channel factors exp(G_i - G_a), exp(G_a - G_j) need only stay finite in
+// fp32 (cumulative decay below 80 nats over half a chunk, checked); outside
+// these limits the fp32 CUDA-core path (KDA_FLAG_CUDA_CORES) is exact.
 //
 // The raw inputs of the next chunk are prefetched with cp.async into the
 // staging buffers as soon as the current chunk no longer reads them, so their
@@ -53,7 +53,7 @@ constexpr int D = 128;      // head size
 constexpr int BV = 64;      // value columns per CTA
 constexpr int NT = 256;     // threads (8 warps)
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls before a wait is declared stuck
-constexpr float kMaxHalfChunkDecay = 11.0f;  // exp(11) < 65504, the largest fp16
+constexpr float kMaxHalfChunkDecay = 80.0f;  // exp(80) stays finite in fp32 and bf16
 
 // padded staging rows (elements)
 constexpr int KS = D + 8;    // k, q rows: bf16, 272 B
@@ -101,9 +101,14 @@ constexpr uint32_t SMEM_BYTES = ET + (BV / 8) * ET_SBO;
 static_assert(KET + 128 * 64 * 2 <= R3, "K~/K_end alias the solve area");
 static_assert(A2 + 128 * 128 * 2 <= R2, "A1/A2 alias the A-GEMM operands");
 static_assert(SMEM_BYTES + 64 <= 227 * 1024, "shared memory budget");
+// per-channel decay: low bf16 halves of K- (A-GEMM B operand) live in the TB^T and V^T
+// buffers, which are dead between a chunk's chain MMA and the next chunk's solve
+constexpr uint32_t BKLO = TBT;
+static_assert(VT == TBT + 64 * 64 * 2, "K- low half spans TB^T and V^T");
 
 // TMEM columns
-constexpr uint32_t T_A = 0, T_X = 64, T_Y = 128, T_D1 = 256, T_D2 = 320, T_COLS = 512;
+constexpr uint32_t T_A = 0, T_X = 64, T_Y = 128, T_D1 = 256, T_D2 = 320, T_ALO = 384,
+                   T_COLS = 512;
 
 // dense K-major tiles: lbo 128, sbo = (K / 8) * 128
 __host__ __device__ constexpr uint32_t dense_sbo(uint32_t K) { return (K / 8) * 128; }
@@ -335,41 +340,89 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       sGam[lane] = gam; sGam[lane + 32] = gam; sGam[lane + 64] = gam; sGam[lane + 96] = gam;
     }
     __syncthreads();
-    // A-GEMM operands: [K+; Q+] (rows 0-63 keys, 64-127 queries) and K-; consecutive
-    // threads fill one core matrix (8 rows x 16 B) at a time
-    for (int u = tid; u < C * (D / 8); u += NT) {
-      const int r = (u / (8 * (D / 8))) * 8 + (u & 7), q8 = (u >> 3) % (D / 8);
-      const uint32_t ks = S_K + (r * KS + q8 * 8) * 2, qs = S_Q + (r * KS + q8 * 8) * 2;
-      const uint32_t kp = AK + tc::cm_offset(r, q8 * 8, 128, dense_sbo(D));
-      const uint32_t qp = AK + tc::cm_offset(r + C, q8 * 8, 128, dense_sbo(D));
-      const uint32_t km = BK + tc::cm_offset(r, q8 * 8, 128, dense_sbo(D));
-      if (!PERCH) {
+    // A-GEMM operands: [K+; Q+] (rows 0-63 keys, 64-127 queries) and K-.
+    if (!PERCH) {
+      // raw bf16 rows; consecutive threads fill one core matrix (8 rows x 16 B) at a time
+      for (int u = tid; u < C * (D / 8); u += NT) {
+        const int r = (u / (8 * (D / 8))) * 8 + (u & 7), q8 = (u >> 3) % (D / 8);
+        const uint32_t ks = S_K + (r * KS + q8 * 8) * 2, qs = S_Q + (r * KS + q8 * 8) * 2;
         const uint4 kv = *reinterpret_cast<const uint4*>(smem + ks);
-        *reinterpret_cast<uint4*>(smem + kp) = kv;
-        *reinterpret_cast<uint4*>(smem + km) = kv;
-        *reinterpret_cast<uint4*>(smem + qp) = *reinterpret_cast<const uint4*>(smem + qs);
-      } else {
-        float kx[8], qx[8], kn[8];
-        bf16x8_load(smem + ks, kx);
-        bf16x8_load(smem + qs, qx);
-        const float rk = sRK[r], rq = sRQ[r];             // normalised rows: entries <= 1
-        const float4 g0 = *reinterpret_cast<const float4*>(sG + r * GS + q8 * 8);
-        const float4 g1 = *reinterpret_cast<const float4*>(sG + r * GS + q8 * 8 + 4);
-        const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        *reinterpret_cast<uint4*>(smem + AK + tc::cm_offset(r, q8 * 8, 128, dense_sbo(D))) = kv;
+        *reinterpret_cast<uint4*>(smem + BK + tc::cm_offset(r, q8 * 8, 128, dense_sbo(D))) = kv;
+        *reinterpret_cast<uint4*>(smem + AK + tc::cm_offset(r + C, q8 * 8, 128, dense_sbo(D))) =
+            *reinterpret_cast<const uint4*>(smem + qs);
+      }
+    } else {
+      // normalised rows times exp(+-(G - G_a)), split into bf16 high and low halves
+      // (x = hi + lo to about 16 bits with the full bf16 exponent range): the high halves
+      // go to the shared-memory operands, the low half of [K+; Q+] to tensor memory
+      {
+        const int i = row < C ? row : row - C;
+        const uint32_t src = (row < C ? S_K : S_Q) + (i * KS) * 2;
+        const float rs = row < C ? sRK[i] : sRQ[i];
+        uint32_t lo[32];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float gd = gv[e] - sGA[q8 * 8 + e];
-          if (fabsf(gd) > kMaxHalfChunkDecay) s_range = 1;
-          const float f = __expf(gd);                       // exp(G_r - G_a)
-          kx[e] *= rk;
-          qx[e] *= rq;
-          kn[e] = kx[e] * __frcp_rn(f);
-          kx[e] *= f;
-          qx[e] *= f;
+        for (int g8 = 0; g8 < 8; ++g8) {
+          const int cc = 64 * chalf + 8 * g8;
+          float x[8];
+          bf16x8_load(smem + src + cc * 2, x);
+          const float4 g0 = *reinterpret_cast<const float4*>(sG + i * GS + cc);
+          const float4 g1 = *reinterpret_cast<const float4*>(sG + i * GS + cc + 4);
+          const float4 a0 = *reinterpret_cast<const float4*>(sGA + cc);
+          const float4 a1 = *reinterpret_cast<const float4*>(sGA + cc + 4);
+          const float gd[8] = {g0.x - a0.x, g0.y - a0.y, g0.z - a0.z, g0.w - a0.w,
+                               g1.x - a1.x, g1.y - a1.y, g1.z - a1.z, g1.w - a1.w};
+          uint32_t hi[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            if (fabsf(gd[e]) > kMaxHalfChunkDecay || fabsf(gd[e + 1]) > kMaxHalfChunkDecay) s_range = 1;
+            const float v0 = x[e] * rs * __expf(gd[e]), v1 = x[e + 1] * rs * __expf(gd[e + 1]);
+            hi[e / 2] = tc::pack_bf16x2(v0, v1);
+            const float h0 = __uint_as_float(hi[e / 2] << 16);
+            const float h1 = __uint_as_float(hi[e / 2] & 0xffff0000u);
+            lo[4 * g8 + e / 2] = tc::pack_bf16x2(v0 - h0, v1 - h1);
+          }
+          *reinterpret_cast<uint4*>(smem + AK + tc::cm_offset(row, cc, 128, dense_sbo(D))) =
+              make_uint4(hi[0], hi[1], hi[2], hi[3]);
         }
-        f16x8_store(smem, kp, kx);
-        f16x8_store(smem, qp, qx);
-        f16x8_store(smem, km, kn);
+        uint32_t l0[16], l1[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          l0[e] = lo[e];
+          l1[e] = lo[16 + e];
+        }
+        tc::tmem_st16(tmem + lane_addr + T_ALO + 32 * chalf, l0);
+        tc::tmem_st16(tmem + lane_addr + T_ALO + 32 * chalf + 16, l1);
+        tc::tmem_wait_st();
+      }
+      {                                                   // K-: 4 threads per key row
+        const int j = tid >> 2, qq = tid & 3;
+        const float rs = sRK[j];
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+          const int cc = 32 * qq + 8 * g8;
+          float x[8];
+          bf16x8_load(smem + S_K + (j * KS + cc) * 2, x);
+          const float4 g0 = *reinterpret_cast<const float4*>(sG + j * GS + cc);
+          const float4 g1 = *reinterpret_cast<const float4*>(sG + j * GS + cc + 4);
+          const float4 a0 = *reinterpret_cast<const float4*>(sGA + cc);
+          const float4 a1 = *reinterpret_cast<const float4*>(sGA + cc + 4);
+          const float gd[8] = {a0.x - g0.x, a0.y - g0.y, a0.z - g0.z, a0.w - g0.w,
+                               a1.x - g1.x, a1.y - g1.y, a1.z - g1.z, a1.w - g1.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float v0 = x[e] * rs * __expf(gd[e]), v1 = x[e + 1] * rs * __expf(gd[e + 1]);
+            hi[e / 2] = tc::pack_bf16x2(v0, v1);
+            const float h0 = __uint_as_float(hi[e / 2] << 16);
+            const float h1 = __uint_as_float(hi[e / 2] & 0xffff0000u);
+            lo[e / 2] = tc::pack_bf16x2(v0 - h0, v1 - h1);
+          }
+          *reinterpret_cast<uint4*>(smem + BK + tc::cm_offset(j, cc, 128, dense_sbo(D))) =
+              make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(smem + BKLO + tc::cm_offset(j, cc, 128, dense_sbo(D))) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
       }
     }
     tc::fence_async_smem();
@@ -379,12 +432,21 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
 
     // ---------------------------------------------------------------- phase 2: A-GEMM
     if (tid == 0) {
-      const uint32_t id = tc::idesc_f16(128, 64, PERCH ? tc::kF16 : tc::kBF16);
-      for (int s = 0; s < D / 16; ++s)
+      const uint32_t id = tc::idesc_f16(128, 64, tc::kBF16);
+      for (int s = 0; s < D / 16; ++s)                   // hi x hi
         tc::mma_ss(tmem + T_A,
                    tc::smem_desc(tc::smem_u32(smem + AK) + s * 256, 128, dense_sbo(D)),
                    tc::smem_desc(tc::smem_u32(smem + BK) + s * 256, 128, dense_sbo(D)), id,
                    s > 0);
+      if (PERCH) {
+        for (int s = 0; s < D / 16; ++s)                 // hi x lo
+          tc::mma_ss(tmem + T_A,
+                     tc::smem_desc(tc::smem_u32(smem + AK) + s * 256, 128, dense_sbo(D)),
+                     tc::smem_desc(tc::smem_u32(smem + BKLO) + s * 256, 128, dense_sbo(D)), id, 1);
+        for (int s = 0; s < D / 16; ++s)                 // lo x hi (low half read from TMEM)
+          tc::mma_ts(tmem + T_A, tmem + T_ALO + s * 8,
+                     tc::smem_desc(tc::smem_u32(smem + BK) + s * 256, 128, dense_sbo(D)), id, 1);
+      }
       tc::mma_commit(&s_bar);
     }
     for (int idx = tid; idx < C * SP; idx += NT) sT[idx] = 0.f;

@@ -90,8 +90,8 @@ typedef enum kda_decay_kind {
 #define KDA_DEVERR_SLOT_DUP 3   /* a slot named twice (KDA_FLAG_CHECKED only) */
 #define KDA_DEVERR_TIMEOUT 4    /* a bounded wait inside a kernel gave up; its work is incomplete */
 #define KDA_DEVERR_DECAY_RANGE 5 /* tensor-core path, per-channel decay: the cumulative log-decay
-                                    over half a chunk exceeded 11 nats in some channel, so its
-                                    fp16 decay factors overflowed; rerun with KDA_FLAG_CUDA_CORES */
+                                    over half a chunk exceeded 80 nats in some channel, so its
+                                    anchored decay factors overflow; rerun with KDA_FLAG_CUDA_CORES */
 
 typedef struct kda_params {
   int32_t num_seqs;    /* B: sequences in the ragged batch (prefill) or decode batch */

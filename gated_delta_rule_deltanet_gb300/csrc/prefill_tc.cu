@@ -2,7 +2,7 @@
 //
 // One CTA owns one (sequence, value head, 64-wide value tile) and walks the
 // sequence's chunks in order, keeping its 128 x 64 slice of the state in fp32
-// registers.  Every contraction of the chunk form ("You Could Have Come Up With
+// in tensor memory.  Every contraction of the chunk form ("You Could Have Come Up With
 // Kimi Delta Attention", sec. 6.3-6.5; "From Attention to Learned Memory",
 // sec. 4, WY/UT transform and the 16x16 blocked inverse) runs as a tcgen05 MMA
 // with fp32 accumulators in tensor memory:
@@ -64,7 +64,7 @@ constexpr int GS = D + 4;    // G rows: fp32, 528 B
 constexpr uint32_t S_K = 0;                     // k staging bf16 [64][KS]
 constexpr uint32_t S_Q = S_K + C * KS * 2;      // q staging bf16 [64][KS]
 constexpr uint32_t S_V = S_Q + C * KS * 2;      // v staging bf16 [64][VS]
-constexpr uint32_t S_G = S_V + C * VS * 2;      // per-channel log-decay -> G, fp32 [64][GS]
+constexpr uint32_t S_G = S_V + C * VS * 2;      // per-channel log-decay -> exp(G - G_a), fp32 [64][GS]
 constexpr uint32_t S_GS = S_G + C * GS * 4;     // scalar log-decay -> G [64]
 constexpr uint32_t S_BETA = S_GS + 256;         // beta [64]
 constexpr uint32_t S_RK = S_BETA + 256;         // 1/|k| [64]
@@ -72,13 +72,15 @@ constexpr uint32_t S_RQ = S_RK + 256;           // scale/|q| [64]
 constexpr uint32_t S_EG = S_RQ + 256;           // scalar: exp(G_i) [64]
 constexpr uint32_t S_EGL = S_EG + 256;          // scalar: exp(G_last - G_i) [64]
 constexpr uint32_t S_GAM = S_EGL + 256;         // exp(G_last) [128]
-constexpr uint32_t S_GA = S_GAM + 512;          // anchor G_a [128]
+constexpr uint32_t S_GA = S_GAM + 512;          // exp(G_a) at the anchor [128]
 constexpr uint32_t R1 = (S_GA + 512 + 1023) & ~1023u;
 //   A-GEMM operands, then the chain's first operands
 constexpr uint32_t AK = R1;                    // [K+; Q+] 128 x 128 (16-bit)
 constexpr uint32_t BK = AK + 128 * 128 * 2;    // K- 64 x 128
 constexpr uint32_t A1 = R1;                    // [TB; A_qk TB] 128 x 64 fp16
 constexpr uint32_t A2 = A1 + 128 * 64 * 2;     // [-W; Q~ - A_qk W] 128 x 128 fp16
+constexpr uint32_t OST = R1;                   // o rows staged for coalesced stores, fp32 [64][OS]
+constexpr int OS = BV + 4;                     // padded row (272 B)
 constexpr uint32_t R2 = BK + 64 * 128 * 2;
 //   triangular solve, then K~^T and K_end^T
 constexpr int SP = 68;                         // padded, 16-byte aligned row of the fp32 solve tiles
@@ -100,6 +102,7 @@ constexpr uint32_t ET_SBO = (C / 8) * LBO_P;
 constexpr uint32_t SMEM_BYTES = ET + (BV / 8) * ET_SBO;
 static_assert(KET + 128 * 64 * 2 <= R3, "K~/K_end alias the solve area");
 static_assert(A2 + 128 * 128 * 2 <= R2, "A1/A2 alias the A-GEMM operands");
+static_assert(OST + C * OS * 4 <= R2, "o staging aliases the consumed chain operands");
 static_assert(SMEM_BYTES + 64 <= 227 * 1024, "shared memory budget");
 // per-channel decay: low bf16 halves of K- (A-GEMM B operand) live in the TB^T and V^T
 // buffers, which are dead between a chunk's chain MMA and the next chunk's solve
@@ -108,7 +111,7 @@ static_assert(VT == TBT + 64 * 64 * 2, "K- low half spans TB^T and V^T");
 
 // TMEM columns
 constexpr uint32_t T_A = 0, T_X = 64, T_Y = 128, T_D1 = 256, T_D2 = 320, T_ALO = 384,
-                   T_COLS = 512;
+                   T_S = 448, T_COLS = 512;
 
 // dense K-major tiles: lbo 128, sbo = (K / 8) * 128
 __host__ __device__ constexpr uint32_t dense_sbo(uint32_t K) { return (K / 8) * 128; }
@@ -246,23 +249,41 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   const int chalf = warp >> 2;                      // 0 or 1
   const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
 
-  // the fp32 master state: row `row` (key channel), value columns [32*chalf, +32)
-  float S[32];
-  {
-    const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
-    for (int j = 0; j < 32; ++j)
-      S[j] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[base + j])
-                   : static_cast<const float*>(P.pool)[base + j];
-  }
-  auto write_state_operand = [&]() {
-    // S^T (N = value column j, K = key channel `row`), fp16, padded layout
+  // the fp32 master state lives in tensor memory (lane = key channel `row`, columns
+  // T_S + value column), so it costs no registers between chunk steps; its fp16 copy
+  // S^T (N = value column j, K = key channel) is the chain MMA's B operand
+  auto write_state_operand = [&](const float* Sv) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       const int jj = 32 * chalf + j;
-      *reinterpret_cast<uint16_t*>(smem + ST + tc::cm_offset(jj, row, LBO_P, ST_SBO)) = f16_bits(S[j]);
+      *reinterpret_cast<uint16_t*>(smem + ST + tc::cm_offset(jj, row, LBO_P, ST_SBO)) = f16_bits(Sv[j]);
     }
   };
-  write_state_operand();
+  {
+    const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
+    float Sv[32];
+    uint32_t s0[16], s1[16];
+    for (int j = 0; j < 32; ++j) {
+      Sv[j] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[base + j])
+                    : static_cast<const float*>(P.pool)[base + j];
+      if (j < 16) s0[j] = __float_as_uint(Sv[j]); else s1[j - 16] = __float_as_uint(Sv[j]);
+    }
+    tc::tmem_st16(tmem + lane_addr + T_S + 32 * chalf, s0);
+    tc::tmem_st16(tmem + lane_addr + T_S + 32 * chalf + 16, s1);
+    tc::tmem_wait_st();
+    write_state_operand(Sv);
+  }
+
+  // the identity rows of L = [I; A_qk] never change
+  if (row < C) {
+    float idv[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) idv[e] = (32 * chalf + e == row) ? 1.f : 0.f;
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8)
+      f16x8_store(smem, LMAT + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, dense_sbo(64)),
+                  idv + 8 * g8);
+  }
 
   auto mma_wait = [&]() -> bool {
     const bool ok = tc::mbar_wait_bounded(&s_bar, phase & 1, kWaitLimit);
@@ -305,8 +326,10 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       }
     }
     if (PERCH) {
-      if (tid < D) {                                    // channel tid: inclusive cumsum
-        float acc = 0.f;
+      if (tid < D) {
+        // channel tid: inclusive cumsum G, then E' = exp(G - G_a) in place, with the anchor
+        // G_a at the chunk's middle token; exp(G_a) and exp(G_last) go to small arrays
+        float acc = 0.f, gmin = 0.f, gmax = -3.0e38f;
 #pragma unroll
         for (int i0 = 0; i0 < C; i0 += 16) {
           float gv[16];
@@ -315,11 +338,23 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             acc += gv[e];
+            gmin = fminf(gmin, acc);
+            gmax = fmaxf(gmax, acc);
             sG[(i0 + e) * GS + tid] = acc;
           }
         }
+        const float ga = sG[((n - 1) / 2) * GS + tid];
+        if (fmaxf(gmax - ga, ga - gmin) > kMaxHalfChunkDecay) s_range = 1;
+#pragma unroll
+        for (int i0 = 0; i0 < C; i0 += 16) {
+          float gv[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) gv[e] = sG[(i0 + e) * GS + tid];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) sG[(i0 + e) * GS + tid] = __expf(gv[e] - ga);
+        }
         sGam[tid] = __expf(acc);
-        sGA[tid] = sG[((n - 1) / 2) * GS + tid];
+        sGA[tid] = __expf(ga);
       }
     } else if (warp == 0) {                             // scalar: warp scan of 64 values
       const float g0 = sGs[2 * lane], g1 = sGs[2 * lane + 1];
@@ -366,17 +401,13 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
           const int cc = 64 * chalf + 8 * g8;
           float x[8];
           bf16x8_load(smem + src + cc * 2, x);
-          const float4 g0 = *reinterpret_cast<const float4*>(sG + i * GS + cc);
+          const float4 g0 = *reinterpret_cast<const float4*>(sG + i * GS + cc);   // E'
           const float4 g1 = *reinterpret_cast<const float4*>(sG + i * GS + cc + 4);
-          const float4 a0 = *reinterpret_cast<const float4*>(sGA + cc);
-          const float4 a1 = *reinterpret_cast<const float4*>(sGA + cc + 4);
-          const float gd[8] = {g0.x - a0.x, g0.y - a0.y, g0.z - a0.z, g0.w - a0.w,
-                               g1.x - a1.x, g1.y - a1.y, g1.z - a1.z, g1.w - a1.w};
+          const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
           uint32_t hi[4];
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
-            if (fabsf(gd[e]) > kMaxHalfChunkDecay || fabsf(gd[e + 1]) > kMaxHalfChunkDecay) s_range = 1;
-            const float v0 = x[e] * rs * __expf(gd[e]), v1 = x[e + 1] * rs * __expf(gd[e + 1]);
+            const float v0 = x[e] * rs * f[e], v1 = x[e + 1] * rs * f[e + 1];
             hi[e / 2] = tc::pack_bf16x2(v0, v1);
             const float h0 = __uint_as_float(hi[e / 2] << 16);
             const float h1 = __uint_as_float(hi[e / 2] & 0xffff0000u);
@@ -403,16 +434,13 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
           const int cc = 32 * qq + 8 * g8;
           float x[8];
           bf16x8_load(smem + S_K + (j * KS + cc) * 2, x);
-          const float4 g0 = *reinterpret_cast<const float4*>(sG + j * GS + cc);
+          const float4 g0 = *reinterpret_cast<const float4*>(sG + j * GS + cc);   // E'
           const float4 g1 = *reinterpret_cast<const float4*>(sG + j * GS + cc + 4);
-          const float4 a0 = *reinterpret_cast<const float4*>(sGA + cc);
-          const float4 a1 = *reinterpret_cast<const float4*>(sGA + cc + 4);
-          const float gd[8] = {a0.x - g0.x, a0.y - g0.y, a0.z - g0.z, a0.w - g0.w,
-                               a1.x - g1.x, a1.y - g1.y, a1.z - g1.z, a1.w - g1.w};
+          const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
           uint32_t hi[4], lo[4];
 #pragma unroll
           for (int e = 0; e < 8; e += 2) {
-            const float v0 = x[e] * rs * __expf(gd[e]), v1 = x[e + 1] * rs * __expf(gd[e + 1]);
+            const float v0 = x[e] * rs * __fdividef(1.f, f[e]), v1 = x[e + 1] * rs * __fdividef(1.f, f[e + 1]);
             hi[e / 2] = tc::pack_bf16x2(v0, v1);
             const float h0 = __uint_as_float(hi[e / 2] << 16);
             const float h1 = __uint_as_float(hi[e / 2] & 0xffff0000u);
@@ -449,7 +477,6 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       }
       tc::mma_commit(&s_bar);
     }
-    for (int idx = tid; idx < C * SP; idx += NT) sT[idx] = 0.f;
     mma_wait();
 
     // ---------------------------------------------------------------- phase 3: A_kk, A_qk
@@ -478,14 +505,6 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
         for (int e = 0; e < 32; e += 4)
           *reinterpret_cast<float4*>(sA + i * SP + 32 * chalf + e) =
               make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-        // identity rows of L = [I; A_qk]
-        float idv[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) idv[e] = (32 * chalf + e == i) ? 1.f : 0.f;
-#pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8)
-          f16x8_store(smem, LMAT + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, dense_sbo(64)),
-                      idv + 8 * g8);
       } else {
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8)
@@ -496,6 +515,11 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     __syncthreads();
 
     // ---------------------------------------------------------------- phase 4: solve
+    // the 32x32 merge reads the strictly-upper 16x16 blocks of T11 and T22: zero them
+    for (int idx = tid; idx < 2 * 256; idx += NT) {
+      const int blk = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
+      sT[(32 * blk + r) * SP + 32 * blk + 16 + c] = 0.f;
+    }
     // diagonal 16x16 blocks: lane (block, column) keeps its column of the block's inverse
     // in registers and substitutes row by row
     if (warp < 2) {
@@ -517,12 +541,19 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     if (tid < 128) {                                      // X = A21 T11, two 16x16 pairs
       const int p = tid >> 6, r = (tid >> 2) & 15, c = (tid & 3) * 4;
       const int r0 = 32 * p + 16, c0 = 32 * p;
+      float a[16];
+#pragma unroll
+      for (int m = 0; m < 16; m += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(sA + (r0 + r) * SP + c0 + m);
+        a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
+      }
+      float4 t[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) t[m] = *reinterpret_cast<const float4*>(sT + (c0 + m) * SP + c0 + c);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
-        const float a = sA[(r0 + r) * SP + c0 + m];
-        const float4 t = *reinterpret_cast<const float4*>(sT + (c0 + m) * SP + c0 + c);
-        acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
+        acc.x += a[m] * t[m].x; acc.y += a[m] * t[m].y; acc.z += a[m] * t[m].z; acc.w += a[m] * t[m].w;
       }
       *reinterpret_cast<float4*>(sX + (16 * p + r) * XP + c) = acc;
     }
@@ -530,12 +561,19 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     if (tid < 128) {                                      // T21 = -T22 X
       const int p = tid >> 6, r = (tid >> 2) & 15, c = (tid & 3) * 4;
       const int r0 = 32 * p + 16, c0 = 32 * p;
+      float a[16];
+#pragma unroll
+      for (int m = 0; m < 16; m += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(sT + (r0 + r) * SP + r0 + m);
+        a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
+      }
+      float4 x[16];
+#pragma unroll
+      for (int m = 0; m < 16; ++m) x[m] = *reinterpret_cast<const float4*>(sX + (16 * p + m) * XP + c);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int m = 0; m < 16; ++m) {
-        const float a = sT[(r0 + r) * SP + r0 + m];
-        const float4 x = *reinterpret_cast<const float4*>(sX + (16 * p + m) * XP + c);
-        acc.x += a * x.x; acc.y += a * x.y; acc.z += a * x.z; acc.w += a * x.w;
+        acc.x += a[m] * x[m].x; acc.y += a[m] * x[m].y; acc.z += a[m] * x[m].z; acc.w += a[m] * x[m].w;
       }
       *reinterpret_cast<float4*>(sT + (r0 + r) * SP + c0 + c) =
           make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
@@ -543,24 +581,46 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     __syncthreads();
     {                                                     // X = A21 T11, one 32x32 pair
       const int r = tid >> 3, c = (tid & 7) * 4;
+      float a[32];                                        // row r of A21, loaded up front
+#pragma unroll
+      for (int m = 0; m < 32; m += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(sA + (32 + r) * SP + m);
+        a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
+      }
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int m = 0; m < 32; ++m) {
-        const float a = sA[(32 + r) * SP + m];
-        const float4 t = *reinterpret_cast<const float4*>(sT + m * SP + c);
-        acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
+      for (int m0 = 0; m0 < 32; m0 += 8) {
+        float4 t[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = *reinterpret_cast<const float4*>(sT + (m0 + e) * SP + c);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float av = a[m0 + e];
+          acc.x += av * t[e].x; acc.y += av * t[e].y; acc.z += av * t[e].z; acc.w += av * t[e].w;
+        }
       }
       *reinterpret_cast<float4*>(sX + r * XP + c) = acc;
     }
     __syncthreads();
     {                                                     // T21 = -T22 X
       const int r = tid >> 3, c = (tid & 7) * 4;
+      float a[32];
+#pragma unroll
+      for (int m = 0; m < 32; m += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(sT + (32 + r) * SP + 32 + m);
+        a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
+      }
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int m = 0; m < 32; ++m) {
-        const float a = sT[(32 + r) * SP + 32 + m];
-        const float4 x = *reinterpret_cast<const float4*>(sX + m * XP + c);
-        acc.x += a * x.x; acc.y += a * x.y; acc.z += a * x.z; acc.w += a * x.w;
+      for (int m0 = 0; m0 < 32; m0 += 8) {
+        float4 x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = *reinterpret_cast<const float4*>(sX + (m0 + e) * XP + c);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float av = a[m0 + e];
+          acc.x += av * x[e].x; acc.y += av * x[e].y; acc.z += av * x[e].z; acc.w += av * x[e].w;
+        }
       }
       *reinterpret_cast<float4*>(sT + (32 + r) * SP + c) =
           make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
@@ -572,7 +632,10 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       const float bj = sBeta[j];
       float x[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = sT[(m8 * 8 + e) * SP + j] * bj;
+      for (int e = 0; e < 8; ++e) {                      // T is lower triangular
+        const int m = m8 * 8 + e;
+        x[e] = m >= j ? sT[m * SP + j] * bj : 0.f;
+      }
       f16x8_store(smem, TBT + tc::cm_offset(j, m8 * 8, 128, dense_sbo(64)), x);
     }
     tc::fence_async_smem();
@@ -595,14 +658,14 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       const int c = u % D, m8 = u / D;
       float kt[8], ke[8];
       if (PERCH) {
-        const float Gl = sG[(C - 1) * GS + c];
+        const float El = sG[(C - 1) * GS + c], ea = sGA[c];   // E'_last, exp(G_a)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int m = m8 * 8 + e;
-          const float Gm = sG[m * GS + c];
+          const float Em = sG[m * GS + c];
           const float kx = bf16_at(smem, S_K, m * KS + c) * sRK[m];
-          kt[e] = kx * __expf(Gm);
-          ke[e] = kx * __expf(Gl - Gm);
+          kt[e] = kx * Em * ea;                              // k^ exp(G_m)
+          ke[e] = kx * __fdividef(El, Em);                   // k^ exp(G_last - G_m)
         }
       } else {
 #pragma unroll
@@ -661,13 +724,22 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     mma_wait();
 
     // ---------------------------------------------------------------- phase 9: A2
+    uint32_t ry[2][32];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t a[16], b[16];
+      tc::tmem_ld16(tmem + lane_addr + T_Y + 64 * chalf + 32 * half, a);
+      tc::tmem_ld16(tmem + lane_addr + T_Y + 64 * chalf + 32 * half + 16, b);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        ry[half][e] = a[e];
+        ry[half][e + 16] = b[e];
+      }
+    }
+    tc::tmem_wait_ld();
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int c0 = 64 * chalf + 32 * half;
-      uint32_t r0[16], r1[16];
-      tc::tmem_ld16(tmem + lane_addr + T_Y + c0, r0);
-      tc::tmem_ld16(tmem + lane_addr + T_Y + c0 + 16, r1);
-      tc::tmem_wait_ld();
       float x[32];
       if (row >= C) {                                     // Q~ = q scale/|q| exp(G)
         const int i = row - C;
@@ -679,9 +751,12 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
           if (PERCH) {
             const float4 ga = *reinterpret_cast<const float4*>(sG + i * GS + c0 + 8 * g8);
             const float4 gb = *reinterpret_cast<const float4*>(sG + i * GS + c0 + 8 * g8 + 4);
-            const float gv[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+            const float4 aa = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8);
+            const float4 ab = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8 + 4);
+            const float gv[8] = {ga.x * aa.x, ga.y * aa.y, ga.z * aa.z, ga.w * aa.w,
+                                 gb.x * ab.x, gb.y * ab.y, gb.z * ab.z, gb.w * ab.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * rq * __expf(gv[e]);
+            for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * rq * gv[e];   // exp(G_i)
           } else {
             const float f = rq * sEG[i];
 #pragma unroll
@@ -693,7 +768,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
         for (int e = 0; e < 32; ++e) x[e] = 0.f;
       }
 #pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] -= __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
+      for (int e = 0; e < 32; ++e) x[e] -= __uint_as_float(ry[half][e]);
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8)
         f16x8_store(smem, A2 + tc::cm_offset(row, c0 + 8 * g8, 128, dense_sbo(D)), x + 8 * g8);
@@ -735,8 +810,10 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
           *reinterpret_cast<uint16_t*>(smem + ET + tc::cm_offset(32 * chalf + e, row, LBO_P, ET_SBO)) =
               f16_bits(ev);
         }
-      } else if (row - C < n) {
-        float* op = P.o + ((t0 + row - C) * HV + h) * D + vt * BV + 32 * chalf;
+      } else {
+        // o rows go through shared memory (the chain operands there are consumed) so
+        // that the global stores below are coalesced
+        float* op = reinterpret_cast<float*>(smem + OST) + (row - C) * OS + 32 * chalf;
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
           *reinterpret_cast<float4*>(op + e) =
@@ -752,6 +829,14 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
+    // coalesced o stores: each warp instruction writes two whole 256-byte token rows
+#pragma unroll
+    for (int k = 0; k < (C * BV / 4) / NT; ++k) {
+      const int idx = tid + k * NT, i = idx / (BV / 4), q = idx % (BV / 4);
+      if (i < n)
+        *reinterpret_cast<float4*>(P.o + ((t0 + i) * HV + h) * D + vt * BV + q * 4) =
+            *reinterpret_cast<const float4*>(smem + OST + (i * OS + q * 4) * 4);
+    }
 
     // ---------------------------------------------------------------- phase 12: dS
     if (tid == 0) {
@@ -767,15 +852,25 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
 
     // ---------------------------------------------------------------- phase 13: S update
     {
-      uint32_t r0[16], r1[16];
+      uint32_t r0[16], r1[16], s0[16], s1[16];
       tc::tmem_ld16(tmem + lane_addr + T_D2 + 32 * chalf, r0);
       tc::tmem_ld16(tmem + lane_addr + T_D2 + 32 * chalf + 16, r1);
+      tc::tmem_ld16(tmem + lane_addr + T_S + 32 * chalf, s0);
+      tc::tmem_ld16(tmem + lane_addr + T_S + 32 * chalf + 16, s1);
       tc::tmem_wait_ld();
       const float gam = sGam[row];
+      float Sv[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e)
-        S[e] = gam * S[e] + __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
-      write_state_operand();
+      for (int e = 0; e < 16; ++e) {
+        Sv[e] = gam * __uint_as_float(s0[e]) + __uint_as_float(r0[e]);
+        Sv[e + 16] = gam * __uint_as_float(s1[e]) + __uint_as_float(r1[e]);
+        s0[e] = __float_as_uint(Sv[e]);
+        s1[e] = __float_as_uint(Sv[e + 16]);
+      }
+      tc::tmem_st16(tmem + lane_addr + T_S + 32 * chalf, s0);
+      tc::tmem_st16(tmem + lane_addr + T_S + 32 * chalf + 16, s1);
+      tc::tmem_wait_st();
+      write_state_operand(Sv);
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -792,11 +887,16 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
   } else {
     const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
+    uint32_t s0[16], s1[16];
+    tc::tmem_ld16(tmem + lane_addr + T_S + 32 * chalf, s0);
+    tc::tmem_ld16(tmem + lane_addr + T_S + 32 * chalf + 16, s1);
+    tc::tmem_wait_ld();
     for (int j = 0; j < 32; ++j) {
+      const float v = __uint_as_float(j < 16 ? s0[j] : s1[j - 16]);
       if (SBF16)
-        static_cast<uint16_t*>(P.pool)[base + j] = f32_to_bf16_bits(S[j]);
+        static_cast<uint16_t*>(P.pool)[base + j] = f32_to_bf16_bits(v);
       else
-        static_cast<float*>(P.pool)[base + j] = S[j];
+        static_cast<float*>(P.pool)[base + j] = v;
     }
   }
   tc::fence_before_sync();

@@ -73,7 +73,9 @@ constexpr uint32_t S_EG = S_RQ + 256;           // scalar: exp(G_i) [64]
 constexpr uint32_t S_EGL = S_EG + 256;          // scalar: exp(G_last - G_i) [64]
 constexpr uint32_t S_GAM = S_EGL + 256;         // exp(G_last) [128]
 constexpr uint32_t S_GA = S_GAM + 512;          // exp(G_a) at the anchor [128]
-constexpr uint32_t R1 = (S_GA + 512 + 1023) & ~1023u;
+constexpr uint32_t S_EA = S_GA + 512;           // scalar: exp(G_i - G_a) [64]
+constexpr uint32_t S_KF = S_EA + 256;           // scalar: exp(G_a - G_j) / |k_j| [64]
+constexpr uint32_t R1 = (S_KF + 256 + 1023) & ~1023u;
 //   A-GEMM operands, then the chain's first operands
 constexpr uint32_t AK = R1;                    // [K+; Q+] 128 x 128 (16-bit)
 constexpr uint32_t BK = AK + 128 * 128 * 2;    // K- 64 x 128
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_range;
+  __shared__ int s_anchored;     // scalar decay: anchored per-token factors are in range
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (plan.info[1] == 0) return;
@@ -217,6 +220,8 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   float* sEGL = reinterpret_cast<float*>(smem + S_EGL);
   float* sGam = reinterpret_cast<float*>(smem + S_GAM);
   float* sGA = reinterpret_cast<float*>(smem + S_GA);
+  float* sEA = reinterpret_cast<float*>(smem + S_EA);
+  float* sKF = reinterpret_cast<float*>(smem + S_KF);
   float* sA = reinterpret_cast<float*>(smem + SOL_A);
   float* sT = reinterpret_cast<float*>(smem + SOL_T);
   float* sX = reinterpret_cast<float*>(smem + SOL_X);
@@ -373,8 +378,20 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       sEGL[2 * lane + 1] = __expf(gl - s);
       const float gam = __expf(gl);
       sGam[lane] = gam; sGam[lane + 32] = gam; sGam[lane + 64] = gam; sGam[lane + 96] = gam;
+      // anchored factors exp(G_i - G_a), exp(G_a - G_j) with the anchor mid-chunk, so that
+      // exp(G_i - G_j) = product of two per-token values (used while both stay finite)
+      const int am = (n - 1) / 2;
+      const float ga = __shfl_sync(0xffffffffu, (am & 1) ? s : s - g1, am >> 1);
+      const float d0 = (s - g1) - ga, d1 = s - ga;
+      const bool ok = __all_sync(0xffffffffu, fmaxf(fabsf(d0), fabsf(d1)) <= kMaxHalfChunkDecay);
+      sEA[2 * lane] = __expf(d0);
+      sEA[2 * lane + 1] = __expf(d1);
+      sKF[2 * lane] = __expf(-d0);
+      sKF[2 * lane + 1] = __expf(-d1);
+      if (lane == 0) s_anchored = ok ? 1 : 0;
     }
     __syncthreads();
+    if (!PERCH && tid < C) sKF[tid] *= sRK[tid];
     // A-GEMM operands: [K+; Q+] (rows 0-63 keys, 64-127 queries) and K-.
     if (!PERCH) {
       // raw bf16 rows; consecutive threads fill one core matrix (8 rows x 16 B) at a time
@@ -491,14 +508,32 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
       // here; per-channel decay multiplied normalised, decayed rows already
       const float ri = is_k ? (PERCH ? 1.f : sRK[i]) * sBeta[i] : (PERCH ? 1.f : sRQ[i]);
       float x[32];
+      if (PERCH) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * ri;
+      } else if (s_anchored) {                        // exp(G_i - G_j) = E_i F_j (anchored)
+        const float rie = ri * sEA[i];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 kf = *reinterpret_cast<const float4*>(sKF + 32 * chalf + e);
+          x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * rie * kf.x;
+          x[e + 1] = __uint_as_float(e + 1 < 16 ? r0[e + 1] : r1[e - 15]) * rie * kf.y;
+          x[e + 2] = __uint_as_float(e + 2 < 16 ? r0[e + 2] : r1[e - 14]) * rie * kf.z;
+          x[e + 3] = __uint_as_float(e + 3 < 16 ? r0[e + 3] : r1[e - 13]) * rie * kf.w;
+        }
+      } else {                                        // exact per pair for extreme decays
+        const float gi = sGs[i];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j = 32 * chalf + e;
+          x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * ri * sRK[j] * __expf(gi - sGs[j]);
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int j = 32 * chalf + e;
-        const float raw = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
-        float a = raw * ri;
-        if (!PERCH) a *= sRK[j] * __expf(sGs[i] - sGs[j]);
         const bool keep = is_k ? (j < i) : (j <= i);
-        x[e] = keep ? a : 0.f;
+        x[e] = keep ? x[e] : 0.f;
       }
       if (is_k) {
 #pragma unroll

@@ -310,3 +310,13 @@ def test_stronger_decay_stays_accurate_on_tensor_cores(factor):
     p = small("mid-decay", [200, 77], 1, 2, 128, "bf16", "f32", "per_channel", 64, seed=52)
     p.g[:] = (p.g * factor).astype(np.float32)
     check_prefill(p)
+
+
+@pytest.mark.parametrize("factor", [1.0, 6.0])
+def test_scalar_decay_anchored_and_exact_pair_paths(factor):
+    """Scalar decay: at the workload's decay the A-matrix decays come from two anchored
+    per-token factors; at 6x (about -5 nats per token, beyond their fp32 range) the
+    kernel uses exp(G_i - G_j) per pair.  Both match the oracle."""
+    p = small("scalar-decay", [200, 64, 33], 2, 2, 128, "bf16", "f32", "scalar", 64, seed=53)
+    p.g[:] = (p.g * factor).astype(np.float32)
+    check_prefill(p)

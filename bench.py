@@ -6,7 +6,8 @@ Headline workload: Gated DeltaNet prefill, 4 sequences x 4096 tokens, 16 heads, 
 bf16 q/k/v, scalar decay, fp32 state, chunk 64 ("gdn_prefill").  A step is one
 kda_prefill_fwd call over that batch (every stage of the prefill path); the metric is
 prefill tokens/s.  The decode step (256 sequences x 32 heads, per-channel decay) is
-measured in the same run and reported under "also" as decode steps/s.
+measured in the same run and reported under "also" as decode steps/s, and so is the
+speculative-decode verification (a 4-token window plus the fold of the accepted prefix).
 
 Multi-GPU: every rank runs an independent replica on its own batch (sequences never
 interact, so nothing is exchanged); value = all ranks' tokens / the slowest rank's time.
@@ -336,6 +337,73 @@ def time_decode(dp, dev, steps, warmup):
     return start.elapsed_time(end) / steps
 
 
+VERIFY_WINDOW = 4
+
+
+def verify_problem():
+    """Speculative-decode verification on the decode workload's shape: 256 sequences x
+    32 heads, d=128, bf16 q/k/v, per-channel decay, fp32 pool, a window of 4 draft tokens."""
+    return workloads.make_problem("kda_verify", num_seqs=256, lengths=[VERIFY_WINDOW] * 256,
+                                  num_k_heads=32, num_v_heads=32, d=128, qkv_dtype="bf16",
+                                  state_dtype="f32", decay_kind="per_channel", chunk=64,
+                                  zero_state=False, seed=2006)
+
+
+def verify_algorithmic_bytes(p, accepted_total: int) -> dict:
+    """Verify reads the state once and every window token's inputs, writes o and one
+    record per token; the fold reads and writes each touched state and reads the
+    accepted records."""
+    B, HK, HV, d, W = p.num_seqs, p.num_k_heads, p.num_v_heads, p.d_k, VERIFY_WINDOW
+    rec = 3 * d if p.decay_kind == "per_channel" else 2 * d + 4
+    st = 2 if p.state_dtype == "bf16" else 4
+    g = d if p.decay_kind == "per_channel" else 1
+    tok = B * W
+    verify = (B * HV * d * d * st + tok * (2 * HK * d * 2 + HV * d * 2 + HV * 4 + HV * g * 4
+                                           + HV * d * 4 + HV * rec * 4))
+    fold = 2 * B * HV * d * d * st + accepted_total * HV * rec * 4
+    return {"verify_window": float(verify), "fold_accepted": float(fold)}
+
+
+def time_verify(dev, steps, warmup):
+    import torch
+    import gated_delta_rule_deltanet_gb300 as kda
+    from workloads import torch_io
+    p = verify_problem()
+    t = torch_io.prefill_inputs(p, dev)
+    B, HV, d = p.num_seqs, p.num_v_heads, p.d_v
+    out = torch.empty((B * VERIFY_WINDOW, HV, d), dtype=torch.float32, device=dev)
+    acc_host = np.arange(B, dtype=np.int32) % (VERIFY_WINDOW + 1)   # 0..W accepted, mean W/2
+    acc = torch.tensor(acc_host, device=dev)
+    ring = None
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+
+    def step(e=None):
+        nonlocal ring
+        if e:
+            e[0].record()
+        _, ring = kda.verify_window(t["q"], t["k"], t["v"], t["beta"], t["log_decay"],
+                                    t["slot_idx"], t["state_pool"], window=VERIFY_WINDOW,
+                                    out=out, ring=ring)
+        if e:
+            e[1].record()
+        kda.fold_accepted(ring, acc, t["slot_idx"], t["state_pool"], window=VERIFY_WINDOW)
+        if e:
+            e[2].record()
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    for s in range(steps):
+        step(ev[s])
+    torch.cuda.synchronize()
+    if kda.get_device_error() != 0:
+        raise RuntimeError("verify/fold raised a device error")
+    ms_v = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    ms_f = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    total = sum(e[0].elapsed_time(e[2]) for e in ev) / steps
+    return p, total, {"verify_window": ms_v, "fold_accepted": ms_f}, int(acc_host.sum())
+
+
 def ours_arm(args, rank, world, local):
     import torch
     import gated_delta_rule_deltanet_gb300 as kda
@@ -390,6 +458,19 @@ def ours_arm(args, rank, world, local):
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": dbytes / (dms / 1e3) / 1e9 / peaks["hbm_gbs"],
                                   "traffic": None}})
+        vp, vms, vstage, vacc = time_verify(dev, max(args.steps, 20), max(args.warmup, 3))
+        vbytes = verify_algorithmic_bytes(vp, vacc)
+        vval, _ = aggregate(float(vp.num_seqs * VERIFY_WINDOW), vms / 1e3, world, dev)
+        vk = max(vstage, key=vstage.get)
+        also.append({"workload": "kda_verify (256 seq x 32 heads, d=128, window 4, "
+                                 "accepted 0..4 per sequence)",
+                     "metric": "verified draft tokens/s", "value": vval, "unit": "tokens/s",
+                     "ms_per_step": vms, "stage_ms": vstage,
+                     "roofline": {"bound": "hbm", "kernel": vk,
+                                  "achieved": vbytes[vk] / (vstage[vk] / 1e3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": vbytes[vk] / (vstage[vk] / 1e3) / 1e9
+                                  / peaks["hbm_gbs"], "traffic": None}})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -27,12 +27,14 @@ KDA_DEVERR_SLOT_RANGE = 2
 KDA_DEVERR_SLOT_DUP = 3
 KDA_DEVERR_TIMEOUT = 4
 KDA_DEVERR_DECAY_RANGE = 5
+KDA_DEVERR_ACCEPTED = 6
 
 # every function include/kda.h declares
 EXPORTS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_size",
            "kda_prefill_fwd", "kda_decode_step", "kda_get_device_error",
            "kda_set_stage_events", "kda_prefill_fwd_no_alloc",
-           "kda_prefill_uses_tensor_cores")
+           "kda_prefill_uses_tensor_cores", "kda_ring_record_elems", "kda_verify_window",
+           "kda_fold_accepted")
 
 KDA_NO_ALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -102,6 +104,12 @@ def load():
         L.kda_decode_step.restype = ctypes.c_int
         L.kda_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_int32)]
         L.kda_get_device_error.restype = ctypes.c_int
+        L.kda_ring_record_elems.argtypes = [pp]
+        L.kda_ring_record_elems.restype = ctypes.c_int
+        L.kda_verify_window.argtypes = [pp, P, P, P, P, P, P, ctypes.c_int32, P, P, P, P]
+        L.kda_verify_window.restype = ctypes.c_int
+        L.kda_fold_accepted.argtypes = [pp, P, ctypes.c_int32, P, P, P, P]
+        L.kda_fold_accepted.restype = ctypes.c_int
         L.kda_prefill_uses_tensor_cores.argtypes = [pp]
         L.kda_prefill_uses_tensor_cores.restype = ctypes.c_int
         L.kda_prefill_fwd_no_alloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P]

@@ -19,6 +19,11 @@ bool tc_prefill_supported(const Problem& P, bool qbf16);
 size_t tc_workspace_bytes(const Problem& P);
 cudaError_t launch_prefill_tc(const Problem& P, void* workspace, bool perch, bool sbf16,
                               cudaStream_t stream, const Stages& st);
+int ring_record_elems(int D, bool perch);
+cudaError_t launch_verify(const Problem& P, int window, float* ring, bool qbf16, bool sbf16,
+                          bool perch, cudaStream_t stream);
+cudaError_t launch_fold(const Problem& P, int window, const float* ring, const uint32_t* accepted,
+                        bool sbf16, bool perch, cudaStream_t stream);
 }  // namespace kda
 
 using kda::Problem;
@@ -206,6 +211,63 @@ kda_status_t kda_decode_step(const kda_params_t* p, const void* q, const void* k
                                       p->state_dtype == KDA_DTYPE_BF16,
                                       p->decay_kind == KDA_DECAY_PER_CHANNEL,
                                       static_cast<cudaStream_t>(stream), st));
+}
+
+int kda_ring_record_elems(const kda_params_t* p) {
+  Problem P{};
+  if (check_common(p, &P) != KDA_OK) return -1;
+  return kda::ring_record_elems(P.D, p->decay_kind == KDA_DECAY_PER_CHANNEL);
+}
+
+kda_status_t kda_verify_window(const kda_params_t* p, const void* q, const void* k, const void* v,
+                               const float* beta, const float* log_decay, const uint32_t* slot_idx,
+                               int32_t window, const void* state_pool, float* o, float* ring,
+                               void* stream) {
+  Problem P{};
+  kda_status_t s = check_common(p, &P);
+  if (s != KDA_OK) return s;
+  if (window < 1 || window > 64) return KDA_ERR_INVALID_ARG;
+  if (p->num_seqs == 0) return KDA_OK;
+  if (static_cast<int64_t>(p->num_seqs) * p->num_v_heads > 0x7fffffffLL ||
+      static_cast<int64_t>(p->num_seqs) * window > 0x7fffffffLL)
+    return KDA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !beta || !log_decay || !slot_idx || !state_pool || !o || !ring)
+    return KDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(state_pool, 16) || !aligned(ring, 16) || !aligned(beta, 4) ||
+      !aligned(log_decay, 4) || !aligned(slot_idx, 4))
+    return KDA_ERR_INVALID_ARG;
+  P.T = static_cast<int64_t>(p->num_seqs) * window;
+  P.q = q; P.k = k; P.v = v; P.beta = beta; P.g = log_decay;
+  P.slot_idx = slot_idx; P.pool = const_cast<void*>(state_pool); P.o = o;
+  P.err = device_error_word();
+  if (!P.err) return KDA_ERR_CUDA;
+  return to_status(kda::launch_verify(P, window, ring, p->qkv_dtype == KDA_DTYPE_BF16,
+                                      p->state_dtype == KDA_DTYPE_BF16,
+                                      p->decay_kind == KDA_DECAY_PER_CHANNEL,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+kda_status_t kda_fold_accepted(const kda_params_t* p, const float* ring, int32_t window,
+                               const uint32_t* accepted, const uint32_t* slot_idx,
+                               void* state_pool, void* stream) {
+  Problem P{};
+  kda_status_t s = check_common(p, &P);
+  if (s != KDA_OK) return s;
+  if (window < 1 || window > 64) return KDA_ERR_INVALID_ARG;
+  if (p->num_seqs == 0) return KDA_OK;
+  if (static_cast<int64_t>(p->num_seqs) * p->num_v_heads > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+  if (!ring || !accepted || !slot_idx || !state_pool) return KDA_ERR_INVALID_ARG;
+  if (!aligned(ring, 16) || !aligned(state_pool, 16) || !aligned(accepted, 4) ||
+      !aligned(slot_idx, 4))
+    return KDA_ERR_INVALID_ARG;
+  P.slot_idx = slot_idx;
+  P.pool = state_pool;
+  P.err = device_error_word();
+  if (!P.err) return KDA_ERR_CUDA;
+  return to_status(kda::launch_fold(P, window, ring, accepted, p->state_dtype == KDA_DTYPE_BF16,
+                                    p->decay_kind == KDA_DECAY_PER_CHANNEL,
+                                    static_cast<cudaStream_t>(stream)));
 }
 
 kda_status_t kda_get_device_error(void* stream, int32_t* code) {

@@ -246,3 +246,91 @@ def set_stage_events(events) -> None:
     st = _lib.load().kda_set_stage_events(handles if events else None, len(events))
     if st != _lib.KDA_OK:
         raise KdaError(st, "kda_set_stage_events")
+
+
+def ring_record_elems(params: KdaParams) -> int:
+    n = _lib.load().kda_ring_record_elems(ctypes.byref(params))
+    if n < 0:
+        raise KdaError(_lib.KDA_ERR_INVALID_ARG, "kda_ring_record_elems")
+    return n
+
+
+def _window_params(q, k, v, beta, log_decay, slot_idx, state_pool, window, scale, l2norm):
+    if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[0] != q.shape[0]:
+        raise ValueError("q, k must be [B*window, HK, D] and v [B*window, HV, D]")
+    BW, HK, D = q.shape
+    HV = v.shape[1]
+    if window < 1 or BW % window != 0:
+        raise ValueError("the token dimension must be B * window")
+    B = BW // window
+    if q.dtype not in _QKV_DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype: float32 or bfloat16")
+    if beta.dtype != torch.float32 or tuple(beta.shape) != (BW, HV) or not beta.is_contiguous():
+        raise ValueError("beta must be contiguous float32 [B*window, HV]")
+    if tuple(log_decay.shape) == (BW, HV):
+        per_channel = False
+    elif tuple(log_decay.shape) == (BW, HV, D):
+        per_channel = True
+    else:
+        raise ValueError("log_decay must be [B*window, HV] or [B*window, HV, D]")
+    if log_decay.dtype != torch.float32 or not log_decay.is_contiguous():
+        raise ValueError("log_decay must be contiguous float32")
+    if slot_idx.dtype not in _INDEX_DTYPES or slot_idx.numel() != B or not slot_idx.is_contiguous():
+        raise ValueError("slot_idx must be contiguous int32/uint32 [B]")
+    if (state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (HV, D, D)
+            or state_pool.dtype not in _QKV_DTYPES or not state_pool.is_contiguous()):
+        raise ValueError("state_pool must be contiguous [num_slots, HV, D, D]")
+    return make_params(num_seqs=B, num_k_heads=HK, num_v_heads=HV, d=D,
+                       num_slots=state_pool.shape[0], qkv_dtype=q.dtype,
+                       state_dtype=state_pool.dtype, per_channel=per_channel, scale=scale,
+                       l2norm=l2norm, q_row_stride=_row_stride(q, "q"),
+                       k_row_stride=_row_stride(k, "k"), v_row_stride=_row_stride(v, "v"))
+
+
+def verify_window(q, k, v, beta, log_decay, slot_idx, state_pool, *, window: int,
+                  scale: float = 0.0, l2norm: bool = True, out=None, ring=None, stream=None):
+    """kda_verify_window: `window` draft tokens per sequence from its pool slot, pool untouched.
+
+    Token t of sequence b is row b*window + t.  Returns (o [B*window, HV, D] fp32,
+    ring [B, window, HV, R] fp32) where R = ring_record_elems.
+    """
+    dev = _check_cuda(q, k, v, beta, log_decay, slot_idx, state_pool)
+    p = _window_params(q, k, v, beta, log_decay, slot_idx, state_pool, window, scale, l2norm)
+    BW, HV, D = v.shape
+    rec = ring_record_elems(p)
+    if out is None:
+        out = torch.empty((BW, HV, D), dtype=torch.float32, device=dev)
+    if ring is None:
+        ring = torch.empty((BW // window, window, HV, rec), dtype=torch.float32, device=dev)
+    elif (ring.dtype != torch.float32 or not ring.is_contiguous()
+          or ring.numel() != BW * HV * rec):
+        raise ValueError("ring must be contiguous float32 [B, window, HV, R]")
+    st = _lib.load().kda_verify_window(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                       _ptr(log_decay), _ptr(slot_idx), int(window),
+                                       _ptr(state_pool), _ptr(out), _ptr(ring),
+                                       _stream_handle(stream, dev))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_verify_window")
+    return out, ring
+
+
+def fold_accepted(ring, accepted, slot_idx, state_pool, *, window: int, num_k_heads: int = 1,
+                  per_channel: bool = True, stream=None):
+    """kda_fold_accepted: apply the first accepted[b] ring records of each sequence to its slot."""
+    dev = _check_cuda(ring, accepted, slot_idx, state_pool)
+    B = slot_idx.numel()
+    HV, D = state_pool.shape[1], state_pool.shape[2]
+    if accepted.dtype not in _INDEX_DTYPES or accepted.numel() != B or not accepted.is_contiguous():
+        raise ValueError("accepted must be contiguous int32/uint32 [B]")
+    p = make_params(num_seqs=B, num_k_heads=num_k_heads, num_v_heads=HV, d=D,
+                    num_slots=state_pool.shape[0], state_dtype=state_pool.dtype,
+                    per_channel=per_channel)
+    rec = ring_record_elems(p)
+    if ring.dtype != torch.float32 or not ring.is_contiguous() or ring.numel() != B * window * HV * rec:
+        raise ValueError("ring does not match [B, window, HV, R]")
+    st = _lib.load().kda_fold_accepted(ctypes.byref(p), _ptr(ring), int(window), _ptr(accepted),
+                                       _ptr(slot_idx), _ptr(state_pool),
+                                       _stream_handle(stream, dev))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_fold_accepted")
+    return state_pool

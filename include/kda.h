@@ -92,6 +92,7 @@ typedef enum kda_decay_kind {
 #define KDA_DEVERR_DECAY_RANGE 5 /* tensor-core path, per-channel decay: the cumulative log-decay
                                     over half a chunk exceeded 80 nats in some channel, so its
                                     anchored decay factors overflow; rerun with KDA_FLAG_CUDA_CORES */
+#define KDA_DEVERR_ACCEPTED 6    /* kda_fold_accepted: accepted[b] > window */
 
 typedef struct kda_params {
   int32_t num_seqs;    /* B: sequences in the ragged batch (prefill) or decode batch */
@@ -180,6 +181,51 @@ kda_status_t kda_prefill_fwd(const kda_params_t *p, const void *q, const void *k
 kda_status_t kda_decode_step(const kda_params_t *p, const void *q, const void *k, const void *v,
                              const float *beta, const float *log_decay, const uint32_t *slot_idx,
                              void *state_pool, float *o, void *stream);
+
+/*
+ * Speculative-decode verification (Modular MAX "gated_delta" module: the verify
+ * kernel runs the recurrence over a verify window and records a ring instead of
+ * writing the state back; the fold applies a verify's accepted records to the
+ * pool).  The module does not spell out a record; here one record is what a
+ * token's state update needs, so that folding it replays that update exactly:
+ *
+ *     record = [ k^ (d_k) | e (d_v) | alpha (d_k; for SCALAR decay one value
+ *                followed by 3 padding elements) ]   fp32
+ *     fold:    S <- S Diag(alpha) + e k^T     (the forget and write steps)
+ *
+ * kda_ring_record_elems returns the record length in fp32 elements
+ * (2 d_k + d_v, or d_k + d_v + 4), or -1 for invalid parameters.
+ */
+int kda_ring_record_elems(const kda_params_t *p);
+
+/*
+ * Runs `window` tokens of each of B = num_seqs sequences from its pool slot
+ * without modifying the pool: writes every token's output and ring record.
+ *   q, k        [B*window, HK, d_k]  (token t of sequence b is row b*window + t)
+ *   v           [B*window, HV, d_v]     beta [B*window, HV] fp32
+ *   log_decay   [B*window, HV] or [B*window, HV, d_k] fp32
+ *   slot_idx    [B] uint32              state_pool read only
+ *   o           [B*window, HV, d_v] fp32
+ *   ring        [B, window, HV, kda_ring_record_elems] fp32, 16-byte aligned
+ * window must be 1..64.  total_tokens and chunk are ignored.
+ */
+kda_status_t kda_verify_window(const kda_params_t *p, const void *q, const void *k, const void *v,
+                               const float *beta, const float *log_decay, const uint32_t *slot_idx,
+                               int32_t window, const void *state_pool, float *o, float *ring,
+                               void *stream);
+
+/*
+ * Applies the first accepted[b] records of sequence b's verify window to its
+ * pool slot, in token order (accepted[b] = 0 leaves the slot unchanged).  The
+ * result equals accepted[b] decode steps of those tokens from the same state.
+ *   ring       as written by kda_verify_window with the same p and window
+ *   accepted   [B] uint32, each <= window (larger values set KDA_DEVERR_ACCEPTED
+ *              on the device and leave that slot unchanged)
+ *   slot_idx   [B] uint32; state_pool updated in place
+ */
+kda_status_t kda_fold_accepted(const kda_params_t *p, const float *ring, int32_t window,
+                               const uint32_t *accepted, const uint32_t *slot_idx,
+                               void *state_pool, void *stream);
 
 /*
  * Waits for `stream`, then returns the device error word of the current device

@@ -146,3 +146,42 @@ def test_path_query(lib):
     assert not K.uses_tensor_cores(good(qkv_dtype=torch.float32))
     assert not K.uses_tensor_cores(good(d=16))
     assert lib.kda_prefill_uses_tensor_cores(None) == -1
+
+
+def test_ring_record_length(lib):
+    """Records are [k^ | e | alpha]; scalar decay pads its one alpha to 4 floats so every
+    record starts on a 16-byte boundary."""
+    pc = make_params(num_seqs=1, num_k_heads=1, num_v_heads=1, d=128, num_slots=1)
+    sc = make_params(num_seqs=1, num_k_heads=1, num_v_heads=1, d=128, num_slots=1,
+                         per_channel=False)
+    assert lib.kda_ring_record_elems(ctypes.byref(pc)) == 3 * 128
+    assert lib.kda_ring_record_elems(ctypes.byref(sc)) == 2 * 128 + 4
+    assert lib.kda_ring_record_elems(ctypes.byref(good(d=64))) == -1
+    assert lib.kda_ring_record_elems(None) == -1
+
+
+def test_verify_and_fold_reject_bad_arguments_before_launch(lib):
+    p = good()
+    a = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    args = [a] * 6
+    for w in (0, 65, -1):
+        assert lib.kda_verify_window(ctypes.byref(p), *args, w, a, a, a, None) == \
+            _lib.KDA_ERR_INVALID_ARG
+        assert lib.kda_fold_accepted(ctypes.byref(p), a, w, a, a, a, None) == \
+            _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_verify_window(ctypes.byref(p), *args, 4, a, a, None, None) == \
+        _lib.KDA_ERR_INVALID_ARG                                   # no ring
+    assert lib.kda_verify_window(ctypes.byref(p), *args, 4, a, a, odd, None) == \
+        _lib.KDA_ERR_INVALID_ARG                                   # ring not 16-byte aligned
+    assert lib.kda_fold_accepted(ctypes.byref(p), odd, 4, a, a, a, None) == \
+        _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_fold_accepted(ctypes.byref(p), a, 4, None, a, a, None) == \
+        _lib.KDA_ERR_INVALID_ARG                                   # no accepted counts
+    assert lib.kda_verify_window(ctypes.byref(good(d=64)), *args, 4, a, a, a, None) == \
+        _lib.KDA_ERR_UNSUPPORTED
+    empty = good(num_seqs=0)
+    assert lib.kda_verify_window(ctypes.byref(empty), *([None] * 6), 4, None, None, None,
+                                 None) == _lib.KDA_OK
+    assert lib.kda_fold_accepted(ctypes.byref(empty), None, 4, None, None, None, None) == \
+        _lib.KDA_OK

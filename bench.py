@@ -59,6 +59,17 @@ def decode_algorithmic_bytes(dp) -> dict:
                 g=g_elems * 4, o=B * HV * d * 4, state=2 * B * HV * d * d * st)
 
 
+def tc_executed_flops(p) -> dict:
+    """Tensor-core FLOPs the two tensor-core kernels issue per launch (d = 128, C = 64):
+    front per (chunk, value head) the A-GEMM (three passes for per-channel decay), X and Y;
+    chain per chunk and value tile of 64 columns [E; O] (K = 192) and K_end^T E."""
+    chunks = sum((int(n) + 63) // 64 for n in p.lengths) * p.num_v_heads
+    agemm = 2 * 128 * 64 * 128 * (3 if p.decay_kind == "per_channel" else 1)
+    front = agemm + 2 * 128 * 64 * 64 + 2 * 128 * 128 * 64
+    chain = 2 * (2 * 128 * 64 * 192 + 2 * 128 * 64 * 64)
+    return {"tc_front": float(front * chunks), "tc_chain": float(chain * chunks)}
+
+
 def prefill_flops(p) -> float:
     """Chunk-form multiply-adds x 2 per token and value head (d_k = d_v = d)."""
     d, C = p.d_k, p.chunk
@@ -67,12 +78,13 @@ def prefill_flops(p) -> float:
 
 
 # The prefill kernels in launch order, with the part of the algorithmic traffic each
-# one carries.  Tensor-core path: the fused chunk kernel moves everything.  CUDA-core
+# one carries.  Tensor-core path: the chunk-parallel front kernel reads the chunk-local
+# inputs (q, k, beta, g); the chain kernel reads v, writes o and reads/writes the states
+# (the chunk records between them are overhead, not algorithmic traffic).  CUDA-core
 # path: the chunk-parallel kernel reads every input once; the scan writes o and
 # reads/writes the states.
-ALL_BYTES = ("q", "k", "v", "beta", "g", "o", "state")
 PREFILL_STAGES = {
-    True: [("plan", ()), ("tc_prefill", ALL_BYTES)],
+    True: [("plan", ()), ("tc_front", ("q", "k", "beta", "g")), ("tc_chain", ("v", "o", "state"))],
     False: [("plan", ()), ("chunk_local", ("q", "k", "v", "beta", "g")),
             ("state_scan", ("o", "state"))],
 }
@@ -440,8 +452,8 @@ def ours_arm(args, rank, world, local):
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                 "peak_source": peaks["source"], "kernel_ms": stage_ms[dom],
                 "stage_ms": {n: m for (n, _), m in zip(stages, stage_ms)},
-                "tensor_tflops": prefill_flops(p) / (stage_ms[dom] / 1e3) / 1e12
-                if tensor_cores else None,
+                "tensor_tflops": tc_executed_flops(p)[name] / (stage_ms[dom] / 1e3) / 1e12
+                if tensor_cores and name in tc_executed_flops(p) else None,
                 "tensor_peak_tflops": peaks["bf16_tflops"]}
     path_bytes = float(sum(abytes.values()))
     also = []

@@ -19,6 +19,9 @@ bool tc_prefill_supported(const Problem& P, bool qbf16);
 size_t tc_workspace_bytes(const Problem& P);
 cudaError_t launch_prefill_tc(const Problem& P, void* workspace, bool perch, bool sbf16,
                               cudaStream_t stream, const Stages& st);
+size_t split_workspace_bytes(const Problem& P);
+cudaError_t launch_prefill_split(const Problem& P, void* workspace, bool perch, bool sbf16,
+                                 cudaStream_t stream, const Stages& st);
 int ring_record_elems(int D, bool perch);
 cudaError_t launch_verify(const Problem& P, int window, float* ring, bool qbf16, bool sbf16,
                           bool perch, cudaStream_t stream);
@@ -76,7 +79,8 @@ kda_status_t check_common(const kda_params_t* p, Problem* P) {
   if (p->state_dtype != KDA_DTYPE_F32 && p->state_dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
   if (p->decay_kind != KDA_DECAY_SCALAR && p->decay_kind != KDA_DECAY_PER_CHANNEL)
     return KDA_ERR_INVALID_ARG;
-  if (p->flags & ~(KDA_FLAG_CHECKED | KDA_FLAG_CUDA_CORES)) return KDA_ERR_INVALID_ARG;
+  if (p->flags & ~(KDA_FLAG_CHECKED | KDA_FLAG_CUDA_CORES | KDA_FLAG_COMPACT))
+    return KDA_ERR_INVALID_ARG;
   const int64_t es = static_cast<int64_t>(elem_size(p->qkv_dtype));
   const int64_t dq = static_cast<int64_t>(p->num_k_heads) * p->d_k;
   const int64_t dv = static_cast<int64_t>(p->num_v_heads) * p->d_v;
@@ -119,8 +123,14 @@ bool use_tc(const kda_params_t* p, const Problem& P) {
          kda::tc_prefill_supported(P, p->qkv_dtype == KDA_DTYPE_BF16);
 }
 
+// Tensor-core path: by default a chunk-parallel front kernel writes every chunk's chain
+// operands to the workspace and a chain kernel walks each sequence; KDA_FLAG_COMPACT runs
+// both parts in one kernel per (sequence, head, value tile) with only the chunk table.
+bool compact_tc(const kda_params_t* p) { return (p->flags & KDA_FLAG_COMPACT) != 0; }
+
 size_t prefill_workspace_bytes(const kda_params_t* p, const Problem& P) {
-  return use_tc(p, P) ? kda::tc_workspace_bytes(P) : kda::simt_workspace_bytes(P);
+  if (!use_tc(p, P)) return kda::simt_workspace_bytes(P);
+  return compact_tc(p) ? kda::tc_workspace_bytes(P) : kda::split_workspace_bytes(P);
 }
 
 }  // namespace
@@ -182,9 +192,13 @@ kda_status_t kda_prefill_fwd(const kda_params_t* p, const void* q, const void* k
   const bool sbf16 = p->state_dtype == KDA_DTYPE_BF16;
   const bool perch = p->decay_kind == KDA_DECAY_PER_CHANNEL;
   const kda::Stages st = current_stages();
-  if (use_tc(p, P))
-    return to_status(kda::launch_prefill_tc(P, workspace, perch, sbf16,
-                                            static_cast<cudaStream_t>(stream), st));
+  if (use_tc(p, P)) {
+    if (compact_tc(p))
+      return to_status(kda::launch_prefill_tc(P, workspace, perch, sbf16,
+                                              static_cast<cudaStream_t>(stream), st));
+    return to_status(kda::launch_prefill_split(P, workspace, perch, sbf16,
+                                               static_cast<cudaStream_t>(stream), st));
+  }
   return to_status(kda::launch_prefill_simt(P, workspace, qbf16, perch, sbf16,
                                             static_cast<cudaStream_t>(stream), st));
 }
@@ -330,10 +344,15 @@ extern "C" kda_status_t kda_prefill_fwd_no_alloc(const kda_params_t* p, const vo
   Problem P{};
   kda_status_t s = check_prefill(p, &P);
   if (s != KDA_OK) return s;
-  if (prefill_workspace_bytes(p, P) > KDA_NO_ALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
+  // the tensor-core path falls back to its single-kernel form when the chunk records
+  // of the two-kernel form do not fit the scratch
+  kda_params_t q_params = *p;
+  if (use_tc(p, P) && prefill_workspace_bytes(p, P) > KDA_NO_ALLOC_SCRATCH_BYTES)
+    q_params.flags |= KDA_FLAG_COMPACT;
+  if (prefill_workspace_bytes(&q_params, P) > KDA_NO_ALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
   if (p->num_seqs == 0) return KDA_OK;
   void* scratch = no_alloc_scratch();
   if (!scratch) return KDA_ERR_CUDA;
-  return kda_prefill_fwd(p, q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, o,
-                         scratch, KDA_NO_ALLOC_SCRATCH_BYTES, stream);
+  return kda_prefill_fwd(&q_params, q, k, v, beta, log_decay, input_row_offsets, slot_idx,
+                         state_pool, o, scratch, KDA_NO_ALLOC_SCRATCH_BYTES, stream);
 }

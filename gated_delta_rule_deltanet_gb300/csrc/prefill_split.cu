@@ -1,0 +1,1013 @@
+// prefill_split.cu -- chunkwise prefill on Blackwell tensor cores in two kernels:
+// a chunk-parallel front kernel and a sequential chain kernel (d = 128, C = 64).
+//
+// The chunk form ("You Could Have Come Up With Kimi Delta Attention", sec. 6.3-6.5;
+// "From Attention to Learned Memory", sec. 4, WY/UT transform) splits every chunk's
+// work into a part that depends only on the chunk's own keys, queries, gates and
+// betas -- the intra-chunk matrices A_kk and A_qk, the inverse T = (I + A_kk)^-1 and
+// the WY factors -- and a part that carries the state from chunk to chunk.  The
+// first part is independent across all chunks of all sequences, so the front kernel
+// runs one CTA per (chunk, value head) over the whole GPU and writes each chunk's
+// chain operands to the workspace:
+//
+//   A1  = [TB; A_qk TB]                 128 x 64   fp16
+//   A2  = [-W; Q~ - A_qk W]             128 x 128  fp16
+//   KET = K_end^T                       128 x 64   fp16
+//   gam = exp(G_last) per key channel   128        fp32
+//
+// already in the no-swizzle K-major core-matrix order in which the tensor core reads
+// them from shared memory, so the chain kernel moves a chunk's record with one bulk
+// copy.  The chain kernel keeps a (sequence, value head, 64 value columns) slice of
+// the state in registers and per chunk issues two MMAs,
+//
+//   [E; O] = A1 V + A2 S              M=128 N=64 K=64+128
+//   S     <- diag(gam) S + KET E      M=128 N=64 K=64
+//
+// while the next chunk's record and values are being fetched.  The front work is done
+// once per (chunk, value head) rather than once per value tile, and none of it sits
+// on the sequential path.
+//
+// The arithmetic of both kernels is that of the single-kernel path in prefill_tc.cu
+// (same operand precisions and factorisations); only where it runs differs.
+#include "kda_common.cuh"
+#include "prefill_plan.cuh"
+#include "tc_utils.cuh"
+
+namespace kda {
+
+namespace tcs {
+
+constexpr int C = 64;       // chunk
+constexpr int D = 128;      // head size
+constexpr int BV = 64;      // value columns per chain CTA
+constexpr int NT = 256;     // threads (8 warps)
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr float kMaxHalfChunkDecay = 80.0f;
+
+// record of one (chunk, value head) in the workspace
+constexpr uint32_t REC_A1 = 0;
+constexpr uint32_t REC_A2 = REC_A1 + 128 * 64 * 2;
+constexpr uint32_t REC_KET = REC_A2 + 128 * 128 * 2;
+constexpr uint32_t REC_GAM = REC_KET + 128 * 64 * 2;
+constexpr uint32_t REC_BYTES = REC_GAM + 128 * 4;    // 66048, a multiple of 16
+static_assert(REC_BYTES % 16 == 0, "records must stay 16-byte aligned");
+
+// per-chunk vectors of the front kernel (byte offsets inside its SMALL area)
+constexpr uint32_t O_GS = 0, O_BETA = 256, O_RK = 512, O_RQ = 768, O_EG = 1024, O_EGL = 1280,
+                   O_GAM = 1536, O_GA = 2048, O_EA = 2560, O_KF = 2816, SMALL_BYTES = 3072;
+
+constexpr int SP = 68;      // padded row of the fp32 solve tiles
+constexpr int XP = 36;      // row of the merge temporaries
+constexpr uint32_t SOL_BYTES = 2 * C * SP * 4 + 32 * XP * 4;
+
+template <bool PERCH>
+struct FrontMap;
+
+// Scalar decay: the raw k and q rows are copied straight into the A-GEMM operand
+// [K; Q] (padded leading offset, so column reads of it are conflict-free); the key
+// rows double as the B operand.
+template <>
+struct FrontMap<false> {
+  static constexpr uint32_t AK_LBO = 144, AK_SBO = (D / 8) * AK_LBO;
+  static constexpr uint32_t AK = 0;
+  static constexpr uint32_t SMALL = AK + 16 * AK_SBO;
+  static constexpr uint32_t R2 = SMALL + SMALL_BYTES;   // solve, then K~^T and A1
+  static constexpr uint32_t LMAT = R2 + SOL_BYTES;      // [I; A_qk] 128 x 64 fp16
+  static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;  // TB^T 64 x 64 fp16
+  static constexpr uint32_t BYTES = TBT + 64 * 64 * 2;
+};
+
+// Per-channel decay: raw rows are staged (padded) and the A-GEMM operands are the
+// normalised, decayed rows as split bf16 (high halves in shared memory, the low half
+// of [K+; Q+] in tensor memory).
+template <>
+struct FrontMap<true> {
+  static constexpr int KS = D + 8, GS = D + 4;
+  static constexpr uint32_t S_K = 0;
+  static constexpr uint32_t S_Q = S_K + C * KS * 2;
+  static constexpr uint32_t S_G = S_Q + C * KS * 2;     // log-decay -> exp(G - G_a), fp32
+  static constexpr uint32_t SMALL = S_G + C * GS * 4;
+  static constexpr uint32_t AK = SMALL + SMALL_BYTES;   // [K+; Q+] high halves
+  static constexpr uint32_t BK = AK + 128 * 128 * 2;    // K- high half
+  static constexpr uint32_t BKLO = BK + 64 * 128 * 2;   // K- low half
+  static constexpr uint32_t R2 = BK;                    // consumed K- halves: solve, K~^T, A1
+  static constexpr uint32_t LMAT = R2 + SOL_BYTES;
+  static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;
+  static constexpr uint32_t BYTES = TBT + 64 * 64 * 2;
+  static_assert(LMAT >= BKLO + 64 * 128 * 2, "solve area covers the K- halves");
+};
+
+// front TMEM columns: A_kk/A_qk, X, Y (the low half of [K+; Q+] shares Y's columns:
+// it is consumed by the A-GEMM before Y is produced)
+constexpr uint32_t F_A = 0, F_X = 64, F_Y = 128, F_ALO = 128, F_COLS = 256;
+
+// chain shared memory
+constexpr int VS = BV + 8;                               // raw v row (bf16), 144 B
+constexpr uint32_t LBO_P = 144;                          // padded leading offset of S^T, E^T
+constexpr uint32_t ST_SBO = (D / 8) * LBO_P;
+constexpr uint32_t ET_SBO = (C / 8) * LBO_P;
+constexpr int OS = BV + 4;                               // o staging row (fp32)
+constexpr uint32_t CH_BUF0 = 0, CH_BUF1 = REC_BYTES;     // two chunk records
+constexpr uint32_t CH_VSTG = 2 * REC_BYTES;              // raw v of the next chunk [64][VS]
+constexpr uint32_t CH_VT = CH_VSTG + C * VS * 2;         // V^T 64 x 64 fp16
+constexpr uint32_t CH_ST = CH_VT + 64 * 64 * 2;          // S^T 64 x 128 fp16, padded
+constexpr uint32_t CH_ET = CH_ST + (BV / 8) * ST_SBO;    // E^T 64 x 64 fp16, padded
+constexpr uint32_t CH_OST = CH_ET + (BV / 8) * ET_SBO;   // o rows fp32 [64][OS]
+constexpr uint32_t CH_BYTES = CH_OST + C * OS * 4;
+static_assert(CH_BYTES + 64 <= 227 * 1024, "chain shared memory budget");
+static_assert(FrontMap<true>::BYTES + 64 <= 227 * 1024, "front shared memory budget");
+constexpr uint32_t T_D1 = 0, T_D2 = 64, CH_COLS = 128;
+
+__device__ __forceinline__ uint4 f16x8_pack(const float* x) {
+  return make_uint4(tc::pack_f16x2(x[0], x[1]), tc::pack_f16x2(x[2], x[3]),
+                    tc::pack_f16x2(x[4], x[5]), tc::pack_f16x2(x[6], x[7]));
+}
+
+}  // namespace tcs
+
+// cp.async copies of one chunk's k, q, beta and log-decay (rows past n zero-filled)
+template <bool PERCH>
+__device__ __forceinline__ void front_issue_loads(const Problem& P, unsigned char* smem,
+                                                  int64_t t0, int n, int kh, int h, int tid) {
+  using namespace tcs;
+  using M = FrontMap<PERCH>;
+  const int HV = P.HV;
+  const uint32_t sb = tc::smem_u32(smem);
+  for (int u = tid; u < C * (D / 8); u += NT) {
+    const int i = u / (D / 8), q8 = u % (D / 8);
+    const bool live = i < n;
+    const int64_t t = live ? t0 + i : t0;
+    const uint32_t nb = live ? 16u : 0u;
+    uint32_t dk, dq;
+    if constexpr (PERCH) {
+      dk = M::S_K + (i * M::KS + q8 * 8) * 2;
+      dq = M::S_Q + (i * M::KS + q8 * 8) * 2;
+    } else {
+      dk = M::AK + tc::cm_offset(i, q8 * 8, M::AK_LBO, M::AK_SBO);
+      dq = M::AK + tc::cm_offset(C + i, q8 * 8, M::AK_LBO, M::AK_SBO);
+    }
+    tc::cp_async16(sb + dk, static_cast<const uint16_t*>(P.k) + t * P.k_stride + static_cast<int64_t>(kh) * D + q8 * 8, nb);
+    tc::cp_async16(sb + dq, static_cast<const uint16_t*>(P.q) + t * P.q_stride + static_cast<int64_t>(kh) * D + q8 * 8, nb);
+  }
+  if constexpr (PERCH) {
+    for (int u = tid; u < C * (D / 4); u += NT) {
+      const int i = u / (D / 4), q4 = u % (D / 4);
+      const bool live = i < n;
+      const int64_t t = live ? t0 + i : t0;
+      tc::cp_async16(sb + M::S_G + (i * M::GS + q4 * 4) * 4, P.g + (t * HV + h) * D + q4 * 4,
+                     live ? 16u : 0u);
+    }
+  }
+  if (tid < C) {
+    const bool live = tid < n;
+    const int64_t t = live ? t0 + tid : t0;
+    tc::cp_async4(sb + M::SMALL + O_BETA + tid * 4, P.beta + t * HV + h, live ? 4u : 0u);
+    if (!PERCH) tc::cp_async4(sb + M::SMALL + O_GS + tid * 4, P.g + t * HV + h, live ? 4u : 0u);
+  }
+  tc::cp_async_commit();
+}
+
+// One CTA per (chunk, value head): everything of the chunk that does not depend on the
+// state, written to the chunk's record.
+template <bool PERCH>
+__global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
+    tc_front_kernel(Problem P, PlanView plan, unsigned char* records) {
+  using namespace tcs;
+  using M = FrontMap<PERCH>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ uint64_t s_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_range;
+  __shared__ int s_anchored;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= plan.info[0]) return;
+  const int gc = blockIdx.x, h = blockIdx.y;
+  const int HV = P.HV;
+  const int kh = h / (HV / P.HK);
+  const ChunkInfo ci = plan.chunks[gc];
+  const int n = ci.n;
+  const int64_t t0 = ci.t0;
+  unsigned char* rec = records + (static_cast<int64_t>(gc) * HV + h) * static_cast<int64_t>(REC_BYTES);
+
+  float* sGs = reinterpret_cast<float*>(smem + M::SMALL + O_GS);
+  float* sBeta = reinterpret_cast<float*>(smem + M::SMALL + O_BETA);
+  float* sRK = reinterpret_cast<float*>(smem + M::SMALL + O_RK);
+  float* sRQ = reinterpret_cast<float*>(smem + M::SMALL + O_RQ);
+  float* sEG = reinterpret_cast<float*>(smem + M::SMALL + O_EG);
+  float* sEGL = reinterpret_cast<float*>(smem + M::SMALL + O_EGL);
+  float* sGam = reinterpret_cast<float*>(smem + M::SMALL + O_GAM);
+  float* sGA = reinterpret_cast<float*>(smem + M::SMALL + O_GA);
+  float* sEA = reinterpret_cast<float*>(smem + M::SMALL + O_EA);
+  float* sKF = reinterpret_cast<float*>(smem + M::SMALL + O_KF);
+  float* sA = reinterpret_cast<float*>(smem + M::R2);
+  float* sT = reinterpret_cast<float*>(smem + M::R2 + C * SP * 4);
+  float* sX = reinterpret_cast<float*>(smem + M::R2 + 2 * C * SP * 4);
+  constexpr uint32_t KTT = M::R2, A1 = M::R2 + 128 * 64 * 2;
+
+  front_issue_loads<PERCH>(P, smem, t0, n, kh, h, tid);
+  if (warp == 0) {
+    tc::tmem_alloc(&s_tmem, F_COLS);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    tc::mbar_init(&s_bar, 1);
+    tc::fence_mbar_init();
+    s_abort = 0;
+    s_range = 0;
+  }
+  const int row = 32 * (warp & 3) + lane;       // TMEM lane = M row
+  const int chalf = warp >> 2;
+  const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  if (row < C) {                                // identity rows of L = [I; A_qk]
+    float idv[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) idv[e] = (32 * chalf + e == row) ? 1.f : 0.f;
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8)
+      tc::f16x8_store(smem, M::LMAT + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64)),
+                      idv + 8 * g8);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = s_tmem;
+  uint32_t phase = 0;
+  auto mma_wait = [&]() {
+    const bool ok = tc::mbar_wait_bounded(&s_bar, phase & 1, kWaitLimit);
+    phase ^= 1;
+    if (!ok) s_abort = 1;
+    tc::fence_after_sync();
+  };
+  // raw bf16 element (token m, channel c) of k or q
+  auto k_raw = [&](int m, int c) -> float {
+    if constexpr (PERCH) return tc::bf16_at(smem, M::S_K, m * M::KS + c);
+    else return tc::bf16_at(smem, M::AK + tc::cm_offset(m, c, M::AK_LBO, M::AK_SBO), 0);
+  };
+  auto kq_piece = [&](bool is_q, int i, int c) -> const unsigned char* {   // 8 channels
+    if constexpr (PERCH) return smem + (is_q ? M::S_Q : M::S_K) + (i * M::KS + c) * 2;
+    else return smem + M::AK + tc::cm_offset(is_q ? C + i : i, c, M::AK_LBO, M::AK_SBO);
+  };
+
+  tc::cp_async_wait_all();
+  __syncthreads();
+
+  // ------------------------------------------------------------------ prep
+  {                                             // L2 norms: 4 threads per row
+    const int i = tid >> 2, part = tid & 3;
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8) {
+      float kx[8], qx[8];
+      tc::bf16x8_load(kq_piece(false, i, part * 32 + g8 * 8), kx);
+      tc::bf16x8_load(kq_piece(true, i, part * 32 + g8 * 8), qx);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        sk += kx[e] * kx[e];
+        sq += qx[e] * qx[e];
+      }
+    }
+    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+    sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+    if (part == 0) {
+      sRK[i] = P.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
+      sRQ[i] = (P.l2norm ? rsqrtf(sq + 1e-6f) : 1.f) * P.scale;
+    }
+  }
+  if constexpr (PERCH) {
+    float* sG = reinterpret_cast<float*>(smem + M::S_G);
+    if (tid < D) {
+      // channel tid: inclusive cumsum G, then exp(G - G_a) in place (anchor G_a at the
+      // chunk's middle token); exp(G_a) and exp(G_last) go to the small arrays
+      float acc = 0.f, gmin = 0.f, gmax = -3.0e38f;
+#pragma unroll
+      for (int i0 = 0; i0 < C; i0 += 16) {
+        float gv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) gv[e] = sG[(i0 + e) * M::GS + tid];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          acc += gv[e];
+          gmin = fminf(gmin, acc);
+          gmax = fmaxf(gmax, acc);
+          sG[(i0 + e) * M::GS + tid] = acc;
+        }
+      }
+      const float ga = sG[((n - 1) / 2) * M::GS + tid];
+      if (fmaxf(gmax - ga, ga - gmin) > kMaxHalfChunkDecay) s_range = 1;
+#pragma unroll
+      for (int i0 = 0; i0 < C; i0 += 16) {
+        float gv[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) gv[e] = sG[(i0 + e) * M::GS + tid];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) sG[(i0 + e) * M::GS + tid] = __expf(gv[e] - ga);
+      }
+      sGam[tid] = __expf(acc);
+      sGA[tid] = __expf(ga);
+    }
+  } else if (warp == 0) {                       // scalar: warp scan of 64 values
+    const float g0 = sGs[2 * lane], g1 = sGs[2 * lane + 1];
+    float s = g0 + g1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += y;
+    }
+    const float gl = __shfl_sync(0xffffffffu, s, 31);
+    sGs[2 * lane] = s - g1;
+    sGs[2 * lane + 1] = s;
+    sEG[2 * lane] = __expf(s - g1);
+    sEG[2 * lane + 1] = __expf(s);
+    sEGL[2 * lane] = __expf(gl - (s - g1));
+    sEGL[2 * lane + 1] = __expf(gl - s);
+    const float gam = __expf(gl);
+    sGam[lane] = gam; sGam[lane + 32] = gam; sGam[lane + 64] = gam; sGam[lane + 96] = gam;
+    // anchored factors exp(G_i - G_a), exp(G_a - G_j), anchor mid-chunk, so that
+    // exp(G_i - G_j) is a product of two per-token values while both stay finite
+    const int am = (n - 1) / 2;
+    const float ga = __shfl_sync(0xffffffffu, (am & 1) ? s : s - g1, am >> 1);
+    const float d0 = (s - g1) - ga, d1 = s - ga;
+    const bool ok = __all_sync(0xffffffffu, fmaxf(fabsf(d0), fabsf(d1)) <= kMaxHalfChunkDecay);
+    sEA[2 * lane] = __expf(d0);
+    sEA[2 * lane + 1] = __expf(d1);
+    sKF[2 * lane] = __expf(-d0);
+    sKF[2 * lane + 1] = __expf(-d1);
+    if (lane == 0) s_anchored = ok ? 1 : 0;
+  }
+  __syncthreads();
+  if (!PERCH && tid < C) sKF[tid] *= sRK[tid];
+  if constexpr (PERCH) {
+    const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
+    {                                           // [K+; Q+]: high halves to smem, low to TMEM
+      const int i = row < C ? row : row - C;
+      const uint32_t src = (row < C ? M::S_K : M::S_Q) + (i * M::KS) * 2;
+      const float rs = row < C ? sRK[i] : sRQ[i];
+      uint32_t lo[32];
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8) {
+        const int cc = 64 * chalf + 8 * g8;
+        float x[8];
+        tc::bf16x8_load(smem + src + cc * 2, x);
+        const float4 g0 = *reinterpret_cast<const float4*>(sG + i * M::GS + cc);
+        const float4 g1 = *reinterpret_cast<const float4*>(sG + i * M::GS + cc + 4);
+        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        uint32_t hi[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const float v0 = x[e] * rs * f[e], v1 = x[e + 1] * rs * f[e + 1];
+          hi[e / 2] = tc::pack_bf16x2(v0, v1);
+          const float h0 = __uint_as_float(hi[e / 2] << 16);
+          const float h1 = __uint_as_float(hi[e / 2] & 0xffff0000u);
+          lo[4 * g8 + e / 2] = tc::pack_bf16x2(v0 - h0, v1 - h1);
+        }
+        *reinterpret_cast<uint4*>(smem + M::AK + tc::cm_offset(row, cc, 128, tc::dense_sbo(D))) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      }
+      uint32_t l0[16], l1[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        l0[e] = lo[e];
+        l1[e] = lo[16 + e];
+      }
+      tc::tmem_st16(tmem + lane_addr + F_ALO + 32 * chalf, l0);
+      tc::tmem_st16(tmem + lane_addr + F_ALO + 32 * chalf + 16, l1);
+      tc::tmem_wait_st();
+    }
+    {                                           // K-: 4 threads per key row
+      const int j = tid >> 2, qq = tid & 3;
+      const float rs = sRK[j];
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        const int cc = 32 * qq + 8 * g8;
+        float x[8];
+        tc::bf16x8_load(smem + M::S_K + (j * M::KS + cc) * 2, x);
+        const float4 g0 = *reinterpret_cast<const float4*>(sG + j * M::GS + cc);
+        const float4 g1 = *reinterpret_cast<const float4*>(sG + j * M::GS + cc + 4);
+        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const float v0 = x[e] * rs * __fdividef(1.f, f[e]);
+          const float v1 = x[e + 1] * rs * __fdividef(1.f, f[e + 1]);
+          hi[e / 2] = tc::pack_bf16x2(v0, v1);
+          const float h0 = __uint_as_float(hi[e / 2] << 16);
+          const float h1 = __uint_as_float(hi[e / 2] & 0xffff0000u);
+          lo[e / 2] = tc::pack_bf16x2(v0 - h0, v1 - h1);
+        }
+        *reinterpret_cast<uint4*>(smem + M::BK + tc::cm_offset(j, cc, 128, tc::dense_sbo(D))) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(smem + M::BKLO + tc::cm_offset(j, cc, 128, tc::dense_sbo(D))) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      }
+    }
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+
+  // ------------------------------------------------------------------ A-GEMM
+  if (tid == 0) {
+    const uint32_t id = tc::idesc_f16(128, 64, tc::kBF16);
+    if constexpr (PERCH) {
+      const uint32_t ak = tc::smem_u32(smem + M::AK), bk = tc::smem_u32(smem + M::BK),
+                     bl = tc::smem_u32(smem + M::BKLO);
+      for (int s = 0; s < D / 16; ++s)          // hi x hi
+        tc::mma_ss(tmem + F_A, tc::smem_desc(ak + s * 256, 128, tc::dense_sbo(D)),
+                   tc::smem_desc(bk + s * 256, 128, tc::dense_sbo(D)), id, s > 0);
+      for (int s = 0; s < D / 16; ++s)          // hi x lo
+        tc::mma_ss(tmem + F_A, tc::smem_desc(ak + s * 256, 128, tc::dense_sbo(D)),
+                   tc::smem_desc(bl + s * 256, 128, tc::dense_sbo(D)), id, 1);
+      for (int s = 0; s < D / 16; ++s)          // lo x hi (low half from TMEM)
+        tc::mma_ts(tmem + F_A, tmem + F_ALO + s * 8,
+                   tc::smem_desc(bk + s * 256, 128, tc::dense_sbo(D)), id, 1);
+    } else {
+      const uint32_t ak = tc::smem_u32(smem + M::AK);
+      for (int s = 0; s < D / 16; ++s)          // [K; Q] K^T on the raw rows
+        tc::mma_ss(tmem + F_A, tc::smem_desc(ak + s * 2 * M::AK_LBO, M::AK_LBO, M::AK_SBO),
+                   tc::smem_desc(ak + s * 2 * M::AK_LBO, M::AK_LBO, M::AK_SBO), id, s > 0);
+    }
+    tc::mma_commit(&s_bar);
+  }
+  mma_wait();
+
+  // ------------------------------------------------------------------ A_kk, A_qk
+  {
+    uint32_t r0[16], r1[16];
+    tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf, r0);
+    tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf + 16, r1);
+    tc::tmem_wait_ld();
+    const bool is_k = row < C;
+    const int i = is_k ? row : row - C;
+    const float ri = is_k ? (PERCH ? 1.f : sRK[i]) * sBeta[i] : (PERCH ? 1.f : sRQ[i]);
+    float x[32];
+    if (PERCH) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * ri;
+    } else if (s_anchored) {                    // exp(G_i - G_j) = E_i F_j
+      const float rie = ri * sEA[i];
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float4 kf = *reinterpret_cast<const float4*>(sKF + 32 * chalf + e);
+        x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * rie * kf.x;
+        x[e + 1] = __uint_as_float(e + 1 < 16 ? r0[e + 1] : r1[e - 15]) * rie * kf.y;
+        x[e + 2] = __uint_as_float(e + 2 < 16 ? r0[e + 2] : r1[e - 14]) * rie * kf.z;
+        x[e + 3] = __uint_as_float(e + 3 < 16 ? r0[e + 3] : r1[e - 13]) * rie * kf.w;
+      }
+    } else {                                    // exact per pair for extreme decays
+      const float gi = sGs[i];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int j = 32 * chalf + e;
+        x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * ri * sRK[j] * __expf(gi - sGs[j]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int j = 32 * chalf + e;
+      const bool keep = is_k ? (j < i) : (j <= i);
+      x[e] = keep ? x[e] : 0.f;
+    }
+    if (is_k) {
+#pragma unroll
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<float4*>(sA + i * SP + 32 * chalf + e) =
+            make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+    } else {
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8)
+        tc::f16x8_store(smem, M::LMAT + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64)),
+                        x + 8 * g8);
+    }
+  }
+  // the 32x32 merge reads the strictly-upper 16x16 blocks of T11 and T22: zero them
+  for (int idx = tid; idx < 2 * 256; idx += NT) {
+    const int blk = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
+    sT[(32 * blk + r) * SP + 32 * blk + 16 + c] = 0.f;
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------------ solve
+  if (warp < 2) {                               // diagonal 16x16 blocks, one column per lane
+    const int base = (warp * 2 + (lane >> 4)) * 16, col = lane & 15;
+    float t[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float v = r == col ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0; m < r; ++m) v -= sA[(base + r) * SP + base + m] * t[m];
+      t[r] = v;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) sT[(base + r) * SP + base + col] = t[r];
+  }
+  __syncthreads();
+  if (tid < 128) {                              // X = A21 T11, two 16x16 pairs
+    const int p = tid >> 6, r = (tid >> 2) & 15, c = (tid & 3) * 4;
+    const int r0 = 32 * p + 16, c0 = 32 * p;
+    float a[16];
+#pragma unroll
+    for (int m = 0; m < 16; m += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(sA + (r0 + r) * SP + c0 + m);
+      a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float4 t = *reinterpret_cast<const float4*>(sT + (c0 + m) * SP + c0 + c);
+      acc.x += a[m] * t.x; acc.y += a[m] * t.y; acc.z += a[m] * t.z; acc.w += a[m] * t.w;
+    }
+    *reinterpret_cast<float4*>(sX + (16 * p + r) * XP + c) = acc;
+  }
+  __syncthreads();
+  if (tid < 128) {                              // T21 = -T22 X
+    const int p = tid >> 6, r = (tid >> 2) & 15, c = (tid & 3) * 4;
+    const int r0 = 32 * p + 16, c0 = 32 * p;
+    float a[16];
+#pragma unroll
+    for (int m = 0; m < 16; m += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(sT + (r0 + r) * SP + r0 + m);
+      a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float4 x = *reinterpret_cast<const float4*>(sX + (16 * p + m) * XP + c);
+      acc.x += a[m] * x.x; acc.y += a[m] * x.y; acc.z += a[m] * x.z; acc.w += a[m] * x.w;
+    }
+    *reinterpret_cast<float4*>(sT + (r0 + r) * SP + c0 + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
+  {                                             // X = A21 T11, one 32x32 pair
+    const int r = tid >> 3, c = (tid & 7) * 4;
+    float a[32];
+#pragma unroll
+    for (int m = 0; m < 32; m += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(sA + (32 + r) * SP + m);
+      a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+      const float4 t = *reinterpret_cast<const float4*>(sT + m * SP + c);
+      acc.x += a[m] * t.x; acc.y += a[m] * t.y; acc.z += a[m] * t.z; acc.w += a[m] * t.w;
+    }
+    *reinterpret_cast<float4*>(sX + r * XP + c) = acc;
+  }
+  __syncthreads();
+  {                                             // T21 = -T22 X
+    const int r = tid >> 3, c = (tid & 7) * 4;
+    float a[32];
+#pragma unroll
+    for (int m = 0; m < 32; m += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(sT + (32 + r) * SP + 32 + m);
+      a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
+    }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 32; ++m) {
+      const float4 x = *reinterpret_cast<const float4*>(sX + m * XP + c);
+      acc.x += a[m] * x.x; acc.y += a[m] * x.y; acc.z += a[m] * x.z; acc.w += a[m] * x.w;
+    }
+    *reinterpret_cast<float4*>(sT + (32 + r) * SP + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+  }
+  __syncthreads();
+  for (int u = tid; u < C * (C / 8); u += NT) { // TB^T[j][m] = T[m][j] beta_j
+    const int j = u % C, m8 = u / C;
+    const float bj = sBeta[j];
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int m = m8 * 8 + e;
+      x[e] = m >= j ? sT[m * SP + j] * bj : 0.f;
+    }
+    tc::f16x8_store(smem, M::TBT + tc::cm_offset(j, m8 * 8, 128, tc::dense_sbo(64)), x);
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+
+  // ------------------------------------------------------------------ X = [I; A_qk] TB
+  if (tid == 0) {
+    const uint32_t id = tc::idesc_f16(128, 64, tc::kF16);
+    for (int s = 0; s < C / 16; ++s)
+      tc::mma_ss(tmem + F_X, tc::smem_desc(tc::smem_u32(smem + M::LMAT) + s * 256, 128, tc::dense_sbo(64)),
+                 tc::smem_desc(tc::smem_u32(smem + M::TBT) + s * 256, 128, tc::dense_sbo(64)), id, s > 0);
+    tc::mma_commit(&s_bar);
+  }
+  // K~^T (smem, the Y operand), K_end^T and gamma (the record); the solve area is free
+  for (int u = tid; u < D * (C / 8); u += NT) { // (channel c, 8 tokens)
+    const int c = u % D, m8 = u / D;
+    float kt[8], ke[8];
+    if constexpr (PERCH) {
+      const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
+      const float El = sG[(C - 1) * M::GS + c], ea = sGA[c];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int m = m8 * 8 + e;
+        const float Em = sG[m * M::GS + c];
+        const float kx = k_raw(m, c) * sRK[m];
+        kt[e] = kx * Em * ea;                   // k^ exp(G_m)
+        ke[e] = kx * __fdividef(El, Em);        // k^ exp(G_last - G_m)
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int m = m8 * 8 + e;
+        const float kx = k_raw(m, c) * sRK[m];
+        kt[e] = kx * sEG[m];
+        ke[e] = kx * sEGL[m];
+      }
+    }
+    tc::f16x8_store(smem, KTT + tc::cm_offset(c, m8 * 8, 128, tc::dense_sbo(64)), kt);
+    *reinterpret_cast<uint4*>(rec + REC_KET + tc::cm_offset(c, m8 * 8, 128, tc::dense_sbo(64))) =
+        f16x8_pack(ke);
+  }
+  if (tid < D) reinterpret_cast<float*>(rec + REC_GAM)[tid] = sGam[tid];
+  tc::fence_async_smem();
+  mma_wait();
+
+  // ------------------------------------------------------------------ A1 = X
+  {
+    uint32_t r0[16], r1[16];
+    tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf, r0);
+    tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf + 16, r1);
+    tc::tmem_wait_ld();
+    float x[32];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      x[e] = __uint_as_float(r0[e]);
+      x[e + 16] = __uint_as_float(r1[e]);
+    }
+#pragma unroll
+    for (int g8 = 0; g8 < 4; ++g8) {
+      const uint32_t off = tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64));
+      const uint4 v = f16x8_pack(x + 8 * g8);
+      *reinterpret_cast<uint4*>(smem + A1 + off) = v;
+      *reinterpret_cast<uint4*>(rec + REC_A1 + off) = v;
+    }
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+
+  // ------------------------------------------------------------------ Y = A1 K~
+  if (tid == 0) {
+    const uint32_t id = tc::idesc_f16(128, 128, tc::kF16);
+    for (int s = 0; s < C / 16; ++s)
+      tc::mma_ss(tmem + F_Y, tc::smem_desc(tc::smem_u32(smem + A1) + s * 256, 128, tc::dense_sbo(64)),
+                 tc::smem_desc(tc::smem_u32(smem + KTT) + s * 256, 128, tc::dense_sbo(64)), id, s > 0);
+    tc::mma_commit(&s_bar);
+  }
+  mma_wait();
+
+  // ------------------------------------------------------------------ A2 = [0; Q~] - Y
+  {
+    uint32_t ry[2][32];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      uint32_t a[16], b[16];
+      tc::tmem_ld16(tmem + lane_addr + F_Y + 64 * chalf + 32 * half, a);
+      tc::tmem_ld16(tmem + lane_addr + F_Y + 64 * chalf + 32 * half + 16, b);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        ry[half][e] = a[e];
+        ry[half][e + 16] = b[e];
+      }
+    }
+    tc::tmem_wait_ld();
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int c0 = 64 * chalf + 32 * half;
+      float x[32];
+      if (row >= C) {                           // Q~ = q scale/|q| exp(G)
+        const int i = row - C;
+        const float rq = sRQ[i];
+#pragma unroll
+        for (int g8 = 0; g8 < 4; ++g8) {
+          float qv[8];
+          tc::bf16x8_load(kq_piece(true, i, c0 + 8 * g8), qv);
+          if constexpr (PERCH) {
+            const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
+            const float4 ga = *reinterpret_cast<const float4*>(sG + i * M::GS + c0 + 8 * g8);
+            const float4 gb = *reinterpret_cast<const float4*>(sG + i * M::GS + c0 + 8 * g8 + 4);
+            const float4 aa = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8);
+            const float4 ab = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8 + 4);
+            const float gv[8] = {ga.x * aa.x, ga.y * aa.y, ga.z * aa.z, ga.w * aa.w,
+                                 gb.x * ab.x, gb.y * ab.y, gb.z * ab.z, gb.w * ab.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * rq * gv[e];
+          } else {
+            const float f = rq * sEG[i];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * f;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = 0.f;
+      }
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] -= __uint_as_float(ry[half][e]);
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8)
+        *reinterpret_cast<uint4*>(rec + REC_A2 + tc::cm_offset(row, c0 + 8 * g8, 128, tc::dense_sbo(D))) =
+            f16x8_pack(x + 8 * g8);
+    }
+  }
+
+  if (PERCH && s_range && tid == 0) raise_device_error(P.err, KDA_DEVERR_DECAY_RANGE);
+  if (s_abort) {
+    tc::mbar_wait_bounded(&s_bar, (phase ^ 1) & 1, kWaitLimit);   // the phase that timed out
+    if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, F_COLS);
+}
+
+// One CTA per (sequence, value head, 64 value columns): the state slice in registers,
+// two MMAs per chunk on the chunk's record, the next record and values in flight.
+template <bool SBF16>
+__global__ void __launch_bounds__(tcs::NT, 1)
+    tc_chain_kernel(Problem P, PlanView plan, const unsigned char* records) {
+  using namespace tcs;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ uint64_t s_mma_bar;
+  __shared__ uint64_t s_ld_bar[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (plan.info[1] == 0) return;
+  const int b = blockIdx.x, h = blockIdx.y, vt = blockIdx.z;
+  const int HV = P.HV;
+  const uint32_t bos = P.offsets[b], eos = P.offsets[b + 1];
+  if (eos <= bos) return;
+  const uint32_t nchunks = (eos - bos + C - 1) / C;
+  const int64_t c0 = plan.seq_chunk0[b];
+  const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + vt * BV;
+  const uint32_t sb = tc::smem_u32(smem);
+  auto rec = [&](uint32_t c) -> const unsigned char* {
+    return records + ((c0 + c) * HV + h) * static_cast<int64_t>(REC_BYTES);
+  };
+  auto chunk_n = [&](uint32_t c) -> int {
+    const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
+    return static_cast<int>(min(static_cast<int64_t>(C), static_cast<int64_t>(eos) - t0));
+  };
+  auto issue_v = [&](uint32_t c) {              // raw v tile of chunk c -> VSTG
+    const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
+    const int n = chunk_n(c);
+    for (int u = tid; u < C * (BV / 8); u += NT) {
+      const int i = u / (BV / 8), q8 = u % (BV / 8);
+      const bool live = i < n;
+      const int64_t t = live ? t0 + i : t0;
+      tc::cp_async16(sb + CH_VSTG + (i * VS + q8 * 8) * 2,
+                     static_cast<const uint16_t*>(P.v) + t * P.v_stride + static_cast<int64_t>(h) * D + vt * BV + q8 * 8,
+                     live ? 16u : 0u);
+    }
+    tc::cp_async_commit();
+  };
+  auto build_vt = [&]() {                       // V^T fp16 (N = value column, K = token)
+    for (int u = tid; u < BV * (C / 8); u += NT) {
+      const int j = u % BV, m8 = u / BV;
+      float x[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] = tc::bf16_at(smem, CH_VSTG, (m8 * 8 + e) * VS + j);
+      tc::f16x8_store(smem, CH_VT + tc::cm_offset(j, m8 * 8, 128, tc::dense_sbo(64)), x);
+    }
+  };
+
+  issue_v(0);
+  if (warp == 0) {
+    tc::tmem_alloc(&s_tmem, CH_COLS);
+    tc::tmem_relinquish();
+  }
+  if (tid == 0) {
+    tc::mbar_init(&s_mma_bar, 1);
+    tc::mbar_init(&s_ld_bar[0], 1);
+    tc::mbar_init(&s_ld_bar[1], 1);
+    tc::fence_mbar_init();
+    s_abort = 0;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&s_ld_bar[0], REC_BYTES);
+    tc::bulk_load(sb + CH_BUF0, rec(0), REC_BYTES, &s_ld_bar[0]);
+  }
+  const uint32_t tmem = s_tmem;
+  const int row = 32 * (warp & 3) + lane;       // TMEM lane = key channel (state row)
+  const int chalf = warp >> 2;
+  const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+
+  // S[row][32 chalf + j] of this CTA's value tile, fp32 in registers; its fp16 copy S^T
+  // (N = value column, K = key channel) is the first MMA's B operand
+  float Sv[32];
+  {
+    const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      Sv[j] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[base + j])
+                    : static_cast<const float*>(P.pool)[base + j];
+  }
+  auto write_state_operand = [&]() {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      *reinterpret_cast<uint16_t*>(smem + CH_ST + tc::cm_offset(32 * chalf + j, row, LBO_P, ST_SBO)) =
+          tc::f16_bits(Sv[j]);
+  };
+  write_state_operand();
+  tc::cp_async_wait_all();
+  __syncthreads();
+  build_vt();
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+
+  uint32_t phase = 0;
+  int pending = 0;                              // chunk whose record load is in flight, or -1
+  auto mma_wait = [&]() {
+    const bool ok = tc::mbar_wait_bounded(&s_mma_bar, phase & 1, kWaitLimit);
+    phase ^= 1;
+    if (!ok) s_abort = 1;
+    tc::fence_after_sync();
+  };
+
+  for (uint32_t c = 0; c < nchunks; ++c) {
+    const uint32_t buf = c & 1;
+    const uint32_t boff = buf ? CH_BUF1 : CH_BUF0;
+    const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
+    const int n = chunk_n(c);
+    const bool more = c + 1 < nchunks;
+    if (!tc::mbar_wait_bounded(&s_ld_bar[buf], (c >> 1) & 1, kWaitLimit)) s_abort = 1;
+    pending = -1;
+
+    // ---------------------------------------------------------------- [E; O] = A1 V + A2 S
+    if (tid == 0) {
+      const uint32_t id = tc::idesc_f16(128, BV, tc::kF16);
+      for (int s = 0; s < C / 16; ++s)
+        tc::mma_ss(tmem + T_D1, tc::smem_desc(sb + boff + REC_A1 + s * 256, 128, tc::dense_sbo(64)),
+                   tc::smem_desc(sb + CH_VT + s * 256, 128, tc::dense_sbo(64)), id, s > 0);
+      for (int s = 0; s < D / 16; ++s)
+        tc::mma_ss(tmem + T_D1, tc::smem_desc(sb + boff + REC_A2 + s * 256, 128, tc::dense_sbo(D)),
+                   tc::smem_desc(sb + CH_ST + s * 2 * LBO_P, LBO_P, ST_SBO), id, 1);
+      tc::mma_commit(&s_mma_bar);
+      if (more) {                               // the other buffer's record was consumed last chunk
+        tc::mbar_arrive_expect_tx(&s_ld_bar[buf ^ 1], REC_BYTES);
+        tc::bulk_load(sb + (buf ? CH_BUF0 : CH_BUF1), rec(c + 1), REC_BYTES, &s_ld_bar[buf ^ 1]);
+      }
+    }
+    if (more) {
+      pending = static_cast<int>(c + 1);
+      issue_v(c + 1);
+    }
+    mma_wait();
+
+    // ---------------------------------------------------------------- E^T, o staging
+    {
+      uint32_t r0[16], r1[16];
+      tc::tmem_ld16(tmem + lane_addr + T_D1 + 32 * chalf, r0);
+      tc::tmem_ld16(tmem + lane_addr + T_D1 + 32 * chalf + 16, r1);
+      tc::tmem_wait_ld();
+      if (row < C) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+          *reinterpret_cast<uint16_t*>(smem + CH_ET + tc::cm_offset(32 * chalf + e, row, LBO_P, ET_SBO)) =
+              tc::f16_bits(__uint_as_float(e < 16 ? r0[e] : r1[e - 16]));
+      } else {
+        float* op = reinterpret_cast<float*>(smem + CH_OST) + (row - C) * OS + 32 * chalf;
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          *reinterpret_cast<float4*>(op + e) =
+              make_float4(__uint_as_float(r0[e]), __uint_as_float(r0[e + 1]),
+                          __uint_as_float(r0[e + 2]), __uint_as_float(r0[e + 3]));
+          *reinterpret_cast<float4*>(op + 16 + e) =
+              make_float4(__uint_as_float(r1[e]), __uint_as_float(r1[e + 1]),
+                          __uint_as_float(r1[e + 2]), __uint_as_float(r1[e + 3]));
+        }
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    // ---------------------------------------------------------------- dS = K_end^T E
+    if (tid == 0) {
+      const uint32_t id = tc::idesc_f16(128, BV, tc::kF16);
+      for (int s = 0; s < C / 16; ++s)
+        tc::mma_ss(tmem + T_D2, tc::smem_desc(sb + boff + REC_KET + s * 256, 128, tc::dense_sbo(64)),
+                   tc::smem_desc(sb + CH_ET + s * 2 * LBO_P, LBO_P, ET_SBO), id, s > 0);
+      tc::mma_commit(&s_mma_bar);
+    }
+    // coalesced o stores: each warp instruction writes two whole 256-byte token rows
+#pragma unroll
+    for (int k = 0; k < (C * BV / 4) / NT; ++k) {
+      const int idx = tid + k * NT, i = idx / (BV / 4), q = idx % (BV / 4);
+      if (i < n)
+        *reinterpret_cast<float4*>(P.o + ((t0 + i) * HV + h) * D + vt * BV + q * 4) =
+            *reinterpret_cast<const float4*>(smem + CH_OST + (i * OS + q * 4) * 4);
+    }
+    if (more) {                                 // V^T of the next chunk (this chunk's is consumed)
+      tc::cp_async_wait_all();
+      __syncthreads();
+      build_vt();
+    }
+    mma_wait();
+
+    // ---------------------------------------------------------------- S <- diag(gam) S + dS
+    {
+      uint32_t r0[16], r1[16];
+      tc::tmem_ld16(tmem + lane_addr + T_D2 + 32 * chalf, r0);
+      tc::tmem_ld16(tmem + lane_addr + T_D2 + 32 * chalf + 16, r1);
+      tc::tmem_wait_ld();
+      const float gam = reinterpret_cast<const float*>(smem + boff + REC_GAM)[row];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) Sv[e] = gam * Sv[e] + __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
+      write_state_operand();
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (s_abort) break;
+  }
+  tc::cp_async_wait_all();
+
+  if (s_abort) {
+    // let what is still in flight finish (bounded) before shared and tensor memory go away
+    tc::mbar_wait_bounded(&s_mma_bar, (phase ^ 1) & 1, kWaitLimit);
+    if (pending >= 0) tc::mbar_wait_bounded(&s_ld_bar[pending & 1], (pending >> 1) & 1, kWaitLimit);
+    if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+  } else {
+    const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (SBF16)
+        static_cast<uint16_t*>(P.pool)[base + j] = f32_to_bf16_bits(Sv[j]);
+      else
+        static_cast<float*>(P.pool)[base + j] = Sv[j];
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, CH_COLS);
+}
+
+size_t split_workspace_bytes(const Problem& P) {
+  const size_t off = plan_layout(P, nullptr, 0, nullptr);
+  return off + static_cast<size_t>(plan_max_chunks(P)) * static_cast<size_t>(P.HV) * tcs::REC_BYTES;
+}
+
+template <bool PERCH>
+static cudaError_t launch_front_t(const Problem& P, const PlanView& plan, unsigned char* recs,
+                                  cudaStream_t st) {
+  auto k = tc_front_kernel<PERCH>;
+  constexpr uint32_t bytes = tcs::FrontMap<PERCH>::BYTES;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  k<<<dim3(static_cast<unsigned>(plan_max_chunks(P)), P.HV), tcs::NT, bytes, st>>>(P, plan, recs);
+  return cudaGetLastError();
+}
+
+template <bool SBF16>
+static cudaError_t launch_chain_t(const Problem& P, const PlanView& plan, const unsigned char* recs,
+                                  cudaStream_t st) {
+  auto k = tc_chain_kernel<SBF16>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(tcs::CH_BYTES));
+  if (e != cudaSuccess) return e;
+  k<<<dim3(P.num_seqs, P.HV, tcs::D / tcs::BV), tcs::NT, tcs::CH_BYTES, st>>>(P, plan, recs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_split(const Problem& P, void* workspace, bool perch, bool sbf16,
+                                 cudaStream_t stream, const Stages& st) {
+  PlanView plan;
+  const size_t off = plan_layout(P, static_cast<char*>(workspace), 0, &plan);
+  unsigned char* recs = static_cast<unsigned char*>(workspace) + off;
+  st.mark(0, stream);
+  cudaError_t e = launch_plan(P, plan, stream);
+  if (e != cudaSuccess) return e;
+  st.mark(1, stream);
+  e = perch ? launch_front_t<true>(P, plan, recs, stream) : launch_front_t<false>(P, plan, recs, stream);
+  if (e != cudaSuccess) return e;
+  st.mark(2, stream);
+  e = sbf16 ? launch_chain_t<true>(P, plan, recs, stream) : launch_chain_t<false>(P, plan, recs, stream);
+  st.mark(3, stream);
+  return e;
+}
+
+}  // namespace kda

@@ -115,36 +115,11 @@ static_assert(VT == TBT + 64 * 64 * 2, "K- low half spans TB^T and V^T");
 constexpr uint32_t T_A = 0, T_X = 64, T_Y = 128, T_D1 = 256, T_D2 = 320, T_ALO = 384,
                    T_S = 448, T_COLS = 512;
 
-// dense K-major tiles: lbo 128, sbo = (K / 8) * 128
-__host__ __device__ constexpr uint32_t dense_sbo(uint32_t K) { return (K / 8) * 128; }
-
-__device__ __forceinline__ void f16x8_store(unsigned char* smem, uint32_t off, const float* x) {
-  uint4 v;
-  v.x = tc::pack_f16x2(x[0], x[1]);
-  v.y = tc::pack_f16x2(x[2], x[3]);
-  v.z = tc::pack_f16x2(x[4], x[5]);
-  v.w = tc::pack_f16x2(x[6], x[7]);
-  *reinterpret_cast<uint4*>(smem + off) = v;
-}
-
-__device__ __forceinline__ uint16_t f16_bits(float x) {
-  return static_cast<uint16_t>(tc::pack_f16x2(x, 0.f) & 0xffffu);
-}
-
-__device__ __forceinline__ float bf16_at(const unsigned char* smem, uint32_t off, int idx) {
-  return bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(smem + off)[idx]);
-}
-
-// 8 bf16 from a 16-byte aligned smem address, widened to fp32
-__device__ __forceinline__ void bf16x8_load(const unsigned char* p, float* x) {
-  const uint4 u = *reinterpret_cast<const uint4*>(p);
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    x[2 * e] = __uint_as_float(w[e] << 16);
-    x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-  }
-}
+using tc::dense_sbo;
+using tc::f16x8_store;
+using tc::f16_bits;
+using tc::bf16_at;
+using tc::bf16x8_load;
 
 }  // namespace tcp
 

@@ -86,6 +86,13 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One arrival that also announces `bytes` of asynchronous copies completing on `bar`.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
 // ------------------------------------------------------------------ fences
 
 // Makes generic-proxy shared-memory writes visible to the tensor core (async proxy).
@@ -196,6 +203,17 @@ __device__ __forceinline__ void cp_async_wait_all() {
 }
 
 // Bulk (TMA-engine) copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
+// from global to shared memory; completion is counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          sdst),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bulk (TMA-engine) copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
 // from shared to global memory, tracked by the issuing thread's bulk groups.
 __device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
@@ -225,6 +243,42 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// ------------------------------------------------------------------ operand tiles
+
+// dense K-major tiles: lbo 128, sbo = (K / 8) * 128
+__host__ __device__ constexpr uint32_t dense_sbo(uint32_t K) { return (K / 8) * 128; }
+
+// 8 fp32 values -> 8 fp16 (round to nearest even) at a 16-byte aligned offset
+__device__ __forceinline__ void f16x8_store(unsigned char* smem, uint32_t off, const float* x) {
+  uint4 v;
+  v.x = pack_f16x2(x[0], x[1]);
+  v.y = pack_f16x2(x[2], x[3]);
+  v.z = pack_f16x2(x[4], x[5]);
+  v.w = pack_f16x2(x[6], x[7]);
+  *reinterpret_cast<uint4*>(smem + off) = v;
+}
+
+__device__ __forceinline__ uint16_t f16_bits(float x) {
+  return static_cast<uint16_t>(pack_f16x2(x, 0.f) & 0xffffu);
+}
+
+// element idx of a bf16 array at byte offset `off`, widened exactly to fp32
+__device__ __forceinline__ float bf16_at(const unsigned char* smem, uint32_t off, int idx) {
+  return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(smem + off)[idx])
+                         << 16);
+}
+
+// 8 bf16 from a 16-byte aligned address, widened to fp32
+__device__ __forceinline__ void bf16x8_load(const unsigned char* p, float* x) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    x[2 * e] = __uint_as_float(w[e] << 16);
+    x[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+  }
 }
 
 }  // namespace tc

@@ -51,7 +51,8 @@ def _check_cuda(*ts):
 
 def make_params(*, num_seqs, num_k_heads, num_v_heads, d, num_slots, total_tokens=0, chunk=64,
                 qkv_dtype=torch.bfloat16, state_dtype=torch.float32, per_channel=True,
-                scale=0.0, l2norm=True, checked=False, cuda_cores=False, q_row_stride=0,
+                scale=0.0, l2norm=True, checked=False, cuda_cores=False, compact=False,
+                q_row_stride=0,
                 k_row_stride=0, v_row_stride=0) -> KdaParams:
     return KdaParams(num_seqs=num_seqs, num_k_heads=num_k_heads, num_v_heads=num_v_heads, d_k=d,
                      d_v=d, num_slots=num_slots, total_tokens=total_tokens, chunk=chunk,
@@ -60,7 +61,8 @@ def make_params(*, num_seqs, num_k_heads, num_v_heads, d, num_slots, total_token
                                  else _lib.KDA_DECAY_SCALAR),
                      scale=float(scale), l2norm_qk=int(bool(l2norm)),
                      flags=((_lib.KDA_FLAG_CHECKED if checked else 0)
-                            | (_lib.KDA_FLAG_CUDA_CORES if cuda_cores else 0)),
+                            | (_lib.KDA_FLAG_CUDA_CORES if cuda_cores else 0)
+                            | (_lib.KDA_FLAG_COMPACT if compact else 0)),
                      q_row_stride=q_row_stride,
                      k_row_stride=k_row_stride, v_row_stride=v_row_stride)
 
@@ -82,7 +84,7 @@ def uses_tensor_cores(params: KdaParams) -> bool:
 
 
 def _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
-                    scale, l2norm, checked, cuda_cores=False):
+                    scale, l2norm, checked, cuda_cores=False, compact=False):
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:
         raise ValueError("q, k must be [T, HK, D] and v [T, HV, D]")
     T, HK, D = q.shape
@@ -116,7 +118,7 @@ def _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state
                        num_slots=state_pool.shape[0], total_tokens=T, chunk=chunk,
                        qkv_dtype=q.dtype, state_dtype=state_pool.dtype, per_channel=per_channel,
                        scale=scale, l2norm=l2norm, checked=checked, cuda_cores=cuda_cores,
-                       q_row_stride=_row_stride(q, "q"), k_row_stride=_row_stride(k, "k"),
+                       compact=compact, q_row_stride=_row_stride(q, "q"), k_row_stride=_row_stride(k, "k"),
                        v_row_stride=_row_stride(v, "v"))
 
 
@@ -124,16 +126,17 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tenso
             log_decay: torch.Tensor, input_row_offsets: torch.Tensor, slot_idx: torch.Tensor,
             state_pool: torch.Tensor, *, chunk: int = 64, scale: float = 0.0,
             l2norm: bool = True, checked: bool = False, cuda_cores: bool = False,
-            out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+            compact: bool = False, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Chunkwise gated-delta-rule prefill (kda_prefill_fwd).  Returns o [T, HV, D] fp32.
 
     The pool slots named by slot_idx are updated in place with each sequence's final state.
-    `cuda_cores=True` asks for the fp32 CUDA-core path where the tensor-core path applies.
+    `cuda_cores=True` asks for the fp32 CUDA-core path where the tensor-core path applies;
+    `compact=True` runs the tensor-core path as a single kernel with a small workspace.
     """
     dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool)
     p = _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
-                        scale, l2norm, checked, cuda_cores)
+                        scale, l2norm, checked, cuda_cores, compact)
     T, HV, D = v.shape
     if out is None:
         out = torch.empty((T, HV, D), dtype=torch.float32, device=dev)

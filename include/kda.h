@@ -82,6 +82,15 @@ typedef enum kda_decay_kind {
  * (bf16 q/k/v, d = 128, chunk 64, whose operands are fp16/bf16 with fp32
  * accumulation).  fp32 q/k/v and the other head sizes and chunks always use it. */
 #define KDA_FLAG_CUDA_CORES 2u
+/* Tensor-core path only: run it as one kernel per (sequence, value head, value
+ * tile) that walks the sequence's chunks, with only the chunk table as workspace
+ * (16 bytes per chunk).  Without it the path runs as two kernels: a chunk-parallel
+ * one that writes every chunk's operands of the state recurrence to the workspace
+ * (66,048 bytes per chunk and value head) and a sequential one over each
+ * sequence's chunks, which keeps the chunk-local work off the sequential path.
+ * The two forms round the same operands the same way; their results agree to
+ * the tolerance, not bit for bit. */
+#define KDA_FLAG_COMPACT 4u
 
 /* Device error codes (kda_get_device_error). */
 #define KDA_DEVERR_NONE 0

@@ -185,3 +185,17 @@ def test_verify_and_fold_reject_bad_arguments_before_launch(lib):
                                  None) == _lib.KDA_OK
     assert lib.kda_fold_accepted(ctypes.byref(empty), None, 4, None, None, None, None) == \
         _lib.KDA_OK
+
+
+def test_compact_flag_shrinks_the_tensor_core_workspace(lib):
+    """The two-kernel tensor-core form stores 66,048 bytes of chain operands per chunk
+    and value head; the single-kernel form needs only the chunk table."""
+    p = good(total_tokens=4096, num_seqs=2)
+    c = good(total_tokens=4096, num_seqs=2, compact=True)
+    assert lib.kda_prefill_uses_tensor_cores(ctypes.byref(c)) == 1
+    full, small = ws_status(lib, p)[1], ws_status(lib, c)[1]
+    assert full - small >= (4096 // 64) * 8 * 66048
+    assert small < 64 * 1024
+    q = good()
+    q.flags |= 8                                            # an unknown flag
+    assert ws_status(lib, q)[0] == _lib.KDA_ERR_INVALID_ARG

@@ -320,3 +320,20 @@ def test_scalar_decay_anchored_and_exact_pair_paths(factor):
     p = small("scalar-decay", [200, 64, 33], 2, 2, 128, "bf16", "f32", "scalar", 64, seed=53)
     p.g[:] = (p.g * factor).astype(np.float32)
     check_prefill(p)
+
+
+@pytest.mark.parametrize("decay", ["scalar", "per_channel"])
+@pytest.mark.parametrize("state", ["f32", "bf16"])
+def test_compact_and_two_kernel_tensor_core_paths_agree(decay, state):
+    """The two-kernel tensor-core path (default) and its single-kernel form
+    (compact=True) agree to the tolerance and each matches the oracle, on ragged
+    lengths around the chunk size, with GQA and shuffled slots."""
+    p = small("split-vs-compact", [1, 63, 64, 65, 190, 128, 257], 2, 4, 128, "bf16", state, decay,
+              64, seed=61 if decay == "scalar" else 62, slots=10)
+    o_sp, s_sp, _ = gpu_prefill(p)
+    o_cp, s_cp, _ = gpu_prefill(p, compact=True)
+    o_ref, pool_ref = oracle.run(p)
+    tol = TOL["bf16"]
+    assert rel_err(o_sp, o_cp) <= tol
+    assert rel_err(o_sp, o_ref) <= tol and rel_err(o_cp, o_ref) <= tol
+    assert state_err(p, s_sp, pool_ref) <= tol and state_err(p, s_cp, pool_ref) <= tol

@@ -12,18 +12,23 @@
 //
 //   A1  = [TB; A_qk TB]                 128 x 64   fp16
 //   A2  = [-W; Q~ - A_qk W]             128 x 128  fp16
-//   KET = K_end^T                       128 x 64   fp16
+//   KE  = K_end (token rows)            64 x 128   fp16
 //   gam = exp(G_last) per key channel   128        fp32
 //
-// already in the no-swizzle K-major core-matrix order in which the tensor core reads
-// them from shared memory, so the chain kernel moves a chunk's record with one bulk
-// copy.  The chain kernel keeps a (sequence, value head, 64 value columns) slice of
-// the state in registers and per chunk issues two MMAs,
+// A1 and A2 are stored per thread of the chain kernel (each thread's 16-byte pieces of
+// its row, interleaved across threads so that every warp access is contiguous): the
+// chain kernel loads them into registers and writes them to tensor memory, where the
+// MMA reads its A operand, so they never pass through shared memory.  KE is stored in
+// the MN-major core-matrix order of an A operand and moved with one bulk copy.  The
+// chain kernel keeps a (sequence, value head, 64 value columns) slice of the state in
+// registers and per chunk issues two MMAs,
 //
-//   [E; O] = A1 V + A2 S              M=128 N=64 K=64+128
-//   S     <- diag(gam) S + KET E      M=128 N=64 K=64
+//   [E; O] = A1 V + A2 S              M=128 N=64 K=64+128   (A from tensor memory)
+//   S     <- diag(gam) S + KE^T E     M=128 N=64 K=64
 //
-// while the next chunk's record and values are being fetched.  The front work is done
+// while the next chunk's operands and values are being fetched.  Every operand the
+// threads produce (V, S, E, and in the front kernel TB and K~) is stored MN-major, so
+// each thread writes whole 16-byte rows of core matrices instead of transposing.  The front work is done
 // once per (chunk, value head) rather than once per value tile, and none of it sits
 // on the sequential path.
 //
@@ -45,12 +50,19 @@ constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr float kMaxHalfChunkDecay = 80.0f;
 
 // record of one (chunk, value head) in the workspace
-constexpr uint32_t REC_A1 = 0;
-constexpr uint32_t REC_A2 = REC_A1 + 128 * 64 * 2;
-constexpr uint32_t REC_KET = REC_A2 + 128 * 128 * 2;
-constexpr uint32_t REC_GAM = REC_KET + 128 * 64 * 2;
+//   BLOB: piece p (0..11) of thread t at (p * NT + t) * 16; thread t (row r, column half h)
+//         holds A1[r][32h .. 32h+32) in pieces 0-3 and A2[r][64h .. 64h+64) in pieces 4-11
+//   KE:   K_end, element (token m, channel c) at mn_offset(m, c, KE_LBO, KE_SBO)
+constexpr uint32_t BLOB_PIECES = 12;
+constexpr uint32_t REC_BLOB = 0;
+constexpr uint32_t REC_KE = REC_BLOB + BLOB_PIECES * 256 * 16;
+constexpr uint32_t REC_GAM = REC_KE + 64 * 128 * 2;
 constexpr uint32_t REC_BYTES = REC_GAM + 128 * 4;    // 66048, a multiple of 16
-static_assert(REC_BYTES % 16 == 0, "records must stay 16-byte aligned");
+constexpr uint32_t REC_TAIL = REC_BYTES - REC_KE;    // KE and gamma, bulk-copied
+constexpr uint32_t KE_LBO = 2048, KE_SBO = 128;      // MN-major: 16 channel groups per token group
+constexpr uint32_t KT_LBO = 2048, KT_SBO = 128;      // K~ (N = channel, K = token), same order
+constexpr uint32_t TB_LBO = 1024, TB_SBO = 128;      // TB (N = column j, K = row m)
+static_assert(REC_BYTES % 16 == 0 && REC_KE % 16 == 0, "records must stay 16-byte aligned");
 
 // per-chunk vectors of the front kernel (byte offsets inside its SMALL area)
 constexpr uint32_t O_GS = 0, O_BETA = 256, O_RK = 512, O_RQ = 768, O_EG = 1024, O_EGL = 1280,
@@ -73,7 +85,7 @@ struct FrontMap<false> {
   static constexpr uint32_t SMALL = AK + 16 * AK_SBO;
   static constexpr uint32_t R2 = SMALL + SMALL_BYTES;   // solve, then K~^T and A1
   static constexpr uint32_t LMAT = R2 + SOL_BYTES;      // [I; A_qk] 128 x 64 fp16
-  static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;  // TB^T 64 x 64 fp16
+  static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;  // TB 64 x 64 fp16, MN-major
   static constexpr uint32_t BYTES = TBT + 64 * 64 * 2;
 };
 
@@ -101,22 +113,24 @@ struct FrontMap<true> {
 // it is consumed by the A-GEMM before Y is produced)
 constexpr uint32_t F_A = 0, F_X = 64, F_Y = 128, F_ALO = 128, F_COLS = 256;
 
-// chain shared memory
-constexpr int VS = BV + 8;                               // raw v row (bf16), 144 B
-constexpr uint32_t LBO_P = 144;                          // padded leading offset of S^T, E^T
-constexpr uint32_t ST_SBO = (D / 8) * LBO_P;
-constexpr uint32_t ET_SBO = (C / 8) * LBO_P;
+// chain shared memory (MN-major operands: core matrices of 8 K-rows x 8 value columns,
+// value-column groups adjacent, K groups 1024 bytes apart)
+constexpr uint32_t OP_LBO = 1024, OP_SBO = 128;
 constexpr int OS = BV + 4;                               // o staging row (fp32)
-constexpr uint32_t CH_BUF0 = 0, CH_BUF1 = REC_BYTES;     // two chunk records
-constexpr uint32_t CH_VSTG = 2 * REC_BYTES;              // raw v of the next chunk [64][VS]
-constexpr uint32_t CH_VT = CH_VSTG + C * VS * 2;         // V^T 64 x 64 fp16
-constexpr uint32_t CH_ST = CH_VT + 64 * 64 * 2;          // S^T 64 x 128 fp16, padded
-constexpr uint32_t CH_ET = CH_ST + (BV / 8) * ST_SBO;    // E^T 64 x 64 fp16, padded
-constexpr uint32_t CH_OST = CH_ET + (BV / 8) * ET_SBO;   // o rows fp32 [64][OS]
+constexpr uint32_t CH_KE = 0;                            // KE and gamma of two chunks
+constexpr uint32_t CH_V = 2 * REC_TAIL;                  // V of two chunks, 64 x 64 (bf16 -> fp16)
+constexpr uint32_t V_BYTES = 64 * 64 * 2;
+constexpr uint32_t CH_ST = CH_V + 2 * V_BYTES;           // S 128 x 64 fp16
+constexpr uint32_t CH_ET = CH_ST + 128 * 64 * 2;         // E 64 x 64 fp16
+constexpr uint32_t CH_OST = CH_ET + 64 * 64 * 2;         // o rows fp32 [64][OS]
 constexpr uint32_t CH_BYTES = CH_OST + C * OS * 4;
 static_assert(CH_BYTES + 64 <= 227 * 1024, "chain shared memory budget");
 static_assert(FrontMap<true>::BYTES + 64 <= 227 * 1024, "front shared memory budget");
-constexpr uint32_t T_D1 = 0, T_D2 = 64, CH_COLS = 128;
+static_assert(CH_V % 128 == 0 && CH_ST % 128 == 0, "operand alignment");
+// chain TMEM columns: A1 | A2 of two chunks (fp16 pairs), [E; O] of two chunks (the next
+// chunk's A1 V is accumulated early), dS
+constexpr uint32_t T_A = 0, A_COLS = 96, T_D1 = 256, T_D2 = 320, CH_COLS = 512;
+__host__ __device__ constexpr uint32_t d1_col(uint32_t c) { return (c & 1) ? 384 : T_D1; }
 
 __device__ __forceinline__ uint4 f16x8_pack(const float* x) {
   return make_uint4(tc::pack_f16x2(x[0], x[1]), tc::pack_f16x2(x[2], x[3]),
@@ -204,7 +218,9 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   float* sA = reinterpret_cast<float*>(smem + M::R2);
   float* sT = reinterpret_cast<float*>(smem + M::R2 + C * SP * 4);
   float* sX = reinterpret_cast<float*>(smem + M::R2 + 2 * C * SP * 4);
-  constexpr uint32_t KTT = M::R2, A1 = M::R2 + 128 * 64 * 2;
+  constexpr uint32_t KTT = M::R2, A1 = M::R2 + 128 * 64 * 2;    // K~ (MN-major), A1 (K-major)
+  const int64_t bt = (static_cast<int64_t>(gc) * HV + h) * static_cast<int64_t>(REC_BYTES);
+  uint4* blob = reinterpret_cast<uint4*>(records + bt + REC_BLOB) + tid;  // piece p at [p * NT]
 
   front_issue_loads<PERCH>(P, smem, t0, n, kh, h, tid);
   if (warp == 0) {
@@ -414,22 +430,24 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   if (tid == 0) {
     const uint32_t id = tc::idesc_f16(128, 64, tc::kBF16);
     if constexpr (PERCH) {
-      const uint32_t ak = tc::smem_u32(smem + M::AK), bk = tc::smem_u32(smem + M::BK),
-                     bl = tc::smem_u32(smem + M::BKLO);
+      const uint64_t dak = tc::smem_desc(tc::smem_u32(smem + M::AK), 128, tc::dense_sbo(D));
+      const uint64_t dbk = tc::smem_desc(tc::smem_u32(smem + M::BK), 128, tc::dense_sbo(D));
+      const uint64_t dbl = tc::smem_desc(tc::smem_u32(smem + M::BKLO), 128, tc::dense_sbo(D));
+#pragma unroll
       for (int s = 0; s < D / 16; ++s)          // hi x hi
-        tc::mma_ss(tmem + F_A, tc::smem_desc(ak + s * 256, 128, tc::dense_sbo(D)),
-                   tc::smem_desc(bk + s * 256, 128, tc::dense_sbo(D)), id, s > 0);
+        tc::mma_ss(tmem + F_A, tc::desc_add(dak, s * 256), tc::desc_add(dbk, s * 256), id, s > 0);
+#pragma unroll
       for (int s = 0; s < D / 16; ++s)          // hi x lo
-        tc::mma_ss(tmem + F_A, tc::smem_desc(ak + s * 256, 128, tc::dense_sbo(D)),
-                   tc::smem_desc(bl + s * 256, 128, tc::dense_sbo(D)), id, 1);
+        tc::mma_ss(tmem + F_A, tc::desc_add(dak, s * 256), tc::desc_add(dbl, s * 256), id, 1);
+#pragma unroll
       for (int s = 0; s < D / 16; ++s)          // lo x hi (low half from TMEM)
-        tc::mma_ts(tmem + F_A, tmem + F_ALO + s * 8,
-                   tc::smem_desc(bk + s * 256, 128, tc::dense_sbo(D)), id, 1);
+        tc::mma_ts(tmem + F_A, tmem + F_ALO + s * 8, tc::desc_add(dbk, s * 256), id, 1);
     } else {
-      const uint32_t ak = tc::smem_u32(smem + M::AK);
+      const uint64_t dak = tc::smem_desc(tc::smem_u32(smem + M::AK), M::AK_LBO, M::AK_SBO);
+#pragma unroll
       for (int s = 0; s < D / 16; ++s)          // [K; Q] K^T on the raw rows
-        tc::mma_ss(tmem + F_A, tc::smem_desc(ak + s * 2 * M::AK_LBO, M::AK_LBO, M::AK_SBO),
-                   tc::smem_desc(ak + s * 2 * M::AK_LBO, M::AK_LBO, M::AK_SBO), id, s > 0);
+        tc::mma_ss(tmem + F_A, tc::desc_add(dak, s * 2 * M::AK_LBO), tc::desc_add(dak, s * 2 * M::AK_LBO),
+                   id, s > 0);
     }
     tc::mma_commit(&s_bar);
   }
@@ -492,6 +510,32 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   __syncthreads();
 
   // ------------------------------------------------------------------ solve
+  // K_end = k^ exp(G_last - G_m) needs no solve: warps 2-7 write it to the record (row
+  // pieces of 8 channels, MN-major order) while warps 0-1 invert the diagonal blocks
+  if (warp >= 2) {
+    for (int u = tid - 64; u < C * (D / 8); u += NT - 64) {
+      const int m = (u >> 7) * 8 + (u & 7), c0 = ((u >> 3) & 15) * 8;
+      float kx[8], ke[8];
+      tc::bf16x8_load(kq_piece(false, m, c0), kx);
+      const float rk = sRK[m];
+      if constexpr (PERCH) {
+        const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
+        const float4 e0 = *reinterpret_cast<const float4*>(sG + m * M::GS + c0);
+        const float4 e1 = *reinterpret_cast<const float4*>(sG + m * M::GS + c0 + 4);
+        const float4 l0 = *reinterpret_cast<const float4*>(sG + (C - 1) * M::GS + c0);
+        const float4 l1 = *reinterpret_cast<const float4*>(sG + (C - 1) * M::GS + c0 + 4);
+        const float Em[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        const float El[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ke[e] = kx[e] * rk * __fdividef(El[e], Em[e]);
+      } else {
+        const float fe = rk * sEGL[m];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ke[e] = kx[e] * fe;
+      }
+      *reinterpret_cast<uint4*>(rec + REC_KE + tc::mn_offset(m, c0, KE_LBO, KE_SBO)) = f16x8_pack(ke);
+    }
+  }
   if (warp < 2) {                               // diagonal 16x16 blocks, one column per lane
     const int base = (warp * 2 + (lane >> 4)) * 16, col = lane & 15;
     float t[16];
@@ -576,16 +620,18 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     *reinterpret_cast<float4*>(sT + (32 + r) * SP + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
-  for (int u = tid; u < C * (C / 8); u += NT) { // TB^T[j][m] = T[m][j] beta_j
-    const int j = u % C, m8 = u / C;
-    const float bj = sBeta[j];
+  for (int u = tid; u < C * (C / 8); u += NT) { // TB[m][j] = T[m][j] beta_j, row pieces
+    const int m = (u >> 6) * 8 + (u & 7), j0 = ((u >> 3) & 7) * 8;
+    const float4 t0 = *reinterpret_cast<const float4*>(sT + m * SP + j0);
+    const float4 t1 = *reinterpret_cast<const float4*>(sT + m * SP + j0 + 4);
+    const float4 b0 = *reinterpret_cast<const float4*>(sBeta + j0);
+    const float4 b1 = *reinterpret_cast<const float4*>(sBeta + j0 + 4);
+    const float tv[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
+                         t1.x * b1.x, t1.y * b1.y, t1.z * b1.z, t1.w * b1.w};
     float x[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int m = m8 * 8 + e;
-      x[e] = m >= j ? sT[m * SP + j] * bj : 0.f;
-    }
-    tc::f16x8_store(smem, M::TBT + tc::cm_offset(j, m8 * 8, 128, tc::dense_sbo(64)), x);
+    for (int e = 0; e < 8; ++e) x[e] = j0 + e <= m ? tv[e] : 0.f;   // T is lower triangular
+    tc::f16x8_store(smem, M::TBT + tc::mn_offset(m, j0, TB_LBO, TB_SBO), x);
   }
   tc::fence_async_smem();
   tc::fence_before_sync();
@@ -594,39 +640,37 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
 
   // ------------------------------------------------------------------ X = [I; A_qk] TB
   if (tid == 0) {
-    const uint32_t id = tc::idesc_f16(128, 64, tc::kF16);
+    const uint32_t id = tc::idesc_f16(128, 64, tc::kF16, false, false, true);
+    const uint64_t dl = tc::smem_desc(tc::smem_u32(smem + M::LMAT), 128, tc::dense_sbo(64));
+    const uint64_t dt = tc::smem_desc(tc::smem_u32(smem + M::TBT), TB_LBO, TB_SBO);
+#pragma unroll
     for (int s = 0; s < C / 16; ++s)
-      tc::mma_ss(tmem + F_X, tc::smem_desc(tc::smem_u32(smem + M::LMAT) + s * 256, 128, tc::dense_sbo(64)),
-                 tc::smem_desc(tc::smem_u32(smem + M::TBT) + s * 256, 128, tc::dense_sbo(64)), id, s > 0);
+      tc::mma_ss(tmem + F_X, tc::desc_add(dl, s * 256), tc::desc_add(dt, s * 2 * TB_LBO), id, s > 0);
     tc::mma_commit(&s_bar);
   }
-  // K~^T (smem, the Y operand), K_end^T and gamma (the record); the solve area is free
-  for (int u = tid; u < D * (C / 8); u += NT) { // (channel c, 8 tokens)
-    const int c = u % D, m8 = u / D;
-    float kt[8], ke[8];
+  // K~ = k^ exp(G_m) (smem, the Y operand) as row pieces of 8 channels in the MN-major
+  // order; the solve area is free
+  for (int u = tid; u < C * (D / 8); u += NT) {
+    const int m = (u >> 7) * 8 + (u & 7), c0 = ((u >> 3) & 15) * 8;
+    float kx[8], kt[8];
+    tc::bf16x8_load(kq_piece(false, m, c0), kx);
+    const float rk = sRK[m];
     if constexpr (PERCH) {
       const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
-      const float El = sG[(C - 1) * M::GS + c], ea = sGA[c];
+      const float4 e0 = *reinterpret_cast<const float4*>(sG + m * M::GS + c0);
+      const float4 e1 = *reinterpret_cast<const float4*>(sG + m * M::GS + c0 + 4);
+      const float4 a0 = *reinterpret_cast<const float4*>(sGA + c0);
+      const float4 a1 = *reinterpret_cast<const float4*>(sGA + c0 + 4);
+      const float Em[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+      const float ea[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int m = m8 * 8 + e;
-        const float Em = sG[m * M::GS + c];
-        const float kx = k_raw(m, c) * sRK[m];
-        kt[e] = kx * Em * ea;                   // k^ exp(G_m)
-        ke[e] = kx * __fdividef(El, Em);        // k^ exp(G_last - G_m)
-      }
+      for (int e = 0; e < 8; ++e) kt[e] = kx[e] * rk * Em[e] * ea[e];
     } else {
+      const float ft = rk * sEG[m];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int m = m8 * 8 + e;
-        const float kx = k_raw(m, c) * sRK[m];
-        kt[e] = kx * sEG[m];
-        ke[e] = kx * sEGL[m];
-      }
+      for (int e = 0; e < 8; ++e) kt[e] = kx[e] * ft;
     }
-    tc::f16x8_store(smem, KTT + tc::cm_offset(c, m8 * 8, 128, tc::dense_sbo(64)), kt);
-    *reinterpret_cast<uint4*>(rec + REC_KET + tc::cm_offset(c, m8 * 8, 128, tc::dense_sbo(64))) =
-        f16x8_pack(ke);
+    tc::f16x8_store(smem, KTT + tc::mn_offset(m, c0, KT_LBO, KT_SBO), kt);
   }
   if (tid < D) reinterpret_cast<float*>(rec + REC_GAM)[tid] = sGam[tid];
   tc::fence_async_smem();
@@ -646,10 +690,9 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     }
 #pragma unroll
     for (int g8 = 0; g8 < 4; ++g8) {
-      const uint32_t off = tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64));
       const uint4 v = f16x8_pack(x + 8 * g8);
-      *reinterpret_cast<uint4*>(smem + A1 + off) = v;
-      *reinterpret_cast<uint4*>(rec + REC_A1 + off) = v;
+      *reinterpret_cast<uint4*>(smem + A1 + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64))) = v;
+      blob[g8 * NT] = v;                        // pieces 0-3
     }
   }
   tc::fence_async_smem();
@@ -659,10 +702,12 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
 
   // ------------------------------------------------------------------ Y = A1 K~
   if (tid == 0) {
-    const uint32_t id = tc::idesc_f16(128, 128, tc::kF16);
+    const uint32_t id = tc::idesc_f16(128, 128, tc::kF16, false, false, true);
+    const uint64_t da = tc::smem_desc(tc::smem_u32(smem + A1), 128, tc::dense_sbo(64));
+    const uint64_t dk = tc::smem_desc(tc::smem_u32(smem + KTT), KT_LBO, KT_SBO);
+#pragma unroll
     for (int s = 0; s < C / 16; ++s)
-      tc::mma_ss(tmem + F_Y, tc::smem_desc(tc::smem_u32(smem + A1) + s * 256, 128, tc::dense_sbo(64)),
-                 tc::smem_desc(tc::smem_u32(smem + KTT) + s * 256, 128, tc::dense_sbo(64)), id, s > 0);
+      tc::mma_ss(tmem + F_Y, tc::desc_add(da, s * 256), tc::desc_add(dk, s * 2 * KT_LBO), id, s > 0);
     tc::mma_commit(&s_bar);
   }
   mma_wait();
@@ -716,9 +761,7 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
 #pragma unroll
       for (int e = 0; e < 32; ++e) x[e] -= __uint_as_float(ry[half][e]);
 #pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8)
-        *reinterpret_cast<uint4*>(rec + REC_A2 + tc::cm_offset(row, c0 + 8 * g8, 128, tc::dense_sbo(D))) =
-            f16x8_pack(x + 8 * g8);
+      for (int g8 = 0; g8 < 4; ++g8) blob[(4 + 4 * half + g8) * NT] = f16x8_pack(x + 8 * g8);   // 4-11
     }
   }
 
@@ -734,13 +777,17 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
 }
 
 // One CTA per (sequence, value head, 64 value columns): the state slice in registers,
-// two MMAs per chunk on the chunk's record, the next record and values in flight.
+// two MMAs per chunk.  Off the sequential path: the next chunk's A1/A2 pieces are loaded
+// into registers and written to tensor memory, its KE and values are fetched (values two
+// chunks ahead), and the previous chunk's o rows are stored while this chunk's first MMA
+// runs.
 template <bool SBF16>
 __global__ void __launch_bounds__(tcs::NT, 1)
     tc_chain_kernel(Problem P, PlanView plan, const unsigned char* records) {
   using namespace tcs;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ uint64_t s_mma_bar;
+  __shared__ uint64_t s_a1v_bar;                // A1 V of a chunk, issued by thread 32
   __shared__ uint64_t s_ld_bar[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -758,40 +805,64 @@ __global__ void __launch_bounds__(tcs::NT, 1)
   auto rec = [&](uint32_t c) -> const unsigned char* {
     return records + ((c0 + c) * HV + h) * static_cast<int64_t>(REC_BYTES);
   };
+  auto ke_off = [](uint32_t c) -> uint32_t { return CH_KE + (c & 1) * REC_TAIL; };
   auto chunk_n = [&](uint32_t c) -> int {
     const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
     return static_cast<int>(min(static_cast<int64_t>(C), static_cast<int64_t>(eos) - t0));
   };
-  auto issue_v = [&](uint32_t c) {              // raw v tile of chunk c -> VSTG
+  // raw bf16 v of chunk c straight into the MN-major positions of V[c & 1]
+  auto issue_v = [&](uint32_t c) {
     const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
     const int n = chunk_n(c);
+    const uint32_t dst = sb + CH_V + (c & 1) * V_BYTES;
     for (int u = tid; u < C * (BV / 8); u += NT) {
-      const int i = u / (BV / 8), q8 = u % (BV / 8);
-      const bool live = i < n;
-      const int64_t t = live ? t0 + i : t0;
-      tc::cp_async16(sb + CH_VSTG + (i * VS + q8 * 8) * 2,
-                     static_cast<const uint16_t*>(P.v) + t * P.v_stride + static_cast<int64_t>(h) * D + vt * BV + q8 * 8,
+      const int m = (u >> 6) * 8 + (u & 7), j0 = ((u >> 3) & 7) * 8;
+      const bool live = m < n;
+      const int64_t t = live ? t0 + m : t0;
+      tc::cp_async16(dst + tc::mn_offset(m, j0, OP_LBO, OP_SBO),
+                     static_cast<const uint16_t*>(P.v) + t * P.v_stride + static_cast<int64_t>(h) * D + vt * BV + j0,
                      live ? 16u : 0u);
     }
     tc::cp_async_commit();
   };
-  auto build_vt = [&]() {                       // V^T fp16 (N = value column, K = token)
-    for (int u = tid; u < BV * (C / 8); u += NT) {
-      const int j = u % BV, m8 = u / BV;
+  auto convert_v = [&](uint32_t c) {            // bf16 -> fp16 in place (16-byte pieces)
+    uint4* p = reinterpret_cast<uint4*>(smem + CH_V + (c & 1) * V_BYTES);
+    for (int u = tid; u < static_cast<int>(V_BYTES / 16); u += NT) {
       float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = tc::bf16_at(smem, CH_VSTG, (m8 * 8 + e) * VS + j);
-      tc::f16x8_store(smem, CH_VT + tc::cm_offset(j, m8 * 8, 128, tc::dense_sbo(64)), x);
+      tc::bf16x8_load(reinterpret_cast<const unsigned char*>(p + u), x);
+      p[u] = f16x8_pack(x);
     }
+  };
+  auto store_o = [&](uint32_t c) {              // o rows of chunk c staged in OST
+    const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
+    const int n = chunk_n(c);
+#pragma unroll
+    for (int k = 0; k < (C * BV / 4) / NT; ++k) {
+      const int idx = tid + k * NT, i = idx / (BV / 4), q = idx % (BV / 4);
+      if (i < n)
+        *reinterpret_cast<float4*>(P.o + ((t0 + i) * HV + h) * D + vt * BV + q * 4) =
+            *reinterpret_cast<const float4*>(smem + CH_OST + (i * OS + q * 4) * 4);
+    }
+  };
+  // this thread's 12 pieces of a chunk's A1 | A2 (coalesced: piece p of all threads is
+  // one contiguous 4 KB run)
+  uint4 ablob[BLOB_PIECES];
+  auto load_blob = [&](uint32_t c) {
+    const uint4* src = reinterpret_cast<const uint4*>(rec(c) + REC_BLOB) + tid;
+#pragma unroll
+    for (int p = 0; p < static_cast<int>(BLOB_PIECES); ++p) ablob[p] = __ldg(src + p * NT);
   };
 
   issue_v(0);
+  if (nchunks > 1) issue_v(1);
+  load_blob(0);
   if (warp == 0) {
     tc::tmem_alloc(&s_tmem, CH_COLS);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
     tc::mbar_init(&s_mma_bar, 1);
+    tc::mbar_init(&s_a1v_bar, 1);
     tc::mbar_init(&s_ld_bar[0], 1);
     tc::mbar_init(&s_ld_bar[1], 1);
     tc::fence_mbar_init();
@@ -801,16 +872,36 @@ __global__ void __launch_bounds__(tcs::NT, 1)
   __syncthreads();
   tc::fence_after_sync();
   if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&s_ld_bar[0], REC_BYTES);
-    tc::bulk_load(sb + CH_BUF0, rec(0), REC_BYTES, &s_ld_bar[0]);
+    tc::mbar_arrive_expect_tx(&s_ld_bar[0], REC_TAIL);
+    tc::bulk_load(sb + ke_off(0), rec(0) + REC_KE, REC_TAIL, &s_ld_bar[0]);
   }
   const uint32_t tmem = s_tmem;
   const int row = 32 * (warp & 3) + lane;       // TMEM lane = key channel (state row)
   const int chalf = warp >> 2;
   const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  // row `row`, K columns of this thread's half: A1 -> 16 columns, A2 -> 32 columns
+  auto store_blob = [&](uint32_t c) {
+    const uint32_t base = tmem + lane_addr + T_A + (c & 1) * A_COLS;
+    uint32_t w[16];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      w[4 * p] = ablob[p].x; w[4 * p + 1] = ablob[p].y; w[4 * p + 2] = ablob[p].z; w[4 * p + 3] = ablob[p].w;
+    }
+    tc::tmem_st16(base + 16 * chalf, w);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const uint4 v = ablob[4 + 4 * half + p];
+        w[4 * p] = v.x; w[4 * p + 1] = v.y; w[4 * p + 2] = v.z; w[4 * p + 3] = v.w;
+      }
+      tc::tmem_st16(base + 32 + 32 * chalf + 16 * half, w);
+    }
+    tc::tmem_wait_st();
+  };
 
-  // S[row][32 chalf + j] of this CTA's value tile, fp32 in registers; its fp16 copy S^T
-  // (N = value column, K = key channel) is the first MMA's B operand
+  // S[row][32 chalf + j] of this CTA's value tile, fp32 in registers; its fp16 copy
+  // (N = value column, K = key channel, MN-major) is the first MMA's B operand
   float Sv[32];
   {
     const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
@@ -821,21 +912,41 @@ __global__ void __launch_bounds__(tcs::NT, 1)
   }
   auto write_state_operand = [&]() {
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      *reinterpret_cast<uint16_t*>(smem + CH_ST + tc::cm_offset(32 * chalf + j, row, LBO_P, ST_SBO)) =
-          tc::f16_bits(Sv[j]);
+    for (int p = 0; p < 4; ++p)
+      *reinterpret_cast<uint4*>(smem + CH_ST + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
+          f16x8_pack(Sv + 8 * p);
   };
   write_state_operand();
-  tc::cp_async_wait_all();
+  store_blob(0);
+  if (nchunks > 1) load_blob(1);
+  if (nchunks > 1) tc::cp_async_wait_one(); else tc::cp_async_wait_all();
   __syncthreads();
-  build_vt();
+  convert_v(0);
   tc::fence_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
 
+  const uint32_t id1 = tc::idesc_f16(128, BV, tc::kF16, false, false, true);
+  const uint32_t id2 = tc::idesc_f16(128, BV, tc::kF16, false, true, true);
+  // operand descriptors, advanced by constant offsets per K step
+  const uint64_t dST = tc::smem_desc(sb + CH_ST, OP_LBO, OP_SBO);
+  const uint64_t dET = tc::smem_desc(sb + CH_ET, OP_LBO, OP_SBO);
+  const uint64_t dV0 = tc::smem_desc(sb + CH_V, OP_LBO, OP_SBO);
+  const uint64_t dKE0 = tc::smem_desc(sb + CH_KE, KE_LBO, KE_SBO);
+  // the state-independent part A1 V of chunk c's first MMA, issued by thread 32 and
+  // committed to its own barrier, which thread 0 waits on before accumulating onto it
+  auto issue_a1v = [&](uint32_t c) {
+    const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
+    const uint64_t dv = tc::desc_add(dV0, (c & 1) * V_BYTES);
+#pragma unroll
+    for (int s = 0; s < C / 16; ++s)
+      tc::mma_ts(tmem + d1_col(c), ta + s * 8, tc::desc_add(dv, s * 2 * OP_LBO), id1, s > 0);
+    tc::mma_commit(&s_a1v_bar);
+  };
+  if (tid == 32) issue_a1v(0);
   uint32_t phase = 0;
-  int pending = 0;                              // chunk whose record load is in flight, or -1
+  int pending = 0;                              // chunk whose KE load is in flight, or -1
   auto mma_wait = [&]() {
     const bool ok = tc::mbar_wait_bounded(&s_mma_bar, phase & 1, kWaitLimit);
     phase ^= 1;
@@ -844,57 +955,53 @@ __global__ void __launch_bounds__(tcs::NT, 1)
   };
 
   for (uint32_t c = 0; c < nchunks; ++c) {
-    const uint32_t buf = c & 1;
-    const uint32_t boff = buf ? CH_BUF1 : CH_BUF0;
-    const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
-    const int n = chunk_n(c);
+    const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
+    const uint32_t d1 = d1_col(c);
     const bool more = c + 1 < nchunks;
-    if (!tc::mbar_wait_bounded(&s_ld_bar[buf], (c >> 1) & 1, kWaitLimit)) s_abort = 1;
+    if (!tc::mbar_wait_bounded(&s_ld_bar[c & 1], (c >> 1) & 1, kWaitLimit)) s_abort = 1;
     pending = -1;
 
-    // ---------------------------------------------------------------- [E; O] = A1 V + A2 S
+    // ---------------------------------------------------------------- [E; O] += A2 S
     if (tid == 0) {
-      const uint32_t id = tc::idesc_f16(128, BV, tc::kF16);
-      for (int s = 0; s < C / 16; ++s)
-        tc::mma_ss(tmem + T_D1, tc::smem_desc(sb + boff + REC_A1 + s * 256, 128, tc::dense_sbo(64)),
-                   tc::smem_desc(sb + CH_VT + s * 256, 128, tc::dense_sbo(64)), id, s > 0);
+      if (!tc::mbar_wait_bounded(&s_a1v_bar, c & 1, kWaitLimit)) s_abort = 1;
+      tc::fence_after_sync();
+#pragma unroll
       for (int s = 0; s < D / 16; ++s)
-        tc::mma_ss(tmem + T_D1, tc::smem_desc(sb + boff + REC_A2 + s * 256, 128, tc::dense_sbo(D)),
-                   tc::smem_desc(sb + CH_ST + s * 2 * LBO_P, LBO_P, ST_SBO), id, 1);
+        tc::mma_ts(tmem + d1, ta + 32 + s * 8, tc::desc_add(dST, s * 2 * OP_LBO), id1, 1);
       tc::mma_commit(&s_mma_bar);
-      if (more) {                               // the other buffer's record was consumed last chunk
-        tc::mbar_arrive_expect_tx(&s_ld_bar[buf ^ 1], REC_BYTES);
-        tc::bulk_load(sb + (buf ? CH_BUF0 : CH_BUF1), rec(c + 1), REC_BYTES, &s_ld_bar[buf ^ 1]);
+      if (more) {                               // chunk c - 1's KE in that buffer is consumed
+        tc::mbar_arrive_expect_tx(&s_ld_bar[(c + 1) & 1], REC_TAIL);
+        tc::bulk_load(sb + ke_off(c + 1), rec(c + 1) + REC_KE, REC_TAIL, &s_ld_bar[(c + 1) & 1]);
       }
     }
+    if (more) pending = static_cast<int>(c + 1);
+    if (c > 0) store_o(c - 1);                  // o rows of the previous chunk
     if (more) {
-      pending = static_cast<int>(c + 1);
-      issue_v(c + 1);
+      store_blob(c + 1);                        // its columns held chunk c - 1's operands
+      if (c + 2 < nchunks) load_blob(c + 2);
+      tc::cp_async_wait_all();                  // the next chunk's values (the only group)
     }
+    __syncthreads();                            // OST free, the next chunk's values landed
+    if (more) convert_v(c + 1);
     mma_wait();
 
-    // ---------------------------------------------------------------- E^T, o staging
+    // ---------------------------------------------------------------- E (critical), o rows
+    float x[32];
     {
       uint32_t r0[16], r1[16];
-      tc::tmem_ld16(tmem + lane_addr + T_D1 + 32 * chalf, r0);
-      tc::tmem_ld16(tmem + lane_addr + T_D1 + 32 * chalf + 16, r1);
+      tc::tmem_ld16(tmem + lane_addr + d1 + 32 * chalf, r0);
+      tc::tmem_ld16(tmem + lane_addr + d1 + 32 * chalf + 16, r1);
       tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        x[e] = __uint_as_float(r0[e]);
+        x[e + 16] = __uint_as_float(r1[e]);
+      }
       if (row < C) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e)
-          *reinterpret_cast<uint16_t*>(smem + CH_ET + tc::cm_offset(32 * chalf + e, row, LBO_P, ET_SBO)) =
-              tc::f16_bits(__uint_as_float(e < 16 ? r0[e] : r1[e - 16]));
-      } else {
-        float* op = reinterpret_cast<float*>(smem + CH_OST) + (row - C) * OS + 32 * chalf;
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          *reinterpret_cast<float4*>(op + e) =
-              make_float4(__uint_as_float(r0[e]), __uint_as_float(r0[e + 1]),
-                          __uint_as_float(r0[e + 2]), __uint_as_float(r0[e + 3]));
-          *reinterpret_cast<float4*>(op + 16 + e) =
-              make_float4(__uint_as_float(r1[e]), __uint_as_float(r1[e + 1]),
-                          __uint_as_float(r1[e + 2]), __uint_as_float(r1[e + 3]));
-        }
+        for (int p = 0; p < 4; ++p)
+          *reinterpret_cast<uint4*>(smem + CH_ET + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
+              f16x8_pack(x + 8 * p);
       }
     }
     tc::fence_async_smem();
@@ -904,25 +1011,21 @@ __global__ void __launch_bounds__(tcs::NT, 1)
 
     // ---------------------------------------------------------------- dS = K_end^T E
     if (tid == 0) {
-      const uint32_t id = tc::idesc_f16(128, BV, tc::kF16);
+      const uint64_t dke = tc::desc_add(dKE0, (c & 1) * REC_TAIL);
+#pragma unroll
       for (int s = 0; s < C / 16; ++s)
-        tc::mma_ss(tmem + T_D2, tc::smem_desc(sb + boff + REC_KET + s * 256, 128, tc::dense_sbo(64)),
-                   tc::smem_desc(sb + CH_ET + s * 2 * LBO_P, LBO_P, ET_SBO), id, s > 0);
+        tc::mma_ss(tmem + T_D2, tc::desc_add(dke, s * 2 * KE_LBO), tc::desc_add(dET, s * 2 * OP_LBO),
+                   id2, s > 0);
       tc::mma_commit(&s_mma_bar);
     }
-    // coalesced o stores: each warp instruction writes two whole 256-byte token rows
+    if (tid == 32 && more) issue_a1v(c + 1);    // its A1 and V are in place since the last barrier
+    if (row >= C) {                             // o rows, stored during the next chunk
+      float* op = reinterpret_cast<float*>(smem + CH_OST) + (row - C) * OS + 32 * chalf;
 #pragma unroll
-    for (int k = 0; k < (C * BV / 4) / NT; ++k) {
-      const int idx = tid + k * NT, i = idx / (BV / 4), q = idx % (BV / 4);
-      if (i < n)
-        *reinterpret_cast<float4*>(P.o + ((t0 + i) * HV + h) * D + vt * BV + q * 4) =
-            *reinterpret_cast<const float4*>(smem + CH_OST + (i * OS + q * 4) * 4);
+      for (int e = 0; e < 32; e += 4)
+        *reinterpret_cast<float4*>(op + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
     }
-    if (more) {                                 // V^T of the next chunk (this chunk's is consumed)
-      tc::cp_async_wait_all();
-      __syncthreads();
-      build_vt();
-    }
+    if (c + 2 < nchunks) issue_v(c + 2);        // into V[c & 1], which MMA1 of this chunk read
     mma_wait();
 
     // ---------------------------------------------------------------- S <- diag(gam) S + dS
@@ -931,7 +1034,7 @@ __global__ void __launch_bounds__(tcs::NT, 1)
       tc::tmem_ld16(tmem + lane_addr + T_D2 + 32 * chalf, r0);
       tc::tmem_ld16(tmem + lane_addr + T_D2 + 32 * chalf + 16, r1);
       tc::tmem_wait_ld();
-      const float gam = reinterpret_cast<const float*>(smem + boff + REC_GAM)[row];
+      const float gam = reinterpret_cast<const float*>(smem + ke_off(c) + (REC_GAM - REC_KE))[row];
 #pragma unroll
       for (int e = 0; e < 32; ++e) Sv[e] = gam * Sv[e] + __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
       write_state_operand();
@@ -947,9 +1050,11 @@ __global__ void __launch_bounds__(tcs::NT, 1)
   if (s_abort) {
     // let what is still in flight finish (bounded) before shared and tensor memory go away
     tc::mbar_wait_bounded(&s_mma_bar, (phase ^ 1) & 1, kWaitLimit);
+    for (uint32_t k = 0; k < 2; ++k) tc::mbar_wait_bounded(&s_a1v_bar, k, kWaitLimit);
     if (pending >= 0) tc::mbar_wait_bounded(&s_ld_bar[pending & 1], (pending >> 1) & 1, kWaitLimit);
     if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
   } else {
+    store_o(nchunks - 1);
     const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
 #pragma unroll
     for (int j = 0; j < 32; ++j) {

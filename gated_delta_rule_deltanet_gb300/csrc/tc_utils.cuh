@@ -26,6 +26,15 @@ __host__ __device__ __forceinline__ uint32_t cm_offset(uint32_t row, uint32_t k,
   return (row >> 3) * sbo + (k >> 3) * lbo + (row & 7) * 16 + (k & 7) * 2;
 }
 
+// MN-major (transposed) operand tiles, no swizzle: a core matrix is 8 K-rows of 16 bytes
+// (8 consecutive M or N elements each), 128 contiguous bytes; core matrices adjacent
+// along K are `lbo` bytes apart and along M/N `sbo` bytes apart (the same roles of the two
+// offsets as in the K-major layout).  Byte offset of element (k, mn):
+__host__ __device__ __forceinline__ uint32_t mn_offset(uint32_t k, uint32_t mn, uint32_t lbo,
+                                                        uint32_t sbo) {
+  return (k >> 3) * lbo + (mn >> 3) * sbo + (k & 7) * 16 + (mn & 7) * 2;
+}
+
 // ------------------------------------------------------------------ descriptors
 
 // Shared-memory matrix descriptor: start address, leading (K) and stride (8-row)
@@ -39,15 +48,21 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;                             // base offset 0, absolute-LBO off, layout 0 (no swizzle)
 }
 
+// The same descriptor with its start address advanced by `bytes` (a multiple of 16 that
+// keeps the address inside shared memory, so the 14-bit field cannot carry).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 enum : uint32_t { kF16 = 0, kBF16 = 1 };
 
-// Instruction descriptor of kind::f16: fp32 accumulator, A/B element types,
-// both operands K-major, optional negation of A, shape M x N.
+// Instruction descriptor of kind::f16: fp32 accumulator, A/B element types, optional
+// negation of A, operands K-major unless a_mn / b_mn (MN-major), shape M x N.
 __host__ __device__ __forceinline__ uint32_t idesc_f16(uint32_t M, uint32_t N, uint32_t ab_type,
-                                                        bool neg_a = false) {
+                                                        bool neg_a = false, bool a_mn = false,
+                                                        bool b_mn = false) {
   return (1u << 4)                      // D = f32
          | (ab_type << 7) | (ab_type << 10)
          | (neg_a ? (1u << 13) : 0u)
+         | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u)
          | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
@@ -200,6 +215,10 @@ __device__ __forceinline__ void cp_async_commit() {
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.wait_group 0;" ::: "memory");
+}
+// Waits until at most one committed group of this thread is still in flight.
+__device__ __forceinline__ void cp_async_wait_one() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 
 // Bulk (TMA-engine) copy of `bytes` (multiple of 16, both addresses 16-byte aligned)

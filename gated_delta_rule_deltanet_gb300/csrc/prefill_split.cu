@@ -45,7 +45,9 @@ namespace tcs {
 constexpr int C = 64;       // chunk
 constexpr int D = 128;      // head size
 constexpr int BV = 64;      // value columns per chain CTA
-constexpr int NT = 256;     // threads (8 warps)
+constexpr int NT = 256;     // threads (8 warps); the chain kernel's compute warps
+constexpr int NTD = 128;    // chain kernel: data warps
+constexpr int NTC = NT + NTD;
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr float kMaxHalfChunkDecay = 80.0f;
 
@@ -118,19 +120,21 @@ constexpr uint32_t F_A = 0, F_X = 64, F_Y = 128, F_ALO = 128, F_COLS = 256;
 constexpr uint32_t OP_LBO = 1024, OP_SBO = 128;
 constexpr int OS = BV + 4;                               // o staging row (fp32)
 constexpr uint32_t CH_KE = 0;                            // KE and gamma of two chunks
-constexpr uint32_t CH_V = 2 * REC_TAIL;                  // V of two chunks, 64 x 64 (bf16 -> fp16)
+constexpr uint32_t CH_V = 2 * REC_TAIL;                  // V of three chunks, 64 x 64 (bf16 -> fp16)
 constexpr uint32_t V_BYTES = 64 * 64 * 2;
-constexpr uint32_t CH_ST = CH_V + 2 * V_BYTES;           // S 128 x 64 fp16
+constexpr uint32_t CH_ST = CH_V + 3 * V_BYTES;           // S 128 x 64 fp16
 constexpr uint32_t CH_ET = CH_ST + 128 * 64 * 2;         // E 64 x 64 fp16
 constexpr uint32_t CH_OST = CH_ET + 64 * 64 * 2;         // o rows fp32 [64][OS]
 constexpr uint32_t CH_BYTES = CH_OST + C * OS * 4;
 static_assert(CH_BYTES + 64 <= 227 * 1024, "chain shared memory budget");
 static_assert(FrontMap<true>::BYTES + 64 <= 227 * 1024, "front shared memory budget");
 static_assert(CH_V % 128 == 0 && CH_ST % 128 == 0, "operand alignment");
-// chain TMEM columns: A1 | A2 of two chunks (fp16 pairs), [E; O] of two chunks (the next
-// chunk's A1 V is accumulated early), dS
-constexpr uint32_t T_A = 0, A_COLS = 96, T_D1 = 256, T_D2 = 320, CH_COLS = 512;
-__host__ __device__ constexpr uint32_t d1_col(uint32_t c) { return (c & 1) ? 384 : T_D1; }
+// chain TMEM columns: A1 | A2 of two chunks (fp16 pairs); [E; O] as two partial sums
+// (key channels 0-63 plus A1 V, double-buffered because the next chunk's A1 V is
+// accumulated early, and key channels 64-127); dS as two partial sums (tokens 0-31, 32-63)
+constexpr uint32_t T_A = 0, A_COLS = 96, T_D1B = 192, T_D1 = 256, T_D2A = 384, T_D2B = 448,
+                   CH_COLS = 512;
+__host__ __device__ constexpr uint32_t d1_col(uint32_t c) { return (c & 1) ? 320 : T_D1; }
 
 __device__ __forceinline__ uint4 f16x8_pack(const float* x) {
   return make_uint4(tc::pack_f16x2(x[0], x[1]), tc::pack_f16x2(x[2], x[3]),
@@ -776,21 +780,30 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   if (warp == 0) tc::tmem_dealloc(tmem, F_COLS);
 }
 
-// One CTA per (sequence, value head, 64 value columns): the state slice in registers,
-// two MMAs per chunk.  Off the sequential path: the next chunk's A1/A2 pieces are loaded
-// into registers and written to tensor memory, its KE and values are fetched (values two
-// chunks ahead), and the previous chunk's o rows are stored while this chunk's first MMA
-// runs.
+// One CTA per (sequence, value head, 64 value columns), warp-specialised:
+//   compute warps 0-7 keep the state slice in registers and run the sequential part of
+//     every chunk -- [E; O] = A1 V + A2 S, extracting E, dS = K_end^T E, S <- gam S + dS --
+//     with the MMAs of each group split between threads 0 and 128 (one thread issues a
+//     tcgen05.mma only about every 100 cycles, half the rate at which the tensor core
+//     completes these N = 64 shapes), into separate accumulators;
+//   data warps 8-11 move everything else concurrently: the o rows of the previous chunk
+//     to global memory, and the next chunk's values (fetched three chunks ahead,
+//     converted to fp16) and A1 | A2 pieces (global -> registers -> tensor memory).
+// The two sides hand over through monotonic step counters in shared memory.
 template <bool SBF16>
-__global__ void __launch_bounds__(tcs::NT, 1)
+__global__ void __launch_bounds__(tcs::NTC, 1)
     tc_chain_kernel(Problem P, PlanView plan, const unsigned char* records) {
   using namespace tcs;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t s_mma_bar;
+  __shared__ uint64_t s_bar1;                   // [E; O]: both halves (threads 0 and 128)
+  __shared__ uint64_t s_bar2;                   // dS: both halves (threads 0 and 128)
   __shared__ uint64_t s_a1v_bar;                // A1 V of a chunk, issued by thread 32
   __shared__ uint64_t s_ld_bar[2];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ int s_e_done;                      // chunks whose E and o rows are extracted
+  __shared__ int s_next_ready;                  // chunks whose V and A1 | A2 are in place
+  __shared__ int s_ost_free;                    // chunks whose o rows are stored
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (plan.info[1] == 0) return;
@@ -802,20 +815,24 @@ __global__ void __launch_bounds__(tcs::NT, 1)
   const int64_t c0 = plan.seq_chunk0[b];
   const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + vt * BV;
   const uint32_t sb = tc::smem_u32(smem);
+  const bool data_warp = warp >= NT / 32;
+  const int dt = tid - NT;                      // data thread 0..127
   auto rec = [&](uint32_t c) -> const unsigned char* {
     return records + ((c0 + c) * HV + h) * static_cast<int64_t>(REC_BYTES);
   };
   auto ke_off = [](uint32_t c) -> uint32_t { return CH_KE + (c & 1) * REC_TAIL; };
+  auto v_off = [](uint32_t c) -> uint32_t { return CH_V + (c % 3) * V_BYTES; };
   auto chunk_n = [&](uint32_t c) -> int {
     const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
     return static_cast<int>(min(static_cast<int64_t>(C), static_cast<int64_t>(eos) - t0));
   };
-  // raw bf16 v of chunk c straight into the MN-major positions of V[c & 1]
-  auto issue_v = [&](uint32_t c) {
+
+  // ---- data-warp work
+  auto issue_v = [&](uint32_t c) {              // raw bf16 v -> MN-major positions of V[c % 3]
     const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
     const int n = chunk_n(c);
-    const uint32_t dst = sb + CH_V + (c & 1) * V_BYTES;
-    for (int u = tid; u < C * (BV / 8); u += NT) {
+    const uint32_t dst = sb + v_off(c);
+    for (int u = dt; u < C * (BV / 8); u += NTD) {
       const int m = (u >> 6) * 8 + (u & 7), j0 = ((u >> 3) & 7) * 8;
       const bool live = m < n;
       const int64_t t = live ? t0 + m : t0;
@@ -825,9 +842,9 @@ __global__ void __launch_bounds__(tcs::NT, 1)
     }
     tc::cp_async_commit();
   };
-  auto convert_v = [&](uint32_t c) {            // bf16 -> fp16 in place (16-byte pieces)
-    uint4* p = reinterpret_cast<uint4*>(smem + CH_V + (c & 1) * V_BYTES);
-    for (int u = tid; u < static_cast<int>(V_BYTES / 16); u += NT) {
+  auto convert_v = [&](uint32_t c) {            // bf16 -> fp16 in place
+    uint4* p = reinterpret_cast<uint4*>(smem + v_off(c));
+    for (int u = dt; u < static_cast<int>(V_BYTES / 16); u += NTD) {
       float x[8];
       tc::bf16x8_load(reinterpret_cast<const unsigned char*>(p + u), x);
       p[u] = f16x8_pack(x);
@@ -837,232 +854,295 @@ __global__ void __launch_bounds__(tcs::NT, 1)
     const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
     const int n = chunk_n(c);
 #pragma unroll
-    for (int k = 0; k < (C * BV / 4) / NT; ++k) {
-      const int idx = tid + k * NT, i = idx / (BV / 4), q = idx % (BV / 4);
+    for (int k = 0; k < (C * BV / 4) / NTD; ++k) {
+      const int idx = dt + k * NTD, i = idx / (BV / 4), q = idx % (BV / 4);
       if (i < n)
         *reinterpret_cast<float4*>(P.o + ((t0 + i) * HV + h) * D + vt * BV + q * 4) =
             *reinterpret_cast<const float4*>(smem + CH_OST + (i * OS + q * 4) * 4);
     }
   };
-  // this thread's 12 pieces of a chunk's A1 | A2 (coalesced: piece p of all threads is
-  // one contiguous 4 KB run)
-  uint4 ablob[BLOB_PIECES];
+  // a data thread serves TMEM lane 32 (warp & 3) + lane for both column halves, i.e. the
+  // A1 | A2 pieces of compute threads dt and dt + 128 (12 pieces each)
+  uint4 ablob[2 * BLOB_PIECES];
   auto load_blob = [&](uint32_t c) {
-    const uint4* src = reinterpret_cast<const uint4*>(rec(c) + REC_BLOB) + tid;
+    const uint4* src = reinterpret_cast<const uint4*>(rec(c) + REC_BLOB) + dt;
 #pragma unroll
-    for (int p = 0; p < static_cast<int>(BLOB_PIECES); ++p) ablob[p] = __ldg(src + p * NT);
+    for (int p = 0; p < static_cast<int>(BLOB_PIECES); ++p) {
+      ablob[p] = __ldg(src + p * NT);
+      ablob[BLOB_PIECES + p] = __ldg(src + p * NT + NTD);
+    }
+  };
+  auto wait_flag = [&](int* flag, int target) -> bool {   // bounded
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+      if (*reinterpret_cast<volatile int*>(flag) >= target) {
+        __threadfence_block();
+        return true;
+      }
+      __nanosleep(20);
+    }
+    s_abort = 1;
+    return false;
+  };
+  auto set_flag = [&](int* flag, int value) {
+    __threadfence_block();
+    *reinterpret_cast<volatile int*>(flag) = value;
   };
 
-  issue_v(0);
-  if (nchunks > 1) issue_v(1);
-  load_blob(0);
+  if (data_warp) {
+    issue_v(0);
+    if (nchunks > 1) issue_v(1);
+    if (nchunks > 2) issue_v(2);
+    load_blob(0);
+  }
   if (warp == 0) {
     tc::tmem_alloc(&s_tmem, CH_COLS);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(&s_mma_bar, 1);
+    tc::mbar_init(&s_bar1, 2);
+    tc::mbar_init(&s_bar2, 2);
     tc::mbar_init(&s_a1v_bar, 1);
     tc::mbar_init(&s_ld_bar[0], 1);
     tc::mbar_init(&s_ld_bar[1], 1);
     tc::fence_mbar_init();
     s_abort = 0;
+    s_e_done = 0;
+    s_next_ready = 0;
+    s_ost_free = 0;
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&s_ld_bar[0], REC_TAIL);
-    tc::bulk_load(sb + ke_off(0), rec(0) + REC_KE, REC_TAIL, &s_ld_bar[0]);
-  }
   const uint32_t tmem = s_tmem;
-  const int row = 32 * (warp & 3) + lane;       // TMEM lane = key channel (state row)
-  const int chalf = warp >> 2;
-  const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-  // row `row`, K columns of this thread's half: A1 -> 16 columns, A2 -> 32 columns
-  auto store_blob = [&](uint32_t c) {
-    const uint32_t base = tmem + lane_addr + T_A + (c & 1) * A_COLS;
-    uint32_t w[16];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-      w[4 * p] = ablob[p].x; w[4 * p + 1] = ablob[p].y; w[4 * p + 2] = ablob[p].z; w[4 * p + 3] = ablob[p].w;
-    }
-    tc::tmem_st16(base + 16 * chalf, w);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const uint4 v = ablob[4 + 4 * half + p];
-        w[4 * p] = v.x; w[4 * p + 1] = v.y; w[4 * p + 2] = v.z; w[4 * p + 3] = v.w;
-      }
-      tc::tmem_st16(base + 32 + 32 * chalf + 16 * half, w);
-    }
-    tc::tmem_wait_st();
-  };
-
-  // S[row][32 chalf + j] of this CTA's value tile, fp32 in registers; its fp16 copy
-  // (N = value column, K = key channel, MN-major) is the first MMA's B operand
-  float Sv[32];
-  {
-    const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      Sv[j] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[base + j])
-                    : static_cast<const float*>(P.pool)[base + j];
-  }
-  auto write_state_operand = [&]() {
-#pragma unroll
-    for (int p = 0; p < 4; ++p)
-      *reinterpret_cast<uint4*>(smem + CH_ST + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
-          f16x8_pack(Sv + 8 * p);
-  };
-  write_state_operand();
-  store_blob(0);
-  if (nchunks > 1) load_blob(1);
-  if (nchunks > 1) tc::cp_async_wait_one(); else tc::cp_async_wait_all();
-  __syncthreads();
-  convert_v(0);
-  tc::fence_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-
   const uint32_t id1 = tc::idesc_f16(128, BV, tc::kF16, false, false, true);
   const uint32_t id2 = tc::idesc_f16(128, BV, tc::kF16, false, true, true);
-  // operand descriptors, advanced by constant offsets per K step
   const uint64_t dST = tc::smem_desc(sb + CH_ST, OP_LBO, OP_SBO);
   const uint64_t dET = tc::smem_desc(sb + CH_ET, OP_LBO, OP_SBO);
   const uint64_t dV0 = tc::smem_desc(sb + CH_V, OP_LBO, OP_SBO);
   const uint64_t dKE0 = tc::smem_desc(sb + CH_KE, KE_LBO, KE_SBO);
-  // the state-independent part A1 V of chunk c's first MMA, issued by thread 32 and
-  // committed to its own barrier, which thread 0 waits on before accumulating onto it
-  auto issue_a1v = [&](uint32_t c) {
-    const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
-    const uint64_t dv = tc::desc_add(dV0, (c & 1) * V_BYTES);
+
+  if (data_warp) {
+    // -------------------------------------------------------------------- data warps
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    auto store_blob = [&](uint32_t c) {
+      const uint32_t base = tmem + lane_addr + T_A + (c & 1) * A_COLS;
 #pragma unroll
-    for (int s = 0; s < C / 16; ++s)
-      tc::mma_ts(tmem + d1_col(c), ta + s * 8, tc::desc_add(dv, s * 2 * OP_LBO), id1, s > 0);
-    tc::mma_commit(&s_a1v_bar);
-  };
-  if (tid == 32) issue_a1v(0);
-  uint32_t phase = 0;
-  int pending = 0;                              // chunk whose KE load is in flight, or -1
-  auto mma_wait = [&]() {
-    const bool ok = tc::mbar_wait_bounded(&s_mma_bar, phase & 1, kWaitLimit);
-    phase ^= 1;
-    if (!ok) s_abort = 1;
-    tc::fence_after_sync();
-  };
-
-  for (uint32_t c = 0; c < nchunks; ++c) {
-    const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
-    const uint32_t d1 = d1_col(c);
-    const bool more = c + 1 < nchunks;
-    if (!tc::mbar_wait_bounded(&s_ld_bar[c & 1], (c >> 1) & 1, kWaitLimit)) s_abort = 1;
-    pending = -1;
-
-    // ---------------------------------------------------------------- [E; O] += A2 S
+      for (int ch = 0; ch < 2; ++ch) {
+        const uint4* a = ablob + ch * BLOB_PIECES;
+        uint32_t w[16];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          w[4 * p] = a[p].x; w[4 * p + 1] = a[p].y; w[4 * p + 2] = a[p].z; w[4 * p + 3] = a[p].w;
+        }
+        tc::tmem_st16(base + 16 * ch, w);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            const uint4 v = a[4 + 4 * half + p];
+            w[4 * p] = v.x; w[4 * p + 1] = v.y; w[4 * p + 2] = v.z; w[4 * p + 3] = v.w;
+          }
+          tc::tmem_st16(base + 32 + 32 * ch + 16 * half, w);
+        }
+      }
+      tc::tmem_wait_st();
+    };
+    // V(q) and A1 | A2 of chunk q in place; A[q & 1] last held chunk q - 2's operands
+    auto prepare = [&](uint32_t q) -> bool {
+      // value groups issued after V(q) so far: V(1), V(2) for q = 0 (issued up front),
+      // otherwise V(q + 1) only (V(q + 2) is issued after chunk q - 1's o rows)
+      const uint32_t newer = q == 0 ? min(nchunks - 1, 2u) : (q + 1 < nchunks ? 1u : 0u);
+      if (newer == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+      else if (newer == 1) tc::cp_async_wait_one();
+      else tc::cp_async_wait_all();
+      tc::named_sync(2, NTD);
+      if (q >= 2 && !wait_flag(&s_e_done, static_cast<int>(q) - 1)) return false;
+      convert_v(q);
+      store_blob(q);
+      if (q + 1 < nchunks) load_blob(q + 1);
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      tc::named_sync(2, NTD);
+      if (dt == 0) set_flag(&s_next_ready, static_cast<int>(q) + 1);
+      return true;
+    };
+    // chunk c's o rows out, then V(c + 3) into V[c % 3] (chunk c's A1 V is complete)
+    auto finish = [&](uint32_t c) -> bool {
+      if (!wait_flag(&s_e_done, static_cast<int>(c) + 1)) return false;
+      store_o(c);
+      if (c + 3 < nchunks) issue_v(c + 3);
+      tc::named_sync(2, NTD);
+      if (dt == 0) set_flag(&s_ost_free, static_cast<int>(c) + 1);
+      return true;
+    };
+    if (prepare(0)) {
+      for (uint32_t c = 0; c < nchunks; ++c) {
+        if (c + 1 < nchunks && !prepare(c + 1)) break;
+        if (!finish(c)) break;
+      }
+    }
+    tc::cp_async_wait_all();
+  } else {
+    // -------------------------------------------------------------------- compute warps
+    const int row = 32 * (warp & 3) + lane;     // TMEM lane = key channel (state row)
+    const int chalf = warp >> 2;
+    const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
     if (tid == 0) {
-      if (!tc::mbar_wait_bounded(&s_a1v_bar, c & 1, kWaitLimit)) s_abort = 1;
-      tc::fence_after_sync();
-#pragma unroll
-      for (int s = 0; s < D / 16; ++s)
-        tc::mma_ts(tmem + d1, ta + 32 + s * 8, tc::desc_add(dST, s * 2 * OP_LBO), id1, 1);
-      tc::mma_commit(&s_mma_bar);
-      if (more) {                               // chunk c - 1's KE in that buffer is consumed
-        tc::mbar_arrive_expect_tx(&s_ld_bar[(c + 1) & 1], REC_TAIL);
-        tc::bulk_load(sb + ke_off(c + 1), rec(c + 1) + REC_KE, REC_TAIL, &s_ld_bar[(c + 1) & 1]);
-      }
+      tc::mbar_arrive_expect_tx(&s_ld_bar[0], REC_TAIL);
+      tc::bulk_load(sb + ke_off(0), rec(0) + REC_KE, REC_TAIL, &s_ld_bar[0]);
     }
-    if (more) pending = static_cast<int>(c + 1);
-    if (c > 0) store_o(c - 1);                  // o rows of the previous chunk
-    if (more) {
-      store_blob(c + 1);                        // its columns held chunk c - 1's operands
-      if (c + 2 < nchunks) load_blob(c + 2);
-      tc::cp_async_wait_all();                  // the next chunk's values (the only group)
-    }
-    __syncthreads();                            // OST free, the next chunk's values landed
-    if (more) convert_v(c + 1);
-    mma_wait();
-
-    // ---------------------------------------------------------------- E (critical), o rows
-    float x[32];
+    float Sv[32];
     {
-      uint32_t r0[16], r1[16];
-      tc::tmem_ld16(tmem + lane_addr + d1 + 32 * chalf, r0);
-      tc::tmem_ld16(tmem + lane_addr + d1 + 32 * chalf + 16, r1);
-      tc::tmem_wait_ld();
+      const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        x[e] = __uint_as_float(r0[e]);
-        x[e + 16] = __uint_as_float(r1[e]);
-      }
-      if (row < C) {
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-          *reinterpret_cast<uint4*>(smem + CH_ET + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
-              f16x8_pack(x + 8 * p);
-      }
+      for (int j = 0; j < 32; ++j)
+        Sv[j] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[base + j])
+                      : static_cast<const float*>(P.pool)[base + j];
     }
+    auto write_state_operand = [&]() {
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        *reinterpret_cast<uint4*>(smem + CH_ST + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
+            f16x8_pack(Sv + 8 * p);
+    };
+    write_state_operand();
     tc::fence_async_smem();
     tc::fence_before_sync();
-    __syncthreads();
+    tc::named_sync(1, NT);
     tc::fence_after_sync();
-
-    // ---------------------------------------------------------------- dS = K_end^T E
-    if (tid == 0) {
-      const uint64_t dke = tc::desc_add(dKE0, (c & 1) * REC_TAIL);
+    auto wait_on = [&](uint64_t* bar, uint32_t parity) {
+      if (!tc::mbar_wait_bounded(bar, parity, kWaitLimit)) s_abort = 1;
+      tc::fence_after_sync();
+    };
+    // the state-independent part A1 V of chunk c, issued by thread 32 once the data warps
+    // have its operands in place
+    auto issue_a1v = [&](uint32_t c) {
+      if (!wait_flag(&s_next_ready, static_cast<int>(c) + 1)) return;
+      tc::fence_after_sync();
+      const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
+      const uint64_t dv = tc::desc_add(dV0, (c % 3) * V_BYTES);
 #pragma unroll
       for (int s = 0; s < C / 16; ++s)
-        tc::mma_ss(tmem + T_D2, tc::desc_add(dke, s * 2 * KE_LBO), tc::desc_add(dET, s * 2 * OP_LBO),
-                   id2, s > 0);
-      tc::mma_commit(&s_mma_bar);
-    }
-    if (tid == 32 && more) issue_a1v(c + 1);    // its A1 and V are in place since the last barrier
-    if (row >= C) {                             // o rows, stored during the next chunk
-      float* op = reinterpret_cast<float*>(smem + CH_OST) + (row - C) * OS + 32 * chalf;
-#pragma unroll
-      for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<float4*>(op + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-    }
-    if (c + 2 < nchunks) issue_v(c + 2);        // into V[c & 1], which MMA1 of this chunk read
-    mma_wait();
+        tc::mma_ts(tmem + d1_col(c), ta + s * 8, tc::desc_add(dv, s * 2 * OP_LBO), id1, s > 0);
+      tc::mma_commit(&s_a1v_bar);
+    };
+    if (tid == 32) issue_a1v(0);
 
-    // ---------------------------------------------------------------- S <- diag(gam) S + dS
-    {
-      uint32_t r0[16], r1[16];
-      tc::tmem_ld16(tmem + lane_addr + T_D2 + 32 * chalf, r0);
-      tc::tmem_ld16(tmem + lane_addr + T_D2 + 32 * chalf + 16, r1);
-      tc::tmem_wait_ld();
-      const float gam = reinterpret_cast<const float*>(smem + ke_off(c) + (REC_GAM - REC_KE))[row];
+    for (uint32_t c = 0; c < nchunks; ++c) {
+      const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
+      const uint32_t d1 = d1_col(c);
+      const bool more = c + 1 < nchunks;
+      wait_on(&s_ld_bar[c & 1], (c >> 1) & 1);
+      // -------------------------------------------------------------- [E; O] += A2 S
+      if (tid == 0) {                           // key channels 0-63, onto A1 V
+        wait_on(&s_a1v_bar, c & 1);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) Sv[e] = gam * Sv[e] + __uint_as_float(e < 16 ? r0[e] : r1[e - 16]);
-      write_state_operand();
+        for (int s = 0; s < D / 32; ++s)
+          tc::mma_ts(tmem + d1, ta + 32 + s * 8, tc::desc_add(dST, s * 2 * OP_LBO), id1, 1);
+        tc::mma_commit(&s_bar1);
+        if (more) {                             // chunk c - 1's KE in that buffer is consumed
+          tc::mbar_arrive_expect_tx(&s_ld_bar[(c + 1) & 1], REC_TAIL);
+          tc::bulk_load(sb + ke_off(c + 1), rec(c + 1) + REC_KE, REC_TAIL, &s_ld_bar[(c + 1) & 1]);
+        }
+      }
+      if (tid == 128) {                         // key channels 64-127
+#pragma unroll
+        for (int s = D / 32; s < D / 16; ++s)
+          tc::mma_ts(tmem + T_D1B, ta + 32 + s * 8, tc::desc_add(dST, s * 2 * OP_LBO), id1, s > D / 32);
+        tc::mma_commit(&s_bar1);
+      }
+      wait_on(&s_bar1, c & 1);
+      // -------------------------------------------------------------- E, o rows
+      {
+        uint32_t r0[16], r1[16], q0[16], q1[16];
+        tc::tmem_ld16(tmem + lane_addr + d1 + 32 * chalf, r0);
+        tc::tmem_ld16(tmem + lane_addr + d1 + 32 * chalf + 16, r1);
+        tc::tmem_ld16(tmem + lane_addr + T_D1B + 32 * chalf, q0);
+        tc::tmem_ld16(tmem + lane_addr + T_D1B + 32 * chalf + 16, q1);
+        tc::tmem_wait_ld();
+        float x[32];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          x[e] = __uint_as_float(r0[e]) + __uint_as_float(q0[e]);
+          x[e + 16] = __uint_as_float(r1[e]) + __uint_as_float(q1[e]);
+        }
+        if (row < C) {
+#pragma unroll
+          for (int p = 0; p < 4; ++p)
+            *reinterpret_cast<uint4*>(smem + CH_ET + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
+                f16x8_pack(x + 8 * p);
+        } else {
+          wait_flag(&s_ost_free, static_cast<int>(c));   // chunk c - 1's o rows are stored
+          float* op = reinterpret_cast<float*>(smem + CH_OST) + (row - C) * OS + 32 * chalf;
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(op + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+        }
+      }
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      tc::named_sync(1, NT);
+      tc::fence_after_sync();
+      if (tid == 0) set_flag(&s_e_done, static_cast<int>(c) + 1);
+      // -------------------------------------------------------------- dS = K_end^T E
+      if (tid == 0 || tid == 128) {             // tokens 0-31 / 32-63
+        const uint64_t dke = tc::desc_add(dKE0, (c & 1) * REC_TAIL);
+        const int s0 = tid == 0 ? 0 : C / 32;
+        const uint32_t d2 = tmem + (tid == 0 ? T_D2A : T_D2B);
+#pragma unroll
+        for (int s = 0; s < C / 32; ++s)
+          tc::mma_ss(d2, tc::desc_add(dke, (s0 + s) * 2 * KE_LBO), tc::desc_add(dET, (s0 + s) * 2 * OP_LBO),
+                     id2, s > 0);
+        tc::mma_commit(&s_bar2);
+      }
+      if (tid == 32 && more) issue_a1v(c + 1);
+      wait_on(&s_bar2, c & 1);
+      // -------------------------------------------------------------- S <- diag(gam) S + dS
+      {
+        uint32_t r0[16], r1[16], q0[16], q1[16];
+        tc::tmem_ld16(tmem + lane_addr + T_D2A + 32 * chalf, r0);
+        tc::tmem_ld16(tmem + lane_addr + T_D2A + 32 * chalf + 16, r1);
+        tc::tmem_ld16(tmem + lane_addr + T_D2B + 32 * chalf, q0);
+        tc::tmem_ld16(tmem + lane_addr + T_D2B + 32 * chalf + 16, q1);
+        tc::tmem_wait_ld();
+        const float gam = reinterpret_cast<const float*>(smem + ke_off(c) + (REC_GAM - REC_KE))[row];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          Sv[e] = gam * Sv[e] + (__uint_as_float(r0[e]) + __uint_as_float(q0[e]));
+          Sv[e + 16] = gam * Sv[e + 16] + (__uint_as_float(r1[e]) + __uint_as_float(q1[e]));
+        }
+        write_state_operand();
+      }
+      tc::fence_async_smem();
+      tc::fence_before_sync();
+      tc::named_sync(1, NT);
+      tc::fence_after_sync();
+      if (s_abort) break;
     }
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (s_abort) break;
+    if (!s_abort) {
+      const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (SBF16)
+          static_cast<uint16_t*>(P.pool)[base + j] = f32_to_bf16_bits(Sv[j]);
+        else
+          static_cast<float*>(P.pool)[base + j] = Sv[j];
+      }
+    } else if (tid == 0) {
+      set_flag(&s_e_done, 1 << 30);             // release the data warps
+    }
   }
-  tc::cp_async_wait_all();
 
   if (s_abort) {
-    // let what is still in flight finish (bounded) before shared and tensor memory go away
-    tc::mbar_wait_bounded(&s_mma_bar, (phase ^ 1) & 1, kWaitLimit);
-    for (uint32_t k = 0; k < 2; ++k) tc::mbar_wait_bounded(&s_a1v_bar, k, kWaitLimit);
-    if (pending >= 0) tc::mbar_wait_bounded(&s_ld_bar[pending & 1], (pending >> 1) & 1, kWaitLimit);
-    if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
-  } else {
-    store_o(nchunks - 1);
-    const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (SBF16)
-        static_cast<uint16_t*>(P.pool)[base + j] = f32_to_bf16_bits(Sv[j]);
-      else
-        static_cast<float*>(P.pool)[base + j] = Sv[j];
+    // let whatever is still in flight finish (bounded) before shared and tensor memory go
+    for (uint32_t k = 0; k < 2; ++k) {
+      tc::mbar_wait_bounded(&s_bar1, k, kWaitLimit);
+      tc::mbar_wait_bounded(&s_bar2, k, kWaitLimit);
+      tc::mbar_wait_bounded(&s_a1v_bar, k, kWaitLimit);
+      tc::mbar_wait_bounded(&s_ld_bar[0], k, kWaitLimit);
+      tc::mbar_wait_bounded(&s_ld_bar[1], k, kWaitLimit);
     }
+    if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1094,7 +1174,7 @@ static cudaError_t launch_chain_t(const Problem& P, const PlanView& plan, const 
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(tcs::CH_BYTES));
   if (e != cudaSuccess) return e;
-  k<<<dim3(P.num_seqs, P.HV, tcs::D / tcs::BV), tcs::NT, tcs::CH_BYTES, st>>>(P, plan, recs);
+  k<<<dim3(P.num_seqs, P.HV, tcs::D / tcs::BV), tcs::NTC, tcs::CH_BYTES, st>>>(P, plan, recs);
   return cudaGetLastError();
 }
 

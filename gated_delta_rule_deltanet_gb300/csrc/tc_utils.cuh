@@ -108,6 +108,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// Barrier `id` (1..15) among the first `count` threads that reach it (a multiple of 32).
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------------------------ fences
 
 // Makes generic-proxy shared-memory writes visible to the tensor core (async proxy).

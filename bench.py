@@ -439,7 +439,7 @@ def ours_arm(args, rank, world, local):
     del t_dev
 
     # end to end through the public API with host buffers
-    e2e_ms, h2d, d2h = time_prefill_e2e(p, dev, max(3, args.steps // 2), 2)
+    e2e_ms, h2d, d2h = time_prefill_e2e(p, dev, max(3, args.steps // 2), 3)
     e2e_value, _ = aggregate(tokens, e2e_ms / 1e3, world, dev)
 
     # roofline of the dominant kernel (its share of the algorithmic bytes / its time)
@@ -484,6 +484,21 @@ def ours_arm(args, rank, world, local):
                                   "frac": vbytes[vk] / (vstage[vk] / 1e3) / 1e9
                                   / peaks["hbm_gbs"], "traffic": None}})
 
+    if not args.no_decode:
+        for wname in ("kda_prefill", "ragged_gqa_kda"):
+            wp = workloads.workload(wname)
+            wms, wst, wt, _, wstages = time_prefill(wp, dev, 30, 3)
+            del wt
+            wbytes = float(sum(prefill_algorithmic_bytes(wp).values()))
+            wval, _ = aggregate(float(wp.total_tokens), wms / 1e3, world, dev)
+            also.append({"workload": wname, "metric": "prefill tokens/s", "value": wval,
+                         "unit": "tokens/s", "ms_per_step": wms,
+                         "stage_ms": {n: m for (n, _), m in zip(wstages, wst)},
+                         "path_roofline": {"algorithmic_bytes": wbytes,
+                                           "achieved_gbs": wbytes / (wms / 1e3) / 1e9,
+                                           "frac_hbm": wbytes / (wms / 1e3) / 1e9
+                                           / peaks["hbm_gbs"]}})
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         rate, dt, threads, take, npairs = cpu_oracle_prefill(p, 1.0)
@@ -516,8 +531,8 @@ def ours_arm(args, rank, world, local):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gdn_prefill",
                     choices=[w for w in workloads.WORKLOADS if w != "kda_decode"])

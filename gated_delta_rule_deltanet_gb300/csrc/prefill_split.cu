@@ -5,35 +5,39 @@
 // "From Attention to Learned Memory", sec. 4, WY/UT transform) splits every chunk's
 // work into a part that depends only on the chunk's own keys, queries, gates and
 // betas -- the intra-chunk matrices A_kk and A_qk, the inverse T = (I + A_kk)^-1 and
-// the WY factors -- and a part that carries the state from chunk to chunk.  The
-// first part is independent across all chunks of all sequences, so the front kernel
-// runs one CTA per (chunk, value head) over the whole GPU and writes each chunk's
-// chain operands to the workspace:
+// the WY factors -- and a part that carries the state from chunk to chunk.  With
+// E = TB V - W S the chunk's corrections, the state update and the output are
 //
-//   A1  = [TB; A_qk TB]                 128 x 64   fp16
-//   A2  = [-W; Q~ - A_qk W]             128 x 128  fp16
-//   KE  = K_end (token rows)            64 x 128   fp16
-//   gam = exp(G_last) per key channel   128        fp32
+//   S' = diag(gam) S + K_end^T E = diag(gam) S + Kb V + P S,   Kb = K_end^T TB, P = -K_end^T W
+//   O  = Q~ S + A_qk E           = A1o V + A2o S,              A1o = A_qk TB,   A2o = Q~ - A_qk W
 //
-// A1 and A2 are stored per thread of the chain kernel (each thread's 16-byte pieces of
-// its row, interleaved across threads so that every warp access is contiguous): the
-// chain kernel loads them into registers and writes them to tensor memory, where the
-// MMA reads its A operand, so they never pass through shared memory.  KE is stored in
-// the MN-major core-matrix order of an A operand and moved with one bulk copy.  The
-// chain kernel keeps a (sequence, value head, 64 value columns) slice of the state in
-// registers and per chunk issues two MMAs,
+// so every product that does not involve the state can be formed before the state is
+// known.  The front kernel runs one CTA per (chunk, value head) over the whole GPU and
+// writes each chunk's operands to the workspace:
 //
-//   [E; O] = A1 V + A2 S              M=128 N=64 K=64+128   (A from tensor memory)
-//   S     <- diag(gam) S + KE^T E     M=128 N=64 K=64
+//   [Kb | P]    128 x (64 + 128)   fp16   (rows = key channels)
+//   [A1o | A2o]  64 x (64 + 128)   fp16   (rows = tokens)
+//   gam = exp(G_last) per key channel, fp32
 //
-// while the next chunk's operands and values are being fetched.  Every operand the
-// threads produce (V, S, E, and in the front kernel TB and K~) is stored MN-major, so
-// each thread writes whole 16-byte rows of core matrices instead of transposing.  The front work is done
-// once per (chunk, value head) rather than once per value tile, and none of it sits
-// on the sequential path.
+// [Kb | P] is stored per thread of the chain kernel (each thread's 16-byte pieces of its
+// row, interleaved across threads so that every warp access is contiguous): the chain
+// kernel loads it into registers and writes it to tensor memory, where the MMA reads its
+// A operand.  [A1o | A2o] is stored in the K-major core-matrix order of a shared-memory A
+// operand and moved with one bulk copy.  The chain kernel keeps a (sequence, value head,
+// 64 value columns) slice of the state in registers; per chunk only one MMA group is on
+// the sequential path,
 //
-// The arithmetic of both kernels is that of the single-kernel path in prefill_tc.cu
-// (same operand precisions and factorisations); only where it runs differs.
+//   D = Kb V + P S                M=128 N=64 K=64+128   (A from tensor memory; Kb V early)
+//   S <- diag(gam) S + D
+//
+// and the output MMA O = [A1o | A2o] [V; S] (M=128, of which rows 0-63 are used) runs
+// beside the next chunk's state update.  Every operand the threads produce (V, S, and in
+// the front kernel TB, K~, -W, K_end) is stored MN-major, so each thread writes whole
+// 16-byte rows of core matrices instead of transposing.
+//
+// Operand precisions are those of the single-kernel path in prefill_tc.cu (fp16 operands,
+// fp32 accumulation and fp32 state); the state passes through fp16 only as the B operand of
+// P S, so a state-independent term never carries the state's rounding forward.
 #include "kda_common.cuh"
 #include "prefill_plan.cuh"
 #include "tc_utils.cuh"
@@ -46,25 +50,29 @@ constexpr int C = 64;       // chunk
 constexpr int D = 128;      // head size
 constexpr int BV = 64;      // value columns per chain CTA
 constexpr int NT = 256;     // threads (8 warps); the chain kernel's compute warps
-constexpr int NTD = 128;    // chain kernel: data warps
-constexpr int NTC = NT + NTD;
+constexpr int NTD = 128;    // chain kernel: operand warps 8-11
+constexpr int NTO = 64;     // chain kernel: output warps 12-13 (TMEM lanes 0-63)
+constexpr int NTC = NT + NTD + NTO + 32;   // + warp 14, whose lane 0 issues the output MMA
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr float kMaxHalfChunkDecay = 80.0f;
 
 // record of one (chunk, value head) in the workspace
-//   BLOB: piece p (0..11) of thread t at (p * NT + t) * 16; thread t (row r, column half h)
-//         holds A1[r][32h .. 32h+32) in pieces 0-3 and A2[r][64h .. 64h+64) in pieces 4-11
-//   KE:   K_end, element (token m, channel c) at mn_offset(m, c, KE_LBO, KE_SBO)
+//   BLOB: piece p (0..11) of thread t at (p * NT + t) * 16; thread t (key channel
+//         r = 32 (warp & 3) + lane, column half h = warp >> 2) holds Kb[r][32h .. 32h+32) in
+//         pieces 0-3 and P[r][64h .. 64h+64) in pieces 4-11
+//   OA:   [A1o | A2o], element (token m, column k) at cm_offset(m, k, OA_LBO, OA_SBO)
+//   GAM:  exp(G_last) per key channel
 constexpr uint32_t BLOB_PIECES = 12;
 constexpr uint32_t REC_BLOB = 0;
-constexpr uint32_t REC_KE = REC_BLOB + BLOB_PIECES * 256 * 16;
-constexpr uint32_t REC_GAM = REC_KE + 64 * 128 * 2;
-constexpr uint32_t REC_BYTES = REC_GAM + 128 * 4;    // 66048, a multiple of 16
-constexpr uint32_t REC_TAIL = REC_BYTES - REC_KE;    // KE and gamma, bulk-copied
-constexpr uint32_t KE_LBO = 2048, KE_SBO = 128;      // MN-major: 16 channel groups per token group
-constexpr uint32_t KT_LBO = 2048, KT_SBO = 128;      // K~ (N = channel, K = token), same order
+constexpr uint32_t REC_OA = REC_BLOB + BLOB_PIECES * 256 * 16;
+constexpr uint32_t OA_LBO = 128, OA_SBO = tc::dense_sbo(C + D);   // K-major, K = 192
+constexpr uint32_t OA_BYTES = C * (C + D) * 2;
+constexpr uint32_t REC_GAM = REC_OA + OA_BYTES;
+constexpr uint32_t REC_BYTES = REC_GAM + 128 * 4;    // 74240, a multiple of 16
+constexpr uint32_t KE_LBO = 2048, KE_SBO = 128;      // K_end (M = channel, K = token), MN-major
+constexpr uint32_t KT_LBO = 2048, KT_SBO = 128;      // K~ (N = channel, K = token)
 constexpr uint32_t TB_LBO = 1024, TB_SBO = 128;      // TB (N = column j, K = row m)
-static_assert(REC_BYTES % 16 == 0 && REC_KE % 16 == 0, "records must stay 16-byte aligned");
+static_assert(REC_BYTES % 16 == 0 && REC_OA % 16 == 0, "records must stay 16-byte aligned");
 
 // per-chunk vectors of the front kernel (byte offsets inside its SMALL area)
 constexpr uint32_t O_GS = 0, O_BETA = 256, O_RK = 512, O_RQ = 768, O_EG = 1024, O_EGL = 1280,
@@ -85,8 +93,8 @@ struct FrontMap<false> {
   static constexpr uint32_t AK_LBO = 144, AK_SBO = (D / 8) * AK_LBO;
   static constexpr uint32_t AK = 0;
   static constexpr uint32_t SMALL = AK + 16 * AK_SBO;
-  static constexpr uint32_t R2 = SMALL + SMALL_BYTES;   // solve, then K~^T and A1
-  static constexpr uint32_t LMAT = R2 + SOL_BYTES;      // [I; A_qk] 128 x 64 fp16
+  static constexpr uint32_t R2 = SMALL + SMALL_BYTES;   // solve, then K_end and K~
+  static constexpr uint32_t LMAT = R2 + SOL_BYTES;      // [*; A_qk] 128 x 64 fp16, then Kb
   static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;  // TB 64 x 64 fp16, MN-major
   static constexpr uint32_t BYTES = TBT + 64 * 64 * 2;
 };
@@ -104,37 +112,43 @@ struct FrontMap<true> {
   static constexpr uint32_t AK = SMALL + SMALL_BYTES;   // [K+; Q+] high halves
   static constexpr uint32_t BK = AK + 128 * 128 * 2;    // K- high half
   static constexpr uint32_t BKLO = BK + 64 * 128 * 2;   // K- low half
-  static constexpr uint32_t R2 = BK;                    // consumed K- halves: solve, K~^T, A1
+  static constexpr uint32_t R2 = BK;                    // consumed K- halves: solve, K_end, K~
   static constexpr uint32_t LMAT = R2 + SOL_BYTES;
   static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;
   static constexpr uint32_t BYTES = TBT + 64 * 64 * 2;
   static_assert(LMAT >= BKLO + 64 * 128 * 2, "solve area covers the K- halves");
 };
 
-// front TMEM columns: A_kk/A_qk, X, Y (the low half of [K+; Q+] shares Y's columns:
-// it is consumed by the A-GEMM before Y is produced)
+// front TMEM columns: A_kk/A_qk (second issuer's half of K in F_X), then Kb | A1o, then
+// Kb K~ | A1o K~ (the low half of [K+; Q+] shares F_Y: the A-GEMM consumes it first)
 constexpr uint32_t F_A = 0, F_X = 64, F_Y = 128, F_ALO = 128, F_COLS = 256;
 
 // chain shared memory (MN-major operands: core matrices of 8 K-rows x 8 value columns,
-// value-column groups adjacent, K groups 1024 bytes apart)
+// value-column groups adjacent, K groups 1024 bytes apart).  The output MMA has M = 128
+// but only rows 0-63 exist: its A operand [A1o | A2o] (K-major) reads its rows 64-127
+// from the next OA_BYTES of shared memory, whatever they hold; those rows of the result
+// are never read.
 constexpr uint32_t OP_LBO = 1024, OP_SBO = 128;
 constexpr int OS = BV + 4;                               // o staging row (fp32)
-constexpr uint32_t CH_KE = 0;                            // KE and gamma of two chunks
-constexpr uint32_t CH_V = 2 * REC_TAIL;                  // V of three chunks, 64 x 64 (bf16 -> fp16)
-constexpr uint32_t V_BYTES = 64 * 64 * 2;
-constexpr uint32_t CH_ST = CH_V + 3 * V_BYTES;           // S 128 x 64 fp16
-constexpr uint32_t CH_ET = CH_ST + 128 * 64 * 2;         // E 64 x 64 fp16
-constexpr uint32_t CH_OST = CH_ET + 64 * 64 * 2;         // o rows fp32 [64][OS]
-constexpr uint32_t CH_BYTES = CH_OST + C * OS * 4;
+constexpr uint32_t OA_SLOTS = 3, V_SLOTS = 5, S_SLOTS = 3;
+constexpr uint32_t V_BYTES = 64 * 64 * 2, S_BYTES = 128 * 64 * 2;
+constexpr uint32_t CH_OA = 0;                            // [A1o | A2o] of three chunks
+constexpr uint32_t CH_V = CH_OA + OA_SLOTS * OA_BYTES;   // V of four chunks, 64 x 64 (bf16 -> fp16)
+constexpr uint32_t CH_ST = CH_V + V_SLOTS * V_BYTES;     // S of three chunks, 128 x 64 fp16
+constexpr uint32_t CH_OST = CH_ST + S_SLOTS * S_BYTES;   // o rows fp32 [64][OS]
+constexpr uint32_t CH_GAM = CH_OST + C * OS * 4;         // gamma of four chunks, fp32 [4][128]
+constexpr uint32_t GAM_SLOTS = 4;
+constexpr uint32_t CH_BYTES = CH_GAM + GAM_SLOTS * D * 4;
 static_assert(CH_BYTES + 64 <= 227 * 1024, "chain shared memory budget");
 static_assert(FrontMap<true>::BYTES + 64 <= 227 * 1024, "front shared memory budget");
-static_assert(CH_V % 128 == 0 && CH_ST % 128 == 0, "operand alignment");
-// chain TMEM columns: A1 | A2 of two chunks (fp16 pairs); [E; O] as two partial sums
-// (key channels 0-63 plus A1 V, double-buffered because the next chunk's A1 V is
-// accumulated early, and key channels 64-127); dS as two partial sums (tokens 0-31, 32-63)
-constexpr uint32_t T_A = 0, A_COLS = 96, T_D1B = 192, T_D1 = 256, T_D2A = 384, T_D2B = 448,
-                   CH_COLS = 512;
-__host__ __device__ constexpr uint32_t d1_col(uint32_t c) { return (c & 1) ? 320 : T_D1; }
+static_assert(CH_V % 128 == 0 && CH_ST % 128 == 0 && OA_BYTES % 128 == 0, "operand alignment");
+static_assert(CH_OA + (OA_SLOTS + 1) * OA_BYTES <= CH_BYTES, "rows 64-127 of the last OA stay in bounds");
+// chain TMEM columns: [Kb | P] of two chunks (fp16 pairs); the state MMA's result as two
+// partial sums (Kb V + P[:, 0:64] S[0:64], double-buffered because the next chunk's Kb V is
+// accumulated early, and P[:, 64:128] S[64:128]); the output MMA's result, double-buffered
+constexpr uint32_t T_A = 0, A_COLS = 96, T_DS = 192, T_DS2 = 320, T_DO = 384, CH_COLS = 512;
+__host__ __device__ constexpr uint32_t ds_col(uint32_t c) { return T_DS + (c & 1) * 64; }
+__host__ __device__ constexpr uint32_t do_col(uint32_t c) { return T_DO + (c & 1) * 64; }
 
 __device__ __forceinline__ uint4 f16x8_pack(const float* x) {
   return make_uint4(tc::pack_f16x2(x[0], x[1]), tc::pack_f16x2(x[2], x[3]),
@@ -193,18 +207,22 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   using namespace tcs;
   using M = FrontMap<PERCH>;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t s_bar;
+  __shared__ uint64_t s_bar;                    // MMAs issued by thread 0
+  __shared__ uint64_t s_bar2;                   // MMAs issued by thread 32
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_range;
   __shared__ int s_anchored;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= plan.info[0]) return;
   const int gc = blockIdx.x, h = blockIdx.y;
+  // the three table reads are independent: issue them together (the grid has the table's
+  // capacity, so gc is in bounds even past the end of this batch's chunks)
+  const int plan_valid = plan.info[1], plan_chunks = plan.info[0];
+  const ChunkInfo ci = plan.chunks[gc];
+  if (plan_valid == 0 || gc >= plan_chunks) return;
   const int HV = P.HV;
   const int kh = h / (HV / P.HK);
-  const ChunkInfo ci = plan.chunks[gc];
   const int n = ci.n;
   const int64_t t0 = ci.t0;
   unsigned char* rec = records + (static_cast<int64_t>(gc) * HV + h) * static_cast<int64_t>(REC_BYTES);
@@ -222,7 +240,7 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   float* sA = reinterpret_cast<float*>(smem + M::R2);
   float* sT = reinterpret_cast<float*>(smem + M::R2 + C * SP * 4);
   float* sX = reinterpret_cast<float*>(smem + M::R2 + 2 * C * SP * 4);
-  constexpr uint32_t KTT = M::R2, A1 = M::R2 + 128 * 64 * 2;    // K~ (MN-major), A1 (K-major)
+  constexpr uint32_t KEA = M::R2, KTT = M::R2 + 64 * 128 * 2;  // K_end, K~ (MN-major)
   const int64_t bt = (static_cast<int64_t>(gc) * HV + h) * static_cast<int64_t>(REC_BYTES);
   uint4* blob = reinterpret_cast<uint4*>(records + bt + REC_BLOB) + tid;  // piece p at [p * NT]
 
@@ -233,6 +251,7 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   }
   if (tid == 0) {
     tc::mbar_init(&s_bar, 1);
+    tc::mbar_init(&s_bar2, 1);
     tc::fence_mbar_init();
     s_abort = 0;
     s_range = 0;
@@ -240,23 +259,22 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   const int row = 32 * (warp & 3) + lane;       // TMEM lane = M row
   const int chalf = warp >> 2;
   const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-  if (row < C) {                                // identity rows of L = [I; A_qk]
-    float idv[32];
-#pragma unroll
-    for (int e = 0; e < 32; ++e) idv[e] = (32 * chalf + e == row) ? 1.f : 0.f;
-#pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8)
-      tc::f16x8_store(smem, M::LMAT + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64)),
-                      idv + 8 * g8);
-  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
-  uint32_t phase = 0;
+  uint32_t phase = 0, phase2 = 0;
   auto mma_wait = [&]() {
     const bool ok = tc::mbar_wait_bounded(&s_bar, phase & 1, kWaitLimit);
     phase ^= 1;
+    if (!ok) s_abort = 1;
+    tc::fence_after_sync();
+  };
+  auto mma_wait2 = [&]() {                      // the second issuer's group as well
+    const bool ok = tc::mbar_wait_bounded(&s_bar, phase & 1, kWaitLimit) &&
+                    tc::mbar_wait_bounded(&s_bar2, phase2 & 1, kWaitLimit);
+    phase ^= 1;
+    phase2 ^= 1;
     if (!ok) s_abort = 1;
     tc::fence_after_sync();
   };
@@ -431,38 +449,56 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   tc::fence_after_sync();
 
   // ------------------------------------------------------------------ A-GEMM
-  if (tid == 0) {
+  // two issuing threads (one issues a tcgen05.mma only about every 100 cycles), the second
+  // into the X columns, which are free until A has been extracted
+  if (tid == 0 || tid == 32) {
+    const bool second = tid == 32;
     const uint32_t id = tc::idesc_f16(128, 64, tc::kBF16);
+    const uint32_t d = tmem + (second ? F_X : F_A);
     if constexpr (PERCH) {
       const uint64_t dak = tc::smem_desc(tc::smem_u32(smem + M::AK), 128, tc::dense_sbo(D));
       const uint64_t dbk = tc::smem_desc(tc::smem_u32(smem + M::BK), 128, tc::dense_sbo(D));
       const uint64_t dbl = tc::smem_desc(tc::smem_u32(smem + M::BKLO), 128, tc::dense_sbo(D));
+      if (!second) {
 #pragma unroll
-      for (int s = 0; s < D / 16; ++s)          // hi x hi
-        tc::mma_ss(tmem + F_A, tc::desc_add(dak, s * 256), tc::desc_add(dbk, s * 256), id, s > 0);
+        for (int s = 0; s < D / 16; ++s)        // hi x hi
+          tc::mma_ss(d, tc::desc_add(dak, s * 256), tc::desc_add(dbk, s * 256), id, s > 0);
 #pragma unroll
-      for (int s = 0; s < D / 16; ++s)          // hi x lo
-        tc::mma_ss(tmem + F_A, tc::desc_add(dak, s * 256), tc::desc_add(dbl, s * 256), id, 1);
+        for (int s = 0; s < D / 32; ++s)        // hi x lo, first half of K
+          tc::mma_ss(d, tc::desc_add(dak, s * 256), tc::desc_add(dbl, s * 256), id, 1);
+      } else {
 #pragma unroll
-      for (int s = 0; s < D / 16; ++s)          // lo x hi (low half from TMEM)
-        tc::mma_ts(tmem + F_A, tmem + F_ALO + s * 8, tc::desc_add(dbk, s * 256), id, 1);
+        for (int s = D / 32; s < D / 16; ++s)   // hi x lo, second half of K
+          tc::mma_ss(d, tc::desc_add(dak, s * 256), tc::desc_add(dbl, s * 256), id, s > D / 32);
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s)        // lo x hi (low half from TMEM)
+          tc::mma_ts(d, tmem + F_ALO + s * 8, tc::desc_add(dbk, s * 256), id, 1);
+      }
     } else {
       const uint64_t dak = tc::smem_desc(tc::smem_u32(smem + M::AK), M::AK_LBO, M::AK_SBO);
+      const int s0 = second ? D / 32 : 0;
 #pragma unroll
-      for (int s = 0; s < D / 16; ++s)          // [K; Q] K^T on the raw rows
-        tc::mma_ss(tmem + F_A, tc::desc_add(dak, s * 2 * M::AK_LBO), tc::desc_add(dak, s * 2 * M::AK_LBO),
-                   id, s > 0);
+      for (int s = s0; s < s0 + D / 32; ++s)    // [K; Q] K^T on the raw rows, half of K each
+        tc::mma_ss(d, tc::desc_add(dak, s * 2 * M::AK_LBO), tc::desc_add(dak, s * 2 * M::AK_LBO),
+                   id, s > s0);
     }
-    tc::mma_commit(&s_bar);
+    tc::mma_commit(second ? &s_bar2 : &s_bar);
   }
-  mma_wait();
+  mma_wait2();
 
   // ------------------------------------------------------------------ A_kk, A_qk
   {
-    uint32_t r0[16], r1[16];
+    uint32_t r0[16], r1[16], q0[16], q1[16];
     tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf, r0);
     tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf + 16, r1);
+    tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf, q0);
+    tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf + 16, q1);
     tc::tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      r0[e] = __float_as_uint(__uint_as_float(r0[e]) + __uint_as_float(q0[e]));
+      r1[e] = __float_as_uint(__uint_as_float(r1[e]) + __uint_as_float(q1[e]));
+    }
     const bool is_k = row < C;
     const int i = is_k ? row : row - C;
     const float ri = is_k ? (PERCH ? 1.f : sRK[i]) * sBeta[i] : (PERCH ? 1.f : sRQ[i]);
@@ -514,32 +550,6 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   __syncthreads();
 
   // ------------------------------------------------------------------ solve
-  // K_end = k^ exp(G_last - G_m) needs no solve: warps 2-7 write it to the record (row
-  // pieces of 8 channels, MN-major order) while warps 0-1 invert the diagonal blocks
-  if (warp >= 2) {
-    for (int u = tid - 64; u < C * (D / 8); u += NT - 64) {
-      const int m = (u >> 7) * 8 + (u & 7), c0 = ((u >> 3) & 15) * 8;
-      float kx[8], ke[8];
-      tc::bf16x8_load(kq_piece(false, m, c0), kx);
-      const float rk = sRK[m];
-      if constexpr (PERCH) {
-        const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
-        const float4 e0 = *reinterpret_cast<const float4*>(sG + m * M::GS + c0);
-        const float4 e1 = *reinterpret_cast<const float4*>(sG + m * M::GS + c0 + 4);
-        const float4 l0 = *reinterpret_cast<const float4*>(sG + (C - 1) * M::GS + c0);
-        const float4 l1 = *reinterpret_cast<const float4*>(sG + (C - 1) * M::GS + c0 + 4);
-        const float Em[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-        const float El[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ke[e] = kx[e] * rk * __fdividef(El[e], Em[e]);
-      } else {
-        const float fe = rk * sEGL[m];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ke[e] = kx[e] * fe;
-      }
-      *reinterpret_cast<uint4*>(rec + REC_KE + tc::mn_offset(m, c0, KE_LBO, KE_SBO)) = f16x8_pack(ke);
-    }
-  }
   if (warp < 2) {                               // diagonal 16x16 blocks, one column per lane
     const int base = (warp * 2 + (lane >> 4)) * 16, col = lane & 15;
     float t[16];
@@ -642,49 +652,79 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   __syncthreads();
   tc::fence_after_sync();
 
-  // ------------------------------------------------------------------ X = [I; A_qk] TB
-  if (tid == 0) {
+  // ------------------------------------------------------------------ A1o = A_qk TB, Kb = K_end^T TB
+  // With W = TB K~ the remaining products all start from TB: Kb = K_end^T TB, A1o = A_qk TB,
+  // then P = -K_end^T W = -Kb K~ and A_qk W = A1o K~.  A1o is rows 64-127 of the
+  // [*; A_qk] TB product (rows 0-63 of that operand are never read back).
+  if (tid == 32) {
     const uint32_t id = tc::idesc_f16(128, 64, tc::kF16, false, false, true);
     const uint64_t dl = tc::smem_desc(tc::smem_u32(smem + M::LMAT), 128, tc::dense_sbo(64));
     const uint64_t dt = tc::smem_desc(tc::smem_u32(smem + M::TBT), TB_LBO, TB_SBO);
 #pragma unroll
     for (int s = 0; s < C / 16; ++s)
       tc::mma_ss(tmem + F_X, tc::desc_add(dl, s * 256), tc::desc_add(dt, s * 2 * TB_LBO), id, s > 0);
-    tc::mma_commit(&s_bar);
+    tc::mma_commit(&s_bar2);
   }
-  // K~ = k^ exp(G_m) (smem, the Y operand) as row pieces of 8 channels in the MN-major
-  // order; the solve area is free
+  // K_end = k^ exp(G_last - G_m) (A operand K_end^T, MN-major) and K~ = k^ exp(G_m) (B
+  // operand of the second round, MN-major) into the consumed solve area, row pieces of 8
+  // channels
   for (int u = tid; u < C * (D / 8); u += NT) {
     const int m = (u >> 7) * 8 + (u & 7), c0 = ((u >> 3) & 15) * 8;
-    float kx[8], kt[8];
+    float kx[8], ke[8], kt[8];
     tc::bf16x8_load(kq_piece(false, m, c0), kx);
     const float rk = sRK[m];
     if constexpr (PERCH) {
       const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
       const float4 e0 = *reinterpret_cast<const float4*>(sG + m * M::GS + c0);
       const float4 e1 = *reinterpret_cast<const float4*>(sG + m * M::GS + c0 + 4);
+      const float4 l0 = *reinterpret_cast<const float4*>(sG + (C - 1) * M::GS + c0);
+      const float4 l1 = *reinterpret_cast<const float4*>(sG + (C - 1) * M::GS + c0 + 4);
       const float4 a0 = *reinterpret_cast<const float4*>(sGA + c0);
       const float4 a1 = *reinterpret_cast<const float4*>(sGA + c0 + 4);
       const float Em[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+      const float El[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
       const float ea[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) kt[e] = kx[e] * rk * Em[e] * ea[e];
+      for (int e = 0; e < 8; ++e) {
+        ke[e] = kx[e] * rk * __fdividef(El[e], Em[e]);
+        kt[e] = kx[e] * rk * Em[e] * ea[e];
+      }
     } else {
-      const float ft = rk * sEG[m];
+      const float fe = rk * sEGL[m], ft = rk * sEG[m];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) kt[e] = kx[e] * ft;
+      for (int e = 0; e < 8; ++e) {
+        ke[e] = kx[e] * fe;
+        kt[e] = kx[e] * ft;
+      }
     }
+    tc::f16x8_store(smem, KEA + tc::mn_offset(m, c0, KE_LBO, KE_SBO), ke);
     tc::f16x8_store(smem, KTT + tc::mn_offset(m, c0, KT_LBO, KT_SBO), kt);
   }
   if (tid < D) reinterpret_cast<float*>(rec + REC_GAM)[tid] = sGam[tid];
   tc::fence_async_smem();
-  mma_wait();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (tid == 0) {
+    const uint32_t id = tc::idesc_f16(128, 64, tc::kF16, false, true, true);
+    const uint64_t dke = tc::smem_desc(tc::smem_u32(smem + KEA), KE_LBO, KE_SBO);
+    const uint64_t dtb = tc::smem_desc(tc::smem_u32(smem + M::TBT), TB_LBO, TB_SBO);
+#pragma unroll
+    for (int s = 0; s < C / 16; ++s)
+      tc::mma_ss(tmem + F_A, tc::desc_add(dke, s * 2 * KE_LBO), tc::desc_add(dtb, s * 2 * TB_LBO), id, s > 0);
+    tc::mma_commit(&s_bar);
+  }
+  mma_wait2();
 
-  // ------------------------------------------------------------------ A1 = X
+  // ------------------------------------------------------------------ Kb, A1o out
+  // Kb (fp16): record pieces 0-3 and the K-major A operand of P (consumed [*; A_qk] area);
+  // A1o (fp16): columns 0-63 of the output operand and rows 64-127 of the A operand of
+  // A1o K~ (in the consumed TB area; its rows 0-63 fall on Kb's rows 64-127, unread)
+  constexpr uint32_t KBA = M::LMAT, A1A = M::TBT - 64 * 64 * 2;
   {
     uint32_t r0[16], r1[16];
-    tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf, r0);
-    tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf + 16, r1);
+    tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf, r0);
+    tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf + 16, r1);
     tc::tmem_wait_ld();
     float x[32];
 #pragma unroll
@@ -695,8 +735,24 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
 #pragma unroll
     for (int g8 = 0; g8 < 4; ++g8) {
       const uint4 v = f16x8_pack(x + 8 * g8);
-      *reinterpret_cast<uint4*>(smem + A1 + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64))) = v;
-      blob[g8 * NT] = v;                        // pieces 0-3
+      blob[g8 * NT] = v;
+      *reinterpret_cast<uint4*>(smem + KBA + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64))) = v;
+    }
+    if (row >= C) {                             // warp-uniform: warps 2, 3, 6, 7
+      tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf, r0);
+      tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf + 16, r1);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        x[e] = __uint_as_float(r0[e]);
+        x[e + 16] = __uint_as_float(r1[e]);
+      }
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        const uint4 v = f16x8_pack(x + 8 * g8);
+        *reinterpret_cast<uint4*>(rec + REC_OA + tc::cm_offset(row - C, 32 * chalf + 8 * g8, OA_LBO, OA_SBO)) = v;
+        *reinterpret_cast<uint4*>(smem + A1A + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64))) = v;
+      }
     }
   }
   tc::fence_async_smem();
@@ -704,74 +760,80 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   __syncthreads();
   tc::fence_after_sync();
 
-  // ------------------------------------------------------------------ Y = A1 K~
-  if (tid == 0) {
+  // ------------------------------------------------------------------ Kb K~, A1o K~
+  if (tid == 0 || tid == 32) {
+    const bool second = tid == 32;
     const uint32_t id = tc::idesc_f16(128, 128, tc::kF16, false, false, true);
-    const uint64_t da = tc::smem_desc(tc::smem_u32(smem + A1), 128, tc::dense_sbo(64));
+    const uint64_t da = tc::smem_desc(tc::smem_u32(smem + (second ? A1A : KBA)), 128, tc::dense_sbo(64));
     const uint64_t dk = tc::smem_desc(tc::smem_u32(smem + KTT), KT_LBO, KT_SBO);
+    const uint32_t d = tmem + (second ? F_Y : F_A);
 #pragma unroll
     for (int s = 0; s < C / 16; ++s)
-      tc::mma_ss(tmem + F_Y, tc::desc_add(da, s * 256), tc::desc_add(dk, s * 2 * KT_LBO), id, s > 0);
-    tc::mma_commit(&s_bar);
+      tc::mma_ss(d, tc::desc_add(da, s * 256), tc::desc_add(dk, s * 2 * KT_LBO), id, s > 0);
+    tc::mma_commit(second ? &s_bar2 : &s_bar);
   }
-  mma_wait();
+  mma_wait2();
 
-  // ------------------------------------------------------------------ A2 = [0; Q~] - Y
-  {
-    uint32_t ry[2][32];
+  // ------------------------------------------------------------------ P, A2o out
+  // P = -Kb K~: record pieces 4-11; A2o = Q~ - A1o K~ (rows 64-127): columns 64-191 of the
+  // output operand
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t a[16], b[16];
-      tc::tmem_ld16(tmem + lane_addr + F_Y + 64 * chalf + 32 * half, a);
-      tc::tmem_ld16(tmem + lane_addr + F_Y + 64 * chalf + 32 * half + 16, b);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        ry[half][e] = a[e];
-        ry[half][e + 16] = b[e];
-      }
-    }
+  for (int half = 0; half < 2; ++half) {
+    const int c0 = 64 * chalf + 32 * half;
+    uint32_t r0[16], r1[16];
+    float x[32];
+    tc::tmem_ld16(tmem + lane_addr + F_A + c0, r0);
+    tc::tmem_ld16(tmem + lane_addr + F_A + c0 + 16, r1);
     tc::tmem_wait_ld();
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int c0 = 64 * chalf + 32 * half;
-      float x[32];
-      if (row >= C) {                           // Q~ = q scale/|q| exp(G)
-        const int i = row - C;
-        const float rq = sRQ[i];
+    for (int e = 0; e < 16; ++e) {
+      x[e] = -__uint_as_float(r0[e]);
+      x[e + 16] = -__uint_as_float(r1[e]);
+    }
 #pragma unroll
-        for (int g8 = 0; g8 < 4; ++g8) {
-          float qv[8];
-          tc::bf16x8_load(kq_piece(true, i, c0 + 8 * g8), qv);
-          if constexpr (PERCH) {
-            const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
-            const float4 ga = *reinterpret_cast<const float4*>(sG + i * M::GS + c0 + 8 * g8);
-            const float4 gb = *reinterpret_cast<const float4*>(sG + i * M::GS + c0 + 8 * g8 + 4);
-            const float4 aa = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8);
-            const float4 ab = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8 + 4);
-            const float gv[8] = {ga.x * aa.x, ga.y * aa.y, ga.z * aa.z, ga.w * aa.w,
-                                 gb.x * ab.x, gb.y * ab.y, gb.z * ab.z, gb.w * ab.w};
+    for (int g8 = 0; g8 < 4; ++g8) blob[(4 + 4 * half + g8) * NT] = f16x8_pack(x + 8 * g8);
+    if (row >= C) {                             // Q~ = q scale/|q| exp(G)
+      tc::tmem_ld16(tmem + lane_addr + F_Y + c0, r0);
+      tc::tmem_ld16(tmem + lane_addr + F_Y + c0 + 16, r1);
+      const int i = row - C;
+      const float rq = sRQ[i];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * rq * gv[e];
-          } else {
-            const float f = rq * sEG[i];
+      for (int g8 = 0; g8 < 4; ++g8) {
+        float qv[8];
+        tc::bf16x8_load(kq_piece(true, i, c0 + 8 * g8), qv);
+        if constexpr (PERCH) {
+          const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
+          const float4 ga = *reinterpret_cast<const float4*>(sG + i * M::GS + c0 + 8 * g8);
+          const float4 gb = *reinterpret_cast<const float4*>(sG + i * M::GS + c0 + 8 * g8 + 4);
+          const float4 aa = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8);
+          const float4 ab = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8 + 4);
+          const float gv[8] = {ga.x * aa.x, ga.y * aa.y, ga.z * aa.z, ga.w * aa.w,
+                               gb.x * ab.x, gb.y * ab.y, gb.z * ab.z, gb.w * ab.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * f;
-          }
+          for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * rq * gv[e];
+        } else {
+          const float f = rq * sEG[i];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * f;
         }
-      } else {
+      }
+      tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[e] = 0.f;
+      for (int e = 0; e < 16; ++e) {
+        x[e] -= __uint_as_float(r0[e]);
+        x[e + 16] -= __uint_as_float(r1[e]);
       }
 #pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] -= __uint_as_float(ry[half][e]);
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) blob[(4 + 4 * half + g8) * NT] = f16x8_pack(x + 8 * g8);   // 4-11
+      for (int g8 = 0; g8 < 4; ++g8)
+        *reinterpret_cast<uint4*>(rec + REC_OA + tc::cm_offset(i, C + c0 + 8 * g8, OA_LBO, OA_SBO)) =
+            f16x8_pack(x + 8 * g8);
     }
   }
 
   if (PERCH && s_range && tid == 0) raise_device_error(P.err, KDA_DEVERR_DECAY_RANGE);
-  if (s_abort) {
-    tc::mbar_wait_bounded(&s_bar, (phase ^ 1) & 1, kWaitLimit);   // the phase that timed out
+  if (s_abort) {                                // the phases that may have timed out
+    tc::mbar_wait_bounded(&s_bar, (phase ^ 1) & 1, kWaitLimit);
+    tc::mbar_wait_bounded(&s_bar2, (phase2 ^ 1) & 1, kWaitLimit);
     if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
   }
   tc::fence_before_sync();
@@ -780,30 +842,40 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   if (warp == 0) tc::tmem_dealloc(tmem, F_COLS);
 }
 
-// One CTA per (sequence, value head, 64 value columns), warp-specialised:
-//   compute warps 0-7 keep the state slice in registers and run the sequential part of
-//     every chunk -- [E; O] = A1 V + A2 S, extracting E, dS = K_end^T E, S <- gam S + dS --
-//     with the MMAs of each group split between threads 0 and 128 (one thread issues a
-//     tcgen05.mma only about every 100 cycles, half the rate at which the tensor core
-//     completes these N = 64 shapes), into separate accumulators;
-//   data warps 8-11 move everything else concurrently: the o rows of the previous chunk
-//     to global memory, and the next chunk's values (fetched three chunks ahead,
-//     converted to fp16) and A1 | A2 pieces (global -> registers -> tensor memory).
-// The two sides hand over through monotonic step counters in shared memory.
+// One CTA per (sequence, value head, 64 value columns), warp-specialised into four
+// groups that each run their own loop over the sequence's chunks:
+//   compute warps 0-7 keep the state slice in registers (thread = key channel, 32 value
+//     columns) and run the sequential part: D = Kb V + P S, then S <- diag(gam) S + D,
+//     publishing the fp16 copy of S.  The MMA group is split between threads 0 and 128
+//     into separate accumulators (one thread issues a tcgen05.mma only about every 90
+//     cycles, slower than the tensor core completes these N = 64 shapes); thread 0 also
+//     accumulates the next chunk's Kb V ahead of time;
+//   operand warps 8-11 prepare chunks ahead: values (bf16 -> fp16, fetched two chunks
+//     ahead), [Kb | P] global -> registers -> tensor memory, gamma -> shared memory;
+//   lane 0 of warp 14 bulk-copies [A1o | A2o] and issues the output MMA
+//     O = [A1o | A2o] [V; S] once the chunk's state MMA is queued, so that it runs beside
+//     the state update;
+//   output warps 12-13 (TMEM lanes 0-63) move the o rows to global memory.
+// The groups hand over through monotonic step counters in shared memory.  Every wait is
+// bounded; a timeout sets s_abort, each group leaves its loop at a barrier whose
+// reduction makes all of its threads agree (or, for the single issuing thread, at once),
+// and the device error word is raised.
 template <bool SBF16>
 __global__ void __launch_bounds__(tcs::NTC, 1)
     tc_chain_kernel(Problem P, PlanView plan, const unsigned char* records) {
   using namespace tcs;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t s_bar1;                   // [E; O]: both halves (threads 0 and 128)
-  __shared__ uint64_t s_bar2;                   // dS: both halves (threads 0 and 128)
-  __shared__ uint64_t s_a1v_bar;                // A1 V of a chunk, issued by thread 32
-  __shared__ uint64_t s_ld_bar[2];
+  __shared__ uint64_t s_bar_s;                  // state MMA of a chunk: both halves (threads 0, 128)
+  __shared__ uint64_t s_bar_o;                  // output MMA of a chunk
+  __shared__ uint64_t s_oa_bar[OA_SLOTS];       // bulk copies of [A1o | A2o]
+  __shared__ uint64_t s_drain;                  // abort only: every MMA issued so far
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_e_done;                      // chunks whose E and o rows are extracted
-  __shared__ int s_next_ready;                  // chunks whose V and A1 | A2 are in place
-  __shared__ int s_ost_free;                    // chunks whose o rows are stored
+  __shared__ int s_ready;                       // chunks whose V, [Kb | P] and gamma are in place
+  __shared__ int s_issued;                      // state-MMA halves issued (two per chunk)
+  __shared__ int s_ps_done;                     // chunks whose state MMA has completed
+  __shared__ int s_o_done;                      // chunks whose output MMA has completed
+  __shared__ int s_o_free;                      // chunks whose o rows have left tensor memory
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (plan.info[1] == 0) return;
@@ -815,69 +887,25 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
   const int64_t c0 = plan.seq_chunk0[b];
   const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + vt * BV;
   const uint32_t sb = tc::smem_u32(smem);
-  const bool data_warp = warp >= NT / 32;
-  const int dt = tid - NT;                      // data thread 0..127
+  float* s_gam = reinterpret_cast<float*>(smem + CH_GAM);
   auto rec = [&](uint32_t c) -> const unsigned char* {
     return records + ((c0 + c) * HV + h) * static_cast<int64_t>(REC_BYTES);
   };
-  auto ke_off = [](uint32_t c) -> uint32_t { return CH_KE + (c & 1) * REC_TAIL; };
-  auto v_off = [](uint32_t c) -> uint32_t { return CH_V + (c % 3) * V_BYTES; };
+  auto v_off = [](uint32_t c) -> uint32_t { return CH_V + (c % V_SLOTS) * V_BYTES; };
+  auto s_off = [](uint32_t c) -> uint32_t { return CH_ST + (c % S_SLOTS) * S_BYTES; };
+  auto oa_off = [](uint32_t c) -> uint32_t { return CH_OA + (c % OA_SLOTS) * OA_BYTES; };
   auto chunk_n = [&](uint32_t c) -> int {
     const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
     return static_cast<int>(min(static_cast<int64_t>(C), static_cast<int64_t>(eos) - t0));
   };
-
-  // ---- data-warp work
-  auto issue_v = [&](uint32_t c) {              // raw bf16 v -> MN-major positions of V[c % 3]
-    const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
-    const int n = chunk_n(c);
-    const uint32_t dst = sb + v_off(c);
-    for (int u = dt; u < C * (BV / 8); u += NTD) {
-      const int m = (u >> 6) * 8 + (u & 7), j0 = ((u >> 3) & 7) * 8;
-      const bool live = m < n;
-      const int64_t t = live ? t0 + m : t0;
-      tc::cp_async16(dst + tc::mn_offset(m, j0, OP_LBO, OP_SBO),
-                     static_cast<const uint16_t*>(P.v) + t * P.v_stride + static_cast<int64_t>(h) * D + vt * BV + j0,
-                     live ? 16u : 0u);
-    }
-    tc::cp_async_commit();
-  };
-  auto convert_v = [&](uint32_t c) {            // bf16 -> fp16 in place
-    uint4* p = reinterpret_cast<uint4*>(smem + v_off(c));
-    for (int u = dt; u < static_cast<int>(V_BYTES / 16); u += NTD) {
-      float x[8];
-      tc::bf16x8_load(reinterpret_cast<const unsigned char*>(p + u), x);
-      p[u] = f16x8_pack(x);
-    }
-  };
-  auto store_o = [&](uint32_t c) {              // o rows of chunk c staged in OST
-    const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
-    const int n = chunk_n(c);
-#pragma unroll
-    for (int k = 0; k < (C * BV / 4) / NTD; ++k) {
-      const int idx = dt + k * NTD, i = idx / (BV / 4), q = idx % (BV / 4);
-      if (i < n)
-        *reinterpret_cast<float4*>(P.o + ((t0 + i) * HV + h) * D + vt * BV + q * 4) =
-            *reinterpret_cast<const float4*>(smem + CH_OST + (i * OS + q * 4) * 4);
-    }
-  };
-  // a data thread serves TMEM lane 32 (warp & 3) + lane for both column halves, i.e. the
-  // A1 | A2 pieces of compute threads dt and dt + 128 (12 pieces each)
-  uint4 ablob[2 * BLOB_PIECES];
-  auto load_blob = [&](uint32_t c) {
-    const uint4* src = reinterpret_cast<const uint4*>(rec(c) + REC_BLOB) + dt;
-#pragma unroll
-    for (int p = 0; p < static_cast<int>(BLOB_PIECES); ++p) {
-      ablob[p] = __ldg(src + p * NT);
-      ablob[BLOB_PIECES + p] = __ldg(src + p * NT + NTD);
-    }
-  };
+  auto aborted = [&]() -> bool { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
   auto wait_flag = [&](int* flag, int target) -> bool {   // bounded
     for (uint32_t i = 0; i < kWaitLimit; ++i) {
       if (*reinterpret_cast<volatile int*>(flag) >= target) {
         __threadfence_block();
         return true;
       }
+      if (aborted()) return false;
       __nanosleep(20);
     }
     s_abort = 1;
@@ -887,43 +915,86 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
     __threadfence_block();
     *reinterpret_cast<volatile int*>(flag) = value;
   };
+  auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {   // bounded
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+      if (tc::mbar_try_wait(bar, parity)) {
+        tc::fence_after_sync();
+        return true;
+      }
+      if ((i & 255) == 255 && aborted()) return false;
+    }
+    s_abort = 1;
+    return false;
+  };
 
-  if (data_warp) {
-    issue_v(0);
-    if (nchunks > 1) issue_v(1);
-    if (nchunks > 2) issue_v(2);
-    load_blob(0);
-  }
   if (warp == 0) {
     tc::tmem_alloc(&s_tmem, CH_COLS);
     tc::tmem_relinquish();
   }
   if (tid == 0) {
-    tc::mbar_init(&s_bar1, 2);
-    tc::mbar_init(&s_bar2, 2);
-    tc::mbar_init(&s_a1v_bar, 1);
-    tc::mbar_init(&s_ld_bar[0], 1);
-    tc::mbar_init(&s_ld_bar[1], 1);
+    tc::mbar_init(&s_bar_s, 2);
+    tc::mbar_init(&s_bar_o, 1);
+    for (uint32_t i = 0; i < OA_SLOTS; ++i) tc::mbar_init(&s_oa_bar[i], 1);
+    tc::mbar_init(&s_drain, 3);
     tc::fence_mbar_init();
     s_abort = 0;
-    s_e_done = 0;
-    s_next_ready = 0;
-    s_ost_free = 0;
+    s_ready = 0;
+    s_issued = 0;
+    s_ps_done = 0;
+    s_o_done = 0;
+    s_o_free = 0;
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
-  const uint32_t id1 = tc::idesc_f16(128, BV, tc::kF16, false, false, true);
-  const uint32_t id2 = tc::idesc_f16(128, BV, tc::kF16, false, true, true);
-  const uint64_t dST = tc::smem_desc(sb + CH_ST, OP_LBO, OP_SBO);
-  const uint64_t dET = tc::smem_desc(sb + CH_ET, OP_LBO, OP_SBO);
+  const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  const uint32_t id_s = tc::idesc_f16(128, BV, tc::kF16, false, false, true);   // A in TMEM
+  const uint32_t id_o = tc::idesc_f16(128, BV, tc::kF16, false, false, true);   // A K-major smem
   const uint64_t dV0 = tc::smem_desc(sb + CH_V, OP_LBO, OP_SBO);
-  const uint64_t dKE0 = tc::smem_desc(sb + CH_KE, KE_LBO, KE_SBO);
+  const uint64_t dS0 = tc::smem_desc(sb + CH_ST, OP_LBO, OP_SBO);
+  const uint64_t dOA0 = tc::smem_desc(sb + CH_OA, OA_LBO, OA_SBO);
+  constexpr int W_OPER = NT / 32, W_OUT = W_OPER + NTD / 32, W_ISSUE = W_OUT + NTO / 32;
 
-  if (data_warp) {
-    // -------------------------------------------------------------------- data warps
-    const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  if (warp >= W_OPER && warp < W_OUT) {
+    // ------------------------------------------------------------------ operand warps
+    const int dt = tid - NT;                    // 0..127
+    auto issue_v = [&](uint32_t c) {            // raw bf16 v -> MN-major positions of V[c % 5]
+      const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
+      const int n = chunk_n(c);
+      const uint32_t dst = sb + v_off(c);
+      for (int u = dt; u < C * (BV / 8); u += NTD) {
+        const int m = (u >> 6) * 8 + (u & 7), j0 = ((u >> 3) & 7) * 8;
+        const bool live = m < n;
+        const int64_t t = live ? t0 + m : t0;
+        tc::cp_async16(dst + tc::mn_offset(m, j0, OP_LBO, OP_SBO),
+                       static_cast<const uint16_t*>(P.v) + t * P.v_stride + static_cast<int64_t>(h) * D + vt * BV + j0,
+                       live ? 16u : 0u);
+      }
+      tc::cp_async_commit();
+    };
+    auto convert_v = [&](uint32_t c) {          // bf16 -> fp16 in place
+      uint4* p = reinterpret_cast<uint4*>(smem + v_off(c));
+      for (int u = dt; u < static_cast<int>(V_BYTES / 16); u += NTD) {
+        float x[8];
+        tc::bf16x8_load(reinterpret_cast<const unsigned char*>(p + u), x);
+        p[u] = f16x8_pack(x);
+      }
+    };
+    // a thread serves TMEM lane 32 (warp & 3) + lane for both column halves, i.e. the
+    // [Kb | P] pieces of compute threads dt and dt + 128 (12 pieces each), and key channel
+    // dt of gamma
+    uint4 ablob[2 * BLOB_PIECES];
+    float gam_next = 0.f;
+    auto load_blob = [&](uint32_t c) {
+      const uint4* src = reinterpret_cast<const uint4*>(rec(c) + REC_BLOB) + dt;
+#pragma unroll
+      for (int p = 0; p < static_cast<int>(BLOB_PIECES); ++p) {
+        ablob[p] = __ldg(src + p * NT);
+        ablob[BLOB_PIECES + p] = __ldg(src + p * NT + NTD);
+      }
+      gam_next = __ldg(reinterpret_cast<const float*>(rec(c) + REC_GAM) + dt);
+    };
     auto store_blob = [&](uint32_t c) {
       const uint32_t base = tmem + lane_addr + T_A + (c & 1) * A_COLS;
 #pragma unroll
@@ -947,50 +1018,107 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
       }
       tc::tmem_wait_st();
     };
-    // V(q) and A1 | A2 of chunk q in place; A[q & 1] last held chunk q - 2's operands
-    auto prepare = [&](uint32_t q) -> bool {
-      // value groups issued after V(q) so far: V(1), V(2) for q = 0 (issued up front),
-      // otherwise V(q + 1) only (V(q + 2) is issued after chunk q - 1's o rows)
-      const uint32_t newer = q == 0 ? min(nchunks - 1, 2u) : (q + 1 < nchunks ? 1u : 0u);
-      if (newer == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+    issue_v(0);
+    if (nchunks > 1) issue_v(1);
+    load_blob(0);
+    for (uint32_t q = 0; q < nchunks; ++q) {
+      // V(q + 2) into the slot of V(q - 3) (its Kb V and output MMA are done), then V(q)
+      // in place: groups issued after V(q) are V(q + 1) and V(q + 2) where they exist
+      bool bad = q >= 3 && !wait_flag(&s_o_done, static_cast<int>(q) - 2);
+      // the tensor-memory buffer of q held chunk q - 2, read by that chunk's state MMA
+      bad = bad || (q >= 2 && !wait_flag(&s_ps_done, static_cast<int>(q) - 1));
+      if (tc::named_sync_or(2, NTD, bad || aborted())) break;
+      if (q + 2 < nchunks) issue_v(q + 2);
+      const uint32_t newer = min(nchunks - 1, q + 2) - q;
+      if (newer == 0) tc::cp_async_wait_all();
       else if (newer == 1) tc::cp_async_wait_one();
-      else tc::cp_async_wait_all();
+      else asm volatile("cp.async.wait_group 2;" ::: "memory");
       tc::named_sync(2, NTD);
-      if (q >= 2 && !wait_flag(&s_e_done, static_cast<int>(q) - 1)) return false;
+      tc::fence_after_sync();
       convert_v(q);
       store_blob(q);
+      s_gam[(q % GAM_SLOTS) * D + dt] = gam_next;
       if (q + 1 < nchunks) load_blob(q + 1);
       tc::fence_async_smem();
       tc::fence_before_sync();
       tc::named_sync(2, NTD);
-      if (dt == 0) set_flag(&s_next_ready, static_cast<int>(q) + 1);
-      return true;
-    };
-    // chunk c's o rows out, then V(c + 3) into V[c % 3] (chunk c's A1 V is complete)
-    auto finish = [&](uint32_t c) -> bool {
-      if (!wait_flag(&s_e_done, static_cast<int>(c) + 1)) return false;
-      store_o(c);
-      if (c + 3 < nchunks) issue_v(c + 3);
-      tc::named_sync(2, NTD);
-      if (dt == 0) set_flag(&s_ost_free, static_cast<int>(c) + 1);
-      return true;
-    };
-    if (prepare(0)) {
-      for (uint32_t c = 0; c < nchunks; ++c) {
-        if (c + 1 < nchunks && !prepare(c + 1)) break;
-        if (!finish(c)) break;
-      }
+      if (dt == 0) set_flag(&s_ready, static_cast<int>(q) + 1);
     }
     tc::cp_async_wait_all();
+  } else if (warp >= W_OUT && warp < W_ISSUE) {
+    // ------------------------------------------------------------------ output warps
+    const int dq = tid - NT - NTD;              // 0..63, TMEM lane and token row
+    float* op = reinterpret_cast<float*>(smem + CH_OST) + dq * OS;
+    for (uint32_t c = 0; c < nchunks; ++c) {
+      const bool bad = !wait_bar(&s_bar_o, c & 1);
+      if (tc::named_sync_or(3, NTO, bad || aborted())) break;
+      if (dq == 0) set_flag(&s_o_done, static_cast<int>(c) + 1);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t r0[16], r1[16];
+        tc::tmem_ld16(tmem + lane_addr + do_col(c) + 32 * half, r0);
+        tc::tmem_ld16(tmem + lane_addr + do_col(c) + 32 * half + 16, r1);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          *reinterpret_cast<float4*>(op + 32 * half + e) =
+              make_float4(__uint_as_float(r0[e]), __uint_as_float(r0[e + 1]),
+                          __uint_as_float(r0[e + 2]), __uint_as_float(r0[e + 3]));
+          *reinterpret_cast<float4*>(op + 32 * half + 16 + e) =
+              make_float4(__uint_as_float(r1[e]), __uint_as_float(r1[e + 1]),
+                          __uint_as_float(r1[e + 2]), __uint_as_float(r1[e + 3]));
+        }
+      }
+      tc::fence_before_sync();
+      tc::named_sync(3, NTO);
+      if (dq == 0) set_flag(&s_o_free, static_cast<int>(c) + 1);
+      const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
+      const int n = chunk_n(c);
+#pragma unroll 4
+      for (int k = 0; k < (C * BV / 4) / NTO; ++k) {
+        const int idx = dq + k * NTO, i = idx / (BV / 4), q4 = idx % (BV / 4);
+        if (i < n)
+          *reinterpret_cast<float4*>(P.o + ((t0 + i) * HV + h) * D + vt * BV + q4 * 4) =
+              *reinterpret_cast<const float4*>(smem + CH_OST + (i * OS + q4 * 4) * 4);
+      }
+      tc::named_sync(3, NTO);                   // staging reads done before it is refilled
+    }
+  } else if (warp == W_ISSUE) {
+    // ------------------------------------------------------------------ output-MMA issuer
+    if (lane == 0) {
+      auto load_oa = [&](uint32_t c) {          // [A1o | A2o] of chunk c, one bulk copy
+        tc::mbar_arrive_expect_tx(&s_oa_bar[c % OA_SLOTS], OA_BYTES);
+        tc::bulk_load(sb + oa_off(c), rec(c) + REC_OA, OA_BYTES, &s_oa_bar[c % OA_SLOTS]);
+      };
+      for (uint32_t q = 0; q < min(nchunks, OA_SLOTS); ++q) load_oa(q);
+      for (uint32_t c = 0; c < nchunks; ++c) {
+        // both halves of the state MMA queued; D_O[c & 1] free (o rows of c - 2 out, and of
+        // c - 1, which also keeps the completion barrier one phase ahead of its waiters)
+        if (!wait_flag(&s_issued, 2 * static_cast<int>(c) + 2)) break;
+        if (!wait_flag(&s_o_free, static_cast<int>(c))) break;
+        if (!wait_bar(&s_oa_bar[c % OA_SLOTS], (c / OA_SLOTS) & 1)) break;
+        const uint32_t d = tmem + do_col(c);
+        const uint64_t da = tc::desc_add(dOA0, (c % OA_SLOTS) * OA_BYTES);
+        const uint64_t dv = tc::desc_add(dV0, (c % V_SLOTS) * V_BYTES);
+        const uint64_t ds = tc::desc_add(dS0, (c % S_SLOTS) * S_BYTES);
+#pragma unroll
+        for (int s = 0; s < C / 16; ++s)
+          tc::mma_ss(d, tc::desc_add(da, s * 2 * OA_LBO), tc::desc_add(dv, s * 2 * OP_LBO), id_o, s > 0);
+#pragma unroll
+        for (int s = 0; s < D / 16; ++s)
+          tc::mma_ss(d, tc::desc_add(da, (C / 16 + s) * 2 * OA_LBO), tc::desc_add(ds, s * 2 * OP_LBO), id_o, 1);
+        tc::mma_commit(&s_bar_o);
+        // the slot of chunk c - 1 is free once its output MMA is done
+        if (c >= 1 && c - 1 + OA_SLOTS < nchunks) {
+          if (!wait_flag(&s_o_done, static_cast<int>(c))) break;
+          load_oa(c - 1 + OA_SLOTS);
+        }
+      }
+    }
   } else {
-    // -------------------------------------------------------------------- compute warps
+    // ------------------------------------------------------------------ compute warps
     const int row = 32 * (warp & 3) + lane;     // TMEM lane = key channel (state row)
     const int chalf = warp >> 2;
-    const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
-    if (tid == 0) {
-      tc::mbar_arrive_expect_tx(&s_ld_bar[0], REC_TAIL);
-      tc::bulk_load(sb + ke_off(0), rec(0) + REC_KE, REC_TAIL, &s_ld_bar[0]);
-    }
     float Sv[32];
     {
       const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
@@ -999,127 +1127,94 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
         Sv[j] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[base + j])
                       : static_cast<const float*>(P.pool)[base + j];
     }
-    auto write_state_operand = [&]() {
+    auto write_state_operand = [&](uint32_t c) {   // S_c, fp16, MN-major
 #pragma unroll
       for (int p = 0; p < 4; ++p)
-        *reinterpret_cast<uint4*>(smem + CH_ST + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
+        *reinterpret_cast<uint4*>(smem + s_off(c) + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
             f16x8_pack(Sv + 8 * p);
     };
-    write_state_operand();
+    // Kb V of chunk c into its accumulator (thread 0; the same thread's P S follows)
+    auto issue_kbv = [&](uint32_t c) {
+      const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
+      const uint64_t dv = tc::desc_add(dV0, (c % V_SLOTS) * V_BYTES);
+#pragma unroll
+      for (int s = 0; s < C / 16; ++s)
+        tc::mma_ts(tmem + ds_col(c), ta + s * 8, tc::desc_add(dv, s * 2 * OP_LBO), id_s, s > 0);
+    };
+    write_state_operand(0);
     tc::fence_async_smem();
     tc::fence_before_sync();
     tc::named_sync(1, NT);
     tc::fence_after_sync();
-    auto wait_on = [&](uint64_t* bar, uint32_t parity) {
-      if (!tc::mbar_wait_bounded(bar, parity, kWaitLimit)) s_abort = 1;
-      tc::fence_after_sync();
-    };
-    // the state-independent part A1 V of chunk c, issued by thread 32 once the data warps
-    // have its operands in place
-    auto issue_a1v = [&](uint32_t c) {
-      if (!wait_flag(&s_next_ready, static_cast<int>(c) + 1)) return;
-      tc::fence_after_sync();
+    bool kbv_ahead = false;                     // thread 0: Kb V of the current chunk issued
+    bool stop = false;
+    for (uint32_t c = 0; c < nchunks && !stop; ++c) {
       const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
-      const uint64_t dv = tc::desc_add(dV0, (c % 3) * V_BYTES);
+      const uint64_t ds = tc::desc_add(dS0, (c % S_SLOTS) * S_BYTES);
+      bool bad = false;
+      if (tid == 0) {                           // Kb V + P[:, 0:64] S[0:64]
+        if (!kbv_ahead) {
+          bad = !wait_flag(&s_ready, static_cast<int>(c) + 1);
+          tc::fence_after_sync();
+          if (!bad) issue_kbv(c);
+        }
+        if (!bad) {
 #pragma unroll
-      for (int s = 0; s < C / 16; ++s)
-        tc::mma_ts(tmem + d1_col(c), ta + s * 8, tc::desc_add(dv, s * 2 * OP_LBO), id1, s > 0);
-      tc::mma_commit(&s_a1v_bar);
-    };
-    if (tid == 32) issue_a1v(0);
-
-    for (uint32_t c = 0; c < nchunks; ++c) {
-      const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
-      const uint32_t d1 = d1_col(c);
-      const bool more = c + 1 < nchunks;
-      wait_on(&s_ld_bar[c & 1], (c >> 1) & 1);
-      // -------------------------------------------------------------- [E; O] += A2 S
-      if (tid == 0) {                           // key channels 0-63, onto A1 V
-        wait_on(&s_a1v_bar, c & 1);
-#pragma unroll
-        for (int s = 0; s < D / 32; ++s)
-          tc::mma_ts(tmem + d1, ta + 32 + s * 8, tc::desc_add(dST, s * 2 * OP_LBO), id1, 1);
-        tc::mma_commit(&s_bar1);
-        if (more) {                             // chunk c - 1's KE in that buffer is consumed
-          tc::mbar_arrive_expect_tx(&s_ld_bar[(c + 1) & 1], REC_TAIL);
-          tc::bulk_load(sb + ke_off(c + 1), rec(c + 1) + REC_KE, REC_TAIL, &s_ld_bar[(c + 1) & 1]);
+          for (int s = 0; s < D / 32; ++s)
+            tc::mma_ts(tmem + ds_col(c), ta + 32 + s * 8, tc::desc_add(ds, s * 2 * OP_LBO), id_s, 1);
+          tc::mma_commit(&s_bar_s);
+          __threadfence_block();
+          atomicAdd(&s_issued, 1);
+        }
+        // the next chunk's Kb V, if its operands are in place (once the other half is queued)
+        kbv_ahead = !bad && c + 1 < nchunks &&
+                    *reinterpret_cast<volatile int*>(&s_ready) >= static_cast<int>(c) + 2 &&
+                    wait_flag(&s_issued, 2 * static_cast<int>(c) + 2);
+        if (kbv_ahead) {
+          tc::fence_after_sync();
+          issue_kbv(c + 1);
         }
       }
-      if (tid == 128) {                         // key channels 64-127
+      if (tid == 128) {                         // P[:, 64:128] S[64:128]
+        bad = !wait_flag(&s_ready, static_cast<int>(c) + 1);
+        tc::fence_after_sync();
+        if (!bad) {
 #pragma unroll
-        for (int s = D / 32; s < D / 16; ++s)
-          tc::mma_ts(tmem + T_D1B, ta + 32 + s * 8, tc::desc_add(dST, s * 2 * OP_LBO), id1, s > D / 32);
-        tc::mma_commit(&s_bar1);
+          for (int s = D / 32; s < D / 16; ++s)
+            tc::mma_ts(tmem + T_DS2, ta + 32 + s * 8, tc::desc_add(ds, s * 2 * OP_LBO), id_s, s > D / 32);
+          tc::mma_commit(&s_bar_s);
+          __threadfence_block();
+          atomicAdd(&s_issued, 1);
+        }
       }
-      wait_on(&s_bar1, c & 1);
-      // -------------------------------------------------------------- E, o rows
-      {
+      bad = bad || !wait_bar(&s_bar_s, c & 1);
+      bad = __any_sync(0xffffffffu, bad);       // tcgen05.ld is warp-collective
+      if (!bad) {
+        if (tid == 0) set_flag(&s_ps_done, static_cast<int>(c) + 1);
         uint32_t r0[16], r1[16], q0[16], q1[16];
-        tc::tmem_ld16(tmem + lane_addr + d1 + 32 * chalf, r0);
-        tc::tmem_ld16(tmem + lane_addr + d1 + 32 * chalf + 16, r1);
-        tc::tmem_ld16(tmem + lane_addr + T_D1B + 32 * chalf, q0);
-        tc::tmem_ld16(tmem + lane_addr + T_D1B + 32 * chalf + 16, q1);
+        tc::tmem_ld16(tmem + lane_addr + ds_col(c) + 32 * chalf, r0);
+        tc::tmem_ld16(tmem + lane_addr + ds_col(c) + 32 * chalf + 16, r1);
+        tc::tmem_ld16(tmem + lane_addr + T_DS2 + 32 * chalf, q0);
+        tc::tmem_ld16(tmem + lane_addr + T_DS2 + 32 * chalf + 16, q1);
         tc::tmem_wait_ld();
-        float x[32];
+        if (wait_flag(&s_ready, static_cast<int>(c) + 1)) {   // gamma(c) in place
+          const float gam = s_gam[(c % GAM_SLOTS) * D + row];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          x[e] = __uint_as_float(r0[e]) + __uint_as_float(q0[e]);
-          x[e + 16] = __uint_as_float(r1[e]) + __uint_as_float(q1[e]);
-        }
-        if (row < C) {
-#pragma unroll
-          for (int p = 0; p < 4; ++p)
-            *reinterpret_cast<uint4*>(smem + CH_ET + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
-                f16x8_pack(x + 8 * p);
-        } else {
-          wait_flag(&s_ost_free, static_cast<int>(c));   // chunk c - 1's o rows are stored
-          float* op = reinterpret_cast<float*>(smem + CH_OST) + (row - C) * OS + 32 * chalf;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(op + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+          for (int e = 0; e < 16; ++e) {
+            Sv[e] = gam * Sv[e] + (__uint_as_float(r0[e]) + __uint_as_float(q0[e]));
+            Sv[e + 16] = gam * Sv[e + 16] + (__uint_as_float(r1[e]) + __uint_as_float(q1[e]));
+          }
+          // S buffer (c + 1) % 3 held S_{c-2}, which the output MMA of chunk c - 2 reads
+          if (c + 1 < nchunks && (c < 2 || wait_flag(&s_o_done, static_cast<int>(c) - 1)))
+            write_state_operand(c + 1);
         }
       }
       tc::fence_async_smem();
       tc::fence_before_sync();
-      tc::named_sync(1, NT);
+      stop = tc::named_sync_or(1, NT, bad || aborted());
       tc::fence_after_sync();
-      if (tid == 0) set_flag(&s_e_done, static_cast<int>(c) + 1);
-      // -------------------------------------------------------------- dS = K_end^T E
-      if (tid == 0 || tid == 128) {             // tokens 0-31 / 32-63
-        const uint64_t dke = tc::desc_add(dKE0, (c & 1) * REC_TAIL);
-        const int s0 = tid == 0 ? 0 : C / 32;
-        const uint32_t d2 = tmem + (tid == 0 ? T_D2A : T_D2B);
-#pragma unroll
-        for (int s = 0; s < C / 32; ++s)
-          tc::mma_ss(d2, tc::desc_add(dke, (s0 + s) * 2 * KE_LBO), tc::desc_add(dET, (s0 + s) * 2 * OP_LBO),
-                     id2, s > 0);
-        tc::mma_commit(&s_bar2);
-      }
-      if (tid == 32 && more) issue_a1v(c + 1);
-      wait_on(&s_bar2, c & 1);
-      // -------------------------------------------------------------- S <- diag(gam) S + dS
-      {
-        uint32_t r0[16], r1[16], q0[16], q1[16];
-        tc::tmem_ld16(tmem + lane_addr + T_D2A + 32 * chalf, r0);
-        tc::tmem_ld16(tmem + lane_addr + T_D2A + 32 * chalf + 16, r1);
-        tc::tmem_ld16(tmem + lane_addr + T_D2B + 32 * chalf, q0);
-        tc::tmem_ld16(tmem + lane_addr + T_D2B + 32 * chalf + 16, q1);
-        tc::tmem_wait_ld();
-        const float gam = reinterpret_cast<const float*>(smem + ke_off(c) + (REC_GAM - REC_KE))[row];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          Sv[e] = gam * Sv[e] + (__uint_as_float(r0[e]) + __uint_as_float(q0[e]));
-          Sv[e + 16] = gam * Sv[e + 16] + (__uint_as_float(r1[e]) + __uint_as_float(q1[e]));
-        }
-        write_state_operand();
-      }
-      tc::fence_async_smem();
-      tc::fence_before_sync();
-      tc::named_sync(1, NT);
-      tc::fence_after_sync();
-      if (s_abort) break;
     }
-    if (!s_abort) {
+    if (!aborted()) {
       const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -1128,20 +1223,18 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
         else
           static_cast<float*>(P.pool)[base + j] = Sv[j];
       }
-    } else if (tid == 0) {
-      set_flag(&s_e_done, 1 << 30);             // release the data warps
     }
   }
 
+  __syncthreads();
   if (s_abort) {
-    // let whatever is still in flight finish (bounded) before shared and tensor memory go
-    for (uint32_t k = 0; k < 2; ++k) {
-      tc::mbar_wait_bounded(&s_bar1, k, kWaitLimit);
-      tc::mbar_wait_bounded(&s_bar2, k, kWaitLimit);
-      tc::mbar_wait_bounded(&s_a1v_bar, k, kWaitLimit);
-      tc::mbar_wait_bounded(&s_ld_bar[0], k, kWaitLimit);
-      tc::mbar_wait_bounded(&s_ld_bar[1], k, kWaitLimit);
-    }
+    // let whatever is still in flight finish (bounded) before shared and tensor memory go:
+    // every MMA of the three issuing threads (one commit each on the drain barrier) and the
+    // bulk copies (both phases of their barriers)
+    if (tid == 0 || tid == 128 || tid == 32 * W_ISSUE) tc::mma_commit(&s_drain);
+    tc::mbar_wait_bounded(&s_drain, 0, kWaitLimit);
+    for (uint32_t k = 0; k < 2; ++k)
+      for (uint32_t i = 0; i < OA_SLOTS; ++i) tc::mbar_wait_bounded(&s_oa_bar[i], k, kWaitLimit);
     if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
   }
   tc::fence_before_sync();

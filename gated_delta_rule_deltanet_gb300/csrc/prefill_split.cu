@@ -38,6 +38,11 @@
 // Operand precisions are those of the single-kernel path in prefill_tc.cu (fp16 operands,
 // fp32 accumulation and fp32 state); the state passes through fp16 only as the B operand of
 // P S, so a state-independent term never carries the state's rounding forward.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "prefill_plan.cuh"
 #include "tc_utils.cuh"
@@ -85,14 +90,14 @@ constexpr uint32_t SOL_BYTES = 2 * C * SP * 4 + 32 * XP * 4;
 template <bool PERCH>
 struct FrontMap;
 
-// Scalar decay: the raw k and q rows are copied straight into the A-GEMM operand
-// [K; Q] (padded leading offset, so column reads of it are conflict-free); the key
-// rows double as the B operand.
+// Scalar decay: four TMA copies put the raw k and q rows straight into the A-GEMM
+// operand [K; Q], K-major in the 128-byte swizzled layout: two halves of 64 channels,
+// each 128 rows (k rows 0-63, q rows 64-127) of 128 bytes; the key rows double as the
+// B operand.
 template <>
 struct FrontMap<false> {
-  static constexpr uint32_t AK_LBO = 144, AK_SBO = (D / 8) * AK_LBO;
-  static constexpr uint32_t AK = 0;
-  static constexpr uint32_t SMALL = AK + 16 * AK_SBO;
+  static constexpr uint32_t AK = 0, AK_HALF = 128 * 128;
+  static constexpr uint32_t SMALL = AK + 2 * AK_HALF;
   static constexpr uint32_t R2 = SMALL + SMALL_BYTES;   // solve, then K_end and K~
   static constexpr uint32_t LMAT = R2 + SOL_BYTES;      // [*; A_qk] 128 x 64 fp16, then Kb
   static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;  // TB 64 x 64 fp16, MN-major
@@ -140,7 +145,8 @@ constexpr uint32_t CH_GAM = CH_OST + C * OS * 4;         // gamma of four chunks
 constexpr uint32_t GAM_SLOTS = 4;
 constexpr uint32_t CH_BYTES = CH_GAM + GAM_SLOTS * D * 4;
 static_assert(CH_BYTES + 64 <= 227 * 1024, "chain shared memory budget");
-static_assert(FrontMap<true>::BYTES + 64 <= 227 * 1024, "front shared memory budget");
+static_assert(FrontMap<true>::BYTES + 1024 + 64 <= 227 * 1024, "front shared memory budget");
+static_assert(2 * (FrontMap<false>::BYTES + 1024 + 1024) <= 228 * 1024, "two scalar front CTAs per SM");
 static_assert(CH_V % 128 == 0 && CH_ST % 128 == 0 && OA_BYTES % 128 == 0, "operand alignment");
 static_assert(CH_OA + (OA_SLOTS + 1) * OA_BYTES <= CH_BYTES, "rows 64-127 of the last OA stay in bounds");
 // chain TMEM columns: [Kb | P] of two chunks (fp16 pairs); the state MMA's result as two
@@ -157,7 +163,8 @@ __device__ __forceinline__ uint4 f16x8_pack(const float* x) {
 
 }  // namespace tcs
 
-// cp.async copies of one chunk's k, q, beta and log-decay (rows past n zero-filled)
+// cp.async copies of one chunk's beta and log-decay, and for per-channel decay its k and
+// q rows (rows past n zero-filled); for scalar decay k and q come by TMA
 template <bool PERCH>
 __device__ __forceinline__ void front_issue_loads(const Problem& P, unsigned char* smem,
                                                   int64_t t0, int n, int kh, int h, int tid) {
@@ -165,21 +172,17 @@ __device__ __forceinline__ void front_issue_loads(const Problem& P, unsigned cha
   using M = FrontMap<PERCH>;
   const int HV = P.HV;
   const uint32_t sb = tc::smem_u32(smem);
-  for (int u = tid; u < C * (D / 8); u += NT) {
-    const int i = u / (D / 8), q8 = u % (D / 8);
-    const bool live = i < n;
-    const int64_t t = live ? t0 + i : t0;
-    const uint32_t nb = live ? 16u : 0u;
-    uint32_t dk, dq;
-    if constexpr (PERCH) {
-      dk = M::S_K + (i * M::KS + q8 * 8) * 2;
-      dq = M::S_Q + (i * M::KS + q8 * 8) * 2;
-    } else {
-      dk = M::AK + tc::cm_offset(i, q8 * 8, M::AK_LBO, M::AK_SBO);
-      dq = M::AK + tc::cm_offset(C + i, q8 * 8, M::AK_LBO, M::AK_SBO);
+  if constexpr (PERCH) {
+    for (int u = tid; u < C * (D / 8); u += NT) {
+      const int i = u / (D / 8), q8 = u % (D / 8);
+      const bool live = i < n;
+      const int64_t t = live ? t0 + i : t0;
+      const uint32_t nb = live ? 16u : 0u;
+      tc::cp_async16(sb + M::S_K + (i * M::KS + q8 * 8) * 2,
+                     static_cast<const uint16_t*>(P.k) + t * P.k_stride + static_cast<int64_t>(kh) * D + q8 * 8, nb);
+      tc::cp_async16(sb + M::S_Q + (i * M::KS + q8 * 8) * 2,
+                     static_cast<const uint16_t*>(P.q) + t * P.q_stride + static_cast<int64_t>(kh) * D + q8 * 8, nb);
     }
-    tc::cp_async16(sb + dk, static_cast<const uint16_t*>(P.k) + t * P.k_stride + static_cast<int64_t>(kh) * D + q8 * 8, nb);
-    tc::cp_async16(sb + dq, static_cast<const uint16_t*>(P.q) + t * P.q_stride + static_cast<int64_t>(kh) * D + q8 * 8, nb);
   }
   if constexpr (PERCH) {
     for (int u = tid; u < C * (D / 4); u += NT) {
@@ -203,12 +206,16 @@ __device__ __forceinline__ void front_issue_loads(const Problem& P, unsigned cha
 // state, written to the chunk's record.
 template <bool PERCH>
 __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
-    tc_front_kernel(Problem P, PlanView plan, unsigned char* records) {
+    tc_front_kernel(Problem P, PlanView plan, unsigned char* records,
+                    const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk) {
   using namespace tcs;
   using M = FrontMap<PERCH>;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the swizzled operand needs a 1024-byte aligned base; the launch adds 1 KB of slack
+  unsigned char* const smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t s_bar;                    // MMAs issued by thread 0
   __shared__ uint64_t s_bar2;                   // MMAs issued by thread 32
+  __shared__ uint64_t s_ld;                     // TMA copies of k and q (scalar decay)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_range;
@@ -252,9 +259,20 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   if (tid == 0) {
     tc::mbar_init(&s_bar, 1);
     tc::mbar_init(&s_bar2, 1);
+    tc::mbar_init(&s_ld, 1);
     tc::fence_mbar_init();
     s_abort = 0;
     s_range = 0;
+    if constexpr (!PERCH) {                     // k and q: both 64-channel halves, 64 rows each
+      const uint32_t sb = tc::smem_u32(smem + M::AK);
+      const int32_t row0 = static_cast<int32_t>(t0);
+      tc::mbar_arrive_expect_tx(&s_ld, 2 * M::AK_HALF);
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        tc::tma_load_3d(sb + a * M::AK_HALF, &tmk, 64 * a, kh, row0, &s_ld);
+        tc::tma_load_3d(sb + a * M::AK_HALF + C * 128, &tmq, 64 * a, kh, row0, &s_ld);
+      }
+    }
   }
   const int row = 32 * (warp & 3) + lane;       // TMEM lane = M row
   const int chalf = warp >> 2;
@@ -278,17 +296,26 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     if (!ok) s_abort = 1;
     tc::fence_after_sync();
   };
-  // raw bf16 element (token m, channel c) of k or q
-  auto k_raw = [&](int m, int c) -> float {
-    if constexpr (PERCH) return tc::bf16_at(smem, M::S_K, m * M::KS + c);
-    else return tc::bf16_at(smem, M::AK + tc::cm_offset(m, c, M::AK_LBO, M::AK_SBO), 0);
-  };
-  auto kq_piece = [&](bool is_q, int i, int c) -> const unsigned char* {   // 8 channels
+  // 8 raw bf16 channels [c, c + 8) of token i of k or q
+  auto kq_piece = [&](bool is_q, int i, int c) -> const unsigned char* {
     if constexpr (PERCH) return smem + (is_q ? M::S_Q : M::S_K) + (i * M::KS + c) * 2;
-    else return smem + M::AK + tc::cm_offset(is_q ? C + i : i, c, M::AK_LBO, M::AK_SBO);
+    else return smem + M::AK + (c >> 6) * M::AK_HALF + tc::sw128_offset(is_q ? C + i : i, (c & 63) >> 3);
   };
 
   tc::cp_async_wait_all();
+  if constexpr (!PERCH) {
+    if (!tc::mbar_wait_bounded(&s_ld, 0, kWaitLimit)) s_abort = 1;
+    // rows past the chunk's end hold the next sequence's tokens (or the TMA's zero fill):
+    // clear them, as the cp.async path does, so nothing of another sequence enters
+    if (n < C) {
+      uint4* ak = reinterpret_cast<uint4*>(smem + M::AK);
+      for (int u = tid; u < (C - n) * 32; u += NT) {      // 2 halves x (k, q) x 8 chunks
+        const int r = n + (u >> 5), part = u & 31;
+        const int a = part >> 4, qk = (part >> 3) & 1, c8 = part & 7;
+        ak[(a * M::AK_HALF + (qk * C + r) * 128) / 16 + c8] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+  }
   __syncthreads();
 
   // ------------------------------------------------------------------ prep
@@ -474,13 +501,11 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
         for (int s = 0; s < D / 16; ++s)        // lo x hi (low half from TMEM)
           tc::mma_ts(d, tmem + F_ALO + s * 8, tc::desc_add(dbk, s * 256), id, 1);
       }
-    } else {
-      const uint64_t dak = tc::smem_desc(tc::smem_u32(smem + M::AK), M::AK_LBO, M::AK_SBO);
-      const int s0 = second ? D / 32 : 0;
+    } else {                                    // [K; Q] K^T on the raw rows, one channel half each
+      const uint64_t dak = tc::smem_desc_sw128(tc::smem_u32(smem + M::AK) + (second ? M::AK_HALF : 0u), 1024);
 #pragma unroll
-      for (int s = s0; s < s0 + D / 32; ++s)    // [K; Q] K^T on the raw rows, half of K each
-        tc::mma_ss(d, tc::desc_add(dak, s * 2 * M::AK_LBO), tc::desc_add(dak, s * 2 * M::AK_LBO),
-                   id, s > s0);
+      for (int s = 0; s < D / 32; ++s)
+        tc::mma_ss(d, tc::desc_add(dak, s * 32), tc::desc_add(dak, s * 32), id, s > 0);
     }
     tc::mma_commit(second ? &s_bar2 : &s_bar);
   }
@@ -1248,15 +1273,50 @@ size_t split_workspace_bytes(const Problem& P) {
   return off + static_cast<size_t>(plan_max_chunks(P)) * static_cast<size_t>(P.HV) * tcs::REC_BYTES;
 }
 
+// cuTensorMapEncodeTiled from the driver (the runtime is linked statically, libcuda is not)
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [T, HK, 128] bf16 rows with a row stride of `stride` elements: boxes of 64 channels x
+// 1 head x 64 tokens, 128-byte swizzle, zero fill past the last token
+static bool encode_rows_map(CUtensorMap* m, const void* base, const Problem& P, int64_t stride) {
+  auto enc = tensor_map_encoder();
+  if (!enc || P.T <= 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(tcs::D), static_cast<cuuint64_t>(P.HK),
+                              static_cast<cuuint64_t>(P.T)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(tcs::D) * 2, static_cast<cuuint64_t>(stride) * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(tcs::C)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool PERCH>
 static cudaError_t launch_front_t(const Problem& P, const PlanView& plan, unsigned char* recs,
                                   cudaStream_t st) {
   auto k = tc_front_kernel<PERCH>;
-  constexpr uint32_t bytes = tcs::FrontMap<PERCH>::BYTES;
+  constexpr uint32_t bytes = tcs::FrontMap<PERCH>::BYTES + 1024;
+  alignas(64) CUtensorMap tmq, tmk;
+  memset(&tmq, 0, sizeof(tmq));
+  memset(&tmk, 0, sizeof(tmk));
+  if (!PERCH && !(encode_rows_map(&tmq, P.q, P, P.q_stride) && encode_rows_map(&tmk, P.k, P, P.k_stride)))
+    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  k<<<dim3(static_cast<unsigned>(plan_max_chunks(P)), P.HV), tcs::NT, bytes, st>>>(P, plan, recs);
+  k<<<dim3(static_cast<unsigned>(plan_max_chunks(P)), P.HV), tcs::NT, bytes, st>>>(P, plan, recs, tmq, tmk);
   return cudaGetLastError();
 }
 

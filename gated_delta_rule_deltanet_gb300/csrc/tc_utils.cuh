@@ -48,6 +48,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;                             // base offset 0, absolute-LBO off, layout 0 (no swizzle)
 }
 
+// Descriptor of a K-major operand in the 128-byte swizzled layout that a TMA copy with
+// 128-byte swizzle writes: rows of 128 bytes, the eight 16-byte chunks of row r stored at
+// chunk ^ (r % 8), 8-row atoms `sbo` bytes apart; the region must be 1024-byte aligned.
+// A K step of 16 elements within the 128-byte row advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t sbo) {
+  return smem_desc(saddr, 16, sbo) | (static_cast<uint64_t>(2) << 61);
+}
+
+// Byte offset of the 16-byte chunk holding elements [8 c8, 8 c8 + 8) of row r in that layout
+// (rows of 128 bytes from a 1024-byte aligned base).
+__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c8) {
+  return r * 128 + ((c8 ^ (r & 7)) << 4);
+}
+
 // The same descriptor with its start address advanced by `bytes` (a multiple of 16 that
 // keeps the address inside shared memory, so the 14-bit field cannot carry).
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
@@ -249,6 +263,17 @@ __device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint3
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           sdst),
       "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Tiled 3-D TMA load of one box of `map` at element coordinates (x, y, z) into shared
+// memory; completion is counted in bytes on `bar`.  x * element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_3d(uint32_t sdst, const void* map, int32_t x, int32_t y,
+                                            int32_t z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(sdst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 

@@ -1097,14 +1097,21 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
       tc::fence_before_sync();
       tc::named_sync(3, NTO);
       if (dq == 0) set_flag(&s_o_free, static_cast<int>(c) + 1);
+      // thread dq stores columns 4 (dq % 16) .. + 3 of rows dq / 16 + 4 k: one pointer step
+      // per row group, the partial-chunk test hoisted out of the full chunks
       const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
       const int n = chunk_n(c);
-#pragma unroll 4
-      for (int k = 0; k < (C * BV / 4) / NTO; ++k) {
-        const int idx = dq + k * NTO, i = idx / (BV / 4), q4 = idx % (BV / 4);
-        if (i < n)
-          *reinterpret_cast<float4*>(P.o + ((t0 + i) * HV + h) * D + vt * BV + q4 * 4) =
-              *reinterpret_cast<const float4*>(smem + CH_OST + (i * OS + q4 * 4) * 4);
+      const int i0 = dq >> 4, q4 = dq & 15;
+      float* gp = P.o + ((t0 + i0) * HV + h) * D + vt * BV + q4 * 4;
+      const float* sp = reinterpret_cast<const float*>(smem + CH_OST) + i0 * OS + q4 * 4;
+      const int64_t gstep = static_cast<int64_t>(NTO / 16) * HV * D;
+      if (n == C) {
+#pragma unroll
+        for (int k = 0; k < C / (NTO / 16); ++k)
+          *reinterpret_cast<float4*>(gp + k * gstep) = *reinterpret_cast<const float4*>(sp + k * (NTO / 16) * OS);
+      } else {
+        for (int k = 0; i0 + k * (NTO / 16) < n; ++k)
+          *reinterpret_cast<float4*>(gp + k * gstep) = *reinterpret_cast<const float4*>(sp + k * (NTO / 16) * OS);
       }
       tc::named_sync(3, NTO);                   // staging reads done before it is refilled
     }

@@ -65,6 +65,11 @@ def _load(mutant: int = 0):
                   P, P, P, P, P, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
                   P, P, P, ctypes.c_int]
     f.restype = ctypes.c_int
+    f = lib.kda_oracle_gdp_run
+    f.argtypes = [ctypes.c_int, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, P, P, P, P, P, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+                  P, P, ctypes.c_int]
+    f.restype = ctypes.c_int
     _LIB_CACHE[mutant] = lib
     return lib
 
@@ -113,6 +118,43 @@ def run_arrays(*, offsets, slot_idx, q, k, v, beta, g, per_channel: bool, pool, 
     return o, pool
 
 
+def run_gdp_arrays(*, offsets, slot_idx, q, k, v, beta, g, per_channel: bool, pool,
+                   scale: float = 0.0, l2norm: bool = True, nthreads: Optional[int] = None,
+                   mutant: int = 0):
+    """Gated DeltaProduct ("Linear attention visualized", Gated Delta Product section): the C
+    recurrence with n_h substeps per token.
+
+    q: [T, HK, dk] (one query per token); k: [T, n_h, HK, dk]; v: [T, n_h, HV, dv];
+    beta: [T, n_h, HV]; g: [T, HV] or [T, HV, dk] (one decay per token, applied before the
+    first substep); pool: [num_slots, HV, dk, dv].  Returns (o fp64 [T, HV, dv], pool fp64).
+    """
+    offsets = np.ascontiguousarray(offsets, dtype=np.int64)
+    slot_idx = np.ascontiguousarray(slot_idx, dtype=np.int64)
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    k = np.ascontiguousarray(k, dtype=np.float32)
+    v = np.ascontiguousarray(v, dtype=np.float32)
+    beta = np.ascontiguousarray(beta, dtype=np.float32)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    pool = np.array(pool, dtype=np.float64, copy=True, order="C")
+    T, HK, dk = q.shape
+    n_h = k.shape[1]
+    HV, dv = v.shape[2], v.shape[3]
+    if k.shape != (T, n_h, HK, dk) or v.shape[:2] != (T, n_h) or beta.shape != (T, n_h, HV):
+        raise ValueError("substep axes of k, v, beta disagree")
+    num_seqs = offsets.shape[0] - 1
+    o = np.zeros((T, HV, dv), dtype=np.float64)
+    if scale is None or scale <= 0:
+        scale = 1.0 / np.sqrt(dk)
+    lib = _load(mutant)
+    rc = lib.kda_oracle_gdp_run(num_seqs, _ptr(offsets), _ptr(slot_idx), HK, HV, dk, dv, n_h,
+                                _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                                int(bool(per_channel)), float(scale), int(bool(l2norm)),
+                                _ptr(pool), _ptr(o), int(nthreads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments")
+    return o, pool
+
+
 def _widen(arr, dtype):
     # exact fp32 view of stored inputs; kept local so the oracle does not
     # depend on anything but numpy for its arithmetic
@@ -131,6 +173,16 @@ def run(problem, *, pair_mask=None, nthreads: Optional[int] = None, mutant: int 
                       pool=_widen(p.pool, p.state_dtype), scale=p.scale, l2norm=l2norm,
                       delta_rule=delta_rule, pair_mask=pair_mask, nthreads=nthreads,
                       mutant=mutant)
+
+
+def run_gdp(problem, *, nthreads: Optional[int] = None, mutant: int = 0):
+    """The Gated DeltaProduct oracle on a `workloads.Problem` with n_h substeps."""
+    p = problem
+    return run_gdp_arrays(offsets=p.offsets, slot_idx=p.slot_idx, q=_widen(p.q, p.qkv_dtype),
+                          k=_widen(p.k, p.qkv_dtype), v=_widen(p.v, p.qkv_dtype), beta=p.beta,
+                          g=p.g, per_channel=(p.decay_kind == "per_channel"),
+                          pool=_widen(p.pool, p.state_dtype), scale=p.scale, nthreads=nthreads,
+                          mutant=mutant)
 
 
 def round_to_bf16(x: np.ndarray) -> np.ndarray:

@@ -17,6 +17,12 @@ sec. 4 for the KDA gate and sec. 5/6 for the decode/chunk schedules; the Modular
   kda_decode      256 sequences x 64 single-token steps, 32 heads, d=128, bf16, per-channel decay,
                   fp32 pool ~N(0, 0.02), one slot per sequence
 
+and one for the Gated DeltaProduct extension ("Linear attention visualized", Gated Delta
+Product section: n_h keys, values and gates per token, one query and one decay):
+
+  gdp_prefill     the gdn_prefill shape (4 x 4096 tokens, 16 heads, d=128, bf16, scalar decay,
+                  fp32 zero state, chunk 64) with n_h = 2 substeps per token; seed 1006
+
 Recipe (fixed draw order so every consumer sees identical values):
   generator   numpy PCG64, seed = 1000 + workload number (1..5)
   order       lengths, q, k, v, beta logits, decay noise, state, slot permutation
@@ -109,6 +115,8 @@ class Problem:
     pool: np.ndarray             # [num_slots, HV, d_k, d_v]
     slot_idx: np.ndarray         # uint32 [num_seqs]
     scale: float = 0.0           # <= 0 means 1/sqrt(d_k)
+    n_h: int = 1                 # substeps per token (Gated DeltaProduct): k [T, n_h, HK, d_k],
+                                 # v [T, n_h, HV, d_v], beta [T, n_h, HV]; q and g stay per token
 
     @property
     def total_tokens(self) -> int:
@@ -194,6 +202,36 @@ def make_problem(name: str, *, num_seqs: int, lengths, num_k_heads: int, num_v_h
                    state_dtype, decay_kind, chunk, q, k, v, beta, g, pool, slot_idx)
 
 
+def make_gdp_problem(name: str, *, num_seqs: int, lengths, n_h: int, num_k_heads: int,
+                     num_v_heads: int, d: int, qkv_dtype: str, state_dtype: str,
+                     decay_kind: str, chunk: int, zero_state: bool,
+                     num_slots: Optional[int] = None, seed: int = 0) -> Problem:
+    """Seeded Gated DeltaProduct prefill problem: the distributions of the other workloads,
+    drawn in the order lengths, q, k, v, beta logits, decay noise, state, slots, with the
+    substep axis right after the token axis of k, v and beta."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lengths = np.asarray(lengths, dtype=np.int64)
+    assert lengths.shape == (num_seqs,) and n_h >= 1
+    offsets = np.zeros(num_seqs + 1, dtype=np.uint32)
+    offsets[1:] = np.cumsum(lengths)
+    T, HK, HV = int(offsets[-1]), num_k_heads, num_v_heads
+    q = _unit_rows(rng.standard_normal((T, HK, d), dtype=np.float32))
+    k = _unit_rows(rng.standard_normal((T, n_h, HK, d), dtype=np.float32))
+    v = rng.standard_normal((T, n_h, HV, d), dtype=np.float32)
+    beta = _sigmoid(rng.standard_normal((T, n_h, HV), dtype=np.float32))
+    if decay_kind == SCALAR:
+        g = _neg_softplus(rng.standard_normal((T, HV), dtype=np.float32))
+    else:
+        g = (-np.exp(rng.normal(-2.0, 0.5, size=(T, HV, d)))).astype(np.float32)
+    if num_slots is None:
+        num_slots = num_seqs
+    pool = _draw_state(rng, (num_slots, HV, d, d), state_dtype, zero_state)
+    slot_idx = rng.permutation(num_slots)[:num_seqs].astype(np.uint32)
+    return Problem(name, num_seqs, offsets, HK, HV, d, d, qkv_dtype, state_dtype, decay_kind,
+                   chunk, _store(q, qkv_dtype), _store(k, qkv_dtype), _store(v, qkv_dtype),
+                   beta, g, pool, slot_idx, n_h=n_h)
+
+
 def ragged_lengths(rng, n: int, lo: int, hi: int) -> np.ndarray:
     """Log-uniform integer lengths in [lo, hi]."""
     u = rng.uniform(math.log(lo), math.log(hi), size=n)
@@ -225,6 +263,10 @@ def workload(name: str):
                             d=128, qkv_dtype=BF16, state_dtype=BF16, decay_kind=PER_CHANNEL,
                             chunk=64, zero_state=False, num_slots=64, seed=1004 + (1 << 20),
                             shuffle_slots=True)
+    if name == "gdp_prefill":
+        return make_gdp_problem(name, num_seqs=4, lengths=[4096] * 4, n_h=2, num_k_heads=16,
+                                num_v_heads=16, d=128, qkv_dtype=BF16, state_dtype=F32,
+                                decay_kind=SCALAR, chunk=64, zero_state=True, seed=1006)
     if name == "kda_decode":
         return make_decode_problem(name, num_seqs=256, steps=64, num_k_heads=32, num_v_heads=32,
                                    d=128, qkv_dtype=BF16, state_dtype=F32,

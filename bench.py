@@ -355,6 +355,37 @@ def time_decode(dp, dev, steps, warmup):
     return start.elapsed_time(end) / steps
 
 
+def time_gdp_prefill(p, dev, steps, warmup):
+    """Gated DeltaProduct prefill (virtual-sequence expansion, prefill, gather), resident inputs."""
+    import torch
+    import gated_delta_rule_deltanet_gb300 as kda
+    from workloads import torch_io
+    t = torch_io.prefill_inputs(p, dev)
+    out = torch.empty((p.total_tokens, p.num_v_heads, p.d_v), dtype=torch.float32, device=dev)
+    ws = None
+
+    def step():
+        nonlocal ws
+        kda.gdp_prefill(t["q"], t["k"], t["v"], t["beta"], t["log_decay"], t["input_row_offsets"],
+                        t["slot_idx"], t["state_pool"], chunk=p.chunk, scale=p.scale, out=out,
+                        workspace=ws)
+
+    p_ws = kda.kda._gdp_params(t["q"], t["k"], t["v"], t["beta"], t["log_decay"], p.num_seqs,
+                               t["slot_idx"], t["state_pool"], p.chunk, p.scale, True, False,
+                               False, False)[2]
+    ws = torch.empty(max(p_ws, 1), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
 VERIFY_WINDOW = 4
 
 
@@ -505,6 +536,15 @@ def ours_arm(args, rank, world, local):
                                            "achieved_gbs": wbytes / (wms / 1e3) / 1e9,
                                            "frac_hbm": wbytes / (wms / 1e3) / 1e9
                                            / peaks["hbm_gbs"]}})
+
+    if not args.no_decode:
+        gp = workloads.workload("gdp_prefill")
+        gms = time_gdp_prefill(gp, dev, 30, 3)
+        gval, _ = aggregate(float(gp.total_tokens), gms / 1e3, world, dev)
+        also.append({"workload": "gdp_prefill (Gated DeltaProduct, 4 x 4096 tokens x 2 substeps, "
+                                 "16 heads, d=128, bf16, scalar decay)",
+                     "metric": "prefill tokens/s", "value": gval, "unit": "tokens/s",
+                     "ms_per_step": gms, "virtual_tokens_per_s": gval * gp.n_h})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

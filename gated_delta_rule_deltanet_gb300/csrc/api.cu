@@ -27,6 +27,12 @@ cudaError_t launch_verify(const Problem& P, int window, float* ring, bool qbf16,
                           bool perch, cudaStream_t stream);
 cudaError_t launch_fold(const Problem& P, int window, const float* ring, const uint32_t* accepted,
                         bool sbf16, bool perch, cudaStream_t stream);
+cudaError_t launch_gdp_expand(const void* q, int64_t q_stride, bool qbf16, const float* g,
+                              const uint32_t* offsets, int64_t T, int n_h, int64_t qrow,
+                              int64_t grow, int num_seqs, void* qv, float* gv, uint32_t* offv,
+                              cudaStream_t st);
+cudaError_t launch_gdp_gather(const float* ov, int64_t T, int n_h, int64_t orow, float* o,
+                              cudaStream_t st);
 }  // namespace kda
 
 using kda::Problem;
@@ -133,6 +139,100 @@ size_t prefill_workspace_bytes(const kda_params_t* p, const Problem& P) {
   return compact_tc(p) ? kda::tc_workspace_bytes(P) : kda::split_workspace_bytes(P);
 }
 
+// The prefill path chosen for p, on a fully filled-in Problem.
+kda_status_t prefill_dispatch(const kda_params_t* p, const Problem& P, void* workspace, cudaStream_t stream) {
+  const bool qbf16 = p->qkv_dtype == KDA_DTYPE_BF16;
+  const bool sbf16 = p->state_dtype == KDA_DTYPE_BF16;
+  const bool perch = p->decay_kind == KDA_DECAY_PER_CHANNEL;
+  const kda::Stages st = current_stages();
+  if (use_tc(p, P)) {
+    if (compact_tc(p)) return to_status(kda::launch_prefill_tc(P, workspace, perch, sbf16, stream, st));
+    return to_status(kda::launch_prefill_split(P, workspace, perch, sbf16, stream, st));
+  }
+  return to_status(kda::launch_prefill_simt(P, workspace, qbf16, perch, sbf16, stream, st));
+}
+
+// Gated DeltaProduct: the parameters of the virtual sequence (n_h positions per token, dense
+// virtual queries; k and v keep the caller's stride between substep rows).  For the decode
+// form (one token per sequence) total_tokens is num_seqs and a chunk of 0 means 64.
+constexpr int32_t kMaxSubsteps = 64;
+kda_status_t gdp_virtual_params(const kda_params_t* p, int32_t n_h, bool decode, kda_params_t* pv) {
+  if (!p || n_h < 1 || n_h > kMaxSubsteps) return KDA_ERR_INVALID_ARG;
+  *pv = *p;
+  const int64_t T = decode ? static_cast<int64_t>(p->num_seqs) : p->total_tokens;
+  if (T < 0) return KDA_ERR_INVALID_ARG;
+  if (T * n_h > 0x7fffffffLL) return KDA_ERR_UNSUPPORTED;
+  pv->total_tokens = T * n_h;
+  pv->q_row_stride = 0;
+  if (decode && pv->chunk == 0) pv->chunk = 64;
+  return KDA_OK;
+}
+
+// Workspace of the GDP forms: [virtual offsets | virtual q | virtual log-decay | virtual o |
+// the prefill's own workspace], 256-byte aligned pieces.
+struct GdpLayout {
+  size_t offv, qv, gv, ov, inner, total;
+};
+GdpLayout gdp_layout(const kda_params_t* pv, const Problem& Pv) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t Tv = static_cast<size_t>(Pv.T);
+  const size_t es = elem_size(pv->qkv_dtype);
+  const size_t gw = pv->decay_kind == KDA_DECAY_PER_CHANNEL ? static_cast<size_t>(Pv.D) : 1;
+  GdpLayout L;
+  L.offv = 0;
+  L.qv = up(L.offv + (static_cast<size_t>(Pv.num_seqs) + 1) * 4);
+  L.gv = up(L.qv + Tv * Pv.HK * Pv.D * es);
+  L.ov = up(L.gv + Tv * Pv.HV * gw * 4);
+  L.inner = up(L.ov + Tv * Pv.HV * Pv.D * 4);
+  L.total = L.inner + prefill_workspace_bytes(pv, Pv);
+  return L;
+}
+
+kda_status_t gdp_run(const kda_params_t* p, int32_t n_h, bool decode, const void* q, const void* k,
+                     const void* v, const float* beta, const float* log_decay,
+                     const uint32_t* input_row_offsets, const uint32_t* slot_idx, void* state_pool,
+                     float* o, void* workspace, size_t workspace_bytes, void* stream) {
+  kda_params_t pv;
+  kda_status_t s = gdp_virtual_params(p, n_h, decode, &pv);
+  if (s != KDA_OK) return s;
+  Problem P{};
+  s = check_prefill(&pv, &P);
+  if (s != KDA_OK) return s;
+  if (p->num_seqs == 0) return KDA_OK;
+  if ((!decode && !input_row_offsets) || !slot_idx || !state_pool) return KDA_ERR_INVALID_ARG;
+  if (P.T > 0 && (!q || !k || !v || !beta || !log_decay || !o)) return KDA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(state_pool, 16) || !aligned(beta, 4) || !aligned(log_decay, 4) ||
+      !aligned(input_row_offsets, 4) || !aligned(slot_idx, 4))
+    return KDA_ERR_INVALID_ARG;
+  // the caller's query rows (one per token) keep its stride
+  const int64_t dq = static_cast<int64_t>(p->num_k_heads) * p->d_k;
+  const int64_t q_stride = p->q_row_stride ? p->q_row_stride : dq;
+  if (q_stride < dq || (q_stride * static_cast<int64_t>(elem_size(p->qkv_dtype))) % 16) return KDA_ERR_INVALID_ARG;
+  const GdpLayout L = gdp_layout(&pv, P);
+  if (!workspace || workspace_bytes < L.total || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  uint32_t* offv = reinterpret_cast<uint32_t*>(ws + L.offv);
+  void* qv = ws + L.qv;
+  float* gv = reinterpret_cast<float*>(ws + L.gv);
+  float* ov = reinterpret_cast<float*>(ws + L.ov);
+  const int64_t T = P.T / n_h;
+  const int64_t grow = static_cast<int64_t>(P.HV) * (p->decay_kind == KDA_DECAY_PER_CHANNEL ? P.D : 1);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (to_status(kda::launch_gdp_expand(q, q_stride, p->qkv_dtype == KDA_DTYPE_BF16, log_decay,
+                                       decode ? nullptr : input_row_offsets, T, n_h, dq, grow,
+                                       p->num_seqs, qv, gv, offv, st)) != KDA_OK)
+    return KDA_ERR_CUDA;
+  P.q = qv; P.k = k; P.v = v; P.beta = beta; P.g = gv;
+  P.offsets = offv; P.slot_idx = slot_idx;
+  P.pool = state_pool; P.o = ov;
+  P.err = device_error_word();
+  if (!P.err) return KDA_ERR_CUDA;
+  s = prefill_dispatch(&pv, P, ws + L.inner, st);
+  if (s != KDA_OK) return s;
+  return to_status(kda::launch_gdp_gather(ov, T, n_h, static_cast<int64_t>(P.HV) * P.D, o, st));
+}
+
 }  // namespace
 
 extern "C" {
@@ -188,19 +288,36 @@ kda_status_t kda_prefill_fwd(const kda_params_t* p, const void* q, const void* k
   P.pool = state_pool; P.o = o;
   P.err = device_error_word();
   if (!P.err) return KDA_ERR_CUDA;
-  const bool qbf16 = p->qkv_dtype == KDA_DTYPE_BF16;
-  const bool sbf16 = p->state_dtype == KDA_DTYPE_BF16;
-  const bool perch = p->decay_kind == KDA_DECAY_PER_CHANNEL;
-  const kda::Stages st = current_stages();
-  if (use_tc(p, P)) {
-    if (compact_tc(p))
-      return to_status(kda::launch_prefill_tc(P, workspace, perch, sbf16,
-                                              static_cast<cudaStream_t>(stream), st));
-    return to_status(kda::launch_prefill_split(P, workspace, perch, sbf16,
-                                               static_cast<cudaStream_t>(stream), st));
-  }
-  return to_status(kda::launch_prefill_simt(P, workspace, qbf16, perch, sbf16,
-                                            static_cast<cudaStream_t>(stream), st));
+  return prefill_dispatch(p, P, workspace, static_cast<cudaStream_t>(stream));
+}
+
+kda_status_t kda_gdp_workspace_size(const kda_params_t* p, int32_t n_h, int32_t decode, size_t* bytes) {
+  if (!bytes) return KDA_ERR_INVALID_ARG;
+  kda_params_t pv;
+  kda_status_t s = gdp_virtual_params(p, n_h, decode != 0, &pv);
+  if (s != KDA_OK) return s;
+  Problem P{};
+  s = check_prefill(&pv, &P);
+  if (s != KDA_OK) return s;
+  *bytes = gdp_layout(&pv, P).total;
+  return KDA_OK;
+}
+
+kda_status_t kda_gdp_prefill_fwd(const kda_params_t* p, int32_t n_h, const void* q, const void* k,
+                                 const void* v, const float* beta, const float* log_decay,
+                                 const uint32_t* input_row_offsets, const uint32_t* slot_idx,
+                                 void* state_pool, float* o, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  return gdp_run(p, n_h, false, q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool,
+                 o, workspace, workspace_bytes, stream);
+}
+
+kda_status_t kda_gdp_decode_step(const kda_params_t* p, int32_t n_h, const void* q, const void* k,
+                                 const void* v, const float* beta, const float* log_decay,
+                                 const uint32_t* slot_idx, void* state_pool, float* o,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  return gdp_run(p, n_h, true, q, k, v, beta, log_decay, nullptr, slot_idx, state_pool, o,
+                 workspace, workspace_bytes, stream);
 }
 
 kda_status_t kda_decode_step(const kda_params_t* p, const void* q, const void* k, const void* v,

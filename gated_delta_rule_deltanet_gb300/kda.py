@@ -337,3 +337,108 @@ def fold_accepted(ring, accepted, slot_idx, state_pool, *, window: int, num_k_he
     if st != _lib.KDA_OK:
         raise KdaError(st, "kda_fold_accepted")
     return state_pool
+
+
+# ----------------------------------------------------------------------------- Gated DeltaProduct
+
+def _gdp_params(q, k, v, beta, log_decay, num_seqs, slot_idx, state_pool, chunk, scale, l2norm,
+                checked, cuda_cores, decode):
+    if q.dim() != 3 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q must be [T, HK, D], k [T, n_h, HK, D], v [T, n_h, HV, D]")
+    T, HK, D = q.shape
+    n_h, HV = k.shape[1], v.shape[2]
+    if tuple(k.shape) != (T, n_h, HK, D) or tuple(v.shape) != (T, n_h, HV, D):
+        raise ValueError("k must be [T, n_h, HK, D] and v [T, n_h, HV, D]")
+    if q.dtype not in _QKV_DTYPES or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share one dtype: float32 or bfloat16")
+    if not (k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("k and v must be contiguous")
+    if beta.dtype != torch.float32 or tuple(beta.shape) != (T, n_h, HV) or not beta.is_contiguous():
+        raise ValueError("beta must be contiguous float32 [T, n_h, HV]")
+    if log_decay.dtype != torch.float32 or not log_decay.is_contiguous():
+        raise ValueError("log_decay must be contiguous float32")
+    if tuple(log_decay.shape) == (T, HV):
+        per_channel = False
+    elif tuple(log_decay.shape) == (T, HV, D):
+        per_channel = True
+    else:
+        raise ValueError("log_decay must be [T, HV] (scalar) or [T, HV, D] (per channel)")
+    if slot_idx.dtype not in _INDEX_DTYPES or not slot_idx.is_contiguous() or slot_idx.numel() != num_seqs:
+        raise ValueError("slot_idx must be contiguous int32/uint32 with one entry per sequence")
+    if (state_pool.dim() != 4 or state_pool.shape[1] != HV or state_pool.shape[2] != D
+            or state_pool.shape[3] != D or state_pool.dtype not in _QKV_DTYPES
+            or not state_pool.is_contiguous()):
+        raise ValueError("state_pool must be contiguous [num_slots, HV, D, D] float32/bfloat16")
+    p = make_params(num_seqs=num_seqs, num_k_heads=HK, num_v_heads=HV, d=D,
+                    num_slots=state_pool.shape[0], total_tokens=T, chunk=chunk,
+                    qkv_dtype=q.dtype, state_dtype=state_pool.dtype, per_channel=per_channel,
+                    scale=scale, l2norm=l2norm, checked=checked, cuda_cores=cuda_cores,
+                    q_row_stride=_row_stride(q, "q"))
+    n = ctypes.c_size_t(0)
+    st = _lib.load().kda_gdp_workspace_size(ctypes.byref(p), n_h, int(decode), ctypes.byref(n))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_gdp_workspace_size")
+    return p, n_h, int(n.value)
+
+
+def _workspace(need, workspace, dev):
+    if workspace is None:
+        return torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    return workspace
+
+
+def gdp_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                log_decay: torch.Tensor, input_row_offsets: torch.Tensor, slot_idx: torch.Tensor,
+                state_pool: torch.Tensor, *, chunk: int = 64, scale: float = 0.0,
+                l2norm: bool = True, checked: bool = False, cuda_cores: bool = False,
+                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Gated DeltaProduct prefill (kda_gdp_prefill_fwd): n_h = k.shape[1] transitions per
+    token.  q [T, HK, D]; k [T, n_h, HK, D]; v [T, n_h, HV, D]; beta [T, n_h, HV];
+    log_decay [T, HV] or [T, HV, D].  Returns o [T, HV, D] fp32; the pool slots are updated
+    in place."""
+    dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool)
+    if input_row_offsets.dtype not in _INDEX_DTYPES or not input_row_offsets.is_contiguous():
+        raise ValueError("input_row_offsets must be contiguous int32/uint32")
+    p, n_h, need = _gdp_params(q, k, v, beta, log_decay, input_row_offsets.numel() - 1, slot_idx,
+                               state_pool, chunk, scale, l2norm, checked, cuda_cores, False)
+    T, HV, D = q.shape[0], v.shape[2], q.shape[2]
+    if out is None:
+        out = torch.empty((T, HV, D), dtype=torch.float32, device=dev)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (T, HV, D) or not out.is_contiguous():
+        raise ValueError("out must be contiguous float32 [T, HV, D]")
+    workspace = _workspace(need, workspace, dev)
+    st = _lib.load().kda_gdp_prefill_fwd(
+        ctypes.byref(p), n_h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_decay),
+        _ptr(input_row_offsets), _ptr(slot_idx), _ptr(state_pool), _ptr(out), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream, dev))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_gdp_prefill_fwd")
+    return out
+
+
+def gdp_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                    log_decay: torch.Tensor, slot_idx: torch.Tensor, state_pool: torch.Tensor, *,
+                    chunk: int = 0, scale: float = 0.0, l2norm: bool = True,
+                    out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """One Gated DeltaProduct decode step (kda_gdp_decode_step): one token of n_h transitions
+    per sequence; arrays as gdp_prefill with T = B.  Returns o [B, HV, D] fp32."""
+    dev = _check_cuda(q, k, v, beta, log_decay, slot_idx, state_pool)
+    p, n_h, need = _gdp_params(q, k, v, beta, log_decay, q.shape[0], slot_idx, state_pool, chunk,
+                               scale, l2norm, False, False, True)
+    B, HV, D = q.shape[0], v.shape[2], q.shape[2]
+    if out is None:
+        out = torch.empty((B, HV, D), dtype=torch.float32, device=dev)
+    elif out.dtype != torch.float32 or tuple(out.shape) != (B, HV, D) or not out.is_contiguous():
+        raise ValueError("out must be contiguous float32 [B, HV, D]")
+    workspace = _workspace(need, workspace, dev)
+    st = _lib.load().kda_gdp_decode_step(
+        ctypes.byref(p), n_h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_decay),
+        _ptr(slot_idx), _ptr(state_pool), _ptr(out), _ptr(workspace),
+        ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream, dev))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_gdp_decode_step")
+    return out

@@ -237,6 +237,55 @@ kda_status_t kda_fold_accepted(const kda_params_t *p, const float *ring, int32_t
                                void *state_pool, void *stream);
 
 /*
+ * Gated DeltaProduct ("Linear attention visualized", Gated Delta Product section and
+ * its virtual-sequence table).  Every token carries n_h transitions, each with its own
+ * key, value and gate; the state decays once (by the token's log_decay) before the
+ * first, the n_h predict / correct / write steps follow in order, and the token's query
+ * reads the state after the last.  n_h = 1 is kda_prefill_fwd.  Computed as the gated
+ * delta rule over the virtual sequence of T * n_h positions (decay on the first
+ * substep, query on the last, every n_h-th output kept) on the same prefill path.
+ *
+ *   n_h                1..64 substeps per token
+ *   q                  [T, HK, d_k], one query per token (q_row_stride between tokens)
+ *   k                  [T, n_h, HK, d_k] (k_row_stride between substep rows)
+ *   v                  [T, n_h, HV, d_v] (v_row_stride between substep rows)
+ *   beta               [T, n_h, HV] fp32
+ *   log_decay          [T, HV] or [T, HV, d_k] fp32, one per token
+ *   input_row_offsets, slot_idx, state_pool: as kda_prefill_fwd, over tokens
+ *   o                  [T, HV, d_v] fp32, one output per token
+ *   workspace          >= kda_gdp_workspace_size(p, n_h, 0) bytes, 256-byte aligned
+ * The workspace also holds the virtual queries, log-decays and outputs
+ * (T * n_h * (HK*d_k*qkv size + HV*gate width*4 + HV*d_v*4) bytes) ahead of the
+ * prefill's own workspace.  Errors as kda_prefill_fwd; n_h outside 1..64 is
+ * KDA_ERR_INVALID_ARG, T * n_h >= 2^31 is KDA_ERR_UNSUPPORTED.
+ */
+kda_status_t kda_gdp_prefill_fwd(const kda_params_t *p, int32_t n_h, const void *q,
+                                 const void *k, const void *v, const float *beta,
+                                 const float *log_decay, const uint32_t *input_row_offsets,
+                                 const uint32_t *slot_idx, void *state_pool, float *o,
+                                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One Gated DeltaProduct decode step: one token (n_h transitions) for each of
+ * B = num_seqs sequences, read from and written back to slot_idx[b] of the pool.
+ * Arrays as kda_gdp_prefill_fwd with T = B and no offsets; total_tokens is ignored,
+ * chunk 0 means 64.  Workspace: kda_gdp_workspace_size(p, n_h, 1) bytes.
+ */
+kda_status_t kda_gdp_decode_step(const kda_params_t *p, int32_t n_h, const void *q,
+                                 const void *k, const void *v, const float *beta,
+                                 const float *log_decay, const uint32_t *slot_idx,
+                                 void *state_pool, float *o, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/*
+ * Workspace bytes of kda_gdp_prefill_fwd (decode = 0) or kda_gdp_decode_step
+ * (decode = 1) for these parameters and n_h.  Returns the status the call would
+ * return for invalid parameters; *bytes is then left unchanged.
+ */
+kda_status_t kda_gdp_workspace_size(const kda_params_t *p, int32_t n_h, int32_t decode,
+                                    size_t *bytes);
+
+/*
  * Waits for `stream`, then returns the device error word of the current device
  * in *code (KDA_DEVERR_*) and clears it.  Returns KDA_ERR_DEVICE when the word
  * was set, KDA_OK when it was clear, KDA_ERR_CUDA when a CUDA call failed.

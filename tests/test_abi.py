@@ -188,14 +188,55 @@ def test_verify_and_fold_reject_bad_arguments_before_launch(lib):
 
 
 def test_compact_flag_shrinks_the_tensor_core_workspace(lib):
-    """The two-kernel tensor-core form stores 66,048 bytes of chain operands per chunk
+    """The two-kernel tensor-core form stores 74,240 bytes of chain operands per chunk
     and value head; the single-kernel form needs only the chunk table."""
     p = good(total_tokens=4096, num_seqs=2)
     c = good(total_tokens=4096, num_seqs=2, compact=True)
     assert lib.kda_prefill_uses_tensor_cores(ctypes.byref(c)) == 1
     full, small = ws_status(lib, p)[1], ws_status(lib, c)[1]
-    assert full - small >= (4096 // 64) * 8 * 66048
+    assert full - small >= (4096 // 64) * 8 * 74240
     assert small < 64 * 1024
     q = good()
     q.flags |= 8                                            # an unknown flag
     assert ws_status(lib, q)[0] == _lib.KDA_ERR_INVALID_ARG
+
+
+def gdp_ws(lib, p, n_h, decode=0):
+    n = ctypes.c_size_t(0)
+    st = lib.kda_gdp_workspace_size(ctypes.byref(p) if p is not None else None, n_h, decode,
+                                    ctypes.byref(n))
+    return st, int(n.value)
+
+
+def test_gdp_rejects_bad_arguments_before_launch(lib):
+    """Gated DeltaProduct: substep count, virtual length, pointers and workspace are checked
+    on the host; the workspace covers the virtual sequence plus the prefill's own."""
+    p = good(total_tokens=1024, num_seqs=2)
+    for n_h in (0, -1, 65):
+        assert gdp_ws(lib, p, n_h)[0] == _lib.KDA_ERR_INVALID_ARG
+    st1, w1 = gdp_ws(lib, p, 1)
+    st3, w3 = gdp_ws(lib, p, 3)
+    assert st1 == st3 == _lib.KDA_OK and w3 > w1 > 0
+    n = ctypes.c_size_t(0)
+    assert lib.kda_prefill_workspace_size(ctypes.byref(p), ctypes.byref(n)) == _lib.KDA_OK
+    assert w1 >= int(n.value) + 1024 * 8 * 128 * 4                   # virtual o at least
+    big = good(total_tokens=(1 << 30), num_seqs=1)
+    assert gdp_ws(lib, big, 2)[0] == _lib.KDA_ERR_UNSUPPORTED        # T * n_h >= 2^31
+    dec = good(num_seqs=4, total_tokens=0, chunk=0)
+    assert gdp_ws(lib, dec, 2, decode=1)[0] == _lib.KDA_OK           # decode: chunk 0 -> 64
+    assert gdp_ws(lib, dec, 2, decode=0)[0] != _lib.KDA_OK
+    a = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 8)
+    args = [a] * 9
+    assert lib.kda_gdp_prefill_fwd(ctypes.byref(p), 0, *args, a, 1 << 40, None) == \
+        _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_gdp_prefill_fwd(ctypes.byref(p), 2, a, a, a, a, a, None, a, a, a, a,
+                                   1 << 40, None) == _lib.KDA_ERR_INVALID_ARG   # no offsets
+    assert lib.kda_gdp_prefill_fwd(ctypes.byref(p), 2, a, mis, a, a, a, a, a, a, a, a,
+                                   1 << 40, None) == _lib.KDA_ERR_INVALID_ARG   # misaligned k
+    assert lib.kda_gdp_prefill_fwd(ctypes.byref(p), 2, *args, a, 16, None) == \
+        _lib.KDA_ERR_WORKSPACE
+    assert lib.kda_gdp_decode_step(ctypes.byref(dec), 2, a, a, a, a, a, None, a, a, a, 1 << 40,
+                                   None) == _lib.KDA_ERR_INVALID_ARG            # no slots
+    empty = good(num_seqs=0, total_tokens=0)
+    assert lib.kda_gdp_prefill_fwd(ctypes.byref(empty), 2, *([None] * 10), 0, None) == _lib.KDA_OK

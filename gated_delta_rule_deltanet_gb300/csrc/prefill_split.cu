@@ -84,6 +84,13 @@ constexpr uint32_t O_GS = 0, O_BETA = 256, O_RK = 512, O_RQ = 768, O_EG = 1024, 
                    O_GAM = 1536, O_GA = 2048, O_EA = 2560, O_KF = 2816, SMALL_BYTES = 3072;
 
 constexpr int SP = 68;      // padded row of the fp32 solve tiles
+
+// float index of element (token m, channel c) of the staged per-channel log-decay: four
+// quarters of 32 channels, 64 rows of 128 bytes each, 16-byte chunks swizzled by m % 8
+// (the TMA copies' 128-byte swizzle); 4 consecutive channels from c % 4 == 0 stay adjacent
+__device__ __forceinline__ int g_off(int m, int c) {
+  return (c >> 5) * (64 * 32) + m * 32 + ((((c & 31) >> 2) ^ (m & 7)) << 2) + (c & 3);
+}
 constexpr int XP = 36;      // row of the merge temporaries
 constexpr uint32_t SOL_BYTES = 2 * C * SP * 4 + 32 * XP * 4;
 
@@ -104,16 +111,16 @@ struct FrontMap<false> {
   static constexpr uint32_t BYTES = TBT + 64 * 64 * 2;
 };
 
-// Per-channel decay: raw rows are staged (padded) and the A-GEMM operands are the
-// normalised, decayed rows as split bf16 (high halves in shared memory, the low half
-// of [K+; Q+] in tensor memory).
+// Per-channel decay: TMA copies stage the raw k and q rows (the 128-byte swizzled layout
+// of the scalar path) and the log-decay rows (four 32-channel quarters, each 64 rows of
+// 128 bytes, swizzled the same way); the A-GEMM operands are the normalised, decayed rows
+// as split bf16 (high halves in shared memory, the low half of [K+; Q+] in tensor memory).
 template <>
 struct FrontMap<true> {
-  static constexpr int KS = D + 8, GS = D + 4;
-  static constexpr uint32_t S_K = 0;
-  static constexpr uint32_t S_Q = S_K + C * KS * 2;
-  static constexpr uint32_t S_G = S_Q + C * KS * 2;     // log-decay -> exp(G - G_a), fp32
-  static constexpr uint32_t SMALL = S_G + C * GS * 4;
+  static constexpr uint32_t AK_HALF = 128 * 128;        // raw k | q, as the scalar AK
+  static constexpr uint32_t RAW = 0;
+  static constexpr uint32_t S_G = RAW + 2 * AK_HALF;    // log-decay -> exp(G - G_a), fp32
+  static constexpr uint32_t SMALL = S_G + C * D * 4;
   static constexpr uint32_t AK = SMALL + SMALL_BYTES;   // [K+; Q+] high halves
   static constexpr uint32_t BK = AK + 128 * 128 * 2;    // K- high half
   static constexpr uint32_t BKLO = BK + 64 * 128 * 2;   // K- low half
@@ -163,8 +170,8 @@ __device__ __forceinline__ uint4 f16x8_pack(const float* x) {
 
 }  // namespace tcs
 
-// cp.async copies of one chunk's beta and log-decay, and for per-channel decay its k and
-// q rows (rows past n zero-filled); for scalar decay k and q come by TMA
+// cp.async copies of one chunk's beta and, for scalar decay, log-decay (rows past n
+// zero-filled); k, q and a per-channel log-decay come by TMA
 template <bool PERCH>
 __device__ __forceinline__ void front_issue_loads(const Problem& P, unsigned char* smem,
                                                   int64_t t0, int n, int kh, int h, int tid) {
@@ -172,27 +179,6 @@ __device__ __forceinline__ void front_issue_loads(const Problem& P, unsigned cha
   using M = FrontMap<PERCH>;
   const int HV = P.HV;
   const uint32_t sb = tc::smem_u32(smem);
-  if constexpr (PERCH) {
-    for (int u = tid; u < C * (D / 8); u += NT) {
-      const int i = u / (D / 8), q8 = u % (D / 8);
-      const bool live = i < n;
-      const int64_t t = live ? t0 + i : t0;
-      const uint32_t nb = live ? 16u : 0u;
-      tc::cp_async16(sb + M::S_K + (i * M::KS + q8 * 8) * 2,
-                     static_cast<const uint16_t*>(P.k) + t * P.k_stride + static_cast<int64_t>(kh) * D + q8 * 8, nb);
-      tc::cp_async16(sb + M::S_Q + (i * M::KS + q8 * 8) * 2,
-                     static_cast<const uint16_t*>(P.q) + t * P.q_stride + static_cast<int64_t>(kh) * D + q8 * 8, nb);
-    }
-  }
-  if constexpr (PERCH) {
-    for (int u = tid; u < C * (D / 4); u += NT) {
-      const int i = u / (D / 4), q4 = u % (D / 4);
-      const bool live = i < n;
-      const int64_t t = live ? t0 + i : t0;
-      tc::cp_async16(sb + M::S_G + (i * M::GS + q4 * 4) * 4, P.g + (t * HV + h) * D + q4 * 4,
-                     live ? 16u : 0u);
-    }
-  }
   if (tid < C) {
     const bool live = tid < n;
     const int64_t t = live ? t0 + tid : t0;
@@ -207,7 +193,8 @@ __device__ __forceinline__ void front_issue_loads(const Problem& P, unsigned cha
 template <bool PERCH>
 __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     tc_front_kernel(Problem P, PlanView plan, unsigned char* records,
-                    const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk) {
+                    const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmg) {
   using namespace tcs;
   using M = FrontMap<PERCH>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -248,6 +235,9 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   float* sT = reinterpret_cast<float*>(smem + M::R2 + C * SP * 4);
   float* sX = reinterpret_cast<float*>(smem + M::R2 + 2 * C * SP * 4);
   constexpr uint32_t KEA = M::R2, KTT = M::R2 + 64 * 128 * 2;  // K_end, K~ (MN-major)
+  constexpr uint32_t M_RAW = PERCH ? FrontMap<true>::RAW : 0u;     // raw k | q (per-channel)
+  constexpr uint32_t M_SG = PERCH ? FrontMap<true>::S_G : 0u;      // staged log-decay
+  constexpr uint32_t M_AK = PERCH ? 0u : FrontMap<false>::AK;      // raw k | q (scalar)
   const int64_t bt = (static_cast<int64_t>(gc) * HV + h) * static_cast<int64_t>(REC_BYTES);
   uint4* blob = reinterpret_cast<uint4*>(records + bt + REC_BLOB) + tid;  // piece p at [p * NT]
 
@@ -263,14 +253,19 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     tc::fence_mbar_init();
     s_abort = 0;
     s_range = 0;
-    if constexpr (!PERCH) {                     // k and q: both 64-channel halves, 64 rows each
-      const uint32_t sb = tc::smem_u32(smem + M::AK);
+    {                                           // k and q: both 64-channel halves, 64 rows each
+      const uint32_t sb = tc::smem_u32(smem + (PERCH ? M_RAW : M_AK));
       const int32_t row0 = static_cast<int32_t>(t0);
-      tc::mbar_arrive_expect_tx(&s_ld, 2 * M::AK_HALF);
+      tc::mbar_arrive_expect_tx(&s_ld, 2 * M::AK_HALF + (PERCH ? C * D * 4 : 0));
 #pragma unroll
       for (int a = 0; a < 2; ++a) {
         tc::tma_load_3d(sb + a * M::AK_HALF, &tmk, 64 * a, kh, row0, &s_ld);
         tc::tma_load_3d(sb + a * M::AK_HALF + C * 128, &tmq, 64 * a, kh, row0, &s_ld);
+      }
+      if constexpr (PERCH) {                    // log-decay: four 32-channel quarters
+        const uint32_t sg = tc::smem_u32(smem + M_SG);
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) tc::tma_load_3d(sg + qq * (C * 128), &tmg, 32 * qq, h, row0, &s_ld);
       }
     }
   }
@@ -298,21 +293,25 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   };
   // 8 raw bf16 channels [c, c + 8) of token i of k or q
   auto kq_piece = [&](bool is_q, int i, int c) -> const unsigned char* {
-    if constexpr (PERCH) return smem + (is_q ? M::S_Q : M::S_K) + (i * M::KS + c) * 2;
-    else return smem + M::AK + (c >> 6) * M::AK_HALF + tc::sw128_offset(is_q ? C + i : i, (c & 63) >> 3);
+    return smem + (PERCH ? M_RAW : M_AK) + (c >> 6) * M::AK_HALF + tc::sw128_offset(is_q ? C + i : i, (c & 63) >> 3);
   };
 
   tc::cp_async_wait_all();
-  if constexpr (!PERCH) {
-    if (!tc::mbar_wait_bounded(&s_ld, 0, kWaitLimit)) s_abort = 1;
-    // rows past the chunk's end hold the next sequence's tokens (or the TMA's zero fill):
-    // clear them, as the cp.async path does, so nothing of another sequence enters
-    if (n < C) {
-      uint4* ak = reinterpret_cast<uint4*>(smem + M::AK);
-      for (int u = tid; u < (C - n) * 32; u += NT) {      // 2 halves x (k, q) x 8 chunks
-        const int r = n + (u >> 5), part = u & 31;
-        const int a = part >> 4, qk = (part >> 3) & 1, c8 = part & 7;
-        ak[(a * M::AK_HALF + (qk * C + r) * 128) / 16 + c8] = make_uint4(0u, 0u, 0u, 0u);
+  if (!tc::mbar_wait_bounded(&s_ld, 0, kWaitLimit)) s_abort = 1;
+  // rows past the chunk's end hold the next sequence's tokens (or the TMA's zero fill):
+  // clear them, as a zero-filling copy would, so nothing of another sequence enters
+  if (n < C) {
+    uint4* ak = reinterpret_cast<uint4*>(smem + (PERCH ? M_RAW : M_AK));
+    for (int u = tid; u < (C - n) * 32; u += NT) {        // 2 halves x (k, q) x 8 chunks
+      const int r = n + (u >> 5), part = u & 31;
+      const int a = part >> 4, qk = (part >> 3) & 1, c8 = part & 7;
+      ak[(a * M::AK_HALF + (qk * C + r) * 128) / 16 + c8] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if constexpr (PERCH) {                      // log-decay rows: 4 quarters x 8 chunks
+      uint4* sgq = reinterpret_cast<uint4*>(smem + M_SG);
+      for (int u = tid; u < (C - n) * 32; u += NT) {
+        const int r = n + (u >> 5), qq = (u >> 3) & 3, c8 = u & 7;
+        sgq[(qq * (C * 128) + r * 128) / 16 + c8] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
   }
@@ -352,24 +351,24 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
       for (int i0 = 0; i0 < C; i0 += 16) {
         float gv[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) gv[e] = sG[(i0 + e) * M::GS + tid];
+        for (int e = 0; e < 16; ++e) gv[e] = sG[g_off(i0 + e, tid)];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           acc += gv[e];
           gmin = fminf(gmin, acc);
           gmax = fmaxf(gmax, acc);
-          sG[(i0 + e) * M::GS + tid] = acc;
+          sG[g_off(i0 + e, tid)] = acc;
         }
       }
-      const float ga = sG[((n - 1) / 2) * M::GS + tid];
+      const float ga = sG[g_off((n - 1) / 2, tid)];
       if (fmaxf(gmax - ga, ga - gmin) > kMaxHalfChunkDecay) s_range = 1;
 #pragma unroll
       for (int i0 = 0; i0 < C; i0 += 16) {
         float gv[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) gv[e] = sG[(i0 + e) * M::GS + tid];
+        for (int e = 0; e < 16; ++e) gv[e] = sG[g_off(i0 + e, tid)];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) sG[(i0 + e) * M::GS + tid] = __expf(gv[e] - ga);
+        for (int e = 0; e < 16; ++e) sG[g_off(i0 + e, tid)] = __expf(gv[e] - ga);
       }
       sGam[tid] = __expf(acc);
       sGA[tid] = __expf(ga);
@@ -409,16 +408,16 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
     {                                           // [K+; Q+]: high halves to smem, low to TMEM
       const int i = row < C ? row : row - C;
-      const uint32_t src = (row < C ? M::S_K : M::S_Q) + (i * M::KS) * 2;
+
       const float rs = row < C ? sRK[i] : sRQ[i];
       uint32_t lo[32];
 #pragma unroll
       for (int g8 = 0; g8 < 8; ++g8) {
         const int cc = 64 * chalf + 8 * g8;
         float x[8];
-        tc::bf16x8_load(smem + src + cc * 2, x);
-        const float4 g0 = *reinterpret_cast<const float4*>(sG + i * M::GS + cc);
-        const float4 g1 = *reinterpret_cast<const float4*>(sG + i * M::GS + cc + 4);
+        tc::bf16x8_load(kq_piece(row >= C, i, cc), x);
+        const float4 g0 = *reinterpret_cast<const float4*>(sG + g_off(i, cc));
+        const float4 g1 = *reinterpret_cast<const float4*>(sG + g_off(i, cc + 4));
         const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         uint32_t hi[4];
 #pragma unroll
@@ -449,9 +448,9 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
       for (int g8 = 0; g8 < 4; ++g8) {
         const int cc = 32 * qq + 8 * g8;
         float x[8];
-        tc::bf16x8_load(smem + M::S_K + (j * M::KS + cc) * 2, x);
-        const float4 g0 = *reinterpret_cast<const float4*>(sG + j * M::GS + cc);
-        const float4 g1 = *reinterpret_cast<const float4*>(sG + j * M::GS + cc + 4);
+        tc::bf16x8_load(kq_piece(false, j, cc), x);
+        const float4 g0 = *reinterpret_cast<const float4*>(sG + g_off(j, cc));
+        const float4 g1 = *reinterpret_cast<const float4*>(sG + g_off(j, cc + 4));
         const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
         uint32_t hi[4], lo[4];
 #pragma unroll
@@ -700,10 +699,10 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     const float rk = sRK[m];
     if constexpr (PERCH) {
       const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
-      const float4 e0 = *reinterpret_cast<const float4*>(sG + m * M::GS + c0);
-      const float4 e1 = *reinterpret_cast<const float4*>(sG + m * M::GS + c0 + 4);
-      const float4 l0 = *reinterpret_cast<const float4*>(sG + (C - 1) * M::GS + c0);
-      const float4 l1 = *reinterpret_cast<const float4*>(sG + (C - 1) * M::GS + c0 + 4);
+      const float4 e0 = *reinterpret_cast<const float4*>(sG + g_off(m, c0));
+      const float4 e1 = *reinterpret_cast<const float4*>(sG + g_off(m, c0 + 4));
+      const float4 l0 = *reinterpret_cast<const float4*>(sG + g_off(C - 1, c0));
+      const float4 l1 = *reinterpret_cast<const float4*>(sG + g_off(C - 1, c0 + 4));
       const float4 a0 = *reinterpret_cast<const float4*>(sGA + c0);
       const float4 a1 = *reinterpret_cast<const float4*>(sGA + c0 + 4);
       const float Em[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
@@ -828,8 +827,8 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
         tc::bf16x8_load(kq_piece(true, i, c0 + 8 * g8), qv);
         if constexpr (PERCH) {
           const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
-          const float4 ga = *reinterpret_cast<const float4*>(sG + i * M::GS + c0 + 8 * g8);
-          const float4 gb = *reinterpret_cast<const float4*>(sG + i * M::GS + c0 + 8 * g8 + 4);
+          const float4 ga = *reinterpret_cast<const float4*>(sG + g_off(i, c0 + 8 * g8));
+          const float4 gb = *reinterpret_cast<const float4*>(sG + g_off(i, c0 + 8 * g8 + 4));
           const float4 aa = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8);
           const float4 ab = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8 + 4);
           const float gv[8] = {ga.x * aa.x, ga.y * aa.y, ga.z * aa.z, ga.w * aa.w,
@@ -1310,20 +1309,36 @@ static bool encode_rows_map(CUtensorMap* m, const void* base, const Problem& P, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// per-channel log-decay [T, HV, 128] fp32: boxes of 32 channels x 1 head x 64 tokens, 128-byte
+// swizzle, zero fill past the last token
+static bool encode_g_map(CUtensorMap* m, const Problem& P) {
+  auto enc = tensor_map_encoder();
+  if (!enc || P.T <= 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(tcs::D), static_cast<cuuint64_t>(P.HV),
+                              static_cast<cuuint64_t>(P.T)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(tcs::D) * 4,
+                                 static_cast<cuuint64_t>(P.HV) * tcs::D * 4};
+  const cuuint32_t box[3] = {32, 1, static_cast<cuuint32_t>(tcs::C)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(P.g), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool PERCH>
 static cudaError_t launch_front_t(const Problem& P, const PlanView& plan, unsigned char* recs,
                                   cudaStream_t st) {
   auto k = tc_front_kernel<PERCH>;
   constexpr uint32_t bytes = tcs::FrontMap<PERCH>::BYTES + 1024;
-  alignas(64) CUtensorMap tmq, tmk;
-  memset(&tmq, 0, sizeof(tmq));
-  memset(&tmk, 0, sizeof(tmk));
-  if (!PERCH && !(encode_rows_map(&tmq, P.q, P, P.q_stride) && encode_rows_map(&tmk, P.k, P, P.k_stride)))
+  alignas(64) CUtensorMap tmq, tmk, tmg;
+  memset(&tmg, 0, sizeof(tmg));
+  if (!(encode_rows_map(&tmq, P.q, P, P.q_stride) && encode_rows_map(&tmk, P.k, P, P.k_stride)))
     return cudaErrorInvalidValue;
+  if (PERCH && !encode_g_map(&tmg, P)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  k<<<dim3(static_cast<unsigned>(plan_max_chunks(P)), P.HV), tcs::NT, bytes, st>>>(P, plan, recs, tmq, tmk);
+  k<<<dim3(static_cast<unsigned>(plan_max_chunks(P)), P.HV), tcs::NT, bytes, st>>>(P, plan, recs, tmq, tmk, tmg);
   return cudaGetLastError();
 }
 

@@ -81,9 +81,14 @@ static_assert(REC_BYTES % 16 == 0 && REC_OA % 16 == 0, "records must stay 16-byt
 
 // per-chunk vectors of the front kernel (byte offsets inside its SMALL area)
 constexpr uint32_t O_GS = 0, O_BETA = 256, O_RK = 512, O_RQ = 768, O_EG = 1024, O_EGL = 1280,
-                   O_GAM = 1536, O_GA = 2048, O_EA = 2560, O_KF = 2816, SMALL_BYTES = 3072;
+                   O_GAM = 1536, O_GA = 2048, O_EA = 2560, O_KF = 2816, O_EL = 3072,
+                   SMALL_BYTES = 3584;
 
-constexpr int SP = 68;      // padded row of the fp32 solve tiles
+// the fp32 solve tiles (A_kk and T, 64 x 64): element (r, c) at sidx(r, c), whose 4-float
+// groups are permuted by r % 8 so that column-wise and row-wise 16-byte accesses both
+// spread over the banks; a 16-byte group from c % 4 == 0 stays contiguous
+__device__ __forceinline__ int sidx(int r, int c) { return r * 64 + (c ^ ((r & 7) << 2)); }
+constexpr int SOL_TILE = 64 * 64 * 4;
 
 // float index of element (token m, channel c) of the staged per-channel log-decay: four
 // quarters of 32 channels, 64 rows of 128 bytes each, 16-byte chunks swizzled by m % 8
@@ -92,7 +97,7 @@ __device__ __forceinline__ int g_off(int m, int c) {
   return (c >> 5) * (64 * 32) + m * 32 + ((((c & 31) >> 2) ^ (m & 7)) << 2) + (c & 3);
 }
 constexpr int XP = 36;      // row of the merge temporaries
-constexpr uint32_t SOL_BYTES = 2 * C * SP * 4 + 32 * XP * 4;
+constexpr uint32_t SOL_BYTES = 2 * SOL_TILE + 32 * XP * 4;
 
 template <bool PERCH>
 struct FrontMap;
@@ -109,26 +114,36 @@ struct FrontMap<false> {
   static constexpr uint32_t LMAT = R2 + SOL_BYTES;      // [*; A_qk] 128 x 64 fp16, then Kb
   static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;  // TB 64 x 64 fp16, MN-major
   static constexpr uint32_t BYTES = TBT + 64 * 64 * 2;
+  static constexpr uint32_t KEA = R2, KTT = R2 + 64 * 128 * 2;     // K_end, K~ (MN-major)
+  static constexpr uint32_t KBA = LMAT, A1A = TBT - 64 * 64 * 2;   // Kb, [*; A1o] (K-major)
 };
 
 // Per-channel decay: TMA copies stage the raw k and q rows (the 128-byte swizzled layout
 // of the scalar path) and the log-decay rows (four 32-channel quarters, each 64 rows of
-// 128 bytes, swizzled the same way); the A-GEMM operands are the normalised, decayed rows
-// as split bf16 (high halves in shared memory, the low half of [K+; Q+] in tensor memory).
+// 128 bytes, swizzled the same way).  The A-GEMM operands are the normalised, decayed rows
+// as split bf16: [K+; Q+] high halves overwrite the raw rows in place, its low halves go to
+// tensor memory, K- (both halves) to BK | BKLO.  Once the A-GEMM is done, K~ and Q~ are
+// rebuilt from the two halves of [K+; Q+] and K_end from K-, so the staged rows, the
+// log-decay and K- can all be reused: every region below serves several phases, which keeps
+// two CTAs per SM.
 template <>
 struct FrontMap<true> {
-  static constexpr uint32_t AK_HALF = 128 * 128;        // raw k | q, as the scalar AK
-  static constexpr uint32_t RAW = 0;
-  static constexpr uint32_t S_G = RAW + 2 * AK_HALF;    // log-decay -> exp(G - G_a), fp32
+  static constexpr uint32_t AK_HALF = 128 * 128;
+  static constexpr uint32_t RAW = 0;                    // raw k | q -> [K+; Q+] high halves;
+                                                        // then TB (half 0 k rows), A_qk (half 1
+                                                        // k rows), Q~ in place (q rows)
+  static constexpr uint32_t S_G = RAW + 2 * AK_HALF;    // log-decay -> exp(G - G_a); then K_end | K~
   static constexpr uint32_t SMALL = S_G + C * D * 4;
-  static constexpr uint32_t AK = SMALL + SMALL_BYTES;   // [K+; Q+] high halves
-  static constexpr uint32_t BK = AK + 128 * 128 * 2;    // K- high half
-  static constexpr uint32_t BKLO = BK + 64 * 128 * 2;   // K- low half
-  static constexpr uint32_t R2 = BK;                    // consumed K- halves: solve, K_end, K~
-  static constexpr uint32_t LMAT = R2 + SOL_BYTES;
-  static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;
-  static constexpr uint32_t BYTES = TBT + 64 * 64 * 2;
-  static_assert(LMAT >= BKLO + 64 * 128 * 2, "solve area covers the K- halves");
+  static constexpr uint32_t BK = SMALL + SMALL_BYTES;   // K- high | low halves; then the solve
+  static constexpr uint32_t BKLO = BK + 64 * 128 * 2;   // tiles; then Kb | [*; A1o]
+  static constexpr uint32_t R2 = BK;
+  static constexpr uint32_t BYTES = R2 + SOL_BYTES;
+  static constexpr uint32_t TBT = RAW;
+  static constexpr uint32_t LMAT = RAW + AK_HALF - 64 * 64 * 2;   // rows 64-127: half 1 k rows
+  static constexpr uint32_t KEA = S_G, KTT = S_G + 64 * 128 * 2;
+  static constexpr uint32_t KBA = BK, A1A = BK + 64 * 128 * 2;
+  static_assert(R2 + 2 * SOL_TILE == BKLO + 64 * 128 * 2, "solve tiles cover the K- halves");
+  static_assert(A1A + 128 * 64 * 2 <= BYTES, "[*; A1o] operand in bounds");
 };
 
 // front TMEM columns: A_kk/A_qk (second issuer's half of K in F_X), then Kb | A1o, then
@@ -152,7 +167,7 @@ constexpr uint32_t CH_GAM = CH_OST + C * OS * 4;         // gamma of four chunks
 constexpr uint32_t GAM_SLOTS = 4;
 constexpr uint32_t CH_BYTES = CH_GAM + GAM_SLOTS * D * 4;
 static_assert(CH_BYTES + 64 <= 227 * 1024, "chain shared memory budget");
-static_assert(FrontMap<true>::BYTES + 1024 + 64 <= 227 * 1024, "front shared memory budget");
+static_assert(2 * (FrontMap<true>::BYTES + 3 * 1024) <= 228 * 1024, "two per-channel front CTAs per SM");
 static_assert(2 * (FrontMap<false>::BYTES + 1024 + 1024) <= 228 * 1024, "two scalar front CTAs per SM");
 static_assert(CH_V % 128 == 0 && CH_ST % 128 == 0 && OA_BYTES % 128 == 0, "operand alignment");
 static_assert(CH_OA + (OA_SLOTS + 1) * OA_BYTES <= CH_BYTES, "rows 64-127 of the last OA stay in bounds");
@@ -191,7 +206,7 @@ __device__ __forceinline__ void front_issue_loads(const Problem& P, unsigned cha
 // One CTA per (chunk, value head): everything of the chunk that does not depend on the
 // state, written to the chunk's record.
 template <bool PERCH>
-__global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
+__global__ void __launch_bounds__(tcs::NT, 2)
     tc_front_kernel(Problem P, PlanView plan, unsigned char* records,
                     const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmg) {
@@ -231,10 +246,11 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   float* sGA = reinterpret_cast<float*>(smem + M::SMALL + O_GA);
   float* sEA = reinterpret_cast<float*>(smem + M::SMALL + O_EA);
   float* sKF = reinterpret_cast<float*>(smem + M::SMALL + O_KF);
+  float* sEL = reinterpret_cast<float*>(smem + M::SMALL + O_EL);
   float* sA = reinterpret_cast<float*>(smem + M::R2);
-  float* sT = reinterpret_cast<float*>(smem + M::R2 + C * SP * 4);
-  float* sX = reinterpret_cast<float*>(smem + M::R2 + 2 * C * SP * 4);
-  constexpr uint32_t KEA = M::R2, KTT = M::R2 + 64 * 128 * 2;  // K_end, K~ (MN-major)
+  float* sT = reinterpret_cast<float*>(smem + M::R2 + SOL_TILE);
+  float* sX = reinterpret_cast<float*>(smem + M::R2 + 2 * SOL_TILE);
+  constexpr uint32_t KEA = M::KEA, KTT = M::KTT;   // K_end, K~ (MN-major)
   constexpr uint32_t M_RAW = PERCH ? FrontMap<true>::RAW : 0u;     // raw k | q (per-channel)
   constexpr uint32_t M_SG = PERCH ? FrontMap<true>::S_G : 0u;      // staged log-decay
   constexpr uint32_t M_AK = PERCH ? 0u : FrontMap<false>::AK;      // raw k | q (scalar)
@@ -292,9 +308,10 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     tc::fence_after_sync();
   };
   // 8 raw bf16 channels [c, c + 8) of token i of k or q
-  auto kq_piece = [&](bool is_q, int i, int c) -> const unsigned char* {
-    return smem + (PERCH ? M_RAW : M_AK) + (c >> 6) * M::AK_HALF + tc::sw128_offset(is_q ? C + i : i, (c & 63) >> 3);
+  auto kq_off = [&](bool is_q, int i, int c) -> uint32_t {
+    return (PERCH ? M_RAW : M_AK) + (c >> 6) * M::AK_HALF + tc::sw128_offset(is_q ? C + i : i, (c & 63) >> 3);
   };
+  auto kq_piece = [&](bool is_q, int i, int c) -> const unsigned char* { return smem + kq_off(is_q, i, c); };
 
   tc::cp_async_wait_all();
   if (!tc::mbar_wait_bounded(&s_ld, 0, kWaitLimit)) s_abort = 1;
@@ -372,6 +389,7 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
       }
       sGam[tid] = __expf(acc);
       sGA[tid] = __expf(ga);
+      sEL[tid] = __expf(acc - ga);              // exp(G_last - G_a)
     }
   } else if (warp == 0) {                       // scalar: warp scan of 64 values
     const float g0 = sGs[2 * lane], g1 = sGs[2 * lane + 1];
@@ -406,43 +424,8 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   if (!PERCH && tid < C) sKF[tid] *= sRK[tid];
   if constexpr (PERCH) {
     const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
-    {                                           // [K+; Q+]: high halves to smem, low to TMEM
-      const int i = row < C ? row : row - C;
-
-      const float rs = row < C ? sRK[i] : sRQ[i];
-      uint32_t lo[32];
-#pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) {
-        const int cc = 64 * chalf + 8 * g8;
-        float x[8];
-        tc::bf16x8_load(kq_piece(row >= C, i, cc), x);
-        const float4 g0 = *reinterpret_cast<const float4*>(sG + g_off(i, cc));
-        const float4 g1 = *reinterpret_cast<const float4*>(sG + g_off(i, cc + 4));
-        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        uint32_t hi[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const float v0 = x[e] * rs * f[e], v1 = x[e + 1] * rs * f[e + 1];
-          hi[e / 2] = tc::pack_bf16x2(v0, v1);
-          const float h0 = __uint_as_float(hi[e / 2] << 16);
-          const float h1 = __uint_as_float(hi[e / 2] & 0xffff0000u);
-          lo[4 * g8 + e / 2] = tc::pack_bf16x2(v0 - h0, v1 - h1);
-        }
-        *reinterpret_cast<uint4*>(smem + M::AK + tc::cm_offset(row, cc, 128, tc::dense_sbo(D))) =
-            make_uint4(hi[0], hi[1], hi[2], hi[3]);
-      }
-      uint32_t l0[16], l1[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        l0[e] = lo[e];
-        l1[e] = lo[16 + e];
-      }
-      tc::tmem_st16(tmem + lane_addr + F_ALO + 32 * chalf, l0);
-      tc::tmem_st16(tmem + lane_addr + F_ALO + 32 * chalf + 16, l1);
-      tc::tmem_wait_st();
-    }
-    {                                           // K-: 4 threads per key row
-      const int j = tid >> 2, qq = tid & 3;
+    {                                           // K- (both halves) first: it reads the raw k rows
+      const int j = tid >> 2, qq = tid & 3;     // 4 threads per key row
       const float rs = sRK[j];
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8) {
@@ -468,6 +451,41 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
             make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
     }
+    __syncthreads();
+    {                                           // [K+; Q+]: high halves over the raw rows, low to TMEM
+      const int i = row < C ? row : row - C;
+      const float rs = row < C ? sRK[i] : sRQ[i];
+      uint32_t lo[32];
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8) {
+        const int cc = 64 * chalf + 8 * g8;
+        unsigned char* piece = const_cast<unsigned char*>(kq_piece(row >= C, i, cc));
+        float x[8];
+        tc::bf16x8_load(piece, x);
+        const float4 g0 = *reinterpret_cast<const float4*>(sG + g_off(i, cc));
+        const float4 g1 = *reinterpret_cast<const float4*>(sG + g_off(i, cc + 4));
+        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        uint32_t hi[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const float v0 = x[e] * rs * f[e], v1 = x[e + 1] * rs * f[e + 1];
+          hi[e / 2] = tc::pack_bf16x2(v0, v1);
+          const float h0 = __uint_as_float(hi[e / 2] << 16);
+          const float h1 = __uint_as_float(hi[e / 2] & 0xffff0000u);
+          lo[4 * g8 + e / 2] = tc::pack_bf16x2(v0 - h0, v1 - h1);
+        }
+        *reinterpret_cast<uint4*>(piece) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      }
+      uint32_t l0[16], l1[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        l0[e] = lo[e];
+        l1[e] = lo[16 + e];
+      }
+      tc::tmem_st16(tmem + lane_addr + F_ALO + 32 * chalf, l0);
+      tc::tmem_st16(tmem + lane_addr + F_ALO + 32 * chalf + 16, l1);
+      tc::tmem_wait_st();
+    }
   }
   tc::fence_async_smem();
   tc::fence_before_sync();
@@ -482,20 +500,25 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     const uint32_t id = tc::idesc_f16(128, 64, tc::kBF16);
     const uint32_t d = tmem + (second ? F_X : F_A);
     if constexpr (PERCH) {
-      const uint64_t dak = tc::smem_desc(tc::smem_u32(smem + M::AK), 128, tc::dense_sbo(D));
+      // [K+; Q+] high halves: the swizzled rows of the raw tiles, K steps of 32 bytes within
+      // a 64-channel half
+      const uint32_t araw = tc::smem_u32(smem + M::RAW);
+      auto dak = [&](int s) {
+        return tc::desc_add(tc::smem_desc_sw128(araw + (s >> 2) * M::AK_HALF, 1024), (s & 3) * 32);
+      };
       const uint64_t dbk = tc::smem_desc(tc::smem_u32(smem + M::BK), 128, tc::dense_sbo(D));
       const uint64_t dbl = tc::smem_desc(tc::smem_u32(smem + M::BKLO), 128, tc::dense_sbo(D));
       if (!second) {
 #pragma unroll
         for (int s = 0; s < D / 16; ++s)        // hi x hi
-          tc::mma_ss(d, tc::desc_add(dak, s * 256), tc::desc_add(dbk, s * 256), id, s > 0);
+          tc::mma_ss(d, dak(s), tc::desc_add(dbk, s * 256), id, s > 0);
 #pragma unroll
         for (int s = 0; s < D / 32; ++s)        // hi x lo, first half of K
-          tc::mma_ss(d, tc::desc_add(dak, s * 256), tc::desc_add(dbl, s * 256), id, 1);
+          tc::mma_ss(d, dak(s), tc::desc_add(dbl, s * 256), id, 1);
       } else {
 #pragma unroll
         for (int s = D / 32; s < D / 16; ++s)   // hi x lo, second half of K
-          tc::mma_ss(d, tc::desc_add(dak, s * 256), tc::desc_add(dbl, s * 256), id, s > D / 32);
+          tc::mma_ss(d, dak(s), tc::desc_add(dbl, s * 256), id, s > D / 32);
 #pragma unroll
         for (int s = 0; s < D / 16; ++s)        // lo x hi (low half from TMEM)
           tc::mma_ts(d, tmem + F_ALO + s * 8, tc::desc_add(dbk, s * 256), id, 1);
@@ -509,6 +532,54 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     tc::mma_commit(second ? &s_bar2 : &s_bar);
   }
   mma_wait2();
+
+  if constexpr (PERCH) {
+    // ---------------------------------------------------------------- K~, Q~, K_end
+    // rebuilt from the split halves the A-GEMM has consumed: K~ = K+ exp(G_a) and
+    // K_end = K- exp(G_last - G_a) (MN-major fp16, over the consumed log-decay),
+    // Q~ = Q+ exp(G_a) (fp16, over its own raw rows)
+    {
+      const int i = row < C ? row : row - C;
+      uint32_t l0[16], l1[16];
+      tc::tmem_ld16(tmem + lane_addr + F_ALO + 32 * chalf, l0);
+      tc::tmem_ld16(tmem + lane_addr + F_ALO + 32 * chalf + 16, l1);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int g8 = 0; g8 < 8; ++g8) {
+        const int cc = 64 * chalf + 8 * g8;
+        const uint32_t off = kq_off(row >= C, i, cc);
+        float x[8];
+        tc::bf16x8_load(smem + off, x);
+        const float4 a0 = *reinterpret_cast<const float4*>(sGA + cc);
+        const float4 a1 = *reinterpret_cast<const float4*>(sGA + cc + 4);
+        const float ea[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const uint32_t w = g8 < 4 ? l0[4 * g8 + e / 2] : l1[4 * (g8 - 4) + e / 2];
+          x[e] = (x[e] + __uint_as_float(w << 16)) * ea[e];
+          x[e + 1] = (x[e + 1] + __uint_as_float(w & 0xffff0000u)) * ea[e + 1];
+        }
+        tc::f16x8_store(smem, row < C ? KTT + tc::mn_offset(i, cc, KT_LBO, KT_SBO) : off, x);
+      }
+    }
+    {
+      const int j = tid >> 2, qq = tid & 3;     // 4 threads per key row
+#pragma unroll
+      for (int g8 = 0; g8 < 4; ++g8) {
+        const int cc = 32 * qq + 8 * g8;
+        float hi[8], lo[8], ke[8];
+        tc::bf16x8_load(smem + M::BK + tc::cm_offset(j, cc, 128, tc::dense_sbo(D)), hi);
+        tc::bf16x8_load(smem + M::BKLO + tc::cm_offset(j, cc, 128, tc::dense_sbo(D)), lo);
+        const float4 e0 = *reinterpret_cast<const float4*>(sEL + cc);
+        const float4 e1 = *reinterpret_cast<const float4*>(sEL + cc + 4);
+        const float el[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ke[e] = (hi[e] + lo[e]) * el[e];
+        tc::f16x8_store(smem, KEA + tc::mn_offset(j, cc, KE_LBO, KE_SBO), ke);
+      }
+    }
+    __syncthreads();                            // the solve tiles and A_qk overwrite K-, k rows
+  }
 
   // ------------------------------------------------------------------ A_kk, A_qk
   {
@@ -557,7 +628,7 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     if (is_k) {
 #pragma unroll
       for (int e = 0; e < 32; e += 4)
-        *reinterpret_cast<float4*>(sA + i * SP + 32 * chalf + e) =
+        *reinterpret_cast<float4*>(sA + sidx(i, 32 * chalf + e)) =
             make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
     } else {
 #pragma unroll
@@ -569,23 +640,29 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   // the 32x32 merge reads the strictly-upper 16x16 blocks of T11 and T22: zero them
   for (int idx = tid; idx < 2 * 256; idx += NT) {
     const int blk = idx >> 8, r = (idx >> 4) & 15, c = idx & 15;
-    sT[(32 * blk + r) * SP + 32 * blk + 16 + c] = 0.f;
+    sT[sidx(32 * blk + r, 32 * blk + 16 + c)] = 0.f;
   }
   __syncthreads();
 
   // ------------------------------------------------------------------ solve
   if (warp < 2) {                               // diagonal 16x16 blocks, one column per lane
     const int base = (warp * 2 + (lane >> 4)) * 16, col = lane & 15;
+    // row base + r keeps its columns [base, base + 16) in the 16-float block at base, or at
+    // base ^ 16 when r % 8 >= 4, permuted inside it by (r % 4) * 4: constant offsets from
+    // two row pointers
+    const float* blk0 = sA + base * 64 + base;
+    const float* blk1 = sA + base * 64 + (base ^ 16);
     float t[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
+      const float* rp = ((r & 4) ? blk1 : blk0) + r * 64;
       float v = r == col ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < r; ++m) v -= sA[(base + r) * SP + base + m] * t[m];
+      for (int m = 0; m < r; ++m) v -= rp[m ^ ((r & 3) << 2)] * t[m];
       t[r] = v;
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) sT[(base + r) * SP + base + col] = t[r];
+    for (int r = 0; r < 16; ++r) sT[sidx(base + r, base + col)] = t[r];
   }
   __syncthreads();
   if (tid < 128) {                              // X = A21 T11, two 16x16 pairs
@@ -594,13 +671,13 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     float a[16];
 #pragma unroll
     for (int m = 0; m < 16; m += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(sA + (r0 + r) * SP + c0 + m);
+      const float4 v = *reinterpret_cast<const float4*>(sA + sidx(r0 + r, c0 + m));
       a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
-      const float4 t = *reinterpret_cast<const float4*>(sT + (c0 + m) * SP + c0 + c);
+      const float4 t = *reinterpret_cast<const float4*>(sT + sidx(c0 + m, c0 + c));
       acc.x += a[m] * t.x; acc.y += a[m] * t.y; acc.z += a[m] * t.z; acc.w += a[m] * t.w;
     }
     *reinterpret_cast<float4*>(sX + (16 * p + r) * XP + c) = acc;
@@ -612,7 +689,7 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     float a[16];
 #pragma unroll
     for (int m = 0; m < 16; m += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(sT + (r0 + r) * SP + r0 + m);
+      const float4 v = *reinterpret_cast<const float4*>(sT + sidx(r0 + r, r0 + m));
       a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -621,7 +698,7 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
       const float4 x = *reinterpret_cast<const float4*>(sX + (16 * p + m) * XP + c);
       acc.x += a[m] * x.x; acc.y += a[m] * x.y; acc.z += a[m] * x.z; acc.w += a[m] * x.w;
     }
-    *reinterpret_cast<float4*>(sT + (r0 + r) * SP + c0 + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    *reinterpret_cast<float4*>(sT + sidx(r0 + r, c0 + c)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
   {                                             // X = A21 T11, one 32x32 pair
@@ -629,13 +706,13 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     float a[32];
 #pragma unroll
     for (int m = 0; m < 32; m += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(sA + (32 + r) * SP + m);
+      const float4 v = *reinterpret_cast<const float4*>(sA + sidx(32 + r, m));
       a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < 32; ++m) {
-      const float4 t = *reinterpret_cast<const float4*>(sT + m * SP + c);
+      const float4 t = *reinterpret_cast<const float4*>(sT + sidx(m, c));
       acc.x += a[m] * t.x; acc.y += a[m] * t.y; acc.z += a[m] * t.z; acc.w += a[m] * t.w;
     }
     *reinterpret_cast<float4*>(sX + r * XP + c) = acc;
@@ -646,7 +723,7 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
     float a[32];
 #pragma unroll
     for (int m = 0; m < 32; m += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(sT + (32 + r) * SP + 32 + m);
+      const float4 v = *reinterpret_cast<const float4*>(sT + sidx(32 + r, 32 + m));
       a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -655,13 +732,13 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
       const float4 x = *reinterpret_cast<const float4*>(sX + m * XP + c);
       acc.x += a[m] * x.x; acc.y += a[m] * x.y; acc.z += a[m] * x.z; acc.w += a[m] * x.w;
     }
-    *reinterpret_cast<float4*>(sT + (32 + r) * SP + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    *reinterpret_cast<float4*>(sT + sidx(32 + r, c)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
   for (int u = tid; u < C * (C / 8); u += NT) { // TB[m][j] = T[m][j] beta_j, row pieces
     const int m = (u >> 6) * 8 + (u & 7), j0 = ((u >> 3) & 7) * 8;
-    const float4 t0 = *reinterpret_cast<const float4*>(sT + m * SP + j0);
-    const float4 t1 = *reinterpret_cast<const float4*>(sT + m * SP + j0 + 4);
+    const float4 t0 = *reinterpret_cast<const float4*>(sT + sidx(m, j0));
+    const float4 t1 = *reinterpret_cast<const float4*>(sT + sidx(m, j0 + 4));
     const float4 b0 = *reinterpret_cast<const float4*>(sBeta + j0);
     const float4 b1 = *reinterpret_cast<const float4*>(sBeta + j0 + 4);
     const float tv[8] = {t0.x * b0.x, t0.y * b0.y, t0.z * b0.z, t0.w * b0.w,
@@ -692,37 +769,22 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   // K_end = k^ exp(G_last - G_m) (A operand K_end^T, MN-major) and K~ = k^ exp(G_m) (B
   // operand of the second round, MN-major) into the consumed solve area, row pieces of 8
   // channels
-  for (int u = tid; u < C * (D / 8); u += NT) {
-    const int m = (u >> 7) * 8 + (u & 7), c0 = ((u >> 3) & 15) * 8;
-    float kx[8], ke[8], kt[8];
-    tc::bf16x8_load(kq_piece(false, m, c0), kx);
-    const float rk = sRK[m];
-    if constexpr (PERCH) {
-      const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
-      const float4 e0 = *reinterpret_cast<const float4*>(sG + g_off(m, c0));
-      const float4 e1 = *reinterpret_cast<const float4*>(sG + g_off(m, c0 + 4));
-      const float4 l0 = *reinterpret_cast<const float4*>(sG + g_off(C - 1, c0));
-      const float4 l1 = *reinterpret_cast<const float4*>(sG + g_off(C - 1, c0 + 4));
-      const float4 a0 = *reinterpret_cast<const float4*>(sGA + c0);
-      const float4 a1 = *reinterpret_cast<const float4*>(sGA + c0 + 4);
-      const float Em[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-      const float El[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-      const float ea[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ke[e] = kx[e] * rk * __fdividef(El[e], Em[e]);
-        kt[e] = kx[e] * rk * Em[e] * ea[e];
-      }
-    } else {
+  // (the per-channel path built both before the A extraction)
+  if constexpr (!PERCH) {
+    for (int u = tid; u < C * (D / 8); u += NT) {
+      const int m = (u >> 7) * 8 + (u & 7), c0 = ((u >> 3) & 15) * 8;
+      float kx[8], ke[8], kt[8];
+      tc::bf16x8_load(kq_piece(false, m, c0), kx);
+      const float rk = sRK[m];
       const float fe = rk * sEGL[m], ft = rk * sEG[m];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         ke[e] = kx[e] * fe;
         kt[e] = kx[e] * ft;
       }
+      tc::f16x8_store(smem, KEA + tc::mn_offset(m, c0, KE_LBO, KE_SBO), ke);
+      tc::f16x8_store(smem, KTT + tc::mn_offset(m, c0, KT_LBO, KT_SBO), kt);
     }
-    tc::f16x8_store(smem, KEA + tc::mn_offset(m, c0, KE_LBO, KE_SBO), ke);
-    tc::f16x8_store(smem, KTT + tc::mn_offset(m, c0, KT_LBO, KT_SBO), kt);
   }
   if (tid < D) reinterpret_cast<float*>(rec + REC_GAM)[tid] = sGam[tid];
   tc::fence_async_smem();
@@ -744,7 +806,7 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
   // Kb (fp16): record pieces 0-3 and the K-major A operand of P (consumed [*; A_qk] area);
   // A1o (fp16): columns 0-63 of the output operand and rows 64-127 of the A operand of
   // A1o K~ (in the consumed TB area; its rows 0-63 fall on Kb's rows 64-127, unread)
-  constexpr uint32_t KBA = M::LMAT, A1A = M::TBT - 64 * 64 * 2;
+  constexpr uint32_t KBA = M::KBA, A1A = M::A1A;
   {
     uint32_t r0[16], r1[16];
     tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf, r0);
@@ -823,19 +885,11 @@ __global__ void __launch_bounds__(tcs::NT, PERCH ? 1 : 2)
       const float rq = sRQ[i];
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8) {
-        float qv[8];
-        tc::bf16x8_load(kq_piece(true, i, c0 + 8 * g8), qv);
-        if constexpr (PERCH) {
-          const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
-          const float4 ga = *reinterpret_cast<const float4*>(sG + g_off(i, c0 + 8 * g8));
-          const float4 gb = *reinterpret_cast<const float4*>(sG + g_off(i, c0 + 8 * g8 + 4));
-          const float4 aa = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8);
-          const float4 ab = *reinterpret_cast<const float4*>(sGA + c0 + 8 * g8 + 4);
-          const float gv[8] = {ga.x * aa.x, ga.y * aa.y, ga.z * aa.z, ga.w * aa.w,
-                               gb.x * ab.x, gb.y * ab.y, gb.z * ab.z, gb.w * ab.w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * rq * gv[e];
+        if constexpr (PERCH) {                  // Q~ was built in place
+          tc::f16x8_load(kq_piece(true, i, c0 + 8 * g8), x + 8 * g8);
         } else {
+          float qv[8];
+          tc::bf16x8_load(kq_piece(true, i, c0 + 8 * g8), qv);
           const float f = rq * sEG[i];
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * f;

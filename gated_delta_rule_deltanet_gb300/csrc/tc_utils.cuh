@@ -345,5 +345,15 @@ __device__ __forceinline__ void bf16x8_load(const unsigned char* p, float* x) {
   }
 }
 
+// 8 fp16 from a 16-byte aligned address, widened to fp32
+__device__ __forceinline__ void f16x8_load(const unsigned char* p, float* x) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e)
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+        : "=f"(x[2 * e]), "=f"(x[2 * e + 1]) : "r"(w[e]));
+}
+
 }  // namespace tc
 }  // namespace kda

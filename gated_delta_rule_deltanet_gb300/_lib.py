@@ -21,6 +21,7 @@ KDA_DECAY_PER_CHANNEL = 1
 KDA_FLAG_CHECKED = 1
 KDA_FLAG_CUDA_CORES = 2
 KDA_FLAG_COMPACT = 4
+KDA_FLAG_NO_DELTA = 8
 
 KDA_DEVERR_NONE = 0
 KDA_DEVERR_OFFSETS = 1

@@ -85,7 +85,7 @@ kda_status_t check_common(const kda_params_t* p, Problem* P) {
   if (p->state_dtype != KDA_DTYPE_F32 && p->state_dtype != KDA_DTYPE_BF16) return KDA_ERR_INVALID_ARG;
   if (p->decay_kind != KDA_DECAY_SCALAR && p->decay_kind != KDA_DECAY_PER_CHANNEL)
     return KDA_ERR_INVALID_ARG;
-  if (p->flags & ~(KDA_FLAG_CHECKED | KDA_FLAG_CUDA_CORES | KDA_FLAG_COMPACT))
+  if (p->flags & ~(KDA_FLAG_CHECKED | KDA_FLAG_CUDA_CORES | KDA_FLAG_COMPACT | KDA_FLAG_NO_DELTA))
     return KDA_ERR_INVALID_ARG;
   const int64_t es = static_cast<int64_t>(elem_size(p->qkv_dtype));
   const int64_t dq = static_cast<int64_t>(p->num_k_heads) * p->d_k;
@@ -158,6 +158,7 @@ kda_status_t prefill_dispatch(const kda_params_t* p, const Problem& P, void* wor
 constexpr int32_t kMaxSubsteps = 64;
 kda_status_t gdp_virtual_params(const kda_params_t* p, int32_t n_h, bool decode, kda_params_t* pv) {
   if (!p || n_h < 1 || n_h > kMaxSubsteps) return KDA_ERR_INVALID_ARG;
+  if (p->flags & KDA_FLAG_NO_DELTA) return KDA_ERR_UNSUPPORTED;   // defined on the delta rule
   *pv = *p;
   const int64_t T = decode ? static_cast<int64_t>(p->num_seqs) : p->total_tokens;
   if (T < 0) return KDA_ERR_INVALID_ARG;

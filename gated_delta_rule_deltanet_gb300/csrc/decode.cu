@@ -117,7 +117,9 @@ __global__ void __launch_bounds__(NT) decode_step_kernel(Problem P) {
     }
     return tot;
   };
-  const float4 vhat = reduce_rows(part, 0);
+  // additive write (no delta rule): nothing is predicted, e = beta v
+  const float4 vhat = (P.flags & KDA_FLAG_NO_DELTA) ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                    : reduce_rows(part, 0);
 
   // 4. correct and write
   const float4 e = make_float4(vbeta * (vv.x - vhat.x), vbeta * (vv.y - vhat.y),

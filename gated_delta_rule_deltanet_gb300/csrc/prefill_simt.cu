@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
   const int kh = h / (HV / P.HK);
   const int n = ci.n;
   const int64_t t0 = ci.t0;
+  // additive write (no delta rule): A_kk = 0 makes T = I, and W = 0
+  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
 
   for (int idx = tid; idx < C * D; idx += NT) {
     const int i = idx / D, c = idx % D;
@@ -176,7 +178,7 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
         aqk *= dec;
       }
     }
-    s_A[i * CP + j] = j < i ? s_beta[i] * akk : 0.f;
+    s_A[i * CP + j] = (delta && j < i) ? s_beta[i] * akk : 0.f;
     s_Aq[i * CP + j] = aqk;
   }
   __syncthreads();
@@ -228,7 +230,7 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
     const float di = expf(Gi);
     gQ[idx] = s_q[i * DP + c] * di;
     gK[idx] = s_k[i * DP + c] * expf(Gl - Gi);
-    s_q[i * DP + c] = s_beta[i] * s_k[i * DP + c] * di;
+    s_q[i * DP + c] = delta ? s_beta[i] * s_k[i * DP + c] * di : 0.f;
     s_v[i * DP + c] *= s_beta[i];
   }
   for (int c = tid; c < D; c += NT)

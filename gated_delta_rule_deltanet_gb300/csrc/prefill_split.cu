@@ -234,6 +234,8 @@ __global__ void __launch_bounds__(tcs::NT, 2)
   const int kh = h / (HV / P.HK);
   const int n = ci.n;
   const int64_t t0 = ci.t0;
+  // additive write (no delta rule): A_kk = 0 makes T = I and K~ = 0 drops W = TB K~
+  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
   unsigned char* rec = records + (static_cast<int64_t>(gc) * HV + h) * static_cast<int64_t>(REC_BYTES);
 
   float* sGs = reinterpret_cast<float*>(smem + M::SMALL + O_GS);
@@ -559,6 +561,10 @@ __global__ void __launch_bounds__(tcs::NT, 2)
           x[e] = (x[e] + __uint_as_float(w << 16)) * ea[e];
           x[e + 1] = (x[e + 1] + __uint_as_float(w & 0xffff0000u)) * ea[e + 1];
         }
+        if (row < C && !delta) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = 0.f;
+        }
         tc::f16x8_store(smem, row < C ? KTT + tc::mn_offset(i, cc, KT_LBO, KT_SBO) : off, x);
       }
     }
@@ -622,7 +628,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const int j = 32 * chalf + e;
-      const bool keep = is_k ? (j < i) : (j <= i);
+      const bool keep = is_k ? (delta && j < i) : (j <= i);
       x[e] = keep ? x[e] : 0.f;
     }
     if (is_k) {
@@ -776,7 +782,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       float kx[8], ke[8], kt[8];
       tc::bf16x8_load(kq_piece(false, m, c0), kx);
       const float rk = sRK[m];
-      const float fe = rk * sEGL[m], ft = rk * sEG[m];
+      const float fe = rk * sEGL[m], ft = delta ? rk * sEG[m] : 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         ke[e] = kx[e] * fe;

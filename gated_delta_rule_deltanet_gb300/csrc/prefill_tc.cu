@@ -182,6 +182,8 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   const int b = blockIdx.x, h = blockIdx.y, vt = blockIdx.z;
   const int HV = P.HV;
   const int kh = h / (HV / P.HK);
+  // additive write (no delta rule): A_kk = 0 makes T = I and K~ = 0 drops W = TB K~
+  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
   const uint32_t bos = P.offsets[b], eos = P.offsets[b + 1];
   if (eos <= bos) return;
   const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + vt * BV;
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int j = 32 * chalf + e;
-        const bool keep = is_k ? (j < i) : (j <= i);
+        const bool keep = is_k ? (delta && j < i) : (j <= i);
         x[e] = keep ? x[e] : 0.f;
       }
       if (is_k) {
@@ -674,7 +676,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
           const int m = m8 * 8 + e;
           const float Em = sG[m * GS + c];
           const float kx = bf16_at(smem, S_K, m * KS + c) * sRK[m];
-          kt[e] = kx * Em * ea;                              // k^ exp(G_m)
+          kt[e] = delta ? kx * Em * ea : 0.f;                // k^ exp(G_m)
           ke[e] = kx * __fdividef(El, Em);                   // k^ exp(G_last - G_m)
         }
       } else {
@@ -682,7 +684,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
         for (int e = 0; e < 8; ++e) {
           const int m = m8 * 8 + e;
           const float kx = bf16_at(smem, S_K, m * KS + c) * sRK[m];
-          kt[e] = kx * sEG[m];
+          kt[e] = delta ? kx * sEG[m] : 0.f;
           ke[e] = kx * sEGL[m];
         }
       }

@@ -99,7 +99,9 @@ __global__ void __launch_bounds__(NT) verify_window_kernel(Problem P, int window
       S[i].x *= a; S[i].y *= a; S[i].z *= a; S[i].w *= a;
       part.x += S[i].x * kc; part.y += S[i].y * kc; part.z += S[i].z * kc; part.w += S[i].w * kc;
     }
-    const float4 vhat = reduce_rows(part, 0);
+    // additive write (no delta rule): nothing is predicted, e = beta v
+    const float4 vhat = (P.flags & KDA_FLAG_NO_DELTA) ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                      : reduce_rows(part, 0);
     const float4 e = make_float4(vbeta * (vv.x - vhat.x), vbeta * (vv.y - vhat.y),
                                  vbeta * (vv.z - vhat.z), vbeta * (vv.w - vhat.w));
     float4 opart = make_float4(0.f, 0.f, 0.f, 0.f);

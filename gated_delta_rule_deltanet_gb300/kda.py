@@ -52,7 +52,7 @@ def _check_cuda(*ts):
 def make_params(*, num_seqs, num_k_heads, num_v_heads, d, num_slots, total_tokens=0, chunk=64,
                 qkv_dtype=torch.bfloat16, state_dtype=torch.float32, per_channel=True,
                 scale=0.0, l2norm=True, checked=False, cuda_cores=False, compact=False,
-                q_row_stride=0,
+                delta_rule=True, q_row_stride=0,
                 k_row_stride=0, v_row_stride=0) -> KdaParams:
     return KdaParams(num_seqs=num_seqs, num_k_heads=num_k_heads, num_v_heads=num_v_heads, d_k=d,
                      d_v=d, num_slots=num_slots, total_tokens=total_tokens, chunk=chunk,
@@ -62,7 +62,8 @@ def make_params(*, num_seqs, num_k_heads, num_v_heads, d, num_slots, total_token
                      scale=float(scale), l2norm_qk=int(bool(l2norm)),
                      flags=((_lib.KDA_FLAG_CHECKED if checked else 0)
                             | (_lib.KDA_FLAG_CUDA_CORES if cuda_cores else 0)
-                            | (_lib.KDA_FLAG_COMPACT if compact else 0)),
+                            | (_lib.KDA_FLAG_COMPACT if compact else 0)
+                            | (0 if delta_rule else _lib.KDA_FLAG_NO_DELTA)),
                      q_row_stride=q_row_stride,
                      k_row_stride=k_row_stride, v_row_stride=v_row_stride)
 
@@ -84,7 +85,7 @@ def uses_tensor_cores(params: KdaParams) -> bool:
 
 
 def _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
-                    scale, l2norm, checked, cuda_cores=False, compact=False):
+                    scale, l2norm, checked, cuda_cores=False, compact=False, delta_rule=True):
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3:
         raise ValueError("q, k must be [T, HK, D] and v [T, HV, D]")
     T, HK, D = q.shape
@@ -118,7 +119,8 @@ def _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state
                        num_slots=state_pool.shape[0], total_tokens=T, chunk=chunk,
                        qkv_dtype=q.dtype, state_dtype=state_pool.dtype, per_channel=per_channel,
                        scale=scale, l2norm=l2norm, checked=checked, cuda_cores=cuda_cores,
-                       compact=compact, q_row_stride=_row_stride(q, "q"), k_row_stride=_row_stride(k, "k"),
+                       compact=compact, delta_rule=delta_rule, q_row_stride=_row_stride(q, "q"),
+                       k_row_stride=_row_stride(k, "k"),
                        v_row_stride=_row_stride(v, "v"))
 
 
@@ -126,17 +128,19 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tenso
             log_decay: torch.Tensor, input_row_offsets: torch.Tensor, slot_idx: torch.Tensor,
             state_pool: torch.Tensor, *, chunk: int = 64, scale: float = 0.0,
             l2norm: bool = True, checked: bool = False, cuda_cores: bool = False,
-            compact: bool = False, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+            compact: bool = False, delta_rule: bool = True, out: Optional[torch.Tensor] = None,
+            workspace: Optional[torch.Tensor] = None,
             stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """Chunkwise gated-delta-rule prefill (kda_prefill_fwd).  Returns o [T, HV, D] fp32.
 
     The pool slots named by slot_idx are updated in place with each sequence's final state.
     `cuda_cores=True` asks for the fp32 CUDA-core path where the tensor-core path applies;
-    `compact=True` runs the tensor-core path as a single kernel with a small workspace.
+    `compact=True` runs the tensor-core path as a single kernel with a small workspace;
+    `delta_rule=False` selects the additive write (KDA_FLAG_NO_DELTA: gated linear attention).
     """
     dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool)
     p = _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
-                        scale, l2norm, checked, cuda_cores, compact)
+                        scale, l2norm, checked, cuda_cores, compact, delta_rule)
     T, HV, D = v.shape
     if out is None:
         out = torch.empty((T, HV, D), dtype=torch.float32, device=dev)
@@ -160,7 +164,7 @@ def prefill_no_alloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
                      log_decay: torch.Tensor, input_row_offsets: torch.Tensor,
                      slot_idx: torch.Tensor, state_pool: torch.Tensor, *, chunk: int = 64,
                      scale: float = 0.0, l2norm: bool = True, checked: bool = False,
-                     cuda_cores: bool = False, out: torch.Tensor,
+                     cuda_cores: bool = False, delta_rule: bool = True, out: torch.Tensor,
                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
     """kda_prefill_fwd_no_alloc: the prefill with the library's built-in scratch array.
 
@@ -171,7 +175,7 @@ def prefill_no_alloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
     """
     dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, out)
     p = _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
-                        scale, l2norm, checked, cuda_cores)
+                        scale, l2norm, checked, cuda_cores, delta_rule=delta_rule)
     T, HV, D = v.shape
     if out.dtype != torch.float32 or tuple(out.shape) != (T, HV, D) or not out.is_contiguous():
         raise ValueError("out must be contiguous float32 [T, HV, D]")
@@ -186,9 +190,11 @@ def prefill_no_alloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
 
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                 log_decay: torch.Tensor, slot_idx: torch.Tensor, state_pool: torch.Tensor, *,
-                scale: float = 0.0, l2norm: bool = True, out: Optional[torch.Tensor] = None,
+                scale: float = 0.0, l2norm: bool = True, delta_rule: bool = True,
+                out: Optional[torch.Tensor] = None,
                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """One recurrent decode step (kda_decode_step) for B sequences.  Returns o [B, HV, D] fp32."""
+    """One recurrent decode step (kda_decode_step) for B sequences.  Returns o [B, HV, D] fp32.
+    `delta_rule=False` selects the additive write (KDA_FLAG_NO_DELTA)."""
     dev = _check_cuda(q, k, v, beta, log_decay, slot_idx, state_pool)
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[0] != q.shape[0]:
         raise ValueError("q, k must be [B, HK, D] and v [B, HV, D]")
@@ -214,7 +220,7 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
     p = make_params(num_seqs=B, num_k_heads=HK, num_v_heads=HV, d=D,
                     num_slots=state_pool.shape[0], qkv_dtype=q.dtype,
                     state_dtype=state_pool.dtype, per_channel=per_channel, scale=scale,
-                    l2norm=l2norm, q_row_stride=_row_stride(q, "q"),
+                    l2norm=l2norm, delta_rule=delta_rule, q_row_stride=_row_stride(q, "q"),
                     k_row_stride=_row_stride(k, "k"), v_row_stride=_row_stride(v, "v"))
     if out is None:
         out = torch.empty((B, HV, D), dtype=torch.float32, device=dev)
@@ -258,7 +264,8 @@ def ring_record_elems(params: KdaParams) -> int:
     return n
 
 
-def _window_params(q, k, v, beta, log_decay, slot_idx, state_pool, window, scale, l2norm):
+def _window_params(q, k, v, beta, log_decay, slot_idx, state_pool, window, scale, l2norm,
+                   delta_rule=True):
     if q.dim() != 3 or k.shape != q.shape or v.dim() != 3 or v.shape[0] != q.shape[0]:
         raise ValueError("q, k must be [B*window, HK, D] and v [B*window, HV, D]")
     BW, HK, D = q.shape
@@ -286,19 +293,21 @@ def _window_params(q, k, v, beta, log_decay, slot_idx, state_pool, window, scale
     return make_params(num_seqs=B, num_k_heads=HK, num_v_heads=HV, d=D,
                        num_slots=state_pool.shape[0], qkv_dtype=q.dtype,
                        state_dtype=state_pool.dtype, per_channel=per_channel, scale=scale,
-                       l2norm=l2norm, q_row_stride=_row_stride(q, "q"),
+                       l2norm=l2norm, delta_rule=delta_rule, q_row_stride=_row_stride(q, "q"),
                        k_row_stride=_row_stride(k, "k"), v_row_stride=_row_stride(v, "v"))
 
 
 def verify_window(q, k, v, beta, log_decay, slot_idx, state_pool, *, window: int,
-                  scale: float = 0.0, l2norm: bool = True, out=None, ring=None, stream=None):
+                  scale: float = 0.0, l2norm: bool = True, delta_rule: bool = True, out=None,
+                  ring=None, stream=None):
     """kda_verify_window: `window` draft tokens per sequence from its pool slot, pool untouched.
 
     Token t of sequence b is row b*window + t.  Returns (o [B*window, HV, D] fp32,
     ring [B, window, HV, R] fp32) where R = ring_record_elems.
     """
     dev = _check_cuda(q, k, v, beta, log_decay, slot_idx, state_pool)
-    p = _window_params(q, k, v, beta, log_decay, slot_idx, state_pool, window, scale, l2norm)
+    p = _window_params(q, k, v, beta, log_decay, slot_idx, state_pool, window, scale, l2norm,
+                       delta_rule)
     BW, HV, D = v.shape
     rec = ring_record_elems(p)
     if out is None:

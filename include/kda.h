@@ -86,11 +86,22 @@ typedef enum kda_decay_kind {
  * tile) that walks the sequence's chunks, with only the chunk table as workspace
  * (16 bytes per chunk).  Without it the path runs as two kernels: a chunk-parallel
  * one that writes every chunk's operands of the state recurrence to the workspace
- * (66,048 bytes per chunk and value head) and a sequential one over each
+ * (74,240 bytes per chunk and value head) and a sequential one over each
  * sequence's chunks, which keeps the chunk-local work off the sequential path.
  * The two forms round the same operands the same way; their results agree to
  * the tolerance, not bit for bit. */
 #define KDA_FLAG_COMPACT 4u
+/* Additive write in place of the delta rule: the correction subtracts no
+ * prediction, e_t = beta_t v_t, so S_t = Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ * (stored orientation: row = key channel).  With per-channel decay this is Gated
+ * Linear Attention, with scalar decay Mamba-2 (beta_t its write step size) or
+ * RetNet (a constant decay), and with zero log-decay and beta = 1 plain causal
+ * linear attention ("Linear attention visualized": the naive linear attention,
+ * RetNet, Mamba-2 and GLA sections; "From Attention to Learned Memory", sec. 1-2).
+ * Accepted by every prefill path, the decode step and the verify window (whose
+ * records then hold beta_t v_t); the Gated DeltaProduct entry points, whose method
+ * is defined on the delta rule, return KDA_ERR_UNSUPPORTED for it. */
+#define KDA_FLAG_NO_DELTA 8u
 
 /* Device error codes (kda_get_device_error). */
 #define KDA_DEVERR_NONE 0

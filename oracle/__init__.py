@@ -197,7 +197,7 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def run_decode(dp, *, steps: Optional[int] = None, nthreads: Optional[int] = None,
-               seq_mask=None):
+               seq_mask=None, delta_rule: bool = True):
     """The oracle on a `workloads.DecodeProblem`: each step is one token per sequence.
 
     Between steps the state lives in the pool, so a bf16 pool holds it rounded to
@@ -222,7 +222,8 @@ def run_decode(dp, *, steps: Optional[int] = None, nthreads: Optional[int] = Non
                              q=_widen(dp.q[s], dp.qkv_dtype), k=_widen(dp.k[s], dp.qkv_dtype),
                              v=_widen(dp.v[s], dp.qkv_dtype), beta=dp.beta[s], g=dp.g[s],
                              per_channel=(dp.decay_kind == "per_channel"), pool=pool,
-                             scale=dp.scale, pair_mask=pair_mask, nthreads=nthreads)
+                             scale=dp.scale, delta_rule=delta_rule, pair_mask=pair_mask,
+                             nthreads=nthreads)
         outs.append(o)
     return np.stack(outs), pool
 

@@ -35,10 +35,13 @@
  * n_h = 1 this is exactly the recurrence above.  (The page defines it on Gated DeltaNet's
  * scalar gate; a per-channel gate is applied the same way, once per token.)
  *
- * With delta_rule = 0 the correction is skipped (e_t = beta_t v_t); that is
- * plain causal linear attention ("From Attention to Learned Memory", sec. 1,
- * the additive write S_t = S_{t-1} + v_t k_t^T), used only to pin the read
- * against the brute-force causal product.
+ * With delta_rule = 0 the correction is skipped (e_t = beta_t v_t): the additive
+ * write of plain causal linear attention ("From Attention to Learned Memory",
+ * sec. 1, S_t = S_{t-1} + v_t k_t^T) and, with the forget step kept, of RetNet,
+ * Mamba-2 and Gated Linear Attention ("Linear attention visualized", those
+ * sections).  It is pinned against the brute-force causal product and the
+ * decayed parallel form, and is the reference for the library's additive-write
+ * mode.
  *
  * Work is split over (sequence, value head) pairs with POSIX threads; each
  * pair's arithmetic is a straight sequential loop (no blocking, no

@@ -197,8 +197,11 @@ def test_compact_flag_shrinks_the_tensor_core_workspace(lib):
     assert full - small >= (4096 // 64) * 8 * 74240
     assert small < 64 * 1024
     q = good()
-    q.flags |= 8                                            # an unknown flag
+    q.flags |= 16                                           # an unknown flag
     assert ws_status(lib, q)[0] == _lib.KDA_ERR_INVALID_ARG
+    nd = good(total_tokens=4096, num_seqs=2, delta_rule=False)  # additive write: same paths
+    assert ws_status(lib, nd) == ws_status(lib, p)
+    assert lib.kda_prefill_uses_tensor_cores(ctypes.byref(nd)) == 1
 
 
 def gdp_ws(lib, p, n_h, decode=0):
@@ -222,6 +225,8 @@ def test_gdp_rejects_bad_arguments_before_launch(lib):
     assert w1 >= int(n.value) + 1024 * 8 * 128 * 4                   # virtual o at least
     big = good(total_tokens=(1 << 30), num_seqs=1)
     assert gdp_ws(lib, big, 2)[0] == _lib.KDA_ERR_UNSUPPORTED        # T * n_h >= 2^31
+    assert gdp_ws(lib, good(total_tokens=1024, num_seqs=2, delta_rule=False), 2)[0] == \
+        _lib.KDA_ERR_UNSUPPORTED                                     # defined on the delta rule
     dec = good(num_seqs=4, total_tokens=0, chunk=0)
     assert gdp_ws(lib, dec, 2, decode=1)[0] == _lib.KDA_OK           # decode: chunk 0 -> 64
     assert gdp_ws(lib, dec, 2, decode=0)[0] != _lib.KDA_OK

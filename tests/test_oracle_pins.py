@@ -156,6 +156,34 @@ def pin_linear_attention_bruteforce(runner):
     np.testing.assert_allclose(S, S0 + kn.T @ v, atol=1e-12)
 
 
+def pin_gated_linear_attention_parallel(runner):
+    """"Linear attention visualized", RetNet, Mamba-2 and GLA sections: without the delta term
+    the decayed recurrence equals its parallel form.  A write at position j reaches the
+    query at t >= j through the decay of the tokens after it, so its score is
+    q^_t . (k^_j * exp(G_t - G_j)) with G the inclusive cumulative log-decay (the diagonal
+    is undecayed), it carries beta_j v_j (Mamba-2's write step), and the incoming state
+    enters as (q^_t * exp(G_t)) S0.  The final state is Diag(exp(G_T)) S0 plus every write
+    decayed to the end.  Scalar gate (Mamba-2) and per-channel gate (GLA)."""
+    T, dk, dv = 10, 8, 5
+    for per_channel in (False, True):
+        q, k, v, beta, g, S0 = small_inputs(19 + per_channel, T, dk, dv, per_channel=per_channel)
+        o, S = one_seq(runner, q, k, v, beta, g, S0, scale=0.0, l2norm=True, delta_rule=False)
+        qn = q / np.sqrt(np.sum(q.astype(np.float64) ** 2, axis=1, keepdims=True) + oracle.L2_EPS)
+        qn = qn / np.sqrt(dk)
+        kn = k / np.sqrt(np.sum(k.astype(np.float64) ** 2, axis=1, keepdims=True) + oracle.L2_EPS)
+        G = np.cumsum(g.astype(np.float64), axis=0)
+        if not per_channel:
+            G = np.repeat(G[:, None], dk, axis=1)
+        # scores[t, j] = sum_c q^_t[c] k^_j[c] exp(G_t[c] - G_j[c]), causal (j <= t)
+        scores = np.einsum("tc,jc,tjc->tj", qn, kn, np.exp(G[:, None, :] - G[None, :, :]))
+        scores *= np.tril(np.ones((T, T)))
+        bv = beta.astype(np.float64)[:, None] * v.astype(np.float64)
+        ref = scores @ bv + (qn * np.exp(G)) @ S0
+        np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+        S_ref = np.exp(G[-1])[:, None] * S0 + (kn * np.exp(G[-1] - G)).T @ bv
+        np.testing.assert_allclose(S, S_ref, rtol=0, atol=1e-12)
+
+
 def pin_beta_zero_pure_decay(runner):
     """Closed form: beta = 0 leaves only the forget gate, S_T = Diag(exp(sum g)) S0 and
     o_t = s q_t^T S_t (KDA page sec. 4, forget then read)."""
@@ -248,7 +276,8 @@ def pin_gqa_ragged_pool(runner):
 
 
 PINS = [pin_beta_one_recall, pin_orthogonal_directions_untouched, pin_erase_write_form,
-        pin_gradient_step, pin_linear_attention_bruteforce, pin_beta_zero_pure_decay,
+        pin_gradient_step, pin_linear_attention_bruteforce, pin_gated_linear_attention_parallel,
+        pin_beta_zero_pure_decay,
         pin_orthonormal_keys, pin_equal_channels_is_scalar_gate, pin_alice_bob,
         pin_gqa_ragged_pool]
 

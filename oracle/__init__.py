@@ -13,6 +13,8 @@ Contents
                                Delta Attention", sec. 6, evaluated densely in fp64 (numpy)
   causal_linear_attention(...) brute force (Q K^T masked) V + Q S0 ("From Attention to Learned
                                Memory", sec. 1-2), the delta-free, decay-free special case
+  backward(problem, ...)       reverse-mode differentiation of the recurrence in fp64
+                               (`oracle/backward.py`), pinned by finite differences
 
 Parity status: every function here is pinned by `tests/test_oracle_pins.py`
 against closed forms, invariants the pages state, brute force and the worked
@@ -340,3 +342,17 @@ def causal_linear_attention(q, k, v, S0, *, scale=None, l2norm=True):
 
 if __name__ == "__main__":  # pragma: no cover - manual build helper
     print(build(int(sys.argv[1]) if len(sys.argv) > 1 else 0, force=True))
+
+
+def backward(problem, d_o, d_state=None, *, delta_rule: bool = True, l2norm: bool = True,
+             pairs=None):
+    """The backward oracle on a `workloads.Problem` (the pool holds the initial states):
+    gradients of the loss whose gradients w.r.t. o and the final states are d_o and d_state.
+    Returns dict(dq, dk, dv, dbeta, dg, d_state0), fp64."""
+    from .backward import backward_arrays
+    p = problem
+    return backward_arrays(offsets=p.offsets, slot_idx=p.slot_idx, q=_widen(p.q, p.qkv_dtype),
+                           k=_widen(p.k, p.qkv_dtype), v=_widen(p.v, p.qkv_dtype), beta=p.beta,
+                           g=p.g, pool=_widen(p.pool, p.state_dtype).astype(np.float64),
+                           d_o=d_o, d_state=d_state, scale=p.scale, l2norm=l2norm,
+                           delta_rule=delta_rule, pairs=pairs)

@@ -33,6 +33,11 @@ cudaError_t launch_gdp_expand(const void* q, int64_t q_stride, bool qbf16, const
                               cudaStream_t st);
 cudaError_t launch_gdp_gather(const float* ov, int64_t T, int n_h, int64_t orow, float* o,
                               cudaStream_t st);
+size_t bwd_workspace_bytes(const Problem& P);
+cudaError_t launch_prefill_bwd(const Problem& P, void* workspace, const float* d_o,
+                               const float* d_state, float* dq, float* dk, float* dv,
+                               float* dbeta, float* dg, float* d_state0, bool qbf16, bool perch,
+                               bool sbf16, cudaStream_t stream);
 }  // namespace kda
 
 using kda::Problem;
@@ -290,6 +295,50 @@ kda_status_t kda_prefill_fwd(const kda_params_t* p, const void* q, const void* k
   P.err = device_error_word();
   if (!P.err) return KDA_ERR_CUDA;
   return prefill_dispatch(p, P, workspace, static_cast<cudaStream_t>(stream));
+}
+
+kda_status_t kda_prefill_bwd_workspace_size(const kda_params_t* p, size_t* bytes) {
+  Problem P{};
+  if (!bytes) return KDA_ERR_INVALID_ARG;
+  kda_status_t s = check_prefill(p, &P);
+  if (s != KDA_OK) return s;
+  *bytes = kda::bwd_workspace_bytes(P);
+  return KDA_OK;
+}
+
+kda_status_t kda_prefill_bwd(const kda_params_t* p, const void* q, const void* k, const void* v,
+                             const float* beta, const float* log_decay,
+                             const uint32_t* input_row_offsets, const uint32_t* slot_idx,
+                             const void* state_pool, const float* d_o, const float* d_state,
+                             float* dq, float* dk, float* dv, float* dbeta, float* dlog_decay,
+                             float* d_state0, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  Problem P{};
+  kda_status_t s = check_prefill(p, &P);
+  if (s != KDA_OK) return s;
+  if (p->num_seqs == 0) return KDA_OK;
+  if (!input_row_offsets || !slot_idx || !state_pool) return KDA_ERR_INVALID_ARG;
+  if (p->total_tokens > 0 && (!q || !k || !v || !beta || !log_decay || !d_o || !dq || !dk ||
+                              !dv || !dbeta || !dlog_decay))
+    return KDA_ERR_INVALID_ARG;
+  if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(state_pool, 4) ||
+      !aligned(beta, 4) || !aligned(log_decay, 4) || !aligned(input_row_offsets, 4) ||
+      !aligned(slot_idx, 4) || !aligned(d_o, 4) || !aligned(d_state, 4) || !aligned(dq, 4) ||
+      !aligned(dk, 4) || !aligned(dv, 4) || !aligned(dbeta, 4) || !aligned(dlog_decay, 4) ||
+      !aligned(d_state0, 4))
+    return KDA_ERR_INVALID_ARG;
+  const size_t need = kda::bwd_workspace_bytes(P);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
+  P.q = q; P.k = k; P.v = v; P.beta = beta; P.g = log_decay;
+  P.offsets = input_row_offsets; P.slot_idx = slot_idx;
+  P.pool = const_cast<void*>(state_pool);   // read only: the initial states
+  P.o = nullptr;
+  P.err = device_error_word();
+  if (!P.err) return KDA_ERR_CUDA;
+  return to_status(kda::launch_prefill_bwd(
+      P, workspace, d_o, d_state, dq, dk, dv, dbeta, dlog_decay, d_state0,
+      p->qkv_dtype == KDA_DTYPE_BF16, p->decay_kind == KDA_DECAY_PER_CHANNEL,
+      p->state_dtype == KDA_DTYPE_BF16, static_cast<cudaStream_t>(stream)));
 }
 
 kda_status_t kda_gdp_workspace_size(const kda_params_t* p, int32_t n_h, int32_t decode, size_t* bytes) {

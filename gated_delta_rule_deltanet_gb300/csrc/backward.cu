@@ -1,0 +1,635 @@
+// backward.cu -- the backward pass of the chunkwise prefill, on CUDA cores in fp32.
+//
+// The chunk form of the forward pass ("You Could Have Come Up With Kimi Delta Attention",
+// sec. 6: per chunk, with the incoming state S (stored d_k x d_v), K~ = k^ exp(G),
+// Q~ = q^ exp(G), K_end = k^ exp(G_last - G), gamma = exp(G_last),
+// L_im = sum_c k^_ic k^_mc exp(G_ic - G_mc) (m < i), M_im = sum_c q^_ic k^_mc exp(G_ic - G_mc)
+// (m <= i), T = (I + diag(beta) L)^-1)
+//
+//     Y = diag(beta) (V - K~ S),   E = T Y,   O = Q~ S + M E,   S' = diag(gamma) S + K_end^T E
+//
+// is differentiated by the chain rule, chunk by chunk.  With dE = M^T dO + K_end dS' and
+// dY = T^T dE:
+//
+//     dS  = Q~^T dO + diag(gamma) dS' - W^T dE          (W = T diag(beta) K~)
+//     dV  = diag(beta) dY
+//     dA  = -dY E^T (strictly lower),  dL = diag(beta) dA,   dM = dO E^T (lower)
+//     dQ~ = dO S^T,  dK~ = -diag(beta) dY S^T,  dK_end = E dS'^T,  dgamma = rowsum(dS' * S)
+//     dbeta_i = dY_i . (V - K~ S)_i + sum_m dA_im L_im
+//
+// and the pairwise products L and M, the decayed rows and gamma pass their gradients on to
+// q^, k^ and the cumulative log-decay G, whose reverse cumulative sum is the gradient of g.
+// The state recursion is the transpose of the forward chain, so it runs as a reverse scan over
+// each sequence's chunks; everything else is chunk-parallel:
+//
+//   local   the forward's chunk-local stage, also keeping T and K~
+//   scan    per (sequence, value head, value tile): forward over the chunks to record each
+//           chunk's incoming state and E, then backward carrying dS: dE, dV, dS per chunk
+//   vc      per (chunk, value head): the contractions over the value dimension
+//           (dQ~, dK~, dK_end, dA, dM, dgamma, the first term of dbeta)
+//   pair    per (chunk, key head), over the value heads of its group: the pairwise terms,
+//           dG and its reverse cumulative sum, dbeta, then the L2 normalisation's backward
+//           and the sum over the group (GQA) for dq and dk
+//
+// The additive write (KDA_FLAG_NO_DELTA) has no L and no K~ S term: T = I, W = 0, and their
+// gradient terms vanish.  The pairwise decay is evaluated per pair and channel, as in the
+// CUDA-core forward, so no factor overflows.
+#include "prefill_simt.cuh"
+
+namespace kda {
+
+struct BwdArgs {
+  const float* d_o;      // [T, HV, D]
+  const float* d_state;  // [num_slots, HV, D, D] or null: gradient w.r.t. the final states
+  float* dq;             // [T, HK, D]
+  float* dk;             // [T, HK, D]
+  float* dv;             // [T, HV, D]
+  float* dbeta;          // [T, HV]
+  float* dg;             // [T, HV] or [T, HV, D]
+  float* d_state0;       // [num_slots, HV, D, D] or null: gradient w.r.t. the initial states
+};
+
+struct BwdWorkspace {
+  SimtWorkspace loc;
+  float* Sck;   // [chunk][HV][D][D] state entering the chunk
+  float* dSck;  // [chunk][HV][D][D] gradient w.r.t. the state leaving the chunk
+  float* E;     // [chunk][HV][C][D] corrected values
+  float* dE;    // [chunk][HV][C][D]
+  float* dQt;   // [chunk][HV][C][D]
+  float* dKt;   // [chunk][HV][C][D]
+  float* dKe;   // [chunk][HV][C][D]
+  float* dA;    // [chunk][HV][C][C]
+  float* dM;    // [chunk][HV][C][C]
+  float* dgam;  // [chunk][HV][D]
+  float* dbr;   // [chunk][HV][C]
+};
+
+static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws) {
+  size_t off = 0;
+  PlanView pv;
+  off = plan_layout(P, base, off, &pv);
+  const size_t units = static_cast<size_t>(plan_max_chunks(P)) * P.HV;
+  const size_t C = P.chunk, D = P.D;
+  auto take = [&](size_t floats) -> float* {
+    float* p = base ? reinterpret_cast<float*>(base + off) : nullptr;
+    off += (floats * 4 + 255) & ~size_t(255);
+    return p;
+  };
+  BwdWorkspace w{};
+  w.loc.plan = pv;
+  w.loc.W = take(units * C * D);
+  w.loc.U = take(units * C * D);
+  w.loc.Qt = take(units * C * D);
+  w.loc.Kend = take(units * C * D);
+  w.loc.Aqk = take(units * C * C);
+  w.loc.gamma = take(units * D);
+  w.loc.T = take(units * C * C);
+  w.loc.Kt = take(units * C * D);
+  w.Sck = take(units * D * D);
+  w.dSck = take(units * D * D);
+  w.E = take(units * C * D);
+  w.dE = take(units * C * D);
+  w.dQt = take(units * C * D);
+  w.dKt = take(units * C * D);
+  w.dKe = take(units * C * D);
+  w.dA = take(units * C * C);
+  w.dM = take(units * C * C);
+  w.dgam = take(units * D);
+  w.dbr = take(units * C);
+  if (ws) *ws = w;
+  return off;
+}
+
+size_t bwd_workspace_bytes(const Problem& P) { return bwd_layout(P, nullptr, nullptr); }
+
+// ------------------------------------------------------------------------------- scan
+
+template <int D, int C, int BV>
+struct BwdScanSmem {
+  static constexpr size_t floats = D * BV + 3 * C * D + 3 * C * BV + 2 * C * C + D + C;
+  static constexpr size_t bytes = floats * sizeof(float);
+};
+
+template <int D, int C, int BV, bool SBF16>
+__global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace ws, BwdArgs A) {
+  constexpr int NT = 256;
+  extern __shared__ float smem[];
+  float* s_S = smem;              // [D][BV] state (forward) / its gradient (backward)
+  float* s_W = s_S + D * BV;      // [C][D]
+  float* s_Q = s_W + C * D;       // [C][D] Q~
+  float* s_K = s_Q + C * D;       // [C][D] K_end
+  float* s_X = s_K + C * D;       // [C][BV] U (forward) / dO (backward)
+  float* s_E = s_X + C * BV;      // [C][BV]
+  float* s_dE = s_E + C * BV;     // [C][BV]
+  float* s_M = s_dE + C * BV;     // [C][C] A_qk
+  float* s_T = s_M + C * C;       // [C][C]
+  float* s_g = s_T + C * C;       // [D] gamma
+  float* s_b = s_g + D;           // [C] beta
+
+  if (ws.loc.plan.info[1] == 0) return;
+  const int b = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
+  const int HV = P.HV;
+  const int tid = threadIdx.x;
+  const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D;
+  for (int idx = tid; idx < D * BV; idx += NT) {
+    const int c = idx / BV, j = idx % BV;
+    s_S[idx] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[sbase + c * D + v0 + j])
+                     : static_cast<const float*>(P.pool)[sbase + c * D + v0 + j];
+  }
+  const int first = ws.loc.plan.seq_chunk0[b], last = ws.loc.plan.seq_chunk0[b + 1];
+  // forward: record each chunk's incoming state and its corrected values E = U - W S
+  for (int cidx = first; cidx < last; ++cidx) {
+    const int64_t unit = static_cast<int64_t>(cidx) * HV + h;
+    __syncthreads();
+    for (int idx = tid; idx < C * D; idx += NT) {
+      s_W[idx] = ws.loc.W[unit * C * D + idx];
+      s_K[idx] = ws.loc.Kend[unit * C * D + idx];
+    }
+    for (int idx = tid; idx < C * BV; idx += NT)
+      s_X[idx] = ws.loc.U[unit * C * D + (idx / BV) * D + v0 + idx % BV];
+    for (int c = tid; c < D; c += NT) s_g[c] = ws.loc.gamma[unit * D + c];
+    for (int idx = tid; idx < D * BV; idx += NT)
+      ws.Sck[unit * D * D + (idx / BV) * D + v0 + idx % BV] = s_S[idx];
+    __syncthreads();
+    for (int idx = tid; idx < C * BV; idx += NT) {
+      const int i = idx / BV, j = idx % BV;
+      float acc = 0.f;
+      for (int c = 0; c < D; ++c) acc += s_W[i * D + c] * s_S[c * BV + j];
+      s_E[idx] = s_X[idx] - acc;
+      ws.E[unit * C * D + i * D + v0 + j] = s_E[idx];
+    }
+    __syncthreads();
+    for (int idx = tid; idx < D * BV; idx += NT) {
+      const int c = idx / BV, j = idx % BV;
+      float acc = s_g[c] * s_S[idx];
+      for (int i = 0; i < C; ++i) acc += s_K[i * D + c] * s_E[i * BV + j];
+      s_S[idx] = acc;
+    }
+  }
+  __syncthreads();
+  // backward: dS starts as the gradient w.r.t. the final state
+  for (int idx = tid; idx < D * BV; idx += NT)
+    s_S[idx] = A.d_state ? A.d_state[sbase + (idx / BV) * D + v0 + idx % BV] : 0.f;
+  for (int cidx = last - 1; cidx >= first; --cidx) {
+    const ChunkInfo ci = ws.loc.plan.chunks[cidx];
+    const int64_t unit = static_cast<int64_t>(cidx) * HV + h;
+    __syncthreads();
+    for (int idx = tid; idx < C * D; idx += NT) {
+      s_W[idx] = ws.loc.W[unit * C * D + idx];
+      s_Q[idx] = ws.loc.Qt[unit * C * D + idx];
+      s_K[idx] = ws.loc.Kend[unit * C * D + idx];
+    }
+    for (int idx = tid; idx < C * C; idx += NT) {
+      s_M[idx] = ws.loc.Aqk[unit * C * C + idx];
+      s_T[idx] = ws.loc.T[unit * C * C + idx];
+    }
+    for (int idx = tid; idx < C * BV; idx += NT) {
+      const int i = idx / BV, j = idx % BV;
+      s_X[idx] = i < ci.n ? A.d_o[((ci.t0 + i) * HV + h) * D + v0 + j] : 0.f;
+      s_E[idx] = ws.E[unit * C * D + i * D + v0 + j];
+    }
+    for (int c = tid; c < D; c += NT) s_g[c] = ws.loc.gamma[unit * D + c];
+    for (int i = tid; i < C; i += NT) s_b[i] = i < ci.n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
+    for (int idx = tid; idx < D * BV; idx += NT)
+      ws.dSck[unit * D * D + (idx / BV) * D + v0 + idx % BV] = s_S[idx];
+    __syncthreads();
+    // dE = A_qk^T dO + K_end dS'
+    for (int idx = tid; idx < C * BV; idx += NT) {
+      const int i = idx / BV, j = idx % BV;
+      float acc = 0.f;
+      for (int m = i; m < C; ++m) acc += s_M[m * C + i] * s_X[m * BV + j];
+      for (int c = 0; c < D; ++c) acc += s_K[i * D + c] * s_S[c * BV + j];
+      s_dE[idx] = acc;
+      ws.dE[unit * C * D + i * D + v0 + j] = acc;
+    }
+    __syncthreads();
+    // dV = diag(beta) T^T dE
+    for (int idx = tid; idx < C * BV; idx += NT) {
+      const int i = idx / BV, j = idx % BV;
+      if (i >= ci.n) continue;
+      float acc = 0.f;
+      for (int m = i; m < C; ++m) acc += s_T[m * C + i] * s_dE[m * BV + j];
+      A.dv[((ci.t0 + i) * HV + h) * D + v0 + j] = s_b[i] * acc;
+    }
+    // dS = diag(gamma) dS' + Q~^T dO - W^T dE (each thread updates its own entries)
+    for (int idx = tid; idx < D * BV; idx += NT) {
+      const int c = idx / BV, j = idx % BV;
+      float acc = s_g[c] * s_S[idx];
+      for (int i = 0; i < C; ++i) acc += s_Q[i * D + c] * s_X[i * BV + j] - s_W[i * D + c] * s_dE[i * BV + j];
+      s_S[idx] = acc;
+    }
+  }
+  __syncthreads();
+  if (A.d_state0)
+    for (int idx = tid; idx < D * BV; idx += NT)
+      A.d_state0[sbase + (idx / BV) * D + v0 + idx % BV] = s_S[idx];
+}
+
+// ------------------------------------------------------------------------------- vc
+
+template <int D, int C, int BV>
+struct BwdVcSmem {
+  static constexpr size_t floats = C * C + C * D + C + 2 * BV * D + 6 * C * BV + BV * C;
+  static constexpr size_t bytes = floats * sizeof(float);
+};
+
+template <int D, int C, int BV, bool QBF16>
+__global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws, BwdArgs A) {
+  constexpr int NT = 256;
+  constexpr int NE = C * D / NT;    // (row, channel) entries per thread
+  constexpr int NA = C * C / NT;    // (row, row) entries per thread
+  static_assert(NE >= 1 && NA >= 1 && C * D % NT == 0 && C * C % NT == 0, "entries must tile");
+  extern __shared__ float smem[];
+  float* s_T = smem;               // [C][C]
+  float* s_Kt = s_T + C * C;       // [C][D] K~
+  float* s_b = s_Kt + C * D;       // [C]
+  float* s_St = s_b + C;           // [BV][D] S tile, transposed
+  float* s_dSt = s_St + BV * D;    // [BV][D] dS' tile, transposed
+  float* s_V = s_dSt + BV * D;     // [C][BV]
+  float* s_E = s_V + C * BV;       // [C][BV]
+  float* s_dE = s_E + C * BV;      // [C][BV]
+  float* s_dO = s_dE + C * BV;     // [C][BV]
+  float* s_dY = s_dO + C * BV;     // [C][BV]
+  float* s_R = s_dY + C * BV;      // [C][BV] V - K~ S
+  float* s_Et = s_R + C * BV;      // [BV][C]
+
+  if (ws.loc.plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= ws.loc.plan.info[0]) return;
+  const ChunkInfo ci = ws.loc.plan.chunks[blockIdx.x];
+  const int h = blockIdx.y, HV = P.HV, tid = threadIdx.x;
+  const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
+  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
+  for (int idx = tid; idx < C * C; idx += NT) s_T[idx] = ws.loc.T[unit * C * C + idx];
+  for (int idx = tid; idx < C * D; idx += NT) s_Kt[idx] = ws.loc.Kt[unit * C * D + idx];
+  for (int i = tid; i < C; i += NT) s_b[i] = i < ci.n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
+
+  float aQ[NE], aK[NE], aE[NE], aA[NA], aM[NA];
+#pragma unroll
+  for (int r = 0; r < NE; ++r) aQ[r] = aK[r] = aE[r] = 0.f;
+#pragma unroll
+  for (int r = 0; r < NA; ++r) aA[r] = aM[r] = 0.f;
+  float gam_acc = 0.f, br_acc = 0.f;
+
+  for (int v0 = 0; v0 < D; v0 += BV) {
+    __syncthreads();
+    for (int idx = tid; idx < D * BV; idx += NT) {
+      const int c = idx / BV, j = idx % BV;
+      s_St[j * D + c] = ws.Sck[unit * D * D + c * D + v0 + j];
+      s_dSt[j * D + c] = ws.dSck[unit * D * D + c * D + v0 + j];
+    }
+    for (int idx = tid; idx < C * BV; idx += NT) {
+      const int i = idx / BV, j = idx % BV;
+      const bool live = i < ci.n;
+      s_V[idx] = live ? load_elem<QBF16>(P.v, (ci.t0 + i) * P.v_stride + static_cast<int64_t>(h) * D + v0 + j) : 0.f;
+      const float e = ws.E[unit * C * D + i * D + v0 + j];
+      s_E[idx] = e;
+      s_Et[j * C + i] = e;
+      s_dE[idx] = ws.dE[unit * C * D + i * D + v0 + j];
+      s_dO[idx] = live ? A.d_o[((ci.t0 + i) * HV + h) * D + v0 + j] : 0.f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < C * BV; idx += NT) {
+      const int i = idx / BV, j = idx % BV;
+      float y = 0.f;
+      for (int m = i; m < C; ++m) y += s_T[m * C + i] * s_dE[m * BV + j];
+      s_dY[idx] = y;
+      float ks = 0.f;
+      if (delta)
+        for (int c = 0; c < D; ++c) ks += s_Kt[i * D + c] * s_St[j * D + c];
+      s_R[idx] = s_V[idx] - ks;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < NE; ++r) {
+      const int u = tid + NT * r, i = u / D, c = u % D;
+      float q = aQ[r], k = aK[r], e = aE[r];
+      for (int j = 0; j < BV; ++j) {
+        const float s = s_St[j * D + c];
+        q += s_dO[i * BV + j] * s;
+        k += s_dY[i * BV + j] * s;
+        e += s_E[i * BV + j] * s_dSt[j * D + c];
+      }
+      aQ[r] = q; aK[r] = k; aE[r] = e;
+    }
+#pragma unroll
+    for (int r = 0; r < NA; ++r) {
+      const int u = tid + NT * r, i = u / C, m = u % C;
+      float a = aA[r], mm = aM[r];
+      for (int j = 0; j < BV; ++j) {
+        const float e = s_Et[j * C + m];
+        a += s_dY[i * BV + j] * e;
+        mm += s_dO[i * BV + j] * e;
+      }
+      aA[r] = a; aM[r] = mm;
+    }
+    if (tid < D)
+      for (int j = 0; j < BV; ++j) gam_acc += s_dSt[j * D + tid] * s_St[j * D + tid];
+    if (tid < C)
+      for (int j = 0; j < BV; ++j) br_acc += s_dY[tid * BV + j] * s_R[tid * BV + j];
+  }
+#pragma unroll
+  for (int r = 0; r < NE; ++r) {
+    const int u = tid + NT * r, i = u / D;
+    ws.dQt[unit * C * D + u] = aQ[r];
+    ws.dKt[unit * C * D + u] = delta ? -s_b[i] * aK[r] : 0.f;
+    ws.dKe[unit * C * D + u] = aE[r];
+  }
+#pragma unroll
+  for (int r = 0; r < NA; ++r) {
+    const int u = tid + NT * r, i = u / C, m = u % C;
+    ws.dA[unit * C * C + u] = (delta && m < i) ? -aA[r] : 0.f;
+    ws.dM[unit * C * C + u] = m <= i ? aM[r] : 0.f;
+  }
+  if (tid < D) ws.dgam[unit * D + tid] = gam_acc;
+  if (tid < C) ws.dbr[unit * C + tid] = br_acc;
+}
+
+// ------------------------------------------------------------------------------- pair
+
+template <int D, int C, bool PERCH>
+struct BwdPairSmem {
+  static constexpr int GW = PERCH ? D : 1;
+  static constexpr size_t floats = 3 * C * D + C * GW + 2 * C * C + 6 * C + 2 * D;
+  static constexpr size_t bytes = floats * sizeof(float);
+};
+
+template <int D, int C, bool QBF16, bool PERCH>
+__global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace ws, BwdArgs A) {
+  constexpr int NT = 256;
+  constexpr int NE = C * D / NT;
+  constexpr int GW = BwdPairSmem<D, C, PERCH>::GW;
+  extern __shared__ float smem[];
+  float* s_q = smem;               // [C][D] q^ = s q / |q| (scaled)
+  float* s_k = s_q + C * D;        // [C][D] k^ = k / |k|
+  float* s_dG = s_k + C * D;       // [C][D] gradient w.r.t. G, one value head at a time
+  float* s_G = s_dG + C * D;       // [C][GW] cumulative log-decay
+  float* s_dA = s_G + C * GW;      // [C][C]
+  float* s_dM = s_dA + C * C;      // [C][C]
+  float* s_b = s_dM + C * C;       // [C] beta
+  float* s_rq = s_b + C;           // [C] 1/|q| (1 without the norm)
+  float* s_rk = s_rq + C;          // [C]
+  float* s_db = s_rk + C;          // [C] pairwise part of dbeta
+  float* s_dotq = s_db + C;        // [C]
+  float* s_dotk = s_dotq + C;      // [C]
+  float* s_dGl = s_dotk + C;       // [D] gradient w.r.t. G_last
+  float* s_gam = s_dGl + D;        // [D]
+
+  if (ws.loc.plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= ws.loc.plan.info[0]) return;
+  const ChunkInfo ci = ws.loc.plan.chunks[blockIdx.x];
+  const int kh = blockIdx.y, HV = P.HV, ratio = HV / P.HK, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
+  const int n = ci.n;
+
+  for (int idx = tid; idx < C * D; idx += NT) {
+    const int i = idx / D, c = idx % D;
+    const bool live = i < n;
+    s_q[idx] = live ? load_elem<QBF16>(P.q, (ci.t0 + i) * P.q_stride + static_cast<int64_t>(kh) * D + c) : 0.f;
+    s_k[idx] = live ? load_elem<QBF16>(P.k, (ci.t0 + i) * P.k_stride + static_cast<int64_t>(kh) * D + c) : 0.f;
+  }
+  __syncthreads();
+  for (int i = warp; i < C; i += NT / 32) {
+    float sq = 0.f, sk = 0.f;
+    for (int c = lane; c < D; c += 32) {
+      sq += s_q[i * D + c] * s_q[i * D + c];
+      sk += s_k[i * D + c] * s_k[i * D + c];
+    }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    if (lane == 0) {
+      s_rq[i] = P.l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
+      s_rk[i] = P.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < C * D; idx += NT) {
+    const int i = idx / D;
+    s_q[idx] *= s_rq[i] * P.scale;
+    s_k[idx] *= s_rk[i];
+  }
+
+  float adq[NE], adk[NE];
+#pragma unroll
+  for (int r = 0; r < NE; ++r) adq[r] = adk[r] = 0.f;
+
+  for (int h = kh * ratio; h < (kh + 1) * ratio; ++h) {
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
+    __syncthreads();
+    // cumulative log-decay (padded rows add nothing), beta, dA, dM
+    if (PERCH) {
+      for (int c = tid; c < D; c += NT) {
+        float acc = 0.f;
+        for (int i = 0; i < C; ++i) {
+          acc += i < n ? P.g[((ci.t0 + i) * HV + h) * D + c] : 0.f;
+          s_G[i * GW + c] = acc;
+        }
+      }
+    } else if (tid == 0) {
+      float acc = 0.f;
+      for (int i = 0; i < C; ++i) {
+        acc += i < n ? P.g[(ci.t0 + i) * HV + h] : 0.f;
+        s_G[i] = acc;
+      }
+    }
+    for (int i = tid; i < C; i += NT) {
+      s_b[i] = i < n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
+      s_db[i] = 0.f;
+    }
+    for (int idx = tid; idx < C * C; idx += NT) {
+      s_dA[idx] = ws.dA[unit * C * C + idx];
+      s_dM[idx] = ws.dM[unit * C * C + idx];
+    }
+    for (int c = tid; c < D; c += NT) s_dGl[c] = 0.f;
+    __syncthreads();
+    for (int c = tid; c < D; c += NT) s_gam[c] = expf(s_G[(C - 1) * GW + (PERCH ? c : 0)]);
+#pragma unroll
+    for (int r = 0; r < NE; ++r) {
+      const int u = tid + NT * r, i = u / D, c = u % D;
+      const int gc = PERCH ? c : 0;
+      const float Gi = s_G[i * GW + gc];
+      const float Gl = s_G[(C - 1) * GW + gc];
+      // pairwise terms with i as the row: P1 from M, P2 from A (both over m <= i, m < i)
+      float p1 = 0.f, p2 = 0.f;
+      for (int m = 0; m <= i; ++m) {
+        const float km = s_k[m * D + c] * expf(Gi - s_G[m * GW + gc]);
+        p1 += s_dM[i * C + m] * km;
+        if (m < i) p2 += s_dA[i * C + m] * km;
+      }
+      // with i as the column: P3 from M (rows i' >= i) and L (rows i' > i)
+      float p3 = 0.f;
+      for (int m = i; m < C; ++m) {
+        const float dec = expf(s_G[m * GW + gc] - Gi);
+        p3 += s_dM[m * C + i] * s_q[m * D + c] * dec;
+        if (m > i && delta) p3 += s_b[m] * s_dA[m * C + i] * s_k[m * D + c] * dec;
+      }
+      const float qv = s_q[u], kv = s_k[u];
+      const float eG = expf(Gi), eL = expf(Gl - Gi);
+      const float dQt = ws.dQt[unit * C * D + u];
+      const float dKt = ws.dKt[unit * C * D + u];
+      const float dKe = ws.dKe[unit * C * D + u];
+      const float bi = s_b[i];
+      adq[r] += p1 + dQt * eG;
+      adk[r] += bi * p2 + p3 + dKt * eG + dKe * eL;
+      s_dG[u] = qv * p1 + kv * bi * p2 - kv * p3 + dQt * qv * eG + dKt * kv * eG - dKe * kv * eL;
+      // dbeta's pairwise part sum_m dA_im L_im = sum_c k^_ic p2_ic; gamma's path into G_last
+      float bl = kv * p2;
+      float gl = dKe * kv * eL;
+      if constexpr (D >= 32) {
+        bl = warp_sum(bl);
+        if (lane == 0) atomicAdd(&s_db[i], bl);
+      } else {
+        atomicAdd(&s_db[i], bl);
+      }
+      atomicAdd(&s_dGl[c], gl);
+    }
+    __syncthreads();
+    for (int c = tid; c < D; c += NT)
+      s_dG[(C - 1) * D + c] += s_dGl[c] + ws.dgam[unit * D + c] * s_gam[c];
+    __syncthreads();
+    // dg = reverse cumulative sum of dG over the chunk's rows
+    if (PERCH) {
+      for (int c = tid; c < D; c += NT) {
+        float acc = 0.f;
+        for (int i = C - 1; i >= 0; --i) {
+          acc += s_dG[i * D + c];
+          if (i < n) A.dg[((ci.t0 + i) * HV + h) * D + c] = acc;
+        }
+      }
+    } else {
+      for (int i = warp; i < C; i += NT / 32) {
+        float s = 0.f;
+        for (int c = lane; c < D; c += 32) s += s_dG[i * D + c];
+        s = warp_sum(s);
+        if (lane == 0) s_dotq[i] = s;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        float acc = 0.f;
+        for (int i = C - 1; i >= 0; --i) {
+          acc += s_dotq[i];
+          if (i < n) A.dg[(ci.t0 + i) * HV + h] = acc;
+        }
+      }
+    }
+    for (int i = tid; i < n; i += NT)
+      A.dbeta[(ci.t0 + i) * HV + h] = ws.dbr[unit * C + i] + (delta ? s_db[i] : 0.f);
+  }
+  __syncthreads();
+  // the L2 normalisation's backward: with u = x / |x|, dx = (du - u (u . du)) / |x|
+  for (int i = tid; i < C; i += NT) {
+    s_dotq[i] = 0.f;
+    s_dotk[i] = 0.f;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < NE; ++r) {
+    const int u = tid + NT * r, i = u / D;
+    float dq = s_q[u] * adq[r], dk = s_k[u] * adk[r];
+    if constexpr (D >= 32) {
+      dq = warp_sum(dq);
+      dk = warp_sum(dk);
+      if (lane == 0) {
+        atomicAdd(&s_dotq[i], dq);
+        atomicAdd(&s_dotk[i], dk);
+      }
+    } else {
+      atomicAdd(&s_dotq[i], dq);
+      atomicAdd(&s_dotk[i], dk);
+    }
+  }
+  __syncthreads();
+  const float inv_s = 1.f / P.scale;
+#pragma unroll
+  for (int r = 0; r < NE; ++r) {
+    const int u = tid + NT * r, i = u / D, c = u % D;
+    if (i >= n) continue;
+    float dq, dk;
+    if (P.l2norm) {
+      // q^ = s u_q with u_q = q / |q|: dq = s (dq^ - u_q (u_q . dq^)) / |q|
+      const float uq = s_q[u] * inv_s;
+      dq = P.scale * s_rq[i] * (adq[r] - uq * s_dotq[i] * inv_s);
+      dk = s_rk[i] * (adk[r] - s_k[u] * s_dotk[i]);
+    } else {
+      dq = P.scale * adq[r];
+      dk = adk[r];
+    }
+    const int64_t o = ((ci.t0 + i) * P.HK + kh) * D + c;
+    A.dq[o] = dq;
+    A.dk[o] = dk;
+  }
+}
+
+// ------------------------------------------------------------------------------- launch
+
+template <typename K>
+static cudaError_t set_smem(K kernel, size_t bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+template <int D, int C, bool QBF16, bool PERCH, bool SBF16>
+static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A,
+                                cudaStream_t st) {
+  constexpr int BV = D >= 32 ? 32 : D;
+  const int mc = plan_max_chunks(P);
+  cudaError_t e;
+  auto lk = simt_local_kernel<D, C, QBF16, PERCH>;
+  if ((e = set_smem(lk, SimtLocalSmem<D, C>::bytes)) != cudaSuccess) return e;
+  auto sk = bwd_scan_kernel<D, C, BV, SBF16>;
+  if ((e = set_smem(sk, BwdScanSmem<D, C, BV>::bytes)) != cudaSuccess) return e;
+  auto vk = bwd_vc_kernel<D, C, BV, QBF16>;
+  if ((e = set_smem(vk, BwdVcSmem<D, C, BV>::bytes)) != cudaSuccess) return e;
+  auto pk = bwd_pair_kernel<D, C, QBF16, PERCH>;
+  if ((e = set_smem(pk, BwdPairSmem<D, C, PERCH>::bytes)) != cudaSuccess) return e;
+  if (mc > 0) {
+    lk<<<dim3(mc, P.HV), 256, SimtLocalSmem<D, C>::bytes, st>>>(P, ws.loc);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  sk<<<dim3(P.num_seqs, P.HV, D / BV), 256, BwdScanSmem<D, C, BV>::bytes, st>>>(P, ws, A);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (mc > 0) {
+    vk<<<dim3(mc, P.HV), 256, BwdVcSmem<D, C, BV>::bytes, st>>>(P, ws, A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    pk<<<dim3(mc, P.HK), 256, BwdPairSmem<D, C, PERCH>::bytes, st>>>(P, ws, A);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <int D, int C>
+static cudaError_t launch_bwd_dc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A,
+                                 bool q, bool pc, bool sb, cudaStream_t st) {
+  if (q) {
+    if (pc) return sb ? launch_bwd_t<D, C, true, true, true>(P, ws, A, st)
+                      : launch_bwd_t<D, C, true, true, false>(P, ws, A, st);
+    return sb ? launch_bwd_t<D, C, true, false, true>(P, ws, A, st)
+              : launch_bwd_t<D, C, true, false, false>(P, ws, A, st);
+  }
+  if (pc) return sb ? launch_bwd_t<D, C, false, true, true>(P, ws, A, st)
+                    : launch_bwd_t<D, C, false, true, false>(P, ws, A, st);
+  return sb ? launch_bwd_t<D, C, false, false, true>(P, ws, A, st)
+            : launch_bwd_t<D, C, false, false, false>(P, ws, A, st);
+}
+
+template <int D>
+static cudaError_t launch_bwd_d(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A,
+                                bool q, bool pc, bool sb, cudaStream_t st) {
+  switch (P.chunk) {
+    case 16: return launch_bwd_dc<D, 16>(P, ws, A, q, pc, sb, st);
+    case 32: return launch_bwd_dc<D, 32>(P, ws, A, q, pc, sb, st);
+    default: return launch_bwd_dc<D, 64>(P, ws, A, q, pc, sb, st);
+  }
+}
+
+cudaError_t launch_prefill_bwd(const Problem& P, void* workspace, const float* d_o,
+                               const float* d_state, float* dq, float* dk, float* dv,
+                               float* dbeta, float* dg, float* d_state0, bool qbf16, bool perch,
+                               bool sbf16, cudaStream_t stream) {
+  BwdWorkspace ws;
+  bwd_layout(P, static_cast<char*>(workspace), &ws);
+  const BwdArgs A{d_o, d_state, dq, dk, dv, dbeta, dg, d_state0};
+  cudaError_t e = launch_plan(P, ws.loc.plan, stream);
+  if (e != cudaSuccess) return e;
+  if (P.D == 128) return launch_bwd_d<128>(P, ws, A, qbf16, perch, sbf16, stream);
+  return launch_bwd_d<16>(P, ws, A, qbf16, perch, sbf16, stream);
+}
+
+}  // namespace kda

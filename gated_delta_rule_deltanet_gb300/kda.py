@@ -188,6 +188,56 @@ def prefill_no_alloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
     return out
 
 
+
+def prefill_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
+                log_decay: torch.Tensor, input_row_offsets: torch.Tensor, slot_idx: torch.Tensor,
+                state_pool: torch.Tensor, d_o: torch.Tensor, d_state: Optional[torch.Tensor] = None,
+                *, chunk: int = 64, scale: float = 0.0, l2norm: bool = True,
+                delta_rule: bool = True, checked: bool = False,
+                d_state0: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None):
+    """Backward of `prefill` (kda_prefill_bwd).  `state_pool` holds the INITIAL states (the
+    pool before the forward call) and is only read; `d_o` [T, HV, D] and `d_state` (pool-shaped
+    fp32, or None for zero) are the loss's gradients w.r.t. o and the final states.
+    Returns (dq, dk [T, HK, D], dv [T, HV, D], dbeta [T, HV], dlog_decay (shape of log_decay),
+    d_state0 (pool-shaped fp32: the touched slots' gradients, zero elsewhere unless given))."""
+    dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, d_o)
+    p = _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
+                        scale, l2norm, checked, delta_rule=delta_rule)
+    T, HK, D = q.shape
+    HV = v.shape[1]
+    if d_o.dtype != torch.float32 or tuple(d_o.shape) != (T, HV, D) or not d_o.is_contiguous():
+        raise ValueError("d_o must be contiguous float32 [T, HV, D]")
+    pool_shape = tuple(state_pool.shape)
+    for name, t in (("d_state", d_state), ("d_state0", d_state0)):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != pool_shape
+                              or not t.is_contiguous()):
+            raise ValueError(f"{name} must be contiguous float32 shaped like state_pool")
+    if d_state is not None:
+        _check_cuda(d_state)
+    if d_state0 is None:
+        d_state0 = torch.zeros(pool_shape, dtype=torch.float32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    dq = torch.empty((T, HK, D), **f32)
+    dk = torch.empty((T, HK, D), **f32)
+    dv = torch.empty((T, HV, D), **f32)
+    dbeta = torch.empty((T, HV), **f32)
+    dlog_decay = torch.empty(tuple(log_decay.shape), **f32)
+    n = ctypes.c_size_t(0)
+    st = _lib.load().kda_prefill_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_prefill_bwd_workspace_size")
+    workspace = _workspace(int(n.value), workspace, dev)
+    st = _lib.load().kda_prefill_bwd(
+        ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_decay),
+        _ptr(input_row_offsets), _ptr(slot_idx), _ptr(state_pool), _ptr(d_o), _ptr(d_state),
+        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dlog_decay), _ptr(d_state0),
+        _ptr(workspace), ctypes.c_size_t(workspace.numel() * workspace.element_size()),
+        _stream_handle(stream, dev))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_prefill_bwd")
+    return dq, dk, dv, dbeta, dlog_decay, d_state0
+
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                 log_decay: torch.Tensor, slot_idx: torch.Tensor, state_pool: torch.Tensor, *,
                 scale: float = 0.0, l2norm: bool = True, delta_rule: bool = True,

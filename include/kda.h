@@ -187,6 +187,43 @@ kda_status_t kda_prefill_fwd(const kda_params_t *p, const void *q, const void *k
                              void *stream);
 
 /*
+ * Backward pass of kda_prefill_fwd: the gradients of a loss w.r.t. every input,
+ * given its gradients w.r.t. the outputs o and the final states.  The chunk form
+ * of the forward ("You Could Have Come Up With Kimi Delta Attention", sec. 6) is
+ * differentiated by the chain rule: the state gradient runs as a reverse scan
+ * over each sequence's chunks (the transpose of the forward's state recursion),
+ * the rest chunk-parallel; the L2 normalisation of q and k and the query scale
+ * are differentiated too.  fp32 arithmetic on CUDA cores for every dtype, head
+ * size and chunk the forward accepts ("From Attention to Learned Memory", sec. 3,
+ * gives the linear-attention backward in full; the delta rule's follows the same
+ * recurrence).
+ *
+ *   q, k, v, beta, log_decay, input_row_offsets, slot_idx: as kda_prefill_fwd
+ *   state_pool  [num_slots, HV, d_k, d_v], state_dtype, read only: the INITIAL
+ *               states (the pool as it was before the forward call)
+ *   d_o         [T, HV, d_v] fp32: dLoss/do
+ *   d_state     [num_slots, HV, d_k, d_v] fp32 or NULL (zero): dLoss/d(final
+ *               state) of the touched slots
+ *   dq, dk      [T, HK, d_k] fp32 (summed over the value heads of each key head)
+ *   dv          [T, HV, d_v] fp32          dbeta [T, HV] fp32
+ *   dlog_decay  the shape of log_decay, fp32
+ *   d_state0    [num_slots, HV, d_k, d_v] fp32 or NULL: dLoss/d(initial state),
+ *               written at the touched slots only; may alias d_state
+ *   workspace   >= kda_prefill_bwd_workspace_size bytes, 256-byte aligned
+ * All arrays 4-byte aligned.  KDA_FLAG_NO_DELTA differentiates the additive
+ * write; KDA_FLAG_CUDA_CORES and KDA_FLAG_COMPACT are ignored.  Device-side
+ * checks (offsets, slots) set the error word and skip the work, as in the forward.
+ */
+kda_status_t kda_prefill_bwd_workspace_size(const kda_params_t *p, size_t *bytes);
+kda_status_t kda_prefill_bwd(const kda_params_t *p, const void *q, const void *k, const void *v,
+                             const float *beta, const float *log_decay,
+                             const uint32_t *input_row_offsets, const uint32_t *slot_idx,
+                             const void *state_pool, const float *d_o, const float *d_state,
+                             float *dq, float *dk, float *dv, float *dbeta, float *dlog_decay,
+                             float *d_state0, void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
  * One recurrent decode step: one token for each of B = num_seqs sequences
  * ("You Could Have Come Up With Kimi Delta Attention", sec. 5, fused recurrent
  * kernel; Modular "gated_delta" module, the five per-token steps).

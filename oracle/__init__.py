@@ -14,7 +14,7 @@ Contents
   causal_linear_attention(...) brute force (Q K^T masked) V + Q S0 ("From Attention to Learned
                                Memory", sec. 1-2), the delta-free, decay-free special case
   backward(problem, ...)       reverse-mode differentiation of the recurrence in fp64
-                               (`oracle/backward.py`), pinned by finite differences
+                               (`oracle/bptt.py`), pinned by finite differences
 
 Parity status: every function here is pinned by `tests/test_oracle_pins.py`
 against closed forms, invariants the pages state, brute force and the worked
@@ -349,7 +349,7 @@ def backward(problem, d_o, d_state=None, *, delta_rule: bool = True, l2norm: boo
     """The backward oracle on a `workloads.Problem` (the pool holds the initial states):
     gradients of the loss whose gradients w.r.t. o and the final states are d_o and d_state.
     Returns dict(dq, dk, dv, dbeta, dg, d_state0), fp64."""
-    from .backward import backward_arrays
+    from .bptt import backward_arrays
     p = problem
     return backward_arrays(offsets=p.offsets, slot_idx=p.slot_idx, q=_widen(p.q, p.qkv_dtype),
                            k=_widen(p.k, p.qkv_dtype), v=_widen(p.v, p.qkv_dtype), beta=p.beta,

@@ -245,3 +245,30 @@ def test_gdp_rejects_bad_arguments_before_launch(lib):
                                    None) == _lib.KDA_ERR_INVALID_ARG            # no slots
     empty = good(num_seqs=0, total_tokens=0)
     assert lib.kda_gdp_prefill_fwd(ctypes.byref(empty), 2, *([None] * 10), 0, None) == _lib.KDA_OK
+
+
+def test_backward_rejects_bad_arguments_before_launch(lib):
+    """kda_prefill_bwd validates on the host like the forward: missing arrays, misalignment and
+    a short workspace are refused before anything is launched; the workspace covers the
+    recorded per-chunk states and their gradients."""
+    p = good(total_tokens=1024, num_seqs=2)
+    n = ctypes.c_size_t(0)
+    assert lib.kda_prefill_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == _lib.KDA_OK
+    chunks = 1024 // 64 + 2
+    assert n.value >= 2 * chunks * 8 * 128 * 128 * 4                 # states and gradients
+    assert lib.kda_prefill_bwd_workspace_size(ctypes.byref(good(chunk=48)),
+                                              ctypes.byref(n)) == _lib.KDA_ERR_UNSUPPORTED
+    # every call below must fail validation: none may reach a launch
+    a = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 2)
+    args = [a] * 17     # q k v beta g offsets slots pool d_o d_state dq dk dv dbeta dg d_state0 ws
+    none_do = list(args)
+    none_do[8] = None                                                 # d_o
+    assert lib.kda_prefill_bwd(ctypes.byref(p), *none_do, 1 << 40, None) == \
+        _lib.KDA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[10] = mis                                                     # dq misaligned
+    assert lib.kda_prefill_bwd(ctypes.byref(p), *bad, 1 << 40, None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_prefill_bwd(ctypes.byref(p), *args, 16, None) == _lib.KDA_ERR_WORKSPACE
+    empty = good(num_seqs=0, total_tokens=0)
+    assert lib.kda_prefill_bwd(ctypes.byref(empty), *([None] * 17), 0, None) == _lib.KDA_OK

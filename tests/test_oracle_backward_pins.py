@@ -1,4 +1,4 @@
-"""Pins for the backward oracle (`oracle/backward.py`): what the definition of a gradient fixes.
+"""Pins for the backward oracle (`oracle/bptt.py`): what the definition of a gradient fixes.
 
 The gradients are those of the scalar loss L = sum_t <d_o_t, o_t> + <d_S, S_T> through the
 forward recurrence, so central finite differences of that forward pass pin every one of them
@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle.backward import backward_arrays, backward_seq
+from oracle.bptt import backward_arrays, backward_seq
 
 
 def rng(seed):

@@ -386,6 +386,55 @@ def time_gdp_prefill(p, dev, steps, warmup):
     return start.elapsed_time(end) / steps
 
 
+def backward_algorithmic_bytes(p) -> float:
+    """Bytes the backward must move once: q, k, v, beta, g, d_o and the initial and final-state
+    gradients of the touched slots read, the initial states read, dq, dk, dv, dbeta, dg and
+    the initial-state gradients written (fp32 gradients)."""
+    T, HK, HV, D = p.total_tokens, p.num_k_heads, p.num_v_heads, p.d_k
+    es = 2 if p.qkv_dtype == "bf16" else 4
+    gw = D if p.decay_kind == "per_channel" else 1
+    states = p.num_seqs * HV * D * D
+    reads = T * (2 * HK * D + HV * D) * es + T * HV * 4 * (1 + gw) + T * HV * D * 4 \
+        + states * ((2 if p.state_dtype == "bf16" else 4) + 4)
+    writes = T * (2 * HK * D + HV * D) * 4 + T * HV * 4 * (1 + gw) + states * 4
+    return float(reads + writes)
+
+
+def time_prefill_bwd(p, dev, steps, warmup):
+    """The backward pass on resident inputs and output gradients (CUDA events)."""
+    import torch
+    import gated_delta_rule_deltanet_gb300 as kda
+    from workloads import torch_io
+    t = torch_io.prefill_inputs(p, dev)
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    d_o = torch.randn((p.total_tokens, p.num_v_heads, p.d_v), generator=gen).to(dev)
+    d_state = torch.randn(tuple(p.pool.shape), generator=gen).to(dev)
+    d_state0 = torch.zeros_like(d_state)
+    params = kda.kda._prefill_params(t["q"], t["k"], t["v"], t["beta"], t["log_decay"],
+                                     t["input_row_offsets"], t["slot_idx"], t["state_pool"],
+                                     p.chunk, p.scale, True, False)
+    import ctypes
+    n = ctypes.c_size_t(0)
+    kda.load().kda_prefill_bwd_workspace_size(ctypes.byref(params), ctypes.byref(n))
+    ws = torch.empty(max(int(n.value), 1), dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.prefill_bwd(t["q"], t["k"], t["v"], t["beta"], t["log_decay"],
+                        t["input_row_offsets"], t["slot_idx"], t["state_pool"], d_o, d_state,
+                        chunk=p.chunk, scale=p.scale, d_state0=d_state0, workspace=ws)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps, int(n.value)
+
+
 VERIFY_WINDOW = 4
 
 
@@ -545,6 +594,18 @@ def ours_arm(args, rank, world, local):
                                  "16 heads, d=128, bf16, scalar decay)",
                      "metric": "prefill tokens/s", "value": gval, "unit": "tokens/s",
                      "ms_per_step": gms, "virtual_tokens_per_s": gval * gp.n_h})
+
+    if not args.no_decode:
+        bms, bws = time_prefill_bwd(p, dev, 10, 3)
+        bval, _ = aggregate(float(p.total_tokens), bms / 1e3, world, dev)
+        bbytes = backward_algorithmic_bytes(p)
+        also.append({"workload": f"{p.name} backward (kda_prefill_bwd, fp32 CUDA cores)",
+                     "metric": "backward tokens/s", "value": bval, "unit": "tokens/s",
+                     "ms_per_step": bms, "workspace_bytes": bws,
+                     "path_roofline": {"algorithmic_bytes": bbytes,
+                                       "achieved_gbs": bbytes / (bms / 1e3) / 1e9,
+                                       "frac_hbm": bbytes / (bms / 1e3) / 1e9
+                                       / peaks["hbm_gbs"]}})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

@@ -104,32 +104,74 @@ size_t bwd_workspace_bytes(const Problem& P) { return bwd_layout(P, nullptr, nul
 
 // ------------------------------------------------------------------------------- scan
 
+// The outputs of an R x BV product spread over the 256 threads as row segments: thread t owns
+// row t / TPR and the JT consecutive columns from (t % TPR) * JT, so it keeps JT independent
+// accumulators and reads operand rows as 16-byte vectors where JT allows.
+template <int R, int BV>
+struct RowTile {
+  static constexpr int JT = R * BV / 256;
+  static constexpr int TPR = BV / JT;
+  static_assert(JT >= 1 && BV % JT == 0 && TPR * R == 256, "R x BV must tile 256 threads");
+};
+
+template <int N>
+__device__ __forceinline__ void ld_row(float (&x)[N], const float* p) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int e = 0; e < N; e += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + e);
+      x[e] = v.x; x[e + 1] = v.y; x[e + 2] = v.z; x[e + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) x[e] = p[e];
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void st_row(float* p, const float (&x)[N]) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int e = 0; e < N; e += 4)
+      *reinterpret_cast<float4*>(p + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) p[e] = x[e];
+  }
+}
+
 template <int D, int C, int BV>
 struct BwdScanSmem {
-  static constexpr size_t floats = D * BV + 3 * C * D + 3 * C * BV + 2 * C * C + D + C;
+  static constexpr int DP = D + 4;   // padded rows: threads on different rows hit different banks
+  static constexpr size_t floats = D * BV + 3 * C * DP + 3 * C * BV + 2 * C * C + D + C;
   static constexpr size_t bytes = floats * sizeof(float);
 };
 
 template <int D, int C, int BV, bool SBF16>
 __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace ws, BwdArgs A) {
   constexpr int NT = 256;
-  extern __shared__ float smem[];
-  float* s_S = smem;              // [D][BV] state (forward) / its gradient (backward)
-  float* s_W = s_S + D * BV;      // [C][D]
-  float* s_Q = s_W + C * D;       // [C][D] Q~
-  float* s_K = s_Q + C * D;       // [C][D] K_end
-  float* s_X = s_K + C * D;       // [C][BV] U (forward) / dO (backward)
-  float* s_E = s_X + C * BV;      // [C][BV]
-  float* s_dE = s_E + C * BV;     // [C][BV]
-  float* s_M = s_dE + C * BV;     // [C][C] A_qk
-  float* s_T = s_M + C * C;       // [C][C]
-  float* s_g = s_T + C * C;       // [D] gamma
-  float* s_b = s_g + D;           // [C] beta
+  constexpr int DP = BwdScanSmem<D, C, BV>::DP;
+  using TC = RowTile<C, BV>;        // the C x BV products
+  using TD = RowTile<D, BV>;        // the D x BV products
+  extern __shared__ __align__(16) float smem[];
+  float* s_S = smem;                // [D][BV] state (forward) / its gradient (backward)
+  float* s_W = s_S + D * BV;        // [C][DP]
+  float* s_Q = s_W + C * DP;        // [C][DP] Q~
+  float* s_K = s_Q + C * DP;        // [C][DP] K_end
+  float* s_X = s_K + C * DP;        // [C][BV] U (forward) / dO (backward)
+  float* s_E = s_X + C * BV;        // [C][BV]
+  float* s_dE = s_E + C * BV;       // [C][BV]
+  float* s_M = s_dE + C * BV;       // [C][C] A_qk
+  float* s_T = s_M + C * C;         // [C][C]
+  float* s_g = s_T + C * C;         // [D] gamma
+  float* s_b = s_g + D;             // [C] beta
 
   if (ws.loc.plan.info[1] == 0) return;
   const int b = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
   const int HV = P.HV;
   const int tid = threadIdx.x;
+  const int ri = tid / TC::TPR, rj = (tid % TC::TPR) * TC::JT;   // row segment of a C x BV product
+  const int dc = tid / TD::TPR, dj = (tid % TD::TPR) * TD::JT;   // row segment of a D x BV product
   const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D;
   for (int idx = tid; idx < D * BV; idx += NT) {
     const int c = idx / BV, j = idx % BV;
@@ -142,8 +184,9 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace w
     const int64_t unit = static_cast<int64_t>(cidx) * HV + h;
     __syncthreads();
     for (int idx = tid; idx < C * D; idx += NT) {
-      s_W[idx] = ws.loc.W[unit * C * D + idx];
-      s_K[idx] = ws.loc.Kend[unit * C * D + idx];
+      const int i = idx / D, c = idx % D;
+      s_W[i * DP + c] = ws.loc.W[unit * C * D + idx];
+      s_K[i * DP + c] = ws.loc.Kend[unit * C * D + idx];
     }
     for (int idx = tid; idx < C * BV; idx += NT)
       s_X[idx] = ws.loc.U[unit * C * D + (idx / BV) * D + v0 + idx % BV];
@@ -151,19 +194,40 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace w
     for (int idx = tid; idx < D * BV; idx += NT)
       ws.Sck[unit * D * D + (idx / BV) * D + v0 + idx % BV] = s_S[idx];
     __syncthreads();
-    for (int idx = tid; idx < C * BV; idx += NT) {
-      const int i = idx / BV, j = idx % BV;
-      float acc = 0.f;
-      for (int c = 0; c < D; ++c) acc += s_W[i * D + c] * s_S[c * BV + j];
-      s_E[idx] = s_X[idx] - acc;
-      ws.E[unit * C * D + i * D + v0 + j] = s_E[idx];
+    {
+      float acc[TC::JT] = {};
+      const float* w = s_W + ri * DP;
+#pragma unroll 4
+      for (int c = 0; c < D; ++c) {
+        float x[TC::JT];
+        ld_row(x, s_S + c * BV + rj);
+        const float wc = w[c];
+#pragma unroll
+        for (int e = 0; e < TC::JT; ++e) acc[e] += wc * x[e];
+      }
+      float u[TC::JT];
+      ld_row(u, s_X + ri * BV + rj);
+#pragma unroll
+      for (int e = 0; e < TC::JT; ++e) acc[e] = u[e] - acc[e];
+      st_row(s_E + ri * BV + rj, acc);
+      st_row(ws.E + unit * C * D + ri * D + v0 + rj, acc);
     }
     __syncthreads();
-    for (int idx = tid; idx < D * BV; idx += NT) {
-      const int c = idx / BV, j = idx % BV;
-      float acc = s_g[c] * s_S[idx];
-      for (int i = 0; i < C; ++i) acc += s_K[i * D + c] * s_E[i * BV + j];
-      s_S[idx] = acc;
+    {
+      float acc[TD::JT];
+      ld_row(acc, s_S + dc * BV + dj);
+      const float gm = s_g[dc];
+#pragma unroll
+      for (int e = 0; e < TD::JT; ++e) acc[e] *= gm;
+#pragma unroll 4
+      for (int i = 0; i < C; ++i) {
+        float x[TD::JT];
+        ld_row(x, s_E + i * BV + dj);
+        const float k = s_K[i * DP + dc];
+#pragma unroll
+        for (int e = 0; e < TD::JT; ++e) acc[e] += k * x[e];
+      }
+      st_row(s_S + dc * BV + dj, acc);
     }
   }
   __syncthreads();
@@ -175,9 +239,10 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace w
     const int64_t unit = static_cast<int64_t>(cidx) * HV + h;
     __syncthreads();
     for (int idx = tid; idx < C * D; idx += NT) {
-      s_W[idx] = ws.loc.W[unit * C * D + idx];
-      s_Q[idx] = ws.loc.Qt[unit * C * D + idx];
-      s_K[idx] = ws.loc.Kend[unit * C * D + idx];
+      const int i = idx / D, c = idx % D;
+      s_W[i * DP + c] = ws.loc.W[unit * C * D + idx];
+      s_Q[i * DP + c] = ws.loc.Qt[unit * C * D + idx];
+      s_K[i * DP + c] = ws.loc.Kend[unit * C * D + idx];
     }
     for (int idx = tid; idx < C * C; idx += NT) {
       s_M[idx] = ws.loc.Aqk[unit * C * C + idx];
@@ -193,30 +258,58 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace w
     for (int idx = tid; idx < D * BV; idx += NT)
       ws.dSck[unit * D * D + (idx / BV) * D + v0 + idx % BV] = s_S[idx];
     __syncthreads();
-    // dE = A_qk^T dO + K_end dS'
-    for (int idx = tid; idx < C * BV; idx += NT) {
-      const int i = idx / BV, j = idx % BV;
-      float acc = 0.f;
-      for (int m = i; m < C; ++m) acc += s_M[m * C + i] * s_X[m * BV + j];
-      for (int c = 0; c < D; ++c) acc += s_K[i * D + c] * s_S[c * BV + j];
-      s_dE[idx] = acc;
-      ws.dE[unit * C * D + i * D + v0 + j] = acc;
+    {                                           // dE = A_qk^T dO + K_end dS'
+      float acc[TC::JT] = {};
+      for (int m = ri; m < C; ++m) {
+        float x[TC::JT];
+        ld_row(x, s_X + m * BV + rj);
+        const float mm = s_M[m * C + ri];
+#pragma unroll
+        for (int e = 0; e < TC::JT; ++e) acc[e] += mm * x[e];
+      }
+      const float* k = s_K + ri * DP;
+#pragma unroll 4
+      for (int c = 0; c < D; ++c) {
+        float x[TC::JT];
+        ld_row(x, s_S + c * BV + rj);
+        const float kc = k[c];
+#pragma unroll
+        for (int e = 0; e < TC::JT; ++e) acc[e] += kc * x[e];
+      }
+      st_row(s_dE + ri * BV + rj, acc);
+      st_row(ws.dE + unit * C * D + ri * D + v0 + rj, acc);
     }
     __syncthreads();
-    // dV = diag(beta) T^T dE
-    for (int idx = tid; idx < C * BV; idx += NT) {
-      const int i = idx / BV, j = idx % BV;
-      if (i >= ci.n) continue;
-      float acc = 0.f;
-      for (int m = i; m < C; ++m) acc += s_T[m * C + i] * s_dE[m * BV + j];
-      A.dv[((ci.t0 + i) * HV + h) * D + v0 + j] = s_b[i] * acc;
+    if (ri < ci.n) {                            // dV = diag(beta) T^T dE
+      float acc[TC::JT] = {};
+      for (int m = ri; m < C; ++m) {
+        float x[TC::JT];
+        ld_row(x, s_dE + m * BV + rj);
+        const float t = s_T[m * C + ri];
+#pragma unroll
+        for (int e = 0; e < TC::JT; ++e) acc[e] += t * x[e];
+      }
+      const float bi = s_b[ri];
+#pragma unroll
+      for (int e = 0; e < TC::JT; ++e) acc[e] *= bi;
+      st_row(A.dv + ((ci.t0 + ri) * HV + h) * D + v0 + rj, acc);
     }
-    // dS = diag(gamma) dS' + Q~^T dO - W^T dE (each thread updates its own entries)
-    for (int idx = tid; idx < D * BV; idx += NT) {
-      const int c = idx / BV, j = idx % BV;
-      float acc = s_g[c] * s_S[idx];
-      for (int i = 0; i < C; ++i) acc += s_Q[i * D + c] * s_X[i * BV + j] - s_W[i * D + c] * s_dE[i * BV + j];
-      s_S[idx] = acc;
+    {                                           // dS = diag(gamma) dS' + Q~^T dO - W^T dE
+      float acc[TD::JT];
+      ld_row(acc, s_S + dc * BV + dj);
+      const float gm = s_g[dc];
+#pragma unroll
+      for (int e = 0; e < TD::JT; ++e) acc[e] *= gm;
+#pragma unroll 2
+      for (int i = 0; i < C; ++i) {
+        float x[TD::JT], y[TD::JT];
+        ld_row(x, s_X + i * BV + dj);
+        ld_row(y, s_dE + i * BV + dj);
+        const float q = s_Q[i * DP + dc], w = s_W[i * DP + dc];
+#pragma unroll
+        for (int e = 0; e < TD::JT; ++e) acc[e] += q * x[e] - w * y[e];
+      }
+      st_row(s_S + dc * BV + dj, acc);
     }
   }
   __syncthreads();
@@ -227,54 +320,66 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace w
 
 // ------------------------------------------------------------------------------- vc
 
+// Accumulators over the value dimension: thread t owns rows (t / 16) * C/16 + a (a < C/16)
+// and, of a C x D product, columns (t % 16) * D/16 + b (b < D/16), of a C x C product
+// columns (t % 16) * C/16 + b.
 template <int D, int C, int BV>
 struct BwdVcSmem {
-  static constexpr size_t floats = C * C + C * D + C + 2 * BV * D + 6 * C * BV + BV * C;
+  static constexpr int DP = D + 4, CP = C + 4;
+  static constexpr size_t floats = C * C + C * DP + C + D * BV + 2 * BV * DP + 6 * C * BV + BV * CP;
   static constexpr size_t bytes = floats * sizeof(float);
 };
 
 template <int D, int C, int BV, bool QBF16>
 __global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws, BwdArgs A) {
   constexpr int NT = 256;
-  constexpr int NE = C * D / NT;    // (row, channel) entries per thread
-  constexpr int NA = C * C / NT;    // (row, row) entries per thread
-  static_assert(NE >= 1 && NA >= 1 && C * D % NT == 0 && C * C % NT == 0, "entries must tile");
-  extern __shared__ float smem[];
-  float* s_T = smem;               // [C][C]
-  float* s_Kt = s_T + C * C;       // [C][D] K~
-  float* s_b = s_Kt + C * D;       // [C]
-  float* s_St = s_b + C;           // [BV][D] S tile, transposed
-  float* s_dSt = s_St + BV * D;    // [BV][D] dS' tile, transposed
-  float* s_V = s_dSt + BV * D;     // [C][BV]
-  float* s_E = s_V + C * BV;       // [C][BV]
-  float* s_dE = s_E + C * BV;      // [C][BV]
-  float* s_dO = s_dE + C * BV;     // [C][BV]
-  float* s_dY = s_dO + C * BV;     // [C][BV]
-  float* s_R = s_dY + C * BV;      // [C][BV] V - K~ S
-  float* s_Et = s_R + C * BV;      // [BV][C]
+  constexpr int DP = BwdVcSmem<D, C, BV>::DP, CP = BwdVcSmem<D, C, BV>::CP;
+  constexpr int IR = C / 16, JC = D / 16, JM = C / 16;
+  using TC = RowTile<C, BV>;
+  extern __shared__ __align__(16) float smem[];
+  float* s_T = smem;                // [C][C]
+  float* s_Kt = s_T + C * C;        // [C][DP] K~
+  float* s_b = s_Kt + C * DP;       // [C]
+  float* s_S = s_b + C;             // [D][BV] S tile
+  float* s_St = s_S + D * BV;       // [BV][DP] S tile, transposed
+  float* s_dSt = s_St + BV * DP;    // [BV][DP] dS' tile, transposed
+  float* s_V = s_dSt + BV * DP;     // [C][BV]
+  float* s_E = s_V + C * BV;        // [C][BV]
+  float* s_dE = s_E + C * BV;       // [C][BV]
+  float* s_dO = s_dE + C * BV;      // [C][BV]
+  float* s_dY = s_dO + C * BV;      // [C][BV]
+  float* s_R = s_dY + C * BV;       // [C][BV] V - K~ S
+  float* s_Et = s_R + C * BV;       // [BV][CP]
 
   if (ws.loc.plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= ws.loc.plan.info[0]) return;
   const ChunkInfo ci = ws.loc.plan.chunks[blockIdx.x];
   const int h = blockIdx.y, HV = P.HV, tid = threadIdx.x;
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
   const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
+  const int ri = tid / TC::TPR, rj = (tid % TC::TPR) * TC::JT;
+  const int r0 = (tid / 16) * IR, c0 = (tid % 16) * JC, m0 = (tid % 16) * JM;
   for (int idx = tid; idx < C * C; idx += NT) s_T[idx] = ws.loc.T[unit * C * C + idx];
-  for (int idx = tid; idx < C * D; idx += NT) s_Kt[idx] = ws.loc.Kt[unit * C * D + idx];
+  for (int idx = tid; idx < C * D; idx += NT) s_Kt[(idx / D) * DP + idx % D] = ws.loc.Kt[unit * C * D + idx];
   for (int i = tid; i < C; i += NT) s_b[i] = i < ci.n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
 
-  float aQ[NE], aK[NE], aE[NE], aA[NA], aM[NA];
+  float aQ[IR][JC], aK[IR][JC], aE[IR][JC], aA[IR][JM], aM[IR][JM];
 #pragma unroll
-  for (int r = 0; r < NE; ++r) aQ[r] = aK[r] = aE[r] = 0.f;
+  for (int a = 0; a < IR; ++a) {
 #pragma unroll
-  for (int r = 0; r < NA; ++r) aA[r] = aM[r] = 0.f;
+    for (int b = 0; b < JC; ++b) aQ[a][b] = aK[a][b] = aE[a][b] = 0.f;
+#pragma unroll
+    for (int b = 0; b < JM; ++b) aA[a][b] = aM[a][b] = 0.f;
+  }
   float gam_acc = 0.f, br_acc = 0.f;
 
   for (int v0 = 0; v0 < D; v0 += BV) {
     __syncthreads();
     for (int idx = tid; idx < D * BV; idx += NT) {
       const int c = idx / BV, j = idx % BV;
-      s_St[j * D + c] = ws.Sck[unit * D * D + c * D + v0 + j];
-      s_dSt[j * D + c] = ws.dSck[unit * D * D + c * D + v0 + j];
+      const float sv = ws.Sck[unit * D * D + c * D + v0 + j];
+      s_S[idx] = sv;
+      s_St[j * DP + c] = sv;
+      s_dSt[j * DP + c] = ws.dSck[unit * D * D + c * D + v0 + j];
     }
     for (int idx = tid; idx < C * BV; idx += NT) {
       const int i = idx / BV, j = idx % BV;
@@ -282,62 +387,93 @@ __global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws,
       s_V[idx] = live ? load_elem<QBF16>(P.v, (ci.t0 + i) * P.v_stride + static_cast<int64_t>(h) * D + v0 + j) : 0.f;
       const float e = ws.E[unit * C * D + i * D + v0 + j];
       s_E[idx] = e;
-      s_Et[j * C + i] = e;
+      s_Et[j * CP + i] = e;
       s_dE[idx] = ws.dE[unit * C * D + i * D + v0 + j];
       s_dO[idx] = live ? A.d_o[((ci.t0 + i) * HV + h) * D + v0 + j] : 0.f;
     }
     __syncthreads();
-    for (int idx = tid; idx < C * BV; idx += NT) {
-      const int i = idx / BV, j = idx % BV;
-      float y = 0.f;
-      for (int m = i; m < C; ++m) y += s_T[m * C + i] * s_dE[m * BV + j];
-      s_dY[idx] = y;
-      float ks = 0.f;
-      if (delta)
-        for (int c = 0; c < D; ++c) ks += s_Kt[i * D + c] * s_St[j * D + c];
-      s_R[idx] = s_V[idx] - ks;
+    {                                           // dY = T^T dE and R = V - K~ S
+      float y[TC::JT] = {}, ks[TC::JT] = {};
+      for (int m = ri; m < C; ++m) {
+        float x[TC::JT];
+        ld_row(x, s_dE + m * BV + rj);
+        const float t = s_T[m * C + ri];
+#pragma unroll
+        for (int e = 0; e < TC::JT; ++e) y[e] += t * x[e];
+      }
+      if (delta) {
+        const float* kt = s_Kt + ri * DP;
+#pragma unroll 4
+        for (int c = 0; c < D; ++c) {
+          float x[TC::JT];
+          ld_row(x, s_S + c * BV + rj);
+          const float kc = kt[c];
+#pragma unroll
+          for (int e = 0; e < TC::JT; ++e) ks[e] += kc * x[e];
+        }
+      }
+      float v[TC::JT];
+      ld_row(v, s_V + ri * BV + rj);
+#pragma unroll
+      for (int e = 0; e < TC::JT; ++e) v[e] -= ks[e];
+      st_row(s_dY + ri * BV + rj, y);
+      st_row(s_R + ri * BV + rj, v);
     }
     __syncthreads();
+#pragma unroll 2
+    for (int j = 0; j < BV; ++j) {
+      float xo[IR], xy[IR], xe[IR], st[JC], dst[JC], et[JM];
 #pragma unroll
-    for (int r = 0; r < NE; ++r) {
-      const int u = tid + NT * r, i = u / D, c = u % D;
-      float q = aQ[r], k = aK[r], e = aE[r];
-      for (int j = 0; j < BV; ++j) {
-        const float s = s_St[j * D + c];
-        q += s_dO[i * BV + j] * s;
-        k += s_dY[i * BV + j] * s;
-        e += s_E[i * BV + j] * s_dSt[j * D + c];
+      for (int a = 0; a < IR; ++a) {
+        xo[a] = s_dO[(r0 + a) * BV + j];
+        xy[a] = s_dY[(r0 + a) * BV + j];
+        xe[a] = s_E[(r0 + a) * BV + j];
       }
-      aQ[r] = q; aK[r] = k; aE[r] = e;
-    }
+      ld_row(st, s_St + j * DP + c0);
+      ld_row(dst, s_dSt + j * DP + c0);
+      ld_row(et, s_Et + j * CP + m0);
 #pragma unroll
-    for (int r = 0; r < NA; ++r) {
-      const int u = tid + NT * r, i = u / C, m = u % C;
-      float a = aA[r], mm = aM[r];
-      for (int j = 0; j < BV; ++j) {
-        const float e = s_Et[j * C + m];
-        a += s_dY[i * BV + j] * e;
-        mm += s_dO[i * BV + j] * e;
+      for (int a = 0; a < IR; ++a) {
+#pragma unroll
+        for (int b = 0; b < JC; ++b) {
+          aQ[a][b] += xo[a] * st[b];
+          aK[a][b] += xy[a] * st[b];
+          aE[a][b] += xe[a] * dst[b];
+        }
+#pragma unroll
+        for (int b = 0; b < JM; ++b) {
+          aA[a][b] += xy[a] * et[b];
+          aM[a][b] += xo[a] * et[b];
+        }
       }
-      aA[r] = a; aM[r] = mm;
     }
     if (tid < D)
-      for (int j = 0; j < BV; ++j) gam_acc += s_dSt[j * D + tid] * s_St[j * D + tid];
+      for (int j = 0; j < BV; ++j) gam_acc += s_dSt[j * DP + tid] * s_St[j * DP + tid];
     if (tid < C)
-      for (int j = 0; j < BV; ++j) br_acc += s_dY[tid * BV + j] * s_R[tid * BV + j];
+      for (int j = 0; j < BV; ++j) {
+        const int jj = (j + tid) % BV;          // rotated start: rows of one warp hit different banks
+        br_acc += s_dY[tid * BV + jj] * s_R[tid * BV + jj];
+      }
   }
 #pragma unroll
-  for (int r = 0; r < NE; ++r) {
-    const int u = tid + NT * r, i = u / D;
-    ws.dQt[unit * C * D + u] = aQ[r];
-    ws.dKt[unit * C * D + u] = delta ? -s_b[i] * aK[r] : 0.f;
-    ws.dKe[unit * C * D + u] = aE[r];
-  }
+  for (int a = 0; a < IR; ++a) {
+    const int i = r0 + a;
+    const float nb = delta ? -s_b[i] : 0.f;
+    float k[JC];
 #pragma unroll
-  for (int r = 0; r < NA; ++r) {
-    const int u = tid + NT * r, i = u / C, m = u % C;
-    ws.dA[unit * C * C + u] = (delta && m < i) ? -aA[r] : 0.f;
-    ws.dM[unit * C * C + u] = m <= i ? aM[r] : 0.f;
+    for (int b = 0; b < JC; ++b) k[b] = nb * aK[a][b];
+    st_row(ws.dQt + unit * C * D + i * D + c0, aQ[a]);
+    st_row(ws.dKt + unit * C * D + i * D + c0, k);
+    st_row(ws.dKe + unit * C * D + i * D + c0, aE[a]);
+    float da[JM], dm[JM];
+#pragma unroll
+    for (int b = 0; b < JM; ++b) {
+      const int m = m0 + b;
+      da[b] = (delta && m < i) ? -aA[a][b] : 0.f;
+      dm[b] = m <= i ? aM[a][b] : 0.f;
+    }
+    st_row(ws.dA + unit * C * C + i * C + m0, da);
+    st_row(ws.dM + unit * C * C + i * C + m0, dm);
   }
   if (tid < D) ws.dgam[unit * D + tid] = gam_acc;
   if (tid < C) ws.dbr[unit * C + tid] = br_acc;
@@ -348,7 +484,7 @@ __global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws,
 template <int D, int C, bool PERCH>
 struct BwdPairSmem {
   static constexpr int GW = PERCH ? D : 1;
-  static constexpr size_t floats = 3 * C * D + C * GW + 2 * C * C + 6 * C + 2 * D;
+  static constexpr size_t floats = 3 * C * D + C * GW + 2 * C * C + 6 * C + 2 * D + (PERCH ? 0 : C * C);
   static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -372,6 +508,7 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
   float* s_dotk = s_dotq + C;      // [C]
   float* s_dGl = s_dotk + C;       // [D] gradient w.r.t. G_last
   float* s_gam = s_dGl + D;        // [D]
+  float* s_dec = s_gam + D;        // [C][C] exp(G_i - G_m), m <= i (scalar decay only)
 
   if (ws.loc.plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= ws.loc.plan.info[0]) return;
   const ChunkInfo ci = ws.loc.plan.chunks[blockIdx.x];
@@ -441,6 +578,13 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
     for (int c = tid; c < D; c += NT) s_dGl[c] = 0.f;
     __syncthreads();
     for (int c = tid; c < D; c += NT) s_gam[c] = expf(s_G[(C - 1) * GW + (PERCH ? c : 0)]);
+    if constexpr (!PERCH) {
+      for (int idx = tid; idx < C * C; idx += NT) {
+        const int i = idx / C, m = idx % C;
+        s_dec[idx] = m <= i ? expf(s_G[i] - s_G[m]) : 0.f;
+      }
+      __syncthreads();
+    }
 #pragma unroll
     for (int r = 0; r < NE; ++r) {
       const int u = tid + NT * r, i = u / D, c = u % D;
@@ -450,14 +594,14 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
       // pairwise terms with i as the row: P1 from M, P2 from A (both over m <= i, m < i)
       float p1 = 0.f, p2 = 0.f;
       for (int m = 0; m <= i; ++m) {
-        const float km = s_k[m * D + c] * expf(Gi - s_G[m * GW + gc]);
+        const float km = s_k[m * D + c] * (PERCH ? expf(Gi - s_G[m * GW + gc]) : s_dec[i * C + m]);
         p1 += s_dM[i * C + m] * km;
         if (m < i) p2 += s_dA[i * C + m] * km;
       }
       // with i as the column: P3 from M (rows i' >= i) and L (rows i' > i)
       float p3 = 0.f;
       for (int m = i; m < C; ++m) {
-        const float dec = expf(s_G[m * GW + gc] - Gi);
+        const float dec = PERCH ? expf(s_G[m * GW + gc] - Gi) : s_dec[m * C + i];
         p3 += s_dM[m * C + i] * s_q[m * D + c] * dec;
         if (m > i && delta) p3 += s_b[m] * s_dA[m * C + i] * s_k[m * D + c] * dec;
       }

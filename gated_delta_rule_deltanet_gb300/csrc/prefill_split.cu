@@ -205,7 +205,9 @@ __device__ __forceinline__ void front_issue_loads(const Problem& P, unsigned cha
 
 // One CTA per (chunk, value head): everything of the chunk that does not depend on the
 // state, written to the chunk's record.
-template <bool PERCH>
+// DELTA = false is the additive write (no delta rule): A_kk = 0 makes T = I and K~ = 0
+// drops W = TB K~; a template parameter, so that the delta rule's code carries no test of it
+template <bool PERCH, bool DELTA>
 __global__ void __launch_bounds__(tcs::NT, 2)
     tc_front_kernel(Problem P, PlanView plan, unsigned char* records,
                     const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -234,8 +236,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
   const int kh = h / (HV / P.HK);
   const int n = ci.n;
   const int64_t t0 = ci.t0;
-  // additive write (no delta rule): A_kk = 0 makes T = I and K~ = 0 drops W = TB K~
-  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
+  constexpr bool delta = DELTA;
   unsigned char* rec = records + (static_cast<int64_t>(gc) * HV + h) * static_cast<int64_t>(REC_BYTES);
 
   float* sGs = reinterpret_cast<float*>(smem + M::SMALL + O_GS);
@@ -1385,10 +1386,10 @@ static bool encode_g_map(CUtensorMap* m, const Problem& P) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool PERCH>
+template <bool PERCH, bool DELTA>
 static cudaError_t launch_front_t(const Problem& P, const PlanView& plan, unsigned char* recs,
                                   cudaStream_t st) {
-  auto k = tc_front_kernel<PERCH>;
+  auto k = tc_front_kernel<PERCH, DELTA>;
   constexpr uint32_t bytes = tcs::FrontMap<PERCH>::BYTES + 1024;
   alignas(64) CUtensorMap tmq, tmk, tmg;
   memset(&tmg, 0, sizeof(tmg));
@@ -1422,7 +1423,11 @@ cudaError_t launch_prefill_split(const Problem& P, void* workspace, bool perch, 
   cudaError_t e = launch_plan(P, plan, stream);
   if (e != cudaSuccess) return e;
   st.mark(1, stream);
-  e = perch ? launch_front_t<true>(P, plan, recs, stream) : launch_front_t<false>(P, plan, recs, stream);
+  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
+  e = perch ? (delta ? launch_front_t<true, true>(P, plan, recs, stream)
+                     : launch_front_t<true, false>(P, plan, recs, stream))
+            : (delta ? launch_front_t<false, true>(P, plan, recs, stream)
+                     : launch_front_t<false, false>(P, plan, recs, stream));
   if (e != cudaSuccess) return e;
   st.mark(2, stream);
   e = sbf16 ? launch_chain_t<true>(P, plan, recs, stream) : launch_chain_t<false>(P, plan, recs, stream);

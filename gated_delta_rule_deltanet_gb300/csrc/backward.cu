@@ -35,6 +35,7 @@
 // gradient terms vanish.  The pairwise decay is evaluated per pair and channel, as in the
 // CUDA-core forward, so no factor overflows.
 #include "prefill_simt.cuh"
+#include "tc_utils.cuh"
 
 namespace kda {
 
@@ -140,30 +141,40 @@ __device__ __forceinline__ void st_row(float* p, const float (&x)[N]) {
   }
 }
 
+// A C x D fp32 matrix of the workspace into a shared buffer with rows of DP floats, as
+// 16-byte asynchronous copies (committed as one group by the caller).
+template <int C, int D, int DP>
+__device__ __forceinline__ void mat_async(float* dst, const float* src, int tid) {
+  for (int u = tid; u < C * D / 4; u += 256) {
+    const int i = u / (D / 4), p4 = 4 * (u % (D / 4));
+    tc::cp_async16(tc::smem_u32(dst + i * DP + p4), src + i * D + p4, 16);
+  }
+}
+
+// Two chunk matrices in shared memory at a time (W and K_end going forward; K_end, then Q~ and
+// W going back), the next one copied in while the current products run, and A_qk / T read
+// through the L1 cache: 109 KB per CTA, two CTAs per SM.
 template <int D, int C, int BV>
 struct BwdScanSmem {
   static constexpr int DP = D + 4;   // padded rows: threads on different rows hit different banks
-  static constexpr size_t floats = D * BV + 3 * C * DP + 3 * C * BV + 2 * C * C + D + C;
+  static constexpr size_t floats = D * BV + 2 * C * DP + 3 * C * BV + D + C;
   static constexpr size_t bytes = floats * sizeof(float);
 };
 
 template <int D, int C, int BV, bool SBF16>
-__global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace ws, BwdArgs A) {
+__global__ void __launch_bounds__(256, 2) bwd_scan_kernel(Problem P, BwdWorkspace ws, BwdArgs A) {
   constexpr int NT = 256;
   constexpr int DP = BwdScanSmem<D, C, BV>::DP;
   using TC = RowTile<C, BV>;        // the C x BV products
   using TD = RowTile<D, BV>;        // the D x BV products
   extern __shared__ __align__(16) float smem[];
   float* s_S = smem;                // [D][BV] state (forward) / its gradient (backward)
-  float* s_W = s_S + D * BV;        // [C][DP]
-  float* s_Q = s_W + C * DP;        // [C][DP] Q~
-  float* s_K = s_Q + C * DP;        // [C][DP] K_end
-  float* s_X = s_K + C * DP;        // [C][BV] U (forward) / dO (backward)
+  float* s_A = s_S + D * BV;        // [C][DP] W (forward) / Q~ (backward)
+  float* s_B = s_A + C * DP;        // [C][DP] K_end, then W (backward)
+  float* s_X = s_B + C * DP;        // [C][BV] U (forward) / dO (backward)
   float* s_E = s_X + C * BV;        // [C][BV]
   float* s_dE = s_E + C * BV;       // [C][BV]
-  float* s_M = s_dE + C * BV;       // [C][C] A_qk
-  float* s_T = s_M + C * C;         // [C][C]
-  float* s_g = s_T + C * C;         // [D] gamma
+  float* s_g = s_dE + C * BV;       // [D] gamma
   float* s_b = s_g + D;             // [C] beta
 
   if (ws.loc.plan.info[1] == 0) return;
@@ -179,24 +190,25 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace w
                      : static_cast<const float*>(P.pool)[sbase + c * D + v0 + j];
   }
   const int first = ws.loc.plan.seq_chunk0[b], last = ws.loc.plan.seq_chunk0[b + 1];
+  auto cunit = [&](int cidx) { return static_cast<int64_t>(cidx) * HV + h; };
   // forward: record each chunk's incoming state and its corrected values E = U - W S
+  if (first < last) {
+    mat_async<C, D, DP>(s_A, ws.loc.W + cunit(first) * C * D, tid);
+    mat_async<C, D, DP>(s_B, ws.loc.Kend + cunit(first) * C * D, tid);
+    tc::cp_async_commit();
+  }
   for (int cidx = first; cidx < last; ++cidx) {
-    const int64_t unit = static_cast<int64_t>(cidx) * HV + h;
-    __syncthreads();
-    for (int idx = tid; idx < C * D; idx += NT) {
-      const int i = idx / D, c = idx % D;
-      s_W[i * DP + c] = ws.loc.W[unit * C * D + idx];
-      s_K[i * DP + c] = ws.loc.Kend[unit * C * D + idx];
-    }
+    const int64_t unit = cunit(cidx);
     for (int idx = tid; idx < C * BV; idx += NT)
       s_X[idx] = ws.loc.U[unit * C * D + (idx / BV) * D + v0 + idx % BV];
     for (int c = tid; c < D; c += NT) s_g[c] = ws.loc.gamma[unit * D + c];
     for (int idx = tid; idx < D * BV; idx += NT)
       ws.Sck[unit * D * D + (idx / BV) * D + v0 + idx % BV] = s_S[idx];
+    tc::cp_async_wait_all();
     __syncthreads();
     {
       float acc[TC::JT] = {};
-      const float* w = s_W + ri * DP;
+      const float* w = s_A + ri * DP;
 #pragma unroll 4
       for (int c = 0; c < D; ++c) {
         float x[TC::JT];
@@ -213,6 +225,10 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace w
       st_row(ws.E + unit * C * D + ri * D + v0 + rj, acc);
     }
     __syncthreads();
+    if (cidx + 1 < last) {                      // W of the next chunk while the state updates
+      mat_async<C, D, DP>(s_A, ws.loc.W + cunit(cidx + 1) * C * D, tid);
+      tc::cp_async_commit();
+    }
     {
       float acc[TD::JT];
       ld_row(acc, s_S + dc * BV + dj);
@@ -223,51 +239,51 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace w
       for (int i = 0; i < C; ++i) {
         float x[TD::JT];
         ld_row(x, s_E + i * BV + dj);
-        const float k = s_K[i * DP + dc];
+        const float k = s_B[i * DP + dc];
 #pragma unroll
         for (int e = 0; e < TD::JT; ++e) acc[e] += k * x[e];
       }
       st_row(s_S + dc * BV + dj, acc);
     }
+    __syncthreads();
+    if (cidx + 1 < last) {
+      mat_async<C, D, DP>(s_B, ws.loc.Kend + cunit(cidx + 1) * C * D, tid);
+      tc::cp_async_commit();
+    }
   }
-  __syncthreads();
   // backward: dS starts as the gradient w.r.t. the final state
   for (int idx = tid; idx < D * BV; idx += NT)
     s_S[idx] = A.d_state ? A.d_state[sbase + (idx / BV) * D + v0 + idx % BV] : 0.f;
+  if (first < last) {
+    mat_async<C, D, DP>(s_B, ws.loc.Kend + cunit(last - 1) * C * D, tid);
+    mat_async<C, D, DP>(s_A, ws.loc.Qt + cunit(last - 1) * C * D, tid);
+    tc::cp_async_commit();
+  }
   for (int cidx = last - 1; cidx >= first; --cidx) {
     const ChunkInfo ci = ws.loc.plan.chunks[cidx];
-    const int64_t unit = static_cast<int64_t>(cidx) * HV + h;
-    __syncthreads();
-    for (int idx = tid; idx < C * D; idx += NT) {
-      const int i = idx / D, c = idx % D;
-      s_W[i * DP + c] = ws.loc.W[unit * C * D + idx];
-      s_Q[i * DP + c] = ws.loc.Qt[unit * C * D + idx];
-      s_K[i * DP + c] = ws.loc.Kend[unit * C * D + idx];
-    }
-    for (int idx = tid; idx < C * C; idx += NT) {
-      s_M[idx] = ws.loc.Aqk[unit * C * C + idx];
-      s_T[idx] = ws.loc.T[unit * C * C + idx];
-    }
+    const int64_t unit = cunit(cidx);
+    const float* gM = ws.loc.Aqk + unit * C * C;
+    const float* gT = ws.loc.T + unit * C * C;
     for (int idx = tid; idx < C * BV; idx += NT) {
       const int i = idx / BV, j = idx % BV;
       s_X[idx] = i < ci.n ? A.d_o[((ci.t0 + i) * HV + h) * D + v0 + j] : 0.f;
-      s_E[idx] = ws.E[unit * C * D + i * D + v0 + j];
     }
     for (int c = tid; c < D; c += NT) s_g[c] = ws.loc.gamma[unit * D + c];
     for (int i = tid; i < C; i += NT) s_b[i] = i < ci.n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
     for (int idx = tid; idx < D * BV; idx += NT)
       ws.dSck[unit * D * D + (idx / BV) * D + v0 + idx % BV] = s_S[idx];
+    tc::cp_async_wait_all();
     __syncthreads();
     {                                           // dE = A_qk^T dO + K_end dS'
       float acc[TC::JT] = {};
       for (int m = ri; m < C; ++m) {
         float x[TC::JT];
         ld_row(x, s_X + m * BV + rj);
-        const float mm = s_M[m * C + ri];
+        const float mm = __ldg(gM + m * C + ri);
 #pragma unroll
         for (int e = 0; e < TC::JT; ++e) acc[e] += mm * x[e];
       }
-      const float* k = s_K + ri * DP;
+      const float* k = s_B + ri * DP;
 #pragma unroll 4
       for (int c = 0; c < D; ++c) {
         float x[TC::JT];
@@ -280,12 +296,14 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace w
       st_row(ws.dE + unit * C * D + ri * D + v0 + rj, acc);
     }
     __syncthreads();
+    mat_async<C, D, DP>(s_B, ws.loc.W + unit * C * D, tid);   // K_end is done with
+    tc::cp_async_commit();
     if (ri < ci.n) {                            // dV = diag(beta) T^T dE
       float acc[TC::JT] = {};
       for (int m = ri; m < C; ++m) {
         float x[TC::JT];
         ld_row(x, s_dE + m * BV + rj);
-        const float t = s_T[m * C + ri];
+        const float t = __ldg(gT + m * C + ri);
 #pragma unroll
         for (int e = 0; e < TC::JT; ++e) acc[e] += t * x[e];
       }
@@ -294,24 +312,44 @@ __global__ void __launch_bounds__(256) bwd_scan_kernel(Problem P, BwdWorkspace w
       for (int e = 0; e < TC::JT; ++e) acc[e] *= bi;
       st_row(A.dv + ((ci.t0 + ri) * HV + h) * D + v0 + rj, acc);
     }
-    {                                           // dS = diag(gamma) dS' + Q~^T dO - W^T dE
-      float acc[TD::JT];
-      ld_row(acc, s_S + dc * BV + dj);
+    // dS = diag(gamma) dS' + Q~^T dO - W^T dE: the Q~ part while W arrives
+    float acc[TD::JT];
+    ld_row(acc, s_S + dc * BV + dj);
+    {
       const float gm = s_g[dc];
 #pragma unroll
       for (int e = 0; e < TD::JT; ++e) acc[e] *= gm;
-#pragma unroll 2
+#pragma unroll 4
       for (int i = 0; i < C; ++i) {
-        float x[TD::JT], y[TD::JT];
+        float x[TD::JT];
         ld_row(x, s_X + i * BV + dj);
-        ld_row(y, s_dE + i * BV + dj);
-        const float q = s_Q[i * DP + dc], w = s_W[i * DP + dc];
+        const float q = s_A[i * DP + dc];
 #pragma unroll
-        for (int e = 0; e < TD::JT; ++e) acc[e] += q * x[e] - w * y[e];
+        for (int e = 0; e < TD::JT; ++e) acc[e] += q * x[e];
       }
-      st_row(s_S + dc * BV + dj, acc);
+    }
+    tc::cp_async_wait_all();
+    __syncthreads();                            // W is in; Q~ is no longer read
+    if (cidx - 1 >= first) {
+      mat_async<C, D, DP>(s_A, ws.loc.Qt + cunit(cidx - 1) * C * D, tid);
+      tc::cp_async_commit();
+    }
+#pragma unroll 4
+    for (int i = 0; i < C; ++i) {
+      float y[TD::JT];
+      ld_row(y, s_dE + i * BV + dj);
+      const float w = s_B[i * DP + dc];
+#pragma unroll
+      for (int e = 0; e < TD::JT; ++e) acc[e] -= w * y[e];
+    }
+    st_row(s_S + dc * BV + dj, acc);
+    __syncthreads();                            // W is no longer read
+    if (cidx - 1 >= first) {
+      mat_async<C, D, DP>(s_B, ws.loc.Kend + cunit(cidx - 1) * C * D, tid);
+      tc::cp_async_commit();
     }
   }
+  tc::cp_async_wait_all();
   __syncthreads();
   if (A.d_state0)
     for (int idx = tid; idx < D * BV; idx += NT)
@@ -481,26 +519,39 @@ __global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws,
 
 // ------------------------------------------------------------------------------- pair
 
+// Thread t owns the entries (r0 + a, c0 + b) of every C x D quantity, r0 = (t / 16) * C/16,
+// c0 = (t % 16) * D/16 (a < C/16, b < D/16): a row group is one half-warp.  The pairwise
+// products are then small matrix products, P1 = (dM o X) k^, P2 = (dA o X) k^,
+// P3 = (dM o X)^T q^ + (diag(beta) dA o X)^T k^ with X the pairwise decay, which for scalar
+// decay is folded into dM and dA once per chunk.
 template <int D, int C, bool PERCH>
 struct BwdPairSmem {
   static constexpr int GW = PERCH ? D : 1;
-  static constexpr size_t floats = 3 * C * D + C * GW + 2 * C * C + 6 * C + 2 * D + (PERCH ? 0 : C * C);
+  static constexpr int DP = D + 4, CP = C + 4;
+  static constexpr size_t floats = 3 * C * DP + C * GW + 2 * C * CP + 6 * C + 2 * D;
   static constexpr size_t bytes = floats * sizeof(float);
 };
+
+__device__ __forceinline__ float halfwarp_sum(float v) {
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
 
 template <int D, int C, bool QBF16, bool PERCH>
 __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace ws, BwdArgs A) {
   constexpr int NT = 256;
-  constexpr int NE = C * D / NT;
+  constexpr int IR = C / 16, JC = D / 16;
   constexpr int GW = BwdPairSmem<D, C, PERCH>::GW;
-  extern __shared__ float smem[];
-  float* s_q = smem;               // [C][D] q^ = s q / |q| (scaled)
-  float* s_k = s_q + C * D;        // [C][D] k^ = k / |k|
-  float* s_dG = s_k + C * D;       // [C][D] gradient w.r.t. G, one value head at a time
-  float* s_G = s_dG + C * D;       // [C][GW] cumulative log-decay
-  float* s_dA = s_G + C * GW;      // [C][C]
-  float* s_dM = s_dA + C * C;      // [C][C]
-  float* s_b = s_dM + C * C;       // [C] beta
+  constexpr int DP = BwdPairSmem<D, C, PERCH>::DP, CP = BwdPairSmem<D, C, PERCH>::CP;
+  extern __shared__ __align__(16) float smem[];
+  float* s_q = smem;               // [C][DP] q^ = s q / |q| (scaled)
+  float* s_k = s_q + C * DP;       // [C][DP] k^ = k / |k|
+  float* s_dG = s_k + C * DP;      // [C][DP] gradient w.r.t. G, one value head at a time
+  float* s_G = s_dG + C * DP;      // [C][GW] cumulative log-decay
+  float* s_dA = s_G + C * GW;      // [C][CP] dA (times the pairwise decay for scalar decay)
+  float* s_dM = s_dA + C * CP;     // [C][CP] dM (likewise)
+  float* s_b = s_dM + C * CP;      // [C] beta
   float* s_rq = s_b + C;           // [C] 1/|q| (1 without the norm)
   float* s_rk = s_rq + C;          // [C]
   float* s_db = s_rk + C;          // [C] pairwise part of dbeta
@@ -508,7 +559,6 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
   float* s_dotk = s_dotq + C;      // [C]
   float* s_dGl = s_dotk + C;       // [D] gradient w.r.t. G_last
   float* s_gam = s_dGl + D;        // [D]
-  float* s_dec = s_gam + D;        // [C][C] exp(G_i - G_m), m <= i (scalar decay only)
 
   if (ws.loc.plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= ws.loc.plan.info[0]) return;
   const ChunkInfo ci = ws.loc.plan.chunks[blockIdx.x];
@@ -516,19 +566,21 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
   const int warp = tid >> 5, lane = tid & 31;
   const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
   const int n = ci.n;
+  const int r0 = (tid / 16) * IR, c0 = (tid % 16) * JC;
+  const bool lead = (tid % 16) == 0;         // writes its half-warp's row sums
 
   for (int idx = tid; idx < C * D; idx += NT) {
     const int i = idx / D, c = idx % D;
     const bool live = i < n;
-    s_q[idx] = live ? load_elem<QBF16>(P.q, (ci.t0 + i) * P.q_stride + static_cast<int64_t>(kh) * D + c) : 0.f;
-    s_k[idx] = live ? load_elem<QBF16>(P.k, (ci.t0 + i) * P.k_stride + static_cast<int64_t>(kh) * D + c) : 0.f;
+    s_q[i * DP + c] = live ? load_elem<QBF16>(P.q, (ci.t0 + i) * P.q_stride + static_cast<int64_t>(kh) * D + c) : 0.f;
+    s_k[i * DP + c] = live ? load_elem<QBF16>(P.k, (ci.t0 + i) * P.k_stride + static_cast<int64_t>(kh) * D + c) : 0.f;
   }
   __syncthreads();
   for (int i = warp; i < C; i += NT / 32) {
     float sq = 0.f, sk = 0.f;
     for (int c = lane; c < D; c += 32) {
-      sq += s_q[i * D + c] * s_q[i * D + c];
-      sk += s_k[i * D + c] * s_k[i * D + c];
+      sq += s_q[i * DP + c] * s_q[i * DP + c];
+      sk += s_k[i * DP + c] * s_k[i * DP + c];
     }
     sq = warp_sum(sq);
     sk = warp_sum(sk);
@@ -539,14 +591,16 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
   }
   __syncthreads();
   for (int idx = tid; idx < C * D; idx += NT) {
-    const int i = idx / D;
-    s_q[idx] *= s_rq[i] * P.scale;
-    s_k[idx] *= s_rk[i];
+    const int i = idx / D, c = idx % D;
+    s_q[i * DP + c] *= s_rq[i] * P.scale;
+    s_k[i * DP + c] *= s_rk[i];
   }
 
-  float adq[NE], adk[NE];
+  float adq[IR][JC], adk[IR][JC];
 #pragma unroll
-  for (int r = 0; r < NE; ++r) adq[r] = adk[r] = 0.f;
+  for (int a = 0; a < IR; ++a)
+#pragma unroll
+    for (int b = 0; b < JC; ++b) adq[a][b] = adk[a][b] = 0.f;
 
   for (int h = kh * ratio; h < (kh + 1) * ratio; ++h) {
     const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
@@ -567,83 +621,112 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
         s_G[i] = acc;
       }
     }
-    for (int i = tid; i < C; i += NT) {
-      s_b[i] = i < n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
-      s_db[i] = 0.f;
-    }
+    for (int i = tid; i < C; i += NT) s_b[i] = i < n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
     for (int idx = tid; idx < C * C; idx += NT) {
-      s_dA[idx] = ws.dA[unit * C * C + idx];
-      s_dM[idx] = ws.dM[unit * C * C + idx];
+      s_dA[(idx / C) * CP + idx % C] = ws.dA[unit * C * C + idx];
+      s_dM[(idx / C) * CP + idx % C] = ws.dM[unit * C * C + idx];
     }
     for (int c = tid; c < D; c += NT) s_dGl[c] = 0.f;
     __syncthreads();
     for (int c = tid; c < D; c += NT) s_gam[c] = expf(s_G[(C - 1) * GW + (PERCH ? c : 0)]);
-    if constexpr (!PERCH) {
+    if constexpr (!PERCH) {                     // fold exp(G_i - G_m) into the lower triangles
       for (int idx = tid; idx < C * C; idx += NT) {
         const int i = idx / C, m = idx % C;
-        s_dec[idx] = m <= i ? expf(s_G[i] - s_G[m]) : 0.f;
+        const float x = m <= i ? expf(s_G[i] - s_G[m]) : 0.f;
+        s_dA[i * CP + m] *= x;
+        s_dM[i * CP + m] *= x;
       }
       __syncthreads();
     }
+    float p1[IR][JC], p2[IR][JC], p3[IR][JC];
 #pragma unroll
-    for (int r = 0; r < NE; ++r) {
-      const int u = tid + NT * r, i = u / D, c = u % D;
-      const int gc = PERCH ? c : 0;
-      const float Gi = s_G[i * GW + gc];
-      const float Gl = s_G[(C - 1) * GW + gc];
-      // pairwise terms with i as the row: P1 from M, P2 from A (both over m <= i, m < i)
-      float p1 = 0.f, p2 = 0.f;
-      for (int m = 0; m <= i; ++m) {
-        const float km = s_k[m * D + c] * (PERCH ? expf(Gi - s_G[m * GW + gc]) : s_dec[i * C + m]);
-        p1 += s_dM[i * C + m] * km;
-        if (m < i) p2 += s_dA[i * C + m] * km;
+    for (int a = 0; a < IR; ++a)
+#pragma unroll
+      for (int b = 0; b < JC; ++b) p1[a][b] = p2[a][b] = p3[a][b] = 0.f;
+    // the entry as the row: P1 = sum_{m<=i} dM_im x_imc k^_mc, P2 = sum_{m<i} dA_im x_imc k^_mc
+    for (int m = 0; m < r0 + IR; ++m) {
+      float km[JC];
+      ld_row(km, s_k + m * DP + c0);
+#pragma unroll
+      for (int a = 0; a < IR; ++a) {
+        const int i = r0 + a;
+        if (m > i) continue;
+        const float fm = s_dM[i * CP + m], fa = s_dA[i * CP + m];
+#pragma unroll
+        for (int b = 0; b < JC; ++b) {
+          const float kd = PERCH ? km[b] * expf(s_G[i * GW + c0 + b] - s_G[m * GW + c0 + b]) : km[b];
+          p1[a][b] += fm * kd;
+          p2[a][b] += fa * kd;
+        }
       }
-      // with i as the column: P3 from M (rows i' >= i) and L (rows i' > i)
-      float p3 = 0.f;
-      for (int m = i; m < C; ++m) {
-        const float dec = PERCH ? expf(s_G[m * GW + gc] - Gi) : s_dec[m * C + i];
-        p3 += s_dM[m * C + i] * s_q[m * D + c] * dec;
-        if (m > i && delta) p3 += s_b[m] * s_dA[m * C + i] * s_k[m * D + c] * dec;
-      }
-      const float qv = s_q[u], kv = s_k[u];
-      const float eG = expf(Gi), eL = expf(Gl - Gi);
-      const float dQt = ws.dQt[unit * C * D + u];
-      const float dKt = ws.dKt[unit * C * D + u];
-      const float dKe = ws.dKe[unit * C * D + u];
-      const float bi = s_b[i];
-      adq[r] += p1 + dQt * eG;
-      adk[r] += bi * p2 + p3 + dKt * eG + dKe * eL;
-      s_dG[u] = qv * p1 + kv * bi * p2 - kv * p3 + dQt * qv * eG + dKt * kv * eG - dKe * kv * eL;
-      // dbeta's pairwise part sum_m dA_im L_im = sum_c k^_ic p2_ic; gamma's path into G_last
-      float bl = kv * p2;
-      float gl = dKe * kv * eL;
-      if constexpr (D >= 32) {
-        bl = warp_sum(bl);
-        if (lane == 0) atomicAdd(&s_db[i], bl);
-      } else {
-        atomicAdd(&s_db[i], bl);
-      }
-      atomicAdd(&s_dGl[c], gl);
     }
+    // the entry as the column: P3 = sum_{m>=i} dM_mi x_mic q^_mc + sum_{m>i} beta_m dA_mi x_mic k^_mc
+    for (int m = r0; m < C; ++m) {
+      float qm[JC], km[JC];
+      ld_row(qm, s_q + m * DP + c0);
+      ld_row(km, s_k + m * DP + c0);
+      const float bm = delta ? s_b[m] : 0.f;
+#pragma unroll
+      for (int a = 0; a < IR; ++a) {
+        const int i = r0 + a;
+        if (m < i) continue;
+        const float fm = s_dM[m * CP + i], fa = bm * s_dA[m * CP + i];
+#pragma unroll
+        for (int b = 0; b < JC; ++b) {
+          const float x = fm * qm[b] + fa * km[b];
+          p3[a][b] += PERCH ? x * expf(s_G[m * GW + c0 + b] - s_G[i * GW + c0 + b]) : x;
+        }
+      }
+    }
+    float gl[JC];
+#pragma unroll
+    for (int b = 0; b < JC; ++b) gl[b] = 0.f;
+#pragma unroll
+    for (int a = 0; a < IR; ++a) {
+      const int i = r0 + a;
+      float dqt[JC], dkt[JC], dke[JC];
+      ld_row(dqt, ws.dQt + unit * C * D + i * D + c0);
+      ld_row(dkt, ws.dKt + unit * C * D + i * D + c0);
+      ld_row(dke, ws.dKe + unit * C * D + i * D + c0);
+      const float bi = s_b[i];
+      float bl = 0.f;
+#pragma unroll
+      for (int b = 0; b < JC; ++b) {
+        const int gc = PERCH ? c0 + b : 0;
+        const float Gi = s_G[i * GW + gc], Gl = s_G[(C - 1) * GW + gc];
+        const float eG = expf(Gi), eL = expf(Gl - Gi);
+        const float qv = s_q[i * DP + c0 + b], kv = s_k[i * DP + c0 + b];
+        adq[a][b] += p1[a][b] + dqt[b] * eG;
+        adk[a][b] += bi * p2[a][b] + p3[a][b] + dkt[b] * eG + dke[b] * eL;
+        s_dG[i * DP + c0 + b] = qv * p1[a][b] + kv * bi * p2[a][b] - kv * p3[a][b] +
+                                dqt[b] * qv * eG + dkt[b] * kv * eG - dke[b] * kv * eL;
+        bl += kv * p2[a][b];                    // dbeta's pairwise part: sum_c k^_ic P2_ic
+        gl[b] += dke[b] * kv * eL;              // K_end's path into G_last
+      }
+      bl = halfwarp_sum(bl);
+      if (lead) s_db[i] = bl;
+    }
+#pragma unroll
+    for (int b = 0; b < JC; ++b) atomicAdd(&s_dGl[c0 + b], gl[b]);
     __syncthreads();
     for (int c = tid; c < D; c += NT)
-      s_dG[(C - 1) * D + c] += s_dGl[c] + ws.dgam[unit * D + c] * s_gam[c];
+      s_dG[(C - 1) * DP + c] += s_dGl[c] + ws.dgam[unit * D + c] * s_gam[c];
     __syncthreads();
     // dg = reverse cumulative sum of dG over the chunk's rows
     if (PERCH) {
       for (int c = tid; c < D; c += NT) {
         float acc = 0.f;
         for (int i = C - 1; i >= 0; --i) {
-          acc += s_dG[i * D + c];
+          acc += s_dG[i * DP + c];
           if (i < n) A.dg[((ci.t0 + i) * HV + h) * D + c] = acc;
         }
       }
     } else {
       for (int i = warp; i < C; i += NT / 32) {
-        float s = 0.f;
-        for (int c = lane; c < D; c += 32) s += s_dG[i * D + c];
-        s = warp_sum(s);
-        if (lane == 0) s_dotq[i] = s;
+        float sm = 0.f;
+        for (int c = lane; c < D; c += 32) sm += s_dG[i * DP + c];
+        sm = warp_sum(sm);
+        if (lane == 0) s_dotq[i] = sm;
       }
       __syncthreads();
       if (tid == 0) {
@@ -657,48 +740,36 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
     for (int i = tid; i < n; i += NT)
       A.dbeta[(ci.t0 + i) * HV + h] = ws.dbr[unit * C + i] + (delta ? s_db[i] : 0.f);
   }
-  __syncthreads();
   // the L2 normalisation's backward: with u = x / |x|, dx = (du - u (u . du)) / |x|
-  for (int i = tid; i < C; i += NT) {
-    s_dotq[i] = 0.f;
-    s_dotk[i] = 0.f;
-  }
-  __syncthreads();
 #pragma unroll
-  for (int r = 0; r < NE; ++r) {
-    const int u = tid + NT * r, i = u / D;
-    float dq = s_q[u] * adq[r], dk = s_k[u] * adk[r];
-    if constexpr (D >= 32) {
-      dq = warp_sum(dq);
-      dk = warp_sum(dk);
-      if (lane == 0) {
-        atomicAdd(&s_dotq[i], dq);
-        atomicAdd(&s_dotk[i], dk);
-      }
-    } else {
-      atomicAdd(&s_dotq[i], dq);
-      atomicAdd(&s_dotk[i], dk);
+  for (int a = 0; a < IR; ++a) {
+    const int i = r0 + a;
+    float dq = 0.f, dk = 0.f;
+#pragma unroll
+    for (int b = 0; b < JC; ++b) {
+      dq += s_q[i * DP + c0 + b] * adq[a][b];
+      dk += s_k[i * DP + c0 + b] * adk[a][b];
     }
-  }
-  __syncthreads();
-  const float inv_s = 1.f / P.scale;
-#pragma unroll
-  for (int r = 0; r < NE; ++r) {
-    const int u = tid + NT * r, i = u / D, c = u % D;
+    dq = halfwarp_sum(dq);
+    dk = halfwarp_sum(dk);
+    const float inv_s = 1.f / P.scale;
     if (i >= n) continue;
-    float dq, dk;
-    if (P.l2norm) {
-      // q^ = s u_q with u_q = q / |q|: dq = s (dq^ - u_q (u_q . dq^)) / |q|
-      const float uq = s_q[u] * inv_s;
-      dq = P.scale * s_rq[i] * (adq[r] - uq * s_dotq[i] * inv_s);
-      dk = s_rk[i] * (adk[r] - s_k[u] * s_dotk[i]);
-    } else {
-      dq = P.scale * adq[r];
-      dk = adk[r];
+    float oq[JC], ok[JC];
+#pragma unroll
+    for (int b = 0; b < JC; ++b) {
+      if (P.l2norm) {
+        // q^ = s u_q with u_q = q / |q|: dq = s (dq^ - u_q (u_q . dq^)) / |q|
+        const float uq = s_q[i * DP + c0 + b] * inv_s;
+        oq[b] = P.scale * s_rq[i] * (adq[a][b] - uq * dq * inv_s);
+        ok[b] = s_rk[i] * (adk[a][b] - s_k[i * DP + c0 + b] * dk);
+      } else {
+        oq[b] = P.scale * adq[a][b];
+        ok[b] = adk[a][b];
+      }
     }
-    const int64_t o = ((ci.t0 + i) * P.HK + kh) * D + c;
-    A.dq[o] = dq;
-    A.dk[o] = dk;
+    const int64_t o = ((ci.t0 + i) * P.HK + kh) * D + c0;
+    st_row(A.dq + o, oq);
+    st_row(A.dk + o, ok);
   }
 }
 

@@ -321,7 +321,7 @@ kda_status_t kda_prefill_bwd(const kda_params_t* p, const void* q, const void* k
   if (p->total_tokens > 0 && (!q || !k || !v || !beta || !log_decay || !d_o || !dq || !dk ||
                               !dv || !dbeta || !dlog_decay))
     return KDA_ERR_INVALID_ARG;
-  if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(state_pool, 4) ||
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(state_pool, 4) ||
       !aligned(beta, 4) || !aligned(log_decay, 4) || !aligned(input_row_offsets, 4) ||
       !aligned(slot_idx, 4) || !aligned(d_o, 4) || !aligned(d_state, 4) || !aligned(dq, 4) ||
       !aligned(dk, 4) || !aligned(dv, 4) || !aligned(dbeta, 4) || !aligned(dlog_decay, 4) ||

@@ -115,32 +115,6 @@ struct RowTile {
   static_assert(JT >= 1 && BV % JT == 0 && TPR * R == 256, "R x BV must tile 256 threads");
 };
 
-template <int N>
-__device__ __forceinline__ void ld_row(float (&x)[N], const float* p) {
-  if constexpr (N % 4 == 0) {
-#pragma unroll
-    for (int e = 0; e < N; e += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(p + e);
-      x[e] = v.x; x[e + 1] = v.y; x[e + 2] = v.z; x[e + 3] = v.w;
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < N; ++e) x[e] = p[e];
-  }
-}
-
-template <int N>
-__device__ __forceinline__ void st_row(float* p, const float (&x)[N]) {
-  if constexpr (N % 4 == 0) {
-#pragma unroll
-    for (int e = 0; e < N; e += 4)
-      *reinterpret_cast<float4*>(p + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
-  } else {
-#pragma unroll
-    for (int e = 0; e < N; ++e) p[e] = x[e];
-  }
-}
-
 // A C x D fp32 matrix of the workspace into a shared buffer with rows of DP floats, as
 // 16-byte asynchronous copies (committed as one group by the caller).
 template <int C, int D, int DP>

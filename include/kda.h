@@ -210,7 +210,8 @@ kda_status_t kda_prefill_fwd(const kda_params_t *p, const void *q, const void *k
  *   d_state0    [num_slots, HV, d_k, d_v] fp32 or NULL: dLoss/d(initial state),
  *               written at the touched slots only; may alias d_state
  *   workspace   >= kda_prefill_bwd_workspace_size bytes, 256-byte aligned
- * All arrays 4-byte aligned.  KDA_FLAG_NO_DELTA differentiates the additive
+ * q, k, v 16-byte aligned with 16-byte aligned rows (as for the forward), every
+ * other array 4-byte aligned.  KDA_FLAG_NO_DELTA differentiates the additive
  * write; KDA_FLAG_CUDA_CORES and KDA_FLAG_COMPACT are ignored.  Device-side
  * checks (offsets, slots) set the error word and skip the work, as in the forward.
  */

@@ -502,7 +502,8 @@ template <int D, int C, bool PERCH>
 struct BwdPairSmem {
   static constexpr int GW = PERCH ? D : 1;
   static constexpr int DP = D + 4, CP = C + 4;
-  static constexpr size_t floats = 3 * C * DP + C * GW + 2 * C * CP + 6 * C + 2 * D;
+  static constexpr size_t floats =
+      3 * C * DP + C * GW + 2 * C * CP + 6 * C + 3 * D + (PERCH ? C * DP : 0);
   static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -533,6 +534,8 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
   float* s_dotk = s_dotq + C;      // [C]
   float* s_dGl = s_dotk + C;       // [D] gradient w.r.t. G_last
   float* s_gam = s_dGl + D;        // [D]
+  float* s_ga = s_gam + D;         // [D] G at the chunk's middle token (per-channel decay)
+  float* s_E = s_ga + D;           // [C][DP] exp(G - G_a) (per-channel decay, anchored)
 
   if (ws.loc.plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= ws.loc.plan.info[0]) return;
   const ChunkInfo ci = ws.loc.plan.chunks[blockIdx.x];
@@ -612,46 +615,115 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
       }
       __syncthreads();
     }
+    // per-channel decay: the pairwise factor exp(G_ic - G_mc) = E+_ic / E+_mc with
+    // E+ = exp(G - G_a) (anchor at the middle token) while the decay stays in range; then
+    // P1, P2 = E+ (dM, dA) K- with K- = k^ / E+ and P3 = (dM^T (q^ E+) + ...)/E+, no exp per pair
+    bool anch = false;
+    if constexpr (PERCH) {
+      const int am = (n - 1) / 2;
+      for (int c = tid; c < D; c += NT) s_ga[c] = s_G[am * GW + c];
+      __syncthreads();
+      bool wide = false;
+      for (int idx = tid; idx < C * D; idx += NT) {
+        const int i = idx / D, c = idx % D;
+        wide |= fabsf(s_G[i * GW + c] - s_ga[c]) > kSimtAnchorRange;
+      }
+      anch = !__syncthreads_or(wide);
+      if (anch) {
+        for (int idx = tid; idx < C * D; idx += NT) {
+          const int i = idx / D, c = idx % D;
+          const float d = s_G[i * GW + c] - s_ga[c];
+          s_E[i * DP + c] = expf(d);
+          s_dG[i * DP + c] = s_k[i * DP + c] * expf(-d);     // K-, until dG is formed
+        }
+        __syncthreads();
+      }
+    }
     float p1[IR][JC], p2[IR][JC], p3[IR][JC];
 #pragma unroll
     for (int a = 0; a < IR; ++a)
 #pragma unroll
       for (int b = 0; b < JC; ++b) p1[a][b] = p2[a][b] = p3[a][b] = 0.f;
-    // the entry as the row: P1 = sum_{m<=i} dM_im x_imc k^_mc, P2 = sum_{m<i} dA_im x_imc k^_mc
-    for (int m = 0; m < r0 + IR; ++m) {
-      float km[JC];
-      ld_row(km, s_k + m * DP + c0);
+    if (PERCH && anch) {
+      for (int m = 0; m < r0 + IR; ++m) {
+        float km[JC];
+        ld_row(km, s_dG + m * DP + c0);
 #pragma unroll
-      for (int a = 0; a < IR; ++a) {
-        const int i = r0 + a;
-        if (m > i) continue;
-        const float fm = s_dM[i * CP + m], fa = s_dA[i * CP + m];
+        for (int a = 0; a < IR; ++a) {
+          const int i = r0 + a;
+          if (m > i) continue;
+          const float fm = s_dM[i * CP + m], fa = s_dA[i * CP + m];
+#pragma unroll
+          for (int b = 0; b < JC; ++b) {
+            p1[a][b] += fm * km[b];
+            p2[a][b] += fa * km[b];
+          }
+        }
+      }
+      for (int m = r0; m < C; ++m) {
+        float qm[JC], km[JC], em[JC];
+        ld_row(qm, s_q + m * DP + c0);
+        ld_row(km, s_k + m * DP + c0);
+        ld_row(em, s_E + m * DP + c0);
+        const float bm = delta ? s_b[m] : 0.f;
+#pragma unroll
+        for (int a = 0; a < IR; ++a) {
+          const int i = r0 + a;
+          if (m < i) continue;
+          const float fm = s_dM[m * CP + i], fa = bm * s_dA[m * CP + i];
+#pragma unroll
+          for (int b = 0; b < JC; ++b) p3[a][b] += (fm * qm[b] + fa * km[b]) * em[b];
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < IR; ++a)
 #pragma unroll
         for (int b = 0; b < JC; ++b) {
-          const float kd = PERCH ? km[b] * expf(s_G[i * GW + c0 + b] - s_G[m * GW + c0 + b]) : km[b];
-          p1[a][b] += fm * kd;
-          p2[a][b] += fa * kd;
+          const int i = r0 + a, c = c0 + b;
+          const float d = s_G[i * GW + c] - s_ga[c];
+          const float ep = s_E[i * DP + c];
+          p1[a][b] *= ep;
+          p2[a][b] *= ep;
+          p3[a][b] *= expf(-d);
+        }
+    } else {
+      // the entry as the row: P1 = sum_{m<=i} dM_im x_imc k^_mc, P2 = sum_{m<i} dA_im x_imc k^_mc
+      for (int m = 0; m < r0 + IR; ++m) {
+        float km[JC];
+        ld_row(km, s_k + m * DP + c0);
+#pragma unroll
+        for (int a = 0; a < IR; ++a) {
+          const int i = r0 + a;
+          if (m > i) continue;
+          const float fm = s_dM[i * CP + m], fa = s_dA[i * CP + m];
+#pragma unroll
+          for (int b = 0; b < JC; ++b) {
+            const float kd = PERCH ? km[b] * expf(s_G[i * GW + c0 + b] - s_G[m * GW + c0 + b]) : km[b];
+            p1[a][b] += fm * kd;
+            p2[a][b] += fa * kd;
+          }
+        }
+      }
+      // the entry as the column: P3 = sum_{m>=i} dM_mi x_mic q^_mc + sum_{m>i} beta_m dA_mi x_mic k^_mc
+      for (int m = r0; m < C; ++m) {
+        float qm[JC], km[JC];
+        ld_row(qm, s_q + m * DP + c0);
+        ld_row(km, s_k + m * DP + c0);
+        const float bm = delta ? s_b[m] : 0.f;
+#pragma unroll
+        for (int a = 0; a < IR; ++a) {
+          const int i = r0 + a;
+          if (m < i) continue;
+          const float fm = s_dM[m * CP + i], fa = bm * s_dA[m * CP + i];
+#pragma unroll
+          for (int b = 0; b < JC; ++b) {
+            const float x = fm * qm[b] + fa * km[b];
+            p3[a][b] += PERCH ? x * expf(s_G[m * GW + c0 + b] - s_G[i * GW + c0 + b]) : x;
+          }
         }
       }
     }
-    // the entry as the column: P3 = sum_{m>=i} dM_mi x_mic q^_mc + sum_{m>i} beta_m dA_mi x_mic k^_mc
-    for (int m = r0; m < C; ++m) {
-      float qm[JC], km[JC];
-      ld_row(qm, s_q + m * DP + c0);
-      ld_row(km, s_k + m * DP + c0);
-      const float bm = delta ? s_b[m] : 0.f;
-#pragma unroll
-      for (int a = 0; a < IR; ++a) {
-        const int i = r0 + a;
-        if (m < i) continue;
-        const float fm = s_dM[m * CP + i], fa = bm * s_dA[m * CP + i];
-#pragma unroll
-        for (int b = 0; b < JC; ++b) {
-          const float x = fm * qm[b] + fa * km[b];
-          p3[a][b] += PERCH ? x * expf(s_G[m * GW + c0 + b] - s_G[i * GW + c0 + b]) : x;
-        }
-      }
-    }
+    __syncthreads();                            // K- (in s_dG) is read no more
     float gl[JC];
 #pragma unroll
     for (int b = 0; b < JC; ++b) gl[b] = 0.f;

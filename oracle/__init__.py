@@ -15,6 +15,9 @@ Contents
                                Memory", sec. 1-2), the delta-free, decay-free special case
   backward(problem, ...)       reverse-mode differentiation of the recurrence in fp64
                                (`oracle/bptt.py`), pinned by finite differences
+  conv.conv_gates(...)         the front end before the recurrence: causal short convolution
+                               with a conv-state pool, SiLU, and the gate activations
+                               (`oracle/conv.py`)
 
 Parity status: every function here is pinned by `tests/test_oracle_pins.py`
 against closed forms, invariants the pages state, brute force and the worked

@@ -93,7 +93,8 @@ PREFILL_STAGES = {
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from the ncu
 # capture summarised in profiles/tc_front_tc_chain_gdn_prefill.md; a kernel changed since
 # its capture has no entry (reported as null).
-NCU_TRAFFIC = {("tc_front", "gdn_prefill"): 384.12e6, ("tc_chain", "gdn_prefill"): 489.77e6}
+NCU_TRAFFIC = {("tc_front", "gdn_prefill"): 384.12e6, ("tc_chain", "gdn_prefill"): 489.77e6,
+               ("conv_kernel", "gdn_prefill"): 358.74e6}
 
 
 def load_peaks() -> dict:
@@ -435,6 +436,53 @@ def time_prefill_bwd(p, dev, steps, warmup):
     return start.elapsed_time(end) / steps, int(n.value)
 
 
+CONV_WIDTH = 4
+
+
+def conv_algorithmic_bytes(p) -> float:
+    """The front end on a prefill's shapes: x read and y written once ([T, conv_dim] in the
+    q/k/v dtype), the gate pre-activations read and the gates written (fp32), the weights."""
+    T, HK, HV, d = p.total_tokens, p.num_k_heads, p.num_v_heads, p.d_k
+    es = 2 if p.qkv_dtype == "bf16" else 4
+    cd = (2 * HK + HV) * d
+    gw = d if p.decay_kind == "per_channel" else 1
+    return float(2 * T * cd * es + 2 * T * HV * (1 + gw) * 4 + cd * (CONV_WIDTH + 1) * 4)
+
+
+def time_conv_gates(p, dev, steps, warmup):
+    """The front end (short causal conv + SiLU + gates) on the prefill's shapes and offsets,
+    conv state in a slot pool, resident inputs (CUDA events)."""
+    import torch
+    import gated_delta_rule_deltanet_gb300 as kda
+    from workloads import torch_io
+    T, HK, HV, d = p.total_tokens, p.num_k_heads, p.num_v_heads, p.d_k
+    cd = (2 * HK + HV) * d
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    dt = torch.bfloat16 if p.qkv_dtype == "bf16" else torch.float32
+    x = torch.randn((T, cd), generator=gen).to(dt).to(dev)
+    w = (torch.randn((cd, CONV_WIDTH), generator=gen) * 0.5).to(dev)
+    a = torch.randn((T, HV, d) if p.decay_kind == "per_channel" else (T, HV), generator=gen).to(dev)
+    b = torch.randn((T, HV), generator=gen).to(dev)
+    state = torch.zeros((p.num_slots, cd, CONV_WIDTH - 1), dtype=dt, device=dev)
+    off = torch_io.index(p.offsets, dev)
+    slots = torch_io.index(p.slot_idx, dev)
+
+    def step():
+        kda.conv_gates(x, w, a, b, num_k_heads=HK, num_v_heads=HV, d=d,
+                       input_row_offsets=off, slot_idx=slots, conv_state=state)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
 VERIFY_WINDOW = 4
 
 
@@ -606,6 +654,19 @@ def ours_arm(args, rank, world, local):
                                        "achieved_gbs": bbytes / (bms / 1e3) / 1e9,
                                        "frac_hbm": bbytes / (bms / 1e3) / 1e9
                                        / peaks["hbm_gbs"]}})
+
+    if not args.no_decode:
+        cms = time_conv_gates(p, dev, 50, 3)
+        cval, _ = aggregate(float(p.total_tokens), cms / 1e3, world, dev)
+        cbytes = conv_algorithmic_bytes(p)
+        also.append({"workload": f"{p.name} front end (kda_conv_gates_fwd: conv width "
+                                 f"{CONV_WIDTH} + SiLU over [Q | K | V], gates)",
+                     "metric": "tokens/s", "value": cval, "unit": "tokens/s", "ms_per_step": cms,
+                     "roofline": {"bound": "hbm", "kernel": "conv_gates (three launches)",
+                                  "achieved": cbytes / (cms / 1e3) / 1e9,
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": cbytes / (cms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                  "traffic": NCU_TRAFFIC.get(("conv_kernel", p.name))}})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

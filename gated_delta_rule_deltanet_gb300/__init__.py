@@ -8,14 +8,15 @@ it:
     decode_step(q, k, v, beta, log_decay, slot_idx, state_pool)
     gdp_prefill / gdp_decode_step   (Gated DeltaProduct: n_h transitions per token)
     prefill_bwd(...)                (the backward pass of prefill)
+    conv_gates(...)                 (the front end: short conv + SiLU, gate activations)
 
 There is no CPU or eager fallback: if the library is missing, calls raise.
 """
 from .kda import (decode_step, get_device_error, make_params, prefill,  # noqa: F401
                   prefill_no_alloc, set_stage_events, uses_tensor_cores,
                   workspace_size, verify_window, fold_accepted, ring_record_elems,
-                  gdp_prefill, gdp_decode_step, prefill_bwd)
+                  gdp_prefill, gdp_decode_step, prefill_bwd, conv_gates)
 from ._lib import KdaError, KdaParams, load  # noqa: F401
 
 __all__ = ["prefill", "decode_step", "workspace_size", "get_device_error", "make_params",
-           "set_stage_events", "prefill_no_alloc", "uses_tensor_cores", "verify_window", "fold_accepted", "ring_record_elems", "gdp_prefill", "gdp_decode_step", "prefill_bwd", "KdaError", "KdaParams", "load"]
+           "set_stage_events", "prefill_no_alloc", "uses_tensor_cores", "verify_window", "fold_accepted", "ring_record_elems", "gdp_prefill", "gdp_decode_step", "prefill_bwd", "conv_gates", "KdaError", "KdaParams", "load"]

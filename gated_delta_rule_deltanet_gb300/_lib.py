@@ -37,7 +37,8 @@ EXPORTS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_size",
            "kda_set_stage_events", "kda_prefill_fwd_no_alloc",
            "kda_prefill_uses_tensor_cores", "kda_ring_record_elems", "kda_verify_window",
            "kda_fold_accepted", "kda_gdp_prefill_fwd", "kda_gdp_decode_step",
-           "kda_gdp_workspace_size", "kda_prefill_bwd", "kda_prefill_bwd_workspace_size")
+           "kda_gdp_workspace_size", "kda_prefill_bwd", "kda_prefill_bwd_workspace_size",
+           "kda_conv_gates_fwd")
 
 KDA_NO_ALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -130,6 +131,8 @@ def load():
         L.kda_prefill_bwd.restype = ctypes.c_int
         L.kda_prefill_bwd_workspace_size.argtypes = [pp, ctypes.POINTER(ctypes.c_size_t)]
         L.kda_prefill_bwd_workspace_size.restype = ctypes.c_int
+        L.kda_conv_gates_fwd.argtypes = [pp, ctypes.c_int32] + [P] * 14
+        L.kda_conv_gates_fwd.restype = ctypes.c_int
         L.kda_set_stage_events.argtypes = [P, ctypes.c_int32]
         L.kda_set_stage_events.restype = ctypes.c_int
         _lib = L

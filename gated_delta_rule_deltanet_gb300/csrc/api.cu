@@ -33,6 +33,12 @@ cudaError_t launch_gdp_expand(const void* q, int64_t q_stride, bool qbf16, const
                               cudaStream_t st);
 cudaError_t launch_gdp_gather(const float* ov, int64_t T, int n_h, int64_t orow, float* o,
                               cudaStream_t st);
+cudaError_t launch_conv_gates(const void* x, const float* w, const float* bias, const float* a,
+                              const float* b, const float* A_log, const float* dt_bias,
+                              const uint32_t* offsets, const uint32_t* slot_idx, void* state,
+                              void* y, float* g, float* beta, int64_t T, int B, int CD, int HV,
+                              int GW, int num_slots, int W, bool bf16, int32_t* err,
+                              cudaStream_t st);
 size_t bwd_workspace_bytes(const Problem& P);
 cudaError_t launch_prefill_bwd(const Problem& P, void* workspace, const float* d_o,
                                const float* d_state, float* dq, float* dk, float* dv,
@@ -339,6 +345,39 @@ kda_status_t kda_prefill_bwd(const kda_params_t* p, const void* q, const void* k
       P, workspace, d_o, d_state, dq, dk, dv, dbeta, dlog_decay, d_state0,
       p->qkv_dtype == KDA_DTYPE_BF16, p->decay_kind == KDA_DECAY_PER_CHANNEL,
       p->state_dtype == KDA_DTYPE_BF16, static_cast<cudaStream_t>(stream)));
+}
+
+kda_status_t kda_conv_gates_fwd(const kda_params_t* p, int32_t width, const void* x,
+                                const float* conv_weight, const float* conv_bias, const float* a,
+                                const float* b, const float* A_log, const float* dt_bias,
+                                const uint32_t* input_row_offsets, const uint32_t* slot_idx,
+                                void* conv_state, void* y, float* log_decay, float* beta,
+                                void* stream) {
+  Problem P{};
+  kda_status_t s = check_common(p, &P);
+  if (s != KDA_OK) return s;
+  if (width < 1 || width > 4) return KDA_ERR_UNSUPPORTED;
+  if (p->q_row_stride || p->k_row_stride || p->v_row_stride) return KDA_ERR_INVALID_ARG;
+  // without offsets every sequence is one token (the decode form)
+  const int64_t T = input_row_offsets ? p->total_tokens : p->num_seqs;
+  if (T < 0 || T > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+  if (p->num_seqs == 0 || T == 0) return KDA_OK;
+  if (!conv_weight || !x || !y || !a || !b || !log_decay || !beta) return KDA_ERR_INVALID_ARG;
+  if (conv_state && width > 1 && !slot_idx) return KDA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(conv_state, 4) || !aligned(conv_weight, 4) ||
+      !aligned(conv_bias, 4) || !aligned(a, 4) || !aligned(b, 4) || !aligned(A_log, 4) ||
+      !aligned(dt_bias, 4) || !aligned(input_row_offsets, 4) || !aligned(slot_idx, 4) ||
+      !aligned(log_decay, 4) || !aligned(beta, 4))
+    return KDA_ERR_INVALID_ARG;
+  const int CD = 2 * p->num_k_heads * p->d_k + p->num_v_heads * p->d_v;
+  const int GW = p->decay_kind == KDA_DECAY_PER_CHANNEL ? p->d_k : 1;
+  int32_t* err = device_error_word();
+  if (!err) return KDA_ERR_CUDA;
+  return to_status(kda::launch_conv_gates(
+      x, conv_weight, conv_bias, a, b, A_log, dt_bias, input_row_offsets, slot_idx,
+      width > 1 ? conv_state : nullptr, y, log_decay, beta, T, p->num_seqs, CD, p->num_v_heads,
+      GW, p->num_slots, width, p->qkv_dtype == KDA_DTYPE_BF16, err,
+      static_cast<cudaStream_t>(stream)));
 }
 
 kda_status_t kda_gdp_workspace_size(const kda_params_t* p, int32_t n_h, int32_t decode, size_t* bytes) {

@@ -238,6 +238,71 @@ def prefill_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
         raise KdaError(st, "kda_prefill_bwd")
     return dq, dk, dv, dbeta, dlog_decay, d_state0
 
+
+def conv_gates(x: torch.Tensor, conv_weight: torch.Tensor, a: torch.Tensor, b: torch.Tensor, *,
+               num_k_heads: int, num_v_heads: int, d: int, conv_bias: Optional[torch.Tensor] = None,
+               A_log: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+               input_row_offsets: Optional[torch.Tensor] = None,
+               slot_idx: Optional[torch.Tensor] = None, conv_state: Optional[torch.Tensor] = None,
+               num_seqs: Optional[int] = None, stream: Optional[torch.cuda.Stream] = None):
+    """The front end before the recurrence (kda_conv_gates_fwd): causal depthwise convolution
+    + SiLU over the packed [Q | K | V] projection x [T, conv_dim], and the gates.  `a` is
+    [T, HV] (scalar decay) or [T, HV, d] (per channel), `b` [T, HV].  Without
+    `input_row_offsets` every row is its own sequence (the decode form).  Returns
+    (y [T, conv_dim] in x's dtype, log_decay shaped like a, beta [T, HV]); `conv_state`
+    [num_slots, conv_dim, width - 1] (x's dtype) is updated in place."""
+    dev = _check_cuda(x, conv_weight, a, b)
+    if x.dim() != 2 or x.dtype not in _QKV_DTYPES or not x.is_contiguous():
+        raise ValueError("x must be contiguous [T, conv_dim] float32/bfloat16")
+    T, CD = x.shape
+    if CD != (2 * num_k_heads + num_v_heads) * d:
+        raise ValueError("x's width must be 2 * HK * d + HV * d")
+    if conv_weight.dtype != torch.float32 or conv_weight.dim() != 2 or conv_weight.shape[0] != CD \
+            or not conv_weight.is_contiguous():
+        raise ValueError("conv_weight must be contiguous float32 [conv_dim, width]")
+    width = conv_weight.shape[1]
+    if tuple(a.shape) == (T, num_v_heads):
+        per_channel = False
+    elif tuple(a.shape) == (T, num_v_heads, d):
+        per_channel = True
+    else:
+        raise ValueError("a must be [T, HV] or [T, HV, d]")
+    for name, t in (("a", a), ("b", b), ("conv_bias", conv_bias), ("A_log", A_log),
+                    ("dt_bias", dt_bias)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be contiguous float32")
+    if tuple(b.shape) != (T, num_v_heads):
+        raise ValueError("b must be [T, HV]")
+    if input_row_offsets is None:
+        B = T
+    else:
+        if input_row_offsets.dtype not in _INDEX_DTYPES or not input_row_offsets.is_contiguous():
+            raise ValueError("input_row_offsets must be contiguous int32/uint32")
+        B = input_row_offsets.numel() - 1
+    if num_seqs is not None and num_seqs != B:
+        raise ValueError("num_seqs does not match input_row_offsets")
+    num_slots = 1
+    if conv_state is not None:
+        if (conv_state.dtype != x.dtype or conv_state.dim() != 3 or conv_state.shape[1] != CD
+                or conv_state.shape[2] != width - 1 or not conv_state.is_contiguous()):
+            raise ValueError("conv_state must be contiguous [num_slots, conv_dim, width - 1] in x's dtype")
+        if slot_idx is None or slot_idx.numel() != B or slot_idx.dtype not in _INDEX_DTYPES:
+            raise ValueError("conv_state needs slot_idx [B] int32/uint32")
+        num_slots = conv_state.shape[0]
+    p = make_params(num_seqs=B, num_k_heads=num_k_heads, num_v_heads=num_v_heads, d=d,
+                    num_slots=num_slots, total_tokens=T, qkv_dtype=x.dtype,
+                    per_channel=per_channel)
+    y = torch.empty_like(x)
+    log_decay = torch.empty(tuple(a.shape), dtype=torch.float32, device=dev)
+    beta = torch.empty((T, num_v_heads), dtype=torch.float32, device=dev)
+    st = _lib.load().kda_conv_gates_fwd(
+        ctypes.byref(p), int(width), _ptr(x), _ptr(conv_weight), _ptr(conv_bias), _ptr(a), _ptr(b),
+        _ptr(A_log), _ptr(dt_bias), _ptr(input_row_offsets), _ptr(slot_idx), _ptr(conv_state),
+        _ptr(y), _ptr(log_decay), _ptr(beta), _stream_handle(stream, dev))
+    if st != _lib.KDA_OK:
+        raise KdaError(st, "kda_conv_gates_fwd")
+    return y, log_decay, beta
+
 def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
                 log_decay: torch.Tensor, slot_idx: torch.Tensor, state_pool: torch.Tensor, *,
                 scale: float = 0.0, l2norm: bool = True, delta_rule: bool = True,

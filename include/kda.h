@@ -187,6 +187,41 @@ kda_status_t kda_prefill_fwd(const kda_params_t *p, const void *q, const void *k
                              void *stream);
 
 /*
+ * The front end before the recurrence ("Pass 1" of the Modular "gated_delta" module, which
+ * consumes its output; SiLU features as in "From Attention to Learned Memory", sec. 1; the
+ * decay built from a log-rate and a softplus step as in the Mamba-2 section of "Linear
+ * attention visualized"): over the packed projection x = [Q | K | V] (conv_dim = 2 HK d_k +
+ * HV d_v channels per token) a depthwise causal convolution of `width` (1..4) taps and SiLU,
+ *
+ *     y[t, c] = SiLU(conv_bias[c] + sum_{i < width} conv_weight[c, i] x[t - width + 1 + i, c]),
+ *
+ * where the width - 1 inputs before a sequence's first token come from its slot of conv_state
+ * (oldest first; zeros when conv_state is NULL), and afterwards the slot holds the sequence's
+ * last width - 1 inputs (an empty sequence leaves it alone); plus the gates
+ *
+ *     beta = sigmoid(b),   log_decay = -exp(A_log[h]) softplus(a + dt_bias).
+ *
+ *   x, y         [T, conv_dim], qkv_dtype, 16-byte aligned; y's column blocks are q, k, v for
+ *                kda_prefill_fwd through q/k/v_row_stride = conv_dim
+ *   conv_weight  [conv_dim, width] fp32       conv_bias [conv_dim] fp32 or NULL
+ *   a            [T, HV] (SCALAR) or [T, HV, d_k] (PER_CHANNEL) fp32; b [T, HV] fp32
+ *   A_log        [HV] fp32 or NULL (rate 1)   dt_bias [HV] or [HV * d_k] fp32 or NULL
+ *   input_row_offsets  [B + 1] as kda_prefill_fwd (T = total_tokens), or NULL for the
+ *                decode form: one token per sequence, T = num_seqs
+ *   slot_idx     [B] (required with conv_state)
+ *   conv_state   [num_slots, conv_dim, width - 1], qkv_dtype, or NULL; read and written in place
+ *   log_decay    the shape of a, fp32;  beta [T, HV] fp32
+ * The row strides in p must be 0 (dense x and y).  Offsets out of order and slots out of
+ * range set the device error word; nothing is read or written out of bounds.
+ */
+kda_status_t kda_conv_gates_fwd(const kda_params_t *p, int32_t width, const void *x,
+                                const float *conv_weight, const float *conv_bias, const float *a,
+                                const float *b, const float *A_log, const float *dt_bias,
+                                const uint32_t *input_row_offsets, const uint32_t *slot_idx,
+                                void *conv_state, void *y, float *log_decay, float *beta,
+                                void *stream);
+
+/*
  * Backward pass of kda_prefill_fwd: the gradients of a loss w.r.t. every input,
  * given its gradients w.r.t. the outputs o and the final states.  The chunk form
  * of the forward ("You Could Have Come Up With Kimi Delta Attention", sec. 6) is

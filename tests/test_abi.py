@@ -272,3 +272,29 @@ def test_backward_rejects_bad_arguments_before_launch(lib):
     assert lib.kda_prefill_bwd(ctypes.byref(p), *args, 16, None) == _lib.KDA_ERR_WORKSPACE
     empty = good(num_seqs=0, total_tokens=0)
     assert lib.kda_prefill_bwd(ctypes.byref(empty), *([None] * 17), 0, None) == _lib.KDA_OK
+
+
+def test_conv_front_end_rejects_bad_arguments_before_launch(lib):
+    """kda_conv_gates_fwd checks widths, missing arrays, alignment and row strides on the host
+    (every call below fails before any launch)."""
+    p = good(total_tokens=64, num_seqs=2)
+    a = ctypes.c_void_p(1 << 20)
+    mis = ctypes.c_void_p((1 << 20) + 4)
+    args = [a] * 13          # x w bias a b A_log dt_bias offsets slots state y log_decay beta
+    for width in (0, 5, -1):
+        assert lib.kda_conv_gates_fwd(ctypes.byref(p), width, *args, None) == \
+            _lib.KDA_ERR_UNSUPPORTED
+    missing = list(args)
+    missing[0] = None                                            # x
+    assert lib.kda_conv_gates_fwd(ctypes.byref(p), 4, *missing, None) == _lib.KDA_ERR_INVALID_ARG
+    nos = list(args)
+    nos[8] = None                                                # state without slots
+    assert lib.kda_conv_gates_fwd(ctypes.byref(p), 4, *nos, None) == _lib.KDA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[10] = mis                                                # y misaligned
+    assert lib.kda_conv_gates_fwd(ctypes.byref(p), 4, *bad, None) == _lib.KDA_ERR_INVALID_ARG
+    strided = good(total_tokens=64, num_seqs=2, q_row_stride=1024)
+    assert lib.kda_conv_gates_fwd(ctypes.byref(strided), 4, *args, None) == \
+        _lib.KDA_ERR_INVALID_ARG
+    empty = good(total_tokens=0, num_seqs=0)
+    assert lib.kda_conv_gates_fwd(ctypes.byref(empty), 4, *([None] * 13), None) == _lib.KDA_OK

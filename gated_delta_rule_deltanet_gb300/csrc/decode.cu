@@ -18,7 +18,9 @@
 
 namespace kda {
 
-template <int D, int NT, bool QBF16, bool SBF16, bool PERCH>
+// DELTA = false: the additive write (no prediction), a template parameter so that the
+// delta rule's code carries no test of it
+template <int D, int NT, bool QBF16, bool SBF16, bool PERCH, bool DELTA>
 __global__ void __launch_bounds__(NT) decode_step_kernel(Problem P) {
   constexpr int VEC = 4;
   constexpr int TPR = D / VEC;        // threads across one state row
@@ -118,8 +120,8 @@ __global__ void __launch_bounds__(NT) decode_step_kernel(Problem P) {
     return tot;
   };
   // additive write (no delta rule): nothing is predicted, e = beta v
-  const float4 vhat = (P.flags & KDA_FLAG_NO_DELTA) ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                                    : reduce_rows(part, 0);
+  float4 vhat = make_float4(0.f, 0.f, 0.f, 0.f);
+  if constexpr (DELTA) vhat = reduce_rows(part, 0);
 
   // 4. correct and write
   const float4 e = make_float4(vbeta * (vv.x - vhat.x), vbeta * (vv.y - vhat.y),
@@ -149,7 +151,10 @@ template <int D, int NT, bool QBF16, bool SBF16, bool PERCH>
 static cudaError_t launch_decode_t(const Problem& P, cudaStream_t stream, const Stages& st) {
   const int64_t blocks = static_cast<int64_t>(P.num_seqs) * P.HV;
   st.mark(0, stream);
-  decode_step_kernel<D, NT, QBF16, SBF16, PERCH><<<dim3(static_cast<unsigned>(blocks)), NT, 0, stream>>>(P);
+  if (P.flags & KDA_FLAG_NO_DELTA)
+    decode_step_kernel<D, NT, QBF16, SBF16, PERCH, false><<<dim3(static_cast<unsigned>(blocks)), NT, 0, stream>>>(P);
+  else
+    decode_step_kernel<D, NT, QBF16, SBF16, PERCH, true><<<dim3(static_cast<unsigned>(blocks)), NT, 0, stream>>>(P);
   cudaError_t e = cudaGetLastError();
   st.mark(1, stream);
   return e;

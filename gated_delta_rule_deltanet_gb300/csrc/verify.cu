@@ -15,7 +15,9 @@
 
 namespace kda {
 
-template <int D, int NT, bool QBF16, bool SBF16, bool PERCH>
+// DELTA = false: the additive write (no prediction), a template parameter so that the
+// delta rule's code carries no test of it
+template <int D, int NT, bool QBF16, bool SBF16, bool PERCH, bool DELTA>
 __global__ void __launch_bounds__(NT) verify_window_kernel(Problem P, int window, float* ring,
                                                            int rec) {
   constexpr int VEC = 4;
@@ -100,8 +102,8 @@ __global__ void __launch_bounds__(NT) verify_window_kernel(Problem P, int window
       part.x += S[i].x * kc; part.y += S[i].y * kc; part.z += S[i].z * kc; part.w += S[i].w * kc;
     }
     // additive write (no delta rule): nothing is predicted, e = beta v
-    const float4 vhat = (P.flags & KDA_FLAG_NO_DELTA) ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                                      : reduce_rows(part, 0);
+    float4 vhat = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (DELTA) vhat = reduce_rows(part, 0);
     const float4 e = make_float4(vbeta * (vv.x - vhat.x), vbeta * (vv.y - vhat.y),
                                  vbeta * (vv.z - vhat.z), vbeta * (vv.w - vhat.w));
     float4 opart = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -182,8 +184,12 @@ int ring_record_elems(int D, bool perch) { return D + D + (perch ? D : 4); }
 template <int D, int NT, bool Q, bool SB, bool PC>
 static cudaError_t launch_verify_t(const Problem& P, int window, float* ring, cudaStream_t s) {
   const int64_t blocks = static_cast<int64_t>(P.num_seqs) * P.HV;
-  verify_window_kernel<D, NT, Q, SB, PC><<<dim3(static_cast<unsigned>(blocks)), NT, 0, s>>>(
-      P, window, ring, ring_record_elems(D, PC));
+  if (P.flags & KDA_FLAG_NO_DELTA)
+    verify_window_kernel<D, NT, Q, SB, PC, false><<<dim3(static_cast<unsigned>(blocks)), NT, 0, s>>>(
+        P, window, ring, ring_record_elems(D, PC));
+  else
+    verify_window_kernel<D, NT, Q, SB, PC, true><<<dim3(static_cast<unsigned>(blocks)), NT, 0, s>>>(
+        P, window, ring, ring_record_elems(D, PC));
   return cudaGetLastError();
 }
 

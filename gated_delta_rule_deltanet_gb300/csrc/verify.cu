@@ -154,15 +154,28 @@ __global__ void __launch_bounds__(NT) fold_accepted_kernel(Problem P, int window
 #pragma unroll
   for (int i = 0; i < RPT; ++i)
     S[i] = load4<SBF16>(P.pool, state_base + static_cast<int64_t>(r0 + i * RPP) * D + cg * VEC);
-  for (uint32_t t = 0; t < acc; ++t) {
+  // the next record, loaded into registers while the current one is applied
+  static_assert(NT >= D, "one key channel per thread");
+  float nk = 0.f, na = 0.f;
+  float4 ne;
+  auto fetch = [&](uint32_t t) {
     const float* rec_p = ring + ((static_cast<int64_t>(b) * window + t) * HV + h) * rec;
-    __syncthreads();
-    for (int c = tid; c < D; c += NT) {
-      s_k[c] = rec_p[c];
-      s_a[c] = PERCH ? rec_p[2 * D + c] : rec_p[2 * D];
+    if (tid < D) {
+      nk = rec_p[tid];
+      na = PERCH ? rec_p[2 * D + tid] : rec_p[2 * D];
     }
+    ne = *reinterpret_cast<const float4*>(rec_p + D + cg * VEC);
+  };
+  fetch(0);
+  for (uint32_t t = 0; t < acc; ++t) {
     __syncthreads();
-    const float4 e = *reinterpret_cast<const float4*>(rec_p + D + cg * VEC);
+    if (tid < D) {
+      s_k[tid] = nk;
+      s_a[tid] = na;
+    }
+    const float4 e = ne;
+    if (t + 1 < acc) fetch(t + 1);
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
       const int r = r0 + i * RPP;

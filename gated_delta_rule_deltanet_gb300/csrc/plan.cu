@@ -63,20 +63,29 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem P, PlanView 
   int base = s_scan[tid] - local;
   for (int b = b0; b < b1; ++b) {
     plan.seq_chunk0[b] = base;
-    const uint32_t bos = P.offsets[b], len = P.offsets[b + 1] - bos;
-    const int nb = static_cast<int>((len + C - 1) / C);
-    for (int c = 0; c < nb && base + c < max_chunks; ++c) {
-      ChunkInfo ci;
-      ci.seq = b;
-      ci.n = static_cast<int32_t>(min(static_cast<uint32_t>(C), len - static_cast<uint32_t>(c * C)));
-      ci.t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
-      plan.chunks[base + c] = ci;
-    }
-    base += nb;
+    base += static_cast<int>((P.offsets[b + 1] - P.offsets[b] + C - 1) / C);
   }
-  if (tid == kPlanThreads - 1) {
-    plan.seq_chunk0[B] = s_scan[tid];
-    plan.info[0] = s_scan[tid];
+  const int total = s_scan[kPlanThreads - 1];
+  if (tid == kPlanThreads - 1) plan.seq_chunk0[B] = total;
+  __syncthreads();                              // the first chunk of every sequence is written
+  // one table entry per thread and step: its sequence by binary search over the first chunks
+  // (an empty sequence shares its first chunk with the next one)
+  for (int g = tid; g < min(total, max_chunks); g += kPlanThreads) {
+    int lo = 0, hi = B;                         // seq_chunk0[lo] <= g < seq_chunk0[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (plan.seq_chunk0[mid] <= g) lo = mid; else hi = mid;
+    }
+    const int c = g - plan.seq_chunk0[lo];
+    const uint32_t bos = P.offsets[lo], len = P.offsets[lo + 1] - bos;
+    ChunkInfo ci;
+    ci.seq = lo;
+    ci.n = static_cast<int32_t>(min(static_cast<uint32_t>(C), len - static_cast<uint32_t>(c * C)));
+    ci.t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
+    plan.chunks[g] = ci;
+  }
+  if (tid == 0) {
+    plan.info[0] = total;
     plan.info[1] = 1;
   }
 }

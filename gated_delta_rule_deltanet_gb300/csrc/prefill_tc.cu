@@ -167,7 +167,9 @@ __device__ __forceinline__ void tc_issue_loads(const Problem& P, unsigned char* 
   tc::cp_async_commit();
 }
 
-template <bool PERCH, bool SBF16>
+// DELTA = false is the additive write (no delta rule): a template parameter, so that the
+// delta rule's code carries no test of it
+template <bool PERCH, bool SBF16, bool DELTA>
 __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanView plan) {
   using namespace tcp;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   const int HV = P.HV;
   const int kh = h / (HV / P.HK);
   // additive write (no delta rule): A_kk = 0 makes T = I and K~ = 0 drops W = TB K~
-  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
+  constexpr bool delta = DELTA;
   const uint32_t bos = P.offsets[b], eos = P.offsets[b + 1];
   if (eos <= bos) return;
   const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + vt * BV;
@@ -925,7 +927,8 @@ size_t tc_workspace_bytes(const Problem& P) { return plan_layout(P, nullptr, 0, 
 
 template <bool PERCH, bool SBF16>
 static cudaError_t launch_tc_t(const Problem& P, const PlanView& plan, cudaStream_t st) {
-  auto k = tc_prefill_kernel<PERCH, SBF16>;
+  auto k = (P.flags & KDA_FLAG_NO_DELTA) ? tc_prefill_kernel<PERCH, SBF16, false>
+                                         : tc_prefill_kernel<PERCH, SBF16, true>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(tcp::SMEM_BYTES));
   if (e != cudaSuccess) return e;

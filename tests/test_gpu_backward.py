@@ -141,3 +141,25 @@ def test_backward_strong_decay_takes_the_exact_pairwise_path():
     got = gpu_backward(p, d_o, d_state)
     ref = oracle.backward(p, d_o.astype(np.float64), d_state.astype(np.float64))
     compare(got, ref, TOL["f32"], label="strong decay")
+
+
+def test_backward_ragged_gqa_workload_sampled():
+    """ragged_gqa_kda (8 ragged sequences, 16 key / 32 value heads, bf16 pool): every gradient
+    of one key head's two value heads on two sequences; dq and dk of that key head sum both."""
+    p = workloads.workload("ragged_gqa_kda")
+    ratio = p.num_v_heads // p.num_k_heads
+    assert ratio == 2
+    d_o, d_state = seeds(p, 12)
+    got = gpu_backward(p, d_o, d_state)
+    kh = 5
+    seqs = [int(np.argmax(p.lengths)), int(np.argmin(p.lengths))]
+    pairs = [(b, kh * ratio + r) for b in seqs for r in range(ratio)]
+    ref = oracle.backward(p, d_o.astype(np.float64), d_state.astype(np.float64), pairs=pairs)
+    offs = p.offsets.astype(np.int64)
+    for b in seqs:
+        s, e = offs[b], offs[b + 1]
+        slot = int(p.slot_idx[b])
+        hs = slice(kh * ratio, (kh + 1) * ratio)
+        rows = {"dq": (slice(s, e), kh), "dk": (slice(s, e), kh), "dv": (slice(s, e), hs),
+                "dbeta": (slice(s, e), hs), "dg": (slice(s, e), hs), "d_state0": (slot, hs)}
+        compare(got, ref, TOL[p.qkv_dtype], rows=rows, label=f"ragged_gqa_kda seq {b}")

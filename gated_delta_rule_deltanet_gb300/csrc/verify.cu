@@ -25,9 +25,12 @@ __global__ void __launch_bounds__(NT) verify_window_kernel(Problem P, int window
   constexpr int RPP = NT / TPR;
   constexpr int RPT = D / RPP;
   constexpr int NWARP = NT / 32;
-  __shared__ float s_k[D], s_q[D], s_a[D];
+  // token inputs double-buffered: token t + 1's are written while token t is worked on and
+  // published by token t's second reduction, so a token costs two barriers (its reductions)
+  __shared__ float s_k[2][D], s_q[2][D], s_a[2][D];
   __shared__ float s_red[2][NWARP][D];
-  __shared__ float s_scale[2];
+  __shared__ float s_scale[2][2];
+  static_assert(NT >= D, "one key channel per thread");
 
   const int HV = P.HV;
   const int64_t bh = blockIdx.x;
@@ -66,30 +69,38 @@ __global__ void __launch_bounds__(NT) verify_window_kernel(Problem P, int window
     return tot;
   };
 
+  auto stage = [&](int t) {                     // token t's k, q, alpha into buffer t & 1
+    const int64_t row_t = static_cast<int64_t>(b) * window + t;
+    if (tid < D) {
+      const int bt = t & 1;
+      s_k[bt][tid] = load_elem<QBF16>(P.k, row_t * P.k_stride + static_cast<int64_t>(kh) * D + tid);
+      s_q[bt][tid] = load_elem<QBF16>(P.q, row_t * P.q_stride + static_cast<int64_t>(kh) * D + tid);
+      s_a[bt][tid] = expf(PERCH ? P.g[(row_t * HV + h) * D + tid] : P.g[row_t * HV + h]);
+    }
+  };
+  stage(0);
+  __syncthreads();
   for (int t = 0; t < window; ++t) {
     const int64_t row_t = static_cast<int64_t>(b) * window + t;
-    __syncthreads();  // the previous token's readers of s_k/s_q/s_a/s_red are done
-    for (int c = tid; c < D; c += NT) {
-      s_k[c] = load_elem<QBF16>(P.k, row_t * P.k_stride + static_cast<int64_t>(kh) * D + c);
-      s_q[c] = load_elem<QBF16>(P.q, row_t * P.q_stride + static_cast<int64_t>(kh) * D + c);
-      s_a[c] = expf(PERCH ? P.g[(row_t * HV + h) * D + c] : P.g[row_t * HV + h]);
-    }
-    __syncthreads();
+    const int bt = t & 1;
+    const float* sk = s_k[bt];
+    const float* sq = s_q[bt];
+    const float* sa = s_a[bt];
+    // the L2 norms of k and q (warps 0 and 1), published by the first reduction below: the
+    // products before it use the raw k and q and take the scales afterwards (they are linear)
     if (warp < 2) {
       constexpr int kStep = NWARP > 1 ? 2 : 1;
       for (int which = NWARP > 1 ? warp : 0; which < 2; which += kStep) {
-        const float* x = which == 0 ? s_k : s_q;
+        const float* x = which == 0 ? sk : sq;
         float ss = 0.f;
         for (int c = lane; c < D; c += 32) ss += x[c] * x[c];
         ss = warp_sum(ss);
         if (lane == 0) {
           const float inv = P.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
-          s_scale[which] = which == 0 ? inv : inv * P.scale;
+          s_scale[bt][which] = which == 0 ? inv : inv * P.scale;
         }
       }
     }
-    __syncthreads();
-    const float kscale = s_scale[0], qscale = s_scale[1];
     const float vbeta = P.beta[row_t * HV + h];
     const float4 vv = load4<QBF16>(P.v, row_t * P.v_stride + static_cast<int64_t>(h) * D + cg * VEC);
 
@@ -97,32 +108,38 @@ __global__ void __launch_bounds__(NT) verify_window_kernel(Problem P, int window
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
       const int r = r0 + i * RPP;
-      const float a = s_a[r], kc = s_k[r] * kscale;
+      const float a = sa[r], kr = sk[r];
       S[i].x *= a; S[i].y *= a; S[i].z *= a; S[i].w *= a;
-      part.x += S[i].x * kc; part.y += S[i].y * kc; part.z += S[i].z * kc; part.w += S[i].w * kc;
+      part.x += S[i].x * kr; part.y += S[i].y * kr; part.z += S[i].z * kr; part.w += S[i].w * kr;
     }
     // additive write (no delta rule): nothing is predicted, e = beta v
     float4 vhat = make_float4(0.f, 0.f, 0.f, 0.f);
     if constexpr (DELTA) vhat = reduce_rows(part, 0);
+    else __syncthreads();
+    const float kscale = s_scale[bt][0], qscale = s_scale[bt][1];
+    vhat.x *= kscale; vhat.y *= kscale; vhat.z *= kscale; vhat.w *= kscale;
     const float4 e = make_float4(vbeta * (vv.x - vhat.x), vbeta * (vv.y - vhat.y),
                                  vbeta * (vv.z - vhat.z), vbeta * (vv.w - vhat.w));
     float4 opart = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
       const int r = r0 + i * RPP;
-      const float kc = s_k[r] * kscale, qc = s_q[r] * qscale;
+      const float kc = sk[r] * kscale, qr = sq[r];
       S[i].x += kc * e.x; S[i].y += kc * e.y; S[i].z += kc * e.z; S[i].w += kc * e.w;
-      opart.x += S[i].x * qc; opart.y += S[i].y * qc; opart.z += S[i].z * qc; opart.w += S[i].w * qc;
+      opart.x += S[i].x * qr; opart.y += S[i].y * qr; opart.z += S[i].z * qr; opart.w += S[i].w * qr;
     }
     // the record of this token: [k^ | e | alpha]
     float* rec_p = ring + (row_t * HV + h) * rec;
-    for (int c = tid; c < D; c += NT) {
-      rec_p[c] = s_k[c] * kscale;
-      if (PERCH) rec_p[2 * D + c] = s_a[c];
+    if (tid < D) {
+      rec_p[tid] = sk[tid] * kscale;
+      if (PERCH) rec_p[2 * D + tid] = sa[tid];
     }
-    if (!PERCH && tid == 0) rec_p[2 * D] = s_a[0];
+    if (!PERCH && tid == 0) rec_p[2 * D] = sa[0];
     if (r0 == 0) *reinterpret_cast<float4*>(rec_p + D + cg * VEC) = e;
-    const float4 o = reduce_rows(opart, 1);
+    // the next token into the other buffer (last read before this token's first barrier)
+    if (t + 1 < window) stage(t + 1);
+    float4 o = reduce_rows(opart, 1);
+    o.x *= qscale; o.y *= qscale; o.z *= qscale; o.w *= qscale;
     if (r0 == 0) *reinterpret_cast<float4*>(P.o + (row_t * HV + h) * D + cg * VEC) = o;
   }
 }

@@ -495,10 +495,12 @@ def verify_problem():
                                   zero_state=False, seed=2006)
 
 
-def verify_algorithmic_bytes(p, accepted_total: int) -> dict:
+def verify_algorithmic_bytes(p, accepted) -> dict:
     """Verify reads the state once and every window token's inputs, writes o and one
-    record per token; the fold reads and writes each touched state and reads the
-    accepted records."""
+    record per token; the fold reads and writes the state of every sequence with at least
+    one accepted token (the others are left alone) and reads the accepted records."""
+    accepted = np.asarray(accepted)
+    accepted_total, touched = int(accepted.sum()), int(np.count_nonzero(accepted))
     B, HK, HV, d, W = p.num_seqs, p.num_k_heads, p.num_v_heads, p.d_k, VERIFY_WINDOW
     rec = 3 * d if p.decay_kind == "per_channel" else 2 * d + 4
     st = 2 if p.state_dtype == "bf16" else 4
@@ -506,7 +508,7 @@ def verify_algorithmic_bytes(p, accepted_total: int) -> dict:
     tok = B * W
     verify = (B * HV * d * d * st + tok * (2 * HK * d * 2 + HV * d * 2 + HV * 4 + HV * g * 4
                                            + HV * d * 4 + HV * rec * 4))
-    fold = 2 * B * HV * d * d * st + accepted_total * HV * rec * 4
+    fold = 2 * touched * HV * d * d * st + accepted_total * HV * rec * 4
     return {"verify_window": float(verify), "fold_accepted": float(fold)}
 
 
@@ -547,7 +549,7 @@ def time_verify(dev, steps, warmup):
     ms_v = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
     ms_f = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
     total = sum(e[0].elapsed_time(e[2]) for e in ev) / steps
-    return p, total, {"verify_window": ms_v, "fold_accepted": ms_f}, int(acc_host.sum())
+    return p, total, {"verify_window": ms_v, "fold_accepted": ms_f}, acc_host
 
 
 def ours_arm(args, rank, world, local):

@@ -6,38 +6,44 @@
 // work into a part that depends only on the chunk's own keys, queries, gates and
 // betas -- the intra-chunk matrices A_kk and A_qk, the inverse T = (I + A_kk)^-1 and
 // the WY factors -- and a part that carries the state from chunk to chunk.  With
-// E = TB V - W S the chunk's corrections, the state update and the output are
+// E = TB V - W S = TB (V - K~ S) the chunk's corrections (W = TB K~), the state update and
+// the output are
 //
-//   S' = diag(gam) S + K_end^T E = diag(gam) S + Kb V + P S,   Kb = K_end^T TB, P = -K_end^T W
-//   O  = Q~ S + A_qk E           = A1o V + A2o S,              A1o = A_qk TB,   A2o = Q~ - A_qk W
+//   S' = diag(gam) S + K_end^T E = diag(gam) S + Kb E',   Kb = K_end^T TB,  E' = V - K~ S
+//   O  = Q~ S + A_qk E           = Q~ S + A1o E',         A1o = A_qk TB
 //
 // so every product that does not involve the state can be formed before the state is
 // known.  The front kernel runs one CTA per (chunk, value head) over the whole GPU and
 // writes each chunk's operands to the workspace:
 //
-//   [Kb | P]    128 x (64 + 128)   fp16   (rows = key channels)
-//   [A1o | A2o]  64 x (64 + 128)   fp16   (rows = tokens)
+//   Kb          128 x 64    fp16   (rows = key channels)
+//   [K~; Q~]    128 x 128   fp16   (rows = tokens; K = key channels)
+//   A1o          64 x 64    fp16
 //   gam = exp(G_last) per key channel, fp32
 //
-// [Kb | P] is stored per thread of the chain kernel (each thread's 16-byte pieces of its
-// row, interleaved across threads so that every warp access is contiguous): the chain
-// kernel loads it into registers and writes it to tensor memory, where the MMA reads its
-// A operand.  [A1o | A2o] is stored in the K-major core-matrix order of a shared-memory A
-// operand and moved with one bulk copy.  The chain kernel keeps a (sequence, value head,
-// 64 value columns) slice of the state in registers; per chunk only one MMA group is on
-// the sequential path,
+// Kb is stored per thread of the chain kernel (each thread's 16-byte pieces of its row,
+// interleaved across threads so that every warp access is contiguous): the chain kernel
+// loads it into registers and writes it to tensor memory, where the MMA reads its A
+// operand.  [K~; Q~] and A1o are stored in the K-major core-matrix order of shared-memory
+// A operands and moved with one bulk copy.  The chain kernel keeps a (sequence, value
+// head, 64 value columns) slice of the state in registers; per chunk two dependent MMA
+// groups are on the sequential path,
 //
-//   D = Kb V + P S                M=128 N=64 K=64+128   (A from tensor memory; Kb V early)
+//   X = [K~; Q~] S                M=128 N=64 K=128     (rows 0-63 K~ S, rows 64-127 Q~ S)
+//   E' = V - X[0:64]              (fp16, over V in shared memory)
+//   D = Kb E'                     M=128 N=64 K=64      (A from tensor memory)
 //   S <- diag(gam) S + D
 //
-// and the output MMA O = [A1o | A2o] [V; S] (M=128, of which rows 0-63 are used) runs
-// beside the next chunk's state update.  Every operand the threads produce (V, S, and in
-// the front kernel TB, K~, -W, K_end) is stored MN-major, so each thread writes whole
-// 16-byte rows of core matrices instead of transposing.
+// and the output MMA A1o E' accumulates onto rows 64-127 of X beside the state update.
+// Every operand the threads produce (V, E', S, and in the front kernel TB and K_end) is
+// stored MN-major, so each thread writes whole 16-byte rows of core matrices instead of
+// transposing.  Against a record holding P = -Kb K~ (128 x 128) and A2o = Q~ - A1o K~ in
+// place of [K~; Q~], this one is 22% smaller and the front kernel runs one MMA round fewer,
+// at the cost of a second dependent MMA on the chain's sequential path.
 //
 // Operand precisions are those of the single-kernel path in prefill_tc.cu (fp16 operands,
-// fp32 accumulation and fp32 state); the state passes through fp16 only as the B operand of
-// P S, so a state-independent term never carries the state's rounding forward.
+// fp32 accumulation and fp32 state); the state passes through fp16 as the B operand of
+// [K~; Q~] S, and E' as that of Kb E' and A1o E'.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -56,28 +62,33 @@ constexpr int D = 128;      // head size
 constexpr int BV = 64;      // value columns per chain CTA
 constexpr int NT = 256;     // threads (8 warps); the chain kernel's compute warps
 constexpr int NTD = 128;    // chain kernel: operand warps 8-11
-constexpr int NTO = 64;     // chain kernel: output warps 12-13 (TMEM lanes 0-63)
-constexpr int NTC = NT + NTD + NTO + 32;   // + warp 14, whose lane 0 issues the output MMA
+constexpr int NTO = 64;     // chain kernel: output warps 14-15 (TMEM lanes 64-127)
+constexpr int NTC = NT + NTD + 64 + NTO;   // + warp 12, whose lane 0 issues the output MMA,
+                                           // and warp 13, which only pads to warp 14
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr float kMaxHalfChunkDecay = 80.0f;
 
 // record of one (chunk, value head) in the workspace
-//   BLOB: piece p (0..11) of thread t at (p * NT + t) * 16; thread t (key channel
-//         r = 32 (warp & 3) + lane, column half h = warp >> 2) holds Kb[r][32h .. 32h+32) in
-//         pieces 0-3 and P[r][64h .. 64h+64) in pieces 4-11
-//   OA:   [A1o | A2o], element (token m, column k) at cm_offset(m, k, OA_LBO, OA_SBO)
+//   BLOB: piece p (0..3) of thread t at (p * NT + t) * 16; thread t (key channel
+//         r = 32 (warp & 3) + lane, column half h = warp >> 2) holds Kb[r][32h .. 32h+32)
+//   KQ:   [K~; Q~] (rows 0-63 K~, rows 64-127 Q~, K = key channel), element (row, channel c)
+//         at cm_offset(row, c, 128, KQ_SBO): the K-major A operand of [K~; Q~] S
+//   A1O:  A1o (token m, column j) at cm_offset(m, j, 128, A1O_SBO), right after KQ, so that
+//         KQ and A1O move with one bulk copy
 //   GAM:  exp(G_last) per key channel
-constexpr uint32_t BLOB_PIECES = 12;
+constexpr uint32_t BLOB_PIECES = 4;
 constexpr uint32_t REC_BLOB = 0;
-constexpr uint32_t REC_OA = REC_BLOB + BLOB_PIECES * 256 * 16;
-constexpr uint32_t OA_LBO = 128, OA_SBO = tc::dense_sbo(C + D);   // K-major, K = 192
-constexpr uint32_t OA_BYTES = C * (C + D) * 2;
-constexpr uint32_t REC_GAM = REC_OA + OA_BYTES;
-constexpr uint32_t REC_BYTES = REC_GAM + 128 * 4;    // 74240, a multiple of 16
+constexpr uint32_t REC_KQ = REC_BLOB + BLOB_PIECES * 256 * 16;
+constexpr uint32_t KQ_SBO = tc::dense_sbo(D), KQ_BYTES = 2 * C * D * 2;
+constexpr uint32_t REC_A1O = REC_KQ + KQ_BYTES;
+constexpr uint32_t A1O_SBO = tc::dense_sbo(C), A1O_BYTES = C * C * 2;
+constexpr uint32_t KQA_BYTES = KQ_BYTES + A1O_BYTES;   // one bulk copy
+constexpr uint32_t REC_GAM = REC_A1O + A1O_BYTES;
+constexpr uint32_t REC_BYTES = REC_GAM + 128 * 4;    // 57856, a multiple of 16
 constexpr uint32_t KE_LBO = 2048, KE_SBO = 128;      // K_end (M = channel, K = token), MN-major
-constexpr uint32_t KT_LBO = 2048, KT_SBO = 128;      // K~ (N = channel, K = token)
 constexpr uint32_t TB_LBO = 1024, TB_SBO = 128;      // TB (N = column j, K = row m)
-static_assert(REC_BYTES % 16 == 0 && REC_OA % 16 == 0, "records must stay 16-byte aligned");
+static_assert(REC_BYTES % 16 == 0 && REC_KQ % 16 == 0 && KQA_BYTES % 16 == 0,
+              "records must stay 16-byte aligned");
 
 // per-chunk vectors of the front kernel (byte offsets inside its SMALL area)
 constexpr uint32_t O_GS = 0, O_BETA = 256, O_RK = 512, O_RQ = 768, O_EG = 1024, O_EGL = 1280,
@@ -110,12 +121,11 @@ template <>
 struct FrontMap<false> {
   static constexpr uint32_t AK = 0, AK_HALF = 128 * 128;
   static constexpr uint32_t SMALL = AK + 2 * AK_HALF;
-  static constexpr uint32_t R2 = SMALL + SMALL_BYTES;   // solve, then K_end and K~
-  static constexpr uint32_t LMAT = R2 + SOL_BYTES;      // [*; A_qk] 128 x 64 fp16, then Kb
+  static constexpr uint32_t R2 = SMALL + SMALL_BYTES;   // solve, then K_end
+  static constexpr uint32_t LMAT = R2 + SOL_BYTES;      // [*; A_qk] 128 x 64 fp16
   static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;  // TB 64 x 64 fp16, MN-major
   static constexpr uint32_t BYTES = TBT + 64 * 64 * 2;
-  static constexpr uint32_t KEA = R2, KTT = R2 + 64 * 128 * 2;     // K_end, K~ (MN-major)
-  static constexpr uint32_t KBA = LMAT, A1A = TBT - 64 * 64 * 2;   // Kb, [*; A1o] (K-major)
+  static constexpr uint32_t KEA = R2;                   // K_end (MN-major)
 };
 
 // Per-channel decay: TMA copies stage the raw k and q rows (the 128-byte swizzled layout
@@ -125,58 +135,58 @@ struct FrontMap<false> {
 // tensor memory, K- (both halves) to BK | BKLO.  Once the A-GEMM is done, K~ and Q~ are
 // rebuilt from the two halves of [K+; Q+] and K_end from K-, so the staged rows, the
 // log-decay and K- can all be reused: every region below serves several phases, which keeps
-// two CTAs per SM.
+// two CTAs per SM.  K~ and Q~ go straight to the record.
 template <>
 struct FrontMap<true> {
   static constexpr uint32_t AK_HALF = 128 * 128;
   static constexpr uint32_t RAW = 0;                    // raw k | q -> [K+; Q+] high halves;
                                                         // then TB (half 0 k rows), A_qk (half 1
                                                         // k rows), Q~ in place (q rows)
-  static constexpr uint32_t S_G = RAW + 2 * AK_HALF;    // log-decay -> exp(G - G_a); then K_end | K~
+  static constexpr uint32_t S_G = RAW + 2 * AK_HALF;    // log-decay -> exp(G - G_a); then K_end
   static constexpr uint32_t SMALL = S_G + C * D * 4;
   static constexpr uint32_t BK = SMALL + SMALL_BYTES;   // K- high | low halves; then the solve
-  static constexpr uint32_t BKLO = BK + 64 * 128 * 2;   // tiles; then Kb | [*; A1o]
+  static constexpr uint32_t BKLO = BK + 64 * 128 * 2;   // tiles
   static constexpr uint32_t R2 = BK;
   static constexpr uint32_t BYTES = R2 + SOL_BYTES;
   static constexpr uint32_t TBT = RAW;
   static constexpr uint32_t LMAT = RAW + AK_HALF - 64 * 64 * 2;   // rows 64-127: half 1 k rows
-  static constexpr uint32_t KEA = S_G, KTT = S_G + 64 * 128 * 2;
-  static constexpr uint32_t KBA = BK, A1A = BK + 64 * 128 * 2;
+  static constexpr uint32_t KEA = S_G;
   static_assert(R2 + 2 * SOL_TILE == BKLO + 64 * 128 * 2, "solve tiles cover the K- halves");
-  static_assert(A1A + 128 * 64 * 2 <= BYTES, "[*; A1o] operand in bounds");
 };
 
-// front TMEM columns: A_kk/A_qk (second issuer's half of K in F_X), then Kb | A1o, then
-// Kb K~ | A1o K~ (the low half of [K+; Q+] shares F_Y: the A-GEMM consumes it first)
-constexpr uint32_t F_A = 0, F_X = 64, F_Y = 128, F_ALO = 128, F_COLS = 256;
+// front TMEM columns: A_kk/A_qk (second issuer's half of K in F_X), then Kb | A1o; the low
+// half of [K+; Q+] in F_ALO
+constexpr uint32_t F_A = 0, F_X = 64, F_ALO = 128, F_COLS = 256;
 
 // chain shared memory (MN-major operands: core matrices of 8 K-rows x 8 value columns,
-// value-column groups adjacent, K groups 1024 bytes apart).  The output MMA has M = 128
-// but only rows 0-63 exist: its A operand [A1o | A2o] (K-major) reads its rows 64-127
-// from the next OA_BYTES of shared memory, whatever they hold; those rows of the result
-// are never read.
+// value-column groups adjacent, K groups 1024 bytes apart).  A slot of the KQA ring holds a
+// record's [K~; Q~ | A1o] as one bulk copy moves it; a V slot holds V, then E' = V - K~ S in
+// place.  The output MMA A1o E' has M = 128 with A1o as rows 64-127: its A operand starts
+// A1O_BYTES before A1o, so that rows 0-63 read the tail of Q~, whose products land in
+// accumulator rows that are never read again.
 constexpr uint32_t OP_LBO = 1024, OP_SBO = 128;
 constexpr int OS = BV + 4;                               // o staging row (fp32)
-constexpr uint32_t OA_SLOTS = 3, V_SLOTS = 5, S_SLOTS = 3;
+constexpr uint32_t KQA_SLOTS = 3, V_SLOTS = 5;
 constexpr uint32_t V_BYTES = 64 * 64 * 2, S_BYTES = 128 * 64 * 2;
-constexpr uint32_t CH_OA = 0;                            // [A1o | A2o] of three chunks
-constexpr uint32_t CH_V = CH_OA + OA_SLOTS * OA_BYTES;   // V of four chunks, 64 x 64 (bf16 -> fp16)
-constexpr uint32_t CH_ST = CH_V + V_SLOTS * V_BYTES;     // S of three chunks, 128 x 64 fp16
-constexpr uint32_t CH_OST = CH_ST + S_SLOTS * S_BYTES;   // o rows fp32 [64][OS]
+constexpr uint32_t CH_KQA = 0;                           // [K~; Q~ | A1o] of three chunks
+constexpr uint32_t CH_V = CH_KQA + KQA_SLOTS * KQA_BYTES;   // V -> E' of five chunks, 64 x 64 fp16
+constexpr uint32_t CH_ST = CH_V + V_SLOTS * V_BYTES;     // S, 128 x 64 fp16
+constexpr uint32_t CH_OST = CH_ST + S_BYTES;             // o rows fp32 [64][OS]
 constexpr uint32_t CH_GAM = CH_OST + C * OS * 4;         // gamma of four chunks, fp32 [4][128]
 constexpr uint32_t GAM_SLOTS = 4;
 constexpr uint32_t CH_BYTES = CH_GAM + GAM_SLOTS * D * 4;
 static_assert(CH_BYTES + 64 <= 227 * 1024, "chain shared memory budget");
 static_assert(2 * (FrontMap<true>::BYTES + 3 * 1024) <= 228 * 1024, "two per-channel front CTAs per SM");
 static_assert(2 * (FrontMap<false>::BYTES + 1024 + 1024) <= 228 * 1024, "two scalar front CTAs per SM");
-static_assert(CH_V % 128 == 0 && CH_ST % 128 == 0 && OA_BYTES % 128 == 0, "operand alignment");
-static_assert(CH_OA + (OA_SLOTS + 1) * OA_BYTES <= CH_BYTES, "rows 64-127 of the last OA stay in bounds");
-// chain TMEM columns: [Kb | P] of two chunks (fp16 pairs); the state MMA's result as two
-// partial sums (Kb V + P[:, 0:64] S[0:64], double-buffered because the next chunk's Kb V is
-// accumulated early, and P[:, 64:128] S[64:128]); the output MMA's result, double-buffered
-constexpr uint32_t T_A = 0, A_COLS = 96, T_DS = 192, T_DS2 = 320, T_DO = 384, CH_COLS = 512;
-__host__ __device__ constexpr uint32_t ds_col(uint32_t c) { return T_DS + (c & 1) * 64; }
-__host__ __device__ constexpr uint32_t do_col(uint32_t c) { return T_DO + (c & 1) * 64; }
+static_assert(CH_V % 128 == 0 && CH_ST % 128 == 0 && KQA_BYTES % 128 == 0, "operand alignment");
+// chain TMEM columns: Kb of two chunks (fp16 pairs); the state MMA Kb E' as two partial
+// sums (one per issuing thread); [K~; Q~] S as two partial sums, double-buffered (rows 0-63
+// K~ S, rows 64-127 Q~ S, onto which A1o E' accumulates the output)
+constexpr uint32_t T_A = 0, A_COLS = 32, T_DS = 64, T_DS2 = 128, T_X = 192, CH_COLS = 512;
+__host__ __device__ constexpr uint32_t x_col(uint32_t c, uint32_t part) {
+  return T_X + (c & 1) * 128 + part * 64;
+}
+static_assert(x_col(1, 1) + 64 <= CH_COLS, "chain tensor-memory columns");
 
 __device__ __forceinline__ uint4 f16x8_pack(const float* x) {
   return make_uint4(tc::pack_f16x2(x[0], x[1]), tc::pack_f16x2(x[2], x[3]),
@@ -253,7 +263,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
   float* sA = reinterpret_cast<float*>(smem + M::R2);
   float* sT = reinterpret_cast<float*>(smem + M::R2 + SOL_TILE);
   float* sX = reinterpret_cast<float*>(smem + M::R2 + 2 * SOL_TILE);
-  constexpr uint32_t KEA = M::KEA, KTT = M::KTT;   // K_end, K~ (MN-major)
+  constexpr uint32_t KEA = M::KEA;              // K_end (MN-major)
   constexpr uint32_t M_RAW = PERCH ? FrontMap<true>::RAW : 0u;     // raw k | q (per-channel)
   constexpr uint32_t M_SG = PERCH ? FrontMap<true>::S_G : 0u;      // staged log-decay
   constexpr uint32_t M_AK = PERCH ? 0u : FrontMap<false>::AK;      // raw k | q (scalar)
@@ -539,8 +549,8 @@ __global__ void __launch_bounds__(tcs::NT, 2)
   if constexpr (PERCH) {
     // ---------------------------------------------------------------- K~, Q~, K_end
     // rebuilt from the split halves the A-GEMM has consumed: K~ = K+ exp(G_a) and
-    // K_end = K- exp(G_last - G_a) (MN-major fp16, over the consumed log-decay),
-    // Q~ = Q+ exp(G_a) (fp16, over its own raw rows)
+    // Q~ = Q+ exp(G_a) (fp16, to the record's [K~; Q~]) and K_end = K- exp(G_last - G_a)
+    // (MN-major fp16, over the consumed log-decay)
     {
       const int i = row < C ? row : row - C;
       uint32_t l0[16], l1[16];
@@ -566,7 +576,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
 #pragma unroll
           for (int e = 0; e < 8; ++e) x[e] = 0.f;
         }
-        tc::f16x8_store(smem, row < C ? KTT + tc::mn_offset(i, cc, KT_LBO, KT_SBO) : off, x);
+        tc::f16x8_store(rec, REC_KQ + tc::cm_offset(row, cc, 128, KQ_SBO), x);
       }
     }
     {
@@ -761,9 +771,9 @@ __global__ void __launch_bounds__(tcs::NT, 2)
   tc::fence_after_sync();
 
   // ------------------------------------------------------------------ A1o = A_qk TB, Kb = K_end^T TB
-  // With W = TB K~ the remaining products all start from TB: Kb = K_end^T TB, A1o = A_qk TB,
-  // then P = -K_end^T W = -Kb K~ and A_qk W = A1o K~.  A1o is rows 64-127 of the
-  // [*; A_qk] TB product (rows 0-63 of that operand are never read back).
+  // With W = TB K~ never formed (the chain kernel forms V - K~ S instead), the remaining
+  // products are Kb = K_end^T TB and A1o = A_qk TB.  A1o is rows 64-127 of the [*; A_qk] TB
+  // product (rows 0-63 of that operand are never read back).
   if (tid == 32) {
     const uint32_t id = tc::idesc_f16(128, 64, tc::kF16, false, false, true);
     const uint64_t dl = tc::smem_desc(tc::smem_u32(smem + M::LMAT), 128, tc::dense_sbo(64));
@@ -773,24 +783,17 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       tc::mma_ss(tmem + F_X, tc::desc_add(dl, s * 256), tc::desc_add(dt, s * 2 * TB_LBO), id, s > 0);
     tc::mma_commit(&s_bar2);
   }
-  // K_end = k^ exp(G_last - G_m) (A operand K_end^T, MN-major) and K~ = k^ exp(G_m) (B
-  // operand of the second round, MN-major) into the consumed solve area, row pieces of 8
-  // channels
-  // (the per-channel path built both before the A extraction)
+  // K_end = k^ exp(G_last - G_m): A operand K_end^T, MN-major, into the consumed solve area,
+  // row pieces of 8 channels (the per-channel path built it before the A extraction)
   if constexpr (!PERCH) {
     for (int u = tid; u < C * (D / 8); u += NT) {
       const int m = (u >> 7) * 8 + (u & 7), c0 = ((u >> 3) & 15) * 8;
-      float kx[8], ke[8], kt[8];
-      tc::bf16x8_load(kq_piece(false, m, c0), kx);
-      const float rk = sRK[m];
-      const float fe = rk * sEGL[m], ft = delta ? rk * sEG[m] : 0.f;
+      float x[8];
+      tc::bf16x8_load(kq_piece(false, m, c0), x);
+      const float fe = sRK[m] * sEGL[m];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        ke[e] = kx[e] * fe;
-        kt[e] = kx[e] * ft;
-      }
-      tc::f16x8_store(smem, KEA + tc::mn_offset(m, c0, KE_LBO, KE_SBO), ke);
-      tc::f16x8_store(smem, KTT + tc::mn_offset(m, c0, KT_LBO, KT_SBO), kt);
+      for (int e = 0; e < 8; ++e) x[e] *= fe;
+      tc::f16x8_store(smem, KEA + tc::mn_offset(m, c0, KE_LBO, KE_SBO), x);
     }
   }
   if (tid < D) reinterpret_cast<float*>(rec + REC_GAM)[tid] = sGam[tid];
@@ -807,13 +810,25 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       tc::mma_ss(tmem + F_A, tc::desc_add(dke, s * 2 * KE_LBO), tc::desc_add(dtb, s * 2 * TB_LBO), id, s > 0);
     tc::mma_commit(&s_bar);
   }
+  // while they run: K~ = k^ exp(G_m) and Q~ = q scale/|q| exp(G_m) to the record's [K~; Q~]
+  // (the per-channel path wrote both before the A extraction)
+  if constexpr (!PERCH) {
+    for (int u = tid; u < 2 * C * (D / 8); u += NT) {
+      const int r = (u >> 7) * 8 + (u & 7), c0 = ((u >> 3) & 15) * 8;   // r: row of [K~; Q~]
+      const bool is_q = r >= C;                 // warp-uniform
+      const int m = is_q ? r - C : r;
+      float x[8];
+      tc::bf16x8_load(kq_piece(is_q, m, c0), x);
+      const float f = (delta || is_q) ? (is_q ? sRQ[m] : sRK[m]) * sEG[m] : 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] *= f;
+      tc::f16x8_store(rec, REC_KQ + tc::cm_offset(r, c0, 128, KQ_SBO), x);
+    }
+  }
   mma_wait2();
 
   // ------------------------------------------------------------------ Kb, A1o out
-  // Kb (fp16): record pieces 0-3 and the K-major A operand of P (consumed [*; A_qk] area);
-  // A1o (fp16): columns 0-63 of the output operand and rows 64-127 of the A operand of
-  // A1o K~ (in the consumed TB area; its rows 0-63 fall on Kb's rows 64-127, unread)
-  constexpr uint32_t KBA = M::KBA, A1A = M::A1A;
+  // Kb (fp16): record pieces 0-3; A1o (fp16, rows 64-127 of the product): the record's A1O
   {
     uint32_t r0[16], r1[16];
     tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf, r0);
@@ -826,11 +841,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       x[e + 16] = __uint_as_float(r1[e]);
     }
 #pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8) {
-      const uint4 v = f16x8_pack(x + 8 * g8);
-      blob[g8 * NT] = v;
-      *reinterpret_cast<uint4*>(smem + KBA + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64))) = v;
-    }
+    for (int g8 = 0; g8 < 4; ++g8) blob[g8 * NT] = f16x8_pack(x + 8 * g8);
     if (row >= C) {                             // warp-uniform: warps 2, 3, 6, 7
       tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf, r0);
       tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf + 16, r1);
@@ -841,76 +852,8 @@ __global__ void __launch_bounds__(tcs::NT, 2)
         x[e + 16] = __uint_as_float(r1[e]);
       }
 #pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        const uint4 v = f16x8_pack(x + 8 * g8);
-        *reinterpret_cast<uint4*>(rec + REC_OA + tc::cm_offset(row - C, 32 * chalf + 8 * g8, OA_LBO, OA_SBO)) = v;
-        *reinterpret_cast<uint4*>(smem + A1A + tc::cm_offset(row, 32 * chalf + 8 * g8, 128, tc::dense_sbo(64))) = v;
-      }
-    }
-  }
-  tc::fence_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-
-  // ------------------------------------------------------------------ Kb K~, A1o K~
-  if (tid == 0 || tid == 32) {
-    const bool second = tid == 32;
-    const uint32_t id = tc::idesc_f16(128, 128, tc::kF16, false, false, true);
-    const uint64_t da = tc::smem_desc(tc::smem_u32(smem + (second ? A1A : KBA)), 128, tc::dense_sbo(64));
-    const uint64_t dk = tc::smem_desc(tc::smem_u32(smem + KTT), KT_LBO, KT_SBO);
-    const uint32_t d = tmem + (second ? F_Y : F_A);
-#pragma unroll
-    for (int s = 0; s < C / 16; ++s)
-      tc::mma_ss(d, tc::desc_add(da, s * 256), tc::desc_add(dk, s * 2 * KT_LBO), id, s > 0);
-    tc::mma_commit(second ? &s_bar2 : &s_bar);
-  }
-  mma_wait2();
-
-  // ------------------------------------------------------------------ P, A2o out
-  // P = -Kb K~: record pieces 4-11; A2o = Q~ - A1o K~ (rows 64-127): columns 64-191 of the
-  // output operand
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int c0 = 64 * chalf + 32 * half;
-    uint32_t r0[16], r1[16];
-    float x[32];
-    tc::tmem_ld16(tmem + lane_addr + F_A + c0, r0);
-    tc::tmem_ld16(tmem + lane_addr + F_A + c0 + 16, r1);
-    tc::tmem_wait_ld();
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      x[e] = -__uint_as_float(r0[e]);
-      x[e + 16] = -__uint_as_float(r1[e]);
-    }
-#pragma unroll
-    for (int g8 = 0; g8 < 4; ++g8) blob[(4 + 4 * half + g8) * NT] = f16x8_pack(x + 8 * g8);
-    if (row >= C) {                             // Q~ = q scale/|q| exp(G)
-      tc::tmem_ld16(tmem + lane_addr + F_Y + c0, r0);
-      tc::tmem_ld16(tmem + lane_addr + F_Y + c0 + 16, r1);
-      const int i = row - C;
-      const float rq = sRQ[i];
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        if constexpr (PERCH) {                  // Q~ was built in place
-          tc::f16x8_load(kq_piece(true, i, c0 + 8 * g8), x + 8 * g8);
-        } else {
-          float qv[8];
-          tc::bf16x8_load(kq_piece(true, i, c0 + 8 * g8), qv);
-          const float f = rq * sEG[i];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[8 * g8 + e] = qv[e] * f;
-        }
-      }
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        x[e] -= __uint_as_float(r0[e]);
-        x[e + 16] -= __uint_as_float(r1[e]);
-      }
-#pragma unroll
       for (int g8 = 0; g8 < 4; ++g8)
-        *reinterpret_cast<uint4*>(rec + REC_OA + tc::cm_offset(i, C + c0 + 8 * g8, OA_LBO, OA_SBO)) =
+        *reinterpret_cast<uint4*>(rec + REC_A1O + tc::cm_offset(row - C, 32 * chalf + 8 * g8, 128, A1O_SBO)) =
             f16x8_pack(x + 8 * g8);
     }
   }
@@ -930,17 +873,16 @@ __global__ void __launch_bounds__(tcs::NT, 2)
 // One CTA per (sequence, value head, 64 value columns), warp-specialised into four
 // groups that each run their own loop over the sequence's chunks:
 //   compute warps 0-7 keep the state slice in registers (thread = key channel, 32 value
-//     columns) and run the sequential part: D = Kb V + P S, then S <- diag(gam) S + D,
-//     publishing the fp16 copy of S.  The MMA group is split between threads 0 and 128
+//     columns) and run the sequential part: X = [K~; Q~] S, then E' = V - X[0:64] (warps
+//     0, 1, 4, 5, whose TMEM lanes are the chunk's tokens), D = Kb E', S <- diag(gam) S + D,
+//     publishing the fp16 copy of S.  Each MMA group is split between threads 0 and 128
 //     into separate accumulators (one thread issues a tcgen05.mma only about every 90
-//     cycles, slower than the tensor core completes these N = 64 shapes); thread 0 also
-//     accumulates the next chunk's Kb V ahead of time;
+//     cycles, slower than the tensor core completes these N = 64 shapes);
 //   operand warps 8-11 prepare chunks ahead: values (bf16 -> fp16, fetched two chunks
-//     ahead), [Kb | P] global -> registers -> tensor memory, gamma -> shared memory;
-//   lane 0 of warp 14 bulk-copies [A1o | A2o] and issues the output MMA
-//     O = [A1o | A2o] [V; S] once the chunk's state MMA is queued, so that it runs beside
-//     the state update;
-//   output warps 12-13 (TMEM lanes 0-63) move the o rows to global memory.
+//     ahead), Kb global -> registers -> tensor memory, gamma -> shared memory;
+//   lane 0 of warp 12 bulk-copies [K~; Q~ | A1o] and issues the output MMA: A1o E'
+//     accumulates onto rows 64-127 of X, which hold Q~ S, beside the state MMA;
+//   output warps 14-15 (TMEM lanes 64-127) move the o rows to global memory.
 // The groups hand over through monotonic step counters in shared memory.  Every wait is
 // bounded; a timeout sets s_abort, each group leaves its loop at a barrier whose
 // reduction makes all of its threads agree (or, for the single issuing thread, at once),
@@ -950,14 +892,15 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
     tc_chain_kernel(Problem P, PlanView plan, const unsigned char* records) {
   using namespace tcs;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t s_bar_s;                  // state MMA of a chunk: both halves (threads 0, 128)
+  __shared__ uint64_t s_bar_x;                  // [K~; Q~] S of a chunk: both halves (threads 0, 128)
+  __shared__ uint64_t s_bar_s;                  // Kb E' of a chunk: both halves
   __shared__ uint64_t s_bar_o;                  // output MMA of a chunk
-  __shared__ uint64_t s_oa_bar[OA_SLOTS];       // bulk copies of [A1o | A2o]
+  __shared__ uint64_t s_kqa_bar[KQA_SLOTS];     // bulk copies of [K~; Q~ | A1o]
   __shared__ uint64_t s_drain;                  // abort only: every MMA issued so far
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_ready;                       // chunks whose V, [Kb | P] and gamma are in place
-  __shared__ int s_issued;                      // state-MMA halves issued (two per chunk)
+  __shared__ int s_ready;                       // chunks whose V, Kb and gamma are in place
+  __shared__ int s_e_ready;                     // chunks whose E' is in place
   __shared__ int s_ps_done;                     // chunks whose state MMA has completed
   __shared__ int s_o_done;                      // chunks whose output MMA has completed
   __shared__ int s_o_free;                      // chunks whose o rows have left tensor memory
@@ -977,8 +920,7 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
     return records + ((c0 + c) * HV + h) * static_cast<int64_t>(REC_BYTES);
   };
   auto v_off = [](uint32_t c) -> uint32_t { return CH_V + (c % V_SLOTS) * V_BYTES; };
-  auto s_off = [](uint32_t c) -> uint32_t { return CH_ST + (c % S_SLOTS) * S_BYTES; };
-  auto oa_off = [](uint32_t c) -> uint32_t { return CH_OA + (c % OA_SLOTS) * OA_BYTES; };
+  auto kqa_off = [](uint32_t c) -> uint32_t { return CH_KQA + (c % KQA_SLOTS) * KQA_BYTES; };
   auto chunk_n = [&](uint32_t c) -> int {
     const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
     return static_cast<int>(min(static_cast<int64_t>(C), static_cast<int64_t>(eos) - t0));
@@ -1017,14 +959,15 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
     tc::tmem_relinquish();
   }
   if (tid == 0) {
+    tc::mbar_init(&s_bar_x, 2);
     tc::mbar_init(&s_bar_s, 2);
     tc::mbar_init(&s_bar_o, 1);
-    for (uint32_t i = 0; i < OA_SLOTS; ++i) tc::mbar_init(&s_oa_bar[i], 1);
+    for (uint32_t i = 0; i < KQA_SLOTS; ++i) tc::mbar_init(&s_kqa_bar[i], 1);
     tc::mbar_init(&s_drain, 3);
     tc::fence_mbar_init();
     s_abort = 0;
     s_ready = 0;
-    s_issued = 0;
+    s_e_ready = 0;
     s_ps_done = 0;
     s_o_done = 0;
     s_o_free = 0;
@@ -1035,13 +978,14 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
   const uint32_t tmem = s_tmem;
   const uint32_t lane_addr = static_cast<uint32_t>(32 * (warp & 3)) << 16;
   const uint32_t id_s = tc::idesc_f16(128, BV, tc::kF16, false, false, true);   // A in TMEM
-  const uint32_t id_o = tc::idesc_f16(128, BV, tc::kF16, false, false, true);   // A K-major smem
+  const uint32_t id_k = tc::idesc_f16(128, BV, tc::kF16, false, false, true);   // A K-major smem
   const uint64_t dV0 = tc::smem_desc(sb + CH_V, OP_LBO, OP_SBO);
-  const uint64_t dS0 = tc::smem_desc(sb + CH_ST, OP_LBO, OP_SBO);
-  const uint64_t dOA0 = tc::smem_desc(sb + CH_OA, OA_LBO, OA_SBO);
-  constexpr int W_OPER = NT / 32, W_OUT = W_OPER + NTD / 32, W_ISSUE = W_OUT + NTO / 32;
+  const uint64_t dS = tc::smem_desc(sb + CH_ST, OP_LBO, OP_SBO);
+  const uint64_t dKQ0 = tc::smem_desc(sb + CH_KQA, 128, KQ_SBO);
+  const uint64_t dA10 = tc::smem_desc(sb + CH_KQA + KQ_BYTES - A1O_BYTES, 128, A1O_SBO);
+  constexpr int W_OPER = NT / 32, W_ISSUE = W_OPER + NTD / 32, W_OUT = W_ISSUE + 2;
 
-  if (warp >= W_OPER && warp < W_OUT) {
+  if (warp >= W_OPER && warp < W_ISSUE) {
     // ------------------------------------------------------------------ operand warps
     const int dt = tid - NT;                    // 0..127
     auto issue_v = [&](uint32_t c) {            // raw bf16 v -> MN-major positions of V[c % 5]
@@ -1066,9 +1010,8 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
         p[u] = f16x8_pack(x);
       }
     };
-    // a thread serves TMEM lane 32 (warp & 3) + lane for both column halves, i.e. the
-    // [Kb | P] pieces of compute threads dt and dt + 128 (12 pieces each), and key channel
-    // dt of gamma
+    // a thread serves TMEM lane 32 (warp & 3) + lane for both column halves, i.e. the Kb
+    // pieces of compute threads dt and dt + 128 (4 pieces each), and key channel dt of gamma
     uint4 ablob[2 * BLOB_PIECES];
     float gam_next = 0.f;
     auto load_blob = [&](uint32_t c) {
@@ -1091,15 +1034,6 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
           w[4 * p] = a[p].x; w[4 * p + 1] = a[p].y; w[4 * p + 2] = a[p].z; w[4 * p + 3] = a[p].w;
         }
         tc::tmem_st16(base + 16 * ch, w);
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int p = 0; p < 4; ++p) {
-            const uint4 v = a[4 + 4 * half + p];
-            w[4 * p] = v.x; w[4 * p + 1] = v.y; w[4 * p + 2] = v.z; w[4 * p + 3] = v.w;
-          }
-          tc::tmem_st16(base + 32 + 32 * ch + 16 * half, w);
-        }
       }
       tc::tmem_wait_st();
     };
@@ -1107,7 +1041,7 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
     if (nchunks > 1) issue_v(1);
     load_blob(0);
     for (uint32_t q = 0; q < nchunks; ++q) {
-      // V(q + 2) into the slot of V(q - 3) (its Kb V and output MMA are done), then V(q)
+      // V(q + 2) into the slot of V(q - 3) (its state and output MMAs are done), then V(q)
       // in place: groups issued after V(q) are V(q + 1) and V(q + 2) where they exist
       bool bad = q >= 3 && !wait_flag(&s_o_done, static_cast<int>(q) - 2);
       // the tensor-memory buffer of q held chunk q - 2, read by that chunk's state MMA
@@ -1130,29 +1064,27 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
       if (dt == 0) set_flag(&s_ready, static_cast<int>(q) + 1);
     }
     tc::cp_async_wait_all();
-  } else if (warp >= W_OUT && warp < W_ISSUE) {
+  } else if (warp >= W_OUT) {
     // ------------------------------------------------------------------ output warps
-    const int dq = tid - NT - NTD;              // 0..63, TMEM lane and token row
+    const int dq = tid - NT - NTD - 64;         // 0..63: token row, TMEM lane 64 + dq
     float* op = reinterpret_cast<float*>(smem + CH_OST) + dq * OS;
     for (uint32_t c = 0; c < nchunks; ++c) {
       const bool bad = !wait_bar(&s_bar_o, c & 1);
       if (tc::named_sync_or(3, NTO, bad || aborted())) break;
       if (dq == 0) set_flag(&s_o_done, static_cast<int>(c) + 1);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int qq = 0; qq < 4; ++qq) {          // 16 columns of both partial sums
         uint32_t r0[16], r1[16];
-        tc::tmem_ld16(tmem + lane_addr + do_col(c) + 32 * half, r0);
-        tc::tmem_ld16(tmem + lane_addr + do_col(c) + 32 * half + 16, r1);
+        tc::tmem_ld16(tmem + lane_addr + x_col(c, 0) + 16 * qq, r0);
+        tc::tmem_ld16(tmem + lane_addr + x_col(c, 1) + 16 * qq, r1);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          *reinterpret_cast<float4*>(op + 32 * half + e) =
-              make_float4(__uint_as_float(r0[e]), __uint_as_float(r0[e + 1]),
-                          __uint_as_float(r0[e + 2]), __uint_as_float(r0[e + 3]));
-          *reinterpret_cast<float4*>(op + 32 * half + 16 + e) =
-              make_float4(__uint_as_float(r1[e]), __uint_as_float(r1[e + 1]),
-                          __uint_as_float(r1[e + 2]), __uint_as_float(r1[e + 3]));
-        }
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4*>(op + 16 * qq + e) =
+              make_float4(__uint_as_float(r0[e]) + __uint_as_float(r1[e]),
+                          __uint_as_float(r0[e + 1]) + __uint_as_float(r1[e + 1]),
+                          __uint_as_float(r0[e + 2]) + __uint_as_float(r1[e + 2]),
+                          __uint_as_float(r0[e + 3]) + __uint_as_float(r1[e + 3]));
       }
       tc::fence_before_sync();
       tc::named_sync(3, NTO);
@@ -1178,39 +1110,36 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
   } else if (warp == W_ISSUE) {
     // ------------------------------------------------------------------ output-MMA issuer
     if (lane == 0) {
-      auto load_oa = [&](uint32_t c) {          // [A1o | A2o] of chunk c, one bulk copy
-        tc::mbar_arrive_expect_tx(&s_oa_bar[c % OA_SLOTS], OA_BYTES);
-        tc::bulk_load(sb + oa_off(c), rec(c) + REC_OA, OA_BYTES, &s_oa_bar[c % OA_SLOTS]);
+      auto load_kqa = [&](uint32_t c) {         // [K~; Q~ | A1o] of chunk c, one bulk copy
+        tc::mbar_arrive_expect_tx(&s_kqa_bar[c % KQA_SLOTS], KQA_BYTES);
+        tc::bulk_load(sb + kqa_off(c), rec(c) + REC_KQ, KQA_BYTES, &s_kqa_bar[c % KQA_SLOTS]);
       };
-      for (uint32_t q = 0; q < min(nchunks, OA_SLOTS); ++q) load_oa(q);
+      for (uint32_t q = 0; q < min(nchunks, KQA_SLOTS); ++q) load_kqa(q);
       for (uint32_t c = 0; c < nchunks; ++c) {
-        // both halves of the state MMA queued; D_O[c & 1] free (o rows of c - 2 out, and of
-        // c - 1, which also keeps the completion barrier one phase ahead of its waiters)
-        if (!wait_flag(&s_issued, 2 * static_cast<int>(c) + 2)) break;
+        // E'(c) in place (so X(c) is complete and its rows 0-63 consumed); o rows of c - 1
+        // out, which keeps the completion barrier one phase ahead of its waiters
+        if (!wait_flag(&s_e_ready, static_cast<int>(c) + 1)) break;
         if (!wait_flag(&s_o_free, static_cast<int>(c))) break;
-        if (!wait_bar(&s_oa_bar[c % OA_SLOTS], (c / OA_SLOTS) & 1)) break;
-        const uint32_t d = tmem + do_col(c);
-        const uint64_t da = tc::desc_add(dOA0, (c % OA_SLOTS) * OA_BYTES);
+        if (!wait_bar(&s_kqa_bar[c % KQA_SLOTS], (c / KQA_SLOTS) & 1)) break;
+        const uint64_t da = tc::desc_add(dA10, (c % KQA_SLOTS) * KQA_BYTES);
         const uint64_t dv = tc::desc_add(dV0, (c % V_SLOTS) * V_BYTES);
-        const uint64_t ds = tc::desc_add(dS0, (c % S_SLOTS) * S_BYTES);
 #pragma unroll
         for (int s = 0; s < C / 16; ++s)
-          tc::mma_ss(d, tc::desc_add(da, s * 2 * OA_LBO), tc::desc_add(dv, s * 2 * OP_LBO), id_o, s > 0);
-#pragma unroll
-        for (int s = 0; s < D / 16; ++s)
-          tc::mma_ss(d, tc::desc_add(da, (C / 16 + s) * 2 * OA_LBO), tc::desc_add(ds, s * 2 * OP_LBO), id_o, 1);
+          tc::mma_ss(tmem + x_col(c, 0), tc::desc_add(da, s * 256), tc::desc_add(dv, s * 2 * OP_LBO), id_k, 1);
         tc::mma_commit(&s_bar_o);
         // the slot of chunk c - 1 is free once its output MMA is done
-        if (c >= 1 && c - 1 + OA_SLOTS < nchunks) {
+        if (c >= 1 && c - 1 + KQA_SLOTS < nchunks) {
           if (!wait_flag(&s_o_done, static_cast<int>(c))) break;
-          load_oa(c - 1 + OA_SLOTS);
+          load_kqa(c - 1 + KQA_SLOTS);
         }
       }
     }
-  } else {
+  } else if (warp < W_OPER) {
     // ------------------------------------------------------------------ compute warps
     const int row = 32 * (warp & 3) + lane;     // TMEM lane = key channel (state row)
     const int chalf = warp >> 2;
+    const int part = tid >> 7;                  // threads 0 and 128 issue one half each
+    const bool extract = row < C;               // warps 0, 1, 4, 5: row = token of X, E'
     float Sv[32];
     {
       const int64_t base = sbase + static_cast<int64_t>(row) * D + 32 * chalf;
@@ -1219,87 +1148,92 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
         Sv[j] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[base + j])
                       : static_cast<const float*>(P.pool)[base + j];
     }
-    auto write_state_operand = [&](uint32_t c) {   // S_c, fp16, MN-major
+    auto write_state_operand = [&]() {          // S, fp16, MN-major
 #pragma unroll
       for (int p = 0; p < 4; ++p)
-        *reinterpret_cast<uint4*>(smem + s_off(c) + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
+        *reinterpret_cast<uint4*>(smem + CH_ST + tc::mn_offset(row, 32 * chalf + 8 * p, OP_LBO, OP_SBO)) =
             f16x8_pack(Sv + 8 * p);
     };
-    // Kb V of chunk c into its accumulator (thread 0; the same thread's P S follows)
-    auto issue_kbv = [&](uint32_t c) {
-      const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
-      const uint64_t dv = tc::desc_add(dV0, (c % V_SLOTS) * V_BYTES);
-#pragma unroll
-      for (int s = 0; s < C / 16; ++s)
-        tc::mma_ts(tmem + ds_col(c), ta + s * 8, tc::desc_add(dv, s * 2 * OP_LBO), id_s, s > 0);
-    };
-    write_state_operand(0);
+    write_state_operand();
     tc::fence_async_smem();
     tc::fence_before_sync();
     tc::named_sync(1, NT);
     tc::fence_after_sync();
-    bool kbv_ahead = false;                     // thread 0: Kb V of the current chunk issued
     bool stop = false;
     for (uint32_t c = 0; c < nchunks && !stop; ++c) {
-      const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
-      const uint64_t ds = tc::desc_add(dS0, (c % S_SLOTS) * S_BYTES);
       bool bad = false;
-      if (tid == 0) {                           // Kb V + P[:, 0:64] S[0:64]
-        if (!kbv_ahead) {
-          bad = !wait_flag(&s_ready, static_cast<int>(c) + 1);
-          tc::fence_after_sync();
-          if (!bad) issue_kbv(c);
-        }
+      if ((tid & 127) == 0) {                   // X = [K~; Q~] S, K half `part`
+        // [K~; Q~ | A1o](c) in place; X(c & 1) free once the o rows of chunk c - 2 are out
+        bad = !wait_bar(&s_kqa_bar[c % KQA_SLOTS], (c / KQA_SLOTS) & 1);
+        bad = bad || (c >= 2 && !wait_flag(&s_o_free, static_cast<int>(c) - 1));
         if (!bad) {
-#pragma unroll
-          for (int s = 0; s < D / 32; ++s)
-            tc::mma_ts(tmem + ds_col(c), ta + 32 + s * 8, tc::desc_add(ds, s * 2 * OP_LBO), id_s, 1);
-          tc::mma_commit(&s_bar_s);
-          __threadfence_block();
-          atomicAdd(&s_issued, 1);
-        }
-        // the next chunk's Kb V, if its operands are in place (once the other half is queued)
-        kbv_ahead = !bad && c + 1 < nchunks &&
-                    *reinterpret_cast<volatile int*>(&s_ready) >= static_cast<int>(c) + 2 &&
-                    wait_flag(&s_issued, 2 * static_cast<int>(c) + 2);
-        if (kbv_ahead) {
           tc::fence_after_sync();
-          issue_kbv(c + 1);
+          const uint64_t da = tc::desc_add(dKQ0, (c % KQA_SLOTS) * KQA_BYTES);
+#pragma unroll
+          for (int s = 4 * part; s < 4 * part + 4; ++s)
+            tc::mma_ss(tmem + x_col(c, part), tc::desc_add(da, s * 256), tc::desc_add(dS, s * 2 * OP_LBO),
+                       id_k, s > 4 * part);
+          tc::mma_commit(&s_bar_x);
         }
       }
-      if (tid == 128) {                         // P[:, 64:128] S[64:128]
-        bad = !wait_flag(&s_ready, static_cast<int>(c) + 1);
-        tc::fence_after_sync();
+      if (extract) {                            // E' = V - K~ S over V's slot
+        bad = bad || !wait_bar(&s_bar_x, c & 1);
+        bad = bad || !wait_flag(&s_ready, static_cast<int>(c) + 1);   // V(c), Kb(c)
+        bad = __any_sync(0xffffffffu, bad);     // tcgen05.ld is warp-collective
         if (!bad) {
+          unsigned char* vp = smem + v_off(c);
 #pragma unroll
-          for (int s = D / 32; s < D / 16; ++s)
-            tc::mma_ts(tmem + T_DS2, ta + 32 + s * 8, tc::desc_add(ds, s * 2 * OP_LBO), id_s, s > D / 32);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t r0[16], r1[16];
+            tc::tmem_ld16(tmem + lane_addr + x_col(c, 0) + 32 * chalf + 16 * hh, r0);
+            tc::tmem_ld16(tmem + lane_addr + x_col(c, 1) + 32 * chalf + 16 * hh, r1);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+              const uint32_t off = tc::mn_offset(row, 32 * chalf + 16 * hh + 8 * p, OP_LBO, OP_SBO);
+              float v[8];
+              tc::f16x8_load(vp + off, v);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                v[e] -= __uint_as_float(r0[8 * p + e]) + __uint_as_float(r1[8 * p + e]);
+              *reinterpret_cast<uint4*>(vp + off) = f16x8_pack(v);
+            }
+          }
+        }
+        tc::fence_async_smem();
+        tc::fence_before_sync();
+        bad = tc::named_sync_or(4, NT / 2, bad || aborted());
+        tc::fence_after_sync();
+        if (!bad && (tid & 127) == 0) {         // D = Kb E', K half `part`
+          if (tid == 0) set_flag(&s_e_ready, static_cast<int>(c) + 1);
+          const uint32_t ta = tmem + T_A + (c & 1) * A_COLS;
+          const uint64_t dv = tc::desc_add(dV0, (c % V_SLOTS) * V_BYTES);
+#pragma unroll
+          for (int s = 2 * part; s < 2 * part + 2; ++s)
+            tc::mma_ts(tmem + (part ? T_DS2 : T_DS), ta + s * 8, tc::desc_add(dv, s * 2 * OP_LBO), id_s,
+                       s > 2 * part);
           tc::mma_commit(&s_bar_s);
-          __threadfence_block();
-          atomicAdd(&s_issued, 1);
         }
       }
       bad = bad || !wait_bar(&s_bar_s, c & 1);
-      bad = __any_sync(0xffffffffu, bad);       // tcgen05.ld is warp-collective
+      bad = bad || !wait_flag(&s_ready, static_cast<int>(c) + 1);     // gamma(c)
+      bad = __any_sync(0xffffffffu, bad);
       if (!bad) {
         if (tid == 0) set_flag(&s_ps_done, static_cast<int>(c) + 1);
         uint32_t r0[16], r1[16], q0[16], q1[16];
-        tc::tmem_ld16(tmem + lane_addr + ds_col(c) + 32 * chalf, r0);
-        tc::tmem_ld16(tmem + lane_addr + ds_col(c) + 32 * chalf + 16, r1);
+        tc::tmem_ld16(tmem + lane_addr + T_DS + 32 * chalf, r0);
+        tc::tmem_ld16(tmem + lane_addr + T_DS + 32 * chalf + 16, r1);
         tc::tmem_ld16(tmem + lane_addr + T_DS2 + 32 * chalf, q0);
         tc::tmem_ld16(tmem + lane_addr + T_DS2 + 32 * chalf + 16, q1);
         tc::tmem_wait_ld();
-        if (wait_flag(&s_ready, static_cast<int>(c) + 1)) {   // gamma(c) in place
-          const float gam = s_gam[(c % GAM_SLOTS) * D + row];
+        const float gam = s_gam[(c % GAM_SLOTS) * D + row];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            Sv[e] = gam * Sv[e] + (__uint_as_float(r0[e]) + __uint_as_float(q0[e]));
-            Sv[e + 16] = gam * Sv[e + 16] + (__uint_as_float(r1[e]) + __uint_as_float(q1[e]));
-          }
-          // S buffer (c + 1) % 3 held S_{c-2}, which the output MMA of chunk c - 2 reads
-          if (c + 1 < nchunks && (c < 2 || wait_flag(&s_o_done, static_cast<int>(c) - 1)))
-            write_state_operand(c + 1);
+        for (int e = 0; e < 16; ++e) {
+          Sv[e] = gam * Sv[e] + (__uint_as_float(r0[e]) + __uint_as_float(q0[e]));
+          Sv[e + 16] = gam * Sv[e + 16] + (__uint_as_float(r1[e]) + __uint_as_float(q1[e]));
         }
+        // S(c) was read only by X(c), complete before Kb E'(c) was issued
+        if (c + 1 < nchunks) write_state_operand();
       }
       tc::fence_async_smem();
       tc::fence_before_sync();
@@ -1326,7 +1260,7 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
     if (tid == 0 || tid == 128 || tid == 32 * W_ISSUE) tc::mma_commit(&s_drain);
     tc::mbar_wait_bounded(&s_drain, 0, kWaitLimit);
     for (uint32_t k = 0; k < 2; ++k)
-      for (uint32_t i = 0; i < OA_SLOTS; ++i) tc::mbar_wait_bounded(&s_oa_bar[i], k, kWaitLimit);
+      for (uint32_t i = 0; i < KQA_SLOTS; ++i) tc::mbar_wait_bounded(&s_kqa_bar[i], k, kWaitLimit);
     if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
   }
   tc::fence_before_sync();

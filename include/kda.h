@@ -86,7 +86,7 @@ typedef enum kda_decay_kind {
  * tile) that walks the sequence's chunks, with only the chunk table as workspace
  * (16 bytes per chunk).  Without it the path runs as two kernels: a chunk-parallel
  * one that writes every chunk's operands of the state recurrence to the workspace
- * (74,240 bytes per chunk and value head) and a sequential one over each
+ * (57,856 bytes per chunk and value head) and a sequential one over each
  * sequence's chunks, which keeps the chunk-local work off the sequential path.
  * The two forms round the same operands the same way; their results agree to
  * the tolerance, not bit for bit. */

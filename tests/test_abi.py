@@ -188,13 +188,13 @@ def test_verify_and_fold_reject_bad_arguments_before_launch(lib):
 
 
 def test_compact_flag_shrinks_the_tensor_core_workspace(lib):
-    """The two-kernel tensor-core form stores 74,240 bytes of chain operands per chunk
+    """The two-kernel tensor-core form stores 57,856 bytes of chain operands per chunk
     and value head; the single-kernel form needs only the chunk table."""
     p = good(total_tokens=4096, num_seqs=2)
     c = good(total_tokens=4096, num_seqs=2, compact=True)
     assert lib.kda_prefill_uses_tensor_cores(ctypes.byref(c)) == 1
     full, small = ws_status(lib, p)[1], ws_status(lib, c)[1]
-    assert full - small >= (4096 // 64) * 8 * 74240
+    assert full - small >= (4096 // 64) * 8 * 57856
     assert small < 64 * 1024
     q = good()
     q.flags |= 16                                           # an unknown flag

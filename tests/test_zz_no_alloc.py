@@ -54,15 +54,15 @@ def test_no_alloc_matches_workspace_prefill_on_two_calls():
 
 @pytest.mark.gpu
 def test_no_alloc_uses_the_single_kernel_form_when_records_do_not_fit():
-    """4096 tokens x 16 value heads need about 69 MB of chunk records on the two-kernel
+    """6144 tokens x 16 value heads need about 92 MB of chunk records on the two-kernel
     tensor-core path, more than the scratch holds: the no-alloc entry runs the
     single-kernel form instead and matches the regular call."""
-    p = workloads.make_problem("no_alloc_big", num_seqs=2, lengths=[2048, 2048], num_k_heads=16,
-                               num_v_heads=16, d=128, qkv_dtype="bf16", state_dtype="f32",
-                               decay_kind="scalar", chunk=64, zero_state=False, num_slots=2,
-                               seed=35)
-    params = kda.make_params(num_seqs=2, num_k_heads=16, num_v_heads=16, d=128, num_slots=2,
-                             total_tokens=4096, per_channel=False)
+    p = workloads.make_problem("no_alloc_big", num_seqs=3, lengths=[2048, 2048, 2048],
+                               num_k_heads=16, num_v_heads=16, d=128, qkv_dtype="bf16",
+                               state_dtype="f32", decay_kind="scalar", chunk=64, zero_state=False,
+                               num_slots=3, seed=35)
+    params = kda.make_params(num_seqs=3, num_k_heads=16, num_v_heads=16, d=128, num_slots=3,
+                             total_tokens=6144, per_channel=False)
     assert kda.workspace_size(params) > _lib.KDA_NO_ALLOC_SCRATCH_BYTES
     t = torch_io.prefill_inputs(p, "cuda:0")
     pool_ref = t["state_pool"].clone()

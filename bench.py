@@ -60,13 +60,15 @@ def decode_algorithmic_bytes(dp) -> dict:
 
 
 def tc_executed_flops(p) -> dict:
-    """Tensor-core FLOPs the two tensor-core kernels issue per launch (d = 128, C = 64):
-    front per (chunk, value head) the A-GEMM (three passes for per-channel decay), X and Y;
-    chain per chunk and value tile of 64 columns [E; O] (K = 192) and K_end^T E."""
+    """Tensor-core FLOPs the two tensor-core kernels issue per launch (d = 128, C = 64), as
+    issued (an M = 128 MMA of which 64 rows are used counts in full): front per (chunk, value
+    head) the A-GEMM (three passes for per-channel decay) and the two M=128 N=64 K=64 products
+    K_end^T TB and [*; A_qk] TB; chain per chunk and value tile of 64 columns [K~; Q~] S
+    (K = 128), Kb E' and A1o E' (K = 64 each)."""
     chunks = sum((int(n) + 63) // 64 for n in p.lengths) * p.num_v_heads
     agemm = 2 * 128 * 64 * 128 * (3 if p.decay_kind == "per_channel" else 1)
-    front = agemm + 2 * 128 * 64 * 64 + 2 * 128 * 128 * 64
-    chain = 2 * (2 * 128 * 64 * 192 + 2 * 128 * 64 * 64)
+    front = agemm + 2 * (2 * 128 * 64 * 64)
+    chain = 2 * (2 * 128 * 64 * 128 + 2 * (2 * 128 * 64 * 64))
     return {"tc_front": float(front * chunks), "tc_chain": float(chain * chunks)}
 
 

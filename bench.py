@@ -297,8 +297,12 @@ def time_prefill(p, dev, steps, warmup):
 
 
 def time_prefill_e2e(p, dev, steps, warmup):
-    """Through the public API with host buffers: pinned H2D of the step's inputs, the call,
-    D2H of the outputs, all inside the timed region."""
+    """Through the public API with host buffers: every step uploads its inputs from pinned host
+    memory, makes the call and reads its outputs back into pinned host memory, all inside the
+    timed region.  Consecutive steps are double-buffered as a serving loop would run them:
+    step i's upload (one stream) overlaps step i - 1's call (the compute stream) and the
+    download of step i - 2's outputs (a third stream); the calls stay in order on the compute
+    stream, since each updates the state pool the next one reads."""
     import torch
     import gated_delta_rule_deltanet_gb300 as kda
     from workloads import torch_io
@@ -310,27 +314,54 @@ def time_prefill_e2e(p, dev, steps, warmup):
             "input_row_offsets": torch_io.index(p.offsets).pin_memory(),
             "slot_idx": torch_io.index(p.slot_idx).pin_memory()}
     pool = torch_io.tensor(p.pool, p.state_dtype, dev)
-    devb = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    devb = [{k: torch.empty_like(v, device=dev) for k, v in host.items()} for _ in range(2)]
     T, HV, d = p.total_tokens, p.num_v_heads, p.d_v
-    out = torch.empty((T, HV, d), dtype=torch.float32, device=dev)
-    out_host = torch.empty((T, HV, d), dtype=torch.float32).pin_memory()
+    out = [torch.empty((T, HV, d), dtype=torch.float32, device=dev) for _ in range(2)]
+    out_host = [torch.empty((T, HV, d), dtype=torch.float32).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    d2h = out_host[0].numel() * out_host[0].element_size()
+    params = kda.kda._prefill_params(devb[0]["q"], devb[0]["k"], devb[0]["v"], devb[0]["beta"],
+                                     devb[0]["log_decay"], devb[0]["input_row_offsets"],
+                                     devb[0]["slot_idx"], pool, p.chunk, p.scale, True, False)
+    ws = torch.empty(max(kda.workspace_size(params), 1), dtype=torch.uint8, device=dev)
+    comp = torch.cuda.current_stream(dev)
+    s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    up_done, comp_done, down_done = [None, None], [None, None], [None, None]
 
-    def step():
-        for k in host:
-            devb[k].copy_(host[k], non_blocking=True)
-        kda.prefill(**devb, state_pool=pool, chunk=p.chunk, scale=p.scale, out=out)
-        out_host.copy_(out, non_blocking=True)
+    def step(i):
+        b = i % 2
+        with torch.cuda.stream(s_up):
+            if comp_done[b] is not None:        # the call of step i - 2 has read devb[b]
+                s_up.wait_event(comp_done[b])
+            for k in host:
+                devb[b][k].copy_(host[k], non_blocking=True)
+            up_done[b] = torch.cuda.Event()
+            up_done[b].record(s_up)
+        comp.wait_event(up_done[b])
+        if down_done[b] is not None:            # out[b] of step i - 2 is downloaded
+            comp.wait_event(down_done[b])
+        kda.prefill(**devb[b], state_pool=pool, chunk=p.chunk, scale=p.scale, out=out[b],
+                    workspace=ws, stream=comp)
+        comp_done[b] = torch.cuda.Event()
+        comp_done[b].record(comp)
+        with torch.cuda.stream(s_down):
+            s_down.wait_event(comp_done[b])
+            out_host[b].copy_(out[b], non_blocking=True)
+            down_done[b] = torch.cuda.Event()
+            down_done[b].record(s_down)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record()
-    for _ in range(steps):
-        step()
-    end.record()
+    start.record(comp)
+    s_up.wait_stream(comp)                      # nothing of the timed steps starts before `start`
+    s_down.wait_stream(comp)
+    for i in range(steps):
+        step(i)
+    for e in down_done:
+        comp.wait_event(e)
+    end.record(comp)
     torch.cuda.synchronize()
     return start.elapsed_time(end) / steps, h2d, d2h
 

@@ -349,7 +349,9 @@ __global__ void __launch_bounds__(tcs::NT, 2)
 
   // ------------------------------------------------------------------ prep
   {                                             // L2 norms: 4 threads per row
-    const int i = tid >> 2, part = tid & 3;
+    // lanes l, l + 8, l + 16, l + 24 share row 8 warp + l: each 8-lane group of a 16-byte
+    // access reads 8 different rows, whose swizzled chunks fall on different banks
+    const int i = 8 * warp + (lane & 7), part = lane >> 3;
     float sk = 0.f, sq = 0.f;
 #pragma unroll
     for (int g8 = 0; g8 < 4; ++g8) {
@@ -362,10 +364,10 @@ __global__ void __launch_bounds__(tcs::NT, 2)
         sq += qx[e] * qx[e];
       }
     }
-    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-    sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+    sk += __shfl_xor_sync(0xffffffffu, sk, 8);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 8);
+    sk += __shfl_xor_sync(0xffffffffu, sk, 16);
+    sq += __shfl_xor_sync(0xffffffffu, sq, 16);
     if (part == 0) {
       sRK[i] = P.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
       sRQ[i] = (P.l2norm ? rsqrtf(sq + 1e-6f) : 1.f) * P.scale;
@@ -438,7 +440,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
   if constexpr (PERCH) {
     const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
     {                                           // K- (both halves) first: it reads the raw k rows
-      const int j = tid >> 2, qq = tid & 3;     // 4 threads per key row
+      const int j = 8 * warp + (lane & 7), qq = lane >> 3;   // 4 threads per key row
       const float rs = sRK[j];
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8) {
@@ -580,7 +582,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       }
     }
     {
-      const int j = tid >> 2, qq = tid & 3;     // 4 threads per key row
+      const int j = 8 * warp + (lane & 7), qq = lane >> 3;   // 4 threads per key row
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8) {
         const int cc = 32 * qq + 8 * g8;

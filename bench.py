@@ -95,7 +95,7 @@ PREFILL_STAGES = {
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from the ncu
 # capture summarised in profiles/tc_front_tc_chain_gdn_prefill.md; a kernel changed since
 # its capture has no entry (reported as null).
-NCU_TRAFFIC = {("tc_front", "gdn_prefill"): 319.59e6, ("tc_chain", "gdn_prefill"): 417.88e6,
+NCU_TRAFFIC = {("tc_front", "gdn_prefill"): 319.74e6, ("tc_chain", "gdn_prefill"): 417.88e6,
                ("conv_kernel", "gdn_prefill"): 358.74e6}
 
 

@@ -287,7 +287,9 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
 
     // ---------------------------------------------------------------- phase 1: prep
     {                                                   // L2 norms: 4 threads per row
-      const int i = tid >> 2, part = tid & 3;
+      // lanes l, l + 8, l + 16, l + 24 share row 8 warp + l, so that each 8-lane group of a
+      // 16-byte shared-memory access reads 8 rows on different banks
+      const int i = 8 * warp + (lane & 7), part = lane >> 3;
       float sk = 0.f, sq = 0.f;
 #pragma unroll
       for (int g8 = 0; g8 < 4; ++g8) {
@@ -300,10 +302,10 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
           sq += qx[e] * qx[e];
         }
       }
-      sk += __shfl_xor_sync(0xffffffffu, sk, 1);
-      sq += __shfl_xor_sync(0xffffffffu, sq, 1);
-      sk += __shfl_xor_sync(0xffffffffu, sk, 2);
-      sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 8);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 8);
+      sk += __shfl_xor_sync(0xffffffffu, sk, 16);
+      sq += __shfl_xor_sync(0xffffffffu, sq, 16);
       if (part == 0) {
         sRK[i] = P.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
         sRQ[i] = (P.l2norm ? rsqrtf(sq + 1e-6f) : 1.f) * P.scale;
@@ -423,7 +425,7 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
         tc::tmem_wait_st();
       }
       {                                                   // K-: 4 threads per key row
-        const int j = tid >> 2, qq = tid & 3;
+        const int j = 8 * warp + (lane & 7), qq = lane >> 3;   // lanes 8 apart, as above
         const float rs = sRK[j];
 #pragma unroll
         for (int g8 = 0; g8 < 4; ++g8) {

@@ -1118,6 +1118,12 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
       };
       for (uint32_t q = 0; q < min(nchunks, KQA_SLOTS); ++q) load_kqa(q);
       for (uint32_t c = 0; c < nchunks; ++c) {
+        // the slot of chunk c - 1 takes chunk c + 2 as soon as that chunk's output MMA is done
+        // (about when chunk c starts): two chunk periods ahead of its use
+        if (c >= 1 && c + 2 < nchunks) {
+          if (!wait_flag(&s_o_done, static_cast<int>(c))) break;
+          load_kqa(c + 2);
+        }
         // E'(c) in place (so X(c) is complete and its rows 0-63 consumed); o rows of c - 1
         // out, which keeps the completion barrier one phase ahead of its waiters
         if (!wait_flag(&s_e_ready, static_cast<int>(c) + 1)) break;
@@ -1129,11 +1135,6 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
         for (int s = 0; s < C / 16; ++s)
           tc::mma_ss(tmem + x_col(c, 0), tc::desc_add(da, s * 256), tc::desc_add(dv, s * 2 * OP_LBO), id_k, 1);
         tc::mma_commit(&s_bar_o);
-        // the slot of chunk c - 1 is free once its output MMA is done
-        if (c >= 1 && c - 1 + KQA_SLOTS < nchunks) {
-          if (!wait_flag(&s_o_done, static_cast<int>(c))) break;
-          load_kqa(c - 1 + KQA_SLOTS);
-        }
       }
     }
   } else if (warp < W_OPER) {

@@ -1,0 +1,89 @@
+"""The factorisation of the chunk form that the tensor-core prefill computes, written out in fp64
+numpy and checked against the oracle's token-by-token recurrence.
+
+Per chunk, in the state's stored orientation (S is d_k x d_v, rows = key channels), with G_i the
+cumulative log-decay from the chunk start through token i:
+
+  K~_i = k^_i exp(G_i),  Q~_i = s q^_i exp(G_i),  K_end_i = k^_i exp(G_last - G_i),  gam = exp(G_last)
+  A_kk[i, j] = beta_i <k^_i, k^_j exp(G_i - G_j)>  (j < i),   T = (I + A_kk)^-1,   TB = T diag(beta)
+  A_qk[i, j] = s <q^_i, k^_j exp(G_i - G_j)>        (j <= i)
+  Kb = K_end^T TB,   A1o = A_qk TB
+  E' = V - K~ S,   S' = diag(gam) S + Kb E',   O = Q~ S + A1o E'
+
+("You Could Have Come Up With Kimi Delta Attention", sec. 6.2-6.5: the corrections there are
+E = TB (V - K~ S), so W = TB K~ and U = TB V need never be formed.)  The additive write drops
+the prediction: A_kk = 0 and K~ S = 0.
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+
+def factorised(q, k, v, beta, g, S0, *, chunk, delta_rule=True, slip=None):
+    T, dk = q.shape
+    scale = 1.0 / np.sqrt(dk)
+    qn = q / np.sqrt(np.sum(q * q, axis=1, keepdims=True) + 1e-6)
+    kn = k / np.sqrt(np.sum(k * k, axis=1, keepdims=True) + 1e-6)
+    gg = g if g.ndim == 2 else np.repeat(g[:, None], dk, axis=1)
+    S = S0.copy()
+    o = np.zeros((T, v.shape[1]))
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(c0 + chunk, T))
+        kc, qc, vc, bc = kn[sl], qn[sl], v[sl], beta[sl]
+        n = kc.shape[0]
+        G = np.cumsum(gg[sl], axis=0)                      # [n, dk]
+        Kt = kc * np.exp(G) if delta_rule else np.zeros_like(kc)
+        Qt = scale * qc * np.exp(G)
+        Kend = kc * np.exp(G[-1] - G)
+        gam = np.exp(G[-1])
+        Akk = np.zeros((n, n))
+        Aqk = np.zeros((n, n))
+        for i in range(n):
+            for j in range(i + 1):
+                dec = np.exp(G[i] - G[j])
+                Aqk[i, j] = scale * np.dot(qc[i], kc[j] * dec)
+                if j < i and delta_rule:
+                    Akk[i, j] = bc[i] * np.dot(kc[i], kc[j] * dec)
+        TB = np.linalg.solve(np.eye(n) + Akk, np.diag(bc))
+        Kb = Kend.T @ TB                                   # [dk, n]
+        A1o = Aqk @ TB                                     # [n, n]
+        if slip == "transposed_A1o":
+            A1o = A1o.T
+        Ep = vc - Kt @ S                                   # [n, dv]
+        o[sl] = Qt @ S + A1o @ (vc if slip == "raw_v_in_output" else Ep)
+        S = (S if slip == "no_state_decay" else gam[:, None] * S) + Kb @ Ep
+    return o, S
+
+
+def inputs(seed, T, dk, dv, per_channel):
+    r = np.random.Generator(np.random.PCG64(seed))
+    q = r.standard_normal((T, dk))
+    k = r.standard_normal((T, dk))
+    v = r.standard_normal((T, dv))
+    beta = r.uniform(0.1, 1.0, T)
+    g = -r.uniform(0.0, 0.2, (T, dk) if per_channel else T)
+    S0 = r.standard_normal((dk, dv)) * 0.3
+    return q, k, v, beta, g, S0
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+@pytest.mark.parametrize("delta_rule", [True, False])
+@pytest.mark.parametrize("T,chunk", [(150, 64), (64, 64), (5, 16), (33, 16)])
+def test_factorisation_equals_the_recurrence(per_channel, delta_rule, T, chunk):
+    q, k, v, beta, g, S0 = inputs(T * 7 + chunk + 2 * per_channel + delta_rule, T, 16, 8,
+                                  per_channel)
+    o, S = factorised(q, k, v, beta, g, S0, chunk=chunk, delta_rule=delta_rule)
+    o_ref, S_ref = oracle.recurrence_py(q, k, v, beta, g, S0, delta_rule=delta_rule)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-11 * max(1.0, np.abs(o_ref).max()))
+    np.testing.assert_allclose(S, S_ref, rtol=0, atol=1e-11 * max(1.0, np.abs(S_ref).max()))
+
+
+@pytest.mark.parametrize("slip", ["no_state_decay", "raw_v_in_output", "transposed_A1o"])
+def test_a_one_term_slip_is_caught(slip):
+    """Each slip planted in the factorisation (the state's decay left out of the update, V in
+    place of E' in the output, A1o transposed) fails the comparison above."""
+    q, k, v, beta, g, S0 = inputs(3, 70, 16, 8, False)
+    o_ref, S_ref = oracle.recurrence_py(q, k, v, beta, g, S0)
+    o, S = factorised(q, k, v, beta, g, S0, chunk=64, slip=slip)
+    assert max(np.abs(o - o_ref).max(), np.abs(S - S_ref).max()) > 1e-3

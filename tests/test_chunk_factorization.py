@@ -13,6 +13,9 @@ cumulative log-decay from the chunk start through token i:
 ("You Could Have Come Up With Kimi Delta Attention", sec. 6.2-6.5: the corrections there are
 E = TB (V - K~ S), so W = TB K~ and U = TB V need never be formed.)  The additive write drops
 the prediction: A_kk = 0 and K~ S = 0.
+
+The compact single-kernel form folds both products into one left operand instead:
+  [E; O] = [TB | -W; A_qk TB | Q~ - A_qk W] [V; S],   W = TB K~,   S' = diag(gam) S + K_end^T E.
 """
 import numpy as np
 import pytest
@@ -56,6 +59,38 @@ def factorised(q, k, v, beta, g, S0, *, chunk, delta_rule=True, slip=None):
     return o, S
 
 
+def folded(q, k, v, beta, g, S0, *, chunk, delta_rule=True):
+    """The compact kernel's single product per chunk, same definitions as above."""
+    T, dk = q.shape
+    scale = 1.0 / np.sqrt(dk)
+    qn = q / np.sqrt(np.sum(q * q, axis=1, keepdims=True) + 1e-6)
+    kn = k / np.sqrt(np.sum(k * k, axis=1, keepdims=True) + 1e-6)
+    gg = g if g.ndim == 2 else np.repeat(g[:, None], dk, axis=1)
+    S = S0.copy()
+    o = np.zeros((T, v.shape[1]))
+    for c0 in range(0, T, chunk):
+        sl = slice(c0, min(c0 + chunk, T))
+        kc, qc, vc, bc = kn[sl], qn[sl], v[sl], beta[sl]
+        n = kc.shape[0]
+        G = np.cumsum(gg[sl], axis=0)
+        Kt = kc * np.exp(G) if delta_rule else np.zeros_like(kc)
+        Qt = scale * qc * np.exp(G)
+        Kend = kc * np.exp(G[-1] - G)
+        dec = np.exp(G[:, None, :] - G[None, :, :])        # [i, j, channel]
+        Akk = np.tril(bc[:, None] * np.einsum("ic,jc,ijc->ij", kc, kc, dec), -1)
+        Aqk = np.tril(scale * np.einsum("ic,jc,ijc->ij", qc, kc, dec))
+        if not delta_rule:
+            Akk[:] = 0.0
+        TB = np.linalg.solve(np.eye(n) + Akk, np.diag(bc))
+        W = TB @ Kt
+        left = np.block([[TB, -W], [Aqk @ TB, Qt - Aqk @ W]])          # [2n, n + dk]
+        EO = left @ np.vstack([vc, S])
+        E, O = EO[:n], EO[n:]
+        o[sl] = O
+        S = np.exp(G[-1])[:, None] * S + Kend.T @ E
+    return o, S
+
+
 def inputs(seed, T, dk, dv, per_channel):
     r = np.random.Generator(np.random.PCG64(seed))
     q = r.standard_normal((T, dk))
@@ -74,6 +109,16 @@ def test_factorisation_equals_the_recurrence(per_channel, delta_rule, T, chunk):
     q, k, v, beta, g, S0 = inputs(T * 7 + chunk + 2 * per_channel + delta_rule, T, 16, 8,
                                   per_channel)
     o, S = factorised(q, k, v, beta, g, S0, chunk=chunk, delta_rule=delta_rule)
+    o_ref, S_ref = oracle.recurrence_py(q, k, v, beta, g, S0, delta_rule=delta_rule)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-11 * max(1.0, np.abs(o_ref).max()))
+    np.testing.assert_allclose(S, S_ref, rtol=0, atol=1e-11 * max(1.0, np.abs(S_ref).max()))
+
+
+@pytest.mark.parametrize("per_channel", [False, True])
+@pytest.mark.parametrize("delta_rule", [True, False])
+def test_folded_form_equals_the_recurrence(per_channel, delta_rule):
+    q, k, v, beta, g, S0 = inputs(11 + 2 * per_channel + delta_rule, 150, 16, 8, per_channel)
+    o, S = folded(q, k, v, beta, g, S0, chunk=64, delta_rule=delta_rule)
     o_ref, S_ref = oracle.recurrence_py(q, k, v, beta, g, S0, delta_rule=delta_rule)
     np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-11 * max(1.0, np.abs(o_ref).max()))
     np.testing.assert_allclose(S, S_ref, rtol=0, atol=1e-11 * max(1.0, np.abs(S_ref).max()))

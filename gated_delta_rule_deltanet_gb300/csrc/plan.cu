@@ -13,6 +13,7 @@ size_t plan_layout(const Problem& P, char* base, size_t off, PlanView* out) {
   v.info = reinterpret_cast<int32_t*>(take(4 * sizeof(int32_t)));
   v.seq_chunk0 = reinterpret_cast<int32_t*>(take((static_cast<size_t>(P.num_seqs) + 1) * 4));
   v.chunks = reinterpret_cast<ChunkInfo*>(take(static_cast<size_t>(plan_max_chunks(P)) * sizeof(ChunkInfo)));
+  v.skip = reinterpret_cast<int32_t*>(take(static_cast<size_t>(P.num_seqs) * P.HV * sizeof(int32_t)));
   if (out) *out = v;
   return off;
 }
@@ -24,6 +25,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem P, PlanView 
   __shared__ int s_scan[kPlanThreads];
   const int B = P.num_seqs, C = P.chunk, tid = threadIdx.x;
   if (tid == 0) s_bad = 0;
+  for (int64_t u = tid; u < static_cast<int64_t>(B) * P.HV; u += kPlanThreads) plan.skip[u] = 0;
   __syncthreads();
   if (tid == 0 && (P.offsets[0] != 0u || static_cast<int64_t>(P.offsets[B]) != P.T)) atomicOr(&s_bad, 1);
   for (int b = tid; b < B; b += kPlanThreads) {

@@ -21,6 +21,9 @@ struct PlanView {
   int32_t* info;        // [0] chunks in the table, [1] 1 if the batch is valid
   int32_t* seq_chunk0;  // [B + 1] first chunk of each sequence (prefix sums)
   ChunkInfo* chunks;    // [max_chunks]
+  int32_t* skip;        // [B * HV] nonzero: a kernel found this (sequence, value head) outside
+                        // the tensor-core path's domain; the kernels that write o and the
+                        // state pool leave it untouched (zeroed by the plan kernel)
 };
 
 inline int plan_max_chunks(const Problem& P) {

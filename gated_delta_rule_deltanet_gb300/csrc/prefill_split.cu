@@ -66,7 +66,7 @@ constexpr int NTO = 64;     // chain kernel: output warps 14-15 (TMEM lanes 64-1
 constexpr int NTC = NT + NTD + 64 + NTO;   // + warp 12, whose lane 0 issues the output MMA,
                                            // and warp 13, which only pads to warp 14
 constexpr uint32_t kWaitLimit = 1u << 22;
-constexpr float kMaxHalfChunkDecay = 80.0f;
+constexpr float kMaxHalfChunkDecay = 80.0f;   // scalar decay: anchored factors in fp32
 
 // record of one (chunk, value head) in the workspace
 //   BLOB: piece p (0..3) of thread t at (p * NT + t) * 16; thread t (key channel
@@ -90,10 +90,37 @@ constexpr uint32_t TB_LBO = 1024, TB_SBO = 128;      // TB (N = column j, K = ro
 static_assert(REC_BYTES % 16 == 0 && REC_KQ % 16 == 0 && KQA_BYTES % 16 == 0,
               "records must stay 16-byte aligned");
 
-// per-chunk vectors of the front kernel (byte offsets inside its SMALL area)
+// per-chunk vectors of the scalar-decay front kernel (byte offsets inside its SMALL area)
 constexpr uint32_t O_GS = 0, O_BETA = 256, O_RK = 512, O_RQ = 768, O_EG = 1024, O_EGL = 1280,
-                   O_GAM = 1536, O_GA = 2048, O_EA = 2560, O_KF = 2816, O_EL = 3072,
-                   SMALL_BYTES = 3584;
+                   O_GAM = 1536, O_EA = 2560, O_KF = 2816, SMALL_BYTES = 3584;
+
+// Per-channel decay: the chunk's 64 tokens form four sub-blocks of 16.  Rows of sub-block I
+// carry their decay relative to the last token before it (G_ref(I): 0 for I = 0, else
+// G_{16I-1}), so that for a key j of an earlier sub-block J < I
+//   exp(G_i - G_j) = exp(G_i - G_ref(I)) * exp(G_ref(I) - G_j),   both factors <= 1,
+// and fp16 operands hold them whatever the decay.  Pairs inside one sub-block use the column
+// factor exp(G_ref(J) - G_j) >= 1, which fp16 holds as long as a channel decays by at most
+// kSubBlockDecay nats from the reference to any token of the sub-block; the (sub-block,
+// channel) pairs above it are summed exactly in fp32 instead (exp per pair).  The row
+// operand is scaled by 2^8 and the column operands by 2^-8 (the product is unchanged), which
+// keeps the small row factors of a strongly decaying channel out of fp16's subnormal range.
+constexpr float kSubBlockDecay = 12.0f;
+constexpr float kRowScale = 256.0f, kColScale = 1.0f / 256.0f;
+// The factors above are <= 1 only for a non-increasing cumulative log-decay: a per-channel
+// log-decay above this bound (a gate above 1) is outside the tensor-core path's domain.
+constexpr float kMaxLogDecay = 1.0f / 64.0f;
+// per-chunk vectors of the per-channel front kernel (byte offsets inside its SMALL area):
+//   BETA, RK, RQ  beta, 1/|k|, scale/|q| per token
+//   GB   G at tokens 15, 31, 47, 63 per channel (the sub-block boundaries)
+//   ES   exp(G_15), exp(G_31), exp(G_47) (K~ and Q~ of sub-blocks 1-3 from their row factors)
+//   W    diagonal column factor exp(G_ref(J) - G_end(J)) of sub-block J (0 for exact channels)
+//   F    exp(G_ref(I) - G_end(J)) for (I, J) = (2, 0), (3, 0), (3, 1) (I = J + 1 needs none)
+//   MASK exact channels: 4 words of 32 channels per sub-block
+constexpr uint32_t P_BETA = 0, P_RK = 256, P_RQ = 512, P_GB = 768, P_ES = P_GB + 4 * 512,
+                   P_W = P_ES + 3 * 512, P_F = P_W + 4 * 512, P_MASK = P_F + 3 * 512,
+                   SMALL_PC_BYTES = P_MASK + 4 * 4 * 4;
+// the off-diagonal column operand holds the six (I, J) pairs J < I, 16 rows each
+__host__ __device__ constexpr int off_slot(int I, int J) { return I * (I - 1) / 2 + J; }
 
 // the fp32 solve tiles (A_kk and T, 64 x 64): element (r, c) at sidx(r, c), whose 4-float
 // groups are permuted by r % 8 so that column-wise and row-wise 16-byte accesses both
@@ -126,37 +153,39 @@ struct FrontMap<false> {
   static constexpr uint32_t TBT = LMAT + 128 * 64 * 2;  // TB 64 x 64 fp16, MN-major
   static constexpr uint32_t BYTES = TBT + 64 * 64 * 2;
   static constexpr uint32_t KEA = R2;                   // K_end (MN-major)
+  static constexpr uint32_t BETA = SMALL + O_BETA, RK = SMALL + O_RK, RQ = SMALL + O_RQ;
 };
 
-// Per-channel decay: TMA copies stage the raw k and q rows (the 128-byte swizzled layout
-// of the scalar path) and the log-decay rows (four 32-channel quarters, each 64 rows of
-// 128 bytes, swizzled the same way).  The A-GEMM operands are the normalised, decayed rows
-// as split bf16: [K+; Q+] high halves overwrite the raw rows in place, its low halves go to
-// tensor memory, K- (both halves) to BK | BKLO.  Once the A-GEMM is done, K~ and Q~ are
-// rebuilt from the two halves of [K+; Q+] and K_end from K-, so the staged rows, the
-// log-decay and K- can all be reused: every region below serves several phases, which keeps
-// two CTAs per SM.  K~ and Q~ go straight to the record.
+// Per-channel decay: TMA copies stage the raw k and q rows (the 128-byte swizzled layout of
+// the scalar path) and the log-decay rows (four 32-channel quarters, each 64 rows of 128
+// bytes, swizzled the same way).  The log-decay becomes G in place; the row operand R
+// (fp16) overwrites the raw rows in place; once every thread holds its G pieces, the
+// diagonal column operand goes over G and the off-diagonal one beside it.  After the A-GEMM
+// the solve tiles reuse both column operands and TB / [*; A_qk] the rows.  K_end lives in
+// tensor memory.
 template <>
 struct FrontMap<true> {
   static constexpr uint32_t AK_HALF = 128 * 128;
-  static constexpr uint32_t RAW = 0;                    // raw k | q -> [K+; Q+] high halves;
-                                                        // then TB (half 0 k rows), A_qk (half 1
-                                                        // k rows), Q~ in place (q rows)
-  static constexpr uint32_t S_G = RAW + 2 * AK_HALF;    // log-decay -> exp(G - G_a); then K_end
-  static constexpr uint32_t SMALL = S_G + C * D * 4;
-  static constexpr uint32_t BK = SMALL + SMALL_BYTES;   // K- high | low halves; then the solve
-  static constexpr uint32_t BKLO = BK + 64 * 128 * 2;   // tiles
-  static constexpr uint32_t R2 = BK;
-  static constexpr uint32_t BYTES = R2 + SOL_BYTES;
+  static constexpr uint32_t RAW = 0;                    // raw k | q -> R; then TB, [*; A_qk]
+  static constexpr uint32_t S_G = RAW + 2 * AK_HALF;    // log-decay -> G -> C_diag; then solve
+  static constexpr uint32_t CD = S_G;                   // C_diag 64 x 128 fp16, K-major
+  static constexpr uint32_t CO = S_G + C * D * 4;       // C_off 96 x 128 fp16, K-major
+  static constexpr uint32_t SMALL = CO + 6 * 16 * D * 2;
+  static constexpr uint32_t BYTES = SMALL + SMALL_PC_BYTES;
+  static constexpr uint32_t R2 = S_G;
   static constexpr uint32_t TBT = RAW;
   static constexpr uint32_t LMAT = RAW + AK_HALF - 64 * 64 * 2;   // rows 64-127: half 1 k rows
-  static constexpr uint32_t KEA = S_G;
-  static_assert(R2 + 2 * SOL_TILE == BKLO + 64 * 128 * 2, "solve tiles cover the K- halves");
+  static constexpr uint32_t BETA = SMALL + P_BETA, RK = SMALL + P_RK, RQ = SMALL + P_RQ;
+  static_assert(R2 + SOL_BYTES <= SMALL, "solve tiles inside the consumed column operands");
+  static_assert(CD + C * D * 2 <= CO, "diagonal column operand inside the consumed G");
 };
 
-// front TMEM columns: A_kk/A_qk (second issuer's half of K in F_X), then Kb | A1o; the low
-// half of [K+; Q+] in F_ALO
-constexpr uint32_t F_A = 0, F_X = 64, F_ALO = 128, F_COLS = 256;
+// front TMEM columns.  Scalar decay: A_kk/A_qk (second issuer's half of K in F_X), then
+// Kb | A1o.  Per-channel decay: the diagonal products (F_D, 64 columns: sub-block J at
+// 16 J) and the off-diagonal ones (F_O, 96 columns: pair (I, J) at 16 off_slot(I, J)), then
+// Kb | A1o over them; K_end^T (lane = channel, 64 tokens as fp16 pairs) at F_KE.
+constexpr uint32_t F_A = 0, F_X = 64, F_D = 0, F_O = 64, F_KE = 160, F_COLS = 256;
+static_assert(F_O + 96 <= F_KE && F_KE + 32 <= F_COLS, "front tensor-memory columns");
 
 // chain shared memory (MN-major operands: core matrices of 8 K-rows x 8 value columns,
 // value-column groups adjacent, K groups 1024 bytes apart).  A slot of the KQA ring holds a
@@ -207,10 +236,17 @@ __device__ __forceinline__ void front_issue_loads(const Problem& P, unsigned cha
   if (tid < C) {
     const bool live = tid < n;
     const int64_t t = live ? t0 + tid : t0;
-    tc::cp_async4(sb + M::SMALL + O_BETA + tid * 4, P.beta + t * HV + h, live ? 4u : 0u);
-    if (!PERCH) tc::cp_async4(sb + M::SMALL + O_GS + tid * 4, P.g + t * HV + h, live ? 4u : 0u);
+    tc::cp_async4(sb + M::BETA + tid * 4, P.beta + t * HV + h, live ? 4u : 0u);
+    if (!PERCH) tc::cp_async4(sb + FrontMap<false>::SMALL + O_GS + tid * 4, P.g + t * HV + h, live ? 4u : 0u);
   }
   tc::cp_async_commit();
+}
+
+__device__ __forceinline__ void load8(float* x, const float* p) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
 // One CTA per (chunk, value head): everything of the chunk that does not depend on the
@@ -224,16 +260,18 @@ __global__ void __launch_bounds__(tcs::NT, 2)
                     const __grid_constant__ CUtensorMap tmg) {
   using namespace tcs;
   using M = FrontMap<PERCH>;
+  using MS = FrontMap<false>;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the swizzled operand needs a 1024-byte aligned base; the launch adds 1 KB of slack
   unsigned char* const smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ uint64_t s_bar;                    // MMAs issued by thread 0
   __shared__ uint64_t s_bar2;                   // MMAs issued by thread 32
-  __shared__ uint64_t s_ld;                     // TMA copies of k and q (scalar decay)
+  __shared__ uint64_t s_ld;                     // TMA copies of k and q (and g)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_range;
-  __shared__ int s_anchored;
+  __shared__ int s_range;                       // per-channel: a log-decay above kMaxLogDecay
+  __shared__ int s_anchored;                    // scalar: anchored factors in range
+  __shared__ int s_anyslow;                     // per-channel: some pair summed exactly
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gc = blockIdx.x, h = blockIdx.y;
@@ -249,26 +287,23 @@ __global__ void __launch_bounds__(tcs::NT, 2)
   constexpr bool delta = DELTA;
   unsigned char* rec = records + (static_cast<int64_t>(gc) * HV + h) * static_cast<int64_t>(REC_BYTES);
 
-  float* sGs = reinterpret_cast<float*>(smem + M::SMALL + O_GS);
-  float* sBeta = reinterpret_cast<float*>(smem + M::SMALL + O_BETA);
-  float* sRK = reinterpret_cast<float*>(smem + M::SMALL + O_RK);
-  float* sRQ = reinterpret_cast<float*>(smem + M::SMALL + O_RQ);
-  float* sEG = reinterpret_cast<float*>(smem + M::SMALL + O_EG);
-  float* sEGL = reinterpret_cast<float*>(smem + M::SMALL + O_EGL);
-  float* sGam = reinterpret_cast<float*>(smem + M::SMALL + O_GAM);
-  float* sGA = reinterpret_cast<float*>(smem + M::SMALL + O_GA);
-  float* sEA = reinterpret_cast<float*>(smem + M::SMALL + O_EA);
-  float* sKF = reinterpret_cast<float*>(smem + M::SMALL + O_KF);
-  float* sEL = reinterpret_cast<float*>(smem + M::SMALL + O_EL);
+  float* sBeta = reinterpret_cast<float*>(smem + M::BETA);
+  float* sRK = reinterpret_cast<float*>(smem + M::RK);
+  float* sRQ = reinterpret_cast<float*>(smem + M::RQ);
   float* sA = reinterpret_cast<float*>(smem + M::R2);
   float* sT = reinterpret_cast<float*>(smem + M::R2 + SOL_TILE);
   float* sX = reinterpret_cast<float*>(smem + M::R2 + 2 * SOL_TILE);
-  constexpr uint32_t KEA = M::KEA;              // K_end (MN-major)
+  // scalar decay only
+  float* sGs = reinterpret_cast<float*>(smem + MS::SMALL + O_GS);
+  float* sEG = reinterpret_cast<float*>(smem + MS::SMALL + O_EG);
+  float* sEGL = reinterpret_cast<float*>(smem + MS::SMALL + O_EGL);
+  float* sGam = reinterpret_cast<float*>(smem + MS::SMALL + O_GAM);
+  float* sEA = reinterpret_cast<float*>(smem + MS::SMALL + O_EA);
+  float* sKF = reinterpret_cast<float*>(smem + MS::SMALL + O_KF);
   constexpr uint32_t M_RAW = PERCH ? FrontMap<true>::RAW : 0u;     // raw k | q (per-channel)
   constexpr uint32_t M_SG = PERCH ? FrontMap<true>::S_G : 0u;      // staged log-decay
   constexpr uint32_t M_AK = PERCH ? 0u : FrontMap<false>::AK;      // raw k | q (scalar)
-  const int64_t bt = (static_cast<int64_t>(gc) * HV + h) * static_cast<int64_t>(REC_BYTES);
-  uint4* blob = reinterpret_cast<uint4*>(records + bt + REC_BLOB) + tid;  // piece p at [p * NT]
+  uint4* blob = reinterpret_cast<uint4*>(rec + REC_BLOB) + tid;    // piece p at [p * NT]
 
   front_issue_loads<PERCH>(P, smem, t0, n, kh, h, tid);
   if (warp == 0) {
@@ -282,6 +317,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
     tc::fence_mbar_init();
     s_abort = 0;
     s_range = 0;
+    s_anyslow = 0;
     {                                           // k and q: both 64-channel halves, 64 rows each
       const uint32_t sb = tc::smem_u32(smem + (PERCH ? M_RAW : M_AK));
       const int32_t row0 = static_cast<int32_t>(t0);
@@ -306,13 +342,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
   tc::fence_after_sync();
   const uint32_t tmem = s_tmem;
   uint32_t phase = 0, phase2 = 0;
-  auto mma_wait = [&]() {
-    const bool ok = tc::mbar_wait_bounded(&s_bar, phase & 1, kWaitLimit);
-    phase ^= 1;
-    if (!ok) s_abort = 1;
-    tc::fence_after_sync();
-  };
-  auto mma_wait2 = [&]() {                      // the second issuer's group as well
+  auto mma_wait2 = [&]() {                      // both issuers' groups
     const bool ok = tc::mbar_wait_bounded(&s_bar, phase & 1, kWaitLimit) &&
                     tc::mbar_wait_bounded(&s_bar2, phase2 & 1, kWaitLimit);
     phase ^= 1;
@@ -375,267 +405,352 @@ __global__ void __launch_bounds__(tcs::NT, 2)
   }
   if constexpr (PERCH) {
     float* sG = reinterpret_cast<float*>(smem + M::S_G);
-    if (tid < D) {
-      // channel tid: inclusive cumsum G, then exp(G - G_a) in place (anchor G_a at the
-      // chunk's middle token); exp(G_a) and exp(G_last) go to the small arrays
-      float acc = 0.f, gmin = 0.f, gmax = -3.0e38f;
+    float* sGB = reinterpret_cast<float*>(smem + M::SMALL + P_GB);
+    float* sES = reinterpret_cast<float*>(smem + M::SMALL + P_ES);
+    float* sW = reinterpret_cast<float*>(smem + M::SMALL + P_W);
+    float* sF = reinterpret_cast<float*>(smem + M::SMALL + P_F);
+    uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + M::SMALL + P_MASK);
+    {
+      // ---------------------------------------------------------------- cumulative log-decay
+      // thread = (channel c, token half hh): each half sums its 32 tokens, the second half
+      // then adds the first half's total
+      const int c = tid & 127, hh = tid >> 7;
+      float gv[32];
+      bool rise = false;
 #pragma unroll
-      for (int i0 = 0; i0 < C; i0 += 16) {
-        float gv[16];
+      for (int e = 0; e < 32; ++e) gv[e] = sG[g_off(32 * hh + e, c)];
+      float acc = 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) gv[e] = sG[g_off(i0 + e, tid)];
+      for (int e = 0; e < 32; ++e) {
+        rise = rise || gv[e] > kMaxLogDecay;
+        acc += gv[e];
+        gv[e] = acc;
+      }
+      float m0 = gv[0], m1 = gv[16];            // lowest G of each of the half's sub-blocks
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          acc += gv[e];
-          gmin = fminf(gmin, acc);
-          gmax = fmaxf(gmax, acc);
-          sG[g_off(i0 + e, tid)] = acc;
+      for (int e = 1; e < 16; ++e) {
+        m0 = fminf(m0, gv[e]);
+        m1 = fminf(m1, gv[16 + e]);
+      }
+      if (rise) s_range = 1;
+      if (hh == 0) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) sG[g_off(e, c)] = gv[e];
+        sGB[c] = gv[15];
+        sGB[128 + c] = gv[31];
+      }
+      __syncthreads();
+      if (hh == 1) {
+        const float off = sGB[128 + c];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          gv[e] += off;
+          sG[g_off(32 + e, c)] = gv[e];
         }
+        m0 += off;
+        m1 += off;
+        sGB[256 + c] = gv[15];
+        sGB[384 + c] = gv[31];
       }
-      const float ga = sG[g_off((n - 1) / 2, tid)];
-      if (fmaxf(gmax - ga, ga - gmin) > kMaxHalfChunkDecay) s_range = 1;
-#pragma unroll
-      for (int i0 = 0; i0 < C; i0 += 16) {
-        float gv[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) gv[e] = sG[g_off(i0 + e, tid)];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) sG[g_off(i0 + e, tid)] = __expf(gv[e] - ga);
+      __syncthreads();
+      // sub-blocks 2 hh and 2 hh + 1: a channel whose decay from the sub-block's reference to
+      // any of its tokens exceeds kSubBlockDecay is summed exactly on the diagonal
+      const float g15 = sGB[c], g31 = sGB[128 + c], g47 = sGB[256 + c], g63 = sGB[384 + c];
+      const float ref0 = hh == 0 ? 0.f : g31, ref1 = hh == 0 ? g15 : g47;
+      const float end1 = hh == 0 ? g31 : g63;
+      const bool slow0 = ref0 - m0 > kSubBlockDecay, slow1 = ref1 - m1 > kSubBlockDecay;
+      const uint32_t b0 = __ballot_sync(0xffffffffu, slow0), b1 = __ballot_sync(0xffffffffu, slow1);
+      if (lane == 0) {
+        sMask[(2 * hh) * 4 + (warp & 3)] = b0;
+        sMask[(2 * hh + 1) * 4 + (warp & 3)] = b1;
+        if (b0 | b1) s_anyslow = 1;
       }
-      sGam[tid] = __expf(acc);
-      sGA[tid] = __expf(ga);
-      sEL[tid] = __expf(acc - ga);              // exp(G_last - G_a)
-    }
-  } else if (warp == 0) {                       // scalar: warp scan of 64 values
-    const float g0 = sGs[2 * lane], g1 = sGs[2 * lane + 1];
-    float s = g0 + g1;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, s, off);
-      if (lane >= off) s += y;
-    }
-    const float gl = __shfl_sync(0xffffffffu, s, 31);
-    sGs[2 * lane] = s - g1;
-    sGs[2 * lane + 1] = s;
-    sEG[2 * lane] = __expf(s - g1);
-    sEG[2 * lane + 1] = __expf(s);
-    sEGL[2 * lane] = __expf(gl - (s - g1));
-    sEGL[2 * lane + 1] = __expf(gl - s);
-    const float gam = __expf(gl);
-    sGam[lane] = gam; sGam[lane + 32] = gam; sGam[lane + 64] = gam; sGam[lane + 96] = gam;
-    // anchored factors exp(G_i - G_a), exp(G_a - G_j), anchor mid-chunk, so that
-    // exp(G_i - G_j) is a product of two per-token values while both stay finite
-    const int am = (n - 1) / 2;
-    const float ga = __shfl_sync(0xffffffffu, (am & 1) ? s : s - g1, am >> 1);
-    const float d0 = (s - g1) - ga, d1 = s - ga;
-    const bool ok = __all_sync(0xffffffffu, fmaxf(fabsf(d0), fabsf(d1)) <= kMaxHalfChunkDecay);
-    sEA[2 * lane] = __expf(d0);
-    sEA[2 * lane + 1] = __expf(d1);
-    sKF[2 * lane] = __expf(-d0);
-    sKF[2 * lane + 1] = __expf(-d1);
-    if (lane == 0) s_anchored = ok ? 1 : 0;
-  }
-  __syncthreads();
-  if (!PERCH && tid < C) sKF[tid] *= sRK[tid];
-  if constexpr (PERCH) {
-    const float* sG = reinterpret_cast<const float*>(smem + M::S_G);
-    {                                           // K- (both halves) first: it reads the raw k rows
-      const int j = 8 * warp + (lane & 7), qq = lane >> 3;   // 4 threads per key row
-      const float rs = sRK[j];
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        const int cc = 32 * qq + 8 * g8;
-        float x[8];
-        tc::bf16x8_load(kq_piece(false, j, cc), x);
-        const float4 g0 = *reinterpret_cast<const float4*>(sG + g_off(j, cc));
-        const float4 g1 = *reinterpret_cast<const float4*>(sG + g_off(j, cc + 4));
-        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const float v0 = x[e] * rs * __fdividef(1.f, f[e]);
-          const float v1 = x[e + 1] * rs * __fdividef(1.f, f[e + 1]);
-          hi[e / 2] = tc::pack_bf16x2(v0, v1);
-          const float h0 = __uint_as_float(hi[e / 2] << 16);
-          const float h1 = __uint_as_float(hi[e / 2] & 0xffff0000u);
-          lo[e / 2] = tc::pack_bf16x2(v0 - h0, v1 - h1);
-        }
-        *reinterpret_cast<uint4*>(smem + M::BK + tc::cm_offset(j, cc, 128, tc::dense_sbo(D))) =
-            make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(smem + M::BKLO + tc::cm_offset(j, cc, 128, tc::dense_sbo(D))) =
-            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      sW[(2 * hh) * 128 + c] = slow0 ? 0.f : __expf(ref0 - ref1);   // the end of 2 hh is ref1
+      sW[(2 * hh + 1) * 128 + c] = slow1 ? 0.f : __expf(ref1 - end1);
+      if (hh == 0) {
+        sES[c] = __expf(g15);
+        sES[128 + c] = __expf(g31);
+        sF[c] = __expf(g31 - g15);              // sub-block 0 seen from sub-block 2
+      } else {
+        sES[256 + c] = __expf(g47);
+        sF[128 + c] = __expf(g47 - g15);        // sub-block 0 seen from sub-block 3
+        sF[256 + c] = __expf(g47 - g31);        // sub-block 1 seen from sub-block 3
+        reinterpret_cast<float*>(rec + REC_GAM)[c] = __expf(g63);
       }
-    }
-    __syncthreads();
-    {                                           // [K+; Q+]: high halves over the raw rows, low to TMEM
-      const int i = row < C ? row : row - C;
-      const float rs = row < C ? sRK[i] : sRQ[i];
-      uint32_t lo[32];
+      // K_end = k^ exp(G_last - G_j) of this thread's 32 tokens in channel c, to tensor
+      // memory (lane = channel c, two tokens per column): the A operand of K_end^T TB
+      uint32_t w[16];
 #pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) {
-        const int cc = 64 * chalf + 8 * g8;
-        unsigned char* piece = const_cast<unsigned char*>(kq_piece(row >= C, i, cc));
-        float x[8];
-        tc::bf16x8_load(piece, x);
-        const float4 g0 = *reinterpret_cast<const float4*>(sG + g_off(i, cc));
-        const float4 g1 = *reinterpret_cast<const float4*>(sG + g_off(i, cc + 4));
-        const float f[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-        uint32_t hi[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const float v0 = x[e] * rs * f[e], v1 = x[e + 1] * rs * f[e + 1];
-          hi[e / 2] = tc::pack_bf16x2(v0, v1);
-          const float h0 = __uint_as_float(hi[e / 2] << 16);
-          const float h1 = __uint_as_float(hi[e / 2] & 0xffff0000u);
-          lo[4 * g8 + e / 2] = tc::pack_bf16x2(v0 - h0, v1 - h1);
-        }
-        *reinterpret_cast<uint4*>(piece) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      for (int e = 0; e < 32; e += 2) {
+        const int j = 32 * hh + e;
+        const float k0 = tc::bf16_at(smem, kq_off(false, j, c), c & 7) * sRK[j] * __expf(g63 - gv[e]);
+        const float k1 = tc::bf16_at(smem, kq_off(false, j + 1, c), c & 7) * sRK[j + 1] *
+                         __expf(g63 - gv[e + 1]);
+        w[e / 2] = tc::pack_f16x2(k0, k1);
       }
-      uint32_t l0[16], l1[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        l0[e] = lo[e];
-        l1[e] = lo[16 + e];
-      }
-      tc::tmem_st16(tmem + lane_addr + F_ALO + 32 * chalf, l0);
-      tc::tmem_st16(tmem + lane_addr + F_ALO + 32 * chalf + 16, l1);
+      tc::tmem_st16(tmem + lane_addr + F_KE + 16 * hh, w);
       tc::tmem_wait_st();
     }
-  }
-  tc::fence_async_smem();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
+    __syncthreads();
 
-  // ------------------------------------------------------------------ A-GEMM
-  // two issuing threads (one issues a tcgen05.mma only about every 100 cycles), the second
-  // into the X columns, which are free until A has been extracted
-  if (tid == 0 || tid == 32) {
-    const bool second = tid == 32;
-    const uint32_t id = tc::idesc_f16(128, 64, tc::kBF16);
-    const uint32_t d = tmem + (second ? F_X : F_A);
-    if constexpr (PERCH) {
-      // [K+; Q+] high halves: the swizzled rows of the raw tiles, K steps of 32 bytes within
-      // a 64-channel half
+    if (s_anyslow) {
+      // ---------------------------------------------------------------- exact diagonal pairs
+      // thread = (row of [K; Q], 8 keys of its row's sub-block): the channels above the
+      // threshold, exp(G_i - G_j) per pair in fp32; the sums initialise the diagonal
+      // accumulator (zeros elsewhere), onto which the A-GEMM adds the other channels
+      const int jh = warp >> 2, p = (warp & 3) & 1;
+      const bool is_q = row >= C;
+      const int i = row & (C - 1), I = i >> 4, jb = 16 * I + 8 * jh;
+      const float rs = is_q ? sRQ[i] : sRK[i];
+      float acc[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+      for (int w4 = 0; w4 < 4; ++w4) {
+        uint32_t bits = sMask[I * 4 + w4];
+        while (bits) {
+          const int cc = 32 * w4 + __ffs(bits) - 1;
+          bits &= bits - 1;
+          const float xi = tc::bf16_at(smem, kq_off(is_q, i, cc), cc & 7) * rs;
+          const float gi = sG[g_off(i, cc)];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int j = jb + e;
+            if (is_q ? j <= i : j < i)
+              acc[e] += xi * tc::bf16_at(smem, kq_off(false, j, cc), cc & 7) * sRK[j] *
+                        __expf(gi - sG[g_off(j, cc)]);
+          }
+        }
+      }
+      const bool lo = (I & 1) == 0;             // this lane's sub-block is 2p, else 2p + 1
+      uint32_t v0[8], v1[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v0[e] = lo ? __float_as_uint(acc[e]) : 0u;
+        v1[e] = lo ? 0u : __float_as_uint(acc[e]);
+      }
+      tc::tmem_st8(tmem + lane_addr + F_D + 32 * p + 8 * jh, v0);
+      tc::tmem_st8(tmem + lane_addr + F_D + 32 * p + 16 + 8 * jh, v1);
+      tc::tmem_wait_st();
+    }
+
+    // ---------------------------------------------------------------- operands
+    // thread: token jr (8-lane groups cover 8 rows, so the swizzled accesses spread over the
+    // banks) and 8-channel pieces c0 = 8 (lane / 8 + 4 it).  First every G piece to registers,
+    // since the diagonal column operand is written over G.
+    const int jr = 8 * warp + (lane & 7);
+    const int J = jr >> 4;                      // warp-uniform
+    float gp[4][8];
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+      const int c0 = 8 * ((lane >> 3) + 4 * it);
+      const float4 a = *reinterpret_cast<const float4*>(sG + g_off(jr, c0));
+      const float4 b = *reinterpret_cast<const float4*>(sG + g_off(jr, c0 + 4));
+      gp[it][0] = a.x; gp[it][1] = a.y; gp[it][2] = a.z; gp[it][3] = a.w;
+      gp[it][4] = b.x; gp[it][5] = b.y; gp[it][6] = b.z; gp[it][7] = b.w;
+    }
+    __syncthreads();
+    {
+      const float rk = sRK[jr], rq = sRQ[jr];
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int c0 = 8 * ((lane >> 3) + 4 * it);
+        float kx[8], qx[8], gref[8], gend[8], es[8], wd[8];
+        tc::bf16x8_load(kq_piece(false, jr, c0), kx);
+        tc::bf16x8_load(kq_piece(true, jr, c0), qx);
+        load8(gend, sGB + J * 128 + c0);
+        load8(wd, sW + J * 128 + c0);
+        if (J == 0) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            gref[e] = 0.f;
+            es[e] = 1.f;
+          }
+        } else {
+          load8(gref, sGB + (J - 1) * 128 + c0);
+          load8(es, sES + (J - 1) * 128 + c0);
+        }
+        const uint32_t mb = (sMask[J * 4 + (c0 >> 5)] >> (c0 & 31)) & 0xffu;
+        float rkv[8], rqv[8], kt[8], qt[8], ke[8], cd[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float r = __expf(gp[it][e] - gref[e]);     // exp(G_j - G_ref(J)) <= 1
+          const float eps = __expf(gend[e] - gp[it][e]);   // exp(G_end(J) - G_j) <= 1
+          const float kr = kx[e] * rk, qr = qx[e] * rq;
+          rkv[e] = kr * r * kRowScale;
+          rqv[e] = qr * r * kRowScale;
+          kt[e] = delta ? kr * r * es[e] : 0.f;            // K~ = k^ exp(G_j)
+          qt[e] = qr * r * es[e];                          // Q~ = q^ exp(G_j)
+          ke[e] = kr * eps * kColScale;
+          cd[e] = ((mb >> e) & 1u) ? 0.f : ke[e] * wd[e];  // k^ exp(G_ref(J) - G_j) / 256
+        }
+        tc::f16x8_store(smem, kq_off(false, jr, c0), rkv);
+        tc::f16x8_store(smem, kq_off(true, jr, c0), rqv);
+        tc::f16x8_store(rec, REC_KQ + tc::cm_offset(jr, c0, 128, KQ_SBO), kt);
+        tc::f16x8_store(rec, REC_KQ + tc::cm_offset(C + jr, c0, 128, KQ_SBO), qt);
+        tc::f16x8_store(smem, M::CD + tc::cm_offset(jr, c0, 128, tc::dense_sbo(D)), cd);
+        // C_off(I, J) = k^ exp(G_ref(I) - G_j) / 256 = ke exp(G_ref(I) - G_end(J)) for every
+        // later sub-block I (warp-uniform J): factor 1 for I = J + 1, F for I = J + 2, J + 3
+        if (J < 3)
+          tc::f16x8_store(smem, M::CO + tc::cm_offset(16 * off_slot(J + 1, J) + (jr & 15), c0, 128,
+                                                      tc::dense_sbo(D)),
+                          ke);
+        if (J < 2) {
+          float f[8], co[8];
+          load8(f, sF + (J == 0 ? 0 : 2) * 128 + c0);      // (2, 0) or (3, 1)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) co[e] = ke[e] * f[e];
+          tc::f16x8_store(smem, M::CO + tc::cm_offset(16 * off_slot(J + 2, J) + (jr & 15), c0, 128,
+                                                      tc::dense_sbo(D)),
+                          co);
+        }
+        if (J == 0) {
+          float f[8], co[8];
+          load8(f, sF + 128 + c0);                         // (3, 0)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) co[e] = ke[e] * f[e];
+          tc::f16x8_store(smem, M::CO + tc::cm_offset(16 * off_slot(3, 0) + (jr & 15), c0, 128,
+                                                      tc::dense_sbo(D)),
+                          co);
+        }
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+
+    // ---------------------------------------------------------------- A-GEMM
+    // R C_diag^T (thread 0, N = 64, onto the exact pairs when there are any) and R C_off^T
+    // (thread 32, N = 96); R is the swizzled K-major row operand, K steps of 32 bytes within
+    // a 64-channel half
+    if (tid == 0 || tid == 32) {
+      const bool second = tid == 32;
       const uint32_t araw = tc::smem_u32(smem + M::RAW);
       auto dak = [&](int s) {
         return tc::desc_add(tc::smem_desc_sw128(araw + (s >> 2) * M::AK_HALF, 1024), (s & 3) * 32);
       };
-      const uint64_t dbk = tc::smem_desc(tc::smem_u32(smem + M::BK), 128, tc::dense_sbo(D));
-      const uint64_t dbl = tc::smem_desc(tc::smem_u32(smem + M::BKLO), 128, tc::dense_sbo(D));
-      if (!second) {
+      const uint64_t db = tc::smem_desc(tc::smem_u32(smem + (second ? M::CO : M::CD)), 128, tc::dense_sbo(D));
+      const uint32_t id = tc::idesc_f16(128, second ? 96 : 64, tc::kF16);
+      const uint32_t d = tmem + (second ? F_O : F_D);
+      const uint32_t acc0 = (!second && s_anyslow) ? 1u : 0u;
 #pragma unroll
-        for (int s = 0; s < D / 16; ++s)        // hi x hi
-          tc::mma_ss(d, dak(s), tc::desc_add(dbk, s * 256), id, s > 0);
+      for (int s = 0; s < D / 16; ++s) tc::mma_ss(d, dak(s), tc::desc_add(db, s * 256), id, s > 0 ? 1u : acc0);
+      tc::mma_commit(second ? &s_bar2 : &s_bar);
+    }
+    mma_wait2();
+  } else {
+    if (warp == 0) {                            // scalar: warp scan of 64 values
+      const float g0 = sGs[2 * lane], g1 = sGs[2 * lane + 1];
+      float s = g0 + g1;
 #pragma unroll
-        for (int s = 0; s < D / 32; ++s)        // hi x lo, first half of K
-          tc::mma_ss(d, dak(s), tc::desc_add(dbl, s * 256), id, 1);
-      } else {
-#pragma unroll
-        for (int s = D / 32; s < D / 16; ++s)   // hi x lo, second half of K
-          tc::mma_ss(d, dak(s), tc::desc_add(dbl, s * 256), id, s > D / 32);
-#pragma unroll
-        for (int s = 0; s < D / 16; ++s)        // lo x hi (low half from TMEM)
-          tc::mma_ts(d, tmem + F_ALO + s * 8, tc::desc_add(dbk, s * 256), id, 1);
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += y;
       }
-    } else {                                    // [K; Q] K^T on the raw rows, one channel half each
-      const uint64_t dak = tc::smem_desc_sw128(tc::smem_u32(smem + M::AK) + (second ? M::AK_HALF : 0u), 1024);
+      const float gl = __shfl_sync(0xffffffffu, s, 31);
+      sGs[2 * lane] = s - g1;
+      sGs[2 * lane + 1] = s;
+      sEG[2 * lane] = __expf(s - g1);
+      sEG[2 * lane + 1] = __expf(s);
+      sEGL[2 * lane] = __expf(gl - (s - g1));
+      sEGL[2 * lane + 1] = __expf(gl - s);
+      const float gam = __expf(gl);
+      sGam[lane] = gam; sGam[lane + 32] = gam; sGam[lane + 64] = gam; sGam[lane + 96] = gam;
+      // anchored factors exp(G_i - G_a), exp(G_a - G_j), anchor mid-chunk, so that
+      // exp(G_i - G_j) is a product of two per-token values while both stay finite
+      const int am = (n - 1) / 2;
+      const float ga = __shfl_sync(0xffffffffu, (am & 1) ? s : s - g1, am >> 1);
+      const float d0 = (s - g1) - ga, d1 = s - ga;
+      const bool ok = __all_sync(0xffffffffu, fmaxf(fabsf(d0), fabsf(d1)) <= kMaxHalfChunkDecay);
+      sEA[2 * lane] = __expf(d0);
+      sEA[2 * lane + 1] = __expf(d1);
+      sKF[2 * lane] = __expf(-d0);
+      sKF[2 * lane + 1] = __expf(-d1);
+      if (lane == 0) s_anchored = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (tid < C) sKF[tid] *= sRK[tid];
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    // A-GEMM [K; Q] K^T on the raw rows: two issuing threads (one issues a tcgen05.mma only
+    // about every 100 cycles), one channel half each, the second into the X columns, which
+    // are free until A has been extracted
+    if (tid == 0 || tid == 32) {
+      const bool second = tid == 32;
+      const uint32_t id = tc::idesc_f16(128, 64, tc::kBF16);
+      const uint32_t d = tmem + (second ? F_X : F_A);
+      const uint64_t dak = tc::smem_desc_sw128(tc::smem_u32(smem + MS::AK) + (second ? MS::AK_HALF : 0u), 1024);
 #pragma unroll
       for (int s = 0; s < D / 32; ++s)
         tc::mma_ss(d, tc::desc_add(dak, s * 32), tc::desc_add(dak, s * 32), id, s > 0);
+      tc::mma_commit(second ? &s_bar2 : &s_bar);
     }
-    tc::mma_commit(second ? &s_bar2 : &s_bar);
-  }
-  mma_wait2();
-
-  if constexpr (PERCH) {
-    // ---------------------------------------------------------------- K~, Q~, K_end
-    // rebuilt from the split halves the A-GEMM has consumed: K~ = K+ exp(G_a) and
-    // Q~ = Q+ exp(G_a) (fp16, to the record's [K~; Q~]) and K_end = K- exp(G_last - G_a)
-    // (MN-major fp16, over the consumed log-decay)
-    {
-      const int i = row < C ? row : row - C;
-      uint32_t l0[16], l1[16];
-      tc::tmem_ld16(tmem + lane_addr + F_ALO + 32 * chalf, l0);
-      tc::tmem_ld16(tmem + lane_addr + F_ALO + 32 * chalf + 16, l1);
-      tc::tmem_wait_ld();
-#pragma unroll
-      for (int g8 = 0; g8 < 8; ++g8) {
-        const int cc = 64 * chalf + 8 * g8;
-        const uint32_t off = kq_off(row >= C, i, cc);
-        float x[8];
-        tc::bf16x8_load(smem + off, x);
-        const float4 a0 = *reinterpret_cast<const float4*>(sGA + cc);
-        const float4 a1 = *reinterpret_cast<const float4*>(sGA + cc + 4);
-        const float ea[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const uint32_t w = g8 < 4 ? l0[4 * g8 + e / 2] : l1[4 * (g8 - 4) + e / 2];
-          x[e] = (x[e] + __uint_as_float(w << 16)) * ea[e];
-          x[e + 1] = (x[e + 1] + __uint_as_float(w & 0xffff0000u)) * ea[e + 1];
-        }
-        if (row < C && !delta) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = 0.f;
-        }
-        tc::f16x8_store(rec, REC_KQ + tc::cm_offset(row, cc, 128, KQ_SBO), x);
-      }
-    }
-    {
-      const int j = 8 * warp + (lane & 7), qq = lane >> 3;   // 4 threads per key row
-#pragma unroll
-      for (int g8 = 0; g8 < 4; ++g8) {
-        const int cc = 32 * qq + 8 * g8;
-        float hi[8], lo[8], ke[8];
-        tc::bf16x8_load(smem + M::BK + tc::cm_offset(j, cc, 128, tc::dense_sbo(D)), hi);
-        tc::bf16x8_load(smem + M::BKLO + tc::cm_offset(j, cc, 128, tc::dense_sbo(D)), lo);
-        const float4 e0 = *reinterpret_cast<const float4*>(sEL + cc);
-        const float4 e1 = *reinterpret_cast<const float4*>(sEL + cc + 4);
-        const float el[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ke[e] = (hi[e] + lo[e]) * el[e];
-        tc::f16x8_store(smem, KEA + tc::mn_offset(j, cc, KE_LBO, KE_SBO), ke);
-      }
-    }
-    __syncthreads();                            // the solve tiles and A_qk overwrite K-, k rows
+    mma_wait2();
   }
 
   // ------------------------------------------------------------------ A_kk, A_qk
   {
-    uint32_t r0[16], r1[16], q0[16], q1[16];
-    tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf, r0);
-    tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf + 16, r1);
-    tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf, q0);
-    tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf + 16, q1);
-    tc::tmem_wait_ld();
-#pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      r0[e] = __float_as_uint(__uint_as_float(r0[e]) + __uint_as_float(q0[e]));
-      r1[e] = __float_as_uint(__uint_as_float(r1[e]) + __uint_as_float(q1[e]));
-    }
     const bool is_k = row < C;
     const int i = is_k ? row : row - C;
-    const float ri = is_k ? (PERCH ? 1.f : sRK[i]) * sBeta[i] : (PERCH ? 1.f : sRQ[i]);
     float x[32];
-    if (PERCH) {
+    if constexpr (PERCH) {
+      // rows of sub-blocks 2p (this warp's lanes 0-15) and 2p + 1 (lanes 16-31); for each
+      // 16-column sub-block J of this thread's half: the diagonal products for J = I, the
+      // off-diagonal ones for J < I, nothing for J > I (the loads are warp-collective, so
+      // both sub-blocks' columns are loaded and each lane keeps its own)
+      const int p = (warp & 3) & 1;
+      const bool hi = ((i >> 4) & 1) != 0;
+      const float ri = is_k ? sBeta[i] : 1.f;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * ri;
-    } else if (s_anchored) {                    // exp(G_i - G_j) = E_i F_j
-      const float rie = ri * sEA[i];
+      for (int jj = 0; jj < 2; ++jj) {
+        const int J = 2 * chalf + jj;
+        const int Ilo = 2 * p, Ihi = 2 * p + 1;
+        const int slo = J < Ilo ? static_cast<int>(F_O) + 16 * off_slot(Ilo, J)
+                                : (J == Ilo ? static_cast<int>(F_D) + 16 * J : -1);
+        const int shi = J < Ihi ? static_cast<int>(F_O) + 16 * off_slot(Ihi, J)
+                                : (J == Ihi ? static_cast<int>(F_D) + 16 * J : -1);
+        uint32_t a[16], b[16];
 #pragma unroll
-      for (int e = 0; e < 32; e += 4) {
-        const float4 kf = *reinterpret_cast<const float4*>(sKF + 32 * chalf + e);
-        x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * rie * kf.x;
-        x[e + 1] = __uint_as_float(e + 1 < 16 ? r0[e + 1] : r1[e - 15]) * rie * kf.y;
-        x[e + 2] = __uint_as_float(e + 2 < 16 ? r0[e + 2] : r1[e - 14]) * rie * kf.z;
-        x[e + 3] = __uint_as_float(e + 3 < 16 ? r0[e + 3] : r1[e - 13]) * rie * kf.w;
+        for (int e = 0; e < 16; ++e) a[e] = b[e] = 0u;
+        if (slo >= 0) tc::tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(slo), a);
+        if (shi >= 0) tc::tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(shi), b);
+        tc::tmem_wait_ld();
+        const bool none = (hi ? shi : slo) < 0;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x[16 * jj + e] = none ? 0.f : __uint_as_float(hi ? b[e] : a[e]) * ri;
       }
-    } else {                                    // exact per pair for extreme decays
-      const float gi = sGs[i];
+    } else {
+      uint32_t r0[16], r1[16], q0[16], q1[16];
+      tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf, r0);
+      tc::tmem_ld16(tmem + lane_addr + F_A + 32 * chalf + 16, r1);
+      tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf, q0);
+      tc::tmem_ld16(tmem + lane_addr + F_X + 32 * chalf + 16, q1);
+      tc::tmem_wait_ld();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int j = 32 * chalf + e;
-        x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * ri * sRK[j] * __expf(gi - sGs[j]);
+      for (int e = 0; e < 16; ++e) {
+        r0[e] = __float_as_uint(__uint_as_float(r0[e]) + __uint_as_float(q0[e]));
+        r1[e] = __float_as_uint(__uint_as_float(r1[e]) + __uint_as_float(q1[e]));
+      }
+      const float ri = is_k ? sRK[i] * sBeta[i] : sRQ[i];
+      if (s_anchored) {                         // exp(G_i - G_j) = E_i F_j
+        const float rie = ri * sEA[i];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 kf = *reinterpret_cast<const float4*>(sKF + 32 * chalf + e);
+          x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * rie * kf.x;
+          x[e + 1] = __uint_as_float(e + 1 < 16 ? r0[e + 1] : r1[e - 15]) * rie * kf.y;
+          x[e + 2] = __uint_as_float(e + 2 < 16 ? r0[e + 2] : r1[e - 14]) * rie * kf.z;
+          x[e + 3] = __uint_as_float(e + 3 < 16 ? r0[e + 3] : r1[e - 13]) * rie * kf.w;
+        }
+      } else {                                  // exact per pair for extreme decays
+        const float gi = sGs[i];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int j = 32 * chalf + e;
+          x[e] = __uint_as_float(e < 16 ? r0[e] : r1[e - 16]) * ri * sRK[j] * __expf(gi - sGs[j]);
+        }
       }
     }
 #pragma unroll
@@ -795,21 +910,28 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       const float fe = sRK[m] * sEGL[m];
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] *= fe;
-      tc::f16x8_store(smem, KEA + tc::mn_offset(m, c0, KE_LBO, KE_SBO), x);
+      tc::f16x8_store(smem, MS::KEA + tc::mn_offset(m, c0, KE_LBO, KE_SBO), x);
     }
   }
-  if (tid < D) reinterpret_cast<float*>(rec + REC_GAM)[tid] = sGam[tid];
+  if (!PERCH && tid < D) reinterpret_cast<float*>(rec + REC_GAM)[tid] = sGam[tid];
   tc::fence_async_smem();
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   if (tid == 0) {
-    const uint32_t id = tc::idesc_f16(128, 64, tc::kF16, false, true, true);
-    const uint64_t dke = tc::smem_desc(tc::smem_u32(smem + KEA), KE_LBO, KE_SBO);
     const uint64_t dtb = tc::smem_desc(tc::smem_u32(smem + M::TBT), TB_LBO, TB_SBO);
+    if constexpr (PERCH) {                      // K_end^T from tensor memory
+      const uint32_t id = tc::idesc_f16(128, 64, tc::kF16, false, false, true);
 #pragma unroll
-    for (int s = 0; s < C / 16; ++s)
-      tc::mma_ss(tmem + F_A, tc::desc_add(dke, s * 2 * KE_LBO), tc::desc_add(dtb, s * 2 * TB_LBO), id, s > 0);
+      for (int s = 0; s < C / 16; ++s)
+        tc::mma_ts(tmem + F_A, tmem + F_KE + s * 8, tc::desc_add(dtb, s * 2 * TB_LBO), id, s > 0);
+    } else {
+      const uint32_t id = tc::idesc_f16(128, 64, tc::kF16, false, true, true);
+      const uint64_t dke = tc::smem_desc(tc::smem_u32(smem + MS::KEA), KE_LBO, KE_SBO);
+#pragma unroll
+      for (int s = 0; s < C / 16; ++s)
+        tc::mma_ss(tmem + F_A, tc::desc_add(dke, s * 2 * KE_LBO), tc::desc_add(dtb, s * 2 * TB_LBO), id, s > 0);
+    }
     tc::mma_commit(&s_bar);
   }
   // while they run: K~ = k^ exp(G_m) and Q~ = q scale/|q| exp(G_m) to the record's [K~; Q~]
@@ -860,8 +982,12 @@ __global__ void __launch_bounds__(tcs::NT, 2)
     }
   }
 
-  if (PERCH && s_range && tid == 0) raise_device_error(P.err, KDA_DEVERR_DECAY_RANGE);
+  if (PERCH && s_range && tid == 0) {           // outside the domain: the chain leaves this
+    plan.skip[static_cast<int64_t>(ci.seq) * HV + h] = 1;   // (sequence, head) untouched
+    raise_device_error(P.err, KDA_DEVERR_DECAY_RANGE);
+  }
   if (s_abort) {                                // the phases that may have timed out
+    if (tid == 0) plan.skip[static_cast<int64_t>(ci.seq) * HV + h] = 1;
     tc::mbar_wait_bounded(&s_bar, (phase ^ 1) & 1, kWaitLimit);
     tc::mbar_wait_bounded(&s_bar2, (phase2 ^ 1) & 1, kWaitLimit);
     if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
@@ -912,7 +1038,9 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
   const int b = blockIdx.x, h = blockIdx.y, vt = blockIdx.z;
   const int HV = P.HV;
   const uint32_t bos = P.offsets[b], eos = P.offsets[b + 1];
-  if (eos <= bos) return;
+  // empty, or a chunk of it outside the tensor-core path's domain (the front kernel raised
+  // the device error): o and the slot are left as they were
+  if (eos <= bos || plan.skip[static_cast<int64_t>(b) * HV + h] != 0) return;
   const uint32_t nchunks = (eos - bos + C - 1) / C;
   const int64_t c0 = plan.seq_chunk0[b];
   const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + vt * BV;

@@ -176,7 +176,6 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   __shared__ uint64_t s_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_range;
   __shared__ int s_anchored;     // scalar decay: anchored per-token factors are in range
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -187,7 +186,8 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   // additive write (no delta rule): A_kk = 0 makes T = I and K~ = 0 drops W = TB K~
   constexpr bool delta = DELTA;
   const uint32_t bos = P.offsets[b], eos = P.offsets[b + 1];
-  if (eos <= bos) return;
+  // empty, or flagged by tc_range_scan_kernel: o and the slot are left as they were
+  if (eos <= bos || plan.skip[static_cast<int64_t>(b) * HV + h] != 0) return;
   const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + vt * BV;
 
   float* sG = reinterpret_cast<float*>(smem + S_G);
@@ -220,7 +220,6 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     tc::mbar_init(&s_bar, 1);
     tc::fence_mbar_init();
     s_abort = 0;
-    s_range = 0;
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -314,8 +313,9 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
     if (PERCH) {
       if (tid < D) {
         // channel tid: inclusive cumsum G, then E' = exp(G - G_a) in place, with the anchor
-        // G_a at the chunk's middle token; exp(G_a) and exp(G_last) go to small arrays
-        float acc = 0.f, gmin = 0.f, gmax = -3.0e38f;
+        // G_a at the chunk's middle token; exp(G_a) and exp(G_last) go to small arrays.
+        // tc_range_scan_kernel has checked that G stays within kMaxHalfChunkDecay of G_a.
+        float acc = 0.f;
 #pragma unroll
         for (int i0 = 0; i0 < C; i0 += 16) {
           float gv[16];
@@ -324,13 +324,10 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             acc += gv[e];
-            gmin = fminf(gmin, acc);
-            gmax = fmaxf(gmax, acc);
             sG[(i0 + e) * GS + tid] = acc;
           }
         }
         const float ga = sG[((n - 1) / 2) * GS + tid];
-        if (fmaxf(gmax - ga, ga - gmin) > kMaxHalfChunkDecay) s_range = 1;
 #pragma unroll
         for (int i0 = 0; i0 < C; i0 += 16) {
           float gv[16];
@@ -896,7 +893,6 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   }
   tc::cp_async_wait_all();
 
-  if (PERCH && s_range && tid == 0) raise_device_error(P.err, KDA_DEVERR_DECAY_RANGE);
   if (s_abort) {
     // give the tensor core a last bounded chance to drain before TMEM is released
     tc::mbar_wait_bounded(&s_bar, phase & 1, kWaitLimit);
@@ -919,6 +915,38 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
   __syncthreads();
   tc::fence_after_sync();
   if (warp == 0) tc::tmem_dealloc(tmem, T_COLS);
+}
+
+// The per-channel factors exp(G_i - G_a), exp(G_a - G_j) of the kernel above (anchor G_a at
+// a chunk's middle token) must stay finite in fp32, which bounds how far a channel's
+// cumulative log-decay may move from the anchor within a chunk.  The kernel walks a
+// sequence's chunks in order and writes o as it goes, so it cannot find a chunk outside
+// that range before it has written the earlier ones.  This pass checks every chunk first
+// (the same cumulative sums, in the same order, against a bound one nat tighter) and marks
+// the (sequence, head) of a chunk outside it: the kernel then leaves its o rows and its slot
+// untouched, and the device error word reports KDA_DEVERR_DECAY_RANGE.
+constexpr float kScanHalfChunkDecay = tcp::kMaxHalfChunkDecay - 1.0f;
+
+__global__ void __launch_bounds__(tcp::D) tc_range_scan_kernel(Problem P, PlanView plan) {
+  using namespace tcp;
+  const int gc = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  const int plan_valid = plan.info[1], plan_chunks = plan.info[0];
+  const ChunkInfo ci = plan.chunks[gc];
+  if (plan_valid == 0 || gc >= plan_chunks) return;
+  const int HV = P.HV, am = (ci.n - 1) / 2;
+  const float* g = P.g + (ci.t0 * HV + h) * D + c;
+  float acc = 0.f, gmin = 0.f, gmax = -3.0e38f, ga = 0.f;
+#pragma unroll 16
+  for (int i = 0; i < C; ++i) {
+    acc += i < ci.n ? g[static_cast<int64_t>(i) * HV * D] : 0.f;
+    gmin = fminf(gmin, acc);
+    gmax = fmaxf(gmax, acc);
+    ga = i == am ? acc : ga;
+  }
+  if (__syncthreads_or(fmaxf(gmax - ga, ga - gmin) > kScanHalfChunkDecay) && c == 0) {
+    plan.skip[static_cast<int64_t>(ci.seq) * HV + h] = 1;
+    raise_device_error(P.err, KDA_DEVERR_DECAY_RANGE);
+  }
 }
 
 bool tc_prefill_supported(const Problem& P, bool qbf16) {
@@ -946,9 +974,17 @@ cudaError_t launch_prefill_tc(const Problem& P, void* workspace, bool perch, boo
   cudaError_t e = launch_plan(P, plan, stream);
   if (e != cudaSuccess) return e;
   st.mark(1, stream);
-  if (perch) e = sbf16 ? launch_tc_t<true, true>(P, plan, stream) : launch_tc_t<true, false>(P, plan, stream);
-  else e = sbf16 ? launch_tc_t<false, true>(P, plan, stream) : launch_tc_t<false, false>(P, plan, stream);
-  st.mark(2, stream);
+  int k = 2;
+  if (perch) {
+    tc_range_scan_kernel<<<dim3(static_cast<unsigned>(plan_max_chunks(P)), P.HV), tcp::D, 0, stream>>>(P, plan);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    st.mark(k++, stream);
+    e = sbf16 ? launch_tc_t<true, true>(P, plan, stream) : launch_tc_t<true, false>(P, plan, stream);
+  } else {
+    e = sbf16 ? launch_tc_t<false, true>(P, plan, stream) : launch_tc_t<false, false>(P, plan, stream);
+  }
+  st.mark(k, stream);
   return e;
 }
 

@@ -132,3 +132,70 @@ def test_a_one_term_slip_is_caught(slip):
     o_ref, S_ref = oracle.recurrence_py(q, k, v, beta, g, S0)
     o, S = factorised(q, k, v, beta, g, S0, chunk=64, slip=slip)
     assert max(np.abs(o - o_ref).max(), np.abs(S - S_ref).max()) > 1e-3
+
+
+def subblock_matrices(q, k, beta, G, *, tau=12.0, row_scale=256.0):
+    """A_kk, A_qk of one chunk as the per-channel tensor-core front kernel forms them: the
+    chunk's tokens in sub-blocks of 16, row i of sub-block I scaled by exp(G_i - G_ref(I))
+    (G_ref(I) = G at the last token before I, 0 for I = 0) and by 2^8; a key j of an earlier
+    sub-block J by exp(G_ref(I) - G_end(J)) exp(G_end(J) - G_j) / 2^8 (both factors <= 1 for a
+    non-increasing G); a key of the row's own sub-block by exp(G_ref(J) - G_end(J))
+    exp(G_end(J) - G_j) / 2^8, except in the channels whose decay from G_ref(J) exceeds tau
+    inside the sub-block, whose pairs are summed directly with exp(G_i - G_j)."""
+    n, dk = k.shape
+    scale = 1.0 / np.sqrt(dk)
+    qn = scale * q / np.sqrt(np.sum(q * q, axis=1, keepdims=True) + 1e-6)
+    kn = k / np.sqrt(np.sum(k * k, axis=1, keepdims=True) + 1e-6)
+    nb = (n + 15) // 16
+    blk = np.arange(n) // 16
+    ref = np.zeros((nb, dk))
+    end = np.zeros((nb, dk))
+    for I in range(nb):
+        if I > 0:
+            ref[I] = G[16 * I - 1]
+        end[I] = G[min(16 * I + 15, n - 1)]
+    slow = np.array([ref[J] - G[16 * J:16 * J + 16].min(axis=0) > tau for J in range(nb)])
+    eps = np.exp(end[blk] - G)                              # exp(G_end(J) - G_j) <= 1
+    ke = kn * eps / row_scale
+    A = np.zeros((2, n, n))
+    for w, x in enumerate((kn, qn)):
+        R = x * np.exp(G - ref[blk]) * row_scale            # exp(G_i - G_ref(I)) <= 1
+        for i in range(n):
+            I = blk[i]
+            for j in range(i + 1):
+                J = blk[j]
+                if J < I:
+                    A[w, i, j] = np.dot(R[i], ke[j] * np.exp(ref[I] - end[J]))
+                else:
+                    col = np.where(slow[J], 0.0, ke[j] * np.exp(ref[J] - end[J]))
+                    exact = np.where(slow[J], x[i] * kn[j] * np.exp(G[i] - G[j]), 0.0)
+                    A[w, i, j] = np.dot(R[i], col) + exact.sum()
+    return beta[:, None] * np.tril(A[0], -1), np.tril(A[1])
+
+
+@pytest.mark.parametrize("factor", [1.0, 4.0, 10.0, 33.0])
+@pytest.mark.parametrize("n", [64, 50, 17])
+def test_subblock_factorization_of_the_intra_chunk_matrices(factor, n):
+    """The per-channel front kernel's sub-block form of A_kk and A_qk equals the pairwise
+    definition (KDA page, sec. 6.3: exp(G_i - G_j) per pair and channel) in fp64, at decays
+    from the kda_prefill workload's to 33x it, where most channels take the exact pairs."""
+    r = np.random.default_rng(int(factor * 10) + n)
+    q, k = r.standard_normal((n, 128)), r.standard_normal((n, 128))
+    beta = 1.0 / (1.0 + np.exp(-r.standard_normal(n)))
+    G = np.cumsum(-np.exp(r.normal(-2.0, 0.5, (n, 128))) * factor, axis=0)
+    Akk, Aqk = subblock_matrices(q, k, beta, G)
+    qn = q / np.sqrt(np.sum(q * q, axis=1, keepdims=True) + 1e-6) / np.sqrt(128)
+    kn = k / np.sqrt(np.sum(k * k, axis=1, keepdims=True) + 1e-6)
+    ref_kk, ref_qk = np.zeros((n, n)), np.zeros((n, n))
+    for i in range(n):
+        for j in range(i + 1):
+            dec = np.exp(G[i] - G[j])
+            ref_qk[i, j] = np.dot(qn[i], kn[j] * dec)
+            if j < i:
+                ref_kk[i, j] = beta[i] * np.dot(kn[i], kn[j] * dec)
+    assert np.allclose(Akk, ref_kk, rtol=1e-12, atol=1e-14)
+    assert np.allclose(Aqk, ref_qk, rtol=1e-12, atol=1e-14)
+    if factor >= 10.0:                                    # the exact pairs are exercised
+        refs = [np.zeros(128)] + [G[16 * J - 1] for J in range(1, (n + 15) // 16)]
+        assert any(np.any(ref - G[16 * J:16 * J + 16].min(axis=0) > 12.0)
+                   for J, ref in enumerate(refs))

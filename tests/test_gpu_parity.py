@@ -288,28 +288,75 @@ def test_tensor_core_path_matches_cuda_core_path(decay, state):
     assert state_err(p, s_tc, pool_ref) <= tol and state_err(p, s_cc, pool_ref) <= tol
 
 
-def test_decay_range_flagged_and_cuda_core_path_exact():
-    """Per-channel decay stronger than the tensor-core path's anchored factors allow (about
-    -5 nats per token, ~160 nats over half a chunk) is reported on the device
-    (KDA_DEVERR_DECAY_RANGE); the fp32 CUDA-core path stays within tolerance."""
-    p = small("strong-decay", [130, 64], 1, 2, 128, "bf16", "f32", "per_channel", 64, seed=51)
-    p.g[:] = (p.g * 33.0).astype(np.float32)              # mean about -5 per token
+def _prefill_keep(p, **kw):
+    """One call on fresh device inputs with o pre-filled by a sentinel; returns the device
+    error code, o, the pool before the call and the inputs (for a second call)."""
     t = torch_io.prefill_inputs(p, DEV)
-    kda.prefill(**t, chunk=64)
+    o = torch.full((p.total_tokens, p.num_v_heads, p.d_v), 7.25, dtype=torch.float32, device=DEV)
+    before = t["state_pool"].clone()
+    kda.prefill(**t, chunk=p.chunk, scale=p.scale, out=o, **kw)
     torch.cuda.synchronize()
-    assert kda.get_device_error() == 5
-    o, pool, _ = gpu_prefill(p, cuda_cores=True)
-    o_ref, pool_ref = oracle.run(p)
-    assert rel_err(o, o_ref) <= TOL["bf16"] and state_err(p, pool, pool_ref) <= TOL["bf16"]
+    return kda.get_device_error(), o, before, t
 
 
-@pytest.mark.parametrize("factor", [1.5, 4.0, 10.0])
-def test_stronger_decay_stays_accurate_on_tensor_cores(factor):
-    """Per-channel decay 1.5x-10x the KDA workload's (up to ~-1.5 nats per token, ~50 nats
-    over half a chunk) stays within tolerance on the tensor-core path and raises nothing."""
-    p = small("mid-decay", [200, 77], 1, 2, 128, "bf16", "f32", "per_channel", 64, seed=52)
+@pytest.mark.parametrize("path", ["default", "compact"])
+@pytest.mark.parametrize("factor", [1.5, 4.0, 10.0, 33.0])
+def test_strong_per_channel_decay_same_pool(path, factor):
+    """Per-channel decay 1.5x-33x the kda_prefill workload's (33x: about -5 nats per token,
+    some channels -20): a call either matches the oracle, or raises KDA_DEVERR_DECAY_RANGE
+    with every slot and o row exactly as before, after which the fp32 CUDA-core path, run on
+    that same pool, matches the oracle.  The default two-kernel path covers every one of
+    these decays (16-token sub-blocks, exact fp32 pairs where fp16 cannot hold a factor);
+    the compact single-kernel path raises the error at 33x."""
+    p = small("strong-decay", [200, 77, 130], 1, 2, 128, "bf16", "f32", "per_channel", 64,
+              seed=52, slots=5)
     p.g[:] = (p.g * factor).astype(np.float32)
-    check_prefill(p)
+    err, o, before, t = _prefill_keep(p, compact=(path == "compact"))
+    o_ref, pool_ref = oracle.run(p)
+    if err == 0:
+        assert rel_err(o.double().cpu().numpy(), o_ref) <= TOL["bf16"]
+        assert state_err(p, torch_io.pool_to_f64(t["state_pool"]), pool_ref) <= TOL["bf16"]
+    else:
+        assert err == 5
+        assert torch.equal(t["state_pool"], before)
+        assert bool(torch.all(o == 7.25))
+        kda.prefill(**t, chunk=64, cuda_cores=True, out=o)
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        assert rel_err(o.double().cpu().numpy(), o_ref) <= TOL["bf16"]
+        assert state_err(p, torch_io.pool_to_f64(t["state_pool"]), pool_ref) <= TOL["bf16"]
+    assert err == (5 if (path == "compact" and factor > 30) else 0)
+
+
+@pytest.mark.parametrize("path", ["default", "compact"])
+def test_out_of_domain_skips_only_its_sequence_and_head(path):
+    """One (sequence, value head) outside the tensor-core path's domain -- a log-decay above
+    zero (a gate above one) on the default path, 33x the workload's decay on the compact
+    path -- raises KDA_DEVERR_DECAY_RANGE and leaves exactly that pair's slot state and o
+    rows as they were; every other pair of the batch matches the oracle."""
+    p = small("one-bad", [150, 90, 70], 1, 2, 128, "bf16", "f32", "per_channel", 64, seed=57,
+              slots=6)
+    rows = slice(int(p.offsets[1]), int(p.offsets[2]))        # sequence 1, value head 0
+    if path == "default":
+        p.g[rows.start + 40, 0, 5] = 0.5
+    else:
+        p.g[rows, 0, :] = (p.g[rows, 0, :] * 33.0).astype(np.float32)
+    err, o, before, t = _prefill_keep(p, compact=(path == "compact"))
+    assert err == 5
+    o_ref, pool_ref = oracle.run(p)
+    on = o.double().cpu().numpy()
+    pool = torch_io.pool_to_f64(t["state_pool"])
+    bad_slot = int(p.slot_idx[1])
+    assert torch.equal(t["state_pool"][bad_slot, 0], before[bad_slot, 0])
+    assert bool(torch.all(o[rows, 0] == 7.25))
+    keep = np.ones(on.shape[:2], bool)
+    keep[rows, 0] = False
+    assert rel_err(on[keep], o_ref[keep]) <= TOL["bf16"]
+    for b in range(p.num_seqs):
+        for h in range(p.num_v_heads):
+            if (b, h) != (1, 0):
+                s = int(p.slot_idx[b])
+                assert rel_err(pool[s, h], pool_ref[s, h]) <= TOL["bf16"]
 
 
 @pytest.mark.parametrize("factor", [1.0, 6.0])

@@ -13,10 +13,10 @@ it:
 There is no CPU or eager fallback: if the library is missing, calls raise.
 """
 from .kda import (decode_step, get_device_error, make_params, prefill,  # noqa: F401
-                  prefill_no_alloc, set_stage_events, uses_tensor_cores,
+                  prefill_no_alloc, no_alloc_form, set_stage_events, uses_tensor_cores,
                   workspace_size, verify_window, fold_accepted, ring_record_elems,
                   gdp_prefill, gdp_decode_step, prefill_bwd, conv_gates)
 from ._lib import KdaError, KdaParams, load  # noqa: F401
 
 __all__ = ["prefill", "decode_step", "workspace_size", "get_device_error", "make_params",
-           "set_stage_events", "prefill_no_alloc", "uses_tensor_cores", "verify_window", "fold_accepted", "ring_record_elems", "gdp_prefill", "gdp_decode_step", "prefill_bwd", "conv_gates", "KdaError", "KdaParams", "load"]
+           "set_stage_events", "prefill_no_alloc", "no_alloc_form", "uses_tensor_cores", "verify_window", "fold_accepted", "ring_record_elems", "gdp_prefill", "gdp_decode_step", "prefill_bwd", "conv_gates", "KdaError", "KdaParams", "load"]

@@ -38,7 +38,7 @@ EXPORTS = ("kda_abi_version", "kda_status_string", "kda_prefill_workspace_size",
            "kda_prefill_uses_tensor_cores", "kda_ring_record_elems", "kda_verify_window",
            "kda_fold_accepted", "kda_gdp_prefill_fwd", "kda_gdp_decode_step",
            "kda_gdp_workspace_size", "kda_prefill_bwd", "kda_prefill_bwd_workspace_size",
-           "kda_conv_gates_fwd")
+           "kda_conv_gates_fwd", "kda_prefill_no_alloc_form")
 
 KDA_NO_ALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -118,6 +118,8 @@ def load():
         L.kda_prefill_uses_tensor_cores.restype = ctypes.c_int
         L.kda_prefill_fwd_no_alloc.argtypes = [pp, P, P, P, P, P, P, P, P, P, P]
         L.kda_prefill_fwd_no_alloc.restype = ctypes.c_int
+        L.kda_prefill_no_alloc_form.argtypes = [pp]
+        L.kda_prefill_no_alloc_form.restype = ctypes.c_int
         L.kda_gdp_prefill_fwd.argtypes = [pp, ctypes.c_int32, P, P, P, P, P, P, P, P, P, P,
                                           ctypes.c_size_t, P]
         L.kda_gdp_prefill_fwd.restype = ctypes.c_int

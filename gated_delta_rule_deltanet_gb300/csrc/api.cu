@@ -541,6 +541,26 @@ void* no_alloc_scratch() {
 }
 }  // namespace
 
+namespace {
+// The parameters kda_prefill_fwd_no_alloc runs: the two-kernel tensor-core form when its
+// chunk records fit the scratch, else the compact form.  False when nothing fits.
+bool no_alloc_params(const kda_params_t* p, const Problem& P, kda_params_t* q_params) {
+  *q_params = *p;
+  if (use_tc(p, P) && prefill_workspace_bytes(p, P) > KDA_NO_ALLOC_SCRATCH_BYTES)
+    q_params->flags |= KDA_FLAG_COMPACT;
+  return prefill_workspace_bytes(q_params, P) <= KDA_NO_ALLOC_SCRATCH_BYTES;
+}
+}  // namespace
+
+extern "C" int kda_prefill_no_alloc_form(const kda_params_t* p) {
+  Problem P{};
+  if (check_prefill(p, &P) != KDA_OK) return -1;
+  kda_params_t q_params;
+  if (!no_alloc_params(p, P, &q_params)) return -1;
+  if (!use_tc(&q_params, P)) return 2;
+  return compact_tc(&q_params) ? 1 : 0;
+}
+
 extern "C" kda_status_t kda_prefill_fwd_no_alloc(const kda_params_t* p, const void* q,
                                                  const void* k, const void* v,
                                                  const float* beta, const float* log_decay,
@@ -552,10 +572,8 @@ extern "C" kda_status_t kda_prefill_fwd_no_alloc(const kda_params_t* p, const vo
   if (s != KDA_OK) return s;
   // the tensor-core path falls back to its single-kernel form when the chunk records
   // of the two-kernel form do not fit the scratch
-  kda_params_t q_params = *p;
-  if (use_tc(p, P) && prefill_workspace_bytes(p, P) > KDA_NO_ALLOC_SCRATCH_BYTES)
-    q_params.flags |= KDA_FLAG_COMPACT;
-  if (prefill_workspace_bytes(&q_params, P) > KDA_NO_ALLOC_SCRATCH_BYTES) return KDA_ERR_WORKSPACE;
+  kda_params_t q_params;
+  if (!no_alloc_params(p, P, &q_params)) return KDA_ERR_WORKSPACE;
   if (p->num_seqs == 0) return KDA_OK;
   void* scratch = no_alloc_scratch();
   if (!scratch) return KDA_ERR_CUDA;

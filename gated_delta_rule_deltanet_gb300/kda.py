@@ -37,6 +37,13 @@ def _row_stride(x: torch.Tensor, name: str) -> int:
     return int(x.stride(0)) if x.shape[0] > 1 else int(x.shape[1] * x.shape[2])
 
 
+def _on(dev, fn, *args):
+    """Calls a library entry point with `dev` current: the library finds its per-device
+    error word and scratch on the current device, and the stream passed belongs to `dev`."""
+    with torch.cuda.device(dev):
+        return fn(*args)
+
+
 def _check_cuda(*ts):
     dev = None
     for t in ts:
@@ -151,13 +158,21 @@ def prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tenso
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     elif workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace needs {need} bytes")
-    st = _lib.load().kda_prefill_fwd(
+    st = _on(dev, _lib.load().kda_prefill_fwd, 
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_decay),
         _ptr(input_row_offsets), _ptr(slot_idx), _ptr(state_pool), _ptr(out), _ptr(workspace),
         ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream, dev))
     if st != _lib.KDA_OK:
         raise KdaError(st, "kda_prefill_fwd")
     return out
+
+
+def no_alloc_form(params: KdaParams) -> str:
+    """Which form kda_prefill_fwd_no_alloc runs for these parameters: "two_kernel" or
+    "compact" (tensor cores), "cuda_cores", or "rejected" (invalid or too large for the
+    library's scratch)."""
+    r = _lib.load().kda_prefill_no_alloc_form(ctypes.byref(params))
+    return {0: "two_kernel", 1: "compact", 2: "cuda_cores"}.get(r, "rejected")
 
 
 def prefill_no_alloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor,
@@ -170,7 +185,9 @@ def prefill_no_alloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
 
     For callers that must not allocate device memory: `out` (fp32 [T, HV, D]) is
     required and nothing is allocated here or in the library.  Problems needing more
-    than KDA_NO_ALLOC_SCRATCH_BYTES of scratch raise KdaError(KDA_ERR_WORKSPACE).
+    than KDA_NO_ALLOC_SCRATCH_BYTES of scratch raise KdaError(KDA_ERR_WORKSPACE); when the
+    tensor-core path's chunk records do not fit, the single-kernel form runs instead
+    (`no_alloc_form` tells which).
     Calls that overlap on the GPU share the scratch and race; keep them on one stream.
     """
     dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, out)
@@ -179,7 +196,7 @@ def prefill_no_alloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: to
     T, HV, D = v.shape
     if out.dtype != torch.float32 or tuple(out.shape) != (T, HV, D) or not out.is_contiguous():
         raise ValueError("out must be contiguous float32 [T, HV, D]")
-    st = _lib.load().kda_prefill_fwd_no_alloc(
+    st = _on(dev, _lib.load().kda_prefill_fwd_no_alloc, 
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_decay),
         _ptr(input_row_offsets), _ptr(slot_idx), _ptr(state_pool), _ptr(out),
         _stream_handle(stream, dev))
@@ -228,7 +245,7 @@ def prefill_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
     if st != _lib.KDA_OK:
         raise KdaError(st, "kda_prefill_bwd_workspace_size")
     workspace = _workspace(int(n.value), workspace, dev)
-    st = _lib.load().kda_prefill_bwd(
+    st = _on(dev, _lib.load().kda_prefill_bwd, 
         ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_decay),
         _ptr(input_row_offsets), _ptr(slot_idx), _ptr(state_pool), _ptr(d_o), _ptr(d_state),
         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dlog_decay), _ptr(d_state0),
@@ -295,7 +312,7 @@ def conv_gates(x: torch.Tensor, conv_weight: torch.Tensor, a: torch.Tensor, b: t
     y = torch.empty_like(x)
     log_decay = torch.empty(tuple(a.shape), dtype=torch.float32, device=dev)
     beta = torch.empty((T, num_v_heads), dtype=torch.float32, device=dev)
-    st = _lib.load().kda_conv_gates_fwd(
+    st = _on(dev, _lib.load().kda_conv_gates_fwd, 
         ctypes.byref(p), int(width), _ptr(x), _ptr(conv_weight), _ptr(conv_bias), _ptr(a), _ptr(b),
         _ptr(A_log), _ptr(dt_bias), _ptr(input_row_offsets), _ptr(slot_idx), _ptr(conv_state),
         _ptr(y), _ptr(log_decay), _ptr(beta), _stream_handle(stream, dev))
@@ -339,7 +356,7 @@ def decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
                     k_row_stride=_row_stride(k, "k"), v_row_stride=_row_stride(v, "v"))
     if out is None:
         out = torch.empty((B, HV, D), dtype=torch.float32, device=dev)
-    st = _lib.load().kda_decode_step(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+    st = _on(dev, _lib.load().kda_decode_step, ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
                                      _ptr(log_decay), _ptr(slot_idx), _ptr(state_pool), _ptr(out),
                                      _stream_handle(stream, dev))
     if st != _lib.KDA_OK:
@@ -351,7 +368,8 @@ def get_device_error(stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronises the stream and returns (and clears) the device error code (0 = none)."""
     code = ctypes.c_int32(0)
     s = stream if stream is not None else torch.cuda.current_stream()
-    st = _lib.load().kda_get_device_error(ctypes.c_void_p(s.cuda_stream), ctypes.byref(code))
+    st = _on(s.device, _lib.load().kda_get_device_error, ctypes.c_void_p(s.cuda_stream),
+             ctypes.byref(code))
     if st not in (_lib.KDA_OK, _lib.KDA_ERR_DEVICE):
         raise KdaError(st, "kda_get_device_error")
     return int(code.value)
@@ -432,7 +450,7 @@ def verify_window(q, k, v, beta, log_decay, slot_idx, state_pool, *, window: int
     elif (ring.dtype != torch.float32 or not ring.is_contiguous()
           or ring.numel() != BW * HV * rec):
         raise ValueError("ring must be contiguous float32 [B, window, HV, R]")
-    st = _lib.load().kda_verify_window(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+    st = _on(dev, _lib.load().kda_verify_window, ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
                                        _ptr(log_decay), _ptr(slot_idx), int(window),
                                        _ptr(state_pool), _ptr(out), _ptr(ring),
                                        _stream_handle(stream, dev))
@@ -455,7 +473,7 @@ def fold_accepted(ring, accepted, slot_idx, state_pool, *, window: int, num_k_he
     rec = ring_record_elems(p)
     if ring.dtype != torch.float32 or not ring.is_contiguous() or ring.numel() != B * window * HV * rec:
         raise ValueError("ring does not match [B, window, HV, R]")
-    st = _lib.load().kda_fold_accepted(ctypes.byref(p), _ptr(ring), int(window), _ptr(accepted),
+    st = _on(dev, _lib.load().kda_fold_accepted, ctypes.byref(p), _ptr(ring), int(window), _ptr(accepted),
                                        _ptr(slot_idx), _ptr(state_pool),
                                        _stream_handle(stream, dev))
     if st != _lib.KDA_OK:
@@ -534,7 +552,7 @@ def gdp_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
     elif out.dtype != torch.float32 or tuple(out.shape) != (T, HV, D) or not out.is_contiguous():
         raise ValueError("out must be contiguous float32 [T, HV, D]")
     workspace = _workspace(need, workspace, dev)
-    st = _lib.load().kda_gdp_prefill_fwd(
+    st = _on(dev, _lib.load().kda_gdp_prefill_fwd, 
         ctypes.byref(p), n_h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_decay),
         _ptr(input_row_offsets), _ptr(slot_idx), _ptr(state_pool), _ptr(out), _ptr(workspace),
         ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream, dev))
@@ -559,7 +577,7 @@ def gdp_decode_step(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: tor
     elif out.dtype != torch.float32 or tuple(out.shape) != (B, HV, D) or not out.is_contiguous():
         raise ValueError("out must be contiguous float32 [B, HV, D]")
     workspace = _workspace(need, workspace, dev)
-    st = _lib.load().kda_gdp_decode_step(
+    st = _on(dev, _lib.load().kda_gdp_decode_step, 
         ctypes.byref(p), n_h, _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(log_decay),
         _ptr(slot_idx), _ptr(state_pool), _ptr(out), _ptr(workspace),
         ctypes.c_size_t(workspace.numel() * workspace.element_size()), _stream_handle(stream, dev))

@@ -44,8 +44,10 @@
  *     enqueued and returned as a status; nothing is launched then.  Problems
  *     only the device can see (offsets not monotone or not ending at
  *     total_tokens, a slot index >= num_slots, repeated slots under
- *     KDA_FLAG_CHECKED) set a device error word and the affected work is
- *     skipped -- no trap, no fault; read it with kda_get_device_error().
+ *     KDA_FLAG_CHECKED; on the tensor-core prefill path, a per-channel
+ *     log-decay outside its domain, see KDA_DEVERR_DECAY_RANGE) set a device
+ *     error word and the affected work is skipped -- no trap, no fault; read it
+ *     with kda_get_device_error().
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -83,8 +85,10 @@ typedef enum kda_decay_kind {
  * accumulation).  fp32 q/k/v and the other head sizes and chunks always use it. */
 #define KDA_FLAG_CUDA_CORES 2u
 /* Tensor-core path only: run it as one kernel per (sequence, value head, value
- * tile) that walks the sequence's chunks, with only the chunk table as workspace
- * (16 bytes per chunk).  Without it the path runs as two kernels: a chunk-parallel
+ * tile) that walks the sequence's chunks, with only the chunk table (16 bytes per
+ * chunk) and one flag per sequence and value head as workspace; its per-channel
+ * factors are anchored at each chunk's middle token, which bounds the decay it takes
+ * (see KDA_DEVERR_DECAY_RANGE).  Without it the path runs as two kernels: a chunk-parallel
  * one that writes every chunk's operands of the state recurrence to the workspace
  * (57,856 bytes per chunk and value head) and a sequential one over each
  * sequence's chunks, which keeps the chunk-local work off the sequential path.
@@ -109,9 +113,14 @@ typedef enum kda_decay_kind {
 #define KDA_DEVERR_SLOT_RANGE 2 /* slot_idx[b] >= num_slots */
 #define KDA_DEVERR_SLOT_DUP 3   /* a slot named twice (KDA_FLAG_CHECKED only) */
 #define KDA_DEVERR_TIMEOUT 4    /* a bounded wait inside a kernel gave up; its work is incomplete */
-#define KDA_DEVERR_DECAY_RANGE 5 /* tensor-core path, per-channel decay: the cumulative log-decay
-                                    over half a chunk exceeded 80 nats in some channel, so its
-                                    anchored decay factors overflow; rerun with KDA_FLAG_CUDA_CORES */
+/* KDA_DEVERR_DECAY_RANGE: tensor-core prefill path, per-channel decay outside its domain.
+ * The default two-kernel form takes any log-decay g <= 1/64 (a forget gate up to
+ * exp(1/64)); a larger g is outside it.  The compact form (KDA_FLAG_COMPACT) also needs
+ * every channel's cumulative log-decay to stay within 79 nats of its value at the chunk's
+ * middle token.  The (sequence, value head) pairs with such a chunk are skipped: their o rows
+ * and their slot's state keep their previous contents, every other pair is computed.  The
+ * fp32 CUDA-core path (KDA_FLAG_CUDA_CORES) takes any finite log-decay. */
+#define KDA_DEVERR_DECAY_RANGE 5
 #define KDA_DEVERR_ACCEPTED 6    /* kda_fold_accepted: accepted[b] > window */
 
 typedef struct kda_params {
@@ -383,21 +392,26 @@ kda_status_t kda_get_device_error(void *stream, int32_t *code);
  *
  * For callers that cannot allocate device memory at the point where they run
  * the prefill: code hosted inside an engine that owns the device's memory
- * budget and hands out no allocator, code running under a CUDA stream capture
- * that must not call cudaMalloc, or a runtime that reserves all of its memory
- * at start-up.  They still pass every input and output buffer.
+ * budget and hands out no allocator, or a runtime that reserves all of its
+ * memory at start-up.  They still pass every input and output buffer.
  *
  *   - The scratch is KDA_NO_ALLOC_SCRATCH_BYTES (64 MiB) of device memory that
  *     every GPU which loads the library holds until the process exits.
- *     Problems whose kda_prefill_workspace_size exceeds it are rejected with
- *     KDA_ERR_WORKSPACE before anything is enqueued.  The tensor-core path
- *     needs only the chunk table (16 bytes per chunk), so it fits for any
- *     practical batch; the fp32 CUDA-core path needs about 150 KB per chunk and
- *     value head (roughly 1,700 tokens x 16 heads at d = 128, chunk 64).
+ *     Problems whose workspace exceeds it are rejected with KDA_ERR_WORKSPACE
+ *     before anything is enqueued.
+ *   - The default two-kernel tensor-core form needs the chunk table and 57,856
+ *     bytes of chunk records per chunk and value head: about 1,150 chunk-heads
+ *     (some 4,600 tokens x 16 value heads at chunk 64) fit.  Larger problems run
+ *     the compact single-kernel form instead (as with KDA_FLAG_COMPACT: the chunk
+ *     table and a flag per sequence and value head, which fits any practical
+ *     batch), which is slower and takes a narrower per-channel decay range (see
+ *     KDA_DEVERR_DECAY_RANGE); kda_prefill_no_alloc_form() says which form a call
+ *     with these parameters runs.  The fp32 CUDA-core path needs about 150 KB per
+ *     chunk and value head (roughly 1,700 tokens x 16 heads at d = 128, chunk 64).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.  Later calls do no CUDA runtime work besides
- *     the kernel launches.
+ *     before any stream capture.  Later calls allocate nothing and enqueue
+ *     nothing on the stream but the kernel launches.
  *   - All calls share the one array and it keeps the last call's contents
  *     (nothing in it needs to start at zero).  Calls whose work overlaps on the
  *     GPU -- different streams, or different host threads -- race on it: order
@@ -410,6 +424,15 @@ kda_status_t kda_prefill_fwd_no_alloc(const kda_params_t *p, const void *q, cons
                                       const void *v, const float *beta, const float *log_decay,
                                       const uint32_t *input_row_offsets, const uint32_t *slot_idx,
                                       void *state_pool, float *o, void *stream);
+
+/*
+ * Which form kda_prefill_fwd_no_alloc runs for these parameters (no counterpart on
+ * the pages): 0 the two-kernel tensor-core form, 1 the compact single-kernel
+ * tensor-core form (the chunk records do not fit the scratch, or KDA_FLAG_COMPACT is
+ * set), 2 the fp32 CUDA-core path, -1 rejected (invalid parameters, or a workspace
+ * larger than KDA_NO_ALLOC_SCRATCH_BYTES).  Never touches the GPU.
+ */
+int kda_prefill_no_alloc_form(const kda_params_t *p);
 
 /*
  * Measurement aid (no counterpart on the pages).  Registers up to 8 CUDA events

@@ -1,8 +1,8 @@
 """kda_prefill_fwd_no_alloc: the prefill for callers that cannot allocate device memory.
 
-Such callers (code inside an engine that owns the device memory budget, code running
-under a stream capture that must not call cudaMalloc, runtimes that reserve all memory
-at start-up) get a prefill whose scratch is a fixed array inside the library.  This
+Such callers (code inside an engine that owns the device memory budget, runtimes that
+reserve all memory at start-up) get a prefill whose scratch is a fixed array inside the
+library.  This
 file is collected last so that a stop-at-first-failure run has already run every other
 test; it also passes on its own in a fresh process.
 """
@@ -64,6 +64,7 @@ def test_no_alloc_uses_the_single_kernel_form_when_records_do_not_fit():
     params = kda.make_params(num_seqs=3, num_k_heads=16, num_v_heads=16, d=128, num_slots=3,
                              total_tokens=6144, per_channel=False)
     assert kda.workspace_size(params) > _lib.KDA_NO_ALLOC_SCRATCH_BYTES
+    assert kda.no_alloc_form(params) == "compact"
     t = torch_io.prefill_inputs(p, "cuda:0")
     pool_ref = t["state_pool"].clone()
     o_ref = kda.prefill(**{**t, "state_pool": pool_ref}, chunk=64)
@@ -86,6 +87,11 @@ def test_no_alloc_rejects_problems_beyond_its_scratch():
     a = P(1 << 20)
     st = lib.kda_prefill_fwd_no_alloc(ctypes.byref(big), a, a, a, a, a, a, a, a, a, None)
     assert st == _lib.KDA_ERR_WORKSPACE
+    assert kda.no_alloc_form(big) == "rejected"
     small = kda.make_params(num_seqs=1, num_k_heads=2, num_v_heads=4, d=128, num_slots=1,
                             total_tokens=300, chunk=64)
     assert kda.workspace_size(small) <= _lib.KDA_NO_ALLOC_SCRATCH_BYTES
+    assert kda.no_alloc_form(small) == "two_kernel"
+    small_cc = kda.make_params(num_seqs=1, num_k_heads=2, num_v_heads=4, d=128, num_slots=1,
+                               total_tokens=300, chunk=64, cuda_cores=True)
+    assert kda.no_alloc_form(small_cc) == "cuda_cores"

@@ -2,12 +2,13 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-Headline workload: Gated DeltaNet prefill, 4 sequences x 4096 tokens, 16 heads, d=128,
-bf16 q/k/v, scalar decay, fp32 state, chunk 64 ("gdn_prefill").  A step is one
-kda_prefill_fwd call over that batch (every stage of the prefill path); the metric is
-prefill tokens/s.  The decode step (256 sequences x 32 heads, per-channel decay) is
-measured in the same run and reported under "also" as decode steps/s, and so is the
-speculative-decode verification (a 4-token window plus the fold of the accepted prefix).
+Headline workload: KDA prefill with per-channel decay, 2 sequences x 16384 tokens, 32 heads,
+d=128, bf16 q/k/v, fp32 state ~N(0, 0.02), chunk 64 ("kda_prefill", the largest of the
+single-GPU workloads).  A step is one kda_prefill_fwd call over that batch (every stage of
+the prefill path); the metric is prefill tokens/s.  The Gated DeltaNet prefill
+("gdn_prefill"), the ragged GQA prefill, the decode step (256 sequences x 32 heads) and the
+speculative-decode verification (a 4-token window plus the fold of the accepted prefix) are
+measured in the same run and reported under "also".
 
 Multi-GPU: every rank runs an independent replica on its own batch (sequences never
 interact, so nothing is exchanged); value = all ranks' tokens / the slowest rank's time.
@@ -92,11 +93,10 @@ PREFILL_STAGES = {
 }
 
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from the ncu
-# capture summarised in profiles/tc_front_tc_chain_gdn_prefill.md; a kernel changed since
-# its capture has no entry (reported as null).
-NCU_TRAFFIC = {("tc_front", "gdn_prefill"): 319.74e6, ("tc_chain", "gdn_prefill"): 417.88e6,
-               ("conv_kernel", "gdn_prefill"): 358.74e6}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a kernel on a
+# workload, from an ncu capture of the kernel as it is built now (see profiles/); a kernel
+# without a capture of its current build has no entry and is reported as null.
+NCU_TRAFFIC = {}
 
 
 def load_peaks() -> dict:
@@ -206,14 +206,38 @@ def aggregate(units_per_rank: float, seconds: float, world: int, device=None) ->
 
 # ----------------------------------------------------------------------------- CPU side
 
-def cpu_oracle_prefill(p, pair_fraction: float = 1.0):
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86 "model name", or the Arm implementer and
+    part numbers), with the count of online cores."""
+    name = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            info = f.read()
+        for key in ("model name", "Model", "cpu model"):
+            for line in info.splitlines():
+                if line.split(":")[0].strip() == key:
+                    name = line.split(":", 1)[1].strip()
+                    break
+            if name:
+                break
+        if not name:
+            impl = [ln.split(":")[1].strip() for ln in info.splitlines() if ln.startswith("CPU implementer")]
+            part = [ln.split(":")[1].strip() for ln in info.splitlines() if ln.startswith("CPU part")]
+            if impl and part:
+                name = f"Arm implementer {impl[0]} part {part[0]}"
+    except OSError:
+        pass
+    return f"{name or 'unknown CPU'}, {os.cpu_count()} cores online"
+
+
+def cpu_oracle_prefill(p, pair_fraction: float = 1.0, threads=None):
     """Times the fp64 oracle on (a seeded subset of) the workload's (sequence, head) pairs."""
     import oracle
     npairs = p.num_seqs * p.num_v_heads
     mask = np.zeros(npairs, np.uint8)
     take = max(1, int(round(npairs * pair_fraction)))
     mask[np.random.Generator(np.random.PCG64(7)).permutation(npairs)[:take]] = 1
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     t0 = time.perf_counter()
     oracle.run(p, pair_mask=mask, nthreads=threads)
     dt = time.perf_counter() - t0
@@ -237,7 +261,7 @@ def reference_arm(args, rank, world):
         secs += dt
     value = tok / secs if secs > 0 else 0.0
     sample = (f"{take} of {npairs} (sequence, value head) pairs of {args.workload} per step, "
-              f"fp64, {threads} threads")
+              f"fp64, {threads} threads on {cpu_model()}")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / max(args.steps, 1), "higher_is_better": True,
@@ -587,6 +611,30 @@ def time_verify(dev, steps, warmup):
     return p, total, {"verify_window": ms_v, "fold_accepted": ms_f}, acc_host
 
 
+def prefill_rooflines(p, stage_ms, stages, span_ms, peaks, tensor_cores) -> tuple:
+    """The dominant kernel's roofline (its share of the algorithmic bytes over its own
+    CUDA-event time) and the whole path's (all algorithmic bytes over the step's device span)."""
+    abytes = prefill_algorithmic_bytes(p)
+    dom = int(np.argmax(stage_ms))
+    name, parts = stages[dom]
+    dom_bytes = float(sum(abytes[x] for x in parts))
+    achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
+    tflops = tc_executed_flops(p) if tensor_cores else {}
+    roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": NCU_TRAFFIC.get((name, p.name)),
+                "peak_source": peaks["source"], "kernel_ms": stage_ms[dom],
+                "algorithmic_bytes_per_launch": dom_bytes,
+                "stage_ms": {n: m for (n, _), m in zip(stages, stage_ms)},
+                "tensor_tflops": tflops[name] / (stage_ms[dom] / 1e3) / 1e12 if name in tflops else None,
+                "tensor_peak_tflops": peaks["bf16_tflops"]}
+    path_bytes = float(sum(abytes.values()))
+    path = {"algorithmic_bytes": path_bytes, "achieved_gbs": path_bytes / (span_ms / 1e3) / 1e9,
+            "frac_hbm": path_bytes / (span_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+            "flops": prefill_flops(p)}
+    return roofline, path
+
+
 def ours_arm(args, rank, world, local):
     import torch
     import gated_delta_rule_deltanet_gb300 as kda
@@ -600,7 +648,7 @@ def ours_arm(args, rank, world, local):
     barrier(world)
     clocks = ClockSampler(local)
     clocks.start()
-    ms, stage_ms, t_dev, _, stages, _ = time_prefill(p, dev, args.steps, args.warmup)
+    ms, stage_ms, t_dev, _, stages, span_ms = time_prefill(p, dev, args.steps, args.warmup)
     tensor_cores = stages is PREFILL_STAGES[True]
     clk = clocks.stop()
     barrier(world)
@@ -608,28 +656,30 @@ def ours_arm(args, rank, world, local):
     value, slowest_s = aggregate(tokens * args.steps, ms * args.steps / 1e3, world, dev)
     ms_per_step = 1e3 * slowest_s / args.steps
     del t_dev
+    roofline, path_roofline = prefill_rooflines(p, stage_ms, stages, ms_per_step, peaks, tensor_cores)
 
     # end to end through the public API with host buffers
-    e2e_ms, h2d, d2h = time_prefill_e2e(p, dev, max(3, args.steps // 2), 3)
+    e2e_ms, h2d, d2h = time_prefill_e2e(p, dev, max(3, min(args.steps // 2, 200)), 3)
     e2e_value, _ = aggregate(tokens, e2e_ms / 1e3, world, dev)
 
-    # roofline of the dominant kernel (its share of the algorithmic bytes / its time)
-    abytes = prefill_algorithmic_bytes(p)
-    dom = int(np.argmax(stage_ms))
-    name, parts = stages[dom]
-    dom_bytes = float(sum(abytes[x] for x in parts))
-    achieved = dom_bytes / (stage_ms[dom] / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": name, "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": NCU_TRAFFIC.get((name, p.name)),
-                "peak_source": peaks["source"], "kernel_ms": stage_ms[dom],
-                "stage_ms": {n: m for (n, _), m in zip(stages, stage_ms)},
-                "tensor_tflops": tc_executed_flops(p)[name] / (stage_ms[dom] / 1e3) / 1e12
-                if tensor_cores and name in tc_executed_flops(p) else None,
-                "tensor_peak_tflops": peaks["bf16_tflops"]}
-    path_bytes = float(sum(abytes.values()))
     also = []
     if not args.no_decode:
+        for wname in ("gdn_prefill", "kda_prefill", "ragged_gqa_kda"):
+            if wname == p.name:
+                continue
+            wp = workloads.workload(wname)
+            # 30 steps of well under a millisecond to a millisecond: a host stall between two
+            # steps would dominate the wall-clock mean, so the line reports the mean device
+            # span of a step
+            _, wst, wt, _, wstages, wms = time_prefill(wp, dev, 30, 3)
+            del wt
+            wroof, wpath = prefill_rooflines(wp, wst, wstages, wms, peaks,
+                                             wstages is PREFILL_STAGES[True])
+            wval, _ = aggregate(float(wp.total_tokens), wms / 1e3, world, dev)
+            also.append({"workload": wname, "metric": "prefill tokens/s", "value": wval,
+                         "unit": "tokens/s", "ms_per_step": wms, "roofline": wroof,
+                         "path_roofline": wpath})
+
         dp = workloads.workload("kda_decode")
         dms = time_decode(dp, dev, max(args.steps, 20), max(args.warmup, 3))
         dbytes = float(sum(decode_algorithmic_bytes(dp).values()))
@@ -641,39 +691,25 @@ def ours_arm(args, rank, world, local):
                                   "achieved": dbytes / (dms / 1e3) / 1e9,
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": dbytes / (dms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                                  "traffic": None}})
+                                  "algorithmic_bytes_per_launch": dbytes,
+                                  "traffic": NCU_TRAFFIC.get(("decode_step", "kda_decode"))}})
         vp, vms, vstage, vacc = time_verify(dev, max(args.steps, 20), max(args.warmup, 3))
         vbytes = verify_algorithmic_bytes(vp, vacc)
         vval, _ = aggregate(float(vp.num_seqs * VERIFY_WINDOW), vms / 1e3, world, dev)
-        vk = max(vstage, key=vstage.get)
+        vroof = {}
+        for vk in ("verify_window", "fold_accepted"):
+            vroof[vk] = {"bound": "hbm", "kernel": vk,
+                         "achieved": vbytes[vk] / (vstage[vk] / 1e3) / 1e9,
+                         "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": vbytes[vk] / (vstage[vk] / 1e3) / 1e9 / peaks["hbm_gbs"],
+                         "algorithmic_bytes_per_launch": vbytes[vk],
+                         "traffic": NCU_TRAFFIC.get((vk, "kda_verify"))}
         also.append({"workload": "kda_verify (256 seq x 32 heads, d=128, window 4, "
                                  "accepted 0..4 per sequence)",
                      "metric": "verified draft tokens/s", "value": vval, "unit": "tokens/s",
                      "ms_per_step": vms, "stage_ms": vstage,
-                     "roofline": {"bound": "hbm", "kernel": vk,
-                                  "achieved": vbytes[vk] / (vstage[vk] / 1e3) / 1e9,
-                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": vbytes[vk] / (vstage[vk] / 1e3) / 1e9
-                                  / peaks["hbm_gbs"], "traffic": None}})
+                     "roofline": vroof["verify_window"], "fold_roofline": vroof["fold_accepted"]})
 
-    if not args.no_decode:
-        for wname in ("kda_prefill", "ragged_gqa_kda"):
-            wp = workloads.workload(wname)
-            # 30 steps of a millisecond: a host stall between two steps would dominate the
-            # wall-clock mean, so the line reports the mean device span of a step
-            _, wst, wt, _, wstages, wms = time_prefill(wp, dev, 30, 3)
-            del wt
-            wbytes = float(sum(prefill_algorithmic_bytes(wp).values()))
-            wval, _ = aggregate(float(wp.total_tokens), wms / 1e3, world, dev)
-            also.append({"workload": wname, "metric": "prefill tokens/s", "value": wval,
-                         "unit": "tokens/s", "ms_per_step": wms,
-                         "stage_ms": {n: m for (n, _), m in zip(wstages, wst)},
-                         "path_roofline": {"algorithmic_bytes": wbytes,
-                                           "achieved_gbs": wbytes / (wms / 1e3) / 1e9,
-                                           "frac_hbm": wbytes / (wms / 1e3) / 1e9
-                                           / peaks["hbm_gbs"]}})
-
-    if not args.no_decode:
         gp = workloads.workload("gdp_prefill")
         gms = time_gdp_prefill(gp, dev, 30, 3)
         gval, _ = aggregate(float(gp.total_tokens), gms / 1e3, world, dev)
@@ -682,11 +718,11 @@ def ours_arm(args, rank, world, local):
                      "metric": "prefill tokens/s", "value": gval, "unit": "tokens/s",
                      "ms_per_step": gms, "virtual_tokens_per_s": gval * gp.n_h})
 
-    if not args.no_decode:
-        bms, bws = time_prefill_bwd(p, dev, 10, 3)
-        bval, _ = aggregate(float(p.total_tokens), bms / 1e3, world, dev)
-        bbytes = backward_algorithmic_bytes(p)
-        also.append({"workload": f"{p.name} backward (kda_prefill_bwd, fp32 CUDA cores)",
+        bp = workloads.workload("gdn_prefill")
+        bms, bws = time_prefill_bwd(bp, dev, 10, 3)
+        bval, _ = aggregate(float(bp.total_tokens), bms / 1e3, world, dev)
+        bbytes = backward_algorithmic_bytes(bp)
+        also.append({"workload": f"{bp.name} backward (kda_prefill_bwd)",
                      "metric": "backward tokens/s", "value": bval, "unit": "tokens/s",
                      "ms_per_step": bms, "workspace_bytes": bws,
                      "path_roofline": {"algorithmic_bytes": bbytes,
@@ -694,40 +730,42 @@ def ours_arm(args, rank, world, local):
                                        "frac_hbm": bbytes / (bms / 1e3) / 1e9
                                        / peaks["hbm_gbs"]}})
 
-    if not args.no_decode:
-        cms = time_conv_gates(p, dev, 50, 3)
-        cval, _ = aggregate(float(p.total_tokens), cms / 1e3, world, dev)
-        cbytes = conv_algorithmic_bytes(p)
-        also.append({"workload": f"{p.name} front end (kda_conv_gates_fwd: conv width "
+        cms = time_conv_gates(bp, dev, 50, 3)
+        cval, _ = aggregate(float(bp.total_tokens), cms / 1e3, world, dev)
+        cbytes = conv_algorithmic_bytes(bp)
+        also.append({"workload": f"{bp.name} front end (kda_conv_gates_fwd: conv width "
                                  f"{CONV_WIDTH} + SiLU over [Q | K | V], gates)",
                      "metric": "tokens/s", "value": cval, "unit": "tokens/s", "ms_per_step": cms,
                      "roofline": {"bound": "hbm", "kernel": "conv_gates (three launches)",
                                   "achieved": cbytes / (cms / 1e3) / 1e9,
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": cbytes / (cms / 1e3) / 1e9 / peaks["hbm_gbs"],
-                                  "traffic": NCU_TRAFFIC.get(("conv_kernel", p.name))}})
+                                  "traffic": NCU_TRAFFIC.get(("conv_kernel", bp.name))}})
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
         rate, dt, threads, take, npairs = cpu_oracle_prefill(p, 1.0)
+        one = max(1, npairs // 32)
+        rate1, dt1, _, take1, _ = cpu_oracle_prefill(p, one / npairs, threads=1)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{take} of {npairs} (sequence, value head) pairs of {p.name} "
-                         f"(the whole workload), fp64, {dt:.1f} s"}
+                         f"(the whole workload), fp64, {threads} threads, {dt:.1f} s",
+               "one_thread": {"value": rate1, "unit": UNIT, "cores": 1,
+                              "sample": f"{take1} of {npairs} pairs, 1 thread, {dt1:.1f} s"},
+               "cpu": cpu_model()}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f16" if tensor_cores else "f32",
-                "accumulate": "f32", "data": "synthetic",
+                "qkv_dtype": p.qkv_dtype, "mma_operands": "f16" if tensor_cores else None,
+                "accumulate": "f32", "state_dtype": p.state_dtype, "data": "synthetic",
                 "config": {**workload_config(p),
-                           "l2": f"inputs larger than L2 ({path_bytes / 1e6:.0f} MB moved "
-                                 f"per step vs 129 MB L2); no flush"},
-                "path_roofline": {"algorithmic_bytes": path_bytes,
-                                  "achieved_gbs": path_bytes / (ms_per_step / 1e3) / 1e9,
-                                  "frac_hbm": path_bytes / (ms_per_step / 1e3) / 1e9
-                                  / peaks["hbm_gbs"],
-                                  "flops": prefill_flops(p)},
+                           "l2": f"inputs larger than L2 ({path_roofline['algorithmic_bytes'] / 1e6:.0f} "
+                                 f"MB moved per step vs 129 MB L2); no flush"},
+                "path_roofline": path_roofline,
                 "roofline": roofline, "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                         "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -736,22 +774,44 @@ def ours_arm(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+def profile_arm(args):
+    """W + K steps of one piece, for an ncu capture (no JSON line; nothing reported here is
+    a bench value): `prefill` on --workload, `decode` on kda_decode, `verify` on the
+    256-sequence window of 4 plus the fold."""
+    import torch
+    import gated_delta_rule_deltanet_gb300 as kda
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kda.load()
+    if args.profile == "prefill":
+        ms = time_prefill(workloads.workload(args.workload), dev, args.steps, args.warmup)[0]
+    elif args.profile == "decode":
+        ms = time_decode(workloads.workload("kda_decode"), dev, args.steps, args.warmup)
+    else:
+        ms = time_verify(dev, args.steps, args.warmup)[1]
+    print(f"profile {args.profile}: {args.warmup} + {args.steps} steps, {ms:.4f} ms per step")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gdn_prefill",
+    ap.add_argument("--workload", default="kda_prefill",
                     choices=[w for w in workloads.WORKLOADS if w != "kda_decode"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--profile", choices=["prefill", "decode", "verify"],
+                    help="run W + K steps of one piece for a profiler, print no JSON line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_setup()
     try:
-        if args.impl == "reference":
+        if args.profile:
+            profile_arm(args)
+        elif args.impl == "reference":
             reference_arm(args, rank, world)
         else:
             ours_arm(args, rank, world, local)

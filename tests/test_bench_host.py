@@ -1,6 +1,7 @@
 """Host-side pieces of bench.py that feed its JSON line, checked on CPU: the algorithmic byte
 and tensor-core FLOP models against hand counts for the gdn_prefill shapes, and the reference
-arm's line (the oracle timed on the host) against the contract's keys."""
+arm's line (the oracle timed on the host, on the kda_prefill headline workload) against the
+contract's keys."""
 import json
 import os
 import subprocess
@@ -74,7 +75,7 @@ def test_reference_arm_prints_the_contract_line():
     assert line["metric"] == "prefill tokens/s" and line["unit"] == "tokens/s"
     assert line["value"] > 0 and line["higher_is_better"] is True
     assert line["steps"] == 1 and line["warmup"] == 3 and line["n_gpus"] == 1
-    assert line["config"]["workload"] == "gdn_prefill"
+    assert line["config"]["workload"] == "kda_prefill"
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0

@@ -8,142 +8,290 @@
 // and write steps of the KDA update ("You Could Have Come Up With Kimi Delta
 // Attention", sec. 4) exactly: S <- S Diag(alpha) + e k^T.
 //
-// Both kernels use the decode step's layout: one CTA per (sequence, value head),
-// each thread holding 16-byte column groups of several state rows in registers,
-// reductions over key channels by warp shuffles plus one shared-memory combine.
+// The verify kernel: one CTA per (sequence, value head); warp w owns the value columns
+// [CW w, CW w + CW) of the state with all d_k key rows, lane = (row group, column
+// quad): RPT consecutive key rows x 4 value columns in registers.  Every sum over key
+// channels (the prediction S k^, the read S q^, the norms of k and q) is a sum over the
+// lane's rows followed by shuffles between the row-group lanes of its warp: no shared
+// memory reduction and no block barrier inside the token loop.
+#include <algorithm>
+
 #include "kda_common.cuh"
+#include "tc_utils.cuh"
+
 
 namespace kda {
 
-// DELTA = false: the additive write (no prediction), a template parameter so that the
-// delta rule's code carries no test of it
-template <int D, int NT, bool QBF16, bool SBF16, bool PERCH, bool DELTA>
-__global__ void __launch_bounds__(NT) verify_window_kernel(Problem P, int window, float* ring,
-                                                           int rec) {
-  constexpr int VEC = 4;
-  constexpr int TPR = D / VEC;
-  constexpr int RPP = NT / TPR;
-  constexpr int RPT = D / RPP;
-  constexpr int NWARP = NT / 32;
-  // token inputs double-buffered: token t + 1's are written while token t is worked on and
-  // published by token t's second reduction, so a token costs two barriers (its reductions)
-  __shared__ float s_k[2][D], s_q[2][D], s_a[2][D];
-  __shared__ float s_red[2][NWARP][D];
-  __shared__ float s_scale[2][2];
-  static_assert(NT >= D, "one key channel per thread");
+// polls before a wait on a copy is declared stuck
+__host__ __device__ constexpr uint32_t kda_wait_limit() { return 1u << 22; }
 
-  const int HV = P.HV;
-  const int64_t bh = blockIdx.x;
-  const int b = static_cast<int>(bh / HV), h = static_cast<int>(bh % HV);
-  const int kh = h / (HV / P.HK);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int cg = tid % TPR, r0 = tid / TPR;
+template <int D, int NT>
+struct VerifyMap {
+  static constexpr int NW = NT / 32;     // warps
+  static constexpr int CW = D / NW;      // value columns per warp
+  static constexpr int NQ = CW / 4;      // column quads per warp
+  static constexpr int NG = 32 / NQ;     // row groups per warp
+  static constexpr int RPT = D / NG;     // key rows per lane
+  static_assert(CW % 4 == 0 && 32 % NQ == 0 && D % NG == 0, "value columns in quads over the warps");
+};
 
-  const uint32_t slot = P.slot_idx[b];
-  if (slot >= static_cast<uint32_t>(P.num_slots)) {
-    if (tid == 0) raise_device_error(P.err, KDA_DEVERR_SLOT_RANGE);
-    return;
-  }
-  const int64_t state_base = (static_cast<int64_t>(slot) * HV + h) * D * D;
-  float4 S[RPT];
+// sum over the row-group lanes of a warp (lanes that differ in the bits above the quad bits)
+template <int NQ>
+__device__ __forceinline__ float rowgroup_sum(float x) {
 #pragma unroll
-  for (int i = 0; i < RPT; ++i)
-    S[i] = load4<SBF16>(P.pool, state_base + static_cast<int64_t>(r0 + i * RPP) * D + cg * VEC);
+  for (int off = NQ; off < 32; off <<= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
 
-  auto reduce_rows = [&](float4 p, int buf) -> float4 {
+// N consecutive q/k/v elements (bf16 or fp32) at p, widened to fp32: 16-byte loads where N
+// and the alignment allow (N % 8 for bf16, N % 4 for fp32), else element by element
+template <bool BF16, int N>
+__device__ __forceinline__ void load_row(const unsigned char* p, float* x) {
+  if constexpr (BF16 && N % 8 == 0) {
 #pragma unroll
-    for (int off = TPR; off < 32; off <<= 1) {
-      p.x += __shfl_xor_sync(0xffffffffu, p.x, off);
-      p.y += __shfl_xor_sync(0xffffffffu, p.y, off);
-      p.z += __shfl_xor_sync(0xffffffffu, p.z, off);
-      p.w += __shfl_xor_sync(0xffffffffu, p.w, off);
-    }
-    if (lane < TPR) *reinterpret_cast<float4*>(&s_red[buf][warp][cg * VEC]) = p;
-    __syncthreads();
-    float4 tot = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e = 0; e < N; e += 8) tc::bf16x8_load(p + 2 * e, x + e);
+  } else if constexpr (!BF16 && N % 4 == 0) {
 #pragma unroll
-    for (int w = 0; w < NWARP; ++w) {
-      const float4 x = *reinterpret_cast<const float4*>(&s_red[buf][w][cg * VEC]);
-      tot.x += x.x; tot.y += x.y; tot.z += x.z; tot.w += x.w;
+    for (int e = 0; e < N; e += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + 4 * e);
+      x[e] = v.x; x[e + 1] = v.y; x[e + 2] = v.z; x[e + 3] = v.w;
     }
-    return tot;
-  };
-
-  auto stage = [&](int t) {                     // token t's k, q, alpha into buffer t & 1
-    const int64_t row_t = static_cast<int64_t>(b) * window + t;
-    if (tid < D) {
-      const int bt = t & 1;
-      s_k[bt][tid] = load_elem<QBF16>(P.k, row_t * P.k_stride + static_cast<int64_t>(kh) * D + tid);
-      s_q[bt][tid] = load_elem<QBF16>(P.q, row_t * P.q_stride + static_cast<int64_t>(kh) * D + tid);
-      s_a[bt][tid] = expf(PERCH ? P.g[(row_t * HV + h) * D + tid] : P.g[row_t * HV + h]);
-    }
-  };
-  stage(0);
-  __syncthreads();
-  for (int t = 0; t < window; ++t) {
-    const int64_t row_t = static_cast<int64_t>(b) * window + t;
-    const int bt = t & 1;
-    const float* sk = s_k[bt];
-    const float* sq = s_q[bt];
-    const float* sa = s_a[bt];
-    // the L2 norms of k and q (warps 0 and 1), published by the first reduction below: the
-    // products before it use the raw k and q and take the scales afterwards (they are linear)
-    if (warp < 2) {
-      constexpr int kStep = NWARP > 1 ? 2 : 1;
-      for (int which = NWARP > 1 ? warp : 0; which < 2; which += kStep) {
-        const float* x = which == 0 ? sk : sq;
-        float ss = 0.f;
-        for (int c = lane; c < D; c += 32) ss += x[c] * x[c];
-        ss = warp_sum(ss);
-        if (lane == 0) {
-          const float inv = P.l2norm ? rsqrtf(ss + 1e-6f) : 1.f;
-          s_scale[bt][which] = which == 0 ? inv : inv * P.scale;
-        }
-      }
-    }
-    const float vbeta = P.beta[row_t * HV + h];
-    const float4 vv = load4<QBF16>(P.v, row_t * P.v_stride + static_cast<int64_t>(h) * D + cg * VEC);
-
-    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const int r = r0 + i * RPP;
-      const float a = sa[r], kr = sk[r];
-      S[i].x *= a; S[i].y *= a; S[i].z *= a; S[i].w *= a;
-      part.x += S[i].x * kr; part.y += S[i].y * kr; part.z += S[i].z * kr; part.w += S[i].w * kr;
-    }
-    // additive write (no delta rule): nothing is predicted, e = beta v
-    float4 vhat = make_float4(0.f, 0.f, 0.f, 0.f);
-    if constexpr (DELTA) vhat = reduce_rows(part, 0);
-    else __syncthreads();
-    const float kscale = s_scale[bt][0], qscale = s_scale[bt][1];
-    vhat.x *= kscale; vhat.y *= kscale; vhat.z *= kscale; vhat.w *= kscale;
-    const float4 e = make_float4(vbeta * (vv.x - vhat.x), vbeta * (vv.y - vhat.y),
-                                 vbeta * (vv.z - vhat.z), vbeta * (vv.w - vhat.w));
-    float4 opart = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const int r = r0 + i * RPP;
-      const float kc = sk[r] * kscale, qr = sq[r];
-      S[i].x += kc * e.x; S[i].y += kc * e.y; S[i].z += kc * e.z; S[i].w += kc * e.w;
-      opart.x += S[i].x * qr; opart.y += S[i].y * qr; opart.z += S[i].z * qr; opart.w += S[i].w * qr;
-    }
-    // the record of this token: [k^ | e | alpha]
-    float* rec_p = ring + (row_t * HV + h) * rec;
-    if (tid < D) {
-      rec_p[tid] = sk[tid] * kscale;
-      if (PERCH) rec_p[2 * D + tid] = sa[tid];
-    }
-    if (!PERCH && tid == 0) rec_p[2 * D] = sa[0];
-    if (r0 == 0) *reinterpret_cast<float4*>(rec_p + D + cg * VEC) = e;
-    // the next token into the other buffer (last read before this token's first barrier)
-    if (t + 1 < window) stage(t + 1);
-    float4 o = reduce_rows(opart, 1);
-    o.x *= qscale; o.y *= qscale; o.z *= qscale; o.w *= qscale;
-    if (r0 == 0) *reinterpret_cast<float4*>(P.o + (row_t * HV + h) * D + cg * VEC) = o;
+    for (int e = 0; e < N; ++e)
+      x[e] = BF16 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(p)[e]) << 16)
+                  : reinterpret_cast<const float*>(p)[e];
   }
 }
 
+// N consecutive fp32 values to global memory (float4 stores when N % 4 == 0)
+template <int N>
+__device__ __forceinline__ void store_rows(float* p, const float* x, float scale) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int e = 0; e < N; e += 4)
+      *reinterpret_cast<float4*>(p + e) = make_float4(x[e] * scale, x[e + 1] * scale, x[e + 2] * scale,
+                                                      x[e + 3] * scale);
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) p[e] = x[e] * scale;
+  }
+}
+
+// Shared-memory map of the verify kernel: the state buffer (the next pair's state, bulk-copied
+// while the current pair is worked on), then two groups of staged token inputs.
+template <int D, bool QBF16, bool SBF16, bool PERCH>
+struct VerifySmem {
+  static constexpr int ES = QBF16 ? 2 : 4;
+  static constexpr int TB = 8;                 // tokens per staged group
+  static constexpr int GW = PERCH ? D : 4;     // log-decay floats staged per token
+  static constexpr int STATE = D * D * (SBF16 ? 2 : 4);
+  static constexpr int O_K = 0, O_Q = O_K + TB * D * ES, O_V = O_Q + TB * D * ES;
+  static constexpr int O_G = O_V + TB * D * ES, O_B = O_G + TB * GW * 4, BUF = O_B + TB * 4;
+  static constexpr int BYTES = STATE + 2 * BUF;
+  static_assert(STATE % 16 == 0 && BUF % 16 == 0, "16-byte aligned pieces");
+};
+
+// Persistent: each CTA walks the (sequence, value head) pairs blockIdx.x, blockIdx.x + gridDim.x,
+// ...  A pair's state arrives in shared memory by one bulk copy issued while the previous pair
+// is worked on, and is moved into registers at the pair's start; its window's token inputs
+// arrive in groups of TB tokens by cp.async, each group staged while the one before it is
+// worked on (the next pair's first group while this pair's last group is).  The token loop
+// itself has no barrier and no global load.
+// DELTA = false: the additive write (no prediction), a template parameter so that the
+// delta rule's code carries no test of it
+template <int D, int NT, bool QBF16, bool SBF16, bool PERCH, bool DELTA>
+__global__ void __launch_bounds__(NT, 2) verify_window_kernel(Problem P, int window, float* ring,
+                                                              int rec, int npairs) {
+  using M = VerifyMap<D, NT>;
+  using L = VerifySmem<D, QBF16, SBF16, PERCH>;
+  constexpr int RPT = M::RPT, NQ = M::NQ, ES = L::ES, TB = L::TB, GW = L::GW;
+  extern __shared__ __align__(128) unsigned char vsmem[];
+  __shared__ uint64_t s_sbar;                  // bulk copy of a pair's state
+  unsigned char* const sstate = vsmem;
+  unsigned char* const sbuf = vsmem + L::STATE;
+
+  const int HV = P.HV;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cq = lane % NQ, rg = lane / NQ;
+  const int col = warp * M::CW + 4 * cq;       // this lane's 4 value columns
+  const int row0 = rg * RPT;                   // and its key rows [row0, row0 + RPT)
+  const int ngroups = (window + TB - 1) / TB;
+
+  auto slot_of = [&](int pr) -> uint32_t { return P.slot_idx[pr / HV]; };
+  auto valid = [&](int pr) -> bool { return slot_of(pr) < static_cast<uint32_t>(P.num_slots); };
+  // one thread: the bulk copy of pair pr's state into the state buffer
+  auto copy_state = [&](int pr) {
+    const int64_t base = (static_cast<int64_t>(slot_of(pr)) * HV + pr % HV) * D * D;
+    tc::mbar_arrive_expect_tx(&s_sbar, L::STATE);
+    tc::bulk_load(tc::smem_u32(sstate), static_cast<const char*>(P.pool) + base * (SBF16 ? 2 : 4),
+                  L::STATE, &s_sbar);
+  };
+  // cp.async copies of tokens [TB gi, TB gi + TB) of pair pr's window into group buffer bi
+  auto stage = [&](int pr, int gi, int bi) {
+    const int b = pr / HV, h = pr % HV, kh = h / (HV / P.HK);
+    const uint32_t sb = tc::smem_u32(sbuf + bi * L::BUF);
+    const int t0 = TB * gi, nt = min(TB, window - t0);
+    constexpr int PR = D * ES / 16;            // 16-byte pieces of a k, q or v row
+    for (int u = tid; u < nt * PR; u += NT) {
+      const int t = u / PR, pc = u % PR;
+      const int64_t row_t = static_cast<int64_t>(b) * window + t0 + t;
+      const char* kp = static_cast<const char*>(P.k) + (row_t * P.k_stride + static_cast<int64_t>(kh) * D) * ES;
+      const char* qp = static_cast<const char*>(P.q) + (row_t * P.q_stride + static_cast<int64_t>(kh) * D) * ES;
+      const char* vp = static_cast<const char*>(P.v) + (row_t * P.v_stride + static_cast<int64_t>(h) * D) * ES;
+      tc::cp_async16(sb + L::O_K + (t * D * ES) + 16 * pc, kp + 16 * pc, 16u);
+      tc::cp_async16(sb + L::O_Q + (t * D * ES) + 16 * pc, qp + 16 * pc, 16u);
+      tc::cp_async16(sb + L::O_V + (t * D * ES) + 16 * pc, vp + 16 * pc, 16u);
+    }
+    if constexpr (PERCH) {
+      for (int u = tid; u < nt * (D / 4); u += NT) {
+        const int t = u / (D / 4), pc = u % (D / 4);
+        const int64_t row_t = static_cast<int64_t>(b) * window + t0 + t;
+        tc::cp_async16(sb + L::O_G + t * GW * 4 + 16 * pc, P.g + (row_t * HV + h) * D + 4 * pc, 16u);
+      }
+    }
+    if (tid < nt) {
+      const int64_t row_t = static_cast<int64_t>(b) * window + t0 + tid;
+      if (!PERCH) tc::cp_async4(sb + L::O_G + tid * GW * 4, P.g + row_t * HV + h, 4u);
+      tc::cp_async4(sb + L::O_B + tid * 4, P.beta + row_t * HV + h, 4u);
+    }
+    tc::cp_async_commit();
+  };
+
+  const int p0 = blockIdx.x;
+  if (tid == 0) {
+    tc::mbar_init(&s_sbar, 1);
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0 && valid(p0)) copy_state(p0);
+  stage(p0, 0, 0);
+  uint32_t sphase = 0;                         // state copies waited for
+  int gcount = 0;                              // token groups consumed (buffer gcount % 2)
+  bool abort = false;
+  for (int pr = p0; pr < npairs && !abort; pr += gridDim.x) {
+    const int b = pr / HV, h = pr % HV;
+    const bool ok_slot = valid(pr);            // block-uniform
+    const int pn = pr + gridDim.x;
+    float2 S01[RPT], S23[RPT];                 // the lane's state: columns (0, 1) and (2, 3)
+    if (ok_slot) {
+      const bool got = tc::mbar_wait_bounded(&s_sbar, sphase & 1, kda_wait_limit());
+      if (__syncthreads_or(!got)) {            // sphase still names the copy in flight
+        if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+        abort = true;
+        break;
+      }
+      ++sphase;
+#pragma unroll
+      for (int i = 0; i < RPT; ++i) {
+        const float4 v = load4<SBF16>(sstate, static_cast<int64_t>(row0 + i) * D + col);
+        S01[i] = make_float2(v.x, v.y);
+        S23[i] = make_float2(v.z, v.w);
+      }
+    } else if (tid == 0) {
+      raise_device_error(P.err, KDA_DEVERR_SLOT_RANGE);
+    }
+    __syncthreads();                           // the state buffer has been read
+    if (tid == 0 && pn < npairs && valid(pn)) {
+      tc::fence_async_smem();
+      copy_state(pn);
+    }
+    for (int gi = 0; gi < ngroups; ++gi, ++gcount) {
+      unsigned char* buf = sbuf + (gcount & 1) * L::BUF;
+      const int nt = min(TB, window - TB * gi);
+      tc::cp_async_wait_all();
+      __syncthreads();                         // this group staged; the other buffer free
+      if (gi + 1 < ngroups) stage(pr, gi + 1, (gcount + 1) & 1);
+      else if (pn < npairs) stage(pn, 0, (gcount + 1) & 1);
+      // the group's decays alpha = exp(g), once per value (every lane reads its rows' alphas)
+      for (int u = tid; u < nt * (PERCH ? D : 1); u += NT) {
+        float* gp = reinterpret_cast<float*>(buf + L::O_G) + (PERCH ? u : u * GW);
+        *gp = __expf(*gp);
+      }
+      __syncthreads();
+      if (!ok_slot) continue;
+      for (int t = 0; t < nt; ++t) {
+        const int64_t row_t = static_cast<int64_t>(b) * window + TB * gi + t;
+        float kr[RPT], a[RPT];
+        load_row<QBF16, RPT>(buf + L::O_K + (t * D + row0) * ES, kr);
+        if constexpr (PERCH) {
+          load_row<false, RPT>(buf + L::O_G + (t * GW + row0) * 4, a);
+        } else {
+          const float a0 = *reinterpret_cast<const float*>(buf + L::O_G + t * GW * 4);
+#pragma unroll
+          for (int i = 0; i < RPT; ++i) a[i] = a0;
+        }
+        float* rec_p = ring + (row_t * HV + h) * rec;   // the record of this token: [k^ | e | alpha]
+        if (warp == 0 && cq == 0) {
+          if (PERCH) store_rows<RPT>(rec_p + 2 * D + row0, a, 1.f);
+          else if (rg == 0) rec_p[2 * D] = a[0];
+        }
+        // forget and predict (raw k; its norm applies after the sum, which is linear); the
+        // state's 4 columns as two pairs, two-wide arithmetic
+        float2 p01 = make_float2(0.f, 0.f), p23 = make_float2(0.f, 0.f);
+        float ssk = 0.f;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+          const float2 ai = make_float2(a[i], a[i]), ki = make_float2(kr[i], kr[i]);
+          S01[i] = mul2(S01[i], ai);
+          S23[i] = mul2(S23[i], ai);
+          if constexpr (DELTA) {
+            p01 = fma2(S01[i], ki, p01);
+            p23 = fma2(S23[i], ki, p23);
+          }
+          ssk += kr[i] * kr[i];
+        }
+        ssk = rowgroup_sum<NQ>(ssk);
+        const float kscale = P.l2norm ? rsqrtf(ssk + 1e-6f) : 1.f;
+        float4 vhat = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (DELTA) {
+          vhat.x = rowgroup_sum<NQ>(p01.x) * kscale; vhat.y = rowgroup_sum<NQ>(p01.y) * kscale;
+          vhat.z = rowgroup_sum<NQ>(p23.x) * kscale; vhat.w = rowgroup_sum<NQ>(p23.y) * kscale;
+        }
+        float vv[4];
+        load_row<QBF16, 4>(buf + L::O_V + (t * D + col) * ES, vv);
+        const float beta = *reinterpret_cast<const float*>(buf + L::O_B + 4 * t);
+        const float4 e = make_float4(beta * (vv[0] - vhat.x), beta * (vv[1] - vhat.y),
+                                     beta * (vv[2] - vhat.z), beta * (vv[3] - vhat.w));
+        const float2 e01 = make_float2(e.x, e.y), e23 = make_float2(e.z, e.w);
+        // write and read (k reloaded from shared memory rather than kept across the sums)
+        float qr[RPT];
+        load_row<QBF16, RPT>(buf + L::O_Q + (t * D + row0) * ES, qr);
+        load_row<QBF16, RPT>(buf + L::O_K + (t * D + row0) * ES, kr);
+        float2 o01 = make_float2(0.f, 0.f), o23 = make_float2(0.f, 0.f);
+        float ssq = 0.f;
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+          const float2 kc = make_float2(kr[i] * kscale, kr[i] * kscale), qi = make_float2(qr[i], qr[i]);
+          S01[i] = fma2(kc, e01, S01[i]);
+          S23[i] = fma2(kc, e23, S23[i]);
+          o01 = fma2(S01[i], qi, o01);
+          o23 = fma2(S23[i], qi, o23);
+          ssq += qr[i] * qr[i];
+        }
+        ssq = rowgroup_sum<NQ>(ssq);
+        const float qscale = (P.l2norm ? rsqrtf(ssq + 1e-6f) : 1.f) * P.scale;
+        float4 o;
+        o.x = rowgroup_sum<NQ>(o01.x) * qscale; o.y = rowgroup_sum<NQ>(o01.y) * qscale;
+        o.z = rowgroup_sum<NQ>(o23.x) * qscale; o.w = rowgroup_sum<NQ>(o23.y) * qscale;
+        // k^ and e into the record, and the output
+        if (warp == 0 && cq == 0) store_rows<RPT>(rec_p + row0, kr, kscale);
+        if (rg == 0) {
+          *reinterpret_cast<float4*>(rec_p + D + col) = e;
+          *reinterpret_cast<float4*>(P.o + (row_t * HV + h) * D + col) = o;
+        }
+      }
+    }
+  }
+  // nothing may still be landing in shared memory when the CTA exits: the last staged token
+  // group, and (after an abort) a state copy in flight
+  tc::cp_async_wait_all();
+  if (abort && tid == 0) tc::mbar_wait_bounded(&s_sbar, sphase & 1, kda_wait_limit());
+}
+
+// The fold keeps the decode step's layout: thread = 16-byte column group of several state
+// rows; k^ and alpha of each record pass through shared memory (one or two barriers per
+// accepted record, few per sequence).
 template <int D, int NT, bool SBF16, bool PERCH>
 __global__ void __launch_bounds__(NT) fold_accepted_kernel(Problem P, int window, const float* ring,
                                                            int rec, const uint32_t* accepted) {
@@ -211,15 +359,31 @@ __global__ void __launch_bounds__(NT) fold_accepted_kernel(Problem P, int window
 // [k^ (D) | e (D) | alpha (D per channel, or 1 padded to 4 so records stay 16-byte aligned)]
 int ring_record_elems(int D, bool perch) { return D + D + (perch ? D : 4); }
 
+// SMs of the current device (cached per device)
+static int sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 template <int D, int NT, bool Q, bool SB, bool PC>
 static cudaError_t launch_verify_t(const Problem& P, int window, float* ring, cudaStream_t s) {
-  const int64_t blocks = static_cast<int64_t>(P.num_seqs) * P.HV;
-  if (P.flags & KDA_FLAG_NO_DELTA)
-    verify_window_kernel<D, NT, Q, SB, PC, false><<<dim3(static_cast<unsigned>(blocks)), NT, 0, s>>>(
-        P, window, ring, ring_record_elems(D, PC));
-  else
-    verify_window_kernel<D, NT, Q, SB, PC, true><<<dim3(static_cast<unsigned>(blocks)), NT, 0, s>>>(
-        P, window, ring, ring_record_elems(D, PC));
+  const int64_t pairs = static_cast<int64_t>(P.num_seqs) * P.HV;
+  // two resident CTAs per SM walk the pairs
+  const int grid = static_cast<int>(std::min<int64_t>(pairs, 2 * static_cast<int64_t>(sm_count())));
+  constexpr int bytes = VerifySmem<D, Q, SB, PC>::BYTES;
+  auto k = (P.flags & KDA_FLAG_NO_DELTA) ? verify_window_kernel<D, NT, Q, SB, PC, false>
+                                         : verify_window_kernel<D, NT, Q, SB, PC, true>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  k<<<dim3(static_cast<unsigned>(grid)), NT, bytes, s>>>(P, window, ring, ring_record_elems(D, PC),
+                                                          static_cast<int>(pairs));
   return cudaGetLastError();
 }
 

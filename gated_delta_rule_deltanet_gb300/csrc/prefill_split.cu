@@ -105,6 +105,7 @@ constexpr uint32_t O_GS = 0, O_BETA = 256, O_RK = 512, O_RQ = 768, O_EG = 1024, 
 // operand is scaled by 2^8 and the column operands by 2^-8 (the product is unchanged), which
 // keeps the small row factors of a strongly decaying channel out of fp16's subnormal range.
 constexpr float kSubBlockDecay = 12.0f;
+constexpr float kLog2e = 1.4426950408889634f;   // the per-channel path keeps G in log2 units
 constexpr float kRowScale = 256.0f, kColScale = 1.0f / 256.0f;
 // The factors above are <= 1 only for a non-increasing cumulative log-decay: a per-channel
 // log-decay above this bound (a gate above 1) is outside the tensor-core path's domain.
@@ -421,9 +422,9 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       for (int e = 0; e < 32; ++e) gv[e] = sG[g_off(32 * hh + e, c)];
       float acc = 0.f;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < 32; ++e) {            // G in log2 units: every factor is one ex2
         rise = rise || gv[e] > kMaxLogDecay;
-        acc += gv[e];
+        acc = fmaf(gv[e], kLog2e, acc);
         gv[e] = acc;
       }
       float m0 = gv[0], m1 = gv[16];            // lowest G of each of the half's sub-blocks
@@ -458,24 +459,24 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       const float g15 = sGB[c], g31 = sGB[128 + c], g47 = sGB[256 + c], g63 = sGB[384 + c];
       const float ref0 = hh == 0 ? 0.f : g31, ref1 = hh == 0 ? g15 : g47;
       const float end1 = hh == 0 ? g31 : g63;
-      const bool slow0 = ref0 - m0 > kSubBlockDecay, slow1 = ref1 - m1 > kSubBlockDecay;
+      const bool slow0 = ref0 - m0 > kSubBlockDecay * kLog2e, slow1 = ref1 - m1 > kSubBlockDecay * kLog2e;
       const uint32_t b0 = __ballot_sync(0xffffffffu, slow0), b1 = __ballot_sync(0xffffffffu, slow1);
       if (lane == 0) {
         sMask[(2 * hh) * 4 + (warp & 3)] = b0;
         sMask[(2 * hh + 1) * 4 + (warp & 3)] = b1;
         if (b0 | b1) s_anyslow = 1;
       }
-      sW[(2 * hh) * 128 + c] = slow0 ? 0.f : __expf(ref0 - ref1);   // the end of 2 hh is ref1
-      sW[(2 * hh + 1) * 128 + c] = slow1 ? 0.f : __expf(ref1 - end1);
+      sW[(2 * hh) * 128 + c] = slow0 ? 0.f : ex2(ref0 - ref1);   // the end of 2 hh is ref1
+      sW[(2 * hh + 1) * 128 + c] = slow1 ? 0.f : ex2(ref1 - end1);
       if (hh == 0) {
-        sES[c] = __expf(g15);
-        sES[128 + c] = __expf(g31);
-        sF[c] = __expf(g31 - g15);              // sub-block 0 seen from sub-block 2
+        sES[c] = ex2(g15);
+        sES[128 + c] = ex2(g31);
+        sF[c] = ex2(g31 - g15);              // sub-block 0 seen from sub-block 2
       } else {
-        sES[256 + c] = __expf(g47);
-        sF[128 + c] = __expf(g47 - g15);        // sub-block 0 seen from sub-block 3
-        sF[256 + c] = __expf(g47 - g31);        // sub-block 1 seen from sub-block 3
-        reinterpret_cast<float*>(rec + REC_GAM)[c] = __expf(g63);
+        sES[256 + c] = ex2(g47);
+        sF[128 + c] = ex2(g47 - g15);        // sub-block 0 seen from sub-block 3
+        sF[256 + c] = ex2(g47 - g31);        // sub-block 1 seen from sub-block 3
+        reinterpret_cast<float*>(rec + REC_GAM)[c] = ex2(g63);
       }
       // K_end = k^ exp(G_last - G_j) of this thread's 32 tokens in channel c, to tensor
       // memory (lane = channel c, two tokens per column): the A operand of K_end^T TB
@@ -483,10 +484,11 @@ __global__ void __launch_bounds__(tcs::NT, 2)
 #pragma unroll
       for (int e = 0; e < 32; e += 2) {
         const int j = 32 * hh + e;
-        const float k0 = tc::bf16_at(smem, kq_off(false, j, c), c & 7) * sRK[j] * __expf(g63 - gv[e]);
-        const float k1 = tc::bf16_at(smem, kq_off(false, j + 1, c), c & 7) * sRK[j + 1] *
-                         __expf(g63 - gv[e + 1]);
-        w[e / 2] = tc::pack_f16x2(k0, k1);
+        const float2 rk = *reinterpret_cast<const float2*>(sRK + j);
+        const float2 kj = make_float2(tc::bf16_at(smem, kq_off(false, j, c), c & 7),
+                                      tc::bf16_at(smem, kq_off(false, j + 1, c), c & 7));
+        const float2 x = mul2(mul2(kj, rk), make_float2(ex2(g63 - gv[e]), ex2(g63 - gv[e + 1])));
+        w[e / 2] = tc::pack_f16x2(x.x, x.y);
       }
       tc::tmem_st16(tmem + lane_addr + F_KE + 16 * hh, w);
       tc::tmem_wait_st();
@@ -517,7 +519,7 @@ __global__ void __launch_bounds__(tcs::NT, 2)
             const int j = jb + e;
             if (is_q ? j <= i : j < i)
               acc[e] += xi * tc::bf16_at(smem, kq_off(false, j, cc), cc & 7) * sRK[j] *
-                        __expf(gi - sG[g_off(j, cc)]);
+                        ex2(gi - sG[g_off(j, cc)]);
           }
         }
       }
@@ -571,17 +573,28 @@ __global__ void __launch_bounds__(tcs::NT, 2)
         }
         const uint32_t mb = (sMask[J * 4 + (c0 >> 5)] >> (c0 & 31)) & 0xffu;
         float rkv[8], rqv[8], kt[8], qt[8], ke[8], cd[8];
+        const float2 rk2 = make_float2(rk, rk), rq2 = make_float2(rq, rq);
+        const float2 rks = make_float2(rk * kRowScale, rk * kRowScale), rqs = make_float2(rq * kRowScale, rq * kRowScale);
+        const float2 rkc = make_float2(rk * kColScale, rk * kColScale);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float r = __expf(gp[it][e] - gref[e]);     // exp(G_j - G_ref(J)) <= 1
-          const float eps = __expf(gend[e] - gp[it][e]);   // exp(G_end(J) - G_j) <= 1
-          const float kr = kx[e] * rk, qr = qx[e] * rq;
-          rkv[e] = kr * r * kRowScale;
-          rqv[e] = qr * r * kRowScale;
-          kt[e] = delta ? kr * r * es[e] : 0.f;            // K~ = k^ exp(G_j)
-          qt[e] = qr * r * es[e];                          // Q~ = q^ exp(G_j)
-          ke[e] = kr * eps * kColScale;
-          cd[e] = ((mb >> e) & 1u) ? 0.f : ke[e] * wd[e];  // k^ exp(G_ref(J) - G_j) / 256
+        for (int e = 0; e < 8; e += 2) {                   // two channels at a time
+          const float2 r = make_float2(ex2(gp[it][e] - gref[e]), ex2(gp[it][e + 1] - gref[e + 1]));   // <= 1
+          const float2 eps = make_float2(ex2(gend[e] - gp[it][e]), ex2(gend[e + 1] - gp[it][e + 1]));  // <= 1
+          const float2 kxr = mul2(make_float2(kx[e], kx[e + 1]), r);
+          const float2 qxr = mul2(make_float2(qx[e], qx[e + 1]), r);
+          const float2 R_k = mul2(kxr, rks), R_q = mul2(qxr, rqs);
+          const float2 es2 = make_float2(es[e], es[e + 1]);
+          const float2 K_t = mul2(mul2(kxr, rk2), es2);   // K~ = k^ exp(G_j)
+          const float2 Q_t = mul2(mul2(qxr, rq2), es2);   // Q~ = q^ exp(G_j)
+          const float2 k_e = mul2(mul2(make_float2(kx[e], kx[e + 1]), eps), rkc);
+          const float2 c_d = mul2(k_e, make_float2(wd[e], wd[e + 1]));   // k^ exp(G_ref(J) - G_j) / 256
+          rkv[e] = R_k.x; rkv[e + 1] = R_k.y;
+          rqv[e] = R_q.x; rqv[e + 1] = R_q.y;
+          kt[e] = delta ? K_t.x : 0.f; kt[e + 1] = delta ? K_t.y : 0.f;
+          qt[e] = Q_t.x; qt[e + 1] = Q_t.y;
+          ke[e] = k_e.x; ke[e + 1] = k_e.y;
+          cd[e] = ((mb >> e) & 1u) ? 0.f : c_d.x;
+          cd[e + 1] = ((mb >> (e + 1)) & 1u) ? 0.f : c_d.y;
         }
         tc::f16x8_store(smem, kq_off(false, jr, c0), rkv);
         tc::f16x8_store(smem, kq_off(true, jr, c0), rqv);
@@ -598,7 +611,11 @@ __global__ void __launch_bounds__(tcs::NT, 2)
           float f[8], co[8];
           load8(f, sF + (J == 0 ? 0 : 2) * 128 + c0);      // (2, 0) or (3, 1)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) co[e] = ke[e] * f[e];
+          for (int e = 0; e < 8; e += 2) {
+            const float2 x = mul2(make_float2(ke[e], ke[e + 1]), make_float2(f[e], f[e + 1]));
+            co[e] = x.x;
+            co[e + 1] = x.y;
+          }
           tc::f16x8_store(smem, M::CO + tc::cm_offset(16 * off_slot(J + 2, J) + (jr & 15), c0, 128,
                                                       tc::dense_sbo(D)),
                           co);
@@ -607,7 +624,11 @@ __global__ void __launch_bounds__(tcs::NT, 2)
           float f[8], co[8];
           load8(f, sF + 128 + c0);                         // (3, 0)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) co[e] = ke[e] * f[e];
+          for (int e = 0; e < 8; e += 2) {
+            const float2 x = mul2(make_float2(ke[e], ke[e + 1]), make_float2(f[e], f[e + 1]));
+            co[e] = x.x;
+            co[e + 1] = x.y;
+          }
           tc::f16x8_store(smem, M::CO + tc::cm_offset(16 * off_slot(3, 0) + (jr & 15), c0, 128,
                                                       tc::dense_sbo(D)),
                           co);
@@ -808,13 +829,15 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       const float4 v = *reinterpret_cast<const float4*>(sA + sidx(r0 + r, c0 + m));
       a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
     }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
       const float4 t = *reinterpret_cast<const float4*>(sT + sidx(c0 + m, c0 + c));
-      acc.x += a[m] * t.x; acc.y += a[m] * t.y; acc.z += a[m] * t.z; acc.w += a[m] * t.w;
+      const float2 am = make_float2(a[m], a[m]);
+      acc01 = fma2(am, make_float2(t.x, t.y), acc01);
+      acc23 = fma2(am, make_float2(t.z, t.w), acc23);
     }
-    *reinterpret_cast<float4*>(sX + (16 * p + r) * XP + c) = acc;
+    *reinterpret_cast<float4*>(sX + (16 * p + r) * XP + c) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
   }
   __syncthreads();
   if (tid < 128) {                              // T21 = -T22 X
@@ -826,13 +849,15 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       const float4 v = *reinterpret_cast<const float4*>(sT + sidx(r0 + r, r0 + m));
       a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
     }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
       const float4 x = *reinterpret_cast<const float4*>(sX + (16 * p + m) * XP + c);
-      acc.x += a[m] * x.x; acc.y += a[m] * x.y; acc.z += a[m] * x.z; acc.w += a[m] * x.w;
+      const float2 am = make_float2(a[m], a[m]);
+      acc01 = fma2(am, make_float2(x.x, x.y), acc01);
+      acc23 = fma2(am, make_float2(x.z, x.w), acc23);
     }
-    *reinterpret_cast<float4*>(sT + sidx(r0 + r, c0 + c)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    *reinterpret_cast<float4*>(sT + sidx(r0 + r, c0 + c)) = make_float4(-acc01.x, -acc01.y, -acc23.x, -acc23.y);
   }
   __syncthreads();
   {                                             // X = A21 T11, one 32x32 pair
@@ -843,13 +868,15 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       const float4 v = *reinterpret_cast<const float4*>(sA + sidx(32 + r, m));
       a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
     }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < 32; ++m) {
       const float4 t = *reinterpret_cast<const float4*>(sT + sidx(m, c));
-      acc.x += a[m] * t.x; acc.y += a[m] * t.y; acc.z += a[m] * t.z; acc.w += a[m] * t.w;
+      const float2 am = make_float2(a[m], a[m]);
+      acc01 = fma2(am, make_float2(t.x, t.y), acc01);
+      acc23 = fma2(am, make_float2(t.z, t.w), acc23);
     }
-    *reinterpret_cast<float4*>(sX + r * XP + c) = acc;
+    *reinterpret_cast<float4*>(sX + r * XP + c) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
   }
   __syncthreads();
   {                                             // T21 = -T22 X
@@ -860,13 +887,15 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       const float4 v = *reinterpret_cast<const float4*>(sT + sidx(32 + r, 32 + m));
       a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
     }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int m = 0; m < 32; ++m) {
       const float4 x = *reinterpret_cast<const float4*>(sX + m * XP + c);
-      acc.x += a[m] * x.x; acc.y += a[m] * x.y; acc.z += a[m] * x.z; acc.w += a[m] * x.w;
+      const float2 am = make_float2(a[m], a[m]);
+      acc01 = fma2(am, make_float2(x.x, x.y), acc01);
+      acc23 = fma2(am, make_float2(x.z, x.w), acc23);
     }
-    *reinterpret_cast<float4*>(sT + sidx(32 + r, c)) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    *reinterpret_cast<float4*>(sT + sidx(32 + r, c)) = make_float4(-acc01.x, -acc01.y, -acc23.x, -acc23.y);
   }
   __syncthreads();
   for (int u = tid; u < C * (C / 8); u += NT) { // TB[m][j] = T[m][j] beta_j, row pieces

@@ -96,7 +96,9 @@ PREFILL_STAGES = {
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a kernel on a
 # workload, from an ncu capture of the kernel as it is built now (see profiles/); a kernel
 # without a capture of its current build has no entry and is reported as null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {("decode_step", "kda_decode"): 547441408 + 480736768,
+               ("fold_accepted", "kda_verify"): 452932864 + 364371200,
+               ("conv_kernel", "gdn_prefill"): 358.74e6}
 
 
 def load_peaks() -> dict:

@@ -112,7 +112,8 @@ constexpr float kRowScale = 256.0f, kColScale = 1.0f / 256.0f;
 constexpr float kMaxLogDecay = 1.0f / 64.0f;
 // per-chunk vectors of the per-channel front kernel (byte offsets inside its SMALL area):
 //   BETA, RK, RQ  beta, 1/|k|, scale/|q| per token
-//   GB   G at tokens 15, 31, 47, 63 per channel (the sub-block boundaries)
+//   GB   G at tokens 15, 31 and, relative to token 31, at 47, 63 per channel (the sub-block
+//        boundaries; each 32-token half keeps its own cumulative sum)
 //   ES   exp(G_15), exp(G_31), exp(G_47) (K~ and Q~ of sub-blocks 1-3 from their row factors)
 //   W    diagonal column factor exp(G_ref(J) - G_end(J)) of sub-block J (0 for exact channels)
 //   F    exp(G_ref(I) - G_end(J)) for (I, J) = (2, 0), (3, 0), (3, 1) (I = J + 1 needs none)
@@ -413,8 +414,11 @@ __global__ void __launch_bounds__(tcs::NT, 2)
     uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + M::SMALL + P_MASK);
     {
       // ---------------------------------------------------------------- cumulative log-decay
-      // thread = (channel c, token half hh): each half sums its 32 tokens, the second half
-      // then adds the first half's total
+      // thread = (channel c, token half hh): each half sums its own 32 tokens.  Every
+      // quantity inside a half (the sub-blocks' row and column factors, the exact diagonal
+      // pairs) depends only on differences within it, so G stays half-local in shared memory
+      // and GB holds, per channel, G_15 and G_31 of the first half and the second half's local
+      // G_47 and G_63; the cross-half values below add the first half's total G_31.
       const int c = tid & 127, hh = tid >> 7;
       float gv[32];
       bool rise = false;
@@ -434,50 +438,36 @@ __global__ void __launch_bounds__(tcs::NT, 2)
         m1 = fminf(m1, gv[16 + e]);
       }
       if (rise) s_range = 1;
-      if (hh == 0) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sG[g_off(e, c)] = gv[e];
-        sGB[c] = gv[15];
-        sGB[128 + c] = gv[31];
-      }
-      __syncthreads();
-      if (hh == 1) {
-        const float off = sGB[128 + c];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          gv[e] += off;
-          sG[g_off(32 + e, c)] = gv[e];
-        }
-        m0 += off;
-        m1 += off;
-        sGB[256 + c] = gv[15];
-        sGB[384 + c] = gv[31];
-      }
-      __syncthreads();
-      // sub-blocks 2 hh and 2 hh + 1: a channel whose decay from the sub-block's reference to
-      // any of its tokens exceeds kSubBlockDecay is summed exactly on the diagonal
-      const float g15 = sGB[c], g31 = sGB[128 + c], g47 = sGB[256 + c], g63 = sGB[384 + c];
-      const float ref0 = hh == 0 ? 0.f : g31, ref1 = hh == 0 ? g15 : g47;
-      const float end1 = hh == 0 ? g31 : g63;
-      const bool slow0 = ref0 - m0 > kSubBlockDecay * kLog2e, slow1 = ref1 - m1 > kSubBlockDecay * kLog2e;
+      for (int e = 0; e < 32; ++e) sG[g_off(32 * hh + e, c)] = gv[e];
+      sGB[(2 * hh) * 128 + c] = gv[15];
+      sGB[(2 * hh + 1) * 128 + c] = gv[31];
+      // sub-blocks 2 hh and 2 hh + 1 (half-local: reference 0 and gv[15], ends gv[15], gv[31]):
+      // a channel whose decay from the sub-block's reference to any of its tokens exceeds
+      // kSubBlockDecay is summed exactly on the diagonal
+      const bool slow0 = -m0 > kSubBlockDecay * kLog2e, slow1 = gv[15] - m1 > kSubBlockDecay * kLog2e;
       const uint32_t b0 = __ballot_sync(0xffffffffu, slow0), b1 = __ballot_sync(0xffffffffu, slow1);
       if (lane == 0) {
         sMask[(2 * hh) * 4 + (warp & 3)] = b0;
         sMask[(2 * hh + 1) * 4 + (warp & 3)] = b1;
         if (b0 | b1) s_anyslow = 1;
       }
-      sW[(2 * hh) * 128 + c] = slow0 ? 0.f : ex2(ref0 - ref1);   // the end of 2 hh is ref1
-      sW[(2 * hh + 1) * 128 + c] = slow1 ? 0.f : ex2(ref1 - end1);
+      sW[(2 * hh) * 128 + c] = slow0 ? 0.f : ex2(-gv[15]);
+      sW[(2 * hh + 1) * 128 + c] = slow1 ? 0.f : ex2(gv[15] - gv[31]);
+      __syncthreads();
+      const float g15 = sGB[c], g31 = sGB[128 + c], l47 = sGB[256 + c], l63 = sGB[384 + c];
       if (hh == 0) {
         sES[c] = ex2(g15);
         sES[128 + c] = ex2(g31);
-        sF[c] = ex2(g31 - g15);              // sub-block 0 seen from sub-block 2
+        sF[c] = ex2(g31 - g15);                 // sub-block 0 seen from sub-block 2
       } else {
-        sES[256 + c] = ex2(g47);
-        sF[128 + c] = ex2(g47 - g15);        // sub-block 0 seen from sub-block 3
-        sF[256 + c] = ex2(g47 - g31);        // sub-block 1 seen from sub-block 3
-        reinterpret_cast<float*>(rec + REC_GAM)[c] = ex2(g63);
+        sES[256 + c] = ex2(g31 + l47);
+        sF[128 + c] = ex2(g31 + l47 - g15);     // sub-block 0 seen from sub-block 3
+        sF[256 + c] = ex2(l47);                 // sub-block 1 seen from sub-block 3
+        reinterpret_cast<float*>(rec + REC_GAM)[c] = ex2(g31 + l63);
       }
+      // the chunk's last G in this half's coordinates
+      const float g63 = hh == 0 ? g31 + l63 : l63;
       // K_end = k^ exp(G_last - G_j) of this thread's 32 tokens in channel c, to tensor
       // memory (lane = channel c, two tokens per column): the A operand of K_end^T TB
       uint32_t w[16];
@@ -561,14 +551,16 @@ __global__ void __launch_bounds__(tcs::NT, 2)
         tc::bf16x8_load(kq_piece(true, jr, c0), qx);
         load8(gend, sGB + J * 128 + c0);
         load8(wd, sW + J * 128 + c0);
-        if (J == 0) {
+        if (J == 0 || J == 2) {                  // the half's first sub-block: reference 0
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            gref[e] = 0.f;
-            es[e] = 1.f;
-          }
+          for (int e = 0; e < 8; ++e) gref[e] = 0.f;
         } else {
           load8(gref, sGB + (J - 1) * 128 + c0);
+        }
+        if (J == 0) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) es[e] = 1.f;
+        } else {
           load8(es, sES + (J - 1) * 128 + c0);
         }
         const uint32_t mb = (sMask[J * 4 + (c0 >> 5)] >> (c0 & 31)) & 0xffu;
@@ -724,23 +716,23 @@ __global__ void __launch_bounds__(tcs::NT, 2)
       const int p = (warp & 3) & 1;
       const bool hi = ((i >> 4) & 1) != 0;
       const float ri = is_k ? sBeta[i] : 1.f;
+      const int Ilo = 2 * p, Ihi = 2 * p + 1;
+      auto src = [&](int J, int I) -> int {      // warp-uniform tensor-memory column, -1: none
+        return J < I ? static_cast<int>(F_O) + 16 * off_slot(I, J) : (J == I ? static_cast<int>(F_D) + 16 * J : -1);
+      };
+      const int J0 = 2 * chalf, J1 = 2 * chalf + 1;
+      const int s0l = src(J0, Ilo), s0h = src(J0, Ihi), s1l = src(J1, Ilo), s1h = src(J1, Ihi);
+      uint32_t a0[16], b0[16], a1[16], b1[16];   // every load issued before one wait
+      if (s0l >= 0) tc::tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(s0l), a0);
+      if (s0h >= 0) tc::tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(s0h), b0);
+      if (s1l >= 0) tc::tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(s1l), a1);
+      if (s1h >= 0) tc::tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(s1h), b1);
+      tc::tmem_wait_ld();
+      const bool none0 = (hi ? s0h : s0l) < 0, none1 = (hi ? s1h : s1l) < 0;
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int J = 2 * chalf + jj;
-        const int Ilo = 2 * p, Ihi = 2 * p + 1;
-        const int slo = J < Ilo ? static_cast<int>(F_O) + 16 * off_slot(Ilo, J)
-                                : (J == Ilo ? static_cast<int>(F_D) + 16 * J : -1);
-        const int shi = J < Ihi ? static_cast<int>(F_O) + 16 * off_slot(Ihi, J)
-                                : (J == Ihi ? static_cast<int>(F_D) + 16 * J : -1);
-        uint32_t a[16], b[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) a[e] = b[e] = 0u;
-        if (slo >= 0) tc::tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(slo), a);
-        if (shi >= 0) tc::tmem_ld16(tmem + lane_addr + static_cast<uint32_t>(shi), b);
-        tc::tmem_wait_ld();
-        const bool none = (hi ? shi : slo) < 0;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) x[16 * jj + e] = none ? 0.f : __uint_as_float(hi ? b[e] : a[e]) * ri;
+      for (int e = 0; e < 16; ++e) {
+        x[e] = none0 ? 0.f : __uint_as_float(hi ? b0[e] : a0[e]) * ri;
+        x[16 + e] = none1 ? 0.f : __uint_as_float(hi ? b1[e] : a1[e]) * ri;
       }
     } else {
       uint32_t r0[16], r1[16], q0[16], q1[16];
@@ -861,40 +853,55 @@ __global__ void __launch_bounds__(tcs::NT, 2)
   }
   __syncthreads();
   {                                             // X = A21 T11, one 32x32 pair
-    const int r = tid >> 3, c = (tid & 7) * 4;
-    float a[32];
-#pragma unroll
-    for (int m = 0; m < 32; m += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(sA + sidx(32 + r, m));
-      a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
-    }
+    // warp w: columns [4w, 4w + 4), lane: row; T11 is lower triangular, so rows m < 4w of it
+    // are zero in these columns and the sum starts at the warp-uniform m = 4w
+    const int r = lane, c = 4 * warp;
     float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int m = 0; m < 32; ++m) {
-      const float4 t = *reinterpret_cast<const float4*>(sT + sidx(m, c));
-      const float2 am = make_float2(a[m], a[m]);
-      acc01 = fma2(am, make_float2(t.x, t.y), acc01);
-      acc23 = fma2(am, make_float2(t.z, t.w), acc23);
+    float2 bcc01 = make_float2(0.f, 0.f), bcc23 = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int m = c; m < 32; m += 4) {
+      const float4 av = *reinterpret_cast<const float4*>(sA + sidx(32 + r, m));
+      const float4 t0 = *reinterpret_cast<const float4*>(sT + sidx(m, c));
+      const float4 t1 = *reinterpret_cast<const float4*>(sT + sidx(m + 1, c));
+      const float4 t2 = *reinterpret_cast<const float4*>(sT + sidx(m + 2, c));
+      const float4 t3 = *reinterpret_cast<const float4*>(sT + sidx(m + 3, c));
+      acc01 = fma2(make_float2(av.x, av.x), make_float2(t0.x, t0.y), acc01);
+      acc23 = fma2(make_float2(av.x, av.x), make_float2(t0.z, t0.w), acc23);
+      bcc01 = fma2(make_float2(av.y, av.y), make_float2(t1.x, t1.y), bcc01);
+      bcc23 = fma2(make_float2(av.y, av.y), make_float2(t1.z, t1.w), bcc23);
+      acc01 = fma2(make_float2(av.z, av.z), make_float2(t2.x, t2.y), acc01);
+      acc23 = fma2(make_float2(av.z, av.z), make_float2(t2.z, t2.w), acc23);
+      bcc01 = fma2(make_float2(av.w, av.w), make_float2(t3.x, t3.y), bcc01);
+      bcc23 = fma2(make_float2(av.w, av.w), make_float2(t3.z, t3.w), bcc23);
     }
+    acc01 = add2(acc01, bcc01);
+    acc23 = add2(acc23, bcc23);
     *reinterpret_cast<float4*>(sX + r * XP + c) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
   }
   __syncthreads();
   {                                             // T21 = -T22 X
-    const int r = tid >> 3, c = (tid & 7) * 4;
-    float a[32];
-#pragma unroll
-    for (int m = 0; m < 32; m += 4) {
-      const float4 v = *reinterpret_cast<const float4*>(sT + sidx(32 + r, 32 + m));
-      a[m] = v.x; a[m + 1] = v.y; a[m + 2] = v.z; a[m + 3] = v.w;
-    }
+    // warp w: rows [4w, 4w + 4); T22 is lower triangular, so the sum stops at m = 4w + 3
+    const int r = tid >> 3, c = (tid & 7) * 4, mend = 4 * warp + 4;
     float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int m = 0; m < 32; ++m) {
-      const float4 x = *reinterpret_cast<const float4*>(sX + m * XP + c);
-      const float2 am = make_float2(a[m], a[m]);
-      acc01 = fma2(am, make_float2(x.x, x.y), acc01);
-      acc23 = fma2(am, make_float2(x.z, x.w), acc23);
+    float2 bcc01 = make_float2(0.f, 0.f), bcc23 = make_float2(0.f, 0.f);
+#pragma unroll 4
+    for (int m = 0; m < mend; m += 4) {
+      const float4 av = *reinterpret_cast<const float4*>(sT + sidx(32 + r, 32 + m));
+      const float4 x0 = *reinterpret_cast<const float4*>(sX + m * XP + c);
+      const float4 x1 = *reinterpret_cast<const float4*>(sX + (m + 1) * XP + c);
+      const float4 x2 = *reinterpret_cast<const float4*>(sX + (m + 2) * XP + c);
+      const float4 x3 = *reinterpret_cast<const float4*>(sX + (m + 3) * XP + c);
+      acc01 = fma2(make_float2(av.x, av.x), make_float2(x0.x, x0.y), acc01);
+      acc23 = fma2(make_float2(av.x, av.x), make_float2(x0.z, x0.w), acc23);
+      bcc01 = fma2(make_float2(av.y, av.y), make_float2(x1.x, x1.y), bcc01);
+      bcc23 = fma2(make_float2(av.y, av.y), make_float2(x1.z, x1.w), bcc23);
+      acc01 = fma2(make_float2(av.z, av.z), make_float2(x2.x, x2.y), acc01);
+      acc23 = fma2(make_float2(av.z, av.z), make_float2(x2.z, x2.w), acc23);
+      bcc01 = fma2(make_float2(av.w, av.w), make_float2(x3.x, x3.y), bcc01);
+      bcc23 = fma2(make_float2(av.w, av.w), make_float2(x3.z, x3.w), bcc23);
     }
+    acc01 = add2(acc01, bcc01);
+    acc23 = add2(acc23, bcc23);
     *reinterpret_cast<float4*>(sT + sidx(32 + r, c)) = make_float4(-acc01.x, -acc01.y, -acc23.x, -acc23.y);
   }
   __syncthreads();

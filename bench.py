@@ -10,8 +10,9 @@ the prefill path); the metric is prefill tokens/s.  The Gated DeltaNet prefill
 speculative-decode verification (a 4-token window plus the fold of the accepted prefix) are
 measured in the same run and reported under "also".
 
-Multi-GPU: every rank runs an independent replica on its own batch (sequences never
-interact, so nothing is exchanged); value = all ranks' tokens / the slowest rank's time.
+Multi-GPU: every rank runs an independent replica on its own batch of the same sizes
+(another seed per rank; sequences never interact, so nothing is exchanged); value = all ranks'
+tokens / the slowest rank's time.
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -97,7 +98,8 @@ PREFILL_STAGES = {
 # workload, from an ncu capture of the kernel as it is built now (see profiles/); a kernel
 # without a capture of its current build has no entry and is reported as null.
 NCU_TRAFFIC = {("decode_step", "kda_decode"): 547441408 + 480736768,
-               ("fold_accepted", "kda_verify"): 452932864 + 364371200,
+               ("verify_window", "kda_verify"): 579015936 + 57849088,
+               ("fold_accepted", "kda_verify"): 453014272 + 364333056,
                ("conv_kernel", "gdn_prefill"): 358.74e6}
 
 
@@ -644,7 +646,7 @@ def ours_arm(args, rank, world, local):
     torch.cuda.set_device(dev)
     kda.load()
     peaks = load_peaks()
-    p = workloads.workload(args.workload)
+    p = workloads.workload(args.workload, replica=rank)
 
     # timed region: K prefill steps on resident inputs (inputs > L2, no flush needed)
     barrier(world)
@@ -669,7 +671,7 @@ def ours_arm(args, rank, world, local):
         for wname in ("gdn_prefill", "kda_prefill", "ragged_gqa_kda"):
             if wname == p.name:
                 continue
-            wp = workloads.workload(wname)
+            wp = workloads.workload(wname, replica=rank)
             # 30 steps of well under a millisecond to a millisecond: a host stall between two
             # steps would dominate the wall-clock mean, so the line reports the mean device
             # span of a step
@@ -682,7 +684,7 @@ def ours_arm(args, rank, world, local):
                          "unit": "tokens/s", "ms_per_step": wms, "roofline": wroof,
                          "path_roofline": wpath})
 
-        dp = workloads.workload("kda_decode")
+        dp = workloads.workload("kda_decode", replica=rank)
         dms = time_decode(dp, dev, max(args.steps, 20), max(args.warmup, 3))
         dbytes = float(sum(decode_algorithmic_bytes(dp).values()))
         dval, _ = aggregate(1.0, dms / 1e3, world, dev)      # one step per dms
@@ -712,7 +714,7 @@ def ours_arm(args, rank, world, local):
                      "ms_per_step": vms, "stage_ms": vstage,
                      "roofline": vroof["verify_window"], "fold_roofline": vroof["fold_accepted"]})
 
-        gp = workloads.workload("gdp_prefill")
+        gp = workloads.workload("gdp_prefill", replica=rank)
         gms = time_gdp_prefill(gp, dev, 30, 3)
         gval, _ = aggregate(float(gp.total_tokens), gms / 1e3, world, dev)
         also.append({"workload": "gdp_prefill (Gated DeltaProduct, 4 x 4096 tokens x 2 substeps, "

@@ -49,3 +49,14 @@ def test_two_rank_weak_scaling_aggregate():
 def test_single_rank_is_identity():
     import bench
     assert bench.aggregate(500.0, 2.0, 1) == (250.0, 2.0)
+
+
+def test_replicas_draw_disjoint_batches_of_the_same_sizes():
+    import numpy as np
+    import workloads
+    a = workloads.workload("tiny_gdn")
+    b = workloads.workload("tiny_gdn", replica=0)
+    c = workloads.workload("tiny_gdn", replica=1)
+    assert np.array_equal(a.q, b.q) and np.array_equal(a.g, b.g)
+    assert c.q.shape == a.q.shape and c.v.shape == a.v.shape and c.total_tokens == a.total_tokens
+    assert not np.array_equal(c.q, a.q) and not np.array_equal(c.v, a.v)

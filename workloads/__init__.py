@@ -241,36 +241,43 @@ def ragged_lengths(rng, n: int, lo: int, hi: int) -> np.ndarray:
 WORKLOADS = ("tiny_gdn", "gdn_prefill", "kda_prefill", "ragged_gqa_kda", "kda_decode")
 
 
-def workload(name: str):
-    """The named workload (Problem, or DecodeProblem for kda_decode)."""
+def workload(name: str, replica: int = 0):
+    """The named workload (Problem, or DecodeProblem for kda_decode).
+
+    replica > 0 draws another batch of the same sizes (same sequence lengths and heads; tensors,
+    and shuffled slots, from a seed offset by replica << 24): what each rank of a multi-GPU run
+    processes.
+    Replica 0 is the workload itself.
+    """
+    off = replica << 24
     if name == "tiny_gdn":
         return make_problem(name, num_seqs=1, lengths=[64], num_k_heads=1, num_v_heads=1, d=16,
                             qkv_dtype=F32, state_dtype=F32, decay_kind=SCALAR, chunk=16,
-                            zero_state=True, seed=1001, shuffle_slots=False)
+                            zero_state=True, seed=1001 + off, shuffle_slots=False)
     if name == "gdn_prefill":
         return make_problem(name, num_seqs=4, lengths=[4096] * 4, num_k_heads=16, num_v_heads=16,
                             d=128, qkv_dtype=BF16, state_dtype=F32, decay_kind=SCALAR, chunk=64,
-                            zero_state=True, seed=1002, shuffle_slots=False)
+                            zero_state=True, seed=1002 + off, shuffle_slots=False)
     if name == "kda_prefill":
         return make_problem(name, num_seqs=2, lengths=[16384] * 2, num_k_heads=32, num_v_heads=32,
                             d=128, qkv_dtype=BF16, state_dtype=F32, decay_kind=PER_CHANNEL,
-                            chunk=64, zero_state=False, seed=1003, shuffle_slots=False)
+                            chunk=64, zero_state=False, seed=1003 + off, shuffle_slots=False)
     if name == "ragged_gqa_kda":
         rng = np.random.Generator(np.random.PCG64(1004))
         lengths = ragged_lengths(rng, 8, 64, 8192)
         # The lengths come from their own stream; the tensors from seed 1004 + 1 << 20.
         return make_problem(name, num_seqs=8, lengths=lengths, num_k_heads=16, num_v_heads=32,
                             d=128, qkv_dtype=BF16, state_dtype=BF16, decay_kind=PER_CHANNEL,
-                            chunk=64, zero_state=False, num_slots=64, seed=1004 + (1 << 20),
+                            chunk=64, zero_state=False, num_slots=64, seed=1004 + (1 << 20) + off,
                             shuffle_slots=True)
     if name == "gdp_prefill":
         return make_gdp_problem(name, num_seqs=4, lengths=[4096] * 4, n_h=2, num_k_heads=16,
                                 num_v_heads=16, d=128, qkv_dtype=BF16, state_dtype=F32,
-                                decay_kind=SCALAR, chunk=64, zero_state=True, seed=1006)
+                                decay_kind=SCALAR, chunk=64, zero_state=True, seed=1006 + off)
     if name == "kda_decode":
         return make_decode_problem(name, num_seqs=256, steps=64, num_k_heads=32, num_v_heads=32,
                                    d=128, qkv_dtype=BF16, state_dtype=F32,
-                                   decay_kind=PER_CHANNEL, zero_state=False, seed=1005)
+                                   decay_kind=PER_CHANNEL, zero_state=False, seed=1005 + off)
     raise KeyError(name)
 
 

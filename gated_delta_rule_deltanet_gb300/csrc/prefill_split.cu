@@ -259,7 +259,7 @@ template <bool PERCH, bool DELTA>
 __global__ void __launch_bounds__(tcs::NT, 2)
     tc_front_kernel(Problem P, PlanView plan, unsigned char* records,
                     const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                    const __grid_constant__ CUtensorMap tmg) {
+                    const __grid_constant__ CUtensorMap tmg, int ahead) {
   using namespace tcs;
   using M = FrontMap<PERCH>;
   using MS = FrontMap<false>;
@@ -333,6 +333,26 @@ __global__ void __launch_bounds__(tcs::NT, 2)
         const uint32_t sg = tc::smem_u32(smem + M_SG);
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) tc::tma_load_3d(sg + qq * (C * 128), &tmg, 32 * qq, h, row0, &s_ld);
+      }
+    }
+  }
+  if (tid == 32 && ahead > 0) {
+    // CTAs start in the order of their linear index, `ahead` of them resident at once: the
+    // one `ahead` places later starts about when this one ends, so its k, q (and log-decay)
+    // tiles go to L2 now and its own copies find them there
+    const int64_t L = static_cast<int64_t>(h) * gridDim.x + gc + ahead;
+    const int gn = static_cast<int>(L % gridDim.x), hn = static_cast<int>(L / gridDim.x);
+    if (hn < HV && gn < plan_chunks) {
+      const int32_t rn = static_cast<int32_t>(plan.chunks[gn].t0);
+      const int khn = hn / (HV / P.HK);
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        tc::tma_prefetch_3d(&tmk, 64 * a, khn, rn);
+        tc::tma_prefetch_3d(&tmq, 64 * a, khn, rn);
+      }
+      if constexpr (PERCH) {
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) tc::tma_prefetch_3d(&tmg, 32 * qq, hn, rn);
       }
     }
   }
@@ -1500,7 +1520,10 @@ static cudaError_t launch_front_t(const Problem& P, const PlanView& plan, unsign
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  k<<<dim3(static_cast<unsigned>(plan_max_chunks(P)), P.HV), tcs::NT, bytes, st>>>(P, plan, recs, tmq, tmk, tmg);
+  // two CTAs per SM: each prefetches for the CTA one full wave later
+  const int ahead = 2 * sm_count();
+  k<<<dim3(static_cast<unsigned>(plan_max_chunks(P)), P.HV), tcs::NT, bytes, st>>>(P, plan, recs, tmq, tmk, tmg,
+                                                                                   ahead);
   return cudaGetLastError();
 }
 

@@ -264,6 +264,11 @@ __device__ __forceinline__ void cp_async_wait_one() {
 
 // Bulk (TMA-engine) copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
 // from global to shared memory; completion is counted in bytes on `bar`.
+// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned global address
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(
@@ -275,6 +280,13 @@ __device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint3
 
 // Tiled 3-D TMA load of one box of `map` at element coordinates (x, y, z) into shared
 // memory; completion is counted in bytes on `bar`.  x * element size must be a multiple of 16.
+// L2 prefetch of one box of a tiled tensor map: no shared memory and no barrier involved
+__device__ __forceinline__ void tma_prefetch_3d(const void* map, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x),
+               "r"(y), "r"(z)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(uint32_t sdst, const void* map, int32_t x, int32_t y,
                                             int32_t z, uint64_t* bar) {
   asm volatile(

@@ -360,18 +360,6 @@ __global__ void __launch_bounds__(NT) fold_accepted_kernel(Problem P, int window
 int ring_record_elems(int D, bool perch) { return D + D + (perch ? D : 4); }
 
 // SMs of the current device (cached per device)
-static int sm_count() {
-  static int cached[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (!cached[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    cached[dev] = n;
-  }
-  return cached[dev];
-}
-
 template <int D, int NT, bool Q, bool SB, bool PC>
 static cudaError_t launch_verify_t(const Problem& P, int window, float* ring, cudaStream_t s) {
   const int64_t pairs = static_cast<int64_t>(P.num_seqs) * P.HV;

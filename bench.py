@@ -781,7 +781,7 @@ def ours_arm(args, rank, world, local):
 def profile_arm(args):
     """W + K steps of one piece, for an ncu capture (no JSON line; nothing reported here is
     a bench value): `prefill` on --workload, `decode` on kda_decode, `verify` on the
-    256-sequence window of 4 plus the fold."""
+    256-sequence window of 4 plus the fold, `backward` on --workload."""
     import torch
     import gated_delta_rule_deltanet_gb300 as kda
     dev = torch.device("cuda", 0)
@@ -791,6 +791,8 @@ def profile_arm(args):
         ms = time_prefill(workloads.workload(args.workload), dev, args.steps, args.warmup)[0]
     elif args.profile == "decode":
         ms = time_decode(workloads.workload("kda_decode"), dev, args.steps, args.warmup)
+    elif args.profile == "backward":
+        ms = time_prefill_bwd(workloads.workload(args.workload), dev, args.steps, args.warmup)[0]
     else:
         ms = time_verify(dev, args.steps, args.warmup)[1]
     print(f"profile {args.profile}: {args.warmup} + {args.steps} steps, {ms:.4f} ms per step")
@@ -806,7 +808,7 @@ def main(argv=None):
                     choices=[w for w in workloads.WORKLOADS if w != "kda_decode"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--profile", choices=["prefill", "decode", "verify"],
+    ap.add_argument("--profile", choices=["prefill", "decode", "verify", "backward"],
                     help="run W + K steps of one piece for a profiler, print no JSON line")
     args = ap.parse_args(argv)
     if args.warmup < 3:

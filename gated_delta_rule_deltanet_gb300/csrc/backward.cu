@@ -24,7 +24,7 @@
 //
 //   local   the forward's chunk-local stage, also keeping T and K~
 //   scan    per (sequence, value head, value tile): forward over the chunks to record each
-//           chunk's incoming state and E, then backward carrying dS: dE, dV, dS per chunk
+//           chunk's incoming state and E, then backward carrying dS: dE, dY, dV, dS per chunk
 //   vc      per (chunk, value head): the contractions over the value dimension
 //           (dQ~, dK~, dK_end, dA, dM, dgamma, the first term of dbeta)
 //   pair    per (chunk, key head), over the value heads of its group: the pairwise terms,
@@ -34,36 +34,10 @@
 // The additive write (KDA_FLAG_NO_DELTA) has no L and no K~ S term: T = I, W = 0, and their
 // gradient terms vanish.  The pairwise decay is evaluated per pair and channel, as in the
 // CUDA-core forward, so no factor overflows.
-#include "prefill_simt.cuh"
+#include "backward.cuh"
 #include "tc_utils.cuh"
 
 namespace kda {
-
-struct BwdArgs {
-  const float* d_o;      // [T, HV, D]
-  const float* d_state;  // [num_slots, HV, D, D] or null: gradient w.r.t. the final states
-  float* dq;             // [T, HK, D]
-  float* dk;             // [T, HK, D]
-  float* dv;             // [T, HV, D]
-  float* dbeta;          // [T, HV]
-  float* dg;             // [T, HV] or [T, HV, D]
-  float* d_state0;       // [num_slots, HV, D, D] or null: gradient w.r.t. the initial states
-};
-
-struct BwdWorkspace {
-  SimtWorkspace loc;
-  float* Sck;   // [chunk][HV][D][D] state entering the chunk
-  float* dSck;  // [chunk][HV][D][D] gradient w.r.t. the state leaving the chunk
-  float* E;     // [chunk][HV][C][D] corrected values
-  float* dE;    // [chunk][HV][C][D]
-  float* dQt;   // [chunk][HV][C][D]
-  float* dKt;   // [chunk][HV][C][D]
-  float* dKe;   // [chunk][HV][C][D]
-  float* dA;    // [chunk][HV][C][C]
-  float* dM;    // [chunk][HV][C][C]
-  float* dgam;  // [chunk][HV][D]
-  float* dbr;   // [chunk][HV][C]
-};
 
 static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws) {
   size_t off = 0;
@@ -89,7 +63,7 @@ static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws) {
   w.Sck = take(units * D * D);
   w.dSck = take(units * D * D);
   w.E = take(units * C * D);
-  w.dE = take(units * C * D);
+  w.dY = take(units * C * D);
   w.dQt = take(units * C * D);
   w.dKt = take(units * C * D);
   w.dKe = take(units * C * D);
@@ -267,24 +241,28 @@ __global__ void __launch_bounds__(256, 2) bwd_scan_kernel(Problem P, BwdWorkspac
         for (int e = 0; e < TC::JT; ++e) acc[e] += kc * x[e];
       }
       st_row(s_dE + ri * BV + rj, acc);
-      st_row(ws.dE + unit * C * D + ri * D + v0 + rj, acc);
     }
     __syncthreads();
     mat_async<C, D, DP>(s_B, ws.loc.W + unit * C * D, tid);   // K_end is done with
     tc::cp_async_commit();
-    if (ri < ci.n) {                            // dV = diag(beta) T^T dE
+    {                                           // dY = T^T dE, dV = diag(beta) dY
       float acc[TC::JT] = {};
-      for (int m = ri; m < C; ++m) {
-        float x[TC::JT];
-        ld_row(x, s_dE + m * BV + rj);
-        const float t = __ldg(gT + m * C + ri);
+      if (ri < ci.n) {
+        for (int m = ri; m < C; ++m) {
+          float x[TC::JT];
+          ld_row(x, s_dE + m * BV + rj);
+          const float t = __ldg(gT + m * C + ri);
 #pragma unroll
-        for (int e = 0; e < TC::JT; ++e) acc[e] += t * x[e];
+          for (int e = 0; e < TC::JT; ++e) acc[e] += t * x[e];
+        }
       }
-      const float bi = s_b[ri];
+      st_row(ws.dY + unit * C * D + ri * D + v0 + rj, acc);
+      if (ri < ci.n) {
+        const float bi = s_b[ri];
 #pragma unroll
-      for (int e = 0; e < TC::JT; ++e) acc[e] *= bi;
-      st_row(A.dv + ((ci.t0 + ri) * HV + h) * D + v0 + rj, acc);
+        for (int e = 0; e < TC::JT; ++e) acc[e] *= bi;
+        st_row(A.dv + ((ci.t0 + ri) * HV + h) * D + v0 + rj, acc);
+      }
     }
     // dS = diag(gamma) dS' + Q~^T dO - W^T dE: the Q~ part while W arrives
     float acc[TD::JT];
@@ -338,7 +316,7 @@ __global__ void __launch_bounds__(256, 2) bwd_scan_kernel(Problem P, BwdWorkspac
 template <int D, int C, int BV>
 struct BwdVcSmem {
   static constexpr int DP = D + 4, CP = C + 4;
-  static constexpr size_t floats = C * C + C * DP + C + D * BV + 2 * BV * DP + 6 * C * BV + BV * CP;
+  static constexpr size_t floats = C * DP + C + D * BV + 2 * BV * DP + 5 * C * BV + BV * CP;
   static constexpr size_t bytes = floats * sizeof(float);
 };
 
@@ -349,16 +327,14 @@ __global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws,
   constexpr int IR = C / 16, JC = D / 16, JM = C / 16;
   using TC = RowTile<C, BV>;
   extern __shared__ __align__(16) float smem[];
-  float* s_T = smem;                // [C][C]
-  float* s_Kt = s_T + C * C;        // [C][DP] K~
+  float* s_Kt = smem;               // [C][DP] K~
   float* s_b = s_Kt + C * DP;       // [C]
   float* s_S = s_b + C;             // [D][BV] S tile
   float* s_St = s_S + D * BV;       // [BV][DP] S tile, transposed
   float* s_dSt = s_St + BV * DP;    // [BV][DP] dS' tile, transposed
   float* s_V = s_dSt + BV * DP;     // [C][BV]
   float* s_E = s_V + C * BV;        // [C][BV]
-  float* s_dE = s_E + C * BV;       // [C][BV]
-  float* s_dO = s_dE + C * BV;      // [C][BV]
+  float* s_dO = s_E + C * BV;       // [C][BV]
   float* s_dY = s_dO + C * BV;      // [C][BV]
   float* s_R = s_dY + C * BV;       // [C][BV] V - K~ S
   float* s_Et = s_R + C * BV;       // [BV][CP]
@@ -370,7 +346,6 @@ __global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws,
   const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
   const int ri = tid / TC::TPR, rj = (tid % TC::TPR) * TC::JT;
   const int r0 = (tid / 16) * IR, c0 = (tid % 16) * JC, m0 = (tid % 16) * JM;
-  for (int idx = tid; idx < C * C; idx += NT) s_T[idx] = ws.loc.T[unit * C * C + idx];
   for (int idx = tid; idx < C * D; idx += NT) s_Kt[(idx / D) * DP + idx % D] = ws.loc.Kt[unit * C * D + idx];
   for (int i = tid; i < C; i += NT) s_b[i] = i < ci.n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
 
@@ -400,19 +375,12 @@ __global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws,
       const float e = ws.E[unit * C * D + i * D + v0 + j];
       s_E[idx] = e;
       s_Et[j * CP + i] = e;
-      s_dE[idx] = ws.dE[unit * C * D + i * D + v0 + j];
+      s_dY[idx] = ws.dY[unit * C * D + i * D + v0 + j];
       s_dO[idx] = live ? A.d_o[((ci.t0 + i) * HV + h) * D + v0 + j] : 0.f;
     }
     __syncthreads();
-    {                                           // dY = T^T dE and R = V - K~ S
-      float y[TC::JT] = {}, ks[TC::JT] = {};
-      for (int m = ri; m < C; ++m) {
-        float x[TC::JT];
-        ld_row(x, s_dE + m * BV + rj);
-        const float t = s_T[m * C + ri];
-#pragma unroll
-        for (int e = 0; e < TC::JT; ++e) y[e] += t * x[e];
-      }
+    {                                           // R = V - K~ S
+      float ks[TC::JT] = {};
       if (delta) {
         const float* kt = s_Kt + ri * DP;
 #pragma unroll 4
@@ -428,7 +396,6 @@ __global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws,
       ld_row(v, s_V + ri * BV + rj);
 #pragma unroll
       for (int e = 0; e < TC::JT; ++e) v[e] -= ks[e];
-      st_row(s_dY + ri * BV + rj, y);
       st_row(s_R + ri * BV + rj, v);
     }
     __syncthreads();
@@ -847,8 +814,14 @@ static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const 
   sk<<<dim3(P.num_seqs, P.HV, D / BV), 256, BwdScanSmem<D, C, BV>::bytes, st>>>(P, ws, A);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (mc > 0) {
-    vk<<<dim3(mc, P.HV), 256, BwdVcSmem<D, C, BV>::bytes, st>>>(P, ws, A);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // bf16 inputs at d = 128, chunk 64: the contractions on tensor cores (tf32 operands; the
+    // fp32 inputs' tighter bound keeps them on CUDA cores)
+    e = (D == 128 && C == 64 && QBF16) ? launch_bwd_vc_tc(P, ws, A, st) : cudaErrorNotSupported;
+    if (e == cudaErrorNotSupported) {
+      vk<<<dim3(mc, P.HV), 256, BwdVcSmem<D, C, BV>::bytes, st>>>(P, ws, A);
+      e = cudaGetLastError();
+    }
+    if (e != cudaSuccess) return e;
     pk<<<dim3(mc, P.HK), 256, BwdPairSmem<D, C, PERCH>::bytes, st>>>(P, ws, A);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

@@ -44,14 +44,10 @@
 // Operand precisions are those of the single-kernel path in prefill_tc.cu (fp16 operands,
 // fp32 accumulation and fp32 state); the state passes through fp16 as the B operand of
 // [K~; Q~] S, and E' as that of Kb E' and A1o E'.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
 #include "kda_common.cuh"
 #include "prefill_plan.cuh"
 #include "tc_utils.cuh"
+#include "tma_maps.cuh"
 
 namespace kda {
 
@@ -1459,21 +1455,6 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
 size_t split_workspace_bytes(const Problem& P) {
   const size_t off = plan_layout(P, nullptr, 0, nullptr);
   return off + static_cast<size_t>(plan_max_chunks(P)) * static_cast<size_t>(P.HV) * tcs::REC_BYTES;
-}
-
-// cuTensorMapEncodeTiled from the driver (the runtime is linked statically, libcuda is not)
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
 }
 
 // [T, HK, 128] bf16 rows with a row stride of `stride` elements: boxes of 64 channels x

@@ -66,7 +66,7 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c
 // keeps the address inside shared memory, so the 14-bit field cannot carry).
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-enum : uint32_t { kF16 = 0, kBF16 = 1 };
+enum : uint32_t { kF16 = 0, kBF16 = 1, kTF32 = 2 };   // A/B type field (kind::f16 / kind::tf32)
 
 // Instruction descriptor of kind::f16: fp32 accumulator, A/B element types, optional
 // negation of A, operands K-major unless a_mn / b_mn (MN-major), shape M x N.
@@ -230,6 +230,18 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// kind::tf32: A and B are fp32 in shared memory, read with a 10-bit mantissa (K = 8 per
+// instruction: 32 bytes of a K-major row, the same byte step as kind::f16's K = 16).
+__device__ __forceinline__ void mma_ss_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on `bar` when every MMA issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
@@ -264,11 +276,6 @@ __device__ __forceinline__ void cp_async_wait_one() {
 
 // Bulk (TMA-engine) copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
 // from global to shared memory; completion is counted in bytes on `bar`.
-// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned global address
-__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint32_t bytes,
                                           uint64_t* bar) {
   asm volatile(
@@ -278,8 +285,6 @@ __device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint3
       : "memory");
 }
 
-// Tiled 3-D TMA load of one box of `map` at element coordinates (x, y, z) into shared
-// memory; completion is counted in bytes on `bar`.  x * element size must be a multiple of 16.
 // L2 prefetch of one box of a tiled tensor map: no shared memory and no barrier involved
 __device__ __forceinline__ void tma_prefetch_3d(const void* map, int32_t x, int32_t y, int32_t z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x),
@@ -287,6 +292,19 @@ __device__ __forceinline__ void tma_prefetch_3d(const void* map, int32_t x, int3
                : "memory");
 }
 
+// Tiled 2-D TMA load of one box of `map` at element coordinates (x, y) into shared memory;
+// completion is counted in bytes on `bar`.  x * element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(uint32_t sdst, const void* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(sdst),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Tiled 3-D TMA load of one box of `map` at element coordinates (x, y, z) into shared
+// memory; completion is counted in bytes on `bar`.  x * element size must be a multiple of 16.
 __device__ __forceinline__ void tma_load_3d(uint32_t sdst, const void* map, int32_t x, int32_t y,
                                             int32_t z, uint64_t* bar) {
   asm volatile(

@@ -39,7 +39,9 @@
 
 namespace kda {
 
-static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws) {
+// tc: the tensor-core scans run (d = 128, chunk 64, bf16 inputs) and need the transposed
+// copies of the local stage's matrices
+static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws, bool tc) {
   size_t off = 0;
   PlanView pv;
   off = plan_layout(P, base, off, &pv);
@@ -60,6 +62,13 @@ static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws) {
   w.loc.gamma = take(units * D);
   w.loc.T = take(units * C * C);
   w.loc.Kt = take(units * C * D);
+  if (tc) {
+    w.loc.KendT = take(units * D * C);
+    w.loc.QtT = take(units * D * C);
+    w.loc.WT = take(units * D * C);
+    w.loc.AqkT = take(units * C * C);
+    w.loc.TT = take(units * C * C);
+  }
   w.Sck = take(units * D * D);
   w.dSck = take(units * D * D);
   w.E = take(units * C * D);
@@ -75,7 +84,11 @@ static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws) {
   return off;
 }
 
-size_t bwd_workspace_bytes(const Problem& P) { return bwd_layout(P, nullptr, nullptr); }
+static bool bwd_tc(const Problem& P, bool qbf16) { return P.D == 128 && P.chunk == 64 && qbf16; }
+
+size_t bwd_workspace_bytes(const Problem& P, bool qbf16) {
+  return bwd_layout(P, nullptr, nullptr, bwd_tc(P, qbf16));
+}
 
 // ------------------------------------------------------------------------------- scan
 
@@ -811,8 +824,13 @@ static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const 
     lk<<<dim3(mc, P.HV), 256, SimtLocalSmem<D, C>::bytes, st>>>(P, ws.loc);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  sk<<<dim3(P.num_seqs, P.HV, D / BV), 256, BwdScanSmem<D, C, BV>::bytes, st>>>(P, ws, A);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // bf16 inputs at d = 128, chunk 64: both directions of the scan on tensor cores
+  e = (D == 128 && C == 64 && QBF16) ? launch_bwd_scans_tc(P, ws, A, SBF16, st) : cudaErrorNotSupported;
+  if (e == cudaErrorNotSupported) {
+    sk<<<dim3(P.num_seqs, P.HV, D / BV), 256, BwdScanSmem<D, C, BV>::bytes, st>>>(P, ws, A);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) return e;
   if (mc > 0) {
     // bf16 inputs at d = 128, chunk 64: the contractions on tensor cores (tf32 operands; the
     // fp32 inputs' tighter bound keeps them on CUDA cores)
@@ -858,7 +876,7 @@ cudaError_t launch_prefill_bwd(const Problem& P, void* workspace, const float* d
                                float* dbeta, float* dg, float* d_state0, bool qbf16, bool perch,
                                bool sbf16, cudaStream_t stream) {
   BwdWorkspace ws;
-  bwd_layout(P, static_cast<char*>(workspace), &ws);
+  bwd_layout(P, static_cast<char*>(workspace), &ws, bwd_tc(P, qbf16));
   const BwdArgs A{d_o, d_state, dq, dk, dv, dbeta, dg, d_state0};
   cudaError_t e = launch_plan(P, ws.loc.plan, stream);
   if (e != cudaSuccess) return e;

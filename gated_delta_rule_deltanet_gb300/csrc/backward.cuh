@@ -39,4 +39,13 @@ struct BwdWorkspace {
 cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A,
                              cudaStream_t st);
 
+// The scan on tensor cores (d = 128, chunk 64): a forward kernel recording each chunk's
+// incoming state and corrected values, then a reverse kernel carrying the state gradient
+// (dY, dV, the state gradients per chunk and w.r.t. the initial states), as bwd_scan_kernel
+// computes them.  Needs the local stage's transposed copies (loc.KendT ... loc.TT); returns
+// cudaErrorNotSupported when a tensor map cannot be encoded, so the caller runs the
+// CUDA-core scan.
+cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, bool sbf16,
+                                cudaStream_t st);
+
 }  // namespace kda

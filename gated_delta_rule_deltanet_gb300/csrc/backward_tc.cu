@@ -258,6 +258,473 @@ __global__ void __launch_bounds__(bvt::NT, 2)
   if (warp == 0) tc::tmem_dealloc(tmem, COLS);
 }
 
+// ------------------------------------------------------------------------------- scans
+//
+// The state recursion and its transpose, per (sequence, value head, 64 value columns), chunk
+// by chunk on tensor cores (kind::tf32).  Every operand is K-major: the local stage's matrices
+// come from the workspace in the orientation each product needs (W and K_end as stored;
+// K_end^T, Q~^T, W^T, A_qk^T and T^T as transposed copies), copied by TMA in 32-column blocks
+// with the 128-byte swizzle; the running state and the per-chunk right-hand sides are written
+// by the threads transposed (value rows, K = key channel or token) into the same layout.
+//
+//   forward   X = W S,  E = U - X,  S <- diag(gamma) S + K_end^T E
+//   reverse   dE = A_qk^T dO + K_end dS',  dY = T^T dE,  dV = diag(beta) dY,
+//             dS = diag(gamma) dS' + Q~^T dO - W^T dE
+//
+// Products with 64 rows (tokens) run as M = 128 MMAs whose rows 64-127 read the next block
+// of shared memory: those accumulator lanes are never read.  Threads: warp w serves tensor-
+// memory lanes 32 (w % 4).. and value columns 32 (w / 4).. of the 64-column accumulators, and
+// keeps that 32-column row segment of the state (thread = key channel) in registers.
+
+namespace bst {
+
+constexpr int C = 64, D = 128, BV = 64, NT = 256;
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint32_t BLK = 8192;                  // a 32-column block of 64 rows (128 B a row)
+// forward: W (4 blocks + 8 KB under the last M = 128 read), K_end^T (2 blocks of 128 rows),
+// U (2 blocks: the CTA's 64 value columns), S^T (4 blocks of 64 value rows), E^T (2 blocks)
+constexpr uint32_t F_W = 0, F_KT = 5 * BLK, F_U = F_KT + 4 * BLK, F_ST = F_U + 2 * BLK,
+                   F_ET = F_ST + 4 * BLK, F_DATA = F_ET + 2 * BLK;
+// reverse: K_end (4 blocks), A_qk^T (2), T^T (2) + 8 KB, Q~^T and W^T (2 blocks of 128 rows
+// each), dO^T (2 blocks of 64 value rows), dS'^T (4), dE^T (2)
+constexpr uint32_t R_KE = 0, R_AQ = 4 * BLK, R_TT = 6 * BLK, R_QT = 9 * BLK, R_WT = R_QT + 4 * BLK,
+                   R_OT = R_WT + 4 * BLK, R_RT = R_OT + 2 * BLK, R_ET = R_RT + 4 * BLK,
+                   R_DATA = R_ET + 2 * BLK;
+constexpr uint32_t F_BYTES_A = 4 * BLK + 2 * BLK, F_BYTES_B = 4 * BLK;   // W + U, K_end^T
+constexpr uint32_t R_BYTES_A = 4 * BLK + 2 * BLK + 4 * BLK, R_BYTES_B = 2 * BLK + 4 * BLK;
+static_assert(F_DATA + 1024 <= 227 * 1024 && R_DATA + 1024 <= 227 * 1024, "shared memory budget");
+
+struct Ctrl {
+  uint64_t full_a, full_b;   // the two TMA groups of a chunk
+  uint64_t bar1, bar2;       // the two MMA groups of a chunk
+  uint32_t tmem;
+  int bad;
+};
+constexpr uint32_t CTRL_BYTES = (sizeof(Ctrl) + 15) & ~15u;
+
+// byte offset of element (row, k) of a K-major operand stored as 32-column blocks of
+// `rows_per_block` rows (128 bytes a row, 128-byte swizzle)
+__device__ __forceinline__ uint32_t kmaj(uint32_t row, uint32_t k, uint32_t rows_per_block) {
+  return (k >> 5) * rows_per_block * 128 + tc::sw128_offset(row, (k & 31) >> 2) + (k & 3) * 4;
+}
+
+}  // namespace bst
+
+template <bool SBF16>
+__global__ void __launch_bounds__(bst::NT, 1)
+    bwd_fwd_scan_tc_kernel(Problem P, BwdWorkspace ws, const __grid_constant__ CUtensorMap tm_w,
+                           const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_kt) {
+  using namespace bst;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t pad = (1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* const data = smem_raw + pad;
+  Ctrl* const ctl = reinterpret_cast<Ctrl*>(pad >= CTRL_BYTES ? smem_raw : data + F_DATA);
+  if (ws.loc.plan.info[1] == 0) return;
+  const int b = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
+  const int HV = P.HV, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int first = ws.loc.plan.seq_chunk0[b], last = ws.loc.plan.seq_chunk0[b + 1];
+  if (first >= last) return;
+  const int qd = warp & 3, chalf = warp >> 2;
+  const int r = 32 * qd + lane;                 // TMEM lane: key channel (state) / token (X)
+  const int vc = 32 * chalf;                    // this thread's 32 value columns within the tile
+  const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
+  const uint32_t sd = tc::smem_u32(data);
+  auto unit_of = [&](int cidx) { return static_cast<int64_t>(cidx) * HV + h; };
+
+  auto load_a = [&](int cidx) {                 // W and the CTA's U columns of chunk cidx
+    const int32_t row = static_cast<int32_t>(unit_of(cidx) * C);
+    tc::mbar_arrive_expect_tx(&ctl->full_a, F_BYTES_A);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) tc::tma_load_2d(sd + F_W + j * BLK, &tm_w, 32 * j, row, &ctl->full_a);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) tc::tma_load_2d(sd + F_U + j * BLK, &tm_u, v0 + 32 * j, row, &ctl->full_a);
+  };
+  auto load_b = [&](int cidx) {                 // K_end^T of chunk cidx
+    const int32_t row = static_cast<int32_t>(unit_of(cidx) * D);
+    tc::mbar_arrive_expect_tx(&ctl->full_b, F_BYTES_B);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) tc::tma_load_2d(sd + F_KT + j * 2 * BLK, &tm_kt, 32 * j, row, &ctl->full_b);
+  };
+  if (tid == 0) {
+    tc::mbar_init(&ctl->full_a, 1);
+    tc::mbar_init(&ctl->full_b, 1);
+    tc::mbar_init(&ctl->bar1, 1);
+    tc::mbar_init(&ctl->bar2, 1);
+    ctl->bad = 0;
+    tc::fence_mbar_init();
+    load_a(first);
+    load_b(first);
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&ctl->tmem, 128);
+    tc::tmem_relinquish();
+  }
+  float Sv[32];
+  const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + static_cast<int64_t>(r) * D + v0 + vc;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    Sv[j] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[sbase + j])
+                  : static_cast<const float*>(P.pool)[sbase + j];
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = ctl->tmem;
+  constexpr uint32_t T_X = 0, T_D = 64;
+  const uint32_t id = tc::idesc_f16(128, BV, tc::kTF32);
+
+  for (int cidx = first; cidx < last; ++cidx) {
+    const uint32_t par = static_cast<uint32_t>(cidx - first) & 1u;
+    const int64_t unit = unit_of(cidx);
+    // S entering the chunk: into the workspace, and transposed as the B operand of W S
+    {
+      float* gs = ws.Sck + (unit * D + r) * D + v0 + vc;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(gs + j) = make_float4(Sv[j], Sv[j + 1], Sv[j + 2], Sv[j + 3]);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(data + F_ST + kmaj(vc + j, r, 64)) = Sv[j];
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      if (tc::mbar_wait_bounded(&ctl->full_a, par, kWaitLimit)) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t da = tc::smem_desc_sw128(sd + F_W + j * BLK, 1024);
+          const uint64_t db = tc::smem_desc_sw128(sd + F_ST + j * BLK, 1024);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_ss_tf32(tmem + T_X, tc::desc_add(da, 32 * k), tc::desc_add(db, 32 * k), id, (j | k) ? 1u : 0u);
+        }
+      } else {
+        ctl->bad = 1;
+      }
+      tc::mma_commit(&ctl->bar1);
+    }
+    // E = U - X on the token rows (lanes 0-63), stored and written transposed
+    const bool ok1 = tc::mbar_wait_bounded(&ctl->bar1, par, kWaitLimit) &&
+                     tc::mbar_wait_bounded(&ctl->full_a, par, kWaitLimit);
+    tc::fence_after_sync();
+    if (!ok1) ctl->bad = 1;
+    if (qd < 2) {
+      uint32_t x0[16], x1[16];
+      tc::tmem_ld16(tmem + lane_addr + T_X + vc, x0);
+      tc::tmem_ld16(tmem + lane_addr + T_X + vc + 16, x1);
+      tc::tmem_wait_ld();
+      float e[32];
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 u = *reinterpret_cast<const float4*>(data + F_U + kmaj(r, vc + j, 64));
+        const uint32_t* x = j < 16 ? x0 + j : x1 + (j - 16);
+        e[j] = u.x - __uint_as_float(x[0]);
+        e[j + 1] = u.y - __uint_as_float(x[1]);
+        e[j + 2] = u.z - __uint_as_float(x[2]);
+        e[j + 3] = u.w - __uint_as_float(x[3]);
+      }
+      float* ge = ws.E + (unit * C + r) * D + v0 + vc;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(ge + j) = make_float4(e[j], e[j + 1], e[j + 2], e[j + 3]);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(data + F_ET + kmaj(vc + j, r, 64)) = e[j];
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      if (cidx + 1 < last) load_a(cidx + 1);    // W and U of this chunk are consumed
+      if (tc::mbar_wait_bounded(&ctl->full_b, par, kWaitLimit)) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint64_t da = tc::smem_desc_sw128(sd + F_KT + j * 2 * BLK, 1024);
+          const uint64_t db = tc::smem_desc_sw128(sd + F_ET + j * BLK, 1024);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_ss_tf32(tmem + T_D, tc::desc_add(da, 32 * k), tc::desc_add(db, 32 * k), id, (j | k) ? 1u : 0u);
+        }
+      } else {
+        ctl->bad = 1;
+      }
+      tc::mma_commit(&ctl->bar2);
+    }
+    // S <- diag(gamma) S + K_end^T E
+    const bool ok2 = tc::mbar_wait_bounded(&ctl->bar2, par, kWaitLimit);
+    tc::fence_after_sync();
+    if (!ok2) ctl->bad = 1;
+    {
+      uint32_t d0[16], d1[16];
+      tc::tmem_ld16(tmem + lane_addr + T_D + vc, d0);
+      tc::tmem_ld16(tmem + lane_addr + T_D + vc + 16, d1);
+      tc::tmem_wait_ld();
+      const float gm = __ldg(ws.loc.gamma + unit * D + r);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        Sv[j] = fmaf(gm, Sv[j], __uint_as_float(d0[j]));
+        Sv[16 + j] = fmaf(gm, Sv[16 + j], __uint_as_float(d1[j]));
+      }
+    }
+    if (tid == 0 && cidx + 1 < last) load_b(cidx + 1);   // K_end^T of this chunk is consumed
+    if (tc::named_sync_or(1, NT, ctl->bad != 0)) break;
+  }
+  if (ctl->bad && tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, 128);
+}
+
+__global__ void __launch_bounds__(bst::NT, 1)
+    bwd_rev_scan_tc_kernel(Problem P, BwdWorkspace ws, BwdArgs A, const __grid_constant__ CUtensorMap tm_ke,
+                           const __grid_constant__ CUtensorMap tm_aq, const __grid_constant__ CUtensorMap tm_qt,
+                           const __grid_constant__ CUtensorMap tm_tt, const __grid_constant__ CUtensorMap tm_wt) {
+  using namespace bst;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t pad = (1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* const data = smem_raw + pad;
+  Ctrl* const ctl = reinterpret_cast<Ctrl*>(pad >= CTRL_BYTES ? smem_raw : data + R_DATA);
+  if (ws.loc.plan.info[1] == 0) return;
+  const int b = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
+  const int HV = P.HV, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int first = ws.loc.plan.seq_chunk0[b], last = ws.loc.plan.seq_chunk0[b + 1];
+  const int qd = warp & 3, chalf = warp >> 2;
+  const int r = 32 * qd + lane;                 // TMEM lane: key channel (dS) / token (dE, dY)
+  const int vc = 32 * chalf;
+  const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
+  const uint32_t sd = tc::smem_u32(data);
+  const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + static_cast<int64_t>(r) * D + v0 + vc;
+  // dS starts as the gradient w.r.t. the final state
+  float Rv[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) Rv[j] = A.d_state ? A.d_state[sbase + j] : 0.f;
+  if (first >= last) {                          // an empty sequence: dS0 = dS_final
+    if (A.d_state0)
+#pragma unroll
+      for (int j = 0; j < 32; ++j) A.d_state0[sbase + j] = Rv[j];
+    return;
+  }
+  auto unit_of = [&](int cidx) { return static_cast<int64_t>(cidx) * HV + h; };
+  auto load_a = [&](int cidx) {                 // K_end, A_qk^T, Q~^T of chunk cidx
+    const int64_t u = unit_of(cidx);
+    tc::mbar_arrive_expect_tx(&ctl->full_a, R_BYTES_A);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      tc::tma_load_2d(sd + R_KE + j * BLK, &tm_ke, 32 * j, static_cast<int32_t>(u * C), &ctl->full_a);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      tc::tma_load_2d(sd + R_AQ + j * BLK, &tm_aq, 32 * j, static_cast<int32_t>(u * C), &ctl->full_a);
+      tc::tma_load_2d(sd + R_QT + j * 2 * BLK, &tm_qt, 32 * j, static_cast<int32_t>(u * D), &ctl->full_a);
+    }
+  };
+  auto load_b = [&](int cidx) {                 // T^T, W^T of chunk cidx
+    const int64_t u = unit_of(cidx);
+    tc::mbar_arrive_expect_tx(&ctl->full_b, R_BYTES_B);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      tc::tma_load_2d(sd + R_TT + j * BLK, &tm_tt, 32 * j, static_cast<int32_t>(u * C), &ctl->full_b);
+      tc::tma_load_2d(sd + R_WT + j * 2 * BLK, &tm_wt, 32 * j, static_cast<int32_t>(u * D), &ctl->full_b);
+    }
+  };
+  if (tid == 0) {
+    tc::mbar_init(&ctl->full_a, 1);
+    tc::mbar_init(&ctl->full_b, 1);
+    tc::mbar_init(&ctl->bar1, 1);
+    tc::mbar_init(&ctl->bar2, 1);
+    ctl->bad = 0;
+    tc::fence_mbar_init();
+    load_a(last - 1);
+    load_b(last - 1);
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&ctl->tmem, 256);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = ctl->tmem;
+  constexpr uint32_t T_DE = 0, T_DY = 64, T_DS = 128;
+  const uint32_t id = tc::idesc_f16(128, BV, tc::kTF32);
+  const int om = tid >> 2, opart = tid & 3;     // dO staging: token om, values 16 opart..
+
+  for (int cidx = last - 1; cidx >= first; --cidx) {
+    const uint32_t par = static_cast<uint32_t>(last - 1 - cidx) & 1u;
+    const int64_t unit = unit_of(cidx);
+    const ChunkInfo ci = ws.loc.plan.chunks[cidx];
+    // dO^T (rows past the chunk's end zero) and dS'^T as B operands; dS' into the workspace
+    {
+      float o[16];
+      if (om < ci.n) {
+        const float* src = A.d_o + ((ci.t0 + om) * HV + h) * D + v0 + 16 * opart;
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src + j);
+          o[j] = x.x; o[j + 1] = x.y; o[j + 2] = x.z; o[j + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[j] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) *reinterpret_cast<float*>(data + R_OT + kmaj(16 * opart + j, om, 64)) = o[j];
+      float* gs = ws.dSck + (unit * D + r) * D + v0 + vc;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(gs + j) = make_float4(Rv[j], Rv[j + 1], Rv[j + 2], Rv[j + 3]);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(data + R_RT + kmaj(vc + j, r, 64)) = Rv[j];
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      if (tc::mbar_wait_bounded(&ctl->full_a, par, kWaitLimit)) {
+        tc::fence_after_sync();
+        // dE = A_qk^T dO + K_end dS'  (rows 0-63);  dS = Q~^T dO  (the rest after dE)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint64_t da = tc::smem_desc_sw128(sd + R_AQ + j * BLK, 1024);
+          const uint64_t dq = tc::smem_desc_sw128(sd + R_QT + j * 2 * BLK, 1024);
+          const uint64_t db = tc::smem_desc_sw128(sd + R_OT + j * BLK, 1024);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            tc::mma_ss_tf32(tmem + T_DE, tc::desc_add(da, 32 * k), tc::desc_add(db, 32 * k), id, (j | k) ? 1u : 0u);
+            tc::mma_ss_tf32(tmem + T_DS, tc::desc_add(dq, 32 * k), tc::desc_add(db, 32 * k), id, (j | k) ? 1u : 0u);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t da = tc::smem_desc_sw128(sd + R_KE + j * BLK, 1024);
+          const uint64_t db = tc::smem_desc_sw128(sd + R_RT + j * BLK, 1024);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            tc::mma_ss_tf32(tmem + T_DE, tc::desc_add(da, 32 * k), tc::desc_add(db, 32 * k), id, 1u);
+        }
+      } else {
+        ctl->bad = 1;
+      }
+      tc::mma_commit(&ctl->bar1);
+    }
+    // -dE^T as the B operand of T^T dE and W^T dE (the sign folded into the operand, so both
+    // products accumulate: dS gets + W^T (-dE), and T^T (-dE) = -dY)
+    const bool ok1 = tc::mbar_wait_bounded(&ctl->bar1, par, kWaitLimit);
+    tc::fence_after_sync();
+    if (!ok1) ctl->bad = 1;
+    if (qd < 2) {
+      uint32_t x0[16], x1[16];
+      tc::tmem_ld16(tmem + lane_addr + T_DE + vc, x0);
+      tc::tmem_ld16(tmem + lane_addr + T_DE + vc + 16, x1);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        *reinterpret_cast<uint32_t*>(data + R_ET + kmaj(vc + j, r, 64)) = x0[j] ^ 0x80000000u;
+        *reinterpret_cast<uint32_t*>(data + R_ET + kmaj(vc + 16 + j, r, 64)) = x1[j] ^ 0x80000000u;
+      }
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      if (cidx > first) load_a(cidx - 1);       // K_end, A_qk^T, Q~^T and dO^T are consumed
+      if (tc::mbar_wait_bounded(&ctl->full_b, par, kWaitLimit)) {
+        tc::fence_after_sync();
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const uint64_t dt = tc::smem_desc_sw128(sd + R_TT + j * BLK, 1024);
+          const uint64_t dw = tc::smem_desc_sw128(sd + R_WT + j * 2 * BLK, 1024);
+          const uint64_t db = tc::smem_desc_sw128(sd + R_ET + j * BLK, 1024);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            tc::mma_ss_tf32(tmem + T_DY, tc::desc_add(dt, 32 * k), tc::desc_add(db, 32 * k), id, (j | k) ? 1u : 0u);
+            tc::mma_ss_tf32(tmem + T_DS, tc::desc_add(dw, 32 * k), tc::desc_add(db, 32 * k), id, 1u);
+          }
+        }
+      } else {
+        ctl->bad = 1;
+      }
+      tc::mma_commit(&ctl->bar2);
+    }
+    // dY and dV on the token rows; dS = diag(gamma) dS' + (Q~^T dO - W^T dE) on every row
+    const bool ok2 = tc::mbar_wait_bounded(&ctl->bar2, par, kWaitLimit);
+    tc::fence_after_sync();
+    if (!ok2) ctl->bad = 1;
+    if (qd < 2) {
+      uint32_t y0[16], y1[16];
+      tc::tmem_ld16(tmem + lane_addr + T_DY + vc, y0);
+      tc::tmem_ld16(tmem + lane_addr + T_DY + vc + 16, y1);
+      tc::tmem_wait_ld();
+      float y[32];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        y[j] = -__uint_as_float(y0[j]);
+        y[16 + j] = -__uint_as_float(y1[j]);
+      }
+      float* gy = ws.dY + (unit * C + r) * D + v0 + vc;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(gy + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
+      if (r < ci.n) {
+        const float bt = P.beta[(ci.t0 + r) * HV + h];
+        float* gv = A.dv + ((ci.t0 + r) * HV + h) * D + v0 + vc;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(gv + j) = make_float4(bt * y[j], bt * y[j + 1], bt * y[j + 2], bt * y[j + 3]);
+      }
+    }
+    {
+      uint32_t d0[16], d1[16];
+      tc::tmem_ld16(tmem + lane_addr + T_DS + vc, d0);
+      tc::tmem_ld16(tmem + lane_addr + T_DS + vc + 16, d1);
+      tc::tmem_wait_ld();
+      const float gm = __ldg(ws.loc.gamma + unit * D + r);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        Rv[j] = fmaf(gm, Rv[j], __uint_as_float(d0[j]));
+        Rv[16 + j] = fmaf(gm, Rv[16 + j], __uint_as_float(d1[j]));
+      }
+    }
+    if (tid == 0 && cidx > first) load_b(cidx - 1);     // T^T and W^T of this chunk are consumed
+    if (tc::named_sync_or(1, NT, ctl->bad != 0)) break;
+  }
+  if (ctl->bad) {
+    if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+  } else if (A.d_state0) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) A.d_state0[sbase + j] = Rv[j];
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, bool sbf16,
+                                cudaStream_t st) {
+  using namespace bst;
+  const int mc = plan_max_chunks(P);
+  const uint64_t units = static_cast<uint64_t>(mc > 0 ? mc : 1) * static_cast<uint64_t>(P.HV);
+  alignas(64) CUtensorMap tw, tu, tkt, tke, taq, tqt, ttt, twt;
+  if (!ws.loc.KendT || !encode_f32_blocks(&tw, ws.loc.W, units * C, D, D, C) ||
+      !encode_f32_blocks(&tu, ws.loc.U, units * C, D, D, C) ||
+      !encode_f32_blocks(&tkt, ws.loc.KendT, units * D, C, C, D) ||
+      !encode_f32_blocks(&tke, ws.loc.Kend, units * C, D, D, C) ||
+      !encode_f32_blocks(&taq, ws.loc.AqkT, units * C, C, C, C) ||
+      !encode_f32_blocks(&tqt, ws.loc.QtT, units * D, C, C, D) ||
+      !encode_f32_blocks(&ttt, ws.loc.TT, units * C, C, C, C) ||
+      !encode_f32_blocks(&twt, ws.loc.WT, units * D, C, C, D))
+    return cudaErrorNotSupported;
+  const dim3 grid(P.num_seqs, P.HV, D / BV);
+  auto fk = sbf16 ? bwd_fwd_scan_tc_kernel<true> : bwd_fwd_scan_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(F_DATA + 1024));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(bwd_rev_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(R_DATA + 1024));
+  if (e != cudaSuccess) return e;
+  fk<<<grid, NT, F_DATA + 1024, st>>>(P, ws, tw, tu, tkt);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_rev_scan_tc_kernel<<<grid, NT, R_DATA + 1024, st>>>(P, ws, A, tke, taq, tqt, ttt, twt);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A,
                              cudaStream_t st) {
   using namespace bvt;

@@ -17,6 +17,12 @@ struct SimtWorkspace {
   float* gamma; // [chunk][HV][D]
   float* T;     // [chunk][HV][C][C] (I + A_kk)^-1, or null (kept only by the backward pass)
   float* Kt;    // [chunk][HV][C][D] K~ = k^ exp(G), or null (likewise)
+  // transposed copies for the backward's tensor-core scans (K-major operands), or null:
+  float* KendT; // [chunk][HV][D][C]
+  float* QtT;   // [chunk][HV][D][C]
+  float* WT;    // [chunk][HV][D][C]
+  float* AqkT;  // [chunk][HV][C][C]
+  float* TT;    // [chunk][HV][C][C]
 };
 
 // 16-byte vector moves of N floats between registers and 16-byte aligned memory (scalar when
@@ -350,6 +356,13 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
     st_row(gQ + i * D + c0, qt);
     st_row(gK + i * D + c0, ke);
     if (ws.Kt) st_row(ws.Kt + unit * C * D + i * D + c0, kt);
+    if (ws.KendT) {
+#pragma unroll
+      for (int b = 0; b < JC; ++b) {
+        ws.KendT[(unit * D + c0 + b) * C + i] = ke[b];
+        ws.QtT[(unit * D + c0 + b) * C + i] = qt[b];
+      }
+    }
 #pragma unroll
     for (int b = 0; b < JC; ++b) {
       s_q[i * DP + c0 + b] = delta ? bi * kt[b] : 0.f;
@@ -359,6 +372,11 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
   for (int idx = tid; idx < C * C; idx += NT) ws.Aqk[unit * C * C + idx] = s_Aq[(idx / C) * CP + idx % C];
   if (ws.T)
     for (int idx = tid; idx < C * C; idx += NT) ws.T[unit * C * C + idx] = s_T[(idx / C) * CP + idx % C];
+  if (ws.TT)
+    for (int idx = tid; idx < C * C; idx += NT) {
+      ws.TT[unit * C * C + idx] = s_T[(idx % C) * CP + idx / C];
+      ws.AqkT[unit * C * C + idx] = s_Aq[(idx % C) * CP + idx / C];
+    }
   __syncthreads();
   // W = T (beta k exp(G)),  U = T (beta v)
   float w[RT][JC], uu[RT][JC];
@@ -384,6 +402,15 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
   for (int a = 0; a < RT; ++a) {
     st_row(gW + (r0 + a) * D + c0, w[a]);
     st_row(gU + (r0 + a) * D + c0, uu[a]);
+  }
+  if (ws.WT) {
+#pragma unroll
+    for (int b = 0; b < JC; ++b) {
+      float col[RT];
+#pragma unroll
+      for (int a = 0; a < RT; ++a) col[a] = w[a][b];
+      st_row(ws.WT + (unit * D + c0 + b) * C + r0, col);
+    }
   }
 }
 

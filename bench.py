@@ -464,8 +464,9 @@ def backward_algorithmic_bytes(p) -> float:
     return float(reads + writes)
 
 
-def time_prefill_bwd(p, dev, steps, warmup):
-    """The backward pass on resident inputs and output gradients (CUDA events)."""
+def time_prefill_bwd(p, dev, steps, warmup, compact=False):
+    """The backward pass on resident inputs and output gradients (CUDA events); `compact`
+    runs it in the bounded workspace (KDA_FLAG_COMPACT)."""
     import torch
     import gated_delta_rule_deltanet_gb300 as kda
     from workloads import torch_io
@@ -476,7 +477,7 @@ def time_prefill_bwd(p, dev, steps, warmup):
     d_state0 = torch.zeros_like(d_state)
     params = kda.kda._prefill_params(t["q"], t["k"], t["v"], t["beta"], t["log_decay"],
                                      t["input_row_offsets"], t["slot_idx"], t["state_pool"],
-                                     p.chunk, p.scale, True, False)
+                                     p.chunk, p.scale, True, False, compact=compact)
     import ctypes
     n = ctypes.c_size_t(0)
     kda.load().kda_prefill_bwd_workspace_size(ctypes.byref(params), ctypes.byref(n))
@@ -485,7 +486,8 @@ def time_prefill_bwd(p, dev, steps, warmup):
     def step():
         kda.prefill_bwd(t["q"], t["k"], t["v"], t["beta"], t["log_decay"],
                         t["input_row_offsets"], t["slot_idx"], t["state_pool"], d_o, d_state,
-                        chunk=p.chunk, scale=p.scale, d_state0=d_state0, workspace=ws)
+                        chunk=p.chunk, scale=p.scale, d_state0=d_state0, workspace=ws,
+                        compact=compact)
 
     for _ in range(warmup):
         step()
@@ -733,6 +735,14 @@ def ours_arm(args, rank, world, local):
                                        "achieved_gbs": bbytes / (bms / 1e3) / 1e9,
                                        "frac_hbm": bbytes / (bms / 1e3) / 1e9
                                        / peaks["hbm_gbs"]}})
+        # the bounded-workspace form on gdn_prefill and on kda_prefill
+        for cp in (bp, workloads.workload("kda_prefill", replica=rank)):
+            cms_, cws_ = time_prefill_bwd(cp, dev, 3, 3, compact=True)
+            cval_, _ = aggregate(float(cp.total_tokens), cms_ / 1e3, world, dev)
+            also.append({"workload": f"{cp.name} backward, bounded workspace "
+                                     "(kda_prefill_bwd, KDA_FLAG_COMPACT)",
+                         "metric": "backward tokens/s", "value": cval_, "unit": "tokens/s",
+                         "ms_per_step": cms_, "workspace_bytes": cws_})
 
         cms = time_conv_gates(bp, dev, 50, 3)
         cval, _ = aggregate(float(bp.total_tokens), cms / 1e3, world, dev)

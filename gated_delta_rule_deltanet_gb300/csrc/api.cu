@@ -39,11 +39,11 @@ cudaError_t launch_conv_gates(const void* x, const float* w, const float* bias, 
                               void* y, float* g, float* beta, int64_t T, int B, int CD, int HV,
                               int GW, int num_slots, int W, bool bf16, int32_t* err,
                               cudaStream_t st);
-size_t bwd_workspace_bytes(const Problem& P, bool qbf16);
+size_t bwd_workspace_bytes(const Problem& P, bool qbf16, bool compact);
 cudaError_t launch_prefill_bwd(const Problem& P, void* workspace, const float* d_o,
                                const float* d_state, float* dq, float* dk, float* dv,
                                float* dbeta, float* dg, float* d_state0, bool qbf16, bool perch,
-                               bool sbf16, cudaStream_t stream);
+                               bool sbf16, bool compact, cudaStream_t stream);
 }  // namespace kda
 
 using kda::Problem;
@@ -308,7 +308,7 @@ kda_status_t kda_prefill_bwd_workspace_size(const kda_params_t* p, size_t* bytes
   if (!bytes) return KDA_ERR_INVALID_ARG;
   kda_status_t s = check_prefill(p, &P);
   if (s != KDA_OK) return s;
-  *bytes = kda::bwd_workspace_bytes(P, p->qkv_dtype == KDA_DTYPE_BF16);
+  *bytes = kda::bwd_workspace_bytes(P, p->qkv_dtype == KDA_DTYPE_BF16, (p->flags & KDA_FLAG_COMPACT) != 0);
   return KDA_OK;
 }
 
@@ -333,7 +333,7 @@ kda_status_t kda_prefill_bwd(const kda_params_t* p, const void* q, const void* k
       !aligned(dk, 4) || !aligned(dv, 4) || !aligned(dbeta, 4) || !aligned(dlog_decay, 4) ||
       !aligned(d_state0, 4))
     return KDA_ERR_INVALID_ARG;
-  const size_t need = kda::bwd_workspace_bytes(P, p->qkv_dtype == KDA_DTYPE_BF16);
+  const size_t need = kda::bwd_workspace_bytes(P, p->qkv_dtype == KDA_DTYPE_BF16, (p->flags & KDA_FLAG_COMPACT) != 0);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
   P.q = q; P.k = k; P.v = v; P.beta = beta; P.g = log_decay;
   P.offsets = input_row_offsets; P.slot_idx = slot_idx;
@@ -344,7 +344,8 @@ kda_status_t kda_prefill_bwd(const kda_params_t* p, const void* q, const void* k
   return to_status(kda::launch_prefill_bwd(
       P, workspace, d_o, d_state, dq, dk, dv, dbeta, dlog_decay, d_state0,
       p->qkv_dtype == KDA_DTYPE_BF16, p->decay_kind == KDA_DECAY_PER_CHANNEL,
-      p->state_dtype == KDA_DTYPE_BF16, static_cast<cudaStream_t>(stream)));
+      p->state_dtype == KDA_DTYPE_BF16, (p->flags & KDA_FLAG_COMPACT) != 0,
+      static_cast<cudaStream_t>(stream)));
 }
 
 kda_status_t kda_conv_gates_fwd(const kda_params_t* p, int32_t width, const void* x,

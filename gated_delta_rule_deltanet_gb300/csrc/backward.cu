@@ -34,18 +34,35 @@
 // The additive write (KDA_FLAG_NO_DELTA) has no L and no K~ S term: T = I, W = 0, and their
 // gradient terms vanish.  The pairwise decay is evaluated per pair and channel, as in the
 // CUDA-core forward, so no factor overflows.
+#include <algorithm>
+
 #include "backward.cuh"
 #include "tc_utils.cuh"
 
 namespace kda {
 
-// tc: the tensor-core scans run (d = 128, chunk 64, bf16 inputs) and need the transposed
-// copies of the local stage's matrices
-static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws, bool tc) {
+// Slots of the bounded workspace: a window of chunk positions holds every sequence's next
+// `wc` chunks, wc = max(1, kBwdWindowSlots / (num_seqs * HV)) (so max(kBwdWindowSlots,
+// num_seqs * HV) (chunk, value head) slots).
+constexpr int kBwdWindowSlots = 512;
+
+static int bwd_window_chunks(const Problem& P) {
+  const int64_t pairs = static_cast<int64_t>(P.num_seqs) * P.HV;
+  return static_cast<int>(std::max<int64_t>(1, kBwdWindowSlots / std::max<int64_t>(1, pairs)));
+}
+
+static bool bwd_tc(const Problem& P, bool qbf16) { return P.D == 128 && P.chunk == 64 && qbf16; }
+
+// tc: the tensor-core kernels run (d = 128, chunk 64, bf16 inputs): the local stage keeps the
+// transposed copies they read instead of Q~, A_qk and T.  wc > 0: the bounded workspace, the
+// per-chunk arrays for one window's slots plus the checkpoints and the carried gradient.
+static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws, bool tc, int wc) {
   size_t off = 0;
   PlanView pv;
   off = plan_layout(P, base, off, &pv);
-  const size_t units = static_cast<size_t>(plan_max_chunks(P)) * P.HV;
+  const int mc = plan_max_chunks(P);
+  const size_t slots = wc > 0 ? static_cast<size_t>(P.num_seqs) * wc : static_cast<size_t>(mc);
+  const size_t units = slots * P.HV;
   const size_t C = P.chunk, D = P.D;
   auto take = [&](size_t floats) -> float* {
     float* p = base ? reinterpret_cast<float*>(base + off) : nullptr;
@@ -56,11 +73,8 @@ static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws, bool tc
   w.loc.plan = pv;
   w.loc.W = take(units * C * D);
   w.loc.U = take(units * C * D);
-  w.loc.Qt = take(units * C * D);
   w.loc.Kend = take(units * C * D);
-  w.loc.Aqk = take(units * C * C);
   w.loc.gamma = take(units * D);
-  w.loc.T = take(units * C * C);
   w.loc.Kt = take(units * C * D);
   if (tc) {
     w.loc.KendT = take(units * D * C);
@@ -68,6 +82,10 @@ static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws, bool tc
     w.loc.WT = take(units * D * C);
     w.loc.AqkT = take(units * C * C);
     w.loc.TT = take(units * C * C);
+  } else {
+    w.loc.Qt = take(units * C * D);
+    w.loc.Aqk = take(units * C * C);
+    w.loc.T = take(units * C * C);
   }
   w.Sck = take(units * D * D);
   w.dSck = take(units * D * D);
@@ -80,14 +98,22 @@ static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws, bool tc
   w.dM = take(units * C * C);
   w.dgam = take(units * D);
   w.dbr = take(units * C);
+  if (wc > 0) {
+    // checkpoint entries: sequence b's windows 1 .. ceil(n_b / wc) - 1 at c0_b / wc + w - 1,
+    // disjoint between sequences and below max_chunks / wc
+    w.ckpt = take(static_cast<size_t>(std::max(1, mc / wc)) * P.HV * D * D);
+    w.carry = take(static_cast<size_t>(P.num_seqs) * P.HV * D * D);
+  }
   if (ws) *ws = w;
   return off;
 }
 
-static bool bwd_tc(const Problem& P, bool qbf16) { return P.D == 128 && P.chunk == 64 && qbf16; }
+static int bwd_wc(const Problem& P, bool qbf16, bool compact) {
+  return compact && bwd_tc(P, qbf16) ? bwd_window_chunks(P) : 0;
+}
 
-size_t bwd_workspace_bytes(const Problem& P, bool qbf16) {
-  return bwd_layout(P, nullptr, nullptr, bwd_tc(P, qbf16));
+size_t bwd_workspace_bytes(const Problem& P, bool qbf16, bool compact) {
+  return bwd_layout(P, nullptr, nullptr, bwd_tc(P, qbf16), bwd_wc(P, qbf16, compact));
 }
 
 // ------------------------------------------------------------------------------- scan
@@ -334,7 +360,7 @@ struct BwdVcSmem {
 };
 
 template <int D, int C, int BV, bool QBF16>
-__global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws, BwdArgs A) {
+__global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws, BwdArgs A, ChunkWindow win) {
   constexpr int NT = 256;
   constexpr int DP = BwdVcSmem<D, C, BV>::DP, CP = BwdVcSmem<D, C, BV>::CP;
   constexpr int IR = C / 16, JC = D / 16, JM = C / 16;
@@ -352,8 +378,9 @@ __global__ void __launch_bounds__(256) bwd_vc_kernel(Problem P, BwdWorkspace ws,
   float* s_R = s_dY + C * BV;       // [C][BV] V - K~ S
   float* s_Et = s_R + C * BV;       // [BV][CP]
 
-  if (ws.loc.plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= ws.loc.plan.info[0]) return;
-  const ChunkInfo ci = ws.loc.plan.chunks[blockIdx.x];
+  int gc;
+  if (ws.loc.plan.info[1] == 0 || !window_chunk(ws.loc.plan, P.num_seqs, win, blockIdx.x, &gc)) return;
+  const ChunkInfo ci = ws.loc.plan.chunks[gc];
   const int h = blockIdx.y, HV = P.HV, tid = threadIdx.x;
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
   const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
@@ -494,7 +521,7 @@ __device__ __forceinline__ float halfwarp_sum(float v) {
 }
 
 template <int D, int C, bool QBF16, bool PERCH>
-__global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace ws, BwdArgs A) {
+__global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace ws, BwdArgs A, ChunkWindow win) {
   constexpr int NT = 256;
   constexpr int IR = C / 16, JC = D / 16;
   constexpr int GW = BwdPairSmem<D, C, PERCH>::GW;
@@ -517,8 +544,9 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
   float* s_ga = s_gam + D;         // [D] G at the chunk's middle token (per-channel decay)
   float* s_E = s_ga + D;           // [C][DP] exp(G - G_a) (per-channel decay, anchored)
 
-  if (ws.loc.plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= ws.loc.plan.info[0]) return;
-  const ChunkInfo ci = ws.loc.plan.chunks[blockIdx.x];
+  int gc;
+  if (ws.loc.plan.info[1] == 0 || !window_chunk(ws.loc.plan, P.num_seqs, win, blockIdx.x, &gc)) return;
+  const ChunkInfo ci = ws.loc.plan.chunks[gc];
   const int kh = blockIdx.y, HV = P.HV, ratio = HV / P.HK, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
@@ -807,10 +835,12 @@ static cudaError_t set_smem(K kernel, size_t bytes) {
 }
 
 template <int D, int C, bool QBF16, bool PERCH, bool SBF16>
-static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A,
+static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, int wc,
                                 cudaStream_t st) {
   constexpr int BV = D >= 32 ? 32 : D;
-  const int mc = plan_max_chunks(P);
+  // bf16 inputs at d = 128, chunk 64: the scans and the value-dimension contractions on tensor
+  // cores (tf32 operands; the fp32 inputs' tighter bound keeps them on CUDA cores)
+  constexpr bool kTc = D == 128 && C == 64 && QBF16;
   cudaError_t e;
   auto lk = simt_local_kernel<D, C, QBF16, PERCH>;
   if ((e = set_smem(lk, SimtLocalSmem<D, C>::bytes)) != cudaSuccess) return e;
@@ -820,68 +850,98 @@ static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const 
   if ((e = set_smem(vk, BwdVcSmem<D, C, BV>::bytes)) != cudaSuccess) return e;
   auto pk = bwd_pair_kernel<D, C, QBF16, PERCH>;
   if ((e = set_smem(pk, BwdPairSmem<D, C, PERCH>::bytes)) != cudaSuccess) return e;
-  if (mc > 0) {
-    lk<<<dim3(mc, P.HV), 256, SimtLocalSmem<D, C>::bytes, st>>>(P, ws.loc);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  // bf16 inputs at d = 128, chunk 64: both directions of the scan on tensor cores
-  e = (D == 128 && C == 64 && QBF16) ? launch_bwd_scans_tc(P, ws, A, SBF16, st) : cudaErrorNotSupported;
-  if (e == cudaErrorNotSupported) {
-    sk<<<dim3(P.num_seqs, P.HV, D / BV), 256, BwdScanSmem<D, C, BV>::bytes, st>>>(P, ws, A);
-    e = cudaGetLastError();
-  }
-  if (e != cudaSuccess) return e;
-  if (mc > 0) {
-    // bf16 inputs at d = 128, chunk 64: the contractions on tensor cores (tf32 operands; the
-    // fp32 inputs' tighter bound keeps them on CUDA cores)
-    e = (D == 128 && C == 64 && QBF16) ? launch_bwd_vc_tc(P, ws, A, st) : cudaErrorNotSupported;
-    if (e == cudaErrorNotSupported) {
-      vk<<<dim3(mc, P.HV), 256, BwdVcSmem<D, C, BV>::bytes, st>>>(P, ws, A);
+  // the chunk-parallel kernels of one window (or of every chunk: wc == 0)
+  auto local = [&](ChunkWindow win, int slots) -> cudaError_t {
+    if (slots <= 0) return cudaSuccess;
+    lk<<<dim3(slots, P.HV), 256, SimtLocalSmem<D, C>::bytes, st>>>(P, ws.loc, win);
+    return cudaGetLastError();
+  };
+  auto contractions = [&](ChunkWindow win, int slots) -> cudaError_t {
+    if (slots <= 0) return cudaSuccess;
+    cudaError_t r = kTc ? launch_bwd_vc_tc(P, ws, A, win, slots, st) : cudaErrorNotSupported;
+    if (r == cudaErrorNotSupported) {
+      vk<<<dim3(slots, P.HV), 256, BwdVcSmem<D, C, BV>::bytes, st>>>(P, ws, A, win);
+      r = cudaGetLastError();
+    }
+    if (r != cudaSuccess) return r;
+    pk<<<dim3(slots, P.HK), 256, BwdPairSmem<D, C, PERCH>::bytes, st>>>(P, ws, A, win);
+    return cudaGetLastError();
+  };
+  if (wc == 0) {
+    const int mc = plan_max_chunks(P);
+    const ChunkWindow all{0, 0};
+    if ((e = local(all, mc)) != cudaSuccess) return e;
+    if (kTc) {
+      e = launch_bwd_scans_tc(P, ws, A, SBF16, all, mc, true, st);
+    } else {
+      sk<<<dim3(P.num_seqs, P.HV, D / BV), 256, BwdScanSmem<D, C, BV>::bytes, st>>>(P, ws, A);
       e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    pk<<<dim3(mc, P.HK), 256, BwdPairSmem<D, C, PERCH>::bytes, st>>>(P, ws, A);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    return contractions(all, mc);
+  }
+  if (!kTc) return cudaErrorNotSupported;
+  // bounded workspace: the longest sequence sets the number of windows (one read of the
+  // chunk table's summary), a forward sweep stores each window's entering state, and the
+  // backward sweep reruns each window from its checkpoint, latest window first
+  int32_t longest = 0;
+  if ((e = cudaMemcpyAsync(&longest, ws.loc.plan.info + 2, sizeof(int32_t), cudaMemcpyDeviceToHost, st)) !=
+          cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess)
+    return e;
+  const int nw = std::max(1, (longest + wc - 1) / wc);
+  const int slots = P.num_seqs * wc;
+  for (int w = 0; w + 1 < nw; ++w) {
+    const ChunkWindow win{w, wc};
+    if ((e = local(win, slots)) != cudaSuccess) return e;
+    if ((e = launch_bwd_scans_tc(P, ws, A, SBF16, win, slots, false, st)) != cudaSuccess) return e;
+  }
+  for (int w = nw - 1; w >= 0; --w) {
+    const ChunkWindow win{w, wc};
+    if ((e = local(win, slots)) != cudaSuccess) return e;
+    if ((e = launch_bwd_scans_tc(P, ws, A, SBF16, win, slots, true, st)) != cudaSuccess) return e;
+    if ((e = contractions(win, slots)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
 template <int D, int C>
 static cudaError_t launch_bwd_dc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A,
-                                 bool q, bool pc, bool sb, cudaStream_t st) {
+                                 bool q, bool pc, bool sb, int wc, cudaStream_t st) {
   if (q) {
-    if (pc) return sb ? launch_bwd_t<D, C, true, true, true>(P, ws, A, st)
-                      : launch_bwd_t<D, C, true, true, false>(P, ws, A, st);
-    return sb ? launch_bwd_t<D, C, true, false, true>(P, ws, A, st)
-              : launch_bwd_t<D, C, true, false, false>(P, ws, A, st);
+    if (pc) return sb ? launch_bwd_t<D, C, true, true, true>(P, ws, A, wc, st)
+                      : launch_bwd_t<D, C, true, true, false>(P, ws, A, wc, st);
+    return sb ? launch_bwd_t<D, C, true, false, true>(P, ws, A, wc, st)
+              : launch_bwd_t<D, C, true, false, false>(P, ws, A, wc, st);
   }
-  if (pc) return sb ? launch_bwd_t<D, C, false, true, true>(P, ws, A, st)
-                    : launch_bwd_t<D, C, false, true, false>(P, ws, A, st);
-  return sb ? launch_bwd_t<D, C, false, false, true>(P, ws, A, st)
-            : launch_bwd_t<D, C, false, false, false>(P, ws, A, st);
+  if (pc) return sb ? launch_bwd_t<D, C, false, true, true>(P, ws, A, wc, st)
+                    : launch_bwd_t<D, C, false, true, false>(P, ws, A, wc, st);
+  return sb ? launch_bwd_t<D, C, false, false, true>(P, ws, A, wc, st)
+            : launch_bwd_t<D, C, false, false, false>(P, ws, A, wc, st);
 }
 
 template <int D>
 static cudaError_t launch_bwd_d(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A,
-                                bool q, bool pc, bool sb, cudaStream_t st) {
+                                bool q, bool pc, bool sb, int wc, cudaStream_t st) {
   switch (P.chunk) {
-    case 16: return launch_bwd_dc<D, 16>(P, ws, A, q, pc, sb, st);
-    case 32: return launch_bwd_dc<D, 32>(P, ws, A, q, pc, sb, st);
-    default: return launch_bwd_dc<D, 64>(P, ws, A, q, pc, sb, st);
+    case 16: return launch_bwd_dc<D, 16>(P, ws, A, q, pc, sb, wc, st);
+    case 32: return launch_bwd_dc<D, 32>(P, ws, A, q, pc, sb, wc, st);
+    default: return launch_bwd_dc<D, 64>(P, ws, A, q, pc, sb, wc, st);
   }
 }
 
 cudaError_t launch_prefill_bwd(const Problem& P, void* workspace, const float* d_o,
                                const float* d_state, float* dq, float* dk, float* dv,
                                float* dbeta, float* dg, float* d_state0, bool qbf16, bool perch,
-                               bool sbf16, cudaStream_t stream) {
+                               bool sbf16, bool compact, cudaStream_t stream) {
   BwdWorkspace ws;
-  bwd_layout(P, static_cast<char*>(workspace), &ws, bwd_tc(P, qbf16));
+  const int wc = bwd_wc(P, qbf16, compact);
+  bwd_layout(P, static_cast<char*>(workspace), &ws, bwd_tc(P, qbf16), wc);
   const BwdArgs A{d_o, d_state, dq, dk, dv, dbeta, dg, d_state0};
   cudaError_t e = launch_plan(P, ws.loc.plan, stream);
   if (e != cudaSuccess) return e;
-  if (P.D == 128) return launch_bwd_d<128>(P, ws, A, qbf16, perch, sbf16, stream);
-  return launch_bwd_d<16>(P, ws, A, qbf16, perch, sbf16, stream);
+  if (P.D == 128) return launch_bwd_d<128>(P, ws, A, qbf16, perch, sbf16, wc, stream);
+  return launch_bwd_d<16>(P, ws, A, qbf16, perch, sbf16, wc, stream);
 }
 
 }  // namespace kda

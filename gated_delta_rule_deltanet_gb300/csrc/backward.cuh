@@ -30,14 +30,17 @@ struct BwdWorkspace {
   float* dM;    // [chunk][HV][C][C]
   float* dgam;  // [chunk][HV][D]
   float* dbr;   // [chunk][HV][C]
+  // bounded workspace (windows of chunk positions; "chunk" above is then a window slot):
+  float* ckpt;  // [entry][HV][D][D] the state entering each window after a sequence's first
+  float* carry; // [num_seqs][HV][D][D] the state gradient handed from window to window
 };
 
 // The contractions over the value dimension of every (chunk, value head) on tensor cores
 // (d = 128, chunk 64): dQ~, dK~, dK_end, dA, dM, dgamma and the first term of dbeta into the
 // workspace, as bwd_vc_kernel computes them.  Returns cudaErrorNotSupported when an operand
 // cannot be copied by TMA (d_o not 16-byte aligned), so the caller runs the CUDA-core kernel.
-cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A,
-                             cudaStream_t st);
+cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, ChunkWindow win,
+                             int slots, cudaStream_t st);
 
 // The scan on tensor cores (d = 128, chunk 64): a forward kernel recording each chunk's
 // incoming state and corrected values, then a reverse kernel carrying the state gradient
@@ -45,7 +48,18 @@ cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const Bwd
 // computes them.  Needs the local stage's transposed copies (loc.KendT ... loc.TT); returns
 // cudaErrorNotSupported when a tensor map cannot be encoded, so the caller runs the
 // CUDA-core scan.
+//
+// Windowed (win.wc > 0, `slots` window slots): the chunks of window win.w only.  With
+// record = false the forward kernel only carries the state through the window and stores it
+// as the next window's checkpoint, and the reverse kernel does not run (the checkpoint sweep);
+// with record = true both run as above, the state entering the window from its checkpoint
+// and the state gradient handed on through ws.carry.
 cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, bool sbf16,
-                                cudaStream_t st);
+                                ChunkWindow win, int slots, bool record, cudaStream_t st);
+
+// index of the checkpoint of window w >= 1 of the sequence whose first chunk is c0
+__host__ __device__ __forceinline__ int64_t ckpt_entry(int c0, ChunkWindow win) {
+  return static_cast<int64_t>(c0 / win.wc) + win.w - 1;
+}
 
 }  // namespace kda

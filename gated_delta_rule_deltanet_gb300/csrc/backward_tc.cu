@@ -19,7 +19,10 @@
 // stored, so TMA copies 32-value column blocks of them with the 128-byte swizzle straight
 // into the operand layout of kind::tf32 MMAs: fp32 operands read with a 10-bit mantissa
 // (the precision of the forward's fp16 operands) and fp32's exponent range, which the
-// gradients need (their scale is the caller's).  The value dimension runs through a
+// gradients need (their scale is the caller's).  The MMA reads only an operand's top bits,
+// which would truncate every copied value toward zero, a bias that accumulates over a
+// contraction; so every operand is rounded to the nearest tf32 first (in place after its
+// copy here, where the threads write it in the scans).  The value dimension runs through a
 // two-stage ring in four blocks; the three accumulators (256 tensor-memory columns) stay in
 // tensor memory until the epilogue stages them in shared memory for coalesced stores.
 #include "backward.cuh"
@@ -60,7 +63,7 @@ __global__ void __launch_bounds__(bvt::NT, 2)
     bwd_vc_tc_kernel(Problem P, BwdWorkspace ws, BwdArgs A,
                      const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dy,
                      const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_ds,
-                     const __grid_constant__ CUtensorMap tm_e) {
+                     const __grid_constant__ CUtensorMap tm_e, ChunkWindow win) {
   using namespace bvt;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the swizzled blocks need a 1024-byte aligned base; the control block takes the slack
@@ -69,12 +72,12 @@ __global__ void __launch_bounds__(bvt::NT, 2)
   unsigned char* const data = smem_raw + pad;
   Ctrl* const ctl = reinterpret_cast<Ctrl*>(pad >= CTRL_BYTES ? smem_raw : data + DATA);
 
-  const int gc = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int plan_valid = ws.loc.plan.info[1], plan_chunks = ws.loc.plan.info[0];
-  if (plan_valid == 0 || gc >= plan_chunks) return;
+  const int slot = blockIdx.x, h = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int gc;
+  if (ws.loc.plan.info[1] == 0 || !window_chunk(ws.loc.plan, P.num_seqs, win, slot, &gc)) return;
   const ChunkInfo ci = ws.loc.plan.chunks[gc];
   const int HV = P.HV, n = ci.n;
-  const int64_t unit = static_cast<int64_t>(gc) * HV + h;
+  const int64_t unit = static_cast<int64_t>(slot) * HV + h;
   const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
   const uint32_t sd = tc::smem_u32(data);
 
@@ -125,24 +128,9 @@ __global__ void __launch_bounds__(bvt::NT, 2)
     const uint32_t par = static_cast<uint32_t>(q >> 1) & 1u;
     const bool landed = tc::mbar_wait_bounded(&ctl->full[st], par, kWaitLimit);
     if (!landed) ctl->bad = 1;
-    if (tid == 0 && landed) {
-      tc::fence_after_sync();
-      const uint32_t base = sd + st * STAGE;
-      const uint64_t da = tc::smem_desc_sw128(base + A_OFF, 1024);
-      const uint64_t ds = tc::smem_desc_sw128(base + S_OFF, 1024);
-      const uint64_t dd = tc::smem_desc_sw128(base + DS_OFF, 1024);
-      const uint64_t de = tc::smem_desc_sw128(base + E_OFF, 1024);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {             // K = 8 values (32 bytes) per instruction
-        const uint32_t acc = (q > 0 || k > 0) ? 1u : 0u;
-        tc::mma_ss_tf32(tmem + T_QK, tc::desc_add(da, 32 * k), tc::desc_add(ds, 32 * k), id_qk, acc);
-        tc::mma_ss_tf32(tmem + T_MA, tc::desc_add(da, 32 * k), tc::desc_add(de, 32 * k), id_e, acc);
-        tc::mma_ss_tf32(tmem + T_KE, tc::desc_add(dd, 32 * k), tc::desc_add(de, 32 * k), id_e, acc);
-      }
-      tc::mma_commit(&ctl->mdone[st]);
-    }
     if (landed) {
-      const unsigned char* blk = data + st * STAGE;
+      unsigned char* blk = data + st * STAGE;
+      // the partial sums from the copied fp32 values ...
 #pragma unroll
       for (int j = 0; j < 4; ++j) {             // S and dS' rows of key channel gcr
         const uint32_t off = tc::sw128_offset(gcr, 4 * ghalf + j);
@@ -159,8 +147,38 @@ __global__ void __launch_bounds__(bvt::NT, 2)
           br += y.x * vv[4 * j] + y.y * vv[4 * j + 1] + y.z * vv[4 * j + 2] + y.w * vv[4 * j + 3];
         }
       }
+      __syncthreads();
+      // ... then every value rounded to tf32 in place for the MMAs
+      float4* b4 = reinterpret_cast<float4*>(blk);
+      for (int u = tid; u < static_cast<int>(STAGE / 16); u += NT) {
+        float4 x = b4[u];
+        x.x = tf32_nearest(x.x);
+        x.y = tf32_nearest(x.y);
+        x.z = tf32_nearest(x.z);
+        x.w = tf32_nearest(x.w);
+        b4[u] = x;
+      }
+    } else {
+      __syncthreads();
     }
-    __syncthreads();                            // the stage's shared-memory reads are done
+    tc::fence_async_smem();
+    __syncthreads();                            // the stage's shared-memory traffic is done
+    if (tid == 0 && landed) {
+      tc::fence_after_sync();
+      const uint32_t base = sd + st * STAGE;
+      const uint64_t da = tc::smem_desc_sw128(base + A_OFF, 1024);
+      const uint64_t ds = tc::smem_desc_sw128(base + S_OFF, 1024);
+      const uint64_t dd = tc::smem_desc_sw128(base + DS_OFF, 1024);
+      const uint64_t de = tc::smem_desc_sw128(base + E_OFF, 1024);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {             // K = 8 values (32 bytes) per instruction
+        const uint32_t acc = (q > 0 || k > 0) ? 1u : 0u;
+        tc::mma_ss_tf32(tmem + T_QK, tc::desc_add(da, 32 * k), tc::desc_add(ds, 32 * k), id_qk, acc);
+        tc::mma_ss_tf32(tmem + T_MA, tc::desc_add(da, 32 * k), tc::desc_add(de, 32 * k), id_e, acc);
+        tc::mma_ss_tf32(tmem + T_KE, tc::desc_add(dd, 32 * k), tc::desc_add(de, 32 * k), id_e, acc);
+      }
+      tc::mma_commit(&ctl->mdone[st]);
+    }
     if (tid == 0 && q + 2 < 4) {
       if (tc::mbar_wait_bounded(&ctl->mdone[st], par, kWaitLimit)) issue(q + 2);
       else ctl->bad = 1;
@@ -313,7 +331,8 @@ __device__ __forceinline__ uint32_t kmaj(uint32_t row, uint32_t k, uint32_t rows
 template <bool SBF16>
 __global__ void __launch_bounds__(bst::NT, 1)
     bwd_fwd_scan_tc_kernel(Problem P, BwdWorkspace ws, const __grid_constant__ CUtensorMap tm_w,
-                           const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_kt) {
+                           const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_kt,
+                           ChunkWindow win, int record) {
   using namespace bst;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -322,14 +341,18 @@ __global__ void __launch_bounds__(bst::NT, 1)
   if (ws.loc.plan.info[1] == 0) return;
   const int b = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
   const int HV = P.HV, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int first = ws.loc.plan.seq_chunk0[b], last = ws.loc.plan.seq_chunk0[b + 1];
-  if (first >= last) return;
+  // this CTA's chunks: the sequence's, or those of window win.w (slots b * wc ..)
+  const int c0 = ws.loc.plan.seq_chunk0[b], nb = ws.loc.plan.seq_chunk0[b + 1] - c0;
+  const int j0 = win.wc ? win.w * win.wc : 0, j1 = win.wc ? min(nb, j0 + win.wc) : nb;
+  if (j0 >= j1) return;
+  const int first = c0 + j0, last = c0 + j1;
+  const int slot0 = win.wc ? b * win.wc - first : 0;   // slot of chunk cidx: slot0 + cidx
   const int qd = warp & 3, chalf = warp >> 2;
   const int r = 32 * qd + lane;                 // TMEM lane: key channel (state) / token (X)
   const int vc = 32 * chalf;                    // this thread's 32 value columns within the tile
   const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
   const uint32_t sd = tc::smem_u32(data);
-  auto unit_of = [&](int cidx) { return static_cast<int64_t>(cidx) * HV + h; };
+  auto unit_of = [&](int cidx) { return static_cast<int64_t>(slot0 + cidx) * HV + h; };
 
   auto load_a = [&](int cidx) {                 // W and the CTA's U columns of chunk cidx
     const int32_t row = static_cast<int32_t>(unit_of(cidx) * C);
@@ -361,10 +384,17 @@ __global__ void __launch_bounds__(bst::NT, 1)
   }
   float Sv[32];
   const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + static_cast<int64_t>(r) * D + v0 + vc;
+  const int64_t row_off = static_cast<int64_t>(r) * D + v0 + vc;
+  if (j0 > 0) {                                 // a later window: from its checkpoint
+    const float* ck = ws.ckpt + (ckpt_entry(c0, win) * HV + h) * D * D + row_off;
 #pragma unroll
-  for (int j = 0; j < 32; ++j)
-    Sv[j] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[sbase + j])
-                  : static_cast<const float*>(P.pool)[sbase + j];
+    for (int j = 0; j < 32; ++j) Sv[j] = ck[j];
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      Sv[j] = SBF16 ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.pool)[sbase + j])
+                    : static_cast<const float*>(P.pool)[sbase + j];
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -377,11 +407,14 @@ __global__ void __launch_bounds__(bst::NT, 1)
     const int64_t unit = unit_of(cidx);
     // S entering the chunk: into the workspace, and transposed as the B operand of W S
     {
-      float* gs = ws.Sck + (unit * D + r) * D + v0 + vc;
+      if (record) {
+        float* gs = ws.Sck + (unit * D + r) * D + v0 + vc;
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(gs + j) = make_float4(Sv[j], Sv[j + 1], Sv[j + 2], Sv[j + 3]);
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(gs + j) = make_float4(Sv[j], Sv[j + 1], Sv[j + 2], Sv[j + 3]);
+      }
 #pragma unroll
-      for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(data + F_ST + kmaj(vc + j, r, 64)) = Sv[j];
+      for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(data + F_ST + kmaj(vc + j, r, 64)) = tf32_nearest(Sv[j]);
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -422,11 +455,14 @@ __global__ void __launch_bounds__(bst::NT, 1)
         e[j + 2] = u.z - __uint_as_float(x[2]);
         e[j + 3] = u.w - __uint_as_float(x[3]);
       }
-      float* ge = ws.E + (unit * C + r) * D + v0 + vc;
+      if (record) {
+        float* ge = ws.E + (unit * C + r) * D + v0 + vc;
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(ge + j) = make_float4(e[j], e[j + 1], e[j + 2], e[j + 3]);
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(ge + j) = make_float4(e[j], e[j + 1], e[j + 2], e[j + 3]);
+      }
 #pragma unroll
-      for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(data + F_ET + kmaj(vc + j, r, 64)) = e[j];
+      for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(data + F_ET + kmaj(vc + j, r, 64)) = tf32_nearest(e[j]);
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -467,7 +503,15 @@ __global__ void __launch_bounds__(bst::NT, 1)
     if (tid == 0 && cidx + 1 < last) load_b(cidx + 1);   // K_end^T of this chunk is consumed
     if (tc::named_sync_or(1, NT, ctl->bad != 0)) break;
   }
-  if (ctl->bad && tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+  if (ctl->bad) {
+    if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+  } else if (!record && j1 < nb) {              // the checkpoint of the next window
+    ChunkWindow next = win;
+    next.w += 1;
+    float* ck = ws.ckpt + (ckpt_entry(c0, next) * HV + h) * D * D + row_off;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(ck + j) = make_float4(Sv[j], Sv[j + 1], Sv[j + 2], Sv[j + 3]);
+  }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -477,7 +521,8 @@ __global__ void __launch_bounds__(bst::NT, 1)
 __global__ void __launch_bounds__(bst::NT, 1)
     bwd_rev_scan_tc_kernel(Problem P, BwdWorkspace ws, BwdArgs A, const __grid_constant__ CUtensorMap tm_ke,
                            const __grid_constant__ CUtensorMap tm_aq, const __grid_constant__ CUtensorMap tm_qt,
-                           const __grid_constant__ CUtensorMap tm_tt, const __grid_constant__ CUtensorMap tm_wt) {
+                           const __grid_constant__ CUtensorMap tm_tt, const __grid_constant__ CUtensorMap tm_wt,
+                           ChunkWindow win) {
   using namespace bst;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   const uint32_t pad = (1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -486,24 +531,28 @@ __global__ void __launch_bounds__(bst::NT, 1)
   if (ws.loc.plan.info[1] == 0) return;
   const int b = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
   const int HV = P.HV, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int first = ws.loc.plan.seq_chunk0[b], last = ws.loc.plan.seq_chunk0[b + 1];
+  const int c0 = ws.loc.plan.seq_chunk0[b], nb = ws.loc.plan.seq_chunk0[b + 1] - c0;
+  const int j0 = win.wc ? win.w * win.wc : 0, j1 = win.wc ? min(nb, j0 + win.wc) : nb;
   const int qd = warp & 3, chalf = warp >> 2;
   const int r = 32 * qd + lane;                 // TMEM lane: key channel (dS) / token (dE, dY)
   const int vc = 32 * chalf;
   const uint32_t lane_addr = static_cast<uint32_t>(32 * qd) << 16;
   const uint32_t sd = tc::smem_u32(data);
   const int64_t sbase = (static_cast<int64_t>(P.slot_idx[b]) * HV + h) * D * D + static_cast<int64_t>(r) * D + v0 + vc;
-  // dS starts as the gradient w.r.t. the final state
-  float Rv[32];
+  float* const carry = ws.carry + (static_cast<int64_t>(b) * HV + h) * D * D + static_cast<int64_t>(r) * D + v0 + vc;
+  if (j0 >= j1) {                               // no chunk here; an empty sequence: dS0 = dS_final
+    if (nb == 0 && A.d_state0)
 #pragma unroll
-  for (int j = 0; j < 32; ++j) Rv[j] = A.d_state ? A.d_state[sbase + j] : 0.f;
-  if (first >= last) {                          // an empty sequence: dS0 = dS_final
-    if (A.d_state0)
-#pragma unroll
-      for (int j = 0; j < 32; ++j) A.d_state0[sbase + j] = Rv[j];
+      for (int j = 0; j < 32; ++j) A.d_state0[sbase + j] = A.d_state ? A.d_state[sbase + j] : 0.f;
     return;
   }
-  auto unit_of = [&](int cidx) { return static_cast<int64_t>(cidx) * HV + h; };
+  const int first = c0 + j0, last = c0 + j1;
+  const int slot0 = win.wc ? b * win.wc - first : 0;
+  // dS starts as the gradient w.r.t. the final state, or what the later window handed on
+  float Rv[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) Rv[j] = j1 < nb ? carry[j] : (A.d_state ? A.d_state[sbase + j] : 0.f);
+  auto unit_of = [&](int cidx) { return static_cast<int64_t>(slot0 + cidx) * HV + h; };
   auto load_a = [&](int cidx) {                 // K_end, A_qk^T, Q~^T of chunk cidx
     const int64_t u = unit_of(cidx);
     tc::mbar_arrive_expect_tx(&ctl->full_a, R_BYTES_A);
@@ -566,12 +615,12 @@ __global__ void __launch_bounds__(bst::NT, 1)
         for (int j = 0; j < 16; ++j) o[j] = 0.f;
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j) *reinterpret_cast<float*>(data + R_OT + kmaj(16 * opart + j, om, 64)) = o[j];
+      for (int j = 0; j < 16; ++j) *reinterpret_cast<float*>(data + R_OT + kmaj(16 * opart + j, om, 64)) = tf32_nearest(o[j]);
       float* gs = ws.dSck + (unit * D + r) * D + v0 + vc;
 #pragma unroll
       for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(gs + j) = make_float4(Rv[j], Rv[j + 1], Rv[j + 2], Rv[j + 3]);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(data + R_RT + kmaj(vc + j, r, 64)) = Rv[j];
+      for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(data + R_RT + kmaj(vc + j, r, 64)) = tf32_nearest(Rv[j]);
     }
     tc::fence_async_smem();
     tc::fence_before_sync();
@@ -616,8 +665,8 @@ __global__ void __launch_bounds__(bst::NT, 1)
       tc::tmem_wait_ld();
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        *reinterpret_cast<uint32_t*>(data + R_ET + kmaj(vc + j, r, 64)) = x0[j] ^ 0x80000000u;
-        *reinterpret_cast<uint32_t*>(data + R_ET + kmaj(vc + 16 + j, r, 64)) = x1[j] ^ 0x80000000u;
+        *reinterpret_cast<float*>(data + R_ET + kmaj(vc + j, r, 64)) = tf32_nearest(-__uint_as_float(x0[j]));
+        *reinterpret_cast<float*>(data + R_ET + kmaj(vc + 16 + j, r, 64)) = tf32_nearest(-__uint_as_float(x1[j]));
       }
     }
     tc::fence_async_smem();
@@ -686,6 +735,9 @@ __global__ void __launch_bounds__(bst::NT, 1)
   }
   if (ctl->bad) {
     if (tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+  } else if (j0 > 0) {                          // handed to the earlier window
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(carry + j) = make_float4(Rv[j], Rv[j + 1], Rv[j + 2], Rv[j + 3]);
   } else if (A.d_state0) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) A.d_state0[sbase + j] = Rv[j];
@@ -697,10 +749,9 @@ __global__ void __launch_bounds__(bst::NT, 1)
 }
 
 cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, bool sbf16,
-                                cudaStream_t st) {
+                                ChunkWindow win, int slots, bool record, cudaStream_t st) {
   using namespace bst;
-  const int mc = plan_max_chunks(P);
-  const uint64_t units = static_cast<uint64_t>(mc > 0 ? mc : 1) * static_cast<uint64_t>(P.HV);
+  const uint64_t units = static_cast<uint64_t>(slots > 0 ? slots : 1) * static_cast<uint64_t>(P.HV);
   alignas(64) CUtensorMap tw, tu, tkt, tke, taq, tqt, ttt, twt;
   if (!ws.loc.KendT || !encode_f32_blocks(&tw, ws.loc.W, units * C, D, D, C) ||
       !encode_f32_blocks(&tu, ws.loc.U, units * C, D, D, C) ||
@@ -719,18 +770,17 @@ cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const 
   e = cudaFuncSetAttribute(bwd_rev_scan_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(R_DATA + 1024));
   if (e != cudaSuccess) return e;
-  fk<<<grid, NT, F_DATA + 1024, st>>>(P, ws, tw, tu, tkt);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_rev_scan_tc_kernel<<<grid, NT, R_DATA + 1024, st>>>(P, ws, A, tke, taq, tqt, ttt, twt);
+  fk<<<grid, NT, F_DATA + 1024, st>>>(P, ws, tw, tu, tkt, win, record ? 1 : 0);
+  if ((e = cudaGetLastError()) != cudaSuccess || !record) return e;
+  bwd_rev_scan_tc_kernel<<<grid, NT, R_DATA + 1024, st>>>(P, ws, A, tke, taq, tqt, ttt, twt, win);
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A,
-                             cudaStream_t st) {
+cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, ChunkWindow win,
+                             int slots, cudaStream_t st) {
   using namespace bvt;
-  const int mc = plan_max_chunks(P);
-  if (mc <= 0) return cudaSuccess;
-  const uint64_t units = static_cast<uint64_t>(mc) * static_cast<uint64_t>(P.HV);
+  if (slots <= 0) return cudaSuccess;
+  const uint64_t units = static_cast<uint64_t>(slots) * static_cast<uint64_t>(P.HV);
   alignas(64) CUtensorMap tdo, tdy, ts, tds, te;
   if (!encode_f32_token_blocks(&tdo, A.d_o, static_cast<uint64_t>(P.T), static_cast<uint64_t>(P.HV), D, C) ||
       !encode_f32_blocks(&tdy, ws.dY, units * C, D, D, C) || !encode_f32_blocks(&ts, ws.Sck, units * D, D, D, D) ||
@@ -739,7 +789,7 @@ cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const Bwd
   cudaError_t e = cudaFuncSetAttribute(bwd_vc_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM));
   if (e != cudaSuccess) return e;
-  bwd_vc_tc_kernel<<<dim3(static_cast<unsigned>(mc), P.HV), NT, SMEM, st>>>(P, ws, A, tdo, tdy, ts, tds, te);
+  bwd_vc_tc_kernel<<<dim3(static_cast<unsigned>(slots), P.HV), NT, SMEM, st>>>(P, ws, A, tdo, tdy, ts, tds, te, win);
   return cudaGetLastError();
 }
 

@@ -87,6 +87,14 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// fp32 rounded to the nearest tf32 (10-bit mantissa, ties away from zero; the low 13 bits
+// zero): what a kind::tf32 MMA operand should hold, since the MMA reads only the top bits
+__device__ __forceinline__ float tf32_nearest(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);

@@ -21,10 +21,13 @@ size_t plan_layout(const Problem& P, char* base, size_t off, PlanView* out) {
 constexpr int kPlanThreads = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem P, PlanView plan, int max_chunks) {
-  __shared__ int s_bad;
+  __shared__ int s_bad, s_longest;
   __shared__ int s_scan[kPlanThreads];
   const int B = P.num_seqs, C = P.chunk, tid = threadIdx.x;
-  if (tid == 0) s_bad = 0;
+  if (tid == 0) {
+    s_bad = 0;
+    s_longest = 0;
+  }
   for (int64_t u = tid; u < static_cast<int64_t>(B) * P.HV; u += kPlanThreads) plan.skip[u] = 0;
   __syncthreads();
   if (tid == 0 && (P.offsets[0] != 0u || static_cast<int64_t>(P.offsets[B]) != P.T)) atomicOr(&s_bad, 1);
@@ -46,14 +49,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem P, PlanView 
                                 : (s_bad & 2) ? KDA_DEVERR_SLOT_RANGE : KDA_DEVERR_SLOT_DUP);
       plan.info[0] = 0;
       plan.info[1] = 0;
+      plan.info[2] = 0;
     }
     return;
   }
   // chunk counts over a contiguous range of sequences per thread, then a block scan
   const int per = (B + kPlanThreads - 1) / kPlanThreads;
   const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
-  int local = 0;
-  for (int b = b0; b < b1; ++b) local += static_cast<int>((P.offsets[b + 1] - P.offsets[b] + C - 1) / C);
+  int local = 0, longest = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int nb = static_cast<int>((P.offsets[b + 1] - P.offsets[b] + C - 1) / C);
+    local += nb;
+    longest = max(longest, nb);
+  }
+  atomicMax(&s_longest, longest);
   s_scan[tid] = local;
   __syncthreads();
   for (int off = 1; off < kPlanThreads; off <<= 1) {
@@ -89,6 +98,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem P, PlanView 
   if (tid == 0) {
     plan.info[0] = total;
     plan.info[1] = 1;
+    plan.info[2] = s_longest;
   }
 }
 

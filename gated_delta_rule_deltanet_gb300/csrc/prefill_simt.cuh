@@ -11,9 +11,9 @@ struct SimtWorkspace {
   PlanView plan;
   float* W;     // [chunk][HV][C][D]
   float* U;     // [chunk][HV][C][D]
-  float* Qt;    // [chunk][HV][C][D]
+  float* Qt;    // [chunk][HV][C][D] (null in the backward's tensor-core path, which takes QtT)
   float* Kend;  // [chunk][HV][C][D]
-  float* Aqk;   // [chunk][HV][C][C]
+  float* Aqk;   // [chunk][HV][C][C] (likewise, AqkT)
   float* gamma; // [chunk][HV][D]
   float* T;     // [chunk][HV][C][C] (I + A_kk)^-1, or null (kept only by the backward pass)
   float* Kt;    // [chunk][HV][C][D] K~ = k^ exp(G), or null (likewise)
@@ -87,7 +87,9 @@ constexpr float kSimtAnchorRange = 80.f;
 // Every thread owns tiles of rows r0 .. r0 + C/16 - 1 (r0 = (t / 16) C/16): of a C x C
 // product the columns (t % 16) C/16 + b, of a C x D product the columns (t % 16) D/16 + b.
 template <int D, int C, bool QBF16, bool PERCH>
-__global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspace ws) {
+// win: the chunks of one window of positions (the backward's bounded workspace), each in the
+// workspace slot of its window; {0, 0} for every chunk in its own slot.
+__global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspace ws, ChunkWindow win) {
   constexpr int NT = 256;
   constexpr int DP = SimtLocalSmem<D, C>::DP;
   constexpr int CP = SimtLocalSmem<D, C>::CP;
@@ -108,8 +110,9 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
   float* s_gl = s_ga + D;         // [D] G_last, then exp(G_last - G_a)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (ws.plan.info[1] == 0 || static_cast<int>(blockIdx.x) >= ws.plan.info[0]) return;
-  const ChunkInfo ci = ws.plan.chunks[blockIdx.x];
+  int gc;
+  if (ws.plan.info[1] == 0 || !window_chunk(ws.plan, P.num_seqs, win, blockIdx.x, &gc)) return;
+  const ChunkInfo ci = ws.plan.chunks[gc];
   const int h = blockIdx.y;
   const int HV = P.HV;
   const int kh = h / (HV / P.HK);
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
   float* gW = ws.W + unit * C * D;
   float* gU = ws.U + unit * C * D;
-  float* gQ = ws.Qt + unit * C * D;
+  float* gQ = ws.Qt ? ws.Qt + unit * C * D : nullptr;
   float* gK = ws.Kend + unit * C * D;
   if (PERCH && anchored) {
     for (int c = tid; c < D; c += NT) {
@@ -353,29 +356,31 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
         ke[b] = s_k[i * DP + c] * expf(Gl - Gi);
       }
     }
-    st_row(gQ + i * D + c0, qt);
-    st_row(gK + i * D + c0, ke);
+    if (gQ) st_row(gQ + i * D + c0, qt);
     if (ws.Kt) st_row(ws.Kt + unit * C * D + i * D + c0, kt);
-    if (ws.KendT) {
+    if (ws.KendT) {                             // the backward's tf32 operands, rounded to nearest
 #pragma unroll
       for (int b = 0; b < JC; ++b) {
+        ke[b] = tf32_nearest(ke[b]);
         ws.KendT[(unit * D + c0 + b) * C + i] = ke[b];
-        ws.QtT[(unit * D + c0 + b) * C + i] = qt[b];
+        ws.QtT[(unit * D + c0 + b) * C + i] = tf32_nearest(qt[b]);
       }
     }
+    st_row(gK + i * D + c0, ke);
 #pragma unroll
     for (int b = 0; b < JC; ++b) {
       s_q[i * DP + c0 + b] = delta ? bi * kt[b] : 0.f;
       s_v[i * DP + c0 + b] *= bi;
     }
   }
-  for (int idx = tid; idx < C * C; idx += NT) ws.Aqk[unit * C * C + idx] = s_Aq[(idx / C) * CP + idx % C];
+  if (ws.Aqk)
+    for (int idx = tid; idx < C * C; idx += NT) ws.Aqk[unit * C * C + idx] = s_Aq[(idx / C) * CP + idx % C];
   if (ws.T)
     for (int idx = tid; idx < C * C; idx += NT) ws.T[unit * C * C + idx] = s_T[(idx / C) * CP + idx % C];
   if (ws.TT)
     for (int idx = tid; idx < C * C; idx += NT) {
-      ws.TT[unit * C * C + idx] = s_T[(idx % C) * CP + idx / C];
-      ws.AqkT[unit * C * C + idx] = s_Aq[(idx % C) * CP + idx / C];
+      ws.TT[unit * C * C + idx] = tf32_nearest(s_T[(idx % C) * CP + idx / C]);
+      ws.AqkT[unit * C * C + idx] = tf32_nearest(s_Aq[(idx % C) * CP + idx / C]);
     }
   __syncthreads();
   // W = T (beta k exp(G)),  U = T (beta v)
@@ -398,12 +403,11 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
       }
     }
   }
+  if (ws.WT) {                                  // the backward's tf32 operands, rounded to nearest
 #pragma unroll
-  for (int a = 0; a < RT; ++a) {
-    st_row(gW + (r0 + a) * D + c0, w[a]);
-    st_row(gU + (r0 + a) * D + c0, uu[a]);
-  }
-  if (ws.WT) {
+    for (int a = 0; a < RT; ++a)
+#pragma unroll
+      for (int b = 0; b < JC; ++b) w[a][b] = tf32_nearest(w[a][b]);
 #pragma unroll
     for (int b = 0; b < JC; ++b) {
       float col[RT];
@@ -411,6 +415,11 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
       for (int a = 0; a < RT; ++a) col[a] = w[a][b];
       st_row(ws.WT + (unit * D + c0 + b) * C + r0, col);
     }
+  }
+#pragma unroll
+  for (int a = 0; a < RT; ++a) {
+    st_row(gW + (r0 + a) * D + c0, w[a]);
+    st_row(gU + (r0 + a) * D + c0, uu[a]);
   }
 }
 

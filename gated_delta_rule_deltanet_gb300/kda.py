@@ -210,17 +210,20 @@ def prefill_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, beta: torch.T
                 log_decay: torch.Tensor, input_row_offsets: torch.Tensor, slot_idx: torch.Tensor,
                 state_pool: torch.Tensor, d_o: torch.Tensor, d_state: Optional[torch.Tensor] = None,
                 *, chunk: int = 64, scale: float = 0.0, l2norm: bool = True,
-                delta_rule: bool = True, checked: bool = False,
+                delta_rule: bool = True, checked: bool = False, compact: bool = False,
                 d_state0: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
                 stream: Optional[torch.cuda.Stream] = None):
     """Backward of `prefill` (kda_prefill_bwd).  `state_pool` holds the INITIAL states (the
     pool before the forward call) and is only read; `d_o` [T, HV, D] and `d_state` (pool-shaped
     fp32, or None for zero) are the loss's gradients w.r.t. o and the final states.
+    `compact` (KDA_FLAG_COMPACT; bf16 q/k/v, d = 128, chunk 64) bounds the workspace: windows of
+    chunk positions with a checkpointed state per window, at the cost of rerunning the forward
+    recurrence and one stream synchronisation.
     Returns (dq, dk [T, HK, D], dv [T, HV, D], dbeta [T, HV], dlog_decay (shape of log_decay),
     d_state0 (pool-shaped fp32: the touched slots' gradients, zero elsewhere unless given))."""
     dev = _check_cuda(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, d_o)
     p = _prefill_params(q, k, v, beta, log_decay, input_row_offsets, slot_idx, state_pool, chunk,
-                        scale, l2norm, checked, delta_rule=delta_rule)
+                        scale, l2norm, checked, compact=compact, delta_rule=delta_rule)
     T, HK, D = q.shape
     HV = v.shape[1]
     if d_o.dtype != torch.float32 or tuple(d_o.shape) != (T, HV, D) or not d_o.is_contiguous():

@@ -93,7 +93,8 @@ typedef enum kda_decay_kind {
  * (57,856 bytes per chunk and value head) and a sequential one over each
  * sequence's chunks, which keeps the chunk-local work off the sequential path.
  * The two forms round the same operands the same way; their results agree to
- * the tolerance, not bit for bit. */
+ * the tolerance, not bit for bit.  In kda_prefill_bwd the flag bounds the
+ * workspace instead (see there). */
 #define KDA_FLAG_COMPACT 4u
 /* Additive write in place of the delta rule: the correction subtracts no
  * prediction, e_t = beta_t v_t, so S_t = Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
@@ -237,10 +238,12 @@ kda_status_t kda_conv_gates_fwd(const kda_params_t *p, int32_t width, const void
  * differentiated by the chain rule: the state gradient runs as a reverse scan
  * over each sequence's chunks (the transpose of the forward's state recursion),
  * the rest chunk-parallel; the L2 normalisation of q and k and the query scale
- * are differentiated too.  fp32 arithmetic on CUDA cores for every dtype, head
- * size and chunk the forward accepts ("From Attention to Learned Memory", sec. 3,
- * gives the linear-attention backward in full; the delta rule's follows the same
- * recurrence).
+ * are differentiated too ("From Attention to Learned Memory", sec. 3, gives the
+ * linear-attention backward in full; the delta rule's follows the same recurrence).
+ * fp32 arithmetic throughout; with bf16 q/k/v at d = 128 and chunk 64 the scan's
+ * two directions and the contractions over the value dimension run on tensor
+ * cores with tf32 operands (10-bit mantissa, fp32 range) and fp32 accumulation,
+ * everything else on CUDA cores.
  *
  *   q, k, v, beta, log_decay, input_row_offsets, slot_idx: as kda_prefill_fwd
  *   state_pool  [num_slots, HV, d_k, d_v], state_dtype, read only: the INITIAL
@@ -256,8 +259,23 @@ kda_status_t kda_conv_gates_fwd(const kda_params_t *p, int32_t width, const void
  *   workspace   >= kda_prefill_bwd_workspace_size bytes, 256-byte aligned
  * q, k, v 16-byte aligned with 16-byte aligned rows (as for the forward), every
  * other array 4-byte aligned.  KDA_FLAG_NO_DELTA differentiates the additive
- * write; KDA_FLAG_CUDA_CORES and KDA_FLAG_COMPACT are ignored.  Device-side
- * checks (offsets, slots) set the error word and skip the work, as in the forward.
+ * write; KDA_FLAG_CUDA_CORES is ignored.  Device-side checks (offsets, slots) set
+ * the error word and skip the work, as in the forward.
+ *
+ * Workspace.  By default it holds every chunk's per-(chunk, value head) matrices,
+ * about 0.6 MB per chunk and value head (9.3 GB for 2 x 16384 tokens, 32 heads).
+ * KDA_FLAG_COMPACT (bf16 q/k/v, d = 128, chunk 64; ignored elsewhere) bounds it:
+ * the chunks run in windows of wc chunk positions per sequence,
+ * wc = max(1, 512 / (num_seqs * HV)), so the per-chunk matrices exist for
+ * max(512, num_seqs * HV) (chunk, value head) slots, plus the state entering
+ * every window after a sequence's first (64 KB per window and value head at
+ * d = 128) and one state gradient per (sequence, value head): 421 MiB for
+ * 2 x 16384 tokens, 32 heads.  A forward sweep over the windows stores those
+ * entering states; the backward sweep then reruns each window's chunk-local stage
+ * and forward scan from its checkpoint, latest window first, with the same
+ * arithmetic per chunk, so the gradients equal the default form's bit for bit.
+ * The call reads the longest sequence's chunk count back to the host once (a
+ * synchronisation of `stream`) to size the sweeps.
  */
 kda_status_t kda_prefill_bwd_workspace_size(const kda_params_t *p, size_t *bytes);
 kda_status_t kda_prefill_bwd(const kda_params_t *p, const void *q, const void *k, const void *v,

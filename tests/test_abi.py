@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from gated_delta_rule_deltanet_gb300 import _lib, build as kbuild
 from gated_delta_rule_deltanet_gb300.kda import make_params
@@ -298,3 +299,30 @@ def test_conv_front_end_rejects_bad_arguments_before_launch(lib):
         _lib.KDA_ERR_INVALID_ARG
     empty = good(total_tokens=0, num_seqs=0)
     assert lib.kda_conv_gates_fwd(ctypes.byref(empty), 4, *([None] * 13), None) == _lib.KDA_OK
+
+
+def test_backward_compact_workspace_is_bounded(lib):
+    """KDA_FLAG_COMPACT bounds the backward's workspace on the tensor-core configuration:
+    windows of chunk positions (512 (chunk, value head) slots) plus one checkpointed state per
+    window and sequence.  On the kda_prefill shapes (2 x 16384 tokens, 32 heads, d = 128) it
+    stays under 0.5 GiB, against several GB for the default form."""
+    def size(**kw):
+        n = ctypes.c_size_t(0)
+        p = make_params(num_seqs=2, num_k_heads=32, num_v_heads=32, d=128, num_slots=2,
+                            total_tokens=32768, **kw)
+        assert lib.kda_prefill_bwd_workspace_size(ctypes.byref(p), ctypes.byref(n)) == _lib.KDA_OK
+        return n.value
+    default, compact = size(), size(compact=True)
+    assert compact <= 512 * 2 ** 20 < 4 * 2 ** 30 < default
+    # the bound does not grow with the sequence length, apart from the checkpoints (64 KB per
+    # window of 8 chunks and head)
+    n = ctypes.c_size_t(0)
+    p4 = make_params(num_seqs=2, num_k_heads=32, num_v_heads=32, d=128, num_slots=2,
+                         total_tokens=4 * 32768, compact=True)
+    assert lib.kda_prefill_bwd_workspace_size(ctypes.byref(p4), ctypes.byref(n)) == _lib.KDA_OK
+    assert n.value - compact <= 3 * 32768 // 64 // 8 * 32 * 128 * 128 * 4 + 2 ** 20
+    # fp32 inputs run on CUDA cores, where the flag does not apply
+    f32 = make_params(num_seqs=2, num_k_heads=32, num_v_heads=32, d=128, num_slots=2,
+                          total_tokens=32768, qkv_dtype=torch.float32, compact=True)
+    assert lib.kda_prefill_bwd_workspace_size(ctypes.byref(f32), ctypes.byref(n)) == _lib.KDA_OK
+    assert n.value > 4 * 2 ** 30

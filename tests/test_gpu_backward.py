@@ -163,3 +163,72 @@ def test_backward_ragged_gqa_workload_sampled():
         rows = {"dq": (slice(s, e), kh), "dk": (slice(s, e), kh), "dv": (slice(s, e), hs),
                 "dbeta": (slice(s, e), hs), "dg": (slice(s, e), hs), "d_state0": (slot, hs)}
         compare(got, ref, TOL[p.qkv_dtype], rows=rows, label=f"ragged_gqa_kda seq {b}")
+
+
+def same_as_default(full, comp):
+    for k in full:
+        if k == "dg":     # shared-memory atomics sum a chunk's last-token terms in any order
+            assert rel_err(comp[k], full[k]) < 1e-5, k
+        else:
+            assert np.array_equal(full[k], comp[k]), k
+
+
+COMPACT_CASES = [
+    # name, lengths, HK, HV, decay, state dtype: 4 x 64 value heads give windows of two chunk
+    # positions (512 slots), so the longest sequence (5 chunks) runs three windows
+    ("compact-kda-gqa", [300, 0, 1, 190], 32, 64, "per_channel", "f32"),
+    ("compact-gdn-bf16pool", [129, 64, 257, 2], 64, 64, "scalar", "bf16"),
+]
+
+
+@pytest.mark.parametrize("cfg", COMPACT_CASES, ids=[c[0] for c in COMPACT_CASES])
+def test_backward_compact_equals_default(cfg):
+    """The bounded-workspace form (KDA_FLAG_COMPACT: windows of chunk positions, each window's
+    entering state from a checkpoint sweep, the state gradient carried between windows) runs
+    the same arithmetic per chunk, so every gradient equals the default form's bit for bit
+    (dg up to the order of the pair kernel's shared-memory atomic sums over a chunk's
+    channels, which no two runs fix); sampled (sequence, head) pairs also match the oracle."""
+    name, lengths, HK, HV, decay, state = cfg
+    p = workloads.make_problem(name, num_seqs=len(lengths), lengths=lengths, num_k_heads=HK,
+                               num_v_heads=HV, d=128, qkv_dtype="bf16", state_dtype=state,
+                               decay_kind=decay, chunk=64, zero_state=False,
+                               num_slots=len(lengths) + 1, seed=sum(map(ord, name)))
+    d_o, d_state = seeds(p, 13)
+    full = gpu_backward(p, d_o, d_state)
+    comp = gpu_backward(p, d_o, d_state, compact=True)
+    same_as_default(full, comp)
+    # every value head of the sampled key heads, so that dq and dk are complete
+    ratio = HV // HK
+    pairs = [(b, kh * ratio + r) for b, kh in ((0, 0), (3, HK - 1), (2, HK // 2))
+             for r in range(ratio)]
+    ref = oracle.backward(p, d_o.astype(np.float64), d_state.astype(np.float64), pairs=pairs)
+    offs = p.offsets.astype(np.int64)
+    # norm-wise over the sample (the bound's reading): each gradient's sampled rows together
+    got_s, ref_s = {}, {}
+    for n in ("dq", "dk", "dv", "dbeta", "dg", "d_state0"):
+        sel = []
+        for b, h in pairs:
+            s, e = offs[b], offs[b + 1]
+            sel.append((int(p.slot_idx[b]), h) if n == "d_state0"
+                       else (slice(s, e), h // ratio if n in ("dq", "dk") else h))
+        got_s[n] = np.concatenate([np.ravel(comp[n][r]) for r in sel])
+        ref_s[n] = np.concatenate([np.ravel(ref[n][r]) for r in sel])
+    compare(got_s, ref_s, TOL["bf16"], label=f"{name} pairs {pairs}")
+
+
+def test_backward_compact_full_size_kda_prefill():
+    """kda_prefill (2 x 16384 tokens, 32 heads, per-channel decay) in the bounded workspace
+    (32 windows of 8 chunk positions): equal to the default form, and a sampled pair against
+    the oracle."""
+    p = workloads.workload("kda_prefill")
+    d_o, d_state = seeds(p, 14)
+    comp = gpu_backward(p, d_o, d_state, compact=True)
+    full = gpu_backward(p, d_o, d_state)
+    same_as_default(full, comp)
+    b, h = 0, 5
+    ref = oracle.backward(p, d_o.astype(np.float64), d_state.astype(np.float64), pairs=[(b, h)])
+    offs = p.offsets.astype(np.int64)
+    s, e = offs[b], offs[b + 1]
+    rows = {n: (slice(s, e), h) for n in ("dq", "dk", "dv", "dbeta", "dg")}
+    rows["d_state0"] = (int(p.slot_idx[b]), h)
+    compare(comp, ref, TOL["bf16"], rows=rows, label="kda_prefill compact")

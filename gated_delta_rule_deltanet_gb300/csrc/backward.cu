@@ -514,11 +514,6 @@ struct BwdPairSmem {
   static constexpr size_t bytes = floats * sizeof(float);
 };
 
-__device__ __forceinline__ float halfwarp_sum(float v) {
-#pragma unroll
-  for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
 
 template <int D, int C, bool QBF16, bool PERCH>
 __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace ws, BwdArgs A, ChunkWindow win) {
@@ -864,6 +859,7 @@ static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const 
       r = cudaGetLastError();
     }
     if (r != cudaSuccess) return r;
+    if (kTc && !PERCH) return launch_bwd_pair_tc(P, ws, A, win, slots, st);   // scalar decay
     pk<<<dim3(slots, P.HK), 256, BwdPairSmem<D, C, PERCH>::bytes, st>>>(P, ws, A, win);
     return cudaGetLastError();
   };

@@ -57,6 +57,11 @@ cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const Bwd
 cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, bool sbf16,
                                 ChunkWindow win, int slots, bool record, cudaStream_t st);
 
+// The pairwise terms, dg, dbeta, dq and dk on tensor cores for scalar decay (d = 128, chunk
+// 64, bf16 q/k), as bwd_pair_kernel computes them.
+cudaError_t launch_bwd_pair_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, ChunkWindow win,
+                               int slots, cudaStream_t st);
+
 // index of the checkpoint of window w >= 1 of the sequence whose first chunk is c0
 __host__ __device__ __forceinline__ int64_t ckpt_entry(int c0, ChunkWindow win) {
   return static_cast<int64_t>(c0 / win.wc) + win.w - 1;

@@ -776,6 +776,327 @@ cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const 
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------- pairwise terms
+//
+// Scalar decay: the pairwise decay exp(G_i - G_m) folds into dM and dA once per chunk
+// (dM', dA'), and the three products the chain rule needs through A_qk = (Q^ K^T) o X and
+// A_kk = diag(beta) (K^ K^T) o X are plain contractions over the chunk's tokens:
+//
+//   [dM'; dA'] K^           rows 0-63: P1 = dM' K^,  rows 64-127: P2 = dA' K^
+//   [dM'^T | (b dA')^T] [Q^; K^]   P3 = dM'^T Q^ + (diag(beta) dA')^T K^
+//
+// on tensor cores (kind::tf32, K-major operands written by the threads: dM' and dA' as
+// stored and transposed, Q^ and K^ transposed), staged to shared memory, then the same
+// elementwise chain rule as bwd_pair_kernel: dq^, dk^, the rows of dG (whose reverse
+// cumulative sum is dg), dbeta's pairwise part, and after the value heads of the key head
+// the L2 normalisation's backward.
+
+namespace bpt {
+
+constexpr int C = 64, D = 128, NT = 256, DP = D + 4;
+constexpr uint32_t Q_OFF = 0, K_OFF = C * DP * 4;                  // q^, k^ rows, fp32
+constexpr uint32_t OPS = 2 * C * DP * 4;                           // 67584, 1024-aligned
+constexpr uint32_t A12 = OPS;                                      // 2 blocks of 128 rows
+constexpr uint32_t A3 = A12 + 32768;                               // 4 blocks of 64 rows
+constexpr uint32_t BQ = A3 + 40960;                                // Q^T 2 blocks, then K^T 2
+constexpr uint32_t BK = BQ + 32768;
+constexpr uint32_t DATA = BK + 32768;                              // 206848
+constexpr uint32_t SMALL = DATA;                                   // per-token and per-channel
+constexpr uint32_t SMEM = DATA + 4096 + 1024;
+constexpr int SP = DP;                                             // staging rows of P1-P3
+constexpr uint32_t kWaitLimit = 1u << 22;
+static_assert(3 * C * SP * 4 <= DATA - OPS, "P1-P3 staging fits the operand region");
+static_assert(SMEM <= 227 * 1024, "shared memory budget");
+static_assert(OPS % 1024 == 0, "operand alignment");
+
+struct Ctrl {
+  uint64_t bar;
+  uint32_t tmem;
+  int bad;
+};
+
+}  // namespace bpt
+
+__global__ void __launch_bounds__(bpt::NT, 1)
+    bwd_pair_tc_kernel(Problem P, BwdWorkspace ws, BwdArgs A, ChunkWindow win) {
+  using namespace bpt;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t pad = (1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* const data = smem_raw + pad;
+  float* const s_q = reinterpret_cast<float*>(data + Q_OFF);
+  float* const s_k = reinterpret_cast<float*>(data + K_OFF);
+  float* const s_G = reinterpret_cast<float*>(data + SMALL);       // [C] cumulative log-decay
+  float* const s_b = s_G + C;                                      // [C] beta
+  float* const s_rq = s_b + C;                                     // [C] 1/|q|
+  float* const s_rk = s_rq + C;                                    // [C] 1/|k|
+  float* const s_db = s_rk + C;                                    // [C] dbeta's pairwise part
+  float* const s_dot = s_db + C;                                   // [C] row sums of dG
+  float* const s_dGl = s_dot + C;                                  // [D] gradient w.r.t. G_last
+  Ctrl* const ctl = reinterpret_cast<Ctrl*>(s_dGl + D);
+  constexpr int IR = C / 16, JC = D / 16;
+
+  int gc;
+  if (ws.loc.plan.info[1] == 0 || !window_chunk(ws.loc.plan, P.num_seqs, win, blockIdx.x, &gc)) return;
+  const ChunkInfo ci = ws.loc.plan.chunks[gc];
+  const int kh = blockIdx.y, HV = P.HV, ratio = HV / P.HK, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
+  const int n = ci.n;
+  const int r0 = (tid / 16) * IR, c0 = (tid % 16) * JC;
+  const bool lead = (tid % 16) == 0;
+  const uint32_t sd = tc::smem_u32(data);
+
+  if (tid == 0) {
+    tc::mbar_init(&ctl->bar, 1);
+    ctl->bad = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&ctl->tmem, 256);
+    tc::tmem_relinquish();
+  }
+  for (int u = tid; u < C * (D / 8); u += NT) {    // q, k rows of the key head (bf16)
+    const int i = u / (D / 8), c = (u % (D / 8)) * 8;
+    float qx[8] = {}, kx[8] = {};
+    if (i < n) {
+      tc::bf16x8_load(reinterpret_cast<const unsigned char*>(
+                          static_cast<const uint16_t*>(P.q) + (ci.t0 + i) * P.q_stride + static_cast<int64_t>(kh) * D + c), qx);
+      tc::bf16x8_load(reinterpret_cast<const unsigned char*>(
+                          static_cast<const uint16_t*>(P.k) + (ci.t0 + i) * P.k_stride + static_cast<int64_t>(kh) * D + c), kx);
+    }
+    *reinterpret_cast<float4*>(s_q + i * DP + c) = make_float4(qx[0], qx[1], qx[2], qx[3]);
+    *reinterpret_cast<float4*>(s_q + i * DP + c + 4) = make_float4(qx[4], qx[5], qx[6], qx[7]);
+    *reinterpret_cast<float4*>(s_k + i * DP + c) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+    *reinterpret_cast<float4*>(s_k + i * DP + c + 4) = make_float4(kx[4], kx[5], kx[6], kx[7]);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = ctl->tmem;
+  for (int i = warp; i < C; i += NT / 32) {
+    float sq = 0.f, sk = 0.f;
+    for (int c = lane; c < D; c += 32) {
+      sq += s_q[i * DP + c] * s_q[i * DP + c];
+      sk += s_k[i * DP + c] * s_k[i * DP + c];
+    }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    if (lane == 0) {
+      s_rq[i] = P.l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
+      s_rk[i] = P.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < C * D; idx += NT) {
+    const int i = idx / D, c = idx % D;
+    s_q[i * DP + c] *= s_rq[i] * P.scale;
+    s_k[i * DP + c] *= s_rk[i];
+  }
+
+  float adq[IR][JC], adk[IR][JC];
+#pragma unroll
+  for (int a = 0; a < IR; ++a)
+#pragma unroll
+    for (int b = 0; b < JC; ++b) adq[a][b] = adk[a][b] = 0.f;
+  const uint32_t id = tc::idesc_f16(128, 128, tc::kTF32);
+
+  for (int h = kh * ratio, it = 0; h < (kh + 1) * ratio; ++h, ++it) {
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
+    __syncthreads();                            // the previous head's staging is read
+    if (tid == 0) {
+      float acc = 0.f;
+      for (int i = 0; i < C; ++i) {
+        acc += i < n ? P.g[(ci.t0 + i) * HV + h] : 0.f;
+        s_G[i] = acc;
+      }
+    }
+    for (int i = tid; i < C; i += NT) s_b[i] = i < n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
+    for (int c = tid; c < D; c += NT) s_dGl[c] = 0.f;
+    // Q^T and K^T (key channel rows, token columns)
+    for (int idx = tid; idx < C * D; idx += NT) {
+      const int c = idx % D, m = idx / D;
+      const uint32_t off = (m >> 5) * 16384 + tc::sw128_offset(c, (m & 31) >> 2) + (m & 3) * 4;
+      *reinterpret_cast<float*>(data + BQ + off) = tf32_nearest(s_q[m * DP + c]);
+      *reinterpret_cast<float*>(data + BK + off) = tf32_nearest(s_k[m * DP + c]);
+    }
+    __syncthreads();                            // G and beta are in
+    // dM' and dA' (decay folded), as stored for [dM'; dA'] and transposed for P3
+    for (int idx = tid; idx < C * C; idx += NT) {
+      const int i = idx / C, m = idx % C;
+      const float x = m <= i ? expf(s_G[i] - s_G[m]) : 0.f;
+      const float dm = ws.dM[unit * C * C + idx] * x, da = ws.dA[unit * C * C + idx] * x;
+      const uint32_t cm = (m & 31) >> 2, wm = (m & 3) * 4, ci2 = (i & 31) >> 2, wi = (i & 3) * 4;
+      *reinterpret_cast<float*>(data + A12 + (m >> 5) * 16384 + tc::sw128_offset(i, cm) + wm) = tf32_nearest(dm);
+      *reinterpret_cast<float*>(data + A12 + (m >> 5) * 16384 + tc::sw128_offset(C + i, cm) + wm) = tf32_nearest(da);
+      *reinterpret_cast<float*>(data + A3 + (i >> 5) * 8192 + tc::sw128_offset(m, ci2) + wi) = tf32_nearest(dm);
+      *reinterpret_cast<float*>(data + A3 + (2 + (i >> 5)) * 8192 + tc::sw128_offset(m, ci2) + wi) =
+          tf32_nearest(delta ? s_b[i] * da : 0.f);
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {             // [dM'; dA'] K^: K = tokens m
+        const uint64_t da = tc::smem_desc_sw128(sd + A12 + j * 16384, 1024);
+        const uint64_t db = tc::smem_desc_sw128(sd + BK + j * 16384, 1024);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_ss_tf32(tmem, tc::desc_add(da, 32 * k), tc::desc_add(db, 32 * k), id, (j | k) ? 1u : 0u);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {             // [dM'^T | (b dA')^T] [Q^; K^]: K = 2 x tokens
+        const uint64_t da = tc::smem_desc_sw128(sd + A3 + j * 8192, 1024);
+        const uint64_t db = tc::smem_desc_sw128(sd + BQ + j * 16384, 1024);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_ss_tf32(tmem + 128, tc::desc_add(da, 32 * k), tc::desc_add(db, 32 * k), id, (j | k) ? 1u : 0u);
+      }
+      tc::mma_commit(&ctl->bar);
+    }
+    if (!tc::mbar_wait_bounded(&ctl->bar, static_cast<uint32_t>(it) & 1u, kWaitLimit)) ctl->bad = 1;
+    tc::fence_after_sync();
+    // stage P1, P2, P3 as rows of SP floats over the operands
+    float* const s_P1 = reinterpret_cast<float*>(data + OPS);
+    float* const s_P2 = s_P1 + C * SP;
+    float* const s_P3 = s_P2 + C * SP;
+    __syncthreads();                            // the operands are read by the MMAs only
+    {
+      const int qd = warp & 3, ch = warp >> 2;
+      const int row = 32 * qd + lane;
+      const uint32_t la = static_cast<uint32_t>(32 * qd) << 16;
+      float* dst12 = row < C ? s_P1 + row * SP : s_P2 + (row - C) * SP;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        uint32_t v[16];
+        tc::tmem_ld16(tmem + la + 64 * ch + 16 * jj, v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4*>(dst12 + 64 * ch + 16 * jj + e) =
+              make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+      }
+      if (qd < 2) {
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          uint32_t v[16];
+          tc::tmem_ld16(tmem + la + 128 + 64 * ch + 16 * jj, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(s_P3 + row * SP + 64 * ch + 16 * jj + e) =
+                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+        }
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    {
+      const float Gl = s_G[C - 1], gam = expf(Gl);
+      float gl[JC];
+#pragma unroll
+      for (int b = 0; b < JC; ++b) gl[b] = 0.f;
+#pragma unroll
+      for (int a = 0; a < IR; ++a) {
+        const int i = r0 + a;
+        float dqt[JC], dkt[JC], dke[JC], p1[JC], p2[JC], p3[JC], qv[JC], kv[JC];
+        ld_row(dqt, ws.dQt + unit * C * D + i * D + c0);
+        ld_row(dkt, ws.dKt + unit * C * D + i * D + c0);
+        ld_row(dke, ws.dKe + unit * C * D + i * D + c0);
+        ld_row(p1, s_P1 + i * SP + c0);
+        ld_row(p2, s_P2 + i * SP + c0);
+        ld_row(p3, s_P3 + i * SP + c0);
+        ld_row(qv, s_q + i * DP + c0);
+        ld_row(kv, s_k + i * DP + c0);
+        const float bi = s_b[i], Gi = s_G[i];
+        const float eG = expf(Gi), eL = expf(Gl - Gi);
+        float bl = 0.f, rsum = 0.f;
+#pragma unroll
+        for (int b = 0; b < JC; ++b) {
+          adq[a][b] += p1[b] + dqt[b] * eG;
+          adk[a][b] += bi * p2[b] + p3[b] + dkt[b] * eG + dke[b] * eL;
+          rsum += qv[b] * p1[b] + kv[b] * bi * p2[b] - kv[b] * p3[b] + dqt[b] * qv[b] * eG +
+                  dkt[b] * kv[b] * eG - dke[b] * kv[b] * eL;
+          bl += kv[b] * p2[b];                  // dbeta's pairwise part: sum_c k^_ic P2_ic
+          gl[b] += dke[b] * kv[b] * eL;         // K_end's path into G_last
+        }
+        bl = halfwarp_sum(bl);
+        rsum = halfwarp_sum(rsum);
+        if (lead) {
+          s_db[i] = bl;
+          s_dot[i] = rsum;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < JC; ++b) atomicAdd(&s_dGl[c0 + b], gl[b]);
+      __syncthreads();
+      if (warp == 0) {                          // G_last's terms join the last row
+        float v = 0.f;
+        for (int c = lane; c < D; c += 32) v += s_dGl[c] + ws.dgam[unit * D + c] * gam;
+        v = warp_sum(v);
+        if (lane == 0) s_dot[C - 1] += v;
+      }
+      __syncthreads();
+      if (tid == 0) {                           // dg = reverse cumulative sum of the rows
+        float acc = 0.f;
+        for (int i = C - 1; i >= 0; --i) {
+          acc += s_dot[i];
+          if (i < n) A.dg[(ci.t0 + i) * HV + h] = acc;
+        }
+      }
+      for (int i = tid; i < n; i += NT)
+        A.dbeta[(ci.t0 + i) * HV + h] = ws.dbr[unit * C + i] + (delta ? s_db[i] : 0.f);
+    }
+  }
+  // the L2 normalisation's backward: with u = x / |x|, dx = (du - u (u . du)) / |x|
+  const float inv_s = 1.f / P.scale;
+#pragma unroll
+  for (int a = 0; a < IR; ++a) {
+    const int i = r0 + a;
+    float dq = 0.f, dk = 0.f;
+#pragma unroll
+    for (int b = 0; b < JC; ++b) {
+      dq += s_q[i * DP + c0 + b] * adq[a][b];
+      dk += s_k[i * DP + c0 + b] * adk[a][b];
+    }
+    dq = halfwarp_sum(dq);
+    dk = halfwarp_sum(dk);
+    if (i >= n) continue;
+    float oq[JC], ok[JC];
+#pragma unroll
+    for (int b = 0; b < JC; ++b) {
+      if (P.l2norm) {
+        const float uq = s_q[i * DP + c0 + b] * inv_s;
+        oq[b] = P.scale * s_rq[i] * (adq[a][b] - uq * dq * inv_s);
+        ok[b] = s_rk[i] * (adk[a][b] - s_k[i * DP + c0 + b] * dk);
+      } else {
+        oq[b] = P.scale * adq[a][b];
+        ok[b] = adk[a][b];
+      }
+    }
+    const int64_t o = ((ci.t0 + i) * P.HK + kh) * D + c0;
+    st_row(A.dq + o, oq);
+    st_row(A.dk + o, ok);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (ctl->bad && tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+cudaError_t launch_bwd_pair_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, ChunkWindow win,
+                               int slots, cudaStream_t st) {
+  using namespace bpt;
+  if (slots <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(bwd_pair_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM));
+  if (e != cudaSuccess) return e;
+  bwd_pair_tc_kernel<<<dim3(static_cast<unsigned>(slots), P.HK), NT, SMEM, st>>>(P, ws, A, win);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, ChunkWindow win,
                              int slots, cudaStream_t st) {
   using namespace bvt;

@@ -95,6 +95,13 @@ __device__ __forceinline__ float tf32_nearest(float x) {
   return __uint_as_float(r);
 }
 
+// sum over the 16 lanes of each half-warp
+__device__ __forceinline__ float halfwarp_sum(float v) {
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);

@@ -802,7 +802,8 @@ def profile_arm(args):
     elif args.profile == "decode":
         ms = time_decode(workloads.workload("kda_decode"), dev, args.steps, args.warmup)
     elif args.profile == "backward":
-        ms = time_prefill_bwd(workloads.workload(args.workload), dev, args.steps, args.warmup)[0]
+        ms = time_prefill_bwd(workloads.workload(args.workload), dev, args.steps, args.warmup,
+                              compact=args.compact)[0]
     else:
         ms = time_verify(dev, args.steps, args.warmup)[1]
     print(f"profile {args.profile}: {args.warmup} + {args.steps} steps, {ms:.4f} ms per step")
@@ -818,6 +819,8 @@ def main(argv=None):
                     choices=[w for w in workloads.WORKLOADS if w != "kda_decode"])
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--compact", action="store_true",
+                    help="with --profile backward: the bounded-workspace form")
     ap.add_argument("--profile", choices=["prefill", "decode", "verify", "backward"],
                     help="run W + K steps of one piece for a profiler, print no JSON line")
     args = ap.parse_args(argv)

@@ -405,6 +405,7 @@ __global__ void __launch_bounds__(bst::NT, 1)
   for (int cidx = first; cidx < last; ++cidx) {
     const uint32_t par = static_cast<uint32_t>(cidx - first) & 1u;
     const int64_t unit = unit_of(cidx);
+    const float gm = __ldg(ws.loc.gamma + unit * D + r);   // read at the update, issued now
     // S entering the chunk: into the workspace, and transposed as the B operand of W S
     {
       if (record) {
@@ -493,7 +494,6 @@ __global__ void __launch_bounds__(bst::NT, 1)
       tc::tmem_ld16(tmem + lane_addr + T_D + vc, d0);
       tc::tmem_ld16(tmem + lane_addr + T_D + vc + 16, d1);
       tc::tmem_wait_ld();
-      const float gm = __ldg(ws.loc.gamma + unit * D + r);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         Sv[j] = fmaf(gm, Sv[j], __uint_as_float(d0[j]));
@@ -595,24 +595,36 @@ __global__ void __launch_bounds__(bst::NT, 1)
   constexpr uint32_t T_DE = 0, T_DY = 64, T_DS = 128;
   const uint32_t id = tc::idesc_f16(128, BV, tc::kTF32);
   const int om = tid >> 2, opart = tid & 3;     // dO staging: token om, values 16 opart..
+  // the next chunk's dO row segment, gamma and beta are loaded one chunk ahead
+  float4 onext[4];
+  auto load_do = [&](const ChunkInfo& c) {
+    const float* src = A.d_o + ((c.t0 + om) * HV + h) * D + v0 + 16 * opart;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      onext[j] = om < c.n ? *reinterpret_cast<const float4*>(src + 4 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  ChunkInfo cnext = ws.loc.plan.chunks[last - 1];
+  load_do(cnext);
+  float gnext = __ldg(ws.loc.gamma + unit_of(last - 1) * D + r);
+  float bnext = r < cnext.n ? P.beta[(cnext.t0 + r) * HV + h] : 0.f;
 
   for (int cidx = last - 1; cidx >= first; --cidx) {
     const uint32_t par = static_cast<uint32_t>(last - 1 - cidx) & 1u;
     const int64_t unit = unit_of(cidx);
-    const ChunkInfo ci = ws.loc.plan.chunks[cidx];
+    const ChunkInfo ci = cnext;
+    const float gm = gnext, bt = bnext;
     // dO^T (rows past the chunk's end zero) and dS'^T as B operands; dS' into the workspace
     {
       float o[16];
-      if (om < ci.n) {
-        const float* src = A.d_o + ((ci.t0 + om) * HV + h) * D + v0 + 16 * opart;
 #pragma unroll
-        for (int j = 0; j < 16; j += 4) {
-          const float4 x = *reinterpret_cast<const float4*>(src + j);
-          o[j] = x.x; o[j + 1] = x.y; o[j + 2] = x.z; o[j + 3] = x.w;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = 0.f;
+      for (int j = 0; j < 4; ++j) {
+        o[4 * j] = onext[j].x; o[4 * j + 1] = onext[j].y; o[4 * j + 2] = onext[j].z; o[4 * j + 3] = onext[j].w;
+      }
+      if (cidx > first) {
+        cnext = ws.loc.plan.chunks[cidx - 1];
+        load_do(cnext);
+        gnext = __ldg(ws.loc.gamma + unit_of(cidx - 1) * D + r);
+        bnext = r < cnext.n ? P.beta[(cnext.t0 + r) * HV + h] : 0.f;
       }
 #pragma unroll
       for (int j = 0; j < 16; ++j) *reinterpret_cast<float*>(data + R_OT + kmaj(16 * opart + j, om, 64)) = tf32_nearest(o[j]);
@@ -711,7 +723,6 @@ __global__ void __launch_bounds__(bst::NT, 1)
 #pragma unroll
       for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4*>(gy + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
       if (r < ci.n) {
-        const float bt = P.beta[(ci.t0 + r) * HV + h];
         float* gv = A.dv + ((ci.t0 + r) * HV + h) * D + v0 + vc;
 #pragma unroll
         for (int j = 0; j < 32; j += 4)
@@ -723,7 +734,6 @@ __global__ void __launch_bounds__(bst::NT, 1)
       tc::tmem_ld16(tmem + lane_addr + T_DS + vc, d0);
       tc::tmem_ld16(tmem + lane_addr + T_DS + vc + 16, d1);
       tc::tmem_wait_ld();
-      const float gm = __ldg(ws.loc.gamma + unit * D + r);
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         Rv[j] = fmaf(gm, Rv[j], __uint_as_float(d0[j]));

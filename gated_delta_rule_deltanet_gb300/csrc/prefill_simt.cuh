@@ -118,7 +118,9 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
   const int kh = h / (HV / P.HK);
   const int n = ci.n;
   const int64_t t0 = ci.t0;
-  const int r0 = (tid / 16) * RT, a0 = (tid % 16) * JA, c0 = (tid % 16) * JC;
+  // C x C products: thread columns (t % 16) + 16 b, so that the 8 threads of a quarter-warp read
+  // 8 consecutive padded rows, whose 16-byte pieces fall on different banks
+  const int r0 = (tid / 16) * RT, a0 = tid % 16, c0 = (tid % 16) * JC;
   // additive write (no delta rule): A_kk = 0 makes T = I, and W = 0
   const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
 
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
         qi[a] = *reinterpret_cast<const float4*>(s_q + (r0 + a) * DP + c);
       }
 #pragma unroll
-      for (int b = 0; b < JA; ++b) kj[b] = *reinterpret_cast<const float4*>(Km + (a0 + b) * DP + c);
+      for (int b = 0; b < JA; ++b) kj[b] = *reinterpret_cast<const float4*>(Km + (a0 + 16 * b) * DP + c);
 #pragma unroll
       for (int a = 0; a < RT; ++a)
 #pragma unroll
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
     for (int a = 0; a < RT; ++a)
 #pragma unroll
       for (int b = 0; b < JA; ++b) {
-        const int i = r0 + a, j = a0 + b;
+        const int i = r0 + a, j = a0 + 16 * b;
         const float dec = PERCH ? 1.f : (j <= i ? expf(s_G[i * DP] - s_G[j * DP]) : 0.f);
         s_A[i * CP + j] = (delta && j < i) ? s_beta[i] * (akk[a][b] * dec) : 0.f;
         s_Aq[i * CP + j] = j <= i ? aqk[a][b] * dec : 0.f;

@@ -848,6 +848,7 @@ static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const 
   // the chunk-parallel kernels of one window (or of every chunk: wc == 0)
   auto local = [&](ChunkWindow win, int slots) -> cudaError_t {
     if (slots <= 0) return cudaSuccess;
+    if (kTc && !PERCH) return launch_bwd_local_tc(P, ws.loc, win, slots, st);   // scalar decay
     lk<<<dim3(slots, P.HV), 256, SimtLocalSmem<D, C>::bytes, st>>>(P, ws.loc, win);
     return cudaGetLastError();
   };

@@ -57,6 +57,11 @@ cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const Bwd
 cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, bool sbf16,
                                 ChunkWindow win, int slots, bool record, cudaStream_t st);
 
+// The chunk-local stage on tensor cores for scalar decay (d = 128, chunk 64, bf16 q/k/v):
+// the workspace arrays simt_local_kernel writes for the tensor-core scans.
+cudaError_t launch_bwd_local_tc(const Problem& P, const SimtWorkspace& ws, ChunkWindow win, int slots,
+                                cudaStream_t st);
+
 // The pairwise terms, dg, dbeta, dq and dk on tensor cores for scalar decay (d = 128, chunk
 // 64, bf16 q/k), as bwd_pair_kernel computes them.
 cudaError_t launch_bwd_pair_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, ChunkWindow win,

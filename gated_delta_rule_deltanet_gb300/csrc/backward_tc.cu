@@ -1107,6 +1107,291 @@ cudaError_t launch_bwd_pair_tc(const Problem& P, const BwdWorkspace& ws, const B
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------- local stage
+//
+// The chunk-local stage for scalar decay with its products on tensor cores (kind::tf32):
+//
+//   [K^; Q^] K^T      rows 0-63: K^ K^T, rows 64-127: Q^ K^T   (then the decay, beta and the
+//                     masks on the CUDA cores: A_kk, A_qk)
+//   T = (I + A_kk)^-1 on the CUDA cores (tri_unit_lower_inverse)
+//   (beta K~)^T T^T = W^T,  (beta V)^T T^T = U^T        (M = 128 key channels / value columns)
+//
+// and the element-wise rest (K~, Q~, K_end, gamma), writing the same workspace arrays as
+// simt_local_kernel does for the tensor-core scans, the MMA operands among them rounded to tf32.
+
+namespace blt {
+
+constexpr int C = 64, D = 128, NT = 256, DP = D + 4, CP = C + 4;
+constexpr uint32_t S_K = 0, S_V = C * DP * 4;                       // k^, v rows (fp32)
+constexpr uint32_t OPS = 2 * C * DP * 4;                            // 67584, 1024-aligned
+// first products: [K^; Q^] as 4 blocks of 128 rows (K = key channels); the second: (beta K~)^T
+// and (beta V)^T as 2 blocks of 128 rows each (K = tokens), T as 2 blocks of 64 rows
+constexpr uint32_t A_W = OPS, A_U = OPS + 32768, B_T = OPS + 65536;
+constexpr uint32_t S_A = OPS + 81920, S_AQ = S_A + C * CP * 4, S_T = S_AQ + C * CP * 4,
+                   S_X = S_T + C * CP * 4, SMALL = S_X + C * CP * 4;
+constexpr uint32_t SMEM = SMALL + 1024 + 64 + 1024;                // small arrays, control, slack
+constexpr uint32_t kWaitLimit = 1u << 22;
+static_assert(C * DP * 4 <= 2 * C * CP * 4, "q rows fit over T and X");
+static_assert(4 * C * 4 + 16 <= 1024 + 64, "small arrays and the control block");
+static_assert(SMEM <= 227 * 1024, "shared memory budget");
+
+struct Ctrl {
+  uint64_t bar;
+  uint32_t tmem;
+  int bad;
+};
+
+}  // namespace blt
+
+__global__ void __launch_bounds__(blt::NT, 1)
+    bwd_local_tc_kernel(Problem P, SimtWorkspace ws, ChunkWindow win) {
+  using namespace blt;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t pad = (1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* const data = smem_raw + pad;
+  float* const s_k = reinterpret_cast<float*>(data + S_K);
+  float* const s_v = reinterpret_cast<float*>(data + S_V);
+  float* const s_q = reinterpret_cast<float*>(data + S_T);          // until A_qk is formed
+  float* const s_A = reinterpret_cast<float*>(data + S_A);
+  float* const s_Aq = reinterpret_cast<float*>(data + S_AQ);
+  float* const s_T = reinterpret_cast<float*>(data + S_T);
+  float* const s_X = reinterpret_cast<float*>(data + S_X);
+  float* const s_G = reinterpret_cast<float*>(data + SMALL);       // [C]
+  float* const s_beta = s_G + C;                                   // [C]
+  float* const s_inv = s_beta + C;                                 // [2C]
+  Ctrl* const ctl = reinterpret_cast<Ctrl*>(s_inv + 2 * C);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int gc;
+  if (ws.plan.info[1] == 0 || !window_chunk(ws.plan, P.num_seqs, win, blockIdx.x, &gc)) return;
+  const ChunkInfo ci = ws.plan.chunks[gc];
+  const int h = blockIdx.y, HV = P.HV, kh = h / (HV / P.HK), n = ci.n;
+  const int64_t t0 = ci.t0;
+  const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
+  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
+  const uint32_t sd = tc::smem_u32(data);
+
+  if (tid == 0) {
+    tc::mbar_init(&ctl->bar, 1);
+    ctl->bad = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&ctl->tmem, 256);
+    tc::tmem_relinquish();
+  }
+  for (int u = tid; u < C * (D / 8); u += NT) {    // k, q (key head), v (value head), bf16
+    const int i = u / (D / 8), c = (u % (D / 8)) * 8;
+    float kx[8] = {}, qx[8] = {}, vx[8] = {};
+    if (i < n) {
+      const int64_t t = t0 + i;
+      tc::bf16x8_load(reinterpret_cast<const unsigned char*>(static_cast<const uint16_t*>(P.k) + t * P.k_stride +
+                                                              static_cast<int64_t>(kh) * D + c), kx);
+      tc::bf16x8_load(reinterpret_cast<const unsigned char*>(static_cast<const uint16_t*>(P.q) + t * P.q_stride +
+                                                              static_cast<int64_t>(kh) * D + c), qx);
+      tc::bf16x8_load(reinterpret_cast<const unsigned char*>(static_cast<const uint16_t*>(P.v) + t * P.v_stride +
+                                                              static_cast<int64_t>(h) * D + c), vx);
+    }
+    st_row(s_k + i * DP + c, kx);
+    st_row(s_q + i * DP + c, qx);
+    st_row(s_v + i * DP + c, vx);
+  }
+  for (int i = tid; i < C; i += NT) {
+    const bool live = i < n;
+    s_beta[i] = live ? P.beta[(t0 + i) * HV + h] : 0.f;
+    s_G[i] = live ? P.g[(t0 + i) * HV + h] : 0.f;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = ctl->tmem;
+  for (int i = warp; i < C; i += NT / 32) {       // L2 norms and the query scale
+    float sk = 0.f, sq = 0.f;
+    for (int c = lane; c < D; c += 32) {
+      sk += s_k[i * DP + c] * s_k[i * DP + c];
+      sq += s_q[i * DP + c] * s_q[i * DP + c];
+    }
+    sk = warp_sum(sk);
+    sq = warp_sum(sq);
+    if (lane == 0) {
+      s_inv[i] = P.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
+      s_inv[C + i] = (P.l2norm ? rsqrtf(sq + 1e-6f) : 1.f) * P.scale;
+    }
+  }
+  if (warp == 0) {                              // inclusive cumulative log-decay, two rows a lane
+    const float a = s_G[2 * lane], b = s_G[2 * lane + 1];
+    float inc = a + b;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += y;
+    }
+    s_G[2 * lane] = inc - b;
+    s_G[2 * lane + 1] = inc;
+  }
+  __syncthreads();
+  // [K^; Q^] rows into the first operand (float4 pieces of 4 key channels), and the
+  // element-wise outputs of k^ and q^: K~ (fp32), K_end, K_end^T, Q~^T (tf32), gamma
+  const float Gl = s_G[C - 1];
+  for (int u = tid; u < 2 * C * (D / 4); u += NT) {
+    const int r = u / (D / 4), c = (u % (D / 4)) * 4;
+    const int i = r & (C - 1);
+    float* src = (r < C ? s_k : s_q) + i * DP + c;
+    float4 x = *reinterpret_cast<float4*>(src);
+    const float sc = s_inv[(r < C ? 0 : C) + i];
+    x.x *= sc; x.y *= sc; x.z *= sc; x.w *= sc;
+    *reinterpret_cast<float4*>(src) = x;
+    *reinterpret_cast<float4*>(data + OPS + (c >> 5) * 16384 + tc::sw128_offset(r, (c & 31) >> 2)) =
+        make_float4(tf32_nearest(x.x), tf32_nearest(x.y), tf32_nearest(x.z), tf32_nearest(x.w));
+    const float eG = expf(s_G[i]);
+    if (r < C) {
+      const float eL = expf(Gl - s_G[i]);
+      *reinterpret_cast<float4*>(ws.Kt + (unit * C + i) * D + c) = make_float4(x.x * eG, x.y * eG, x.z * eG, x.w * eG);
+      const float4 ke = make_float4(tf32_nearest(x.x * eL), tf32_nearest(x.y * eL), tf32_nearest(x.z * eL),
+                                    tf32_nearest(x.w * eL));
+      *reinterpret_cast<float4*>(ws.Kend + (unit * C + i) * D + c) = ke;
+      ws.KendT[(unit * D + c) * C + i] = ke.x;
+      ws.KendT[(unit * D + c + 1) * C + i] = ke.y;
+      ws.KendT[(unit * D + c + 2) * C + i] = ke.z;
+      ws.KendT[(unit * D + c + 3) * C + i] = ke.w;
+    } else {
+      ws.QtT[(unit * D + c) * C + i] = tf32_nearest(x.x * eG);
+      ws.QtT[(unit * D + c + 1) * C + i] = tf32_nearest(x.y * eG);
+      ws.QtT[(unit * D + c + 2) * C + i] = tf32_nearest(x.z * eG);
+      ws.QtT[(unit * D + c + 3) * C + i] = tf32_nearest(x.w * eG);
+    }
+  }
+  for (int c = tid; c < D; c += NT) ws.gamma[unit * D + c] = expf(Gl);
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {                               // [K^; Q^] K^T: K^ is the operand's rows 0-63
+    tc::fence_after_sync();
+    const uint32_t id = tc::idesc_f16(128, 64, tc::kTF32);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint64_t da = tc::smem_desc_sw128(sd + OPS + j * 16384, 1024);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        tc::mma_ss_tf32(tmem, tc::desc_add(da, 32 * k), tc::desc_add(da, 32 * k), id, (j | k) ? 1u : 0u);
+    }
+    tc::mma_commit(&ctl->bar);
+  }
+  if (!tc::mbar_wait_bounded(&ctl->bar, 0, kWaitLimit)) ctl->bad = 1;
+  tc::fence_after_sync();
+  // A_kk and A_qk from the products: the decay exp(G_i - G_j), beta and the masks
+  const int qd = warp & 3, ch = warp >> 2;
+  const int row = 32 * qd + lane;               // TMEM lane
+  const uint32_t la = static_cast<uint32_t>(32 * qd) << 16;
+  {
+    uint32_t v0[16], v1[16];
+    tc::tmem_ld16(tmem + la + 32 * ch, v0);
+    tc::tmem_ld16(tmem + la + 32 * ch + 16, v1);
+    tc::tmem_wait_ld();
+    const int i = row & (C - 1);
+    const float Gi = s_G[i], bi = s_beta[i];
+    float* dst = (row < C ? s_A : s_Aq) + i * CP + 32 * ch;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int j = 32 * ch + e;
+      const float x = __uint_as_float(e < 16 ? v0[e] : v1[e - 16]);
+      const float dec = j <= i ? expf(Gi - s_G[j]) : 0.f;
+      dst[e] = row < C ? ((delta && j < i) ? bi * x * dec : 0.f) : x * dec;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();                              // the q rows over T and X are dead
+  for (int idx = tid; idx < C * CP; idx += NT) s_T[idx] = 0.f;
+  __syncthreads();
+  tri_unit_lower_inverse<C, CP, NT>(s_A, s_T, s_X, tid);
+  // (beta K~)^T and (beta V)^T (rows: key channel / value column, K = token), T (rows i, K = j)
+  for (int u = tid; u < 2 * D * (C / 4); u += NT) {
+    const int which = u / (D * (C / 4)), rem = u % (D * (C / 4));
+    const int c = rem % D, j0 = (rem / D) * 4;
+    float x[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = j0 + e;
+      x[e] = which == 0 ? (delta ? s_beta[j] * s_k[j * DP + c] * expf(s_G[j]) : 0.f)
+                        : s_beta[j] * s_v[j * DP + c];
+    }
+    *reinterpret_cast<float4*>(data + (which ? A_U : A_W) + (j0 >> 5) * 16384 + tc::sw128_offset(c, (j0 & 31) >> 2)) =
+        make_float4(tf32_nearest(x[0]), tf32_nearest(x[1]), tf32_nearest(x[2]), tf32_nearest(x[3]));
+  }
+  for (int u = tid; u < C * (C / 4); u += NT) {
+    const int i = u / (C / 4), j0 = (u % (C / 4)) * 4;
+    const float4 t = *reinterpret_cast<const float4*>(s_T + i * CP + j0);
+    *reinterpret_cast<float4*>(data + B_T + (j0 >> 5) * 8192 + tc::sw128_offset(i, (j0 & 31) >> 2)) =
+        make_float4(tf32_nearest(t.x), tf32_nearest(t.y), tf32_nearest(t.z), tf32_nearest(t.w));
+  }
+  tc::fence_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  if (tid == 0) {
+    tc::fence_after_sync();
+    const uint32_t id = tc::idesc_f16(128, 64, tc::kTF32);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const uint64_t dt = tc::smem_desc_sw128(sd + B_T + j * 8192, 1024);
+      const uint64_t dw = tc::smem_desc_sw128(sd + A_W + j * 16384, 1024);
+      const uint64_t du = tc::smem_desc_sw128(sd + A_U + j * 16384, 1024);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        tc::mma_ss_tf32(tmem + 64, tc::desc_add(dw, 32 * k), tc::desc_add(dt, 32 * k), id, (j | k) ? 1u : 0u);
+        tc::mma_ss_tf32(tmem + 128, tc::desc_add(du, 32 * k), tc::desc_add(dt, 32 * k), id, (j | k) ? 1u : 0u);
+      }
+    }
+    tc::mma_commit(&ctl->bar);
+  }
+  if (!tc::mbar_wait_bounded(&ctl->bar, 1, kWaitLimit)) ctl->bad = 1;
+  tc::fence_after_sync();
+  // W^T rows (lane = key channel) and U^T rows (lane = value column), 32 tokens a warp
+  {
+    uint32_t w0[16], w1[16], u0[16], u1[16];
+    tc::tmem_ld16(tmem + la + 64 + 32 * ch, w0);
+    tc::tmem_ld16(tmem + la + 64 + 32 * ch + 16, w1);
+    tc::tmem_ld16(tmem + la + 128 + 32 * ch, u0);
+    tc::tmem_ld16(tmem + la + 128 + 32 * ch + 16, u1);
+    tc::tmem_wait_ld();
+    float w[32];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      w[e] = tf32_nearest(__uint_as_float(w0[e]));
+      w[16 + e] = tf32_nearest(__uint_as_float(w1[e]));
+    }
+    float* wt = ws.WT + (unit * D + row) * C + 32 * ch;
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(wt + e) = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int64_t o = (unit * C + 32 * ch + e) * D + row;
+      ws.W[o] = w[e];
+      ws.U[o] = __uint_as_float(e < 16 ? u0[e] : u1[e - 16]);
+    }
+  }
+  for (int idx = tid; idx < C * C; idx += NT) {
+    const int i = idx / C, j = idx % C;
+    ws.AqkT[unit * C * C + idx] = tf32_nearest(s_Aq[j * CP + i]);
+    ws.TT[unit * C * C + idx] = tf32_nearest(s_T[j * CP + i]);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (ctl->bad && tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+cudaError_t launch_bwd_local_tc(const Problem& P, const SimtWorkspace& ws, ChunkWindow win, int slots,
+                                cudaStream_t st) {
+  using namespace blt;
+  if (slots <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(SMEM));
+  if (e != cudaSuccess) return e;
+  bwd_local_tc_kernel<<<dim3(static_cast<unsigned>(slots), P.HV), NT, SMEM, st>>>(P, ws, win);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, ChunkWindow win,
                              int slots, cudaStream_t st) {
   using namespace bvt;

@@ -79,6 +79,45 @@ struct SimtLocalSmem {
   static constexpr size_t bytes = floats * sizeof(float);
 };
 
+// T = (I + A)^-1 for a strictly lower C x C matrix A (rows of CP floats in shared memory; s_T
+// zero on entry): forward substitution inside each 16 x 16 diagonal block by one half-warp,
+// then neighbouring blocks merged, T21 = -T22 (A21 T11), doubling the block size.  s_X is
+// scratch.  Called by all NT threads; ends with a block barrier.
+template <int C, int CP, int NT>
+__device__ __forceinline__ void tri_unit_lower_inverse(const float* s_A, float* s_T, float* s_X, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < C / 16 && lane < 16) {
+    const int base = warp * 16, col = base + lane;
+    for (int r = 0; r < 16; ++r) {
+      const int row = base + r;
+      float val = r == lane ? 1.f : 0.f;
+      for (int m = lane; m < r; ++m) val -= s_A[row * CP + base + m] * s_T[(base + m) * CP + col];
+      s_T[row * CP + col] = r >= lane ? val : 0.f;
+      __syncwarp(0x0000ffffu);
+    }
+  }
+  __syncthreads();
+  for (int s = 16; s < C; s *= 2) {
+    const int pairs = C / (2 * s);
+    for (int idx = tid; idx < pairs * s * s; idx += NT) {
+      const int p = idx / (s * s), r = (idx / s) % s, c = idx % s;
+      const int rr = 2 * p * s + s, cc = 2 * p * s;
+      float acc = 0.f;
+      for (int m = c; m < s; ++m) acc += s_A[(rr + r) * CP + cc + m] * s_T[(cc + m) * CP + cc + c];
+      s_X[(rr + r) * CP + cc + c] = acc;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < pairs * s * s; idx += NT) {
+      const int p = idx / (s * s), r = (idx / s) % s, c = idx % s;
+      const int rr = 2 * p * s + s, cc = 2 * p * s;
+      float acc = 0.f;
+      for (int m = 0; m <= r; ++m) acc += s_T[(rr + r) * CP + rr + m] * s_X[(rr + m) * CP + cc + c];
+      s_T[(rr + r) * CP + cc + c] = -acc;
+    }
+    __syncthreads();
+  }
+}
+
 // Per-channel decay spans at most this many nats between a token and the chunk's middle token
 // for the anchored factors exp(G - G_a), exp(G_a - G) to be used (they stay far inside fp32);
 // beyond it the pairwise decay is evaluated per pair and channel.
@@ -285,38 +324,7 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
   }
   __syncthreads();
 
-  // T = (I + A)^-1: forward substitution inside each 16x16 diagonal block ...
-  if (warp < C / 16 && lane < 16) {
-    const int base = warp * 16, col = base + lane;
-    for (int r = 0; r < 16; ++r) {
-      const int row = base + r;
-      float val = r == lane ? 1.f : 0.f;
-      for (int m = lane; m < r; ++m) val -= s_A[row * CP + base + m] * s_T[(base + m) * CP + col];
-      s_T[row * CP + col] = r >= lane ? val : 0.f;
-      __syncwarp(0x0000ffffu);
-    }
-  }
-  __syncthreads();
-  // ... then merge neighbours: T21 = -T22 (A21 T11), doubling the block size
-  for (int s = 16; s < C; s *= 2) {
-    const int pairs = C / (2 * s);
-    for (int idx = tid; idx < pairs * s * s; idx += NT) {
-      const int p = idx / (s * s), r = (idx / s) % s, c = idx % s;
-      const int rr = 2 * p * s + s, cc = 2 * p * s;
-      float acc = 0.f;
-      for (int m = c; m < s; ++m) acc += s_A[(rr + r) * CP + cc + m] * s_T[(cc + m) * CP + cc + c];
-      s_X[(rr + r) * CP + cc + c] = acc;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < pairs * s * s; idx += NT) {
-      const int p = idx / (s * s), r = (idx / s) % s, c = idx % s;
-      const int rr = 2 * p * s + s, cc = 2 * p * s;
-      float acc = 0.f;
-      for (int m = 0; m <= r; ++m) acc += s_T[(rr + r) * CP + rr + m] * s_X[(rr + m) * CP + cc + c];
-      s_T[(rr + r) * CP + cc + c] = -acc;
-    }
-    __syncthreads();
-  }
+  tri_unit_lower_inverse<C, CP, NT>(s_A, s_T, s_X, tid);
 
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
   float* gW = ws.W + unit * C * D;

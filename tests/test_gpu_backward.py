@@ -71,6 +71,9 @@ CASES = [
     ("bf16-d128-c16-kda", [90], 1, 2, 128, "bf16", "f32", "per_channel", 16, True),
     ("f32-d128-c32-gla", [100, 29], 2, 2, 128, "f32", "f32", "per_channel", 32, False),
     ("bf16-d16-c64-mamba2", [129, 0, 7], 1, 1, 16, "bf16", "f32", "scalar", 64, False),
+    # the tensor-core kernels' additive-write branches (bf16, d = 128, chunk 64)
+    ("bf16-d128-c64-mamba2", [129, 0, 70], 2, 4, 128, "bf16", "f32", "scalar", 64, False),
+    ("bf16-d128-c64-gla", [100, 29], 2, 2, 128, "bf16", "bf16", "per_channel", 64, False),
 ]
 
 

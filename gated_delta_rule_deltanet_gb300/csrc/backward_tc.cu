@@ -803,7 +803,7 @@ cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const 
 
 namespace bpt {
 
-constexpr int C = 64, D = 128, NT = 256, DP = D + 4;
+constexpr int C = 64, D = 128, NT = 512, DP = D + 4;
 constexpr uint32_t Q_OFF = 0, K_OFF = C * DP * 4;                  // q^, k^ rows, fp32
 constexpr uint32_t OPS = 2 * C * DP * 4;                           // 67584, 1024-aligned
 constexpr uint32_t A12 = OPS;                                      // 2 blocks of 128 rows
@@ -843,7 +843,7 @@ __global__ void __launch_bounds__(bpt::NT, 1)
   float* const s_dot = s_db + C;                                   // [C] row sums of dG
   float* const s_dGl = s_dot + C;                                  // [D] gradient w.r.t. G_last
   Ctrl* const ctl = reinterpret_cast<Ctrl*>(s_dGl + D);
-  constexpr int IR = C / 16, JC = D / 16;
+  constexpr int IR = C * 16 / NT, JC = D / 16;   // a thread's rows and columns of C x D tiles
 
   int gc;
   if (ws.loc.plan.info[1] == 0 || !window_chunk(ws.loc.plan, P.num_seqs, win, blockIdx.x, &gc)) return;
@@ -978,24 +978,24 @@ __global__ void __launch_bounds__(bpt::NT, 1)
       const uint32_t la = static_cast<uint32_t>(32 * qd) << 16;
       float* dst12 = row < C ? s_P1 + row * SP : s_P2 + (row - C) * SP;
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
+      for (int jj = 0; jj < 2; ++jj) {          // warp w: columns 32 (w / 4) ..
         uint32_t v[16];
-        tc::tmem_ld16(tmem + la + 64 * ch + 16 * jj, v);
+        tc::tmem_ld16(tmem + la + 32 * ch + 16 * jj, v);
         tc::tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; e += 4)
-          *reinterpret_cast<float4*>(dst12 + 64 * ch + 16 * jj + e) =
+          *reinterpret_cast<float4*>(dst12 + 32 * ch + 16 * jj + e) =
               make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
       }
       if (qd < 2) {
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
+        for (int jj = 0; jj < 2; ++jj) {
           uint32_t v[16];
-          tc::tmem_ld16(tmem + la + 128 + 64 * ch + 16 * jj, v);
+          tc::tmem_ld16(tmem + la + 128 + 32 * ch + 16 * jj, v);
           tc::tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(s_P3 + row * SP + 64 * ch + 16 * jj + e) =
+            *reinterpret_cast<float4*>(s_P3 + row * SP + 32 * ch + 16 * jj + e) =
                 make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
         }
       }
@@ -1121,7 +1121,8 @@ cudaError_t launch_bwd_pair_tc(const Problem& P, const BwdWorkspace& ws, const B
 
 namespace blt {
 
-constexpr int C = 64, D = 128, NT = 256, DP = D + 4, CP = C + 4;
+constexpr int C = 64, D = 128, NT = 512, DP = D + 4, CP = C + 4;
+constexpr int CW = 64 / (NT / 128);             // accumulator columns a warp reads (16)
 constexpr uint32_t S_K = 0, S_V = C * DP * 4;                       // k^, v rows (fp32)
 constexpr uint32_t OPS = 2 * C * DP * 4;                            // 67584, 1024-aligned
 // first products: [K^; Q^] as 4 blocks of 128 rows (K = key channels); the second: (beta K~)^T
@@ -1230,8 +1231,7 @@ __global__ void __launch_bounds__(blt::NT, 1)
     s_G[2 * lane + 1] = inc;
   }
   __syncthreads();
-  // [K^; Q^] rows into the first operand (float4 pieces of 4 key channels), and the
-  // element-wise outputs of k^ and q^: K~ (fp32), K_end, K_end^T, Q~^T (tf32), gamma
+  // [K^; Q^] rows into the first operand (float4 pieces of 4 key channels)
   const float Gl = s_G[C - 1];
   for (int u = tid; u < 2 * C * (D / 4); u += NT) {
     const int r = u / (D / 4), c = (u % (D / 4)) * 4;
@@ -1243,23 +1243,6 @@ __global__ void __launch_bounds__(blt::NT, 1)
     *reinterpret_cast<float4*>(src) = x;
     *reinterpret_cast<float4*>(data + OPS + (c >> 5) * 16384 + tc::sw128_offset(r, (c & 31) >> 2)) =
         make_float4(tf32_nearest(x.x), tf32_nearest(x.y), tf32_nearest(x.z), tf32_nearest(x.w));
-    const float eG = expf(s_G[i]);
-    if (r < C) {
-      const float eL = expf(Gl - s_G[i]);
-      *reinterpret_cast<float4*>(ws.Kt + (unit * C + i) * D + c) = make_float4(x.x * eG, x.y * eG, x.z * eG, x.w * eG);
-      const float4 ke = make_float4(tf32_nearest(x.x * eL), tf32_nearest(x.y * eL), tf32_nearest(x.z * eL),
-                                    tf32_nearest(x.w * eL));
-      *reinterpret_cast<float4*>(ws.Kend + (unit * C + i) * D + c) = ke;
-      ws.KendT[(unit * D + c) * C + i] = ke.x;
-      ws.KendT[(unit * D + c + 1) * C + i] = ke.y;
-      ws.KendT[(unit * D + c + 2) * C + i] = ke.z;
-      ws.KendT[(unit * D + c + 3) * C + i] = ke.w;
-    } else {
-      ws.QtT[(unit * D + c) * C + i] = tf32_nearest(x.x * eG);
-      ws.QtT[(unit * D + c + 1) * C + i] = tf32_nearest(x.y * eG);
-      ws.QtT[(unit * D + c + 2) * C + i] = tf32_nearest(x.z * eG);
-      ws.QtT[(unit * D + c + 3) * C + i] = tf32_nearest(x.w * eG);
-    }
   }
   for (int c = tid; c < D; c += NT) ws.gamma[unit * D + c] = expf(Gl);
   tc::fence_async_smem();
@@ -1284,23 +1267,42 @@ __global__ void __launch_bounds__(blt::NT, 1)
   const int row = 32 * qd + lane;               // TMEM lane
   const uint32_t la = static_cast<uint32_t>(32 * qd) << 16;
   {
-    uint32_t v0[16], v1[16];
-    tc::tmem_ld16(tmem + la + 32 * ch, v0);
-    tc::tmem_ld16(tmem + la + 32 * ch + 16, v1);
+    uint32_t v0[16];
+    tc::tmem_ld16(tmem + la + CW * ch, v0);
     tc::tmem_wait_ld();
     const int i = row & (C - 1);
     const float Gi = s_G[i], bi = s_beta[i];
-    float* dst = (row < C ? s_A : s_Aq) + i * CP + 32 * ch;
+    float* dst = (row < C ? s_A : s_Aq) + i * CP + CW * ch;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int j = 32 * ch + e;
-      const float x = __uint_as_float(e < 16 ? v0[e] : v1[e - 16]);
+    for (int e = 0; e < CW; ++e) {
+      const int j = CW * ch + e;
+      const float x = __uint_as_float(v0[e]);
       const float dec = j <= i ? expf(Gi - s_G[j]) : 0.f;
       dst[e] = row < C ? ((delta && j < i) ? bi * x * dec : 0.f) : x * dec;
     }
   }
+  // the element-wise outputs of k^ and q^: K~ (fp32), K_end (tf32) as rows; K_end^T and Q~^T
+  // (tf32) through a transposing stage over the first operand (free once its product is done),
+  // rows of 65 floats so that neither side of the transpose meets bank conflicts
+  float* const stg_kt = reinterpret_cast<float*>(data + OPS);
+  float* const stg_qt = stg_kt + D * (C + 1);
+  for (int idx = tid; idx < C * D; idx += NT) {
+    const int i = idx / D, c = idx % D;
+    const float kv = s_k[i * DP + c], qv = s_q[i * DP + c];
+    const float eG = expf(s_G[i]), eL = expf(Gl - s_G[i]);
+    const float ke = tf32_nearest(kv * eL);
+    ws.Kt[(unit * C + i) * D + c] = kv * eG;
+    ws.Kend[(unit * C + i) * D + c] = ke;
+    stg_kt[c * (C + 1) + i] = ke;
+    stg_qt[c * (C + 1) + i] = tf32_nearest(qv * eG);
+  }
   tc::fence_before_sync();
   __syncthreads();                              // the q rows over T and X are dead
+  for (int idx = tid; idx < C * D; idx += NT) {
+    const int c = idx / C, i = idx % C;
+    ws.KendT[(unit * D + c) * C + i] = stg_kt[c * (C + 1) + i];
+    ws.QtT[(unit * D + c) * C + i] = stg_qt[c * (C + 1) + i];
+  }
   for (int idx = tid; idx < C * CP; idx += NT) s_T[idx] = 0.f;
   __syncthreads();
   tri_unit_lower_inverse<C, CP, NT>(s_A, s_T, s_X, tid);
@@ -1345,34 +1347,39 @@ __global__ void __launch_bounds__(blt::NT, 1)
   }
   if (!tc::mbar_wait_bounded(&ctl->bar, 1, kWaitLimit)) ctl->bad = 1;
   tc::fence_after_sync();
-  // W^T rows (lane = key channel) and U^T rows (lane = value column), 32 tokens a warp
+  // W^T rows (lane = key channel) and U^T rows (lane = value column), CW tokens a warp
   {
-    uint32_t w0[16], w1[16], u0[16], u1[16];
-    tc::tmem_ld16(tmem + la + 64 + 32 * ch, w0);
-    tc::tmem_ld16(tmem + la + 64 + 32 * ch + 16, w1);
-    tc::tmem_ld16(tmem + la + 128 + 32 * ch, u0);
-    tc::tmem_ld16(tmem + la + 128 + 32 * ch + 16, u1);
+    uint32_t w0[16], u0[16];
+    tc::tmem_ld16(tmem + la + 64 + CW * ch, w0);
+    tc::tmem_ld16(tmem + la + 128 + CW * ch, u0);
     tc::tmem_wait_ld();
-    float w[32];
+    float w[CW];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      w[e] = tf32_nearest(__uint_as_float(w0[e]));
-      w[16 + e] = tf32_nearest(__uint_as_float(w1[e]));
-    }
-    float* wt = ws.WT + (unit * D + row) * C + 32 * ch;
+    for (int e = 0; e < CW; ++e) w[e] = tf32_nearest(__uint_as_float(w0[e]));
+    float* wt = ws.WT + (unit * D + row) * C + CW * ch;
 #pragma unroll
-    for (int e = 0; e < 32; e += 4) *reinterpret_cast<float4*>(wt + e) = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
+    for (int e = 0; e < CW; e += 4) *reinterpret_cast<float4*>(wt + e) = make_float4(w[e], w[e + 1], w[e + 2], w[e + 3]);
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int64_t o = (unit * C + 32 * ch + e) * D + row;
+    for (int e = 0; e < CW; ++e) {
+      const int64_t o = (unit * C + CW * ch + e) * D + row;
       ws.W[o] = w[e];
-      ws.U[o] = __uint_as_float(e < 16 ? u0[e] : u1[e - 16]);
+      ws.U[o] = __uint_as_float(u0[e]);
     }
   }
-  for (int idx = tid; idx < C * C; idx += NT) {
-    const int i = idx / C, j = idx % C;
-    ws.AqkT[unit * C * C + idx] = tf32_nearest(s_Aq[j * CP + i]);
-    ws.TT[unit * C * C + idx] = tf32_nearest(s_T[j * CP + i]);
+  {                                             // A_qk^T and T^T through a transposing stage
+    float* const stg_a = reinterpret_cast<float*>(data + OPS);
+    float* const stg_t = stg_a + C * (C + 1);
+    for (int idx = tid; idx < C * C; idx += NT) {
+      const int j = idx / C, i = idx % C;
+      stg_a[i * (C + 1) + j] = tf32_nearest(s_Aq[j * CP + i]);
+      stg_t[i * (C + 1) + j] = tf32_nearest(s_T[j * CP + i]);
+    }
+    __syncthreads();
+    for (int idx = tid; idx < C * C; idx += NT) {
+      const int i = idx / C, j = idx % C;
+      ws.AqkT[unit * C * C + idx] = stg_a[i * (C + 1) + j];
+      ws.TT[unit * C * C + idx] = stg_t[i * (C + 1) + j];
+    }
   }
   tc::fence_before_sync();
   __syncthreads();

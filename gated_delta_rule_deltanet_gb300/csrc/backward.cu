@@ -585,20 +585,18 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
   for (int h = kh * ratio; h < (kh + 1) * ratio; ++h) {
     const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
     __syncthreads();
-    // cumulative log-decay (padded rows add nothing), beta, dA, dM
-    if (PERCH) {
-      for (int c = tid; c < D; c += NT) {
-        float acc = 0.f;
-        for (int i = 0; i < C; ++i) {
-          acc += i < n ? P.g[((ci.t0 + i) * HV + h) * D + c] : 0.f;
-          s_G[i * GW + c] = acc;
-        }
-      }
-    } else if (tid == 0) {
+    // cumulative log-decay (padded rows add nothing), beta, dA, dM: the log-decay rows are
+    // loaded by all threads at once, then summed down the rows in shared memory
+    for (int idx = tid; idx < C * GW; idx += NT) {
+      const int i = idx / GW, c = idx % GW;
+      s_G[idx] = i < n ? (PERCH ? P.g[((ci.t0 + i) * HV + h) * D + c] : P.g[(ci.t0 + i) * HV + h]) : 0.f;
+    }
+    __syncthreads();
+    for (int c = tid; c < GW; c += NT) {
       float acc = 0.f;
       for (int i = 0; i < C; ++i) {
-        acc += i < n ? P.g[(ci.t0 + i) * HV + h] : 0.f;
-        s_G[i] = acc;
+        acc += s_G[i * GW + c];
+        s_G[i * GW + c] = acc;
       }
     }
     for (int i = tid; i < C; i += NT) s_b[i] = i < n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;

@@ -913,12 +913,17 @@ __global__ void __launch_bounds__(bpt::NT, 1)
   for (int h = kh * ratio, it = 0; h < (kh + 1) * ratio; ++h, ++it) {
     const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
     __syncthreads();                            // the previous head's staging is read
-    if (tid == 0) {
-      float acc = 0.f;
-      for (int i = 0; i < C; ++i) {
-        acc += i < n ? P.g[(ci.t0 + i) * HV + h] : 0.f;
-        s_G[i] = acc;
+    if (warp == 0) {                            // cumulative log-decay: two rows a lane, one scan
+      const float a = 2 * lane < n ? P.g[(ci.t0 + 2 * lane) * HV + h] : 0.f;
+      const float b = 2 * lane + 1 < n ? P.g[(ci.t0 + 2 * lane + 1) * HV + h] : 0.f;
+      float inc = a + b;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += y;
       }
+      s_G[2 * lane] = inc - b;
+      s_G[2 * lane + 1] = inc;
     }
     for (int i = tid; i < C; i += NT) s_b[i] = i < n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
     for (int c = tid; c < D; c += NT) s_dGl[c] = 0.f;
@@ -1048,12 +1053,17 @@ __global__ void __launch_bounds__(bpt::NT, 1)
         if (lane == 0) s_dot[C - 1] += v;
       }
       __syncthreads();
-      if (tid == 0) {                           // dg = reverse cumulative sum of the rows
-        float acc = 0.f;
-        for (int i = C - 1; i >= 0; --i) {
-          acc += s_dot[i];
-          if (i < n) A.dg[(ci.t0 + i) * HV + h] = acc;
+      if (warp == 0) {                          // dg = reverse cumulative sum of the rows
+        const int i1 = C - 1 - 2 * lane, i0 = i1 - 1;    // lane l: rows 63 - 2l and 62 - 2l
+        const float a = s_dot[i1], b = s_dot[i0];
+        float inc = a + b;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, inc, off);
+          if (lane >= off) inc += y;
         }
+        if (i1 < n) A.dg[(ci.t0 + i1) * HV + h] = inc - b;
+        if (i0 < n) A.dg[(ci.t0 + i0) * HV + h] = inc;
       }
       for (int i = tid; i < n; i += NT)
         A.dbeta[(ci.t0 + i) * HV + h] = ws.dbr[unit * C + i] + (delta ? s_db[i] : 0.f);

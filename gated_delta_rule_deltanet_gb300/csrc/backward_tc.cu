@@ -970,6 +970,14 @@ __global__ void __launch_bounds__(bpt::NT, 1)
       }
       tc::mma_commit(&ctl->bar);
     }
+    // the contractions' rows of this thread, requested while the products run
+    float gq[IR][JC], gk[IR][JC], ge[IR][JC];
+#pragma unroll
+    for (int a = 0; a < IR; ++a) {
+      ld_row(gq[a], ws.dQt + unit * C * D + (r0 + a) * D + c0);
+      ld_row(gk[a], ws.dKt + unit * C * D + (r0 + a) * D + c0);
+      ld_row(ge[a], ws.dKe + unit * C * D + (r0 + a) * D + c0);
+    }
     if (!tc::mbar_wait_bounded(&ctl->bar, static_cast<uint32_t>(it) & 1u, kWaitLimit)) ctl->bad = 1;
     tc::fence_after_sync();
     // stage P1, P2, P3 as rows of SP floats over the operands
@@ -1015,10 +1023,10 @@ __global__ void __launch_bounds__(bpt::NT, 1)
 #pragma unroll
       for (int a = 0; a < IR; ++a) {
         const int i = r0 + a;
-        float dqt[JC], dkt[JC], dke[JC], p1[JC], p2[JC], p3[JC], qv[JC], kv[JC];
-        ld_row(dqt, ws.dQt + unit * C * D + i * D + c0);
-        ld_row(dkt, ws.dKt + unit * C * D + i * D + c0);
-        ld_row(dke, ws.dKe + unit * C * D + i * D + c0);
+        float p1[JC], p2[JC], p3[JC], qv[JC], kv[JC];
+        const float* dqt = gq[a];
+        const float* dkt = gk[a];
+        const float* dke = ge[a];
         ld_row(p1, s_P1 + i * SP + c0);
         ld_row(p2, s_P2 + i * SP + c0);
         ld_row(p3, s_P3 + i * SP + c0);
@@ -1140,10 +1148,10 @@ constexpr uint32_t OPS = 2 * C * DP * 4;                            // 67584, 10
 constexpr uint32_t A_W = OPS, A_U = OPS + 32768, B_T = OPS + 65536;
 constexpr uint32_t S_A = OPS + 81920, S_AQ = S_A + C * CP * 4, S_T = S_AQ + C * CP * 4,
                    S_X = S_T + C * CP * 4, SMALL = S_X + C * CP * 4;
-constexpr uint32_t SMEM = SMALL + 1024 + 64 + 1024;                // small arrays, control, slack
+constexpr uint32_t SMEM = SMALL + 1536 + 64 + 1024;                // small arrays, control, slack
 constexpr uint32_t kWaitLimit = 1u << 22;
 static_assert(C * DP * 4 <= 2 * C * CP * 4, "q rows fit over T and X");
-static_assert(4 * C * 4 + 16 <= 1024 + 64, "small arrays and the control block");
+static_assert(6 * C * 4 + 16 <= 1536 + 64, "small arrays and the control block");
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
 
 struct Ctrl {
@@ -1170,7 +1178,9 @@ __global__ void __launch_bounds__(blt::NT, 1)
   float* const s_G = reinterpret_cast<float*>(data + SMALL);       // [C]
   float* const s_beta = s_G + C;                                   // [C]
   float* const s_inv = s_beta + C;                                 // [2C]
-  Ctrl* const ctl = reinterpret_cast<Ctrl*>(s_inv + 2 * C);
+  float* const s_eG = s_inv + 2 * C;                               // [C] exp(G_i)
+  float* const s_eL = s_eG + C;                                    // [C] exp(G_last - G_i)
+  Ctrl* const ctl = reinterpret_cast<Ctrl*>(s_eL + C);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int gc;
@@ -1243,6 +1253,10 @@ __global__ void __launch_bounds__(blt::NT, 1)
   __syncthreads();
   // [K^; Q^] rows into the first operand (float4 pieces of 4 key channels)
   const float Gl = s_G[C - 1];
+  for (int i = tid; i < C; i += NT) {
+    s_eG[i] = expf(s_G[i]);
+    s_eL[i] = expf(Gl - s_G[i]);
+  }
   for (int u = tid; u < 2 * C * (D / 4); u += NT) {
     const int r = u / (D / 4), c = (u % (D / 4)) * 4;
     const int i = r & (C - 1);
@@ -1299,7 +1313,7 @@ __global__ void __launch_bounds__(blt::NT, 1)
   for (int idx = tid; idx < C * D; idx += NT) {
     const int i = idx / D, c = idx % D;
     const float kv = s_k[i * DP + c], qv = s_q[i * DP + c];
-    const float eG = expf(s_G[i]), eL = expf(Gl - s_G[i]);
+    const float eG = s_eG[i], eL = s_eL[i];
     const float ke = tf32_nearest(kv * eL);
     ws.Kt[(unit * C + i) * D + c] = kv * eG;
     ws.Kend[(unit * C + i) * D + c] = ke;
@@ -1324,7 +1338,7 @@ __global__ void __launch_bounds__(blt::NT, 1)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int j = j0 + e;
-      x[e] = which == 0 ? (delta ? s_beta[j] * s_k[j * DP + c] * expf(s_G[j]) : 0.f)
+      x[e] = which == 0 ? (delta ? s_beta[j] * s_k[j * DP + c] * s_eG[j] : 0.f)
                         : s_beta[j] * s_v[j * DP + c];
     }
     *reinterpret_cast<float4*>(data + (which ? A_U : A_W) + (j0 >> 5) * 16384 + tc::sw128_offset(c, (j0 & 31) >> 2)) =

@@ -98,6 +98,7 @@ static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws, bool tc
   w.dM = take(units * C * C);
   w.dgam = take(units * D);
   w.dbr = take(units * C);
+  if (tc) w.pair_fb = reinterpret_cast<int32_t*>(take(slots * P.HK));
   if (wc > 0) {
     // checkpoint entries: sequence b's windows 1 .. ceil(n_b / wc) - 1 at c0_b / wc + w - 1,
     // disjoint between sequences and below max_chunks / wc
@@ -516,7 +517,8 @@ struct BwdPairSmem {
 
 
 template <int D, int C, bool QBF16, bool PERCH>
-__global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace ws, BwdArgs A, ChunkWindow win) {
+__global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace ws, BwdArgs A, ChunkWindow win,
+                                                        int fb_only) {
   constexpr int NT = 256;
   constexpr int IR = C / 16, JC = D / 16;
   constexpr int GW = BwdPairSmem<D, C, PERCH>::GW;
@@ -541,6 +543,8 @@ __global__ void __launch_bounds__(256) bwd_pair_kernel(Problem P, BwdWorkspace w
 
   int gc;
   if (ws.loc.plan.info[1] == 0 || !window_chunk(ws.loc.plan, P.num_seqs, win, blockIdx.x, &gc)) return;
+  // after the tensor-core kernel: only the (chunk, key head) pairs it left here
+  if (fb_only && ws.pair_fb[static_cast<int64_t>(blockIdx.x) * P.HK + blockIdx.y] == 0) return;
   const ChunkInfo ci = ws.loc.plan.chunks[gc];
   const int kh = blockIdx.y, HV = P.HV, ratio = HV / P.HK, tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -858,8 +862,14 @@ static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const 
       r = cudaGetLastError();
     }
     if (r != cudaSuccess) return r;
-    if (kTc && !PERCH) return launch_bwd_pair_tc(P, ws, A, win, slots, st);   // scalar decay
-    pk<<<dim3(slots, P.HK), 256, BwdPairSmem<D, C, PERCH>::bytes, st>>>(P, ws, A, win);
+    if (kTc) {
+      r = launch_bwd_pair_tc(P, ws, A, win, slots, PERCH, st);
+      if (r != cudaSuccess || !PERCH) return r;
+      // per-channel decay: the chunks outside the anchored factors' range, exactly
+      pk<<<dim3(slots, P.HK), 256, BwdPairSmem<D, C, PERCH>::bytes, st>>>(P, ws, A, win, 1);
+      return cudaGetLastError();
+    }
+    pk<<<dim3(slots, P.HK), 256, BwdPairSmem<D, C, PERCH>::bytes, st>>>(P, ws, A, win, 0);
     return cudaGetLastError();
   };
   if (wc == 0) {

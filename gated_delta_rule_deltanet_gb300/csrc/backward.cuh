@@ -31,6 +31,8 @@ struct BwdWorkspace {
   float* dgam;  // [chunk][HV][D]
   float* dbr;   // [chunk][HV][C]
   // bounded workspace (windows of chunk positions; "chunk" above is then a window slot):
+  int32_t* pair_fb;  // [chunk][HK] tensor-core path, per-channel decay: the pairwise terms of
+                     // this (chunk, key head) are left to the CUDA-core kernel
   float* ckpt;  // [entry][HV][D][D] the state entering each window after a sequence's first
   float* carry; // [num_seqs][HV][D][D] the state gradient handed from window to window
 };
@@ -62,10 +64,12 @@ cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const 
 cudaError_t launch_bwd_local_tc(const Problem& P, const SimtWorkspace& ws, ChunkWindow win, int slots,
                                 cudaStream_t st);
 
-// The pairwise terms, dg, dbeta, dq and dk on tensor cores for scalar decay (d = 128, chunk
-// 64, bf16 q/k), as bwd_pair_kernel computes them.
+// The pairwise terms, dg, dbeta, dq and dk on tensor cores (d = 128, chunk 64, bf16 q/k), as
+// bwd_pair_kernel computes them.  Per-channel decay (perch): with factors anchored at each
+// chunk's middle token; a (chunk, key head) whose decay leaves the anchor's range is flagged in
+// ws.pair_fb and left to bwd_pair_kernel.
 cudaError_t launch_bwd_pair_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, ChunkWindow win,
-                               int slots, cudaStream_t st);
+                               int slots, bool perch, cudaStream_t st);
 
 // index of the checkpoint of window w >= 1 of the sequence whose first chunk is c0
 __host__ __device__ __forceinline__ int64_t ckpt_entry(int c0, ChunkWindow win) {

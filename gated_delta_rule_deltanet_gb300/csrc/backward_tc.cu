@@ -1114,10 +1114,372 @@ __global__ void __launch_bounds__(bpt::NT, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
+// Per-channel decay: with the anchor G_a at the chunk's middle token and E+ = exp(G - G_a), the
+// pairwise factor exp(G_ic - G_mc) is E+_ic / E+_mc, so the three products take anchored
+// operands and are rescaled after:
+//
+//   [dM; dA] K-^T          P1 = E+ o (dM K-),  P2 = E+ o (dA K-),   K- = k^ / E+
+//   [dM^T | (b dA)^T] [(q^ E+); (k^ E+)]     P3 = (...) / E+
+//
+// (bwd_pair_kernel's anchored branch, on tensor cores).  A chunk whose decay leaves the anchor's
+// range (80 nats) for some value head of the group is left to bwd_pair_kernel: the CTA records
+// it in ws.pair_fb and writes no dq or dk.
+
+namespace bpc {
+
+constexpr int C = 64, D = 128, NT = 512, DP = D + 4, SP = DP;
+constexpr uint32_t S_Q = 0, S_K = C * DP * 4, S_G = 2 * C * DP * 4;
+constexpr uint32_t OPS = 3 * C * DP * 4;                           // 101376, 1024-aligned
+// first products: [dM; dA] (2 blocks of 128 rows) and K-^T (2 blocks of 128 rows); second:
+// [dM^T | (b dA)^T] (4 blocks of 64 rows + 8 KB under the last M = 128 read) and
+// [(q^ E+)^T; (k^ E+)^T] (4 blocks of 128 rows); then the staged P1, P2, P3
+constexpr uint32_t A12 = OPS, B12 = OPS + 32768;
+constexpr uint32_t A3 = OPS, B3 = OPS + 40960;
+constexpr uint32_t DATA = OPS + 40960 + 65536;                    // 207872
+constexpr uint32_t SMALL = DATA;
+constexpr uint32_t SMEM = DATA + 4096 + 1024;
+constexpr uint32_t kWaitLimit = 1u << 22;
+static_assert(OPS % 1024 == 0, "operand alignment");
+static_assert(3 * C * SP * 4 <= DATA - OPS, "P1-P3 staging fits the operand region");
+static_assert(SMEM <= 227 * 1024, "shared memory budget");
+
+struct Ctrl {
+  uint64_t bar;
+  uint32_t tmem;
+  int bad;
+  int fb;                                                          // a head left the anchor's range
+};
+
+}  // namespace bpc
+
+__global__ void __launch_bounds__(bpc::NT, 1)
+    bwd_pair_tc_pc_kernel(Problem P, BwdWorkspace ws, BwdArgs A, ChunkWindow win) {
+  using namespace bpc;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  const uint32_t pad = (1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u;
+  unsigned char* const data = smem_raw + pad;
+  float* const s_q = reinterpret_cast<float*>(data + S_Q);
+  float* const s_k = reinterpret_cast<float*>(data + S_K);
+  float* const s_G = reinterpret_cast<float*>(data + S_G);        // [C][DP] cumulative log-decay
+  float* const s_b = reinterpret_cast<float*>(data + SMALL);       // [C] beta
+  float* const s_rq = s_b + C;                                     // [C] 1/|q|
+  float* const s_rk = s_rq + C;                                    // [C] 1/|k|
+  float* const s_db = s_rk + C;                                    // [C] dbeta's pairwise part
+  float* const s_ga = s_db + C;                                    // [D] G at the anchor token
+  float* const s_dGl = s_ga + D;                                   // [D] gradient w.r.t. G_last
+  float* const s_gam = s_dGl + D;                                  // [D] exp(G_last)
+  Ctrl* const ctl = reinterpret_cast<Ctrl*>(s_gam + D);
+  constexpr int IR = C * 16 / NT, JC = D / 16;
+
+  int gc;
+  if (ws.loc.plan.info[1] == 0 || !window_chunk(ws.loc.plan, P.num_seqs, win, blockIdx.x, &gc)) return;
+  const ChunkInfo ci = ws.loc.plan.chunks[gc];
+  const int kh = blockIdx.y, HV = P.HV, ratio = HV / P.HK, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const bool delta = !(P.flags & KDA_FLAG_NO_DELTA);
+  const int n = ci.n;
+  const int r0 = (tid / 16) * IR, c0 = (tid % 16) * JC;
+  const bool lead = (tid % 16) == 0;
+  const uint32_t sd = tc::smem_u32(data);
+
+  if (tid == 0) {
+    tc::mbar_init(&ctl->bar, 1);
+    ctl->bad = 0;
+    ctl->fb = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc(&ctl->tmem, 256);
+    tc::tmem_relinquish();
+  }
+  for (int u = tid; u < C * (D / 8); u += NT) {    // q, k rows of the key head (bf16)
+    const int i = u / (D / 8), c = (u % (D / 8)) * 8;
+    float qx[8] = {}, kx[8] = {};
+    if (i < n) {
+      tc::bf16x8_load(reinterpret_cast<const unsigned char*>(
+                          static_cast<const uint16_t*>(P.q) + (ci.t0 + i) * P.q_stride + static_cast<int64_t>(kh) * D + c), qx);
+      tc::bf16x8_load(reinterpret_cast<const unsigned char*>(
+                          static_cast<const uint16_t*>(P.k) + (ci.t0 + i) * P.k_stride + static_cast<int64_t>(kh) * D + c), kx);
+    }
+    st_row(s_q + i * DP + c, qx);
+    st_row(s_k + i * DP + c, kx);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = ctl->tmem;
+  for (int i = warp; i < C; i += NT / 32) {
+    float sq = 0.f, sk = 0.f;
+    for (int c = lane; c < D; c += 32) {
+      sq += s_q[i * DP + c] * s_q[i * DP + c];
+      sk += s_k[i * DP + c] * s_k[i * DP + c];
+    }
+    sq = warp_sum(sq);
+    sk = warp_sum(sk);
+    if (lane == 0) {
+      s_rq[i] = P.l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
+      s_rk[i] = P.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < C * D; idx += NT) {
+    const int i = idx / D, c = idx % D;
+    s_q[i * DP + c] *= s_rq[i] * P.scale;
+    s_k[i * DP + c] *= s_rk[i];
+  }
+
+  float adq[IR][JC], adk[IR][JC];
+#pragma unroll
+  for (int a = 0; a < IR; ++a)
+#pragma unroll
+    for (int b = 0; b < JC; ++b) adq[a][b] = adk[a][b] = 0.f;
+  const uint32_t id = tc::idesc_f16(128, 128, tc::kTF32);
+  uint32_t phase = 0;
+  const int am = (n - 1) / 2;                   // the anchor token
+
+  for (int h = kh * ratio; h < (kh + 1) * ratio; ++h) {
+    const int64_t unit = static_cast<int64_t>(blockIdx.x) * HV + h;
+    __syncthreads();                            // the previous head's staging is read
+    for (int idx = tid; idx < C * D; idx += NT) {
+      const int i = idx / D, c = idx % D;
+      s_G[i * DP + c] = i < n ? P.g[((ci.t0 + i) * HV + h) * D + c] : 0.f;
+    }
+    for (int i = tid; i < C; i += NT) s_b[i] = i < n ? P.beta[(ci.t0 + i) * HV + h] : 0.f;
+    for (int c = tid; c < D; c += NT) s_dGl[c] = 0.f;
+    __syncthreads();
+    if (tid < D) {                              // cumulative log-decay down each channel
+      float acc = 0.f;
+      for (int i = 0; i < C; ++i) {
+        acc += s_G[i * DP + tid];
+        s_G[i * DP + tid] = acc;
+      }
+      s_ga[tid] = s_G[am * DP + tid];
+      s_gam[tid] = expf(acc);
+    }
+    __syncthreads();
+    bool wide = false;
+    for (int idx = tid; idx < C * D; idx += NT) {
+      const int i = idx / D, c = idx % D;
+      wide |= fabsf(s_G[i * DP + c] - s_ga[c]) > kSimtAnchorRange;
+    }
+    if (__syncthreads_or(wide)) {               // left to the exact CUDA-core kernel
+      if (tid == 0) ctl->fb = 1;
+      continue;
+    }
+    // [dM; dA] as stored and K-^T (key channel rows, token columns)
+    for (int idx = tid; idx < C * C; idx += NT) {
+      const int i = idx / C, m = idx % C;
+      const uint32_t cm = (m & 31) >> 2, wm = (m & 3) * 4;
+      *reinterpret_cast<float*>(data + A12 + (m >> 5) * 16384 + tc::sw128_offset(i, cm) + wm) =
+          tf32_nearest(ws.dM[unit * C * C + idx]);
+      *reinterpret_cast<float*>(data + A12 + (m >> 5) * 16384 + tc::sw128_offset(C + i, cm) + wm) =
+          tf32_nearest(ws.dA[unit * C * C + idx]);
+    }
+    for (int idx = tid; idx < C * D; idx += NT) {
+      const int m = idx / D, c = idx % D;
+      const float km = s_k[m * DP + c] * expf(s_ga[c] - s_G[m * DP + c]);
+      *reinterpret_cast<float*>(data + B12 + (m >> 5) * 16384 + tc::sw128_offset(c, (m & 31) >> 2) + (m & 3) * 4) =
+          tf32_nearest(km);
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint64_t da = tc::smem_desc_sw128(sd + A12 + j * 16384, 1024);
+        const uint64_t db = tc::smem_desc_sw128(sd + B12 + j * 16384, 1024);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_ss_tf32(tmem, tc::desc_add(da, 32 * k), tc::desc_add(db, 32 * k), id, (j | k) ? 1u : 0u);
+      }
+      tc::mma_commit(&ctl->bar);
+    }
+    if (!tc::mbar_wait_bounded(&ctl->bar, phase & 1u, kWaitLimit)) ctl->bad = 1;
+    ++phase;
+    tc::fence_after_sync();
+    __syncthreads();                            // the first operands are read
+    // [dM^T | (b dA)^T] and [(q^ E+)^T; (k^ E+)^T]
+    for (int idx = tid; idx < C * C; idx += NT) {
+      const int i = idx / C, m = idx % C;
+      const uint32_t ci2 = (i & 31) >> 2, wi = (i & 3) * 4;
+      *reinterpret_cast<float*>(data + A3 + (i >> 5) * 8192 + tc::sw128_offset(m, ci2) + wi) =
+          tf32_nearest(ws.dM[unit * C * C + idx]);
+      *reinterpret_cast<float*>(data + A3 + (2 + (i >> 5)) * 8192 + tc::sw128_offset(m, ci2) + wi) =
+          tf32_nearest(delta ? s_b[i] * ws.dA[unit * C * C + idx] : 0.f);
+    }
+    for (int idx = tid; idx < C * D; idx += NT) {
+      const int m = idx / D, c = idx % D;
+      const float e = expf(s_G[m * DP + c] - s_ga[c]);
+      const uint32_t off = (m >> 5) * 16384 + tc::sw128_offset(c, (m & 31) >> 2) + (m & 3) * 4;
+      *reinterpret_cast<float*>(data + B3 + off) = tf32_nearest(s_q[m * DP + c] * e);
+      *reinterpret_cast<float*>(data + B3 + 32768 + off) = tf32_nearest(s_k[m * DP + c] * e);
+    }
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+      tc::fence_after_sync();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint64_t da = tc::smem_desc_sw128(sd + A3 + j * 8192, 1024);
+        const uint64_t db = tc::smem_desc_sw128(sd + B3 + j * 16384, 1024);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_ss_tf32(tmem + 128, tc::desc_add(da, 32 * k), tc::desc_add(db, 32 * k), id, (j | k) ? 1u : 0u);
+      }
+      tc::mma_commit(&ctl->bar);
+    }
+    // the contractions' rows of this thread, requested while the second products run
+    float gq[IR][JC], gk[IR][JC], ge[IR][JC];
+#pragma unroll
+    for (int a = 0; a < IR; ++a) {
+      ld_row(gq[a], ws.dQt + unit * C * D + (r0 + a) * D + c0);
+      ld_row(gk[a], ws.dKt + unit * C * D + (r0 + a) * D + c0);
+      ld_row(ge[a], ws.dKe + unit * C * D + (r0 + a) * D + c0);
+    }
+    if (!tc::mbar_wait_bounded(&ctl->bar, phase & 1u, kWaitLimit)) ctl->bad = 1;
+    ++phase;
+    tc::fence_after_sync();
+    float* const s_P1 = reinterpret_cast<float*>(data + OPS);
+    float* const s_P2 = s_P1 + C * SP;
+    float* const s_P3 = s_P2 + C * SP;
+    __syncthreads();                            // the second operands are read
+    {
+      const int qd = warp & 3, ch = warp >> 2;
+      const int row = 32 * qd + lane;
+      const uint32_t la = static_cast<uint32_t>(32 * qd) << 16;
+      float* dst12 = row < C ? s_P1 + row * SP : s_P2 + (row - C) * SP;
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        uint32_t v[16];
+        tc::tmem_ld16(tmem + la + 32 * ch + 16 * jj, v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e += 4)
+          *reinterpret_cast<float4*>(dst12 + 32 * ch + 16 * jj + e) =
+              make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+      }
+      if (qd < 2) {
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          uint32_t v[16];
+          tc::tmem_ld16(tmem + la + 128 + 32 * ch + 16 * jj, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; e += 4)
+            *reinterpret_cast<float4*>(s_P3 + row * SP + 32 * ch + 16 * jj + e) =
+                make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+        }
+      }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    {
+      // the rescaled products and the chain rule; dG_ic in place of P1_ic
+      float gl[JC];
+#pragma unroll
+      for (int b = 0; b < JC; ++b) gl[b] = 0.f;
+#pragma unroll
+      for (int a = 0; a < IR; ++a) {
+        const int i = r0 + a;
+        float p1[JC], p2[JC], p3[JC], qv[JC], kv[JC], gi[JC], ga[JC], glast[JC];
+        ld_row(p1, s_P1 + i * SP + c0);
+        ld_row(p2, s_P2 + i * SP + c0);
+        ld_row(p3, s_P3 + i * SP + c0);
+        ld_row(qv, s_q + i * DP + c0);
+        ld_row(kv, s_k + i * DP + c0);
+        ld_row(gi, s_G + i * DP + c0);
+        ld_row(ga, s_ga + c0);
+        ld_row(glast, s_G + (C - 1) * DP + c0);
+        const float bi = s_b[i];
+        float bl = 0.f, dgr[JC];
+#pragma unroll
+        for (int b = 0; b < JC; ++b) {
+          const float d = gi[b] - ga[b];
+          const float ep = expf(d), em = expf(-d);
+          const float eG = expf(gi[b]), eL = expf(glast[b] - gi[b]);
+          const float q1 = p1[b] * ep, q2 = p2[b] * ep, q3 = p3[b] * em;
+          const float dqt = gq[a][b], dkt = gk[a][b], dke = ge[a][b];
+          adq[a][b] += q1 + dqt * eG;
+          adk[a][b] += bi * q2 + q3 + dkt * eG + dke * eL;
+          dgr[b] = qv[b] * q1 + kv[b] * bi * q2 - kv[b] * q3 + dqt * qv[b] * eG + dkt * kv[b] * eG -
+                   dke * kv[b] * eL;
+          bl += kv[b] * q2;                     // dbeta's pairwise part: sum_c k^_ic P2_ic
+          gl[b] += dke * kv[b] * eL;            // K_end's path into G_last
+        }
+        st_row(s_P1 + i * SP + c0, dgr);
+        bl = halfwarp_sum(bl);
+        if (lead) s_db[i] = bl;
+      }
+#pragma unroll
+      for (int b = 0; b < JC; ++b) atomicAdd(&s_dGl[c0 + b], gl[b]);
+      __syncthreads();
+      if (tid < D) {                            // dg = reverse cumulative sum down each channel
+        float acc = s_dGl[tid] + ws.dgam[unit * D + tid] * s_gam[tid];
+        for (int i = C - 1; i >= 0; --i) {
+          acc += s_P1[i * SP + tid];
+          if (i < n) A.dg[((ci.t0 + i) * HV + h) * D + tid] = acc;
+        }
+      }
+      for (int i = tid; i < n; i += NT)
+        A.dbeta[(ci.t0 + i) * HV + h] = ws.dbr[unit * C + i] + (delta ? s_db[i] : 0.f);
+    }
+  }
+  // a head outside the anchor's range: bwd_pair_kernel redoes the whole chunk and key head
+  __syncthreads();
+  const bool fb = ctl->fb != 0;
+  if (tid == 0) ws.pair_fb[static_cast<int64_t>(blockIdx.x) * P.HK + kh] = fb ? 1 : 0;
+  if (!fb) {
+    const float inv_s = 1.f / P.scale;
+#pragma unroll
+    for (int a = 0; a < IR; ++a) {
+      const int i = r0 + a;
+      float dq = 0.f, dk = 0.f;
+#pragma unroll
+      for (int b = 0; b < JC; ++b) {
+        dq += s_q[i * DP + c0 + b] * adq[a][b];
+        dk += s_k[i * DP + c0 + b] * adk[a][b];
+      }
+      dq = halfwarp_sum(dq);
+      dk = halfwarp_sum(dk);
+      if (i >= n) continue;
+      float oq[JC], ok[JC];
+#pragma unroll
+      for (int b = 0; b < JC; ++b) {
+        if (P.l2norm) {
+          const float uq = s_q[i * DP + c0 + b] * inv_s;
+          oq[b] = P.scale * s_rq[i] * (adq[a][b] - uq * dq * inv_s);
+          ok[b] = s_rk[i] * (adk[a][b] - s_k[i * DP + c0 + b] * dk);
+        } else {
+          oq[b] = P.scale * adq[a][b];
+          ok[b] = adk[a][b];
+        }
+      }
+      const int64_t o = ((ci.t0 + i) * P.HK + kh) * D + c0;
+      st_row(A.dq + o, oq);
+      st_row(A.dk + o, ok);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (ctl->bad && tid == 0) raise_device_error(P.err, KDA_DEVERR_TIMEOUT);
+  if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
 cudaError_t launch_bwd_pair_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, ChunkWindow win,
-                               int slots, cudaStream_t st) {
+                               int slots, bool perch, cudaStream_t st) {
   using namespace bpt;
   if (slots <= 0) return cudaSuccess;
+  if (perch) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_pair_tc_pc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(bpc::SMEM));
+    if (e != cudaSuccess) return e;
+    bwd_pair_tc_pc_kernel<<<dim3(static_cast<unsigned>(slots), P.HK), bpc::NT, bpc::SMEM, st>>>(P, ws, A, win);
+    return cudaGetLastError();
+  }
   cudaError_t e = cudaFuncSetAttribute(bwd_pair_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SMEM));
   if (e != cudaSuccess) return e;

@@ -146,6 +146,22 @@ def test_backward_strong_decay_takes_the_exact_pairwise_path():
     compare(got, ref, TOL["f32"], label="strong decay")
 
 
+def test_backward_tensor_core_path_strong_decay_falls_back_exactly():
+    """bf16, d = 128, chunk 64, per-channel decay strong enough (x40) that some chunks leave the
+    anchored factors' 80-nat range: the tensor-core pairwise kernel leaves those (chunk, key
+    head) pairs to the exact CUDA-core kernel; every gradient still matches the oracle."""
+    p = workloads.make_problem("strong128", num_seqs=2, lengths=[150, 40], num_k_heads=1,
+                               num_v_heads=2, d=128, qkv_dtype="bf16", state_dtype="f32",
+                               decay_kind="per_channel", chunk=64, zero_state=False, num_slots=3,
+                               seed=34)
+    p.g[...] = p.g * 40.0
+    assert float(np.max(-p.g)) * 32 > 80.0
+    d_o, d_state = seeds(p, 15)
+    got = gpu_backward(p, d_o, d_state)
+    ref = oracle.backward(p, d_o.astype(np.float64), d_state.astype(np.float64))
+    compare(got, ref, TOL["bf16"], label="strong decay, tensor-core path")
+
+
 def test_backward_ragged_gqa_workload_sampled():
     """ragged_gqa_kda (8 ragged sequences, 16 key / 32 value heads, bf16 pool): every gradient
     of one key head's two value heads on two sequences; dq and dk of that key head sum both."""

@@ -82,6 +82,7 @@ static size_t bwd_layout(const Problem& P, char* base, BwdWorkspace* ws, bool tc
     w.loc.WT = take(units * D * C);
     w.loc.AqkT = take(units * C * C);
     w.loc.TT = take(units * C * C);
+    w.loc.local_fb = reinterpret_cast<int32_t*>(take(units));
   } else {
     w.loc.Qt = take(units * C * D);
     w.loc.Aqk = take(units * C * C);
@@ -850,8 +851,14 @@ static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const 
   // the chunk-parallel kernels of one window (or of every chunk: wc == 0)
   auto local = [&](ChunkWindow win, int slots) -> cudaError_t {
     if (slots <= 0) return cudaSuccess;
-    if (kTc && !PERCH) return launch_bwd_local_tc(P, ws.loc, win, slots, st);   // scalar decay
-    lk<<<dim3(slots, P.HV), 256, SimtLocalSmem<D, C>::bytes, st>>>(P, ws.loc, win);
+    if (kTc) {
+      cudaError_t r = launch_bwd_local_tc(P, ws.loc, win, slots, PERCH, st);
+      if (r != cudaSuccess || !PERCH) return r;
+      // per-channel decay: the chunks outside the anchored factors' range, exactly
+      lk<<<dim3(slots, P.HV), 256, SimtLocalSmem<D, C>::bytes, st>>>(P, ws.loc, win, 1);
+      return cudaGetLastError();
+    }
+    lk<<<dim3(slots, P.HV), 256, SimtLocalSmem<D, C>::bytes, st>>>(P, ws.loc, win, 0);
     return cudaGetLastError();
   };
   auto contractions = [&](ChunkWindow win, int slots) -> cudaError_t {

@@ -59,10 +59,12 @@ cudaError_t launch_bwd_vc_tc(const Problem& P, const BwdWorkspace& ws, const Bwd
 cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const BwdArgs& A, bool sbf16,
                                 ChunkWindow win, int slots, bool record, cudaStream_t st);
 
-// The chunk-local stage on tensor cores for scalar decay (d = 128, chunk 64, bf16 q/k/v):
-// the workspace arrays simt_local_kernel writes for the tensor-core scans.
+// The chunk-local stage on tensor cores (d = 128, chunk 64, bf16 q/k/v): the workspace arrays
+// simt_local_kernel writes for the tensor-core scans.  Per-channel decay (perch): with factors
+// anchored at each chunk's middle token; a chunk whose decay leaves the anchor's range is
+// flagged in ws.local_fb and left to simt_local_kernel.
 cudaError_t launch_bwd_local_tc(const Problem& P, const SimtWorkspace& ws, ChunkWindow win, int slots,
-                                cudaStream_t st);
+                                bool perch, cudaStream_t st);
 
 // The pairwise terms, dg, dbeta, dq and dk on tensor cores (d = 128, chunk 64, bf16 q/k), as
 // bwd_pair_kernel computes them.  Per-channel decay (perch): with factors anchored at each

@@ -1510,10 +1510,11 @@ constexpr uint32_t OPS = 2 * C * DP * 4;                            // 67584, 10
 constexpr uint32_t A_W = OPS, A_U = OPS + 32768, B_T = OPS + 65536;
 constexpr uint32_t S_A = OPS + 81920, S_AQ = S_A + C * CP * 4, S_T = S_AQ + C * CP * 4,
                    S_X = S_T + C * CP * 4, SMALL = S_X + C * CP * 4;
-constexpr uint32_t SMEM = SMALL + 1536 + 64 + 1024;                // small arrays, control, slack
+constexpr uint32_t SMEM = SMALL + 3072 + 64 + 1024;                // small arrays, control, slack
 constexpr uint32_t kWaitLimit = 1u << 22;
 static_assert(C * DP * 4 <= 2 * C * CP * 4, "q rows fit over T and X");
-static_assert(6 * C * 4 + 16 <= 1536 + 64, "small arrays and the control block");
+static_assert((6 * C + 3 * D) * 4 + 16 <= 3072 + 64, "small arrays and the control block");
+static_assert(4 * 8192 <= 2 * C * CP * 4 && S_A % 1024 == 0, "K- operand over A_kk and A_qk");
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
 
 struct Ctrl {
@@ -1524,6 +1525,11 @@ struct Ctrl {
 
 }  // namespace blt
 
+// PERCH: per-channel decay with factors anchored at the chunk's middle token, K+ = k^ E+,
+// Q+ = q^ E+, K- = k^ / E+ (E+ = exp(G - G_a)): [K+; Q+] K-^T carries the pairwise decay
+// exp(G_ic - G_jc) inside the product (simt_local_kernel's anchored branch).  A chunk whose decay
+// leaves the anchor's range (80 nats) is flagged in ws.local_fb and left to simt_local_kernel.
+template <bool PERCH>
 __global__ void __launch_bounds__(blt::NT, 1)
     bwd_local_tc_kernel(Problem P, SimtWorkspace ws, ChunkWindow win) {
   using namespace blt;
@@ -1531,7 +1537,8 @@ __global__ void __launch_bounds__(blt::NT, 1)
   const uint32_t pad = (1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u;
   unsigned char* const data = smem_raw + pad;
   float* const s_k = reinterpret_cast<float*>(data + S_K);
-  float* const s_v = reinterpret_cast<float*>(data + S_V);
+  float* const s_v = reinterpret_cast<float*>(data + S_V);          // scalar: v rows
+  float* const s_Gc = reinterpret_cast<float*>(data + S_V);         // per channel: G, then K-
   float* const s_q = reinterpret_cast<float*>(data + S_T);          // until A_qk is formed
   float* const s_A = reinterpret_cast<float*>(data + S_A);
   float* const s_Aq = reinterpret_cast<float*>(data + S_AQ);
@@ -1542,7 +1549,10 @@ __global__ void __launch_bounds__(blt::NT, 1)
   float* const s_inv = s_beta + C;                                 // [2C]
   float* const s_eG = s_inv + 2 * C;                               // [C] exp(G_i)
   float* const s_eL = s_eG + C;                                    // [C] exp(G_last - G_i)
-  Ctrl* const ctl = reinterpret_cast<Ctrl*>(s_eL + C);
+  float* const s_ga = s_eL + C;                                    // [D] per channel: G_a
+  float* const s_eA = s_ga + D;                                    // [D] exp(G_a)
+  float* const s_eLA = s_eA + D;                                   // [D] exp(G_last - G_a)
+  Ctrl* const ctl = reinterpret_cast<Ctrl*>(s_eLA + D);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int gc;
@@ -1563,7 +1573,7 @@ __global__ void __launch_bounds__(blt::NT, 1)
     tc::tmem_alloc(&ctl->tmem, 256);
     tc::tmem_relinquish();
   }
-  for (int u = tid; u < C * (D / 8); u += NT) {    // k, q (key head), v (value head), bf16
+  for (int u = tid; u < C * (D / 8); u += NT) {    // k, q (key head), v or g (value head)
     const int i = u / (D / 8), c = (u % (D / 8)) * 8;
     float kx[8] = {}, qx[8] = {}, vx[8] = {};
     if (i < n) {
@@ -1572,8 +1582,14 @@ __global__ void __launch_bounds__(blt::NT, 1)
                                                               static_cast<int64_t>(kh) * D + c), kx);
       tc::bf16x8_load(reinterpret_cast<const unsigned char*>(static_cast<const uint16_t*>(P.q) + t * P.q_stride +
                                                               static_cast<int64_t>(kh) * D + c), qx);
-      tc::bf16x8_load(reinterpret_cast<const unsigned char*>(static_cast<const uint16_t*>(P.v) + t * P.v_stride +
-                                                              static_cast<int64_t>(h) * D + c), vx);
+      if constexpr (PERCH) {                    // log-decay: 4-byte aligned, so scalar loads
+        const float* gp = P.g + (t * HV + h) * D + c;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) vx[e] = gp[e];
+      } else {
+        tc::bf16x8_load(reinterpret_cast<const unsigned char*>(static_cast<const uint16_t*>(P.v) + t * P.v_stride +
+                                                                static_cast<int64_t>(h) * D + c), vx);
+      }
     }
     st_row(s_k + i * DP + c, kx);
     st_row(s_q + i * DP + c, qx);
@@ -1582,7 +1598,7 @@ __global__ void __launch_bounds__(blt::NT, 1)
   for (int i = tid; i < C; i += NT) {
     const bool live = i < n;
     s_beta[i] = live ? P.beta[(t0 + i) * HV + h] : 0.f;
-    s_G[i] = live ? P.g[(t0 + i) * HV + h] : 0.f;
+    if (!PERCH) s_G[i] = live ? P.g[(t0 + i) * HV + h] : 0.f;
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1601,7 +1617,7 @@ __global__ void __launch_bounds__(blt::NT, 1)
       s_inv[C + i] = (P.l2norm ? rsqrtf(sq + 1e-6f) : 1.f) * P.scale;
     }
   }
-  if (warp == 0) {                              // inclusive cumulative log-decay, two rows a lane
+  if (!PERCH && warp == 0) {                    // inclusive cumulative log-decay, two rows a lane
     const float a = s_G[2 * lane], b = s_G[2 * lane + 1];
     float inc = a + b;
 #pragma unroll
@@ -1612,43 +1628,90 @@ __global__ void __launch_bounds__(blt::NT, 1)
     s_G[2 * lane] = inc - b;
     s_G[2 * lane + 1] = inc;
   }
+  if (PERCH && tid < D) {                       // down each channel; the anchor's factors
+    float acc = 0.f;
+    for (int i = 0; i < C; ++i) {
+      acc += s_Gc[i * DP + tid];
+      s_Gc[i * DP + tid] = acc;
+    }
+    const float ga = s_Gc[((n - 1) / 2) * DP + tid];
+    s_ga[tid] = ga;
+    s_eA[tid] = expf(ga);
+    s_eLA[tid] = expf(acc - ga);
+    ws.gamma[unit * D + tid] = expf(acc);
+  }
   __syncthreads();
-  // [K^; Q^] rows into the first operand (float4 pieces of 4 key channels)
+  if constexpr (PERCH) {                        // out of the anchor's range: the exact kernel
+    bool wide = false;
+    for (int idx = tid; idx < C * D; idx += NT)
+      wide |= fabsf(s_Gc[(idx / D) * DP + idx % D] - s_ga[idx % D]) > kSimtAnchorRange;
+    wide = __syncthreads_or(wide);
+    if (tid == 0) ws.local_fb[unit] = wide ? 1 : 0;
+    if (wide) {
+      tc::fence_before_sync();
+      __syncthreads();
+      tc::fence_after_sync();
+      if (warp == 0) tc::tmem_dealloc(tmem, 256);
+      return;
+    }
+  }
+  // [K^; Q^] (per channel [K+; Q+]) rows into the first operand, float4 pieces of 4 key
+  // channels; per channel also K- into the second operand over A_kk and A_qk
   const float Gl = s_G[C - 1];
-  for (int i = tid; i < C; i += NT) {
-    s_eG[i] = expf(s_G[i]);
-    s_eL[i] = expf(Gl - s_G[i]);
+  if (!PERCH)
+    for (int i = tid; i < C; i += NT) {
+      s_eG[i] = expf(s_G[i]);
+      s_eL[i] = expf(Gl - s_G[i]);
+    }
+  for (int u = tid; u < C * (D / 4); u += NT) {
+    const int i = u / (D / 4), c = (u % (D / 4)) * 4;
+    float4 k4 = *reinterpret_cast<float4*>(s_k + i * DP + c);
+    float4 q4 = *reinterpret_cast<float4*>(s_q + i * DP + c);
+    const float sk = s_inv[i], sq = s_inv[C + i];
+    float kx[4] = {k4.x * sk, k4.y * sk, k4.z * sk, k4.w * sk};
+    float qx[4] = {q4.x * sq, q4.y * sq, q4.z * sq, q4.w * sq};
+    if constexpr (PERCH) {
+      float km[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float d = s_Gc[i * DP + c + e] - s_ga[c + e];
+        const float ep = expf(d), em = expf(-d);
+        km[e] = kx[e] * em;
+        kx[e] *= ep;
+        qx[e] *= ep;
+      }
+      *reinterpret_cast<float4*>(s_Gc + i * DP + c) = make_float4(km[0], km[1], km[2], km[3]);
+      *reinterpret_cast<float4*>(data + S_A + (c >> 5) * 8192 + tc::sw128_offset(i, (c & 31) >> 2)) =
+          make_float4(tf32_nearest(km[0]), tf32_nearest(km[1]), tf32_nearest(km[2]), tf32_nearest(km[3]));
+    }
+    *reinterpret_cast<float4*>(s_k + i * DP + c) = make_float4(kx[0], kx[1], kx[2], kx[3]);
+    *reinterpret_cast<float4*>(s_q + i * DP + c) = make_float4(qx[0], qx[1], qx[2], qx[3]);
+    *reinterpret_cast<float4*>(data + OPS + (c >> 5) * 16384 + tc::sw128_offset(i, (c & 31) >> 2)) =
+        make_float4(tf32_nearest(kx[0]), tf32_nearest(kx[1]), tf32_nearest(kx[2]), tf32_nearest(kx[3]));
+    *reinterpret_cast<float4*>(data + OPS + (c >> 5) * 16384 + tc::sw128_offset(C + i, (c & 31) >> 2)) =
+        make_float4(tf32_nearest(qx[0]), tf32_nearest(qx[1]), tf32_nearest(qx[2]), tf32_nearest(qx[3]));
   }
-  for (int u = tid; u < 2 * C * (D / 4); u += NT) {
-    const int r = u / (D / 4), c = (u % (D / 4)) * 4;
-    const int i = r & (C - 1);
-    float* src = (r < C ? s_k : s_q) + i * DP + c;
-    float4 x = *reinterpret_cast<float4*>(src);
-    const float sc = s_inv[(r < C ? 0 : C) + i];
-    x.x *= sc; x.y *= sc; x.z *= sc; x.w *= sc;
-    *reinterpret_cast<float4*>(src) = x;
-    *reinterpret_cast<float4*>(data + OPS + (c >> 5) * 16384 + tc::sw128_offset(r, (c & 31) >> 2)) =
-        make_float4(tf32_nearest(x.x), tf32_nearest(x.y), tf32_nearest(x.z), tf32_nearest(x.w));
-  }
-  for (int c = tid; c < D; c += NT) ws.gamma[unit * D + c] = expf(Gl);
+  if (!PERCH)
+    for (int c = tid; c < D; c += NT) ws.gamma[unit * D + c] = expf(Gl);
   tc::fence_async_smem();
   tc::fence_before_sync();
   __syncthreads();
-  if (tid == 0) {                               // [K^; Q^] K^T: K^ is the operand's rows 0-63
+  if (tid == 0) {                               // [K^; Q^] K^T (K^ the operand's rows 0-63), or [K+; Q+] K-^T
     tc::fence_after_sync();
     const uint32_t id = tc::idesc_f16(128, 64, tc::kTF32);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const uint64_t da = tc::smem_desc_sw128(sd + OPS + j * 16384, 1024);
+      const uint64_t db = PERCH ? tc::smem_desc_sw128(sd + S_A + j * 8192, 1024) : da;
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        tc::mma_ss_tf32(tmem, tc::desc_add(da, 32 * k), tc::desc_add(da, 32 * k), id, (j | k) ? 1u : 0u);
+        tc::mma_ss_tf32(tmem, tc::desc_add(da, 32 * k), tc::desc_add(db, 32 * k), id, (j | k) ? 1u : 0u);
     }
     tc::mma_commit(&ctl->bar);
   }
   if (!tc::mbar_wait_bounded(&ctl->bar, 0, kWaitLimit)) ctl->bad = 1;
   tc::fence_after_sync();
-  // A_kk and A_qk from the products: the decay exp(G_i - G_j), beta and the masks
+  // A_kk and A_qk from the products: the decay exp(G_i - G_j) (scalar), beta and the masks
   const int qd = warp & 3, ch = warp >> 2;
   const int row = 32 * qd + lane;               // TMEM lane
   const uint32_t la = static_cast<uint32_t>(32 * qd) << 16;
@@ -1657,13 +1720,13 @@ __global__ void __launch_bounds__(blt::NT, 1)
     tc::tmem_ld16(tmem + la + CW * ch, v0);
     tc::tmem_wait_ld();
     const int i = row & (C - 1);
-    const float Gi = s_G[i], bi = s_beta[i];
+    const float Gi = PERCH ? 0.f : s_G[i], bi = s_beta[i];
     float* dst = (row < C ? s_A : s_Aq) + i * CP + CW * ch;
 #pragma unroll
     for (int e = 0; e < CW; ++e) {
       const int j = CW * ch + e;
       const float x = __uint_as_float(v0[e]);
-      const float dec = j <= i ? expf(Gi - s_G[j]) : 0.f;
+      const float dec = j <= i ? (PERCH ? 1.f : expf(Gi - s_G[j])) : 0.f;
       dst[e] = row < C ? ((delta && j < i) ? bi * x * dec : 0.f) : x * dec;
     }
   }
@@ -1674,9 +1737,10 @@ __global__ void __launch_bounds__(blt::NT, 1)
   float* const stg_qt = stg_kt + D * (C + 1);
   for (int idx = tid; idx < C * D; idx += NT) {
     const int i = idx / D, c = idx % D;
+    // K~ = k^ exp(G), K_end = k^ exp(G_last - G), Q~ = q^ exp(G); per channel from K+, K-, Q+
     const float kv = s_k[i * DP + c], qv = s_q[i * DP + c];
-    const float eG = s_eG[i], eL = s_eL[i];
-    const float ke = tf32_nearest(kv * eL);
+    const float eG = PERCH ? s_eA[c] : s_eG[i];
+    const float ke = tf32_nearest(PERCH ? s_Gc[i * DP + c] * s_eLA[c] : kv * s_eL[i]);
     ws.Kt[(unit * C + i) * D + c] = kv * eG;
     ws.Kend[(unit * C + i) * D + c] = ke;
     stg_kt[c * (C + 1) + i] = ke;
@@ -1700,8 +1764,15 @@ __global__ void __launch_bounds__(blt::NT, 1)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int j = j0 + e;
-      x[e] = which == 0 ? (delta ? s_beta[j] * s_k[j * DP + c] * s_eG[j] : 0.f)
-                        : s_beta[j] * s_v[j * DP + c];
+      float vj;
+      if constexpr (PERCH)                      // the value rows straight from global memory
+        vj = (which == 1 && j < n) ? bf16_bits_to_f32(static_cast<const uint16_t*>(P.v)[(t0 + j) * P.v_stride +
+                                                                                     static_cast<int64_t>(h) * D + c])
+                                   : 0.f;
+      else
+        vj = s_v[j * DP + c];
+      x[e] = which == 0 ? (delta ? s_beta[j] * s_k[j * DP + c] * (PERCH ? s_eA[c] : s_eG[j]) : 0.f)
+                        : s_beta[j] * vj;
     }
     *reinterpret_cast<float4*>(data + (which ? A_U : A_W) + (j0 >> 5) * 16384 + tc::sw128_offset(c, (j0 & 31) >> 2)) =
         make_float4(tf32_nearest(x[0]), tf32_nearest(x[1]), tf32_nearest(x[2]), tf32_nearest(x[3]));
@@ -1775,13 +1846,13 @@ __global__ void __launch_bounds__(blt::NT, 1)
 }
 
 cudaError_t launch_bwd_local_tc(const Problem& P, const SimtWorkspace& ws, ChunkWindow win, int slots,
-                                cudaStream_t st) {
+                                bool perch, cudaStream_t st) {
   using namespace blt;
   if (slots <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(bwd_local_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(SMEM));
+  auto k = perch ? bwd_local_tc_kernel<true> : bwd_local_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
   if (e != cudaSuccess) return e;
-  bwd_local_tc_kernel<<<dim3(static_cast<unsigned>(slots), P.HV), NT, SMEM, st>>>(P, ws, win);
+  k<<<dim3(static_cast<unsigned>(slots), P.HV), NT, SMEM, st>>>(P, ws, win);
   return cudaGetLastError();
 }
 

@@ -140,7 +140,7 @@ static cudaError_t launch_simt_t(const Problem& P, const SimtWorkspace& ws, cuda
   cudaError_t e = cudaFuncSetAttribute(lk, cudaFuncAttributeMaxDynamicSharedMemorySize, lbytes);
   if (e != cudaSuccess) return e;
   if (mc > 0) {
-    lk<<<dim3(mc, P.HV), 256, lbytes, st>>>(P, ws, ChunkWindow{0, 0});
+    lk<<<dim3(mc, P.HV), 256, lbytes, st>>>(P, ws, ChunkWindow{0, 0}, 0);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   stages.mark(2, st);

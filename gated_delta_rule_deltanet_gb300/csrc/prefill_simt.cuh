@@ -23,6 +23,8 @@ struct SimtWorkspace {
   float* WT;    // [chunk][HV][D][C]
   float* AqkT;  // [chunk][HV][C][C]
   float* TT;    // [chunk][HV][C][C]
+  int32_t* local_fb;  // [chunk][HV] per-channel decay, tensor-core path: this chunk's decay left
+                      // the anchored factors' range and the CUDA-core stage computes it
 };
 
 // 16-byte vector moves of N floats between registers and 16-byte aligned memory (scalar when
@@ -128,7 +130,8 @@ constexpr float kSimtAnchorRange = 80.f;
 template <int D, int C, bool QBF16, bool PERCH>
 // win: the chunks of one window of positions (the backward's bounded workspace), each in the
 // workspace slot of its window; {0, 0} for every chunk in its own slot.
-__global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspace ws, ChunkWindow win) {
+__global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspace ws, ChunkWindow win,
+                                                          int fb_only) {
   constexpr int NT = 256;
   constexpr int DP = SimtLocalSmem<D, C>::DP;
   constexpr int CP = SimtLocalSmem<D, C>::CP;
@@ -151,6 +154,8 @@ __global__ void __launch_bounds__(256) simt_local_kernel(Problem P, SimtWorkspac
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   int gc;
   if (ws.plan.info[1] == 0 || !window_chunk(ws.plan, P.num_seqs, win, blockIdx.x, &gc)) return;
+  // after the tensor-core local stage: only the chunks it left here
+  if (fb_only && ws.local_fb[static_cast<int64_t>(blockIdx.x) * P.HV + blockIdx.y] == 0) return;
   const ChunkInfo ci = ws.plan.chunks[gc];
   const int h = blockIdx.y;
   const int HV = P.HV;

@@ -798,7 +798,9 @@ def profile_arm(args):
     torch.cuda.set_device(dev)
     kda.load()
     if args.profile == "prefill":
-        ms = time_prefill(workloads.workload(args.workload), dev, args.steps, args.warmup)[0]
+        ms, stage_ms, _, _, stages, _ = time_prefill(workloads.workload(args.workload), dev, args.steps,
+                                                     args.warmup)
+        print("stages: " + ", ".join(f"{n} {m:.4f} ms" for (n, _), m in zip(stages, stage_ms)))
     elif args.profile == "decode":
         ms = time_decode(workloads.workload("kda_decode"), dev, args.steps, args.warmup)
     elif args.profile == "backward":

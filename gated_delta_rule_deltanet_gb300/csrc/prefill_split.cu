@@ -1124,6 +1124,10 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
     __threadfence_block();
     *reinterpret_cast<volatile int*>(flag) = value;
   };
+  // for the output warps' flags: they publish no data (an MMA seen complete through its
+  // barrier, or tensor-memory reads fenced and synchronised before), and a CTA fence there
+  // would wait for the previous chunk's o stores to global memory
+  auto note_flag = [&](int* flag, int value) { *reinterpret_cast<volatile int*>(flag) = value; };
   auto wait_bar = [&](uint64_t* bar, uint32_t parity) -> bool {   // bounded
     for (uint32_t i = 0; i < kWaitLimit; ++i) {
       if (tc::mbar_try_wait(bar, parity)) {
@@ -1253,7 +1257,7 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
     for (uint32_t c = 0; c < nchunks; ++c) {
       const bool bad = !wait_bar(&s_bar_o, c & 1);
       if (tc::named_sync_or(3, NTO, bad || aborted())) break;
-      if (dq == 0) set_flag(&s_o_done, static_cast<int>(c) + 1);
+      if (dq == 0) note_flag(&s_o_done, static_cast<int>(c) + 1);
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {          // 16 columns of both partial sums
         uint32_t r0[16], r1[16];
@@ -1270,7 +1274,7 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
       }
       tc::fence_before_sync();
       tc::named_sync(3, NTO);
-      if (dq == 0) set_flag(&s_o_free, static_cast<int>(c) + 1);
+      if (dq == 0) note_flag(&s_o_free, static_cast<int>(c) + 1);
       // thread dq stores columns 4 (dq % 16) .. + 3 of rows dq / 16 + 4 k: one pointer step
       // per row group, the partial-chunk test hoisted out of the full chunks
       const int64_t t0 = static_cast<int64_t>(bos) + static_cast<int64_t>(c) * C;
@@ -1359,6 +1363,7 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
           tc::mma_commit(&s_bar_x);
         }
       }
+      __syncwarp();                             // the other lanes wait here, not beside the issuer
       if (extract) {                            // E' = V - K~ S over V's slot
         bad = bad || !wait_bar(&s_bar_x, c & 1);
         bad = bad || !wait_flag(&s_ready, static_cast<int>(c) + 1);   // V(c), Kb(c)
@@ -1397,6 +1402,7 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
                        s > 2 * part);
           tc::mma_commit(&s_bar_s);
         }
+        __syncwarp();
       }
       bad = bad || !wait_bar(&s_bar_s, c & 1);
       bad = bad || !wait_flag(&s_ready, static_cast<int>(c) + 1);     // gamma(c)

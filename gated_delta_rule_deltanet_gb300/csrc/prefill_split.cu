@@ -1247,7 +1247,15 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
       tc::fence_async_smem();
       tc::fence_before_sync();
       tc::named_sync(2, NTD);
-      if (dt == 0) set_flag(&s_ready, static_cast<int>(q) + 1);
+      if (dt == 0) {
+        // one flag for the compute warps: V(q), Kb(q) and gamma(q) are in place, and the X MMA
+        // of chunk q may start -- its [K~; Q~] has landed and the o rows of chunk q - 2, which
+        // shared its X buffer, are out.  A failed wait stops the group at its next barrier.
+        if (wait_bar(&s_kqa_bar[q % KQA_SLOTS], (q / KQA_SLOTS) & 1) &&
+            (q < 2 || wait_flag(&s_o_free, static_cast<int>(q) - 1)))
+          set_flag(&s_ready, static_cast<int>(q) + 1);
+      }
+      __syncwarp();
     }
     tc::cp_async_wait_all();
   } else if (warp >= W_OUT) {
@@ -1350,9 +1358,8 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
     for (uint32_t c = 0; c < nchunks && !stop; ++c) {
       bool bad = false;
       if ((tid & 127) == 0) {                   // X = [K~; Q~] S, K half `part`
-        // [K~; Q~ | A1o](c) in place; X(c & 1) free once the o rows of chunk c - 2 are out
-        bad = !wait_bar(&s_kqa_bar[c % KQA_SLOTS], (c / KQA_SLOTS) & 1);
-        bad = bad || (c >= 2 && !wait_flag(&s_o_free, static_cast<int>(c) - 1));
+        // ready(c + 1): [K~; Q~ | A1o](c) in place, X(c & 1) free, V(c) and Kb(c) in place
+        bad = !wait_flag(&s_ready, static_cast<int>(c) + 1);
         if (!bad) {
           tc::fence_after_sync();
           const uint64_t da = tc::desc_add(dKQ0, (c % KQA_SLOTS) * KQA_BYTES);
@@ -1365,8 +1372,9 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
       }
       __syncwarp();                             // the other lanes wait here, not beside the issuer
       if (extract) {                            // E' = V - K~ S over V's slot
+        // V(c), Kb(c): the issuing threads saw ready(c + 1) above; the rest look while X runs
+        if ((tid & 127) != 0) bad = bad || !wait_flag(&s_ready, static_cast<int>(c) + 1);
         bad = bad || !wait_bar(&s_bar_x, c & 1);
-        bad = bad || !wait_flag(&s_ready, static_cast<int>(c) + 1);   // V(c), Kb(c)
         bad = __any_sync(0xffffffffu, bad);     // tcgen05.ld is warp-collective
         if (!bad) {
           unsigned char* vp = smem + v_off(c);
@@ -1404,8 +1412,9 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
         }
         __syncwarp();
       }
+      // gamma(c): the E' threads saw ready(c + 1) above; the rest look while Kb E' runs
+      if (!extract) bad = bad || !wait_flag(&s_ready, static_cast<int>(c) + 1);
       bad = bad || !wait_bar(&s_bar_s, c & 1);
-      bad = bad || !wait_flag(&s_ready, static_cast<int>(c) + 1);     // gamma(c)
       bad = __any_sync(0xffffffffu, bad);
       if (!bad) {
         if (tid == 0) set_flag(&s_ps_done, static_cast<int>(c) + 1);

@@ -807,7 +807,8 @@ def profile_arm(args):
         ms = time_prefill_bwd(workloads.workload(args.workload), dev, args.steps, args.warmup,
                               compact=args.compact)[0]
     else:
-        ms = time_verify(dev, args.steps, args.warmup)[1]
+        _, ms, vstage, _ = time_verify(dev, args.steps, args.warmup)
+        print("stages: " + ", ".join(f"{n} {m:.4f} ms" for n, m in vstage.items()))
     print(f"profile {args.profile}: {args.warmup} + {args.steps} steps, {ms:.4f} ms per step")
 
 

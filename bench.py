@@ -97,10 +97,17 @@ PREFILL_STAGES = {
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a kernel on a
 # workload, from an ncu capture of the kernel as it is built now (see profiles/); a kernel
 # without a capture of its current build has no entry and is reported as null.
+# The prefill entries: launches 7 and 8 of
+#   ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum --clock-control none
+#       -k regex:"tc_front|tc_chain" -s 6 -c 2 python bench.py --profile prefill --workload W --steps 1 --warmup 3
 NCU_TRAFFIC = {("decode_step", "kda_decode"): 547441408 + 480736768,
                ("verify_window", "kda_verify"): 579015936 + 57849088,
                ("fold_accepted", "kda_verify"): 453014272 + 364333056,
-               ("conv_kernel", "gdn_prefill"): 358.74e6}
+               ("conv_kernel", "gdn_prefill"): 358.74e6,
+               ("tc_front", "kda_prefill"): 1165454080 + 906119680,
+               ("tc_chain", "kda_prefill"): 1220652032 + 508882944,
+               ("tc_front", "gdn_prefill"): 138534144 + 181688320,
+               ("tc_chain", "gdn_prefill"): 308346368 + 107801856}
 
 
 def load_peaks() -> dict:

@@ -285,12 +285,6 @@ __device__ __forceinline__ void bulk_load(uint32_t sdst, const void* gsrc, uint3
       : "memory");
 }
 
-// L2 prefetch of `bytes` (multiple of 16, 16-byte aligned) of global memory: no shared memory
-// and no barrier involved
-__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
-}
-
 // L2 prefetch of one box of a tiled tensor map: no shared memory and no barrier involved
 __device__ __forceinline__ void tma_prefetch_3d(const void* map, int32_t x, int32_t y, int32_t z) {
   asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(x),

@@ -13,6 +13,7 @@ size_t plan_layout(const Problem& P, char* base, size_t off, PlanView* out) {
   v.info = reinterpret_cast<int32_t*>(take(4 * sizeof(int32_t)));
   v.seq_chunk0 = reinterpret_cast<int32_t*>(take((static_cast<size_t>(P.num_seqs) + 1) * 4));
   v.chunks = reinterpret_cast<ChunkInfo*>(take(static_cast<size_t>(plan_max_chunks(P)) * sizeof(ChunkInfo)));
+  v.seq_order = reinterpret_cast<int32_t*>(take(static_cast<size_t>(P.num_seqs) * sizeof(int32_t)));
   v.skip = reinterpret_cast<int32_t*>(take(static_cast<size_t>(P.num_seqs) * P.HV * sizeof(int32_t)));
   if (out) *out = v;
   return off;
@@ -23,6 +24,7 @@ constexpr int kPlanThreads = 1024;
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem P, PlanView plan, int max_chunks) {
   __shared__ int s_bad, s_longest;
   __shared__ int s_scan[kPlanThreads];
+  __shared__ int s_n[kPlanThreads];            // chunks per sequence (B <= kPlanThreads)
   const int B = P.num_seqs, C = P.chunk, tid = threadIdx.x;
   if (tid == 0) {
     s_bad = 0;
@@ -79,6 +81,20 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem P, PlanView 
   const int total = s_scan[kPlanThreads - 1];
   if (tid == kPlanThreads - 1) plan.seq_chunk0[B] = total;
   __syncthreads();                              // the first chunk of every sequence is written
+  // the sequences by decreasing chunk count: a sequence's rank is the number of sequences with
+  // more chunks, or as many and a lower index
+  if (B <= kPlanThreads) {
+    if (tid < B) s_n[tid] = plan.seq_chunk0[tid + 1] - plan.seq_chunk0[tid];
+    __syncthreads();
+    if (tid < B) {
+      const int nb = s_n[tid];
+      int r = 0;
+      for (int j = 0; j < B; ++j) r += (s_n[j] > nb) || (s_n[j] == nb && j < tid);
+      plan.seq_order[r] = tid;
+    }
+  } else {
+    for (int b = tid; b < B; b += kPlanThreads) plan.seq_order[b] = b;
+  }
   // one table entry per thread and step: its sequence by binary search over the first chunks
   // (an empty sequence shares its first chunk with the next one)
   for (int g = tid; g < min(total, max_chunks); g += kPlanThreads) {

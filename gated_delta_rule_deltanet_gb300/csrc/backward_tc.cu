@@ -339,7 +339,8 @@ __global__ void __launch_bounds__(bst::NT, 1)
   unsigned char* const data = smem_raw + pad;
   Ctrl* const ctl = reinterpret_cast<Ctrl*>(pad >= CTRL_BYTES ? smem_raw : data + F_DATA);
   if (ws.loc.plan.info[1] == 0) return;
-  const int b = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
+  const SeqHeadTile cta = seq_head_tile(ws.loc.plan, P.HV, D / BV);
+  const int b = cta.b, h = cta.h, v0 = cta.vt * BV;
   const int HV = P.HV, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // this CTA's chunks: the sequence's, or those of window win.w (slots b * wc ..)
   const int c0 = ws.loc.plan.seq_chunk0[b], nb = ws.loc.plan.seq_chunk0[b + 1] - c0;
@@ -529,7 +530,8 @@ __global__ void __launch_bounds__(bst::NT, 1)
   unsigned char* const data = smem_raw + pad;
   Ctrl* const ctl = reinterpret_cast<Ctrl*>(pad >= CTRL_BYTES ? smem_raw : data + R_DATA);
   if (ws.loc.plan.info[1] == 0) return;
-  const int b = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
+  const SeqHeadTile cta = seq_head_tile(ws.loc.plan, P.HV, D / BV);
+  const int b = cta.b, h = cta.h, v0 = cta.vt * BV;
   const int HV = P.HV, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c0 = ws.loc.plan.seq_chunk0[b], nb = ws.loc.plan.seq_chunk0[b + 1] - c0;
   const int j0 = win.wc ? win.w * win.wc : 0, j1 = win.wc ? min(nb, j0 + win.wc) : nb;
@@ -772,7 +774,8 @@ cudaError_t launch_bwd_scans_tc(const Problem& P, const BwdWorkspace& ws, const 
       !encode_f32_blocks(&ttt, ws.loc.TT, units * C, C, C, C) ||
       !encode_f32_blocks(&twt, ws.loc.WT, units * D, C, C, D))
     return cudaErrorNotSupported;
-  const dim3 grid(P.num_seqs, P.HV, D / BV);
+  const unsigned grid = seq_head_tile_ctas(P, D / BV);
+  if (grid == 0) return cudaErrorInvalidConfiguration;
   auto fk = sbf16 ? bwd_fwd_scan_tc_kernel<true> : bwd_fwd_scan_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(F_DATA + 1024));

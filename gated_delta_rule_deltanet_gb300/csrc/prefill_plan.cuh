@@ -51,6 +51,22 @@ __device__ __forceinline__ bool window_chunk(const PlanView& plan, int num_seqs,
   return c < plan.seq_chunk0[b + 1];
 }
 
+// The per-sequence scans (one CTA per sequence, value head and value tile) run on a 1-D grid of
+// B x HV x NVT CTAs, taken in the plan's order of decreasing sequence length: CTAs start in
+// linear order, so the longest scans start first and the short ones fill in behind them.
+struct SeqHeadTile {
+  int b, h, vt;
+};
+__device__ __forceinline__ SeqHeadTile seq_head_tile(const PlanView& plan, int HV, int NVT) {
+  const int L = static_cast<int>(blockIdx.x);
+  return {plan.seq_order[L / (NVT * HV)], (L / NVT) % HV, L % NVT};
+}
+// The grid of seq_head_tile, or 0 CTAs when it would not fit a 1-D grid.
+inline unsigned seq_head_tile_ctas(const Problem& P, int NVT) {
+  const int64_t n = static_cast<int64_t>(P.num_seqs) * P.HV * NVT;
+  return n > 0x7fffffff ? 0u : static_cast<unsigned>(n);
+}
+
 inline int plan_max_chunks(const Problem& P) {
   return static_cast<int>(P.T / P.chunk) + P.num_seqs;
 }

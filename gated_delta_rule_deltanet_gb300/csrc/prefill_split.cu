@@ -1087,11 +1087,9 @@ __global__ void __launch_bounds__(tcs::NTC, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (plan.info[1] == 0) return;
-  // CTA (rank, head, value tile), ranks in the plan's order of decreasing sequence length
-  constexpr int NVT = D / BV;
   const int HV = P.HV;
-  const int b = plan.seq_order[blockIdx.x / (NVT * HV)];
-  const int h = (blockIdx.x / NVT) % HV, vt = blockIdx.x % NVT;
+  const SeqHeadTile cta = seq_head_tile(plan, HV, D / BV);
+  const int b = cta.b, h = cta.h, vt = cta.vt;
   const uint32_t bos = P.offsets[b], eos = P.offsets[b + 1];
   // empty, or a chunk of it outside the tensor-core path's domain (the front kernel raised
   // the device error): o and the slot are left as they were
@@ -1533,9 +1531,9 @@ static cudaError_t launch_chain_t(const Problem& P, const PlanView& plan, const 
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(tcs::CH_BYTES));
   if (e != cudaSuccess) return e;
-  const int64_t ctas = static_cast<int64_t>(P.num_seqs) * P.HV * (tcs::D / tcs::BV);
-  if (ctas > 0x7fffffff) return cudaErrorInvalidConfiguration;
-  k<<<static_cast<unsigned>(ctas), tcs::NTC, tcs::CH_BYTES, st>>>(P, plan, recs);
+  const unsigned ctas = seq_head_tile_ctas(P, tcs::D / tcs::BV);
+  if (ctas == 0) return cudaErrorInvalidConfiguration;
+  k<<<ctas, tcs::NTC, tcs::CH_BYTES, st>>>(P, plan, recs);
   return cudaGetLastError();
 }
 

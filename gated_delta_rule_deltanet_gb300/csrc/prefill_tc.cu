@@ -180,8 +180,9 @@ __global__ void __launch_bounds__(tcp::NT, 1) tc_prefill_kernel(Problem P, PlanV
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (plan.info[1] == 0) return;
-  const int b = blockIdx.x, h = blockIdx.y, vt = blockIdx.z;
   const int HV = P.HV;
+  const SeqHeadTile cta = seq_head_tile(plan, HV, tcp::D / tcp::BV);
+  const int b = cta.b, h = cta.h, vt = cta.vt;
   const int kh = h / (HV / P.HK);
   // additive write (no delta rule): A_kk = 0 makes T = I and K~ = 0 drops W = TB K~
   constexpr bool delta = DELTA;
@@ -962,7 +963,9 @@ static cudaError_t launch_tc_t(const Problem& P, const PlanView& plan, cudaStrea
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(tcp::SMEM_BYTES));
   if (e != cudaSuccess) return e;
-  k<<<dim3(P.num_seqs, P.HV, tcp::D / tcp::BV), tcp::NT, tcp::SMEM_BYTES, st>>>(P, plan);
+  const unsigned ctas = seq_head_tile_ctas(P, tcp::D / tcp::BV);
+  if (ctas == 0) return cudaErrorInvalidConfiguration;
+  k<<<ctas, tcp::NT, tcp::SMEM_BYTES, st>>>(P, plan);
   return cudaGetLastError();
 }
 

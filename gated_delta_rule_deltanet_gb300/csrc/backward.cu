@@ -167,8 +167,9 @@ __global__ void __launch_bounds__(256, 2) bwd_scan_kernel(Problem P, BwdWorkspac
   float* s_b = s_g + D;             // [C] beta
 
   if (ws.loc.plan.info[1] == 0) return;
-  const int b = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
   const int HV = P.HV;
+  const SeqHeadTile cta = seq_head_tile(ws.loc.plan, HV, D / BV);
+  const int b = cta.b, h = cta.h, v0 = cta.vt * BV;
   const int tid = threadIdx.x;
   const int ri = tid / TC::TPR, rj = (tid % TC::TPR) * TC::JT;   // row segment of a C x BV product
   const int dc = tid / TD::TPR, dj = (tid % TD::TPR) * TD::JT;   // row segment of a D x BV product
@@ -886,7 +887,7 @@ static cudaError_t launch_bwd_t(const Problem& P, const BwdWorkspace& ws, const 
     if (kTc) {
       e = launch_bwd_scans_tc(P, ws, A, SBF16, all, mc, true, st);
     } else {
-      sk<<<dim3(P.num_seqs, P.HV, D / BV), 256, BwdScanSmem<D, C, BV>::bytes, st>>>(P, ws, A);
+      sk<<<seq_head_tile_ctas(P, D / BV), 256, BwdScanSmem<D, C, BV>::bytes, st>>>(P, ws, A);
       e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;

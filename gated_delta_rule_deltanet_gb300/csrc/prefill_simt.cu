@@ -69,8 +69,9 @@ __global__ void __launch_bounds__(256) simt_scan_kernel(Problem P, SimtWorkspace
   float* s_g = s_A + C * C;       // [D]
 
   if (ws.plan.info[1] == 0) return;
-  const int b = blockIdx.x, h = blockIdx.y, v0 = blockIdx.z * BV;
   const int HV = P.HV;
+  const SeqHeadTile cta = seq_head_tile(ws.plan, HV, D / BV);
+  const int b = cta.b, h = cta.h, v0 = cta.vt * BV;
   const int tid = threadIdx.x;
   const uint32_t bos = P.offsets[b], eos = P.offsets[b + 1];
   if (eos <= bos) return;
@@ -148,7 +149,9 @@ static cudaError_t launch_simt_t(const Problem& P, const SimtWorkspace& ws, cuda
   constexpr size_t sbytes = SimtScanSmem<D, C, BV>::bytes;
   if ((e = cudaFuncSetAttribute(sk, cudaFuncAttributeMaxDynamicSharedMemorySize, sbytes)) != cudaSuccess)
     return e;
-  sk<<<dim3(P.num_seqs, P.HV, D / BV), 256, sbytes, st>>>(P, ws);
+  const unsigned ctas = seq_head_tile_ctas(P, D / BV);
+  if (ctas == 0) return cudaErrorInvalidConfiguration;
+  sk<<<ctas, 256, sbytes, st>>>(P, ws);
   e = cudaGetLastError();
   stages.mark(3, st);
   return e;

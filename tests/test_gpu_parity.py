@@ -384,3 +384,23 @@ def test_compact_and_two_kernel_tensor_core_paths_agree(decay, state):
     assert rel_err(o_sp, o_cp) <= tol
     assert rel_err(o_sp, o_ref) <= tol and rel_err(o_cp, o_ref) <= tol
     assert state_err(p, s_sp, pool_ref) <= tol and state_err(p, s_cp, pool_ref) <= tol
+
+
+@pytest.mark.parametrize("path", ["default", "compact"])
+@pytest.mark.parametrize("case", ["over_1024_sequences", "one_long_many_short"])
+def test_many_sequences_in_length_order(path, case):
+    """The per-sequence scans start in the plan's order of decreasing length (ranked for up to
+    1024 sequences, in index order beyond): both branches, with empty sequences, ties and one
+    sequence far longer than the rest, match the oracle on every output and state."""
+    rng = np.random.Generator(np.random.PCG64(2718))
+    if case == "over_1024_sequences":
+        lengths = [int(x) for x in rng.integers(0, 24, size=1030)]
+    else:
+        lengths = [int(x) for x in rng.integers(1, 70, size=299)] + [2500]
+        lengths[17] = 0
+    p = small(f"order-{case}", lengths, 1, 2, 128, "bf16", "f32", "per_channel", 64, seed=31)
+    o, pool, _ = gpu_prefill(p, compact=(path == "compact"))
+    o_ref, pool_ref = oracle.run(p, nthreads=8)
+    tol = TOL["bf16"]
+    eo, es = rel_err(o, o_ref), state_err(p, pool, pool_ref)
+    assert eo <= tol and es <= tol, f"{case} ({path}): o err {eo:.3e}, state err {es:.3e}"

@@ -293,6 +293,8 @@ kda_status_t kda_prefill_fwd(const kda_params_t* p, const void* q, const void* k
       !aligned(state_pool, 16) || !aligned(beta, 4) || !aligned(log_decay, 4) ||
       !aligned(input_row_offsets, 4) || !aligned(slot_idx, 4))
     return KDA_ERR_INVALID_ARG;
+  // per-channel log-decay rows are staged in 16-byte pieces (tensor copies, cp.async)
+  if (p->decay_kind == KDA_DECAY_PER_CHANNEL && !aligned(log_decay, 16)) return KDA_ERR_INVALID_ARG;
   const size_t need = prefill_workspace_bytes(p, P);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return KDA_ERR_WORKSPACE;
   P.q = q; P.k = k; P.v = v; P.beta = beta; P.g = log_decay;

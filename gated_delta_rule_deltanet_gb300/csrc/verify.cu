@@ -102,7 +102,7 @@ struct VerifySmem {
 // delta rule's code carries no test of it
 template <int D, int NT, bool QBF16, bool SBF16, bool PERCH, bool DELTA>
 __global__ void __launch_bounds__(NT, 2) verify_window_kernel(Problem P, int window, float* ring,
-                                                              int rec, int npairs) {
+                                                              int rec, int npairs, int g16) {
   using M = VerifyMap<D, NT>;
   using L = VerifySmem<D, QBF16, SBF16, PERCH>;
   constexpr int RPT = M::RPT, NQ = M::NQ, ES = L::ES, TB = L::TB, GW = L::GW;
@@ -144,10 +144,18 @@ __global__ void __launch_bounds__(NT, 2) verify_window_kernel(Problem P, int win
       tc::cp_async16(sb + L::O_V + (t * D * ES) + 16 * pc, vp + 16 * pc, 16u);
     }
     if constexpr (PERCH) {
-      for (int u = tid; u < nt * (D / 4); u += NT) {
-        const int t = u / (D / 4), pc = u % (D / 4);
-        const int64_t row_t = static_cast<int64_t>(b) * window + t0 + t;
-        tc::cp_async16(sb + L::O_G + t * GW * 4 + 16 * pc, P.g + (row_t * HV + h) * D + 4 * pc, 16u);
+      if (g16) {                               // 16-byte pieces where the log-decay array allows
+        for (int u = tid; u < nt * (D / 4); u += NT) {
+          const int t = u / (D / 4), pc = u % (D / 4);
+          const int64_t row_t = static_cast<int64_t>(b) * window + t0 + t;
+          tc::cp_async16(sb + L::O_G + t * GW * 4 + 16 * pc, P.g + (row_t * HV + h) * D + 4 * pc, 16u);
+        }
+      } else {                                 // the entry point asks for 4-byte alignment only
+        for (int u = tid; u < nt * D; u += NT) {
+          const int t = u / D, c = u % D;
+          const int64_t row_t = static_cast<int64_t>(b) * window + t0 + t;
+          tc::cp_async4(sb + L::O_G + (t * GW + c) * 4, P.g + (row_t * HV + h) * D + c, 4u);
+        }
       }
     }
     if (tid < nt) {
@@ -370,8 +378,9 @@ static cudaError_t launch_verify_t(const Problem& P, int window, float* ring, cu
                                          : verify_window_kernel<D, NT, Q, SB, PC, true>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e != cudaSuccess) return e;
+  const bool g16 = (reinterpret_cast<uintptr_t>(P.g) & 15u) == 0;
   k<<<dim3(static_cast<unsigned>(grid)), NT, bytes, s>>>(P, window, ring, ring_record_elems(D, PC),
-                                                          static_cast<int>(pairs));
+                                                          static_cast<int>(pairs), g16 ? 1 : 0);
   return cudaGetLastError();
 }
 

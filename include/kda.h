@@ -178,7 +178,9 @@ int kda_prefill_uses_tensor_cores(const kda_params_t *p);
  *   q, k               [T, HK, d_k], qkv_dtype, rows 16-byte aligned
  *   v                  [T, HV, d_v], qkv_dtype
  *   beta               [T, HV] fp32
- *   log_decay          [T, HV] or [T, HV, d_k] fp32 (decay_kind)
+ *   log_decay          [T, HV] or [T, HV, d_k] fp32 (decay_kind); 4-byte aligned, and
+ *                      16-byte aligned for KDA_DECAY_PER_CHANNEL (its rows are copied in
+ *                      16-byte pieces), else KDA_ERR_INVALID_ARG
  *   input_row_offsets  [B+1] uint32: sequence b is tokens [off[b], off[b+1]);
  *                      off[0] = 0, non-decreasing, off[B] = T.  Empty sequences
  *                      are allowed and leave their slot untouched.

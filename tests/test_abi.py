@@ -114,6 +114,15 @@ def test_null_and_misaligned_pointers_rejected_before_launch(lib):
     mis = P((1 << 20) + 8)
     assert lib.kda_prefill_fwd(ctypes.byref(p), mis, a, a, a, a, a, a, a, a, a, 1 << 30,
                                None) == _lib.KDA_ERR_INVALID_ARG
+    # per-channel log-decay 16-byte aligned, scalar 4-byte (the latter then fails on the
+    # missing workspace)
+    g4 = P((1 << 20) + 4)
+    pc = good(per_channel=True)
+    assert lib.kda_prefill_fwd(ctypes.byref(pc), a, a, a, a, g4, a, a, a, a, None, 1 << 30,
+                               None) == _lib.KDA_ERR_INVALID_ARG
+    sc = good(per_channel=False)
+    assert lib.kda_prefill_fwd(ctypes.byref(sc), a, a, a, a, g4, a, a, a, a, None, 1 << 30,
+                               None) == _lib.KDA_ERR_WORKSPACE
     # workspace missing / too small / misaligned
     assert lib.kda_prefill_fwd(ctypes.byref(p), a, a, a, a, a, a, a, a, a, None, 1 << 30,
                                None) == _lib.KDA_ERR_WORKSPACE

@@ -404,3 +404,21 @@ def test_many_sequences_in_length_order(path, case):
     tol = TOL["bf16"]
     eo, es = rel_err(o, o_ref), state_err(p, pool, pool_ref)
     assert eo <= tol and es <= tol, f"{case} ({path}): o err {eo:.3e}, state err {es:.3e}"
+
+
+def test_per_channel_log_decay_must_be_16_byte_aligned():
+    """Per-channel log-decay rows are staged in 16-byte pieces: a log-decay array that is only
+    4-byte aligned is refused before any work is enqueued, and the pool is untouched."""
+    p = small("g-align", [70, 5], 2, 4, 128, "bf16", "f32", "per_channel", 64, seed=77)
+    t = torch_io.prefill_inputs(p, DEV)
+    g = t["log_decay"]
+    buf = torch.empty(g.numel() + 1, dtype=g.dtype, device=DEV)
+    g_off = buf[1:].view(g.shape)
+    g_off.copy_(g)
+    before = t["state_pool"].clone()
+    t["log_decay"] = g_off
+    with pytest.raises(kda.KdaError) as e:
+        kda.prefill(**t, chunk=p.chunk, scale=p.scale)
+    assert e.value.status == 1                  # KDA_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert torch.equal(t["state_pool"], before)

@@ -167,3 +167,28 @@ def test_fold_rejects_more_accepted_than_the_window():
     kda.verify_window(t["q"], t["k"], t["v"], t["beta"], t["log_decay"], bad, pool, window=6)
     assert kda.get_device_error() == 2
     assert kda.get_device_error() == 0
+
+
+@pytest.mark.parametrize("qkv", ["bf16", "f32"])
+def test_verify_with_log_decay_only_4_byte_aligned(qkv):
+    """Per-channel log-decay rows are staged in 16-byte pieces when the array is 16-byte aligned
+    and in 4-byte pieces otherwise (the entry point asks for 4 bytes): both give the same o and
+    ring."""
+    window = 9
+    p = window_problem(6, window, 128, qkv, "f32", "per_channel", seed=515)
+    t = torch_io.prefill_inputs(p, DEV)
+    g = t["log_decay"]
+    buf = torch.empty(g.numel() + 1, dtype=g.dtype, device=DEV)
+    g_off = buf[1:].view(g.shape)
+    g_off.copy_(g)
+    assert g_off.data_ptr() % 16 == 4
+    outs = []
+    for lg in (g, g_off):
+        o, ring = kda.verify_window(t["q"], t["k"], t["v"], t["beta"], lg, t["slot_idx"], t["state_pool"],
+                                    window=window, scale=p.scale)
+        torch.cuda.synchronize()
+        assert kda.get_device_error() == 0
+        outs.append((o, ring))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    o_ref, _ = oracle.run(p)
+    assert rel_err(outs[1][0].double().cpu().numpy(), o_ref) <= TOL[qkv]

@@ -671,8 +671,11 @@ def ours_arm(args, rank, world, local):
     del t_dev
     roofline, path_roofline = prefill_rooflines(p, stage_ms, stages, ms_per_step, peaks, tensor_cores)
 
-    # end to end through the public API with host buffers
-    e2e_ms, h2d, d2h = time_prefill_e2e(p, dev, max(3, min(args.steps // 2, 200)), 3)
+    # end to end through the public API with host buffers: the median of three runs, since the
+    # host link is shared with the rest of the machine
+    e2e_runs = [time_prefill_e2e(p, dev, max(3, min(args.steps // 2, 200)), 3) for _ in range(3)]
+    e2e_ms = float(np.median([r[0] for r in e2e_runs]))
+    h2d, d2h = e2e_runs[0][1], e2e_runs[0][2]
     e2e_value, _ = aggregate(tokens, e2e_ms / 1e3, world, dev)
 
     also = []

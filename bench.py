@@ -92,6 +92,11 @@ PREFILL_STAGES = {
     False: [("plan", ()), ("chunk_local", ("q", "k", "v", "beta", "g")),
             ("state_scan", ("o", "state"))],
 }
+# the single-kernel form (KDA_FLAG_COMPACT), by decay kind (per-channel: True)
+COMPACT_STAGES = {
+    True: [("plan", ()), ("tc_range_scan", ("g",)), ("tc_prefill", ("q", "k", "v", "beta", "o", "state"))],
+    False: [("plan", ()), ("tc_prefill", ("q", "k", "v", "beta", "g", "o", "state"))],
+}
 
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of a kernel on a
@@ -294,7 +299,7 @@ def workload_config(p) -> dict:
 
 # ----------------------------------------------------------------------------- GPU side
 
-def time_prefill(p, dev, steps, warmup):
+def time_prefill(p, dev, steps, warmup, compact=False):
     import torch
     import gated_delta_rule_deltanet_gb300 as kda
     from workloads import torch_io
@@ -303,12 +308,13 @@ def time_prefill(p, dev, steps, warmup):
     out = torch.empty((T, HV, d), dtype=torch.float32, device=dev)
     params = kda.kda._prefill_params(t["q"], t["k"], t["v"], t["beta"], t["log_decay"],
                                      t["input_row_offsets"], t["slot_idx"], t["state_pool"],
-                                     p.chunk, p.scale, True, False)
+                                     p.chunk, p.scale, True, False, compact=compact)
     ws = torch.empty(max(kda.workspace_size(params), 1), dtype=torch.uint8, device=dev)
-    stages = PREFILL_STAGES[kda.uses_tensor_cores(params)]
+    stages = (COMPACT_STAGES[p.decay_kind == "per_channel"] if compact
+              else PREFILL_STAGES[kda.uses_tensor_cores(params)])
 
     def step():
-        kda.prefill(**t, chunk=p.chunk, scale=p.scale, out=out, workspace=ws)
+        kda.prefill(**t, chunk=p.chunk, scale=p.scale, out=out, workspace=ws, compact=compact)
 
     for _ in range(warmup):
         step()
@@ -809,7 +815,7 @@ def profile_arm(args):
     kda.load()
     if args.profile == "prefill":
         ms, stage_ms, _, _, stages, _ = time_prefill(workloads.workload(args.workload), dev, args.steps,
-                                                     args.warmup)
+                                                     args.warmup, compact=args.compact)
         print("stages: " + ", ".join(f"{n} {m:.4f} ms" for (n, _), m in zip(stages, stage_ms)))
     elif args.profile == "decode":
         ms = time_decode(workloads.workload("kda_decode"), dev, args.steps, args.warmup)
@@ -833,7 +839,7 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--compact", action="store_true",
-                    help="with --profile backward: the bounded-workspace form")
+                    help="with --profile prefill or backward: the single-kernel / bounded-workspace form")
     ap.add_argument("--profile", choices=["prefill", "decode", "verify", "backward"],
                     help="run W + K steps of one piece for a profiler, print no JSON line")
     args = ap.parse_args(argv)

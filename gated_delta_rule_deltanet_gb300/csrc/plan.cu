@@ -20,6 +20,7 @@ size_t plan_layout(const Problem& P, char* base, size_t off, PlanView* out) {
 }
 
 constexpr int kPlanThreads = 1024;
+static_assert(kPlanThreads == 32 * 32, "the plan's scan takes 32 warps of 32");
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem P, PlanView plan, int max_chunks) {
   __shared__ int s_bad, s_longest;
@@ -65,20 +66,35 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Problem P, PlanView 
     longest = max(longest, nb);
   }
   atomicMax(&s_longest, longest);
-  s_scan[tid] = local;
-  __syncthreads();
-  for (int off = 1; off < kPlanThreads; off <<= 1) {
-    const int add = tid >= off ? s_scan[tid - off] : 0;
-    __syncthreads();
-    s_scan[tid] += add;
-    __syncthreads();
+  // block-wide inclusive scan of `local`: within each warp by shuffles, then over the warp totals
+  const int lane = tid & 31, warp = tid >> 5;
+  int inc = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += y;
   }
-  int base = s_scan[tid] - local;
+  if (lane == 31) s_scan[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_scan[lane];                       // kPlanThreads / 32 == 32 warp totals
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    s_scan[32 + lane] = w;                      // inclusive totals of warps 0..lane
+  }
+  __syncthreads();
+  inc += warp > 0 ? s_scan[32 + warp - 1] : 0;
+  if (tid == kPlanThreads - 1) s_scan[0] = inc;   // the grand total, read below
+  __syncthreads();
+  int base = inc - local;
   for (int b = b0; b < b1; ++b) {
     plan.seq_chunk0[b] = base;
     base += static_cast<int>((P.offsets[b + 1] - P.offsets[b] + C - 1) / C);
   }
-  const int total = s_scan[kPlanThreads - 1];
+  const int total = s_scan[0];
   if (tid == kPlanThreads - 1) plan.seq_chunk0[B] = total;
   __syncthreads();                              // the first chunk of every sequence is written
   // the sequences by decreasing chunk count: a sequence's rank is the number of sequences with

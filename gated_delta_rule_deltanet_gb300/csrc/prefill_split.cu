@@ -1518,8 +1518,8 @@ static cudaError_t launch_front_t(const Problem& P, const PlanView& plan, unsign
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
   // two CTAs per SM: each prefetches for the CTA one full wave later (scalar decay), or half a
-  // wave later (per-channel decay, whose CTAs run about twice as long: measured 0.679 -> 0.674 ms
-  // on 2 x 16384 tokens, 32 heads)
+  // wave later (per-channel decay: measured 0.679 -> 0.674 ms on 2 x 16384 tokens, 32 heads,
+  // against a full wave)
   const int ahead = PERCH ? sm_count() : 2 * sm_count();
   k<<<dim3(static_cast<unsigned>(plan_max_chunks(P)), P.HV), tcs::NT, bytes, st>>>(P, plan, recs, tmq, tmk, tmg,
                                                                                    ahead);

@@ -109,8 +109,8 @@ NCU_TRAFFIC = {("decode_step", "kda_decode"): 547441408 + 480736768,
                ("verify_window", "kda_verify"): 579015936 + 57849088,
                ("fold_accepted", "kda_verify"): 453014272 + 364333056,
                ("conv_kernel", "gdn_prefill"): 358.74e6,
-               ("tc_front", "kda_prefill"): 1165939968 + 906236672,
-               ("tc_chain", "kda_prefill"): 1220629760 + 504709120,
+               ("tc_front", "kda_prefill"): 1118451968 + 905703424,
+               ("tc_chain", "kda_prefill"): 1220631040 + 504979200,
                ("tc_front", "gdn_prefill"): 138534656 + 182024192,
                ("tc_chain", "gdn_prefill"): 308361728 + 103951616}
 

@@ -23,8 +23,8 @@ struct PlanView {
   int32_t* seq_chunk0;  // [B + 1] first chunk of each sequence (prefix sums)
   ChunkInfo* chunks;    // [max_chunks]
   int32_t* seq_order;   // [B] the sequences by decreasing chunk count (ties by index) when B is
-                        // at most 1024, else in index order: the chain kernel starts its CTAs in
-                        // this order, so that the longest scans are not left to a last wave
+                        // at most 1024, else in index order: the per-sequence scans start their
+                        // CTAs in this order, so that the longest scans are not left to a last wave
   int32_t* skip;        // [B * HV] nonzero: a kernel found this (sequence, value head) outside
                         // the tensor-core path's domain; the kernels that write o and the
                         // state pool leave it untouched (zeroed by the plan kernel)
